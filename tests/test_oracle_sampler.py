@@ -1,0 +1,138 @@
+"""Pins of the oracle's Markov head and samplers against closed forms, library
+routines on tiny inputs, and chi-square on V=8 (P2 section 3.4; P1 section 3.7)."""
+import numpy as np
+import pytest
+from scipy import special, stats
+
+import oracle as O
+
+
+def _bf16(a):
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    b = a.view(np.uint32)
+    r = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+    return r
+
+
+def test_markov_r0_is_identity():
+    rng = np.random.default_rng(0)
+    base = rng.normal(0, 2, 16).astype(np.float32)
+    z = O.markov_logits(base, None, None, 3)
+    assert np.array_equal(z, base.astype(np.float64))
+
+
+def test_markov_one_hot_w1_reads_one_w2_column():
+    rng = np.random.default_rng(1)
+    V, r = 10, 4
+    base = rng.normal(0, 1, V).astype(np.float32)
+    W1 = np.zeros((V, r), np.float32)
+    W1[6, 2] = 1.0
+    W2 = rng.normal(0, 1, (V, r)).astype(np.float32)
+    z = O.markov_logits(base, W1, W2, 6)
+    np.testing.assert_array_equal(z, base.astype(np.float64) + W2[:, 2].astype(np.float64))
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_markov_matches_matmul(dt):
+    rng = np.random.default_rng(2)
+    V, r = 8, 2
+    base = rng.normal(0, 3, V).astype(np.float32)
+    W1 = rng.normal(0, 0.5, (V, r)).astype(np.float32)
+    W2 = rng.normal(0, 0.5, (V, r)).astype(np.float32)
+    if dt == "bf16":
+        base, W1, W2 = _bf16(base), _bf16(W1), _bf16(W2)
+    for prev in range(V):
+        z = O.markov_logits(base, W1, W2, prev)
+        ref = O.to_f64(base) + O.to_f64(W2) @ O.to_f64(W1)[prev]
+        np.testing.assert_allclose(z, ref, rtol=0, atol=1e-14)
+
+
+def test_argmax_lowest_index_on_ties():
+    z = np.array([1.0, 3.0, 2.0, 3.0])
+    x, m = O.argmax(z)
+    assert x == 1 and m == 0.0
+    z = np.array([0.5, -1.0, 2.0])
+    assert O.argmax(z) == (2, 1.5)
+    rng = np.random.default_rng(3)
+    for _ in range(50):
+        z = rng.normal(size=33)
+        assert O.argmax(z)[0] == int(np.argmax(z))
+
+
+def test_single_tile_is_inverse_cdf():
+    rng = np.random.default_rng(4)
+    lw = rng.normal(0, 1.5, 8)
+    p = special.softmax(lw)
+    cdf = np.cumsum(p)
+    for j in range(200):
+        x, m, lse = O.tile_gumbel(lw, 8, 5, j, 2)
+        u = O.uniform(5, j, 2, O.P_SAMPLE_INTILE, 0)
+        assert x == int(np.searchsorted(cdf, u, side="right"))
+        assert abs(lse - special.logsumexp(lw)) < 1e-12
+
+
+def test_tile_lse_output_and_no_mass_tiles():
+    lw = np.array([-np.inf, -np.inf, 0.3, 1.0, -np.inf, -np.inf, -np.inf, -2.0])
+    for j in range(300):
+        x, m, lse = O.tile_gumbel(lw, 2, 9, j, 1)
+        assert np.isfinite(lw[x])  # zero-weight entries are never drawn
+    assert abs(lse - special.logsumexp(lw)) < 1e-12
+
+
+def _chi2_p(counts, probs):
+    exp = probs * counts.sum()
+    return stats.chisquare(counts, exp).pvalue
+
+
+@pytest.mark.parametrize("T", [0.7, 1.0])
+@pytest.mark.parametrize("TS,variant", [(2, 0), (3, 0), (8, 0), (8, 1)])
+def test_samplers_chi_square(T, TS, variant):
+    rng = np.random.default_rng(10)
+    z = rng.normal(0, 1.2, 8)
+    lw = z / T
+    counts = O.trials_sampler(lw, TS, 1234 + TS, 1_000_000, variant)
+    assert _chi2_p(counts, special.softmax(lw)) > 1e-3
+
+
+def test_chi_square_detects_a_wrong_law():
+    # the same test must reject a sampler drawing from a slightly different law
+    rng = np.random.default_rng(10)
+    lw = rng.normal(0, 1.2, 8)
+    counts = O.trials_sampler(lw, 2, 77, 1_000_000, 0)
+    wrong = special.softmax(lw * 1.02)
+    assert _chi2_p(counts, wrong) < 1e-6
+
+
+def test_sample_request_greedy_chain():
+    rng = np.random.default_rng(5)
+    B, gamma, V, r = 2, 4, 64, 3
+    base = rng.normal(0, 2, (B, gamma, V)).astype(np.float32)
+    W1 = rng.normal(0, 0.7, (V, r)).astype(np.float32)
+    W2 = rng.normal(0, 0.7, (V, r)).astype(np.float32)
+    anchor = np.array([5, 17], np.int32)
+    for j in range(B):
+        tok, lse, zx, mg = O.sample_request(base, W1, W2, anchor[j], j, 0.0, 0, 1024)
+        prev = anchor[j]
+        for i in range(gamma):
+            z = base[j, i].astype(np.float64) + W2.astype(np.float64) @ W1[prev].astype(np.float64)
+            assert tok[i] == int(np.argmax(z))
+            assert np.isnan(lse[i])
+            assert abs(zx[i] - z[tok[i]]) < 1e-12
+            prev = tok[i]
+
+
+def test_sample_request_carries_token_and_lse():
+    rng = np.random.default_rng(6)
+    B, gamma, V, r = 1, 5, 50, 4
+    base = rng.normal(0, 1, (B, gamma, V)).astype(np.float32)
+    W1 = rng.normal(0, 1.0, (V, r)).astype(np.float32)
+    W2 = rng.normal(0, 1.0, (V, r)).astype(np.float32)
+    T = 0.8
+    tok, lse, zx, mg = O.sample_request(base, W1, W2, 7, 0, T, 99, 16)
+    prev = 7
+    for i in range(gamma):
+        z = base[0, i].astype(np.float64) + W2.astype(np.float64) @ W1[prev].astype(np.float64)
+        x, m, l = O.tile_gumbel(z / T, 16, 99, 0, i + 1)
+        assert tok[i] == x and abs(lse[i] - special.logsumexp(z / T)) < 1e-12
+        assert abs(zx[i] - z[x]) < 1e-12
+        prev = x
