@@ -1,0 +1,368 @@
+"""Benchmark of the DSpark hot path on one or more GPUs (one process per GPU).
+
+A step is one pass of the whole hot path over one batch of the b32_r64 workload (B=32
+requests, gamma=8, V=151936, Markov rank 64, bf16 logits and weights, T=1):
+  schedule  (dspark_schedule_verify_len, budget B*gamma: every position verified)
+  sample    (dspark_markov_sample_block)
+  verify    (dspark_verify, the scheduled lengths, dense target rows)
+  tv        (dspark_accept_rate_tv on the batch's draft/target logits, eval_mask and tau)
+metric = drafted tokens per second = N * B * gamma / step time (replicas: every rank runs its own
+batch, "weak" scaling).  Inputs are synthetic, seeded, resident in HBM before timing; L2 is
+flushed (256 MB write) before every step, outside the per-step CUDA-event interval.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "draft tokens/s (sample+verify) at V=151936; achieved HBM GB/s vs peak"
+WORKLOAD = "b32_r64"
+KERNEL_SOURCES = {
+    "sample": ["sample.cu", "markov_tile.cuh", "common.cuh"],
+    "verify": ["verify.cu", "markov_tile.cuh", "common.cuh"],
+    "tv": ["tv.cu", "common.cuh"],
+    "schedule": ["schedule.cu", "common.cuh"],
+}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def source_hash(kernel: str) -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "semi_ar_draft_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f).get(kernel)
+    except Exception:
+        return None
+    if not rec or rec.get("source_hash") != source_hash(kernel):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx = float(p[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def algorithmic_bytes(wl, n_rejected: int):
+    B, g, V, r = wl.B, wl.gamma, wl.V, wl.r
+    e = 2  # bf16
+    sample = B * g * V * e + V * r * e + B * g * r * e + B * g * 12
+    verify = B * g * V * e + n_rejected * V * (e + e) + (V * r * e if n_rejected else 0) + B * 8
+    tv = 2 * B * g * V * e + B * g * 8 + B * 4
+    schedule = B * g * 4 + (2 * B + 1) * 4
+    return {"sample": sample, "verify": verify, "tv": tv, "schedule": schedule}
+
+
+def run_cpu_baseline(wl_host, seconds: float = 15.0):
+    """The oracle, as it stands, on a bounded sample of the same batch: whole requests of the
+    step (sample + verify + their accept-rate rows), plus the scheduler over the batch."""
+    import numpy as np
+
+    import oracle as O
+
+    base, W1, W2, anchor, target, conf = wl_host
+    B, g, V = base.shape
+    t0 = time.perf_counter()
+    O.schedule(conf, B * g)
+    done = 0
+    for j in range(B):
+        tok, lse, zat, _ = O.sample_request(base, W1, W2, int(anchor[j]), j, 1.0, 0, 1024)
+        O.verify_request(base, W1, W2, int(anchor[j]), j, tok, lse.astype(np.float32), zat.astype(np.float32), target,
+                         g, 1.0, 0, 1024)
+        for i in range(g):
+            O.tv_row(base[j, i], target[j, i])
+        done += 1
+        if time.perf_counter() - t0 > seconds:
+            break
+    el = time.perf_counter() - t0
+    return {"value": done * g / el, "unit": "draft tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} of {B} requests of {WORKLOAD} (sample+verify+tv rows) + schedule over the batch, "
+                      f"single-threaded C oracle, {el:.1f} s"}
+
+
+def host_workload(device):
+    from semi_ar_draft_gb300 import workloads as W
+
+    wl = W.b32_r64(device=device)
+    t = wl.tensors
+    return wl, (W.np_view(t["base"]), W.np_view(t["W1"]), W.np_view(t["W2"]), t["anchor"].cpu().numpy(),
+                W.np_view(t["target"]), t["conf"].cpu().numpy())
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return
+    import numpy as np  # noqa: F401
+
+    wl, host = host_workload("cpu")
+    B, g = wl.B, wl.gamma
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm-up state
+    per_step = max(5.0, 60.0 / max(args.steps, 1))
+    vals = []
+    samples = []
+    for _ in range(args.steps):
+        cb = run_cpu_baseline(host, seconds=per_step)
+        vals.append(cb["value"])
+        samples.append(cb["sample"])
+    v = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "draft tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": B * g / v * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "B": B, "gamma": g, "V": wl.V, "r": wl.r, "T": wl.T},
+            "cpu_baseline": {"value": v, "unit": "draft tokens/s", "cores": 1, "kind": "oracle", "sample": samples[0]},
+            "e2e": {"value": v, "unit": "draft tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+
+    import torch
+
+    from semi_ar_draft_gb300 import api, binding
+    from semi_ar_draft_gb300 import build as B_
+
+    B_.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    wl, host = host_workload(dev)
+    t = wl.tensors
+    B, g, V = wl.B, wl.gamma, wl.V
+    budget = B * g
+    base, W1, W2, anchor, target, conf = t["base"], t["W1"], t["W2"], t["anchor"], t["target"], t["conf"]
+    d4 = base.view(1, B, g, V)
+    t4 = target.view(1, B, g, V)
+    keep = torch.ones((1, B), dtype=torch.uint8, device=dev)
+    # outputs and workspaces allocated once (caller-owned)
+    Lout = torch.empty(B, dtype=torch.int32, device=dev)
+    off = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    obj = torch.empty(1, device=dev)
+    tok = torch.empty((B, g), dtype=torch.int32, device=dev)
+    lse = torch.empty((B, g), device=dev)
+    zat = torch.empty((B, g), device=dev)
+    nacc = torch.empty(B, dtype=torch.int32, device=dev)
+    corr = torch.empty(B, dtype=torch.int32, device=dev)
+    acc = torch.empty((1, B, g), device=dev)
+    emask = torch.empty((1, B, g), device=dev)
+    tau = torch.empty((1, B), device=dev)
+    p = api.make_params(base, W1, wl.T, wl.seed)
+    ws_s = binding.workspace(binding.dspark_schedule_workspace_size(B, g), dev)
+    ws_a = binding.workspace(binding.dspark_sample_workspace_size(p), dev)
+    ws_v = binding.workspace(binding.dspark_verify_workspace_size(p, g), dev)
+    ws_t = binding.workspace(binding.dspark_accept_rate_tv_workspace_size(1, B, g, V, binding.BF16), dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def step(src=None):
+        bs, ts, cs, an = (base, target, conf, anchor) if src is None else src
+        d_, t_ = bs.view(1, B, g, V), ts.view(1, B, g, V)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        ev[0].record()
+        binding.dspark_schedule_verify_len(B, g, cs, budget, Lout, off, obj, ws_s)
+        ev[1].record()
+        binding.dspark_markov_sample_block(p, bs, W1, W2, an, tok, lse, zat, ws_a)
+        ev[2].record()
+        binding.dspark_verify(p, bs, W1, W2, an, tok, lse, zat, ts, g, Lout, None, nacc, corr, ws_v)
+        ev[3].record()
+        binding.dspark_accept_rate_tv(1, B, g, V, binding.BF16, d_, t_, keep, None, acc, emask, tau, ws_t)
+        ev[4].record()
+        return ev
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    for w in (ws_s, ws_a, ws_v, ws_t):
+        assert binding.dspark_get_device_status(w) == 0
+    n_rej = int((nacc < Lout).sum().item())
+
+    names = ["schedule", "sample", "verify", "tv"]
+    per = {n: [] for n in names}
+    step_ms = []
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        evs = []
+        for _ in range(args.steps):
+            flush.zero_()
+            evs.append(step())
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    for ev in evs:
+        for k, n in enumerate(names):
+            per[n].append(ev[k].elapsed_time(ev[k + 1]))
+        step_ms.append(ev[0].elapsed_time(ev[4]))
+    t_step = sum(step_ms) / len(step_ms)
+    if pg:
+        tt = torch.tensor([t_step], device=dev)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        t_step = float(tt.item())
+    value = world * B * g / (t_step * 1e-3)
+
+    # e2e: the same step through the C ABI with host inputs copied in and results read back
+    pin = {k: v.cpu().pin_memory() for k, v in (("base", base), ("target", target), ("conf", conf), ("anchor", anchor))}
+    dbuf = {k: torch.empty_like(v) for k, v in (("base", base), ("target", target), ("conf", conf), ("anchor", anchor))}
+    outs = [tok, nacc, corr, acc, emask, tau, Lout]
+    hout = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+    e2e_ms = []
+    for it in range(max(args.warmup, 3) + args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for k in pin:
+            dbuf[k].copy_(pin[k], non_blocking=True)
+        step((dbuf["base"], dbuf["target"], dbuf["conf"], dbuf["anchor"]))
+        for o, h in zip(outs, hout):
+            h.copy_(o, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        if it >= max(args.warmup, 3):
+            e2e_ms.append(e0.elapsed_time(e1))
+    t_e2e = sum(e2e_ms) / len(e2e_ms)
+    if pg:
+        tt = torch.tensor([t_e2e], device=dev)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        t_e2e = float(tt.item())
+
+    avg = {n: sum(v) / len(v) for n, v in per.items()}
+    algo = algorithmic_bytes(wl, n_rej)
+    peak, peak_kind = peaks()
+    dom = max(["sample", "verify", "tv"], key=lambda n: avg[n])
+    achieved = algo[dom] / (avg[dom] * 1e-3) / 1e9
+    kernels = {n: {"ms": round(avg[n], 5), "bytes": algo[n],
+                   "gbs": round(algo[n] / (avg[n] * 1e-3) / 1e9, 1),
+                   "frac_of_peak": round(algo[n] / (avg[n] * 1e-3) / 1e9 / peak, 4)} for n in names}
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "draft tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(t_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; shapes and distributions of the workload)",
+        "config": {"workload": WORKLOAD, "B": B, "gamma": g, "V": V, "r": wl.r, "T": wl.T, "budget": budget,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "flushed (256 MB write) before each step; per-step CUDA events exclude the flush",
+                   "step": "schedule + sample + verify + tv(eval_mask, tau)"},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
+                     "traffic": profiled_traffic(dom), "algorithmic_bytes": algo[dom]},
+        "kernels": kernels,
+        "n_rejected": n_rej,
+        "e2e": {"value": round(world * B * g / (t_e2e * 1e-3), 1), "unit": "draft tokens/s", "ms_per_step": round(t_e2e, 4),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 6 * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed": round(wall, 3),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = run_cpu_baseline(host)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

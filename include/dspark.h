@@ -1,0 +1,218 @@
+/*
+ * dspark.h -- C ABI of libdspark, the GB300 (sm_103a) hot path of DSpark
+ * semi-autoregressive speculative decoding.
+ *
+ * The operations follow four web pages about DSpark, cited by title and section:
+ *   P1 "03 · DSpark 建模：Markov 与 Confidence"
+ *   P2 "从 DFlash 到 dLLM Self-Spec（三）：DSpark 的半自回归 Draft 与负载感知 Verify"
+ *   P3 "如何评价 DeepSeek 发布 DSpark？哪些亮点值得关注？" (reading notes)
+ *   P4 "DSpark 深度解读：DeepSeek-V4 如何用「半自回归」把推理速度提升 85%"
+ *
+ * Conventions for every entry point
+ *   - Pointers to tensors are DEVICE pointers (cudaMalloc / torch CUDA memory) unless
+ *     stated otherwise; all tensors are dense, row-major, C-contiguous.
+ *   - The caller owns every buffer.  The library allocates no device memory: scratch
+ *     comes from a caller-provided workspace of at least dspark_*_workspace_size()
+ *     bytes, 256-byte aligned.  A workspace may be reused by later calls on the same
+ *     stream but must not be shared by calls that can run concurrently.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous: they validate arguments on the host, enqueue kernels and return.
+ *     Host-detected errors return a status and enqueue nothing.  Errors detected on
+ *     the device (out-of-range token ids, a device wait that gave up) are written to
+ *     a status word at the start of the workspace; read it with
+ *     dspark_get_device_status(), which synchronises the stream.
+ *   - Token ids are int32 in [0, V).  Logits are fp32 or bf16 (DSPARK_F32 /
+ *     DSPARK_BF16); arithmetic is fp32 with fp32 accumulation.
+ *   - Randomness is counter-based (Philox4x32-10; Salmon et al., SC 2011), so every
+ *     call is reproducible from its arguments: key = (low 32 bits of seed, high 32
+ *     bits), counter = (n / 4, i, j, purpose), output word n mod 4, mapped to
+ *     (0,1) as (floor(word / 2^9) + 1/2) * 2^-23.  j = request index within the call,
+ *     i = 1-based block position, purpose = one of DSPARK_P_*, n = draw index.
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* dspark_stream_t;
+
+typedef enum {
+    DSPARK_OK = 0,
+    DSPARK_ERR_INVALID_ARG = 1, /* bad pointer, size, dtype or value */
+    DSPARK_ERR_UNSUPPORTED = 2, /* valid but outside what this build handles */
+    DSPARK_ERR_CUDA = 3,        /* a CUDA runtime call failed */
+    DSPARK_ERR_TIMEOUT = 4,     /* device: a grid-wide wait gave up (status word only) */
+    DSPARK_ERR_BUDGET = 5,      /* scheduler: budget < B */
+    DSPARK_ERR_WORKSPACE = 6,   /* workspace NULL, misaligned or too small */
+    DSPARK_ERR_TOKEN_RANGE = 7  /* device: a token/anchor id outside [0, V) or a bad row count (status word only) */
+} dspark_status;
+
+enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 };
+
+/* Random-draw purposes (the fourth Philox counter word). */
+enum {
+    DSPARK_P_SAMPLE_TILE = 1,   /* draft sampling: one uniform per vocabulary tile */
+    DSPARK_P_SAMPLE_INTILE = 2, /* draft sampling: the in-tile inverse-CDF uniform */
+    DSPARK_P_ACCEPT = 3,        /* verify: the acceptance uniform u_i */
+    DSPARK_P_RESID_TILE = 4,    /* verify: residual draw, per tile */
+    DSPARK_P_RESID_INTILE = 5,  /* verify: residual draw, in tile */
+    DSPARK_P_BONUS_TILE = 6,    /* verify: bonus draw from the next target row, per tile */
+    DSPARK_P_BONUS_INTILE = 7   /* verify: bonus draw, in tile */
+};
+
+/* Vocabulary tile of the sampler (see "Sampling contract" below). */
+#define DSPARK_TILE 1024
+
+/*
+ * Sampling contract (the pages never show the body of sample_tokens, P2 section 3.4;
+ * any exact categorical draw is lossless, bit-parity needs one fixed definition):
+ *   T == 0: x = argmax_v z_v, lowest index on ties.
+ *   T  > 0: s = z / T.  Tiles of DSPARK_TILE consecutive ids; LSE_t = log sum_{v in t} e^{s_v}.
+ *           t* = argmax_t (LSE_t - ln E_t), E_t = -ln U(seed, j, i, SAMPLE_TILE, t), lowest t on
+ *           ties.  x = smallest v in t* with sum_{w in t*, w <= v} e^{s_w - LSE_t*} > U(seed, j, i,
+ *           SAMPLE_INTILE, 0) (if rounding leaves none: the last v of t* with nonzero weight).
+ *   This is softmax(s) exactly: Gumbel-max over tiles picks t with probability proportional to
+ *   e^{LSE_t}, the inverse CDF picks v within t proportionally to e^{s_v}.  Residual and bonus
+ *   draws in dspark_verify use the same contract on their own weights and purposes.
+ */
+
+typedef struct {
+    int B;             /* requests in the call */
+    int gamma;         /* block length: draft positions per request */
+    int V;             /* vocabulary size */
+    int r;             /* Markov rank (0 = no Markov head: the DFlash configuration, P1 section 3.13) */
+    float temperature; /* 0 = greedy; > 0 = sample softmax(z / T) */
+    uint64_t seed;     /* Philox key */
+    int logits_dtype;  /* dtype of base (and target) logits: DSPARK_F32 or DSPARK_BF16 */
+    int w_dtype;       /* dtype of W1 and W2 */
+} dspark_sample_params;
+
+/*
+ * Markov-head block sampling (P2 section 3.4, VanillaMarkov and sample_block_tokens;
+ * P1 section 3.7; P4 section 3.3):
+ *   prev_1 = anchor[j];  for i = 1..gamma:
+ *     z_{j,i} = base[j, i-1, :] + W2 . W1[prev_i]      (bias_v = sum_k W1[prev_i, k] W2[v, k])
+ *     x_{j,i} ~ sampling contract on z_{j,i} / T;  prev_{i+1} = x_{j,i}
+ * Arguments
+ *   base_logits [B, gamma, V] (logits_dtype); W1 [V, r], W2 [V, r] (w_dtype; W2 is the
+ *   nn.Linear(r, V).weight layout, i.e. the page's r x V matrix transposed in memory;
+ *   both may be NULL when r == 0); anchor [B] int32 (the token before the block).
+ * Outputs
+ *   tokens [B, gamma] int32; draft_lse [B, gamma] float = LSE_v(z/T) (NaN when T == 0);
+ *   draft_logit_at_tok [B, gamma] float = z at the drafted token.
+ * The gamma steps run inside one persistent kernel (a grid-wide wait per step).
+ * Device status: DSPARK_ERR_TOKEN_RANGE for an anchor outside [0, V) (it is clamped and
+ * the outputs are then undefined), DSPARK_ERR_TIMEOUT if a grid-wide wait gave up.
+ */
+size_t dspark_sample_workspace_size(const dspark_sample_params* p);
+dspark_status dspark_markov_sample_block(const dspark_sample_params* p, const void* base_logits, const void* W1,
+                                         const void* W2, const int32_t* anchor, int32_t* tokens, float* draft_lse,
+                                         float* draft_logit_at_tok, void* workspace, size_t ws_bytes,
+                                         dspark_stream_t stream);
+
+/*
+ * Lossless verification by rejection sampling (P3 "Speculative Decoding": the target checks
+ * the drafted positions in parallel, accepts left to right, truncates at the first failure
+ * and resamples from the target, so the output law is the target's; the verify tokens of all
+ * requests are one flattened list, P2 section 3.7.2):
+ *   for i = 1..L_j:  p = softmax(t_{j,i} / T),  q(x) = exp(z_x / T - draft_lse)
+ *     accept x_{j,i} iff ln U(seed, j, i, ACCEPT, 0) < ln p(x) - ln q(x)   (u < p/q)
+ *   first rejection at k:  correction ~ norm(max(0, p_k - q_k)) (RESID purposes), where q_k over
+ *     the vocabulary is rebuilt from base, W1, W2 and prev = x_{k-1} (anchor for k = 1) and
+ *     normalised by draft_lse; if that residual has no mass, correction ~ p_k instead.
+ *   all L_j accepted:  correction ~ p_{L_j+1} (BONUS purposes) if target row L_j+1 exists,
+ *     else -1.
+ *   T == 0: accept iff argmax t_{j,i} == x_{j,i}; the correction is the argmax of the
+ *     rejecting (or bonus) target row.
+ * Arguments
+ *   p: the same parameters as the sampling call (B, gamma, V, r, T, seed, dtypes).
+ *   base_logits, W1, W2, anchor: as for dspark_markov_sample_block.
+ *   tokens, draft_lse, draft_logit_at_tok [B, gamma]: the sampling call's outputs.
+ *   target_logits: target row i (1-based) of request j is
+ *     dense  (target_row_offsets == NULL): target_logits[j, i-1, :] of a [B, gamma_t, V] tensor;
+ *     flattened (target_row_offsets != NULL, [B+1] int32 CSR): row target_row_offsets[j] + i - 1
+ *       of a [target_row_offsets[B], V] tensor; request j owns target_row_offsets[j+1] -
+ *       target_row_offsets[j] rows (gamma_t is then ignored and may be 0).
+ *   verify_len [B] int32 in [1, gamma] (NULL = gamma for every request): L_j.  Request j must own
+ *     at least L_j target rows; a row L_j+1, when present, is the bonus row.
+ * Outputs
+ *   n_accepted [B] int32; correction_token [B] int32 (-1 = none).
+ * Device status: DSPARK_ERR_TOKEN_RANGE for a token outside [0, V) or a request with fewer
+ * than L_j target rows.
+ */
+size_t dspark_verify_workspace_size(const dspark_sample_params* p, int gamma_t);
+dspark_status dspark_verify(const dspark_sample_params* p, const void* base_logits, const void* W1, const void* W2,
+                            const int32_t* anchor, const int32_t* tokens, const float* draft_lse,
+                            const float* draft_logit_at_tok, const void* target_logits, int gamma_t,
+                            const int32_t* verify_len, const int32_t* target_row_offsets, int32_t* n_accepted,
+                            int32_t* correction_token, void* workspace, size_t ws_bytes, dspark_stream_t stream);
+
+/*
+ * Training-side accept-rate targets (P1 section 3.9 "Accept rate 3D", P2 section 3.5) and the
+ * prefix-validity mask (P1 sections 3.6 and 3.10):
+ *   acc[s,a,i] = clamp(1 - 0.5 sum_v |softmax(d)_v - softmax(t)_v|, 0, 1) = clamp(sum_v min(p_v, q_v))
+ *     with softmax over fp32 logits and no temperature;
+ *   eval_mask[s,a,i] = prod_{k<=i} (block_keep[s,a] != 0 && pos_valid[s,a,k] != 0)   (cumprod)
+ *   tau[s,a] = 1 + sum_i prod_{k<=i} acc[s,a,k] * eval_mask[s,a,k]   (optional)
+ * Arguments
+ *   draft_logits, target_logits [S, A, gamma, V] (dtype); block_keep [S, A] uint8;
+ *   pos_valid [S, A, gamma] uint8 or NULL (all valid).
+ * Outputs
+ *   accept_rate, eval_mask [S, A, gamma] float; tau [S, A] float or NULL.
+ */
+size_t dspark_accept_rate_tv_workspace_size(int S, int A, int gamma, int V, int dtype);
+dspark_status dspark_accept_rate_tv(int S, int A, int gamma, int V, int dtype, const void* draft_logits,
+                                    const void* target_logits, const uint8_t* block_keep, const uint8_t* pos_valid,
+                                    float* accept_rate, float* eval_mask, float* tau, void* workspace,
+                                    size_t ws_bytes, dspark_stream_t stream);
+
+/*
+ * Confidence-scheduled verify length (P3 section "置信度调度与验证截断":
+ *   max_{L} sum_j sum_{i<=L_j} c~_{t+i}^{(j)},  1 <= L_j <= gamma, under a latency SLA;
+ * survival a_k = prod_{i<=k} c_i, P2 section 3.8.3).  The SLA is a total verify-token budget:
+ *   sum_j L_j <= budget.
+ *   c is clamped to [0, 1] (NaN -> 0); a_{j,i} = prod_{k<=i} c_{j,k}, formed left to right in fp32.
+ *   Each request verifies one token; the remaining budget - B slots go to the largest a_{j,i}
+ *   with i >= 2, ordered by (a desc, j asc, i asc).  Since a is non-increasing along i the choice
+ *   is prefix-closed and optimal.
+ * Arguments
+ *   conf [B, gamma] float: conditional confidences c_{j,i}; budget: total verify tokens.
+ * Outputs
+ *   verify_len [B] int32; offsets [B+1] int32 = exclusive prefix sum of verify_len (CSR of the
+ *   flattened verify-token list); objective [1] float (sum of the chosen a) or NULL.
+ * Host errors: DSPARK_ERR_BUDGET when budget < B; DSPARK_ERR_UNSUPPORTED when B * gamma > 16384.
+ */
+size_t dspark_schedule_workspace_size(int B, int gamma);
+dspark_status dspark_schedule_verify_len(int B, int gamma, const float* conf, int budget, int32_t* verify_len,
+                                         int32_t* offsets, float* objective, void* workspace, size_t ws_bytes,
+                                         dspark_stream_t stream);
+
+/* Reads the device status word of `workspace` after synchronising `stream`
+ * (DSPARK_OK when no device-side error was recorded).  `workspace` is a device pointer;
+ * `out` is a host pointer. */
+dspark_status dspark_get_device_status(const void* workspace, dspark_stream_t stream, int32_t* out);
+
+/* Upper bound, in nanoseconds, on every grid-wide wait inside the kernels (default 2e9).
+ * A wait that exceeds it records DSPARK_ERR_TIMEOUT and its kernel returns early.
+ * Process-wide; affects launches made after the call. */
+void dspark_set_wait_limit_ns(uint64_t ns);
+
+/* Test support: launches `nblocks` co-resident blocks that meet at one grid-wide wait which
+ * expects `nblocks + missing` arrivals.  With missing > 0 the wait cannot complete and must
+ * give up after the wait limit, recording DSPARK_ERR_TIMEOUT in the workspace status word.
+ * Needs a workspace of dspark_sample_workspace_size-style header size (256 bytes). */
+dspark_status dspark_selftest_grid_wait(int nblocks, int missing, void* workspace, size_t ws_bytes,
+                                        dspark_stream_t stream);
+
+const char* dspark_status_string(dspark_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSPARK_H */

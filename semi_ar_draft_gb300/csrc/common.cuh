@@ -1,0 +1,192 @@
+// common.cuh -- device utilities shared by the libdspark kernels (GPU side only).
+//
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC 2011), the (0,1) mapping, bf16
+// loads, warp reductions and a bounded grid-wide wait.  Nothing here is shared
+// with the CPU oracle.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include "dspark.h"
+
+namespace dspark {
+
+// ---------------------------------------------------------------- workspace
+// Every workspace starts with a 256-byte header: the device status word and
+// the grid-wait arrival counter, on separate 128-byte lines.
+struct WsHeader {
+    int32_t status;
+    int32_t pad0[31];
+    uint32_t arrivals;
+    uint32_t pad1[31];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+constexpr size_t kHeaderBytes = 256;
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+__device__ __forceinline__ void record_status(int32_t* st, int code) { atomicCAS(st, 0, code); }
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ int32_t ld_relaxed_s32(const int32_t* p) {
+    int32_t v;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+// Hardware base-2 exponential / logarithm (PTX ex2.approx / lg2.approx, max rel. error ~2^-22).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ---------------------------------------------------------------- loads
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+template <typename T>
+__device__ __forceinline__ float load_logit(const T* p, size_t idx);
+template <>
+__device__ __forceinline__ float load_logit<float>(const float* p, size_t idx) {
+    return __ldg(p + idx);
+}
+template <>
+__device__ __forceinline__ float load_logit<__nv_bfloat16>(const __nv_bfloat16* p, size_t idx) {
+    return bf16_bits_to_f32(__ldg(reinterpret_cast<const unsigned short*>(p) + idx));
+}
+
+// Eight consecutive logits starting at an index that is a multiple of 8 (16-byte aligned for
+// bf16, 32-byte aligned for fp32).  `streaming` marks data read once (evict-first).
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, size_t idx, float (&v)[8]);
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, size_t idx, float (&v)[8]) {
+    uint4 w = __ldg(reinterpret_cast<const uint4*>(p + idx));
+    v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+    v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+}
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, size_t idx, float (&v)[8]) {
+    float4 a = __ldg(reinterpret_cast<const float4*>(p + idx));
+    float4 b = __ldg(reinterpret_cast<const float4*>(p + idx) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+// ---------------------------------------------------------------- Philox4x32-10
+// Ten rounds; each multiplies counter words 0 and 2 by two fixed odd constants, xors the
+// high halves with the other counter words and the round key, and the key is advanced by
+// two Weyl increments between rounds.
+__device__ __forceinline__ uint4 philox10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint32_t lo_a = 0xD2511F53u * c.x, hi_a = __umulhi(0xD2511F53u, c.x);
+        const uint32_t lo_b = 0xCD9E8D57u * c.z, hi_b = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(hi_b ^ c.y ^ k0, lo_b, hi_a ^ c.w ^ k1, lo_a);
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c;
+}
+__device__ __forceinline__ uint32_t philox_word(uint64_t seed, uint32_t j, uint32_t i, uint32_t purpose,
+                                                uint32_t n) {
+    const uint4 o = philox10(make_uint4(n >> 2, i, j, purpose), (uint32_t)seed, (uint32_t)(seed >> 32));
+    const uint32_t s = n & 3u;
+    return s == 0 ? o.x : (s == 1 ? o.y : (s == 2 ? o.z : o.w));
+}
+// (floor(x / 2^9) + 1/2) * 2^-23: exact in fp32, in [2^-24, 1 - 2^-24].
+__device__ __forceinline__ float u01(uint32_t x) { return ((float)(x >> 9) + 0.5f) * (1.0f / 8388608.0f); }
+__device__ __forceinline__ float uniform(uint64_t seed, uint32_t j, uint32_t i, uint32_t purpose, uint32_t n) {
+    return u01(philox_word(seed, j, i, purpose, n));
+}
+// ln E with E = -ln u, accurate for u near 1 (1 - u is exact for these u).
+__device__ __forceinline__ float log_neg_log_u(float u) {
+    const float e = (u < 0.5f) ? -logf(u) : -log1pf(-(1.0f - u));
+    return logf(e);
+}
+
+// ---------------------------------------------------------------- reductions
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_incl_scan(float v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+    }
+    return v;
+}
+// Argmax over a warp: larger value wins, lower index on equal values.
+__device__ __forceinline__ void warp_argmax(float& v, int& idx) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+        if (ov > v || (ov == v && oi < idx)) {
+            v = ov;
+            idx = oi;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- grid-wide wait
+// All blocks of a co-resident (cooperative) grid meet here.  `target` is the total number of
+// arrivals expected so far (a monotonically growing counter, zeroed before the launch).
+// The wait is bounded: past `limit_ns`, or once another block has recorded an error, it
+// records DSPARK_ERR_TIMEOUT (first error wins) and returns false; the caller must return.
+__device__ __forceinline__ bool grid_wait(WsHeader* h, uint32_t target, uint64_t limit_ns) {
+    __shared__ int s_ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(&h->arrivals, 1u);
+        int ok = 1;
+        const uint64_t t0 = global_ns();
+        while (ld_acquire_u32(&h->arrivals) < target) {
+            if (ld_relaxed_s32(&h->status) != 0) {
+                ok = 0;
+                break;
+            }
+            if (global_ns() - t0 > limit_ns) {
+                record_status(&h->status, DSPARK_ERR_TIMEOUT);
+                ok = 0;
+                break;
+            }
+        }
+        __threadfence();
+        s_ok = ok;
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
+
+}  // namespace dspark

@@ -1,0 +1,272 @@
+// sample.cu -- dspark_markov_sample_block: Markov-head block sampling.
+//
+// Method (P2 "从 DFlash 到 dLLM Self-Spec（三）" section 3.4, VanillaMarkov and the
+// sample_block_tokens loop; P1 "03 · DSpark 建模：Markov 与 Confidence" section 3.7):
+// for i = 1..gamma, z = base_i + W2 . W1[prev]; sample; prev = sampled.  The sampling
+// contract is the tile-Gumbel draw stated in dspark.h.
+//
+// One persistent cooperative kernel runs all gamma steps:
+//   - vocabulary split: block b owns tiles t = b, b + G, ... (G <= number of SMs);
+//   - per step and tile, rows go in blocks of 16 requests: the producer writes z = base + bias
+//     for 16 rows x 1024 ids to shared memory with per-32-id chunk statistics (tensor-core
+//     mma.sync bias with the accumulator initialised from the base logits, or a CUDA-core GEMV
+//     for fp32 weights); a warp per row turns them into the tile's record {Gumbel key, log-mass,
+//     in-tile candidate, z at it} in global scratch;
+//   - bounded grid-wide wait; block b reduces the records of requests b, b + G, ... to the
+//     step's token, LSE(z/T) and z at the token; bounded grid-wide wait; next step.
+// When each block owns a single tile and the W2 rows of it fit, they are staged in shared
+// memory once for all gamma steps.
+#include <algorithm>
+#include <cmath>
+
+#include "host_util.h"
+#include "markov_tile.cuh"
+
+namespace dspark {
+namespace {
+
+struct SampleArgs {
+    int B, gamma, V, r, nt, G;
+    int greedy;
+    float scale2;  // log2(e) / T
+    uint64_t seed;
+    const void* base;
+    const void* W1;
+    const void* W2;
+    const int32_t* anchor;
+    int32_t* tokens;
+    float* draft_lse;
+    float* zat;
+    WsHeader* hdr;
+    int32_t* cur_tok;
+    float4* part;  // [B][nt] tile records
+    uint64_t limit_ns;
+    int w2_smem;
+    int vec_ok;  // base rows start on 16-byte boundaries: 8-wide loads allowed
+};
+
+size_t sample_smem_bytes(int B, int r, bool mma, bool w2_smem) {
+    size_t b = sizeof(float) * kRows * kSRow + sizeof(float2) * kRows * kChunks + sizeof(RowBlock) +
+               align_up(sizeof(int) * (size_t)B, 16);
+    if (mma) {
+        if (w2_smem) b += (size_t)kTS * r * 2;
+    } else {
+        b += sizeof(float) * kRows * (size_t)r;
+    }
+    return b;
+}
+
+template <typename TL, int KS, typename TW>
+__global__ void __launch_bounds__(kThreads, 1) sample_kernel(SampleArgs a) {
+    constexpr bool kMMA = KS > 0;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    float* zbuf = reinterpret_cast<float*>(smem_raw);
+    float2* cstat = reinterpret_cast<float2*>(zbuf + kRows * kSRow);
+    RowBlock* rb = reinterpret_cast<RowBlock*>(cstat + kRows * kChunks);
+    int* prev = reinterpret_cast<int*>(rb + 1);
+    unsigned char* wreg = reinterpret_cast<unsigned char*>(prev) + align_up(sizeof(int) * (size_t)a.B, 16);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const TL* base = reinterpret_cast<const TL*>(a.base);
+
+    const uint4* w2s = nullptr;
+    if constexpr (kMMA) {
+        if (a.w2_smem) {
+            stage_w2_tile<KS>(reinterpret_cast<const uint16_t*>(a.W2), blockIdx.x * kTS, a.V,
+                              reinterpret_cast<uint4*>(wreg));
+            w2s = reinterpret_cast<const uint4*>(wreg);
+        }
+    }
+
+    uint32_t target = 0;
+    for (int step = 0; step < a.gamma; ++step) {
+        for (int j = tid; j < a.B; j += kThreads) {
+            int p;
+            if (step == 0) {
+                p = a.anchor[j];
+                if (p < 0 || p >= a.V) {
+                    record_status(&a.hdr->status, DSPARK_ERR_TOKEN_RANGE);
+                    p = min(max(p, 0), a.V - 1);
+                }
+            } else {
+                p = __ldcg(a.cur_tok + j);
+                if (p < 0 || p >= a.V) {  // only when every tile of a row had no mass (non-finite logits)
+                    record_status(&a.hdr->status, DSPARK_ERR_TOKEN_RANGE);
+                    p = min(max(p, 0), a.V - 1);
+                }
+            }
+            prev[j] = p;
+        }
+        __syncthreads();
+        for (int tile = blockIdx.x; tile < a.nt; tile += a.G) {
+            for (int row0 = 0; row0 < a.B; row0 += kRows) {
+                if (tid < kRows) {
+                    const int j = row0 + tid;
+                    rb->prev[tid] = (j < a.B) ? prev[j] : 0;
+                    rb->brow[tid] = (j < a.B) ? ((long long)j * a.gamma + step) * (long long)a.V : -1;
+                }
+                __syncthreads();
+                if constexpr (kMMA) {
+                    produce_z_mma<TL, KS>(base, reinterpret_cast<const uint16_t*>(a.W1),
+                                          reinterpret_cast<const uint16_t*>(a.W2), w2s, a.V, a.vec_ok != 0, tile,
+                                          *rb, zbuf, cstat, true, a.greedy, a.scale2);
+                } else {
+                    float* w1s = reinterpret_cast<float*>(wreg);
+                    const TW* W1 = reinterpret_cast<const TW*>(a.W1);
+                    for (int idx = tid; idx < kRows * a.r; idx += kThreads) {
+                        const int q = idx / a.r, k = idx % a.r;
+                        w1s[idx] = (rb->brow[q] >= 0) ? load_logit<TW>(W1, (size_t)rb->prev[q] * a.r + k) : 0.f;
+                    }
+                    __syncthreads();
+                    produce_z_gemv<TL, TW>(base, reinterpret_cast<const TW*>(a.W2), w1s, a.r, a.V, tile, *rb, zbuf,
+                                           cstat, true, a.greedy, a.scale2);
+                }
+                __syncthreads();
+                for (int rl = warp; rl < kRows; rl += kWarps) {
+                    const int j = row0 + rl;
+                    if (j >= a.B) continue;
+                    const float4 rec = finalize_tile(zbuf + rl * kSRow, cstat[rl * kChunks + lane], tile, a.V,
+                                                     a.greedy, a.scale2, a.seed, (uint32_t)j, (uint32_t)step + 1u,
+                                                     DSPARK_P_SAMPLE_TILE, DSPARK_P_SAMPLE_INTILE);
+                    if (lane == 0) a.part[(size_t)j * a.nt + tile] = rec;
+                }
+                __syncthreads();
+            }
+        }
+        target += (uint32_t)a.G;
+        if (!grid_wait(a.hdr, target, a.limit_ns)) return;
+        for (int j = blockIdx.x + a.G * warp; j < a.B; j += a.G * kWarps) {
+            const TileWinner w = reduce_tiles(a.part + (size_t)j * a.nt, a.nt, !a.greedy);
+            if (lane == 0) {
+                a.cur_tok[j] = w.cand;
+                const size_t o = (size_t)j * a.gamma + step;
+                a.tokens[o] = w.cand;
+                a.draft_lse[o] = a.greedy ? CUDART_NAN_F : w.lse;
+                a.zat[o] = w.val;
+            }
+        }
+        if (step + 1 < a.gamma) {
+            target += (uint32_t)a.G;
+            if (!grid_wait(a.hdr, target, a.limit_ns)) return;
+        }
+    }
+}
+
+using KernelFn = void (*)(SampleArgs);
+
+template <typename TL>
+KernelFn pick_mma(int r) {
+    switch (r) {
+        case 16: return sample_kernel<TL, 1, uint16_t>;
+        case 32: return sample_kernel<TL, 2, uint16_t>;
+        case 64: return sample_kernel<TL, 4, uint16_t>;
+        case 128: return sample_kernel<TL, 8, uint16_t>;
+        case 256: return sample_kernel<TL, 16, uint16_t>;
+        default: return nullptr;
+    }
+}
+
+KernelFn pick_kernel(const dspark_sample_params* p, bool mma) {
+    const bool lb = p->logits_dtype == DSPARK_BF16;
+    if (mma) return lb ? pick_mma<__nv_bfloat16>(p->r) : pick_mma<float>(p->r);
+    const bool wb = p->w_dtype == DSPARK_BF16;
+    if (lb) return wb ? sample_kernel<__nv_bfloat16, 0, __nv_bfloat16> : sample_kernel<__nv_bfloat16, 0, float>;
+    return wb ? sample_kernel<float, 0, __nv_bfloat16> : sample_kernel<float, 0, float>;
+}
+
+}  // namespace
+
+bool markov_use_mma(const dspark_sample_params* p) {
+    return p->r > 0 && p->w_dtype == DSPARK_BF16 &&
+           (p->r == 16 || p->r == 32 || p->r == 64 || p->r == 128 || p->r == 256);
+}
+
+dspark_status validate_sample_params(const dspark_sample_params* p) {
+    if (!p) return DSPARK_ERR_INVALID_ARG;
+    if (p->B < 1 || p->gamma < 1 || p->V < 1 || p->r < 0) return DSPARK_ERR_INVALID_ARG;
+    if (!(p->temperature >= 0.f) || std::isinf(p->temperature)) return DSPARK_ERR_INVALID_ARG;
+    if (p->logits_dtype != DSPARK_F32 && p->logits_dtype != DSPARK_BF16) return DSPARK_ERR_INVALID_ARG;
+    if (p->r > 0 && p->w_dtype != DSPARK_F32 && p->w_dtype != DSPARK_BF16) return DSPARK_ERR_INVALID_ARG;
+    if (p->B > 4096 || p->r > 1024 || p->gamma > 1024) return DSPARK_ERR_UNSUPPORTED;
+    return DSPARK_OK;
+}
+
+size_t sample_workspace_bytes(const dspark_sample_params* p) {
+    const size_t nt = (size_t)(p->V + kTS - 1) / kTS;
+    return kHeaderBytes + align_up(sizeof(int32_t) * (size_t)p->B, 256) +
+           align_up(sizeof(float4) * (size_t)p->B * nt, 256);
+}
+
+}  // namespace dspark
+
+using namespace dspark;
+
+extern "C" size_t dspark_sample_workspace_size(const dspark_sample_params* p) {
+    if (validate_sample_params(p) != DSPARK_OK) return 0;
+    return sample_workspace_bytes(p);
+}
+
+extern "C" dspark_status dspark_markov_sample_block(const dspark_sample_params* p, const void* base_logits,
+                                                    const void* W1, const void* W2, const int32_t* anchor,
+                                                    int32_t* tokens, float* draft_lse, float* draft_logit_at_tok,
+                                                    void* workspace, size_t ws_bytes, dspark_stream_t stream) {
+    dspark_status st = validate_sample_params(p);
+    if (st != DSPARK_OK) return st;
+    if (!base_logits || !anchor || !tokens || !draft_lse || !draft_logit_at_tok) return DSPARK_ERR_INVALID_ARG;
+    if (p->r > 0 && (!W1 || !W2)) return DSPARK_ERR_INVALID_ARG;
+    if (!workspace || ((uintptr_t)workspace & 255u) || ws_bytes < sample_workspace_bytes(p))
+        return DSPARK_ERR_WORKSPACE;
+
+    const bool mma = markov_use_mma(p);
+    const int nt = (p->V + kTS - 1) / kTS;
+    int sms = 0;
+    if (device_sm_count(&sms) != cudaSuccess) return DSPARK_ERR_CUDA;
+    KernelFn fn = pick_kernel(p, mma);
+    bool w2_smem = mma && (size_t)kTS * p->r * 2 <= 128 * 1024 && nt <= sms;
+    size_t smem = sample_smem_bytes(p->B, p->r, mma, w2_smem);
+    if (smem > kMaxSmem && w2_smem) {
+        w2_smem = false;
+        smem = sample_smem_bytes(p->B, p->r, mma, false);
+    }
+    if (smem > kMaxSmem) return DSPARK_ERR_UNSUPPORTED;
+    if (cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, (const void*)fn, kThreads, smem) != cudaSuccess ||
+        per_sm < 1)
+        return DSPARK_ERR_CUDA;
+    const int G = std::min(nt, sms * per_sm);
+    if (G < nt) w2_smem = false;  // a block owning several tiles cannot keep one tile's W2
+
+    SampleArgs a;
+    a.B = p->B;
+    a.gamma = p->gamma;
+    a.V = p->V;
+    a.r = p->r;
+    a.nt = nt;
+    a.G = G;
+    a.greedy = p->temperature == 0.f;
+    a.scale2 = a.greedy ? 1.f : kLog2e / p->temperature;
+    a.seed = p->seed;
+    a.base = base_logits;
+    a.W1 = W1;
+    a.W2 = W2;
+    a.anchor = anchor;
+    a.tokens = tokens;
+    a.draft_lse = draft_lse;
+    a.zat = draft_logit_at_tok;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    a.hdr = reinterpret_cast<WsHeader*>(ws);
+    a.cur_tok = reinterpret_cast<int32_t*>(ws + kHeaderBytes);
+    a.part = reinterpret_cast<float4*>(ws + kHeaderBytes + align_up(sizeof(int32_t) * (size_t)p->B, 256));
+    a.limit_ns = wait_limit_ns();
+    a.w2_smem = w2_smem;
+    const size_t esz = p->logits_dtype == DSPARK_BF16 ? 2 : 4;
+    a.vec_ok = ((uintptr_t)base_logits % 16 == 0) && (((size_t)p->V * esz) % 16 == 0);
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(workspace, 0, kHeaderBytes, s) != cudaSuccess) return DSPARK_ERR_CUDA;
+    void* args[] = {&a};
+    if (cudaLaunchCooperativeKernel((const void*)fn, dim3(G), dim3(kThreads), args, smem, s) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
+    return DSPARK_OK;
+}

@@ -1,0 +1,554 @@
+// verify.cu -- dspark_verify: lossless rejection-sampling verification.
+//
+// Method (P3 "如何评价 DeepSeek 发布 DSpark？" section "Speculative Decoding": the target scores
+// the drafted positions in one parallel pass, accepts left to right by rejection sampling,
+// truncates at the first failure and resamples from the target, so the output law equals the
+// target's; the verify tokens of all requests form one flattened list, P2 section 3.7.2).
+// Contract in dspark.h.
+//
+// Two launches, no grid-wide waits:
+//   1. rows: one block per (vocabulary segment, position, request) streams a target row segment
+//      and writes its (max, sum 2^(s2 - max)) (T > 0) or (max, argmax) (T = 0); the last block
+//      of a request (arrival counter) combines the segments and walks the accept tests
+//      left to right, writing n_accepted and, when needed, a job: RESID at the rejecting
+//      position or BONUS from target row L+1.
+//   2. jobs: one block per (tile, 16 requests): z = base + bias for RESID rows (same producer as
+//      the sampler), then per-id weights max(0, p - q) (RESID) or the target softmax (BONUS),
+//      chunk statistics and the tile's Gumbel record; the last block of a row block reduces the
+//      tile records to the correction token.  A residual without any mass falls back to a draw
+//      from p, done by that last block alone.
+#include <algorithm>
+
+#include "host_util.h"
+#include "markov_tile.cuh"
+
+namespace dspark {
+namespace {
+
+enum { JOB_NONE = 0, JOB_RESID = 1, JOB_BONUS = 2 };
+
+struct VerifyArgs {
+    int B, gamma, V, r, nt, nseg, segsz, gamma_t, nrb;
+    int greedy;
+    float scale2;  // log2(e) / T
+    float invT;
+    uint64_t seed;
+    const void* base;
+    const void* W1;
+    const void* W2;
+    const int32_t* anchor;
+    const int32_t* tokens;
+    const float* dlse;
+    const float* zat;
+    const void* target;
+    const int32_t* vlen;
+    const int32_t* toff;
+    int32_t* nacc;
+    int32_t* corr;
+    WsHeader* hdr;
+    uint32_t* cnt_req;  // [B]
+    uint32_t* cnt_rb;   // [nrb]
+    float2* rowpart;    // [B][gamma][nseg]
+    int4* job;          // [B] {type, position (1-based), prev token, lse2 bits of the target row}
+    float4* jobpart;    // [B][nt]
+    int vec_b, vec_t;
+};
+
+__device__ __forceinline__ int req_len(const VerifyArgs& a, int j) { return a.vlen ? a.vlen[j] : a.gamma; }
+__device__ __forceinline__ int req_rows(const VerifyArgs& a, int j) {
+    return a.toff ? a.toff[j + 1] - a.toff[j] : a.gamma_t;
+}
+__device__ __forceinline__ long long trow_off(const VerifyArgs& a, int j, int i) {
+    return a.toff ? ((long long)a.toff[j] + i - 1) * a.V : ((long long)j * a.gamma_t + i - 1) * a.V;
+}
+
+// Block-wide combine of per-thread (max, sum 2^(x - max)) pairs; result valid in thread 0.
+__device__ float2 block_lse_pair(float m, float s, float2* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    float wm = warp_max(m);
+    float ws = warp_sum(m == -CUDART_INF_F ? 0.f : s * ex2(m - wm));
+    if (lane == 0) red[warp] = make_float2(wm, ws);
+    __syncthreads();
+    float2 out = make_float2(-CUDART_INF_F, 0.f);
+    if (warp == 0) {
+        const float2 v = lane < nw ? red[lane] : make_float2(-CUDART_INF_F, 0.f);
+        const float M = warp_max(v.x);
+        const float S = warp_sum(v.x == -CUDART_INF_F ? 0.f : v.y * ex2(v.x - M));
+        out = make_float2(M, S);
+    }
+    __syncthreads();
+    return out;
+}
+
+__device__ float2 block_argmax_pair(float m, int idx, float2* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    warp_argmax(m, idx);
+    if (lane == 0) red[warp] = make_float2(m, __int_as_float(idx));
+    __syncthreads();
+    float2 out = make_float2(-CUDART_INF_F, __int_as_float(0x7fffffff));
+    if (warp == 0) {
+        float2 v = lane < nw ? red[lane] : make_float2(-CUDART_INF_F, __int_as_float(0x7fffffff));
+        float vm = v.x;
+        int vi = __float_as_int(v.y);
+        warp_argmax(vm, vi);
+        out = make_float2(vm, __int_as_float(vi));
+    }
+    __syncthreads();
+    return out;
+}
+
+// ------------------------------------------------------------------------------- launch 1
+template <typename TL>
+__global__ void __launch_bounds__(kThreads) verify_rows_kernel(VerifyArgs a) {
+    __shared__ float2 red[kWarps];
+    __shared__ int s_last;
+    const int seg = blockIdx.x, i = blockIdx.y + 1, j = blockIdx.z;
+    const int tid = threadIdx.x;
+    const int L = req_len(a, j);
+    const bool ok = L >= 1 && L <= a.gamma && req_rows(a, j) >= L;
+    if (!ok) {
+        if (i == 1 && seg == 0 && tid == 0) {
+            record_status(&a.hdr->status, DSPARK_ERR_TOKEN_RANGE);
+            a.nacc[j] = 0;
+            a.corr[j] = -1;
+            a.job[j] = make_int4(JOB_NONE, 0, 0, 0);
+        }
+        return;
+    }
+    if (i > L) return;
+    const TL* row = reinterpret_cast<const TL*>(a.target) + trow_off(a, j, i);
+    const int v_lo = seg * a.segsz, v_hi = min(a.V, v_lo + a.segsz);
+    float2 res;
+    if (a.greedy) {
+        float m = -CUDART_INF_F;
+        int idx = 0x7fffffff;
+        for (int v0 = v_lo + 8 * tid; v0 < v_hi; v0 += 8 * kThreads) {
+            float x[8];
+            load_vals8<TL>(row, v0, a.V, a.vec_t != 0, x);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (x[e] > m) {
+                    m = x[e];
+                    idx = v0 + e;
+                }
+        }
+        res = block_argmax_pair(m, idx, red);
+    } else {
+        float m = -CUDART_INF_F, s = 0.f;
+        for (int v0 = v_lo + 8 * tid; v0 < v_hi; v0 += 8 * kThreads) {
+            float x[8];
+            load_vals8<TL>(row, v0, a.V, a.vec_t != 0, x);
+            float gm = x[0];
+#pragma unroll
+            for (int e = 1; e < 8; ++e) gm = fmaxf(gm, x[e]);
+            const float mn = fmaxf(m, gm * a.scale2);
+            if (mn != -CUDART_INF_F) {
+                s = (m == -CUDART_INF_F) ? 0.f : s * ex2(m - mn);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s += ex2(fmaf(x[e], a.scale2, -mn));
+                m = mn;
+            }
+        }
+        res = block_lse_pair(m, s, red);
+    }
+    if (tid == 0) {
+        a.rowpart[((size_t)j * a.gamma + (i - 1)) * a.nseg + seg] = res;
+        __threadfence();
+        const uint32_t old = atomicAdd(&a.cnt_req[j], 1u);
+        s_last = (old == (uint32_t)(a.nseg * L - 1));
+    }
+    __syncthreads();
+    if (!s_last || tid >= 32) return;
+    __threadfence();
+
+    // ---- accept walk of request j (one warp; lane = segment)
+    const int lane = tid;
+    int n = L, corr = -1, jtype = JOB_NONE, jpos = 0, jprev = 0;
+    float jlse2 = 0.f;
+    const TL* tgt = reinterpret_cast<const TL*>(a.target);
+    for (int ii = 1; ii <= L; ++ii) {
+        const float2 p = lane < a.nseg ? __ldcg(&a.rowpart[((size_t)j * a.gamma + (ii - 1)) * a.nseg + lane])
+                                       : (a.greedy ? make_float2(-CUDART_INF_F, __int_as_float(0x7fffffff))
+                                                   : make_float2(-CUDART_INF_F, 0.f));
+        const int x = a.tokens[(size_t)j * a.gamma + ii - 1];
+        const bool xok = x >= 0 && x < a.V;
+        int accept;
+        int am = 0;
+        float lse2 = 0.f;
+        if (a.greedy) {
+            float m = p.x;
+            int idx = __float_as_int(p.y);
+            warp_argmax(m, idx);
+            am = idx;
+            accept = xok && (am == x);
+        } else {
+            const float M = warp_max(p.x);
+            const float S = warp_sum(p.x == -CUDART_INF_F ? 0.f : p.y * ex2(p.x - M));
+            lse2 = M + lg2(S);
+            accept = 0;
+            if (lane == 0 && xok) {
+                const float tx = load_logit<TL>(tgt, (size_t)(trow_off(a, j, ii) + x));
+                const float lnp = (tx * a.scale2 - lse2) * kLn2;
+                const float lnq = a.zat[(size_t)j * a.gamma + ii - 1] * a.invT - a.dlse[(size_t)j * a.gamma + ii - 1];
+                const float lnu = logf(uniform(a.seed, (uint32_t)j, (uint32_t)ii, DSPARK_P_ACCEPT, 0u));
+                accept = lnu < lnp - lnq;
+            }
+            accept = __shfl_sync(0xffffffffu, accept, 0);
+        }
+        if (!xok && lane == 0) record_status(&a.hdr->status, DSPARK_ERR_TOKEN_RANGE);
+        if (!accept) {
+            n = ii - 1;
+            if (!xok) break;
+            if (a.greedy) {
+                corr = am;
+            } else {
+                jtype = JOB_RESID;
+                jpos = ii;
+                jlse2 = lse2;
+                jprev = (ii == 1) ? a.anchor[j] : a.tokens[(size_t)j * a.gamma + ii - 2];
+                if (jprev < 0 || jprev >= a.V) {
+                    if (lane == 0) record_status(&a.hdr->status, DSPARK_ERR_TOKEN_RANGE);
+                    jtype = JOB_NONE;
+                }
+            }
+            break;
+        }
+    }
+    if (n == L && req_rows(a, j) > L) {
+        jtype = JOB_BONUS;
+        jpos = L + 1;
+    }
+    if (lane == 0) {
+        a.nacc[j] = n;
+        a.corr[j] = corr;
+        a.job[j] = make_int4(jtype, jpos, jprev, __float_as_int(jlse2));
+    }
+}
+
+// ------------------------------------------------------------------------------- launch 2
+// Whole-block tile-Gumbel draw from softmax(target row / T) with the RESID purposes: the
+// fallback when a residual max(0, p - q) has no mass at all.
+template <typename TL>
+__device__ int block_sample_row(const VerifyArgs& a, const TL* row, int j, int pos, float* sh) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float2* red = reinterpret_cast<float2*>(sh);
+    float* wsum = sh + 2 * kWarps;
+    float best_key = -CUDART_INF_F, best_mass = 0.f, best_m = 0.f;
+    int best_t = 0;
+    constexpr int per = kTS / kThreads;
+    for (int t = 0; t < a.nt; ++t) {
+        float x[per];
+        float m = -CUDART_INF_F;
+#pragma unroll
+        for (int e = 0; e < per; ++e) {
+            const int v = t * kTS + per * tid + e;
+            x[e] = v < a.V ? load_logit<TL>(row, (size_t)v) * a.scale2 : -CUDART_INF_F;
+            m = fmaxf(m, x[e]);
+        }
+        float s = 0.f;
+        if (m != -CUDART_INF_F)
+#pragma unroll
+            for (int e = 0; e < per; ++e) s += ex2(x[e] - m);
+        const float2 ms = block_lse_pair(m, s, red);
+        if (tid == 0 && ms.y > 0.f) {
+            const float key = (ms.x + lg2(ms.y)) * kLn2 -
+                              log_neg_log_u(uniform(a.seed, (uint32_t)j, (uint32_t)pos, DSPARK_P_RESID_TILE, (uint32_t)t));
+            if (key > best_key) {
+                best_key = key;
+                best_t = t;
+                best_mass = ms.y;
+                best_m = ms.x;
+            }
+        }
+    }
+    if (tid == 0) {
+        wsum[0] = __int_as_float(best_t);
+        wsum[1] = best_mass;
+        wsum[2] = best_m;
+    }
+    __syncthreads();
+    const int t = __float_as_int(wsum[0]);
+    const float St = wsum[1], mt = wsum[2];
+    __syncthreads();
+    float e[per], tot = 0.f;
+#pragma unroll
+    for (int q = 0; q < per; ++q) {
+        const int v = t * kTS + per * tid + q;
+        e[q] = v < a.V ? ex2(load_logit<TL>(row, (size_t)v) * a.scale2 - mt) : 0.f;
+        tot += e[q];
+    }
+    // exclusive scan of per-thread totals in id order
+    const float incl = warp_incl_scan(tot);
+    if (lane == 31) wsum[4 + warp] = incl;
+    __syncthreads();
+    float woff = 0.f;
+    for (int w = 0; w < warp; ++w) woff += wsum[4 + w];
+    const float up = uniform(a.seed, (uint32_t)j, (uint32_t)pos, DSPARK_P_RESID_INTILE, 0u);
+    const float target = up * St;
+    float c = woff + incl - tot;
+    int found = 0x7fffffff, lastnz = -1;
+#pragma unroll
+    for (int q = 0; q < per; ++q) {
+        c += e[q];
+        if (c > target && found == 0x7fffffff) found = t * kTS + per * tid + q;
+        if (e[q] > 0.f) lastnz = t * kTS + per * tid + q;
+    }
+    __syncthreads();
+    // lowest id crossing the target; else the highest id with mass
+    int* ires = reinterpret_cast<int*>(wsum + 4 + kWarps);
+    if (tid == 0) {
+        ires[0] = 0x7fffffff;
+        ires[1] = -1;
+    }
+    __syncthreads();
+    if (found != 0x7fffffff) atomicMin(&ires[0], found);
+    if (lastnz >= 0) atomicMax(&ires[1], lastnz);
+    __syncthreads();
+    const int x = ires[0] != 0x7fffffff ? ires[0] : ires[1];
+    __syncthreads();
+    return x;
+}
+
+template <typename TL, int KS, typename TW>
+__global__ void __launch_bounds__(kThreads, 1) verify_jobs_kernel(VerifyArgs a) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    float* zbuf = reinterpret_cast<float*>(smem_raw);
+    float2* cstat = reinterpret_cast<float2*>(zbuf + kRows * kSRow);
+    RowBlock* rb = reinterpret_cast<RowBlock*>(cstat + kRows * kChunks);
+    int4* jb = reinterpret_cast<int4*>(rb + 1);             // [kRows]
+    float* scratch = reinterpret_cast<float*>(jb + kRows);  // fallback scratch [64]
+    float* w1s = scratch + 64;                              // GEMV: [kRows][r]
+    __shared__ int s_any, s_last;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tile = blockIdx.x, row0 = blockIdx.y * kRows;
+    if (tid == 0) s_any = 0;
+    __syncthreads();
+    if (tid < kRows) {
+        const int j = row0 + tid;
+        int4 q = make_int4(JOB_NONE, 0, 0, 0);
+        if (j < a.B) q = a.job[j];
+        jb[tid] = q;
+        rb->prev[tid] = q.x == JOB_RESID ? q.z : 0;
+        rb->brow[tid] = q.x == JOB_RESID ? ((long long)j * a.gamma + q.y - 1) * (long long)a.V : -1;
+        if (q.x != JOB_NONE) atomicOr(&s_any, 1);
+    }
+    __syncthreads();
+    if (!s_any) return;
+    const TL* base = reinterpret_cast<const TL*>(a.base);
+    const TL* tgt = reinterpret_cast<const TL*>(a.target);
+    if constexpr (KS > 0) {
+        produce_z_mma<TL, KS>(base, reinterpret_cast<const uint16_t*>(a.W1), reinterpret_cast<const uint16_t*>(a.W2),
+                              nullptr, a.V, a.vec_b != 0, tile, *rb, zbuf, cstat, false, 0, a.scale2);
+    } else {
+        const TW* W1 = reinterpret_cast<const TW*>(a.W1);
+        for (int idx = tid; idx < kRows * a.r; idx += kThreads) {
+            const int q = idx / a.r, k = idx % a.r;
+            w1s[idx] = (rb->brow[q] >= 0) ? load_logit<TW>(W1, (size_t)rb->prev[q] * a.r + k) : 0.f;
+        }
+        __syncthreads();
+        produce_z_gemv<TL, TW>(base, reinterpret_cast<const TW*>(a.W2), w1s, a.r, a.V, tile, *rb, zbuf, cstat, false,
+                               0, a.scale2);
+    }
+    __syncthreads();
+    const int tile0 = tile * kTS;
+    for (int q = warp; q < kRows; q += kWarps) {
+        const int4 job = jb[q];
+        if (job.x == JOB_NONE) continue;
+        const int j = row0 + q;
+        const bool gre = a.greedy != 0;  // only BONUS jobs exist when T == 0
+        const TL* trow = tgt + trow_off(a, j, job.y);
+        const float lse2 = __int_as_float(job.w);
+        const float dl2 = job.x == JOB_RESID ? a.dlse[(size_t)j * a.gamma + job.y - 1] * kLog2e : 0.f;
+        float* xrow = zbuf + q * kSRow;
+        for (int c = 0; c < kChunks; ++c) {
+            const int v = tile0 + 32 * c + lane;
+            float l = -CUDART_INF_F;
+            if (v < a.V) {
+                const float t = load_logit<TL>(trow, (size_t)v);
+                if (gre) {
+                    l = t;
+                } else if (job.x == JOB_BONUS) {
+                    l = t * a.scale2;
+                } else {
+                    const float w = ex2(fmaf(t, a.scale2, -lse2)) - ex2(fmaf(xrow[32 * c + lane], a.scale2, -dl2));
+                    l = w > 0.f ? lg2(w) : -CUDART_INF_F;
+                }
+            }
+            xrow[32 * c + lane] = l;
+            float2 st;
+            if (gre) {
+                float m = l;
+                int idx = v < a.V ? v : 0x7fffffff;
+                warp_argmax(m, idx);
+                st = make_float2(m, __int_as_float(idx));
+            } else {
+                const float m = warp_max(l);
+                st = make_float2(m, warp_sum(m == -CUDART_INF_F ? 0.f : ex2(l - m)));
+            }
+            if (lane == 0) cstat[q * kChunks + c] = st;
+        }
+        __syncwarp();
+        const uint32_t pt = job.x == JOB_RESID ? DSPARK_P_RESID_TILE : DSPARK_P_BONUS_TILE;
+        const uint32_t pi = job.x == JOB_RESID ? DSPARK_P_RESID_INTILE : DSPARK_P_BONUS_INTILE;
+        const float4 rec = finalize_tile(xrow, cstat[q * kChunks + lane], tile, a.V, gre ? 1 : 0, 1.f, a.seed,
+                                         (uint32_t)j, (uint32_t)job.y, pt, pi);
+        if (lane == 0) a.jobpart[(size_t)j * a.nt + tile] = rec;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        const uint32_t old = atomicAdd(&a.cnt_rb[blockIdx.y], 1u);
+        s_last = (old == (uint32_t)(a.nt - 1));
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    __shared__ int s_fallback[kRows];
+    for (int q = warp; q < kRows; q += kWarps) {
+        const int4 job = jb[q];
+        if (job.x == JOB_NONE) continue;
+        const int j = row0 + q;
+        const TileWinner w = reduce_tiles(a.jobpart + (size_t)j * a.nt, a.nt, false);
+        if (lane == 0) {
+            s_fallback[q] = (w.cand < 0);
+            if (w.cand >= 0) a.corr[j] = w.cand;
+        }
+    }
+    __syncthreads();
+    for (int q = 0; q < kRows; ++q) {
+        const int4 job = jb[q];
+        if (job.x != JOB_RESID || !s_fallback[q]) continue;
+        const int j = row0 + q;
+        const int x = block_sample_row<TL>(a, tgt + trow_off(a, j, job.y), j, job.y, scratch);
+        if (tid == 0) a.corr[j] = x;
+    }
+}
+
+using RowsFn = void (*)(VerifyArgs);
+
+template <typename TL>
+RowsFn pick_jobs_mma(int r) {
+    switch (r) {
+        case 16: return verify_jobs_kernel<TL, 1, uint16_t>;
+        case 32: return verify_jobs_kernel<TL, 2, uint16_t>;
+        case 64: return verify_jobs_kernel<TL, 4, uint16_t>;
+        case 128: return verify_jobs_kernel<TL, 8, uint16_t>;
+        case 256: return verify_jobs_kernel<TL, 16, uint16_t>;
+        default: return nullptr;
+    }
+}
+
+RowsFn pick_jobs(const dspark_sample_params* p, bool mma) {
+    const bool lb = p->logits_dtype == DSPARK_BF16;
+    if (mma) return lb ? pick_jobs_mma<__nv_bfloat16>(p->r) : pick_jobs_mma<float>(p->r);
+    const bool wb = p->w_dtype == DSPARK_BF16;
+    if (lb) return wb ? verify_jobs_kernel<__nv_bfloat16, 0, __nv_bfloat16> : verify_jobs_kernel<__nv_bfloat16, 0, float>;
+    return wb ? verify_jobs_kernel<float, 0, __nv_bfloat16> : verify_jobs_kernel<float, 0, float>;
+}
+
+struct Layout {
+    int nt, nseg, segsz, nrb;
+    size_t off_cnt_req, off_cnt_rb, zero_bytes, off_rowpart, off_job, off_jobpart, total;
+};
+
+Layout layout(const dspark_sample_params* p) {
+    Layout L;
+    L.nt = (p->V + kTS - 1) / kTS;
+    int nseg = (p->V + 16383) / 16384;
+    nseg = std::max(1, std::min(32, nseg));
+    L.segsz = (int)align_up((size_t)((p->V + nseg - 1) / nseg), 8);
+    L.nseg = (p->V + L.segsz - 1) / L.segsz;
+    L.nrb = (p->B + kRows - 1) / kRows;
+    L.off_cnt_req = kHeaderBytes;
+    L.off_cnt_rb = L.off_cnt_req + sizeof(uint32_t) * (size_t)p->B;
+    L.zero_bytes = align_up(L.off_cnt_rb + sizeof(uint32_t) * (size_t)L.nrb, 256);
+    L.off_rowpart = L.zero_bytes;
+    L.off_job = L.off_rowpart + align_up(sizeof(float2) * (size_t)p->B * p->gamma * L.nseg, 256);
+    L.off_jobpart = L.off_job + align_up(sizeof(int4) * (size_t)p->B, 256);
+    L.total = L.off_jobpart + align_up(sizeof(float4) * (size_t)p->B * L.nt, 256);
+    return L;
+}
+
+}  // namespace
+}  // namespace dspark
+
+using namespace dspark;
+
+extern "C" size_t dspark_verify_workspace_size(const dspark_sample_params* p, int gamma_t) {
+    (void)gamma_t;
+    if (validate_sample_params(p) != DSPARK_OK) return 0;
+    return layout(p).total;
+}
+
+extern "C" dspark_status dspark_verify(const dspark_sample_params* p, const void* base_logits, const void* W1,
+                                       const void* W2, const int32_t* anchor, const int32_t* tokens,
+                                       const float* draft_lse, const float* draft_logit_at_tok,
+                                       const void* target_logits, int gamma_t, const int32_t* verify_len,
+                                       const int32_t* target_row_offsets, int32_t* n_accepted,
+                                       int32_t* correction_token, void* workspace, size_t ws_bytes,
+                                       dspark_stream_t stream) {
+    dspark_status st = validate_sample_params(p);
+    if (st != DSPARK_OK) return st;
+    if (!base_logits || !anchor || !tokens || !draft_lse || !draft_logit_at_tok || !target_logits || !n_accepted ||
+        !correction_token)
+        return DSPARK_ERR_INVALID_ARG;
+    if (p->r > 0 && (!W1 || !W2)) return DSPARK_ERR_INVALID_ARG;
+    if (!target_row_offsets && gamma_t < 1) return DSPARK_ERR_INVALID_ARG;
+    const Layout L = layout(p);
+    if (!workspace || ((uintptr_t)workspace & 255u) || ws_bytes < L.total) return DSPARK_ERR_WORKSPACE;
+    const bool mma = markov_use_mma(p);
+
+    VerifyArgs a;
+    a.B = p->B;
+    a.gamma = p->gamma;
+    a.V = p->V;
+    a.r = p->r;
+    a.nt = L.nt;
+    a.nseg = L.nseg;
+    a.segsz = L.segsz;
+    a.gamma_t = target_row_offsets ? 0 : gamma_t;
+    a.nrb = L.nrb;
+    a.greedy = p->temperature == 0.f;
+    a.scale2 = a.greedy ? 1.f : kLog2e / p->temperature;
+    a.invT = a.greedy ? 0.f : 1.f / p->temperature;
+    a.seed = p->seed;
+    a.base = base_logits;
+    a.W1 = W1;
+    a.W2 = W2;
+    a.anchor = anchor;
+    a.tokens = tokens;
+    a.dlse = draft_lse;
+    a.zat = draft_logit_at_tok;
+    a.target = target_logits;
+    a.vlen = verify_len;
+    a.toff = target_row_offsets;
+    a.nacc = n_accepted;
+    a.corr = correction_token;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    a.hdr = reinterpret_cast<WsHeader*>(ws);
+    a.cnt_req = reinterpret_cast<uint32_t*>(ws + L.off_cnt_req);
+    a.cnt_rb = reinterpret_cast<uint32_t*>(ws + L.off_cnt_rb);
+    a.rowpart = reinterpret_cast<float2*>(ws + L.off_rowpart);
+    a.job = reinterpret_cast<int4*>(ws + L.off_job);
+    a.jobpart = reinterpret_cast<float4*>(ws + L.off_jobpart);
+    const size_t esz = p->logits_dtype == DSPARK_BF16 ? 2 : 4;
+    const bool rows16 = ((size_t)p->V * esz) % 16 == 0;
+    a.vec_b = rows16 && ((uintptr_t)base_logits % 16 == 0);
+    a.vec_t = rows16 && ((uintptr_t)target_logits % 16 == 0);
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(workspace, 0, L.zero_bytes, s) != cudaSuccess) return DSPARK_ERR_CUDA;
+    void* args[] = {&a};
+    RowsFn rows = p->logits_dtype == DSPARK_BF16 ? verify_rows_kernel<__nv_bfloat16> : verify_rows_kernel<float>;
+    if (cudaLaunchKernel((const void*)rows, dim3(L.nseg, p->gamma, p->B), dim3(kThreads), args, 0, s) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
+    RowsFn jobs = pick_jobs(p, mma);
+    size_t smem = sizeof(float) * kRows * kSRow + sizeof(float2) * kRows * kChunks + sizeof(RowBlock) +
+                  sizeof(int4) * kRows + sizeof(float) * 64 + (mma ? 0 : sizeof(float) * kRows * (size_t)p->r);
+    if (smem > kMaxSmem) return DSPARK_ERR_UNSUPPORTED;
+    if (cudaFuncSetAttribute((const void*)jobs, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
+    if (cudaLaunchKernel((const void*)jobs, dim3(L.nt, L.nrb), dim3(kThreads), args, smem, s) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
+    return DSPARK_OK;
+}

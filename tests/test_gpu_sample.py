@@ -1,0 +1,113 @@
+"""Parity of dspark_markov_sample_block (CUDA) with the oracle on the same seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from parity import Tally, compare_block
+from semi_ar_draft_gb300 import api, binding
+from semi_ar_draft_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+TS = 1024
+
+
+def run_and_compare(wl, requests=None, tally=None):
+    t = wl.tensors
+    tok, lse, zat, ws = api.markov_sample_block(t["base"], t["W1"], t["W2"], t["anchor"], wl.T, wl.seed)
+    torch.cuda.synchronize()
+    assert binding.dspark_get_device_status(ws) == 0
+    base = W.np_view(t["base"])
+    W1 = None if t["W1"] is None else W.np_view(t["W1"])
+    W2 = None if t["W2"] is None else W.np_view(t["W2"])
+    anchor = t["anchor"].cpu().numpy()
+    g_tok, g_lse, g_zat = tok.cpu().numpy(), lse.cpu().numpy(), zat.cpu().numpy()
+    tally = tally or Tally()
+    reqs = range(wl.B) if requests is None else requests
+    for j in reqs:
+        ref = O.sample_request(base, W1, W2, int(anchor[j]), int(j), wl.T, wl.seed, TS)
+        compare_block(tally, g_tok[j], g_lse[j], g_zat[j], ref, wl.T, j)
+    return tally, (tok, lse, zat)
+
+
+@pytest.mark.parametrize("T", [0.0, 1.0])
+def test_tiny_fp32(T):
+    wl = W.tiny(T, device="cuda")
+    tally, _ = run_and_compare(wl)
+    tally.check_fraction()
+
+
+@pytest.mark.parametrize("r", [0, 16, 32, 64, 128, 256])
+@pytest.mark.parametrize("T", [0.0, 0.8])
+def test_bf16_ranks_ragged(r, T):
+    # V = 5000: four full tiles and a ragged one; B = 20: a full and a partial row block
+    wl = W.make_sample_workload("ragged", 20, 3, 5000, r, T, device="cuda", data_seed=r + 7, philox_seed=11,
+                                planted=3)
+    tally, _ = run_and_compare(wl)
+    tally.check_fraction()
+
+
+@pytest.mark.parametrize("wdt,r", [(torch.float32, 16), (torch.float32, 24), (torch.bfloat16, 24)])
+def test_cuda_core_path(wdt, r):
+    wl = W.make_sample_workload("gemv", 5, 4, 3000, r, 1.0, device="cuda", data_seed=3, philox_seed=5,
+                                logits_dtype=torch.float32, w_dtype=wdt, w_std=0.3)
+    tally, _ = run_and_compare(wl)
+    tally.check_fraction()
+
+
+def test_unaligned_vocab_scalar_loads():
+    wl = W.make_sample_workload("odd", 3, 3, 1001, 32, 1.0, device="cuda", data_seed=9, philox_seed=2, w_std=0.3)
+    tally, _ = run_and_compare(wl)
+    tally.check_fraction()
+
+
+def test_fp32_logits_bf16_weights_single_step():
+    wl = W.make_sample_workload("f32b", 17, 1, 2048, 64, 0.5, device="cuda", data_seed=4, philox_seed=9,
+                                logits_dtype=torch.float32, w_std=0.2)
+    tally, _ = run_and_compare(wl)
+    tally.check_fraction()
+
+
+def test_markov_bias_matters():
+    # with large weights the bias changes the drafted tokens: parity then really checks the GEMM
+    wl = W.make_sample_workload("bias", 16, 4, 4096, 64, 0.0, device="cuda", data_seed=1, w_std=0.5)
+    tally, (tok, _, _) = run_and_compare(wl)
+    t = wl.tensors
+    no_bias = torch.argmax(t["base"].float(), dim=-1).to(torch.int32)
+    assert (tok != no_bias).float().mean().item() > 0.5
+
+
+def test_deterministic_and_seed_dependent():
+    wl = W.make_sample_workload("det", 8, 4, 3000, 64, 1.0, device="cuda", data_seed=2)
+    t = wl.tensors
+    a = api.markov_sample_block(t["base"], t["W1"], t["W2"], t["anchor"], 1.0, 5)[0].clone()
+    b = api.markov_sample_block(t["base"], t["W1"], t["W2"], t["anchor"], 1.0, 5)[0].clone()
+    c = api.markov_sample_block(t["base"], t["W1"], t["W2"], t["anchor"], 1.0, 6)[0].clone()
+    assert torch.equal(a, b) and not torch.equal(a, c)
+
+
+def test_anchor_out_of_range_sets_status():
+    wl = W.make_sample_workload("bad", 4, 2, 2048, 16, 1.0, device="cuda")
+    t = wl.tensors
+    anchor = t["anchor"].clone()
+    anchor[2] = 5000
+    _, _, _, ws = api.markov_sample_block(t["base"], t["W1"], t["W2"], anchor, 1.0, 0)
+    assert binding.dspark_get_device_status(ws) == 7
+
+
+def test_full_b32_r64():
+    wl = W.b32_r64(device="cuda")
+    tally, _ = run_and_compare(wl)
+    tally.check_fraction()
+
+
+def test_full_b128_r256_sampled_requests():
+    wl = W.b128_r256(device="cuda")
+    tally, _ = run_and_compare(wl, requests=[0, 45, 127])
+    tally.check_fraction()
+
+
+def test_full_b512_r64_sampled_requests():
+    wl = W.b512_sched(device="cuda")
+    tally, _ = run_and_compare(wl, requests=[0, 300, 511])
+    tally.check_fraction()

@@ -1,0 +1,52 @@
+"""Parity of dspark_accept_rate_tv (CUDA) with the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from parity import close
+from semi_ar_draft_gb300 import api
+from semi_ar_draft_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def check(tv, rows=None):
+    t = tv.tensors
+    acc, mask, tau, _ = api.accept_rate_tv(t["d"], t["t"], t["keep"], t["pos_valid"])
+    torch.cuda.synchronize()
+    S, A, g = tv.S, tv.A, tv.gamma
+    keep = t["keep"].cpu().numpy()
+    pv = None if t["pos_valid"] is None else t["pos_valid"].cpu().numpy()
+    g_acc, g_mask, g_tau = acc.cpu().numpy(), mask.cpu().numpy(), tau.cpu().numpy()
+    # eval_mask is exact everywhere (integer decisions)
+    for s in range(S):
+        for a in range(A):
+            m, _ = O.eval_mask_tau(np.ones(g), int(keep[s, a]), None if pv is None else pv[s, a])
+            assert np.array_equal(g_mask[s, a], m.astype(np.float32))
+    blocks = [(s, a) for s in range(S) for a in range(A)] if rows is None else rows
+    for s, a in blocks:
+        d = W.np_view(t["d"][s, a])
+        tt = W.np_view(t["t"][s, a])
+        ref = np.array([O.tv_row(d[i], tt[i])[0] for i in range(g)])
+        close(g_acc[s, a], ref, what=f"acc[{s},{a}]")
+        _, rtau = O.eval_mask_tau(ref, int(keep[s, a]), None if pv is None else pv[s, a])
+        close([g_tau[s, a]], [rtau], what=f"tau[{s},{a}]")
+
+
+@pytest.mark.parametrize("V", [8, 1000, 4096, 33333])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_small(V, dtype):
+    check(W.make_tv_workload(2, 5, 3, V, device="cuda", dtype=dtype, data_seed=V, truncate=True, drop=0.3))
+
+
+def test_identical_rows_give_one():
+    tv = W.make_tv_workload(1, 3, 2, 5000, device="cuda")
+    t = tv.tensors
+    acc, mask, tau, _ = api.accept_rate_tv(t["d"], t["d"].clone(), t["keep"])
+    assert torch.allclose(acc, torch.ones_like(acc), atol=2e-6)
+
+
+def test_full_tv_4x512x8_sampled_rows():
+    tv = W.make_tv_workload(device="cuda", truncate=True)
+    check(tv, rows=[(0, 0), (1, 77), (2, 300), (3, 511)])
