@@ -66,20 +66,24 @@ enum {
     DSPARK_P_BONUS_INTILE = 7   /* verify: bonus draw, in tile */
 };
 
-/* Vocabulary tile of the sampler (see "Sampling contract" below). */
+/* Vocabulary tile and chunk of the sampler (see "Sampling contract" below). */
 #define DSPARK_TILE 1024
+#define DSPARK_CHUNK 32
 
 /*
  * Sampling contract (the pages never show the body of sample_tokens, P2 section 3.4;
  * any exact categorical draw is lossless, bit-parity needs one fixed definition):
  *   T == 0: x = argmax_v z_v, lowest index on ties.
- *   T  > 0: s = z / T.  Tiles of DSPARK_TILE consecutive ids; LSE_t = log sum_{v in t} e^{s_v}.
- *           t* = argmax_t (LSE_t - ln E_t), E_t = -ln U(seed, j, i, SAMPLE_TILE, t), lowest t on
- *           ties.  x = smallest v in t* with sum_{w in t*, w <= v} e^{s_w - LSE_t*} > U(seed, j, i,
- *           SAMPLE_INTILE, 0) (if rounding leaves none: the last v of t* with nonzero weight).
+ *   T  > 0: s = z / T.  Tiles of DSPARK_TILE consecutive ids, chunks of DSPARK_CHUNK consecutive
+ *           ids inside a tile; LSE of a set = log sum e^{s_v} over it.
+ *           t* = argmax_t (LSE_t - ln E_t), E_t = -ln U(seed, j, i, SAMPLE_TILE, t), lowest t on ties;
+ *           c* = smallest chunk c of t* with sum_{c' <= c} e^{LSE_c' - LSE_t*} > U(.., SAMPLE_INTILE, 0);
+ *           x  = smallest id v of c* with sum_{w in c*, w <= v} e^{s_w - LSE_c*} > U(.., SAMPLE_INTILE, 1);
+ *           where rounding leaves no crossing: the last chunk (id) with nonzero mass.
  *   This is softmax(s) exactly: Gumbel-max over tiles picks t with probability proportional to
- *   e^{LSE_t}, the inverse CDF picks v within t proportionally to e^{s_v}.  Residual and bonus
- *   draws in dspark_verify use the same contract on their own weights and purposes.
+ *   e^{LSE_t}; the two inverse CDFs, on independent uniforms, pick c and then v proportionally to
+ *   their masses.  Residual and bonus draws in dspark_verify use the same contract on their own
+ *   weights and purposes.
  */
 
 typedef struct {

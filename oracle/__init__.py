@@ -21,6 +21,7 @@ import subprocess
 import numpy as np
 
 F32, BF16 = 0, 1
+TILE, CHUNK = 1024, 32  # the library's vocabulary tile and chunk sizes
 P_SAMPLE_TILE, P_SAMPLE_INTILE, P_ACCEPT = 1, 2, 3
 P_RESID_TILE, P_RESID_INTILE, P_BONUS_TILE, P_BONUS_INTILE, P_ELEM_GUMBEL = 4, 5, 6, 7, 8
 
@@ -54,13 +55,13 @@ def lib():
         L.oracle_markov_logits.argtypes = [i32, i32, i32, i32, vp, vp, vp, i32, vp]
         L.oracle_argmax.argtypes = [vp, i32, vp]
         L.oracle_argmax.restype = i32
-        L.oracle_tile_gumbel.argtypes = [vp, i32, i32, u64, i32, i32, i32, i32, vp, vp]
+        L.oracle_tile_gumbel.argtypes = [vp, i32, i32, i32, u64, i32, i32, i32, i32, vp, vp]
         L.oracle_tile_gumbel.restype = i32
         L.oracle_gumbel_elem.argtypes = [vp, i32, u64, i32, i32, vp]
         L.oracle_gumbel_elem.restype = i32
-        L.oracle_sample_request.argtypes = [i32, i32, i32, i32, dbl, u64, i32, i32, vp, vp, vp, i32, i32,
+        L.oracle_sample_request.argtypes = [i32, i32, i32, i32, i32, dbl, u64, i32, i32, vp, vp, vp, i32, i32,
                                             vp, vp, vp, vp]
-        L.oracle_verify_request.argtypes = [i32, i32, i32, i32, i32, dbl, u64, i32, i32, i32, vp, vp, vp,
+        L.oracle_verify_request.argtypes = [i32, i32, i32, i32, i32, i32, dbl, u64, i32, i32, i32, vp, vp, vp,
                                             i32, i32, vp, vp, vp, vp, i32, vp, vp, vp]
         L.oracle_verify_request.restype = i32
         L.oracle_tv_row.argtypes = [i32, i32, vp, vp, vp]
@@ -71,9 +72,9 @@ def lib():
         L.oracle_schedule.restype = i32
         L.oracle_theta_schedule.argtypes = [i32, vp, vp, vp]
         L.oracle_theta_schedule.restype = i32
-        L.oracle_trials_sampler.argtypes = [i32, i32, vp, u64, i64, i32, vp]
-        L.oracle_trials_spec_one.argtypes = [i32, i32, dbl, vp, vp, u64, i64, vp, vp]
-        L.oracle_trials_spec_block.argtypes = [i32, i32, i32, i32, dbl, vp, vp, vp, i32, vp, u64, i64, vp]
+        L.oracle_trials_sampler.argtypes = [i32, i32, i32, vp, u64, i64, i32, vp]
+        L.oracle_trials_spec_one.argtypes = [i32, i32, i32, dbl, vp, vp, u64, i64, vp, vp]
+        L.oracle_trials_spec_block.argtypes = [i32, i32, i32, i32, i32, dbl, vp, vp, vp, i32, vp, u64, i64, vp]
         _lib = L
     return _lib
 
@@ -134,10 +135,11 @@ def argmax(z: np.ndarray):
     return int(x), float(m[0])
 
 
-def tile_gumbel(lw: np.ndarray, TS: int, seed: int, j: int, i: int, p_tile=P_SAMPLE_TILE, p_intile=P_SAMPLE_INTILE):
+def tile_gumbel(lw: np.ndarray, TS: int, seed: int, j: int, i: int, p_tile=P_SAMPLE_TILE, p_intile=P_SAMPLE_INTILE,
+                CS: int = CHUNK):
     lw = np.ascontiguousarray(lw, dtype=np.float64)
     m, lse = np.zeros(1), np.zeros(1)
-    x = lib().oracle_tile_gumbel(_p(lw), lw.shape[0], TS, seed, j, i, p_tile, p_intile, _p(m), _p(lse))
+    x = lib().oracle_tile_gumbel(_p(lw), lw.shape[0], TS, CS, seed, j, i, p_tile, p_intile, _p(m), _p(lse))
     return int(x), float(m[0]), float(lse[0])
 
 
@@ -148,7 +150,8 @@ def gumbel_elem(lw: np.ndarray, seed: int, j: int, i: int):
     return int(x), float(m[0])
 
 
-def sample_request(base: np.ndarray, W1, W2, anchor: int, j: int, T: float, seed: int, TS: int, row=None):
+def sample_request(base: np.ndarray, W1, W2, anchor: int, j: int, T: float, seed: int, TS: int, row=None,
+                   CS: int = CHUNK):
     """One request of dspark_markov_sample_block.  base: [B, gamma, V]; j is the
     request index (random stream); `row` selects the data block (default j)."""
     B, gamma, V = base.shape
@@ -157,25 +160,25 @@ def sample_request(base: np.ndarray, W1, W2, anchor: int, j: int, T: float, seed
     tok = np.zeros(gamma, dtype=np.int32)
     lse, zx, mg = np.zeros(gamma), np.zeros(gamma), np.zeros(gamma)
     w_dt = _dtype_code(W1) if r else F32
-    lib().oracle_sample_request(V, r, gamma, TS, float(T), seed, _dtype_code(base), w_dt, _p(blk),
+    lib().oracle_sample_request(V, r, gamma, TS, CS, float(T), seed, _dtype_code(base), w_dt, _p(blk),
                                 _p(W1) if r else None, _p(W2) if r else None, int(anchor), int(j),
                                 _p(tok), _p(lse), _p(zx), _p(mg))
     return tok, lse, zx, mg
 
 
-def sample_block(base, W1, W2, anchor, T, seed, TS, requests=None):
+def sample_block(base, W1, W2, anchor, T, seed, TS, requests=None, CS: int = CHUNK):
     """Oracle of dspark_markov_sample_block for the listed requests (default all)."""
     B, gamma, V = base.shape
     req = range(B) if requests is None else requests
     out = {}
     for j in req:
-        out[int(j)] = sample_request(base, W1, W2, int(anchor[j]), int(j), T, seed, TS)
+        out[int(j)] = sample_request(base, W1, W2, int(anchor[j]), int(j), T, seed, TS, CS=CS)
     return out
 
 
 # ----------------------------------------------------------------- verify
 def verify_request(base, W1, W2, anchor: int, j: int, tokens, draft_lse, z_at_tok, target, L: int,
-                   T: float, seed: int, TS: int, row=None):
+                   T: float, seed: int, TS: int, row=None, CS: int = CHUNK):
     """One request of dspark_verify.  base [B,gamma,V], target [B,gamma_t,V];
     tokens/draft_lse/z_at_tok: this request's gamma entries (int32 / float32);
     j is the request index (random stream); `row` selects the data (default j)."""
@@ -192,7 +195,7 @@ def verify_request(base, W1, W2, anchor: int, j: int, tokens, draft_lse, z_at_to
     mm = np.zeros(1)
     fb = np.zeros(1, dtype=np.int32)
     w_dt = _dtype_code(W1) if r else F32
-    n = lib().oracle_verify_request(V, r, gamma, gamma_t, TS, float(T), seed, _dtype_code(base), w_dt,
+    n = lib().oracle_verify_request(V, r, gamma, gamma_t, TS, CS, float(T), seed, _dtype_code(base), w_dt,
                                     _dtype_code(target), _p(bblk), _p(W1) if r else None,
                                     _p(W2) if r else None, int(anchor), int(j), _p(tok), _p(dl), _p(zx),
                                     _p(tblk), int(L), _p(corr), _p(mm), _p(fb))
@@ -241,23 +244,23 @@ def theta_schedule(c, sps):
 
 
 # ----------------------------------------------------------------- trial drivers
-def trials_sampler(lw, TS, seed, ntrials, variant=0):
+def trials_sampler(lw, TS, seed, ntrials, variant=0, CS: int = CHUNK):
     lw = np.ascontiguousarray(lw, dtype=np.float64)
     counts = np.zeros(lw.shape[0], dtype=np.int64)
-    lib().oracle_trials_sampler(lw.shape[0], TS, _p(lw), seed, int(ntrials), int(variant), _p(counts))
+    lib().oracle_trials_sampler(lw.shape[0], TS, CS, _p(lw), seed, int(ntrials), int(variant), _p(counts))
     return counts
 
 
-def trials_spec_one(zd, zt, T, TS, seed, ntrials):
+def trials_spec_one(zd, zt, T, TS, seed, ntrials, CS: int = CHUNK):
     zd = np.ascontiguousarray(zd, dtype=np.float32)
     zt = np.ascontiguousarray(zt, dtype=np.float32)
     em = np.zeros(zd.shape[0], dtype=np.int64)
     na = np.zeros(1, dtype=np.int64)
-    lib().oracle_trials_spec_one(zd.shape[0], TS, float(T), _p(zd), _p(zt), seed, int(ntrials), _p(em), _p(na))
+    lib().oracle_trials_spec_one(zd.shape[0], TS, CS, float(T), _p(zd), _p(zt), seed, int(ntrials), _p(em), _p(na))
     return em, int(na[0])
 
 
-def trials_spec_block(base_req, W1, W2, anchor, target_req, T, TS, seed, ntrials):
+def trials_spec_block(base_req, W1, W2, anchor, target_req, T, TS, seed, ntrials, CS: int = CHUNK):
     """fp32 blocks: base_req/target_req [gamma, V], W1/W2 [V, r].  Returns the
     histogram of the accepted length over ntrials independent draws."""
     base_req = np.ascontiguousarray(base_req, dtype=np.float32)
@@ -266,6 +269,6 @@ def trials_spec_block(base_req, W1, W2, anchor, target_req, T, TS, seed, ntrials
     W2 = np.ascontiguousarray(W2, dtype=np.float32)
     gamma, V = base_req.shape
     hist = np.zeros(gamma + 1, dtype=np.int64)
-    lib().oracle_trials_spec_block(V, W1.shape[1], gamma, TS, float(T), _p(base_req), _p(W1), _p(W2), int(anchor),
+    lib().oracle_trials_spec_block(V, W1.shape[1], gamma, TS, CS, float(T), _p(base_req), _p(W1), _p(W2), int(anchor),
                                    _p(target_req), seed, int(ntrials), _p(hist))
     return hist

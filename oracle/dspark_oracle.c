@@ -23,8 +23,8 @@
  * Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011).
  *
  * Pins (checked by the CPU test-suite): Philox known-answer vectors, closed
- * forms (sum-min = 1 - TV, residual + accepted mass = target), chi-square of
- * every sampler on V=8, brute force for the scheduler, exact enumeration of the
+ * forms (sum-min = 1 - TV, residual + accepted mass = target), direct checks of
+ * the tile / chunk / id inverse CDFs, chi-square of every sampler on V=8, brute force for the scheduler, exact enumeration of the
  * accepted-length law, and the worked example of the throughput-aware Theta
  * scheduler (P4 section 5.1).
  */
@@ -148,18 +148,41 @@ static double neg_log_u(double u) { return -log(u); }
 /* Tile-Gumbel categorical sampler over log-weights lw[0..V).          */
 /* The pages never show the body of sample_tokens (P2 section 3.4);    */
 /* this is the exact categorical draw fixed for bit-parity:            */
-/*   tiles of TS consecutive indices; LSE_t = log sum_{v in t} e^lw_v;  */
+/*   tiles of TS consecutive ids, chunks of CS consecutive ids inside  */
+/*   a tile; LSE of a set = log sum e^lw over it;                      */
 /*   t* = argmax_t LSE_t - ln E_t, E_t = -ln U(.., p_tile, t)          */
 /*   (lowest t on ties; tiles without mass never win);                 */
-/*   x = smallest v in t* whose in-order cumulative mass               */
-/*   sum_{w<=v} e^(lw_w - LSE_t*) exceeds u' = U(.., p_intile, 0);     */
-/*   if rounding leaves none, the last v of t* with nonzero weight.    */
-/* Gumbel-max over tiles gives P(t) proportional to e^LSE_t and the    */
-/* inverse CDF gives P(v | t) proportional to e^lw_v: the product is   */
+/*   c* = smallest chunk of t* whose in-order cumulative mass          */
+/*   sum_{c'<=c} e^(LSE_c' - LSE_t*) exceeds u1 = U(.., p_intile, 0);  */
+/*   x  = smallest id of c* whose in-order cumulative mass             */
+/*   sum_{w<=v} e^(lw_w - LSE_c*) exceeds u2 = U(.., p_intile, 1);     */
+/*   where rounding leaves no crossing, the last chunk (id) with mass. */
+/* Gumbel-max over tiles gives P(t) proportional to e^LSE_t; the two   */
+/* inverse CDFs (independent uniforms) give P(c | t) proportional to   */
+/* e^LSE_c and P(v | c) proportional to e^lw_v: the product is         */
 /* softmax(lw).  Returns x; *lse_all = log-sum-exp of all lw;          */
-/* *margin = min(tile-key gap, distance of u' to the CDF boundaries).  */
+/* *margin = min(tile-key gap, distance of u1 to the chunk CDF         */
+/* boundaries around c*, distance of u2 to the id CDF boundaries).     */
 /* ------------------------------------------------------------------ */
-int oracle_tile_gumbel(const double* lw, int V, int TS, uint64_t seed, int j, int i, int p_tile, int p_intile,
+static int inverse_cdf(const double* lw, int n, double lse, double u, double* margin) {
+    double cum = 0.0, prev_cum = 0.0;
+    int last_nz = -1;
+    for (int k = 0; k < n; ++k) {
+        double w = exp(lw[k] - lse);
+        if (w > 0.0) last_nz = k;
+        prev_cum = cum;
+        cum += w;
+        if (cum > u) {
+            double a = u - prev_cum, b = cum - u;
+            *margin = a < b ? a : b;
+            return k;
+        }
+    }
+    *margin = 0.0; /* rounding left the total below u */
+    return last_nz;
+}
+
+int oracle_tile_gumbel(const double* lw, int V, int TS, int CS, uint64_t seed, int j, int i, int p_tile, int p_intile,
                        double* margin, double* lse_all) {
     int nt = (V + TS - 1) / TS;
     double* lse_t = (double*)malloc(sizeof(double) * (size_t)nt);
@@ -186,32 +209,27 @@ int oracle_tile_gumbel(const double* lw, int V, int TS, uint64_t seed, int j, in
         if (margin) *margin = 0.0;
         return -1;
     }
-    double tile_margin = best_key - second_key; /* +inf when a single tile has mass */
-    double up = oracle_uniform(seed, (uint32_t)j, (uint32_t)i, (uint32_t)p_intile, 0u);
+    double m_tile = best_key - second_key; /* +inf when a single tile has mass */
+    double u1 = oracle_uniform(seed, (uint32_t)j, (uint32_t)i, (uint32_t)p_intile, 0u);
+    double u2 = oracle_uniform(seed, (uint32_t)j, (uint32_t)i, (uint32_t)p_intile, 1u);
     int lo = best * TS, n = (lo + TS <= V) ? TS : V - lo;
-    double cum = 0.0, prev_cum = 0.0;
-    int x = -1, last_nz = -1;
-    for (int v = lo; v < lo + n; ++v) {
-        double w = exp(lw[v] - lse_t[best]);
-        if (w > 0.0) last_nz = v;
-        prev_cum = cum;
-        cum += w;
-        if (cum > up) {
-            x = v;
-            break;
-        }
+    int nc = (n + CS - 1) / CS;
+    double* lse_c = (double*)malloc(sizeof(double) * (size_t)nc);
+    for (int c = 0; c < nc; ++c) {
+        int clo = lo + c * CS, cn = (c * CS + CS <= n) ? CS : n - c * CS;
+        lse_c[c] = logsumexp(lw + clo, cn);
     }
-    double cdf_margin;
-    if (x < 0) { /* rounding left the total below u' */
-        x = last_nz;
-        cdf_margin = 0.0;
-    } else {
-        double a = up - prev_cum, b = cum - up;
-        cdf_margin = a < b ? a : b;
+    double m_chunk, m_id;
+    int c = inverse_cdf(lse_c, nc, lse_t[best], u1, &m_chunk);
+    int clo = lo + c * CS, cn = (c * CS + CS <= n) ? CS : n - c * CS;
+    int k = inverse_cdf(lw + clo, cn, lse_c[c], u2, &m_id);
+    if (margin) {
+        double mg = m_tile < m_chunk ? m_tile : m_chunk;
+        *margin = mg < m_id ? mg : m_id;
     }
-    if (margin) *margin = tile_margin < cdf_margin ? tile_margin : cdf_margin;
     free(lse_t);
-    return x;
+    free(lse_c);
+    return clo + k;
 }
 
 /* Second sampler (reference for the chi-square test): per-element Gumbel-max,
@@ -243,7 +261,7 @@ int oracle_gumbel_elem(const double* lw, int V, uint64_t seed, int j, int i, dou
 /*   base_req: this request's [gamma, V] block of base logits;          */
 /*   W1, W2: [V, r]; j: request index (selects the random stream).      */
 /* ------------------------------------------------------------------ */
-void oracle_sample_request(int V, int r, int gamma, int TS, double T, uint64_t seed, int logits_dtype,
+void oracle_sample_request(int V, int r, int gamma, int TS, int CS, double T, uint64_t seed, int logits_dtype,
                            int w_dtype, const void* base_req, const void* W1, const void* W2, int anchor, int j,
                            int32_t* tokens, double* draft_lse, double* z_at_tok, double* margin) {
     double* z = (double*)malloc(sizeof(double) * (size_t)V);
@@ -261,7 +279,7 @@ void oracle_sample_request(int V, int r, int gamma, int TS, double T, uint64_t s
             lse = NAN;
         } else {
             for (int v = 0; v < V; ++v) s[v] = z[v] / T;
-            x = oracle_tile_gumbel(s, V, TS, seed, j, i, OR_P_SAMPLE_TILE, OR_P_SAMPLE_INTILE, &mg, &lse);
+            x = oracle_tile_gumbel(s, V, TS, CS, seed, j, i, OR_P_SAMPLE_TILE, OR_P_SAMPLE_INTILE, &mg, &lse);
         }
         tokens[step] = x;
         draft_lse[step] = lse;
@@ -295,7 +313,7 @@ void oracle_sample_request(int V, int r, int gamma, int TS, double T, uint64_t s
 /*   *min_margin over all decisions; *resid_fallback = 1 when the       */
 /*   residual had no mass and p was used instead.                       */
 /* ------------------------------------------------------------------ */
-int oracle_verify_request(int V, int r, int gamma, int gamma_t, int TS, double T, uint64_t seed,
+int oracle_verify_request(int V, int r, int gamma, int gamma_t, int TS, int CS, double T, uint64_t seed,
                           int logits_dtype, int w_dtype, int target_dtype, const void* base_req, const void* W1,
                           const void* W2, int anchor, int j, const int32_t* tokens, const float* draft_lse,
                           const float* z_at_tok, const void* target_req, int L, int32_t* correction,
@@ -351,10 +369,10 @@ int oracle_verify_request(int V, int r, int gamma, int gamma_t, int TS, double T
                 }
                 double mg;
                 if (any) {
-                    *correction = oracle_tile_gumbel(z, V, TS, seed, j, i, OR_P_RESID_TILE, OR_P_RESID_INTILE, &mg, NULL);
+                    *correction = oracle_tile_gumbel(z, V, TS, CS, seed, j, i, OR_P_RESID_TILE, OR_P_RESID_INTILE, &mg, NULL);
                 } else { /* p == q everywhere yet a float rejection: fall back to p */
                     if (resid_fallback) *resid_fallback = 1;
-                    *correction = oracle_tile_gumbel(lw, V, TS, seed, j, i, OR_P_RESID_TILE, OR_P_RESID_INTILE, &mg, NULL);
+                    *correction = oracle_tile_gumbel(lw, V, TS, CS, seed, j, i, OR_P_RESID_TILE, OR_P_RESID_INTILE, &mg, NULL);
                 }
                 if (mg < mm) mm = mg;
                 free(z);
@@ -371,7 +389,7 @@ int oracle_verify_request(int V, int r, int gamma, int gamma_t, int TS, double T
             *correction = oracle_argmax(tl, V, &mg);
         } else {
             for (int v = 0; v < V; ++v) lw[v] = tl[v] / T;
-            *correction = oracle_tile_gumbel(lw, V, TS, seed, j, i, OR_P_BONUS_TILE, OR_P_BONUS_INTILE, &mg, NULL);
+            *correction = oracle_tile_gumbel(lw, V, TS, CS, seed, j, i, OR_P_BONUS_TILE, OR_P_BONUS_INTILE, &mg, NULL);
         }
         if (mg < mm) mm = mg;
     }
@@ -523,13 +541,13 @@ int oracle_theta_schedule(int gamma, const double* c, const double* sps, double*
 /* ------------------------------------------------------------------ */
 /* Trial loops for the chi-square pins (thin drivers of the above).    */
 /* ------------------------------------------------------------------ */
-/* variant 0: tile-Gumbel with tile size TS; 1: per-element Gumbel-max.
+/* variant 0: tile-Gumbel with tile size TS and chunk size CS; 1: per-element Gumbel-max.
  * Trial n uses request index j = n, position i = 1. */
-void oracle_trials_sampler(int V, int TS, const double* lw, uint64_t seed, long ntrials, int variant,
+void oracle_trials_sampler(int V, int TS, int CS, const double* lw, uint64_t seed, long ntrials, int variant,
                            int64_t* counts) {
     for (int v = 0; v < V; ++v) counts[v] = 0;
     for (long n = 0; n < ntrials; ++n) {
-        int x = variant == 0 ? oracle_tile_gumbel(lw, V, TS, seed, (int)n, 1, OR_P_SAMPLE_TILE, OR_P_SAMPLE_INTILE, NULL, NULL)
+        int x = variant == 0 ? oracle_tile_gumbel(lw, V, TS, CS, seed, (int)n, 1, OR_P_SAMPLE_TILE, OR_P_SAMPLE_INTILE, NULL, NULL)
                              : oracle_gumbel_elem(lw, V, seed, (int)n, 1, NULL);
         counts[x] += 1;
     }
@@ -539,7 +557,7 @@ void oracle_trials_sampler(int V, int TS, const double* lw, uint64_t seed, long 
  * position, no bonus row): draft x ~ softmax(zd/T) by the tile sampler, verify
  * against softmax(zt/T); counts the emitted token (x if accepted, else the
  * residual draw) and the number of acceptances. */
-void oracle_trials_spec_one(int V, int TS, double T, const float* zd, const float* zt, uint64_t seed, long ntrials,
+void oracle_trials_spec_one(int V, int TS, int CS, double T, const float* zd, const float* zt, uint64_t seed, long ntrials,
                             int64_t* emitted, int64_t* n_accept) {
     double* s = (double*)malloc(sizeof(double) * (size_t)V);
     for (int v = 0; v < V; ++v) s[v] = (double)zd[v] / T;
@@ -547,10 +565,10 @@ void oracle_trials_spec_one(int V, int TS, double T, const float* zd, const floa
     *n_accept = 0;
     for (int v = 0; v < V; ++v) emitted[v] = 0;
     for (long n = 0; n < ntrials; ++n) {
-        int32_t x = oracle_tile_gumbel(s, V, TS, seed, (int)n, 1, OR_P_SAMPLE_TILE, OR_P_SAMPLE_INTILE, NULL, NULL);
+        int32_t x = oracle_tile_gumbel(s, V, TS, CS, seed, (int)n, 1, OR_P_SAMPLE_TILE, OR_P_SAMPLE_INTILE, NULL, NULL);
         float lse_f = (float)lse_d, zx_f = zd[x];
         int32_t corr;
-        int nacc = oracle_verify_request(V, 0, 1, 1, TS, T, seed, OR_F32, OR_F32, OR_F32, zd, NULL, NULL, 0, (int)n,
+        int nacc = oracle_verify_request(V, 0, 1, 1, TS, CS, T, seed, OR_F32, OR_F32, OR_F32, zd, NULL, NULL, 0, (int)n,
                                          &x, &lse_f, &zx_f, zt, 1, &corr, NULL, NULL);
         if (nacc == 1) {
             emitted[x] += 1;
@@ -566,7 +584,7 @@ void oracle_trials_spec_one(int V, int TS, double T, const float* zd, const floa
  * block base_req [gamma, V], target_req [gamma, V], W1/W2 [V, r] fp32):
  * trial n draws with request id n.  hist[k] counts trials with k accepted
  * tokens (k = 0..gamma). */
-void oracle_trials_spec_block(int V, int r, int gamma, int TS, double T, const float* base_req, const float* W1,
+void oracle_trials_spec_block(int V, int r, int gamma, int TS, int CS, double T, const float* base_req, const float* W1,
                               const float* W2, int anchor, const float* target_req, uint64_t seed, long ntrials,
                               int64_t* hist) {
     int32_t* tok = (int32_t*)malloc(sizeof(int32_t) * (size_t)gamma);
@@ -577,13 +595,13 @@ void oracle_trials_spec_block(int V, int r, int gamma, int TS, double T, const f
     float* zx_f = (float*)malloc(sizeof(float) * (size_t)gamma);
     for (int k = 0; k <= gamma; ++k) hist[k] = 0;
     for (long n = 0; n < ntrials; ++n) {
-        oracle_sample_request(V, r, gamma, TS, T, seed, OR_F32, OR_F32, base_req, W1, W2, anchor, (int)n, tok, lse, zx, mg);
+        oracle_sample_request(V, r, gamma, TS, CS, T, seed, OR_F32, OR_F32, base_req, W1, W2, anchor, (int)n, tok, lse, zx, mg);
         for (int i = 0; i < gamma; ++i) {
             lse_f[i] = (float)lse[i];
             zx_f[i] = (float)zx[i];
         }
         int32_t corr;
-        int nacc = oracle_verify_request(V, r, gamma, gamma, TS, T, seed, OR_F32, OR_F32, OR_F32, base_req, W1, W2,
+        int nacc = oracle_verify_request(V, r, gamma, gamma, TS, CS, T, seed, OR_F32, OR_F32, OR_F32, base_req, W1, W2,
                                          anchor, (int)n, tok, lse_f, zx_f, target_req, gamma, &corr, NULL, NULL);
         hist[nacc] += 1;
     }

@@ -59,22 +59,37 @@ def test_argmax_lowest_index_on_ties():
         assert O.argmax(z)[0] == int(np.argmax(z))
 
 
-def test_single_tile_is_inverse_cdf():
+def test_single_chunk_is_inverse_cdf():
     rng = np.random.default_rng(4)
     lw = rng.normal(0, 1.5, 8)
     p = special.softmax(lw)
     cdf = np.cumsum(p)
     for j in range(200):
-        x, m, lse = O.tile_gumbel(lw, 8, 5, j, 2)
-        u = O.uniform(5, j, 2, O.P_SAMPLE_INTILE, 0)
-        assert x == int(np.searchsorted(cdf, u, side="right"))
+        x, m, lse = O.tile_gumbel(lw, 8, 5, j, 2, CS=8)
+        u2 = O.uniform(5, j, 2, O.P_SAMPLE_INTILE, 1)
+        assert x == int(np.searchsorted(cdf, u2, side="right"))
         assert abs(lse - special.logsumexp(lw)) < 1e-12
+
+
+def test_two_level_inverse_cdf_within_a_tile():
+    # one tile of 12 ids in chunks of 4: chunk by u1 over chunk masses, id by u2 within it
+    rng = np.random.default_rng(14)
+    lw = rng.normal(0, 1.0, 12)
+    p = special.softmax(lw)
+    cmass = p.reshape(3, 4).sum(1)
+    for j in range(300):
+        x, m, lse = O.tile_gumbel(lw, 12, 6, j, 3, CS=4)
+        u1 = O.uniform(6, j, 3, O.P_SAMPLE_INTILE, 0)
+        u2 = O.uniform(6, j, 3, O.P_SAMPLE_INTILE, 1)
+        c = int(np.searchsorted(np.cumsum(cmass), u1, side="right"))
+        k = int(np.searchsorted(np.cumsum(p[4 * c:4 * c + 4] / cmass[c]), u2, side="right"))
+        assert x == 4 * c + k
 
 
 def test_tile_lse_output_and_no_mass_tiles():
     lw = np.array([-np.inf, -np.inf, 0.3, 1.0, -np.inf, -np.inf, -np.inf, -2.0])
     for j in range(300):
-        x, m, lse = O.tile_gumbel(lw, 2, 9, j, 1)
+        x, m, lse = O.tile_gumbel(lw, 4, 9, j, 1, CS=2)
         assert np.isfinite(lw[x])  # zero-weight entries are never drawn
     assert abs(lse - special.logsumexp(lw)) < 1e-12
 
@@ -85,12 +100,12 @@ def _chi2_p(counts, probs):
 
 
 @pytest.mark.parametrize("T", [0.7, 1.0])
-@pytest.mark.parametrize("TS,variant", [(2, 0), (3, 0), (8, 0), (8, 1)])
-def test_samplers_chi_square(T, TS, variant):
+@pytest.mark.parametrize("TS,CS,variant", [(2, 1, 0), (3, 2, 0), (8, 8, 0), (8, 3, 0), (4, 2, 0), (8, 8, 1)])
+def test_samplers_chi_square(T, TS, CS, variant):
     rng = np.random.default_rng(10)
     z = rng.normal(0, 1.2, 8)
     lw = z / T
-    counts = O.trials_sampler(lw, TS, 1234 + TS, 1_000_000, variant)
+    counts = O.trials_sampler(lw, TS, 1234 + TS + 7 * CS, 1_000_000, variant, CS=CS)
     assert _chi2_p(counts, special.softmax(lw)) > 1e-3
 
 
@@ -98,7 +113,7 @@ def test_chi_square_detects_a_wrong_law():
     # the same test must reject a sampler drawing from a slightly different law
     rng = np.random.default_rng(10)
     lw = rng.normal(0, 1.2, 8)
-    counts = O.trials_sampler(lw, 2, 77, 1_000_000, 0)
+    counts = O.trials_sampler(lw, 4, 77, 1_000_000, 0, CS=2)
     wrong = special.softmax(lw * 1.02)
     assert _chi2_p(counts, wrong) < 1e-6
 
@@ -128,11 +143,11 @@ def test_sample_request_carries_token_and_lse():
     W1 = rng.normal(0, 1.0, (V, r)).astype(np.float32)
     W2 = rng.normal(0, 1.0, (V, r)).astype(np.float32)
     T = 0.8
-    tok, lse, zx, mg = O.sample_request(base, W1, W2, 7, 0, T, 99, 16)
+    tok, lse, zx, mg = O.sample_request(base, W1, W2, 7, 0, T, 99, 16, CS=4)
     prev = 7
     for i in range(gamma):
         z = base[0, i].astype(np.float64) + W2.astype(np.float64) @ W1[prev].astype(np.float64)
-        x, m, l = O.tile_gumbel(z / T, 16, 99, 0, i + 1)
+        x, m, l = O.tile_gumbel(z / T, 16, 99, 0, i + 1, CS=4)
         assert tok[i] == x and abs(lse[i] - special.logsumexp(z / T)) < 1e-12
         assert abs(zx[i] - z[x]) < 1e-12
         prev = x

@@ -17,17 +17,17 @@ def test_accept_probability_is_sum_min(T):
     zd, zt = _logits(1), _logits(2)
     q, p = special.softmax(zd.astype(np.float64) / T), special.softmax(zt.astype(np.float64) / T)
     N = 400_000
-    em, na = O.trials_spec_one(zd, zt, T, 3, 21, N)
+    em, na = O.trials_spec_one(zd, zt, T, 3, 21, N, CS=2)
     pa = np.minimum(p, q).sum()
     assert abs(pa - (1 - 0.5 * np.abs(p - q).sum())) < 1e-12
     assert abs(na / N - pa) < 5 * np.sqrt(pa * (1 - pa) / N)
 
 
-@pytest.mark.parametrize("T,TS", [(1.0, 8), (0.7, 2), (1.0, 3)])
-def test_emitted_token_law_is_target(T, TS):
+@pytest.mark.parametrize("T,TS,CS", [(1.0, 8, 8), (0.7, 2, 1), (1.0, 3, 2), (1.0, 8, 4)])
+def test_emitted_token_law_is_target(T, TS, CS):
     zd, zt = _logits(3), _logits(4)
     p = special.softmax(zt.astype(np.float64) / T)
-    em, na = O.trials_spec_one(zd, zt, T, TS, 31 + TS, 1_000_000)
+    em, na = O.trials_spec_one(zd, zt, T, TS, 31 + TS + CS, 1_000_000, CS=CS)
     assert stats.chisquare(em, p * em.sum()).pvalue > 1e-3
 
 
@@ -57,9 +57,9 @@ def test_residual_support_is_where_target_exceeds_draft():
     tgt = zt.reshape(1, 1, 8)
     seen = set()
     for j in range(3000):
-        x, _, _ = O.tile_gumbel(zd.astype(np.float64) / T, 8, 3, j, 1)
+        x, _, _ = O.tile_gumbel(zd.astype(np.float64) / T, 8, 3, j, 1, CS=4)
         n, corr, mm, fb = O.verify_request(base, None, None, 0, j, np.array([x], np.int32), np.array([lse_d]),
-                                           np.array([zd[x]]), tgt, 1, T, 3, 8, row=0)
+                                           np.array([zd[x]]), tgt, 1, T, 3, 8, row=0, CS=4)
         if n == 0:
             assert p[corr] > q[corr] and fb == 0
             seen.add(corr)
@@ -105,8 +105,8 @@ def _exact_accept_len_law(base, W1, W2, anchor, tgt, T):
     return np.array([ge[k] - ge[k + 1] for k in range(gamma + 1)])
 
 
-@pytest.mark.parametrize("T,TS", [(1.0, 8), (0.7, 3)])
-def test_accepted_length_law_exact(T, TS):
+@pytest.mark.parametrize("T,TS,CS", [(1.0, 8, 8), (0.7, 3, 2)])
+def test_accepted_length_law_exact(T, TS, CS):
     rng = np.random.default_rng(12)
     V, gamma, r = 8, 3, 2
     base = rng.normal(0, 1.0, (gamma, V)).astype(np.float32)
@@ -115,7 +115,7 @@ def test_accepted_length_law_exact(T, TS):
     tgt = (base + rng.normal(0, 0.6, (gamma, V))).astype(np.float32)
     law = _exact_accept_len_law(base, W1, W2, 4, tgt, T)
     assert abs(law.sum() - 1) < 1e-12
-    hist = O.trials_spec_block(base, W1, W2, 4, tgt, T, TS, 55, 1_000_000)
+    hist = O.trials_spec_block(base, W1, W2, 4, tgt, T, TS, 55, 1_000_000, CS=CS)
     assert stats.chisquare(hist, law * hist.sum()).pvalue > 1e-3
     # a plausible mistake (ignoring the Markov bias when verifying) changes the law
     law0 = _exact_accept_len_law(base, W1 * 0, W2, 4, tgt, T)
