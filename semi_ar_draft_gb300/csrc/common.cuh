@@ -161,18 +161,24 @@ __device__ __forceinline__ void warp_argmax(float& v, int& idx) {
 // ---------------------------------------------------------------- grid-wide wait
 // All blocks of a co-resident (cooperative) grid meet here.  `target` is the total number of
 // arrivals expected so far (a monotonically growing counter, zeroed before the launch).
-// The wait is bounded: past `limit_ns`, or once another block has recorded an error, it
-// records DSPARK_ERR_TIMEOUT (first error wins) and returns false; the caller must return.
-__device__ __forceinline__ bool grid_wait(WsHeader* h, uint32_t target, uint64_t limit_ns) {
-    __shared__ int s_ok;
+// The wait is bounded: past `limit_ns` it records DSPARK_ERR_TIMEOUT (first error wins) and
+// returns false, as it does once another block has recorded a timeout; the caller must return.
+// Split phase: grid_arrive() then independent work then grid_wait_arrived().
+__device__ __forceinline__ void grid_arrive(WsHeader* h) {
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
         atomicAdd(&h->arrivals, 1u);
+    }
+}
+
+__device__ __forceinline__ bool grid_wait_arrived(WsHeader* h, uint32_t target, uint64_t limit_ns) {
+    __shared__ int s_ok;
+    if (threadIdx.x == 0) {
         int ok = 1;
         const uint64_t t0 = global_ns();
         while (ld_acquire_u32(&h->arrivals) < target) {
-            if (ld_relaxed_s32(&h->status) != 0) {
+            if (ld_relaxed_s32(&h->status) == DSPARK_ERR_TIMEOUT) {  // another block gave up
                 ok = 0;
                 break;
             }
@@ -187,6 +193,11 @@ __device__ __forceinline__ bool grid_wait(WsHeader* h, uint32_t target, uint64_t
     }
     __syncthreads();
     return s_ok != 0;
+}
+
+__device__ __forceinline__ bool grid_wait(WsHeader* h, uint32_t target, uint64_t limit_ns) {
+    grid_arrive(h);
+    return grid_wait_arrived(h, target, limit_ns);
 }
 
 }  // namespace dspark

@@ -1,11 +1,15 @@
-// markov_tile.cuh -- the per-tile building blocks shared by the sampling and verify kernels.
+// markov_tile.cuh -- per-tile building blocks shared by the sampling and verify kernels.
 //
-// A "tile" is DSPARK_TILE consecutive vocabulary ids; a "row block" is 16 rows (requests).
-// Producers compute z = base + W2 . W1[prev] for a row block over one tile into a shared
-// memory buffer (fp32, padded stride) and, optionally, per-32-id chunk statistics.
-// finalize_tile() turns a row's chunk statistics and buffered values into the tile's record
-// of the tile-Gumbel contract (dspark.h): log-mass, Gumbel key, and the in-tile inverse-CDF
-// candidate, drawn speculatively before the winning tile is known.
+// A "tile" is DSPARK_TILE consecutive vocabulary ids, a "chunk" DSPARK_CHUNK consecutive ids
+// of a tile, a "row block" 16 rows (requests).  The producer computes, for a row block over
+// one tile, z = base + W2 . W1[prev] in registers (tensor-core mma.sync bf16 with the
+// accumulator initialised from the base logits, or a CUDA-core GEMV), turns it into the row's
+// log2-weights (draft sampling, residual or bonus draw) and reduces every chunk to a record
+//   {max log2-weight m_c, sum 2^(l - m_c), in-chunk inverse-CDF candidate, value at it}
+// (greedy: {max value, -, lowest argmax, max value}).  finalize_chunks() turns a row's 32 chunk
+// records into the tile record of the sampling contract (dspark.h): the Gumbel key, the
+// tile's log-mass, and the chunk-level inverse-CDF choice -- all before the winning tile is
+// known, so no per-id data has to stay on chip.
 #pragma once
 
 #include "common.cuh"
@@ -15,20 +19,27 @@ namespace dspark {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kTS = DSPARK_TILE;
-constexpr int kChunks = kTS / 32;
+constexpr int kCS = DSPARK_CHUNK;
+constexpr int kChunks = kTS / kCS;
 constexpr int kRows = 16;
-constexpr int kSRow = kTS + 4;  // padded row stride (floats): the 16-byte stores of a quarter-warp are conflict-free
-static_assert(kChunks == 32, "one warp lane per chunk");
+constexpr int kChunksPerWarp = kChunks / kWarps;
+static_assert(kChunks == 32, "one warp lane per chunk in finalize_chunks");
+static_assert(kCS == 32, "a lane quad holds one chunk: 4 lanes x 8 ids");
+
+enum RowMode { ROW_OFF = 0, ROW_SAMPLE = 1, ROW_RESID = 2, ROW_BONUS = 3 };
 
 // Per-row inputs of a row block, staged in shared memory by the caller.
 struct RowBlock {
-    int prev[kRows];      // W1 row (previous token) of each row
-    long long brow[kRows];  // element offset of the row's base logits (-1: row not computed)
+    int prev[kRows];         // W1 row (previous token)
+    int mode[kRows];         // RowMode
+    long long brow[kRows];   // element offset of the base-logit row (-1: z not needed)
+    long long trow[kRows];   // element offset of the target-logit row (-1: none)
+    float u1[kRows];         // chunk-level uniform
+    float u2[kRows];         // id-level uniform
+    float lnE[kRows];        // ln of the tile's exponential variate
+    float lse2[kRows];       // residual: log2-sum-exp of the target row (t * scale2)
+    float dl2[kRows];        // residual: draft LSE in log2 units
 };
-
-__device__ __forceinline__ float2 empty_stat(int greedy) {
-    return greedy ? make_float2(-CUDART_INF_F, __int_as_float(0x7fffffff)) : make_float2(-CUDART_INF_F, 0.f);
-}
 
 __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t a0, const uint32_t a1, const uint32_t a2,
                                          const uint32_t a3, const uint32_t b0, const uint32_t b1) {
@@ -37,6 +48,11 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t a0, const
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// L2 prefetch of a contiguous byte range (16-byte aligned, multiple of 16 bytes).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // --------------------------------------------------------------------------------------------
@@ -50,7 +66,7 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t a0, const
 // --------------------------------------------------------------------------------------------
 template <int KS>
 struct Frag {
-    uint32_t w[2 * KS];  // the lane's r/4 weights of one row, as bf16 pairs
+    uint32_t w[KS > 0 ? 2 * KS : 1];  // the lane's r/4 weights of one row, as bf16 pairs
 };
 
 template <int KS>
@@ -127,27 +143,69 @@ __device__ void stage_w2_tile(const uint16_t* W2, int tile0, int V, uint4* dst) 
     }
 }
 
+// --------------------------------------------------------------------------------------------
+// Eight consecutive logits kept as raw words until needed (so many loads can be in flight).
+// --------------------------------------------------------------------------------------------
 template <typename TL>
-__device__ __forceinline__ void load_vals8(const TL* row, int v0, int V, bool vec, float (&x)[8]) {
+struct Raw8 {
+    static constexpr int kWords = sizeof(TL) * 2;  // bf16: 4 words, fp32: 8 words
+    uint32_t w[kWords];
+};
+
+template <typename TL>
+__device__ __forceinline__ void load_raw8(const TL* row, int v0, int V, bool vec, Raw8<TL>& r) {
     if (vec && v0 + 8 <= V) {
-        load8<TL>(row, (size_t)v0, x);
-    } else {
+        const uint4* p = reinterpret_cast<const uint4*>(row + v0);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = (v0 + e < V) ? load_logit<TL>(row, (size_t)(v0 + e)) : -CUDART_INF_F;
+        for (int q = 0; q < Raw8<TL>::kWords / 4; ++q) {
+            const uint4 u = __ldg(p + q);
+            r.w[4 * q] = u.x;
+            r.w[4 * q + 1] = u.y;
+            r.w[4 * q + 2] = u.z;
+            r.w[4 * q + 3] = u.w;
+        }
+    } else if constexpr (sizeof(TL) == 2) {
+        const unsigned short* p = reinterpret_cast<const unsigned short*>(row);
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            const uint32_t lo = (v0 + e < V) ? __ldg(p + v0 + e) : 0xFF80u;  // bf16 -inf past V
+            const uint32_t hi = (v0 + e + 1 < V) ? __ldg(p + v0 + e + 1) : 0xFF80u;
+            r.w[e / 2] = lo | (hi << 16);
+        }
+    } else {
+        const float* p = reinterpret_cast<const float*>(row);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) r.w[e] = (v0 + e < V) ? __float_as_uint(__ldg(p + v0 + e)) : 0xFF800000u;
     }
 }
 
-// Chunk statistics of 8 values per lane, combined over the lane quad (tq = 0..3 hold ids
-// 8*tq.. of the chunk).  T > 0: (max s2, sum 2^(s2 - max)) with s2 = x * scale2;
-// greedy: (max x, lowest argmax id).
-__device__ __forceinline__ float2 quad_stats(const float (&z)[8], int id0, int greedy, float scale2) {
+template <typename TL>
+__device__ __forceinline__ void unpack8(const Raw8<TL>& r, float (&x)[8]) {
+    if constexpr (sizeof(TL) == 2) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            x[2 * q] = bf16_lo(r.w[q]);
+            x[2 * q + 1] = bf16_hi(r.w[q]);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(r.w[e]);
+    }
+}
+
+// --------------------------------------------------------------------------------------------
+// Chunk record from one lane quad (lane tq holds ids id0 .. id0+7 = chunk base + 8 tq).
+// --------------------------------------------------------------------------------------------
+__device__ __forceinline__ float4 chunk_record(const float (&l)[8], const float (&val)[8], int id0, float u2,
+                                               int greedy) {
+    const int tq = threadIdx.x & 3;
     if (greedy) {
-        float m = z[0];
+        float m = l[0];
         int idx = id0;
 #pragma unroll
         for (int e = 1; e < 8; ++e)
-            if (z[e] > m) {
-                m = z[e];
+            if (l[e] > m) {
+                m = l[e];
                 idx = id0 + e;
             }
 #pragma unroll
@@ -159,187 +217,252 @@ __device__ __forceinline__ float2 quad_stats(const float (&z)[8], int id0, int g
                 idx = oi;
             }
         }
-        return make_float2(m, __int_as_float(idx));
+        return make_float4(m, 0.f, __int_as_float(idx), m);
     }
-    float s[8];
-    float m = -CUDART_INF_F;
+    // Every lane runs every shuffle below (full-warp masks): a quad without mass is only
+    // masked out at the end, never by an early return.
+    float m = l[0];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        s[e] = z[e] * scale2;
-        m = fmaxf(m, s[e]);
-    }
+    for (int e = 1; e < 8; ++e) m = fmaxf(m, l[e]);
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-    float acc = 0.f;
-    if (m != -CUDART_INF_F) {
+    const bool empty = m == -CUDART_INF_F;  // quad-uniform
+    const float mref = empty ? 0.f : m;
+    float cum[8];
+    float run = 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc += ex2(s[e] - m);
+    for (int e = 0; e < 8; ++e) {
+        run += ex2(l[e] - mref);  // 0 for -inf entries
+        cum[e] = run;
     }
-    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-    return make_float2(m, acc);
+    // inclusive scan of the lane totals over the quad (ids are in lane order)
+    float incl = run;
+    float t = __shfl_up_sync(0xffffffffu, incl, 1, 4);
+    if (tq >= 1) incl += t;
+    t = __shfl_up_sync(0xffffffffu, incl, 2, 4);
+    if (tq >= 2) incl += t;
+    const float before = incl - run;
+    const float S = __shfl_sync(0xffffffffu, incl, 3, 4);
+    const float target = u2 * S;
+    int first = 0x7fffffff, lastnz = -1;
+    float vfirst = 0.f, vlast = 0.f;
+#pragma unroll
+    for (int e = 7; e >= 0; --e) {
+        if (before + cum[e] > target) {
+            first = id0 + e;
+            vfirst = val[e];
+        }
+        const float w = (e == 0) ? cum[0] : cum[e] - cum[e - 1];
+        if (lastnz < 0 && w > 0.f) {
+            lastnz = id0 + e;
+            vlast = val[e];
+        }
+    }
+    // quad: lowest crossing id; else highest id with mass
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+        const int of = __shfl_xor_sync(0xffffffffu, first, o);
+        const float ovf = __shfl_xor_sync(0xffffffffu, vfirst, o);
+        if (of < first) {
+            first = of;
+            vfirst = ovf;
+        }
+        const int ol = __shfl_xor_sync(0xffffffffu, lastnz, o);
+        const float ovl = __shfl_xor_sync(0xffffffffu, vlast, o);
+        if (ol > lastnz) {
+            lastnz = ol;
+            vlast = ovl;
+        }
+    }
+    if (empty) return make_float4(-CUDART_INF_F, 0.f, __int_as_float(-1), 0.f);
+    const bool hit = first != 0x7fffffff;
+    return make_float4(m, S, __int_as_float(hit ? first : lastnz), hit ? vfirst : vlast);
 }
 
-// z = base + bias for the row block over one tile, tensor-core path.  Writes zbuf[16][kSRow]
-// and, when `stats`, cstat[16][kChunks].  Rows with brow < 0 get A = 0 and base = 0.
-template <typename TL, int KS>
-__device__ inline void produce_z_mma(const TL* base, const uint16_t* W1, const uint16_t* W2, const uint4* w2s, int V,
-                              bool vec_ok, int tile, const RowBlock& rb, float* zbuf, float2* cstat, bool stats,
-                              int greedy, float scale2) {
+__device__ __forceinline__ float4 empty_record(int greedy) {
+    return greedy ? make_float4(-CUDART_INF_F, 0.f, __int_as_float(0x7fffffff), -CUDART_INF_F)
+                  : make_float4(-CUDART_INF_F, 0.f, __int_as_float(-1), 0.f);
+}
+
+// --------------------------------------------------------------------------------------------
+// Producer: chunk records crec[16][32] of a row block over one tile.
+// --------------------------------------------------------------------------------------------
+struct ProdArgs {
+    const void* base;
+    const void* target;
+    const void* W1;
+    const void* W2;
+    const uint4* w2s;   // W2 tile in shared memory (tensor-core path) or null
+    const float* w1s;   // W1 rows of the row block as fp32 [16][r] (CUDA-core path)
+    int V, r;
+    int greedy;
+    float scale2;       // log2(e) / T
+    int vec_b, vec_t;   // 16-byte aligned rows: 8-wide loads allowed
+};
+
+// HAS_T: rows may read target logits (residual / bonus draws of the verify pass).
+template <typename TL, int KS, typename TW, bool HAS_T>
+__device__ __forceinline__ void produce_chunks(const ProdArgs& pa, int tile, const RowBlock& rb, float4* crec) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, tq = lane & 3;
-    const bool okA = rb.brow[g] >= 0, okB = rb.brow[g + 8] >= 0;
+    const int ma = rb.mode[g], mb = rb.mode[g + 8];
+    const bool za = ma == ROW_SAMPLE || ma == ROW_RESID, zb = mb == ROW_SAMPLE || mb == ROW_RESID;
+    const bool ta = HAS_T && (ma == ROW_RESID || ma == ROW_BONUS);
+    const bool tb = HAS_T && (mb == ROW_RESID || mb == ROW_BONUS);
+    const bool need_z = __any_sync(0xffffffffu, za || zb);
+    const bool need_t = HAS_T && __any_sync(0xffffffffu, ta || tb);
+    const TL* base = reinterpret_cast<const TL*>(pa.base);
+    const TL* tgt = reinterpret_cast<const TL*>(pa.target);
+    const TL* browA = base + (za ? rb.brow[g] : 0);
+    const TL* browB = base + (zb ? rb.brow[g + 8] : 0);
+    const TL* trowA = tgt + (ta ? rb.trow[g] : 0);
+    const TL* trowB = tgt + (tb ? rb.trow[g + 8] : 0);
+    const int tile0 = tile * kTS;
+
+    // all of this warp's loads first: kChunksPerWarp chunks x 2 rows (x 2 tensors)
+    Raw8<TL> xb_[kChunksPerWarp][2];
+    Raw8<TL> xt_[HAS_T ? kChunksPerWarp : 1][2];
+#pragma unroll
+    for (int k = 0; k < kChunksPerWarp; ++k) {
+        const int v0 = tile0 + kCS * (warp + kWarps * k) + 8 * tq;
+        if (need_z) {
+            if (za) load_raw8<TL>(browA, v0, pa.V, pa.vec_b, xb_[k][0]);
+            if (zb) load_raw8<TL>(browB, v0, pa.V, pa.vec_b, xb_[k][1]);
+        }
+        if constexpr (HAS_T) {
+            if (need_t) {
+                if (ta) load_raw8<TL>(trowA, v0, pa.V, pa.vec_t, xt_[k][0]);
+                if (tb) load_raw8<TL>(trowB, v0, pa.V, pa.vec_t, xt_[k][1]);
+            }
+        }
+    }
     Frag<KS> fa, fb;
-    if (okA) load_frag_global<KS>(W1, rb.prev[g], tq, fa);
-    else frag_zero<KS>(fa);
-    if (okB) load_frag_global<KS>(W1, rb.prev[g + 8], tq, fb);
-    else frag_zero<KS>(fb);
-    const TL* rowA = base + (okA ? rb.brow[g] : 0);
-    const TL* rowB = base + (okB ? rb.brow[g + 8] : 0);
-    const int tile0 = tile * kTS;
-    for (int c = warp; c < kChunks; c += kWarps) {
-        const int cb = tile0 + 32 * c;
-        if (cb >= V) {
-            if (stats && tq == 0) {
-                cstat[g * kChunks + c] = empty_stat(greedy);
-                cstat[(g + 8) * kChunks + c] = empty_stat(greedy);
-            }
-            continue;
-        }
-        float xa[8], xb[8];
-        if (okA) load_vals8<TL>(rowA, cb + 8 * tq, V, vec_ok, xa);
-        else
+    if constexpr (KS > 0) {
+        const uint16_t* W1 = reinterpret_cast<const uint16_t*>(pa.W1);
+        if (za) load_frag_global<KS>(W1, rb.prev[g], tq, fa);
+        else frag_zero<KS>(fa);
+        if (zb) load_frag_global<KS>(W1, rb.prev[g + 8], tq, fb);
+        else frag_zero<KS>(fb);
+    }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) xa[e] = 0.f;
-        if (okB) load_vals8<TL>(rowB, cb + 8 * tq, V, vec_ok, xb);
-        else
-#pragma unroll
-            for (int e = 0; e < 8; ++e) xb[e] = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            float d[4] = {xa[2 * nt], xa[2 * nt + 1], xb[2 * nt], xb[2 * nt + 1]};
-            const int vcol = cb + 8 * (g >> 1) + 2 * nt + (g & 1);  // id this lane feeds as MMA column g
-            Frag<KS> fw;
-            if (vcol < V) {
-                if (w2s) load_frag_smem<KS>(w2s, vcol - tile0, tq, fw);
-                else load_frag_global<KS>(W2, vcol, tq, fw);
-            } else {
-                frag_zero<KS>(fw);
-            }
-#pragma unroll
-            for (int s = 0; s < KS; ++s)
-                mma_bf16(d, fa.w[2 * s], fb.w[2 * s], fa.w[2 * s + 1], fb.w[2 * s + 1], fw.w[2 * s], fw.w[2 * s + 1]);
-            xa[2 * nt] = d[0];
-            xa[2 * nt + 1] = d[1];
-            xb[2 * nt] = d[2];
-            xb[2 * nt + 1] = d[3];
-        }
-        float4* zA = reinterpret_cast<float4*>(zbuf + g * kSRow + 32 * c + 8 * tq);
-        float4* zB = reinterpret_cast<float4*>(zbuf + (g + 8) * kSRow + 32 * c + 8 * tq);
-        zA[0] = make_float4(xa[0], xa[1], xa[2], xa[3]);
-        zA[1] = make_float4(xa[4], xa[5], xa[6], xa[7]);
-        zB[0] = make_float4(xb[0], xb[1], xb[2], xb[3]);
-        zB[1] = make_float4(xb[4], xb[5], xb[6], xb[7]);
-        if (stats) {
-            const float2 sA = quad_stats(xa, cb + 8 * tq, greedy, scale2);
-            const float2 sB = quad_stats(xb, cb + 8 * tq, greedy, scale2);
+    for (int k = 0; k < kChunksPerWarp; ++k) {
+        const int c = warp + kWarps * k;
+        const int cb = tile0 + kCS * c;
+        if (cb >= pa.V) {
             if (tq == 0) {
-                cstat[g * kChunks + c] = sA;
-                cstat[(g + 8) * kChunks + c] = sB;
+                crec[g * kChunks + c] = empty_record(pa.greedy);
+                crec[(g + 8) * kChunks + c] = empty_record(pa.greedy);
             }
-        }
-    }
-}
-
-// CUDA-core path (fp32 weights, ranks not in {16,...,256}, r = 0).  Lane = id; the W1 rows of
-// the row block are staged as fp32 in w1s[16][r] by the caller.
-template <typename TL, typename TW>
-__device__ void produce_z_gemv(const TL* base, const TW* W2, const float* w1s, int r, int V, int tile,
-                               const RowBlock& rb, float* zbuf, float2* cstat, bool stats, int greedy,
-                               float scale2) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tile0 = tile * kTS;
-    for (int c = warp; c < kChunks; c += kWarps) {
-        const int cb = tile0 + 32 * c;
-        if (cb >= V) {
-            if (stats && lane < kRows) cstat[lane * kChunks + c] = empty_stat(greedy);
             continue;
         }
-        const int v = cb + lane;
-        const bool vok = v < V;
-        float acc[kRows];
+        const int id0 = cb + 8 * tq;
+        float xa[8], xb[8];
 #pragma unroll
-        for (int q = 0; q < kRows; ++q) acc[q] = 0.f;
-        for (int k0 = 0; k0 < r; k0 += 8) {
-            float w[8];
+        for (int e = 0; e < 8; ++e) xa[e] = xb[e] = 0.f;
+        if (need_z) {
+            if (za) unpack8<TL>(xb_[k][0], xa);
+            if (zb) unpack8<TL>(xb_[k][1], xb);
+            if constexpr (KS > 0) {
+                const uint16_t* W2 = reinterpret_cast<const uint16_t*>(pa.W2);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) w[e] = (vok && k0 + e < r) ? load_logit<TW>(W2, (size_t)v * r + k0 + e) : 0.f;
+                for (int nt = 0; nt < 4; ++nt) {
+                    float d[4] = {xa[2 * nt], xa[2 * nt + 1], xb[2 * nt], xb[2 * nt + 1]};
+                    const int vcol = cb + 8 * (g >> 1) + 2 * nt + (g & 1);  // id this lane feeds as column g
+                    Frag<KS> fw;
+                    if (vcol < pa.V) {
+                        if (pa.w2s) load_frag_smem<KS>(pa.w2s, vcol - tile0, tq, fw);
+                        else load_frag_global<KS>(W2, vcol, tq, fw);
+                    } else {
+                        frag_zero<KS>(fw);
+                    }
 #pragma unroll
-            for (int q = 0; q < kRows; ++q) {
-                const float* w1 = w1s + q * r + k0;
+                    for (int s = 0; s < KS; ++s)
+                        mma_bf16(d, fa.w[2 * s], fb.w[2 * s], fa.w[2 * s + 1], fb.w[2 * s + 1], fw.w[2 * s],
+                                 fw.w[2 * s + 1]);
+                    xa[2 * nt] = d[0];
+                    xa[2 * nt + 1] = d[1];
+                    xb[2 * nt] = d[2];
+                    xb[2 * nt + 1] = d[3];
+                }
+            } else if (pa.r > 0) {
+                const TW* W2 = reinterpret_cast<const TW*>(pa.W2);
+                const float* w1a = pa.w1s + g * pa.r;
+                const float* w1b = pa.w1s + (g + 8) * pa.r;
+                for (int kk = 0; kk < pa.r; ++kk) {
+                    const float wa = w1a[kk], wb = w1b[kk];
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    if (k0 + e < r) acc[q] = fmaf(w1[e], w[e], acc[q]);
+                    for (int e = 0; e < 8; ++e) {
+                        const float w2 = (id0 + e < pa.V) ? load_logit<TW>(W2, (size_t)(id0 + e) * pa.r + kk) : 0.f;
+                        xa[e] = fmaf(wa, w2, xa[e]);
+                        xb[e] = fmaf(wb, w2, xb[e]);
+                    }
+                }
             }
         }
-#pragma unroll 1
-        for (int q = 0; q < kRows; ++q) {
-            float z = -CUDART_INF_F;
-            if (vok && rb.brow[q] >= 0) z = load_logit<TL>(base, (size_t)rb.brow[q] + v) + acc[q];
-            zbuf[q * kSRow + 32 * c + lane] = z;
-            if (stats) {
-                float2 st;
-                if (greedy) {
-                    float m = z;
-                    int idx = vok ? v : 0x7fffffff;
-                    warp_argmax(m, idx);
-                    st = make_float2(m, __int_as_float(idx));
+        // per-row log2-weights (greedy: the values themselves)
+        float la[8], lb[8];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int mode = h ? mb : ma;
+            float(&x)[8] = h ? xb : xa;
+            float(&l)[8] = h ? lb : la;
+            const int row = h ? g + 8 : g;
+            if (mode == ROW_SAMPLE) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) l[e] = pa.greedy ? x[e] : x[e] * pa.scale2;
+            } else if (HAS_T && (mode == ROW_BONUS || mode == ROW_RESID)) {
+                float t[8];
+                unpack8<TL>(xt_[HAS_T ? k : 0][h], t);
+                if (mode == ROW_BONUS) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        l[e] = pa.greedy ? t[e] : t[e] * pa.scale2;
+                        x[e] = t[e];
+                    }
                 } else {
-                    const float s2 = z * scale2;
-                    const float m = warp_max(s2);
-                    const float e = (m == -CUDART_INF_F) ? 0.f : ex2(s2 - m);
-                    st = make_float2(m, warp_sum(e));
+                    const float lse2 = rb.lse2[row], dl2 = rb.dl2[row];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float w = ex2(fmaf(t[e], pa.scale2, -lse2)) - ex2(fmaf(x[e], pa.scale2, -dl2));
+                        l[e] = w > 0.f ? lg2(w) : -CUDART_INF_F;
+                    }
                 }
-                if (lane == 0) cstat[q * kChunks + c] = st;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) l[e] = -CUDART_INF_F;
             }
+        }
+        const float4 ra = chunk_record(la, xa, id0, rb.u2[g], pa.greedy);
+        const float4 rbk = chunk_record(lb, xb, id0, rb.u2[g + 8], pa.greedy);
+        if (tq == 0) {
+            crec[g * kChunks + c] = ra;
+            crec[(g + 8) * kChunks + c] = rbk;
         }
     }
 }
 
 // --------------------------------------------------------------------------------------------
-// Tile record of one row (one warp, lane = chunk).  The buffered value x_v of id v has weight
-// 2^(x_v * lscale - m) (lscale = log2(e)/T when the buffer holds z, 1 when it holds log2-weights).
-// T > 0 record: {key = ln(mass_t) - ln E_t, ln(mass_t), candidate id, buffered value at it};
-// greedy record: {max, NaN, argmax id, max}.  Only lane 0's return value is meaningful.
+// Tile record from a row's 32 chunk records (one warp, lane = chunk).
+// T > 0: {key = ln(mass_t) - ln E_t, ln(mass_t), candidate id, value at it};
+// greedy: {max, NaN, argmax id, max}.  A tile without mass gets key -inf and candidate -1.
 // --------------------------------------------------------------------------------------------
-__device__ inline float4 finalize_tile(const float* xrow, float2 cs, int tile, int V, int greedy, float lscale,
-                                uint64_t seed, uint32_t j, uint32_t i, uint32_t p_tile, uint32_t p_intile) {
-    const int lane = threadIdx.x & 31;
-    const int tile0 = tile * kTS;
-    const bool valid = tile0 + 32 * lane < V;
+__device__ __forceinline__ float4 finalize_chunks(float4 cr, bool valid, int greedy, float u1, float lnE) {
     if (greedy) {
-        float m = valid ? cs.x : -CUDART_INF_F;
-        int idx = valid ? __float_as_int(cs.y) : 0x7fffffff;
+        float m = valid ? cr.x : -CUDART_INF_F;
+        int idx = valid ? __float_as_int(cr.z) : 0x7fffffff;
         warp_argmax(m, idx);
         return make_float4(m, CUDART_NAN_F, __int_as_float(idx), m);
     }
-    const float mc = valid ? cs.x : -CUDART_INF_F;
-    const float sc = valid ? cs.y : 0.f;
+    const float mc = valid ? cr.x : -CUDART_INF_F;
+    const float sc = valid ? cr.y : 0.f;
     const float mt = warp_max(mc);
+    if (mt == -CUDART_INF_F) return make_float4(-CUDART_INF_F, -CUDART_INF_F, __int_as_float(-1), 0.f);
     const float w = (sc > 0.f) ? sc * ex2(mc - mt) : 0.f;
     const float P = warp_incl_scan(w);
     const float St = __shfl_sync(0xffffffffu, P, 31);
-    if (!(St > 0.f)) {  // no mass in this tile: it can never win
-        return make_float4(-CUDART_INF_F, -CUDART_INF_F, __int_as_float(-1), 0.f);
-    }
+    if (!(St > 0.f)) return make_float4(-CUDART_INF_F, -CUDART_INF_F, __int_as_float(-1), 0.f);
     const float lmass = (mt + lg2(St)) * kLn2;
-    float key = 0.f, up = 0.f;
-    if (lane == 0) {
-        key = lmass - log_neg_log_u(uniform(seed, j, i, p_tile, (uint32_t)tile));
-        up = uniform(seed, j, i, p_intile, 0u);
-    }
-    up = __shfl_sync(0xffffffffu, up, 0);
-    const float target = up * St;
+    const float target = u1 * St;
     const unsigned hit = __ballot_sync(0xffffffffu, P > target);
     int cstar;
     if (hit) {
@@ -348,25 +471,12 @@ __device__ inline float4 finalize_tile(const float* xrow, float2 cs, int tile, i
         const unsigned nz = __ballot_sync(0xffffffffu, w > 0.f);
         cstar = nz ? 31 - __clz(nz) : 0;
     }
-    const float before = __shfl_sync(0xffffffffu, P - w, cstar);
-    const int vl = 32 * cstar + lane;
-    const float xv = xrow[vl];
-    const float e = (tile0 + vl < V) ? ex2(xv * lscale - mt) : 0.f;
-    const float Q = warp_incl_scan(e) + before;
-    const unsigned hit2 = __ballot_sync(0xffffffffu, Q > target);
-    int xl;
-    if (hit2) {
-        xl = __ffs(hit2) - 1;
-    } else {
-        const unsigned nz = __ballot_sync(0xffffffffu, e > 0.f);
-        xl = nz ? 31 - __clz(nz) : 0;
-    }
-    const float xc = __shfl_sync(0xffffffffu, xv, xl);
-    return make_float4(key, lmass, __int_as_float(tile0 + 32 * cstar + xl), xc);
+    const int cand = __shfl_sync(0xffffffffu, __float_as_int(cr.z), cstar);
+    const float val = __shfl_sync(0xffffffffu, cr.w, cstar);
+    return make_float4(lmass - lnE, lmass, __int_as_float(cand), val);
 }
 
 // Reduction of a request's tile records (one warp): the highest key wins, lowest tile on ties.
-// Returns (candidate, value at it) in lane 0 and, optionally, the log-sum of the tiles' masses.
 struct TileWinner {
     int cand;
     float val;

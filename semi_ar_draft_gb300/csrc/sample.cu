@@ -42,12 +42,12 @@ struct SampleArgs {
     float4* part;  // [B][nt] tile records
     uint64_t limit_ns;
     int w2_smem;
-    int vec_ok;  // base rows start on 16-byte boundaries: 8-wide loads allowed
+    int vec_ok;  // base rows start on 16-byte boundaries: 8-wide loads and L2 prefetch allowed
 };
 
 size_t sample_smem_bytes(int B, int r, bool mma, bool w2_smem) {
-    size_t b = sizeof(float) * kRows * kSRow + sizeof(float2) * kRows * kChunks + sizeof(RowBlock) +
-               align_up(sizeof(int) * (size_t)B, 16);
+    size_t b = sizeof(float4) * kRows * kChunks + align_up(sizeof(RowBlock), 16) + align_up(sizeof(int) * (size_t)B, 16) +
+               sizeof(float4) * (size_t)B;
     if (mma) {
         if (w2_smem) b += (size_t)kTS * r * 2;
     } else {
@@ -56,26 +56,62 @@ size_t sample_smem_bytes(int B, int r, bool mma, bool w2_smem) {
     return b;
 }
 
+// The step's random draws of every request that do not depend on the drafted tokens:
+// (u1, u2) of SAMPLE_INTILE (one Philox call, words 0 and 1) and ln E of this block's first tile.
+__device__ void step_randoms(const SampleArgs& a, int step, float4* rnd) {
+    const uint32_t i = (uint32_t)step + 1u;
+    for (int j = threadIdx.x; j < a.B; j += kThreads) {
+        const uint4 w = philox10(make_uint4(0u, i, (uint32_t)j, DSPARK_P_SAMPLE_INTILE), (uint32_t)a.seed,
+                                 (uint32_t)(a.seed >> 32));
+        const float lnE = log_neg_log_u(uniform(a.seed, (uint32_t)j, i, DSPARK_P_SAMPLE_TILE, blockIdx.x));
+        rnd[j] = make_float4(u01(w.x), u01(w.y), lnE, 0.f);
+    }
+}
+
+// L2 prefetch of the base rows of row block [row0, row0 + 16) at `step` over this block's tile.
+template <typename TL>
+__device__ void prefetch_rows(const SampleArgs& a, int tile, int row0, int step) {
+    const int q = threadIdx.x;
+    if (!a.vec_ok || q >= kRows || row0 + q >= a.B || step >= a.gamma || tile >= a.nt) return;
+    const int tile0 = tile * kTS;
+    const int n = min(kTS, a.V - tile0);
+    const TL* p = reinterpret_cast<const TL*>(a.base) + ((size_t)(row0 + q) * a.gamma + step) * (size_t)a.V + tile0;
+    prefetch_l2(p, (uint32_t)(n * sizeof(TL)));
+}
+
 template <typename TL, int KS, typename TW>
 __global__ void __launch_bounds__(kThreads, 1) sample_kernel(SampleArgs a) {
     constexpr bool kMMA = KS > 0;
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    float* zbuf = reinterpret_cast<float*>(smem_raw);
-    float2* cstat = reinterpret_cast<float2*>(zbuf + kRows * kSRow);
-    RowBlock* rb = reinterpret_cast<RowBlock*>(cstat + kRows * kChunks);
-    int* prev = reinterpret_cast<int*>(rb + 1);
-    unsigned char* wreg = reinterpret_cast<unsigned char*>(prev) + align_up(sizeof(int) * (size_t)a.B, 16);
+    float4* crec = reinterpret_cast<float4*>(smem_raw);
+    RowBlock* rb = reinterpret_cast<RowBlock*>(crec + kRows * kChunks);
+    int* prev = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(rb) + align_up(sizeof(RowBlock), 16));
+    float4* rnd = reinterpret_cast<float4*>(reinterpret_cast<unsigned char*>(prev) + align_up(sizeof(int) * (size_t)a.B, 16));
+    unsigned char* wreg = reinterpret_cast<unsigned char*>(rnd + a.B);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const TL* base = reinterpret_cast<const TL*>(a.base);
 
-    const uint4* w2s = nullptr;
+    ProdArgs pa;
+    pa.base = a.base;
+    pa.target = nullptr;
+    pa.W1 = a.W1;
+    pa.W2 = a.W2;
+    pa.w2s = nullptr;
+    pa.w1s = reinterpret_cast<const float*>(wreg);
+    pa.V = a.V;
+    pa.r = a.r;
+    pa.greedy = a.greedy;
+    pa.scale2 = a.scale2;
+    pa.vec_b = a.vec_ok;
+    pa.vec_t = 0;
     if constexpr (kMMA) {
         if (a.w2_smem) {
             stage_w2_tile<KS>(reinterpret_cast<const uint16_t*>(a.W2), blockIdx.x * kTS, a.V,
                               reinterpret_cast<uint4*>(wreg));
-            w2s = reinterpret_cast<const uint4*>(wreg);
+            pa.w2s = reinterpret_cast<const uint4*>(wreg);
         }
     }
+    prefetch_rows<TL>(a, blockIdx.x, 0, 0);
+    if (!a.greedy) step_randoms(a, 0, rnd);
 
     uint32_t target = 0;
     for (int step = 0; step < a.gamma; ++step) {
@@ -101,32 +137,38 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(SampleArgs a) {
             for (int row0 = 0; row0 < a.B; row0 += kRows) {
                 if (tid < kRows) {
                     const int j = row0 + tid;
-                    rb->prev[tid] = (j < a.B) ? prev[j] : 0;
-                    rb->brow[tid] = (j < a.B) ? ((long long)j * a.gamma + step) * (long long)a.V : -1;
+                    const bool ok = j < a.B;
+                    rb->prev[tid] = ok ? prev[j] : 0;
+                    rb->mode[tid] = ok ? ROW_SAMPLE : ROW_OFF;
+                    rb->brow[tid] = ok ? ((long long)j * a.gamma + step) * (long long)a.V : -1;
+                    rb->trow[tid] = -1;
+                    float4 q = ok && !a.greedy ? rnd[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (ok && !a.greedy && tile != blockIdx.x)  // blocks owning several tiles: per-tile variate
+                        q.z = log_neg_log_u(uniform(a.seed, (uint32_t)j, (uint32_t)step + 1u, DSPARK_P_SAMPLE_TILE,
+                                                    (uint32_t)tile));
+                    rb->u1[tid] = q.x;
+                    rb->u2[tid] = q.y;
+                    rb->lnE[tid] = q.z;
                 }
-                __syncthreads();
-                if constexpr (kMMA) {
-                    produce_z_mma<TL, KS>(base, reinterpret_cast<const uint16_t*>(a.W1),
-                                          reinterpret_cast<const uint16_t*>(a.W2), w2s, a.V, a.vec_ok != 0, tile,
-                                          *rb, zbuf, cstat, true, a.greedy, a.scale2);
-                } else {
+                // next row block of this step (or the first of the next step is prefetched at the wait)
+                if (row0 + kRows < a.B) prefetch_rows<TL>(a, tile, row0 + kRows, step);
+                if constexpr (!kMMA) {
+                    __syncthreads();
                     float* w1s = reinterpret_cast<float*>(wreg);
                     const TW* W1 = reinterpret_cast<const TW*>(a.W1);
                     for (int idx = tid; idx < kRows * a.r; idx += kThreads) {
                         const int q = idx / a.r, k = idx % a.r;
                         w1s[idx] = (rb->brow[q] >= 0) ? load_logit<TW>(W1, (size_t)rb->prev[q] * a.r + k) : 0.f;
                     }
-                    __syncthreads();
-                    produce_z_gemv<TL, TW>(base, reinterpret_cast<const TW*>(a.W2), w1s, a.r, a.V, tile, *rb, zbuf,
-                                           cstat, true, a.greedy, a.scale2);
                 }
+                __syncthreads();
+                produce_chunks<TL, KS, TW, false>(pa, tile, *rb, crec);
                 __syncthreads();
                 for (int rl = warp; rl < kRows; rl += kWarps) {
                     const int j = row0 + rl;
                     if (j >= a.B) continue;
-                    const float4 rec = finalize_tile(zbuf + rl * kSRow, cstat[rl * kChunks + lane], tile, a.V,
-                                                     a.greedy, a.scale2, a.seed, (uint32_t)j, (uint32_t)step + 1u,
-                                                     DSPARK_P_SAMPLE_TILE, DSPARK_P_SAMPLE_INTILE);
+                    const bool valid = tile * kTS + kCS * lane < a.V;
+                    const float4 rec = finalize_chunks(crec[rl * kChunks + lane], valid, a.greedy, rb->u1[rl], rb->lnE[rl]);
                     if (lane == 0) a.part[(size_t)j * a.nt + tile] = rec;
                 }
                 __syncthreads();
@@ -145,8 +187,13 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(SampleArgs a) {
             }
         }
         if (step + 1 < a.gamma) {
+            // everything of the next step that does not depend on its tokens happens while the
+            // last blocks arrive
             target += (uint32_t)a.G;
-            if (!grid_wait(a.hdr, target, a.limit_ns)) return;
+            grid_arrive(a.hdr);
+            prefetch_rows<TL>(a, blockIdx.x, 0, step + 1);
+            if (!a.greedy) step_randoms(a, step + 1, rnd);
+            if (!grid_wait_arrived(a.hdr, target, a.limit_ns)) return;
         }
     }
 }

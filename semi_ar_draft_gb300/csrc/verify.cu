@@ -119,34 +119,57 @@ __global__ void __launch_bounds__(kThreads) verify_rows_kernel(VerifyArgs a) {
     const TL* row = reinterpret_cast<const TL*>(a.target) + trow_off(a, j, i);
     const int v_lo = seg * a.segsz, v_hi = min(a.V, v_lo + a.segsz);
     float2 res;
+    constexpr int U = 4;  // 8-id groups per thread in flight
     if (a.greedy) {
         float m = -CUDART_INF_F;
         int idx = 0x7fffffff;
-        for (int v0 = v_lo + 8 * tid; v0 < v_hi; v0 += 8 * kThreads) {
-            float x[8];
-            load_vals8<TL>(row, v0, a.V, a.vec_t != 0, x);
+        for (int v0 = v_lo + 8 * tid; v0 < v_hi; v0 += 8 * kThreads * U) {
+            Raw8<TL> raw[U];
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                if (x[e] > m) {
-                    m = x[e];
-                    idx = v0 + e;
-                }
+            for (int u = 0; u < U; ++u) {
+                const int vv = v0 + 8 * kThreads * u;
+                if (vv < v_hi) load_raw8<TL>(row, vv, a.V, a.vec_t != 0, raw[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int vv = v0 + 8 * kThreads * u;
+                if (vv >= v_hi) break;
+                float x[8];
+                unpack8<TL>(raw[u], x);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    if (x[e] > m) {
+                        m = x[e];
+                        idx = vv + e;
+                    }
+            }
         }
         res = block_argmax_pair(m, idx, red);
     } else {
         float m = -CUDART_INF_F, s = 0.f;
-        for (int v0 = v_lo + 8 * tid; v0 < v_hi; v0 += 8 * kThreads) {
-            float x[8];
-            load_vals8<TL>(row, v0, a.V, a.vec_t != 0, x);
-            float gm = x[0];
+        for (int v0 = v_lo + 8 * tid; v0 < v_hi; v0 += 8 * kThreads * U) {
+            Raw8<TL> raw[U];
 #pragma unroll
-            for (int e = 1; e < 8; ++e) gm = fmaxf(gm, x[e]);
-            const float mn = fmaxf(m, gm * a.scale2);
-            if (mn != -CUDART_INF_F) {
-                s = (m == -CUDART_INF_F) ? 0.f : s * ex2(m - mn);
+            for (int u = 0; u < U; ++u) {
+                const int vv = v0 + 8 * kThreads * u;
+                if (vv < v_hi) load_raw8<TL>(row, vv, a.V, a.vec_t != 0, raw[u]);
+            }
 #pragma unroll
-                for (int e = 0; e < 8; ++e) s += ex2(fmaf(x[e], a.scale2, -mn));
-                m = mn;
+            for (int u = 0; u < U; ++u) {
+                const int vv = v0 + 8 * kThreads * u;
+                if (vv >= v_hi) break;
+                float x[8];
+                unpack8<TL>(raw[u], x);
+                float gm = x[0];
+#pragma unroll
+                for (int e = 1; e < 8; ++e) gm = fmaxf(gm, x[e]);
+                const float mn = fmaxf(m, gm * a.scale2);
+                if (mn != -CUDART_INF_F) {
+                    s = (m == -CUDART_INF_F) ? 0.f : s * ex2(m - mn);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) s += ex2(fmaf(x[e], a.scale2, -mn));
+                    m = mn;
+                }
             }
         }
         res = block_lse_pair(m, s, red);
@@ -226,16 +249,18 @@ __global__ void __launch_bounds__(kThreads) verify_rows_kernel(VerifyArgs a) {
 }
 
 // ------------------------------------------------------------------------------- launch 2
-// Whole-block tile-Gumbel draw from softmax(target row / T) with the RESID purposes: the
-// fallback when a residual max(0, p - q) has no mass at all.
+// Whole-block draw from softmax(target row / T) with the RESID purposes and the sampling
+// contract (tile by Gumbel race, chunk by u1, id by u2): the fallback when a residual
+// max(0, p - q) has no mass at all.  sh: 64 floats of shared scratch.
 template <typename TL>
 __device__ int block_sample_row(const VerifyArgs& a, const TL* row, int j, int pos, float* sh) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    float2* red = reinterpret_cast<float2*>(sh);
-    float* wsum = sh + 2 * kWarps;
-    float best_key = -CUDART_INF_F, best_mass = 0.f, best_m = 0.f;
+    float2* red = reinterpret_cast<float2*>(sh);  // sh[0..15]
+    float* cmass = sh + 16;                       // sh[16..47]
+    float* misc = sh + 48;                        // sh[48..63]
+    constexpr int per = kTS / kThreads;           // 4 ids per thread, in id order
+    float best_key = -CUDART_INF_F, best_m = 0.f;
     int best_t = 0;
-    constexpr int per = kTS / kThreads;
     for (int t = 0; t < a.nt; ++t) {
         float x[per];
         float m = -CUDART_INF_F;
@@ -245,66 +270,61 @@ __device__ int block_sample_row(const VerifyArgs& a, const TL* row, int j, int p
             x[e] = v < a.V ? load_logit<TL>(row, (size_t)v) * a.scale2 : -CUDART_INF_F;
             m = fmaxf(m, x[e]);
         }
-        float s = 0.f;
+        float sum = 0.f;
         if (m != -CUDART_INF_F)
 #pragma unroll
-            for (int e = 0; e < per; ++e) s += ex2(x[e] - m);
-        const float2 ms = block_lse_pair(m, s, red);
+            for (int e = 0; e < per; ++e) sum += ex2(x[e] - m);
+        const float2 ms = block_lse_pair(m, sum, red);
         if (tid == 0 && ms.y > 0.f) {
             const float key = (ms.x + lg2(ms.y)) * kLn2 -
                               log_neg_log_u(uniform(a.seed, (uint32_t)j, (uint32_t)pos, DSPARK_P_RESID_TILE, (uint32_t)t));
             if (key > best_key) {
                 best_key = key;
                 best_t = t;
-                best_mass = ms.y;
                 best_m = ms.x;
             }
         }
     }
     if (tid == 0) {
-        wsum[0] = __int_as_float(best_t);
-        wsum[1] = best_mass;
-        wsum[2] = best_m;
+        misc[0] = __int_as_float(best_t);
+        misc[1] = best_m;
     }
     __syncthreads();
-    const int t = __float_as_int(wsum[0]);
-    const float St = wsum[1], mt = wsum[2];
-    __syncthreads();
-    float e[per], tot = 0.f;
+    const int t = __float_as_int(misc[0]);
+    const float mt = misc[1];
+    // chunk masses of tile t (8 threads per 32-id chunk)
+    float tot = 0.f;
 #pragma unroll
-    for (int q = 0; q < per; ++q) {
-        const int v = t * kTS + per * tid + q;
-        e[q] = v < a.V ? ex2(load_logit<TL>(row, (size_t)v) * a.scale2 - mt) : 0.f;
-        tot += e[q];
+    for (int e = 0; e < per; ++e) {
+        const int v = t * kTS + per * tid + e;
+        tot += v < a.V ? ex2(load_logit<TL>(row, (size_t)v) * a.scale2 - mt) : 0.f;
     }
-    // exclusive scan of per-thread totals in id order
-    const float incl = warp_incl_scan(tot);
-    if (lane == 31) wsum[4 + warp] = incl;
+    tot += __shfl_xor_sync(0xffffffffu, tot, 1);
+    tot += __shfl_xor_sync(0xffffffffu, tot, 2);
+    tot += __shfl_xor_sync(0xffffffffu, tot, 4);
+    if ((tid & 7) == 0) cmass[tid >> 3] = tot;
     __syncthreads();
-    float woff = 0.f;
-    for (int w = 0; w < warp; ++w) woff += wsum[4 + w];
-    const float up = uniform(a.seed, (uint32_t)j, (uint32_t)pos, DSPARK_P_RESID_INTILE, 0u);
-    const float target = up * St;
-    float c = woff + incl - tot;
-    int found = 0x7fffffff, lastnz = -1;
-#pragma unroll
-    for (int q = 0; q < per; ++q) {
-        c += e[q];
-        if (c > target && found == 0x7fffffff) found = t * kTS + per * tid + q;
-        if (e[q] > 0.f) lastnz = t * kTS + per * tid + q;
+    const uint4 w = philox10(make_uint4(0u, (uint32_t)pos, (uint32_t)j, DSPARK_P_RESID_INTILE), (uint32_t)a.seed,
+                             (uint32_t)(a.seed >> 32));
+    if (warp == 0) {  // chunk by u1
+        const float cw = cmass[lane];
+        const float P = warp_incl_scan(cw);
+        const float S = __shfl_sync(0xffffffffu, P, 31);
+        const unsigned hit = __ballot_sync(0xffffffffu, P > u01(w.x) * S);
+        const unsigned nz = __ballot_sync(0xffffffffu, cw > 0.f);
+        const int c = hit ? __ffs(hit) - 1 : (nz ? 31 - __clz(nz) : 0);
+        // id by u2 inside chunk c, masses relative to the same tile maximum
+        const int v = t * kTS + kCS * c + lane;
+        const float e = v < a.V ? ex2(load_logit<TL>(row, (size_t)v) * a.scale2 - mt) : 0.f;
+        const float Q = warp_incl_scan(e);
+        const float Sc = __shfl_sync(0xffffffffu, Q, 31);
+        const unsigned hit2 = __ballot_sync(0xffffffffu, Q > u01(w.y) * Sc);
+        const unsigned nz2 = __ballot_sync(0xffffffffu, e > 0.f);
+        const int k = hit2 ? __ffs(hit2) - 1 : (nz2 ? 31 - __clz(nz2) : 0);
+        if (lane == 0) misc[2] = __int_as_float(t * kTS + kCS * c + k);
     }
     __syncthreads();
-    // lowest id crossing the target; else the highest id with mass
-    int* ires = reinterpret_cast<int*>(wsum + 4 + kWarps);
-    if (tid == 0) {
-        ires[0] = 0x7fffffff;
-        ires[1] = -1;
-    }
-    __syncthreads();
-    if (found != 0x7fffffff) atomicMin(&ires[0], found);
-    if (lastnz >= 0) atomicMax(&ires[1], lastnz);
-    __syncthreads();
-    const int x = ires[0] != 0x7fffffff ? ires[0] : ires[1];
+    const int x = __float_as_int(misc[2]);
     __syncthreads();
     return x;
 }
@@ -312,13 +332,12 @@ __device__ int block_sample_row(const VerifyArgs& a, const TL* row, int j, int p
 template <typename TL, int KS, typename TW>
 __global__ void __launch_bounds__(kThreads, 1) verify_jobs_kernel(VerifyArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    float* zbuf = reinterpret_cast<float*>(smem_raw);
-    float2* cstat = reinterpret_cast<float2*>(zbuf + kRows * kSRow);
-    RowBlock* rb = reinterpret_cast<RowBlock*>(cstat + kRows * kChunks);
-    int4* jb = reinterpret_cast<int4*>(rb + 1);             // [kRows]
+    float4* crec = reinterpret_cast<float4*>(smem_raw);  // [kRows][kChunks]
+    RowBlock* rb = reinterpret_cast<RowBlock*>(crec + kRows * kChunks);
+    int4* jb = reinterpret_cast<int4*>(reinterpret_cast<unsigned char*>(rb) + align_up(sizeof(RowBlock), 16));
     float* scratch = reinterpret_cast<float*>(jb + kRows);  // fallback scratch [64]
-    float* w1s = scratch + 64;                              // GEMV: [kRows][r]
-    __shared__ int s_any, s_last;
+    float* w1s = scratch + 64;                              // CUDA-core path: [kRows][r]
+    __shared__ int s_any, s_last, s_fallback[kRows];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tile = blockIdx.x, row0 = blockIdx.y * kRows;
     if (tid == 0) s_any = 0;
@@ -328,70 +347,59 @@ __global__ void __launch_bounds__(kThreads, 1) verify_jobs_kernel(VerifyArgs a) 
         int4 q = make_int4(JOB_NONE, 0, 0, 0);
         if (j < a.B) q = a.job[j];
         jb[tid] = q;
-        rb->prev[tid] = q.x == JOB_RESID ? q.z : 0;
-        rb->brow[tid] = q.x == JOB_RESID ? ((long long)j * a.gamma + q.y - 1) * (long long)a.V : -1;
-        if (q.x != JOB_NONE) atomicOr(&s_any, 1);
+        const bool resid = q.x == JOB_RESID, bonus = q.x == JOB_BONUS;
+        rb->mode[tid] = resid ? ROW_RESID : (bonus ? ROW_BONUS : ROW_OFF);
+        rb->prev[tid] = resid ? q.z : 0;
+        rb->brow[tid] = resid ? ((long long)j * a.gamma + q.y - 1) * (long long)a.V : -1;
+        rb->trow[tid] = (resid || bonus) ? trow_off(a, j, q.y) : -1;
+        float u1 = 0.f, u2 = 0.f, lnE = 0.f, dl2 = 0.f;
+        if (resid || bonus) {
+            const uint32_t pt = resid ? DSPARK_P_RESID_TILE : DSPARK_P_BONUS_TILE;
+            const uint32_t pi = resid ? DSPARK_P_RESID_INTILE : DSPARK_P_BONUS_INTILE;
+            const uint4 w = philox10(make_uint4(0u, (uint32_t)q.y, (uint32_t)j, pi), (uint32_t)a.seed,
+                                     (uint32_t)(a.seed >> 32));
+            u1 = u01(w.x);
+            u2 = u01(w.y);
+            lnE = log_neg_log_u(uniform(a.seed, (uint32_t)j, (uint32_t)q.y, pt, (uint32_t)tile));
+            if (resid) dl2 = a.dlse[(size_t)j * a.gamma + q.y - 1] * kLog2e;
+            atomicOr(&s_any, 1);
+        }
+        rb->u1[tid] = u1;
+        rb->u2[tid] = u2;
+        rb->lnE[tid] = lnE;
+        rb->lse2[tid] = __int_as_float(q.w);
+        rb->dl2[tid] = dl2;
     }
     __syncthreads();
-    if (!s_any) return;
-    const TL* base = reinterpret_cast<const TL*>(a.base);
-    const TL* tgt = reinterpret_cast<const TL*>(a.target);
-    if constexpr (KS > 0) {
-        produce_z_mma<TL, KS>(base, reinterpret_cast<const uint16_t*>(a.W1), reinterpret_cast<const uint16_t*>(a.W2),
-                              nullptr, a.V, a.vec_b != 0, tile, *rb, zbuf, cstat, false, 0, a.scale2);
-    } else {
+    if (!s_any) return;  // uniform over the row block's tiles: no arrival is expected from them either
+    ProdArgs pa;
+    pa.base = a.base;
+    pa.target = a.target;
+    pa.W1 = a.W1;
+    pa.W2 = a.W2;
+    pa.w2s = nullptr;
+    pa.w1s = w1s;
+    pa.V = a.V;
+    pa.r = a.r;
+    pa.greedy = a.greedy;
+    pa.scale2 = a.scale2;
+    pa.vec_b = a.vec_b;
+    pa.vec_t = a.vec_t;
+    if constexpr (KS == 0) {
         const TW* W1 = reinterpret_cast<const TW*>(a.W1);
         for (int idx = tid; idx < kRows * a.r; idx += kThreads) {
             const int q = idx / a.r, k = idx % a.r;
             w1s[idx] = (rb->brow[q] >= 0) ? load_logit<TW>(W1, (size_t)rb->prev[q] * a.r + k) : 0.f;
         }
         __syncthreads();
-        produce_z_gemv<TL, TW>(base, reinterpret_cast<const TW*>(a.W2), w1s, a.r, a.V, tile, *rb, zbuf, cstat, false,
-                               0, a.scale2);
     }
+    produce_chunks<TL, KS, TW, true>(pa, tile, *rb, crec);
     __syncthreads();
-    const int tile0 = tile * kTS;
     for (int q = warp; q < kRows; q += kWarps) {
-        const int4 job = jb[q];
-        if (job.x == JOB_NONE) continue;
+        if (rb->mode[q] == ROW_OFF) continue;
         const int j = row0 + q;
-        const bool gre = a.greedy != 0;  // only BONUS jobs exist when T == 0
-        const TL* trow = tgt + trow_off(a, j, job.y);
-        const float lse2 = __int_as_float(job.w);
-        const float dl2 = job.x == JOB_RESID ? a.dlse[(size_t)j * a.gamma + job.y - 1] * kLog2e : 0.f;
-        float* xrow = zbuf + q * kSRow;
-        for (int c = 0; c < kChunks; ++c) {
-            const int v = tile0 + 32 * c + lane;
-            float l = -CUDART_INF_F;
-            if (v < a.V) {
-                const float t = load_logit<TL>(trow, (size_t)v);
-                if (gre) {
-                    l = t;
-                } else if (job.x == JOB_BONUS) {
-                    l = t * a.scale2;
-                } else {
-                    const float w = ex2(fmaf(t, a.scale2, -lse2)) - ex2(fmaf(xrow[32 * c + lane], a.scale2, -dl2));
-                    l = w > 0.f ? lg2(w) : -CUDART_INF_F;
-                }
-            }
-            xrow[32 * c + lane] = l;
-            float2 st;
-            if (gre) {
-                float m = l;
-                int idx = v < a.V ? v : 0x7fffffff;
-                warp_argmax(m, idx);
-                st = make_float2(m, __int_as_float(idx));
-            } else {
-                const float m = warp_max(l);
-                st = make_float2(m, warp_sum(m == -CUDART_INF_F ? 0.f : ex2(l - m)));
-            }
-            if (lane == 0) cstat[q * kChunks + c] = st;
-        }
-        __syncwarp();
-        const uint32_t pt = job.x == JOB_RESID ? DSPARK_P_RESID_TILE : DSPARK_P_BONUS_TILE;
-        const uint32_t pi = job.x == JOB_RESID ? DSPARK_P_RESID_INTILE : DSPARK_P_BONUS_INTILE;
-        const float4 rec = finalize_tile(xrow, cstat[q * kChunks + lane], tile, a.V, gre ? 1 : 0, 1.f, a.seed,
-                                         (uint32_t)j, (uint32_t)job.y, pt, pi);
+        const bool valid = tile * kTS + kCS * lane < a.V;
+        const float4 rec = finalize_chunks(crec[q * kChunks + lane], valid, a.greedy, rb->u1[q], rb->lnE[q]);
         if (lane == 0) a.jobpart[(size_t)j * a.nt + tile] = rec;
     }
     __syncthreads();
@@ -403,7 +411,6 @@ __global__ void __launch_bounds__(kThreads, 1) verify_jobs_kernel(VerifyArgs a) 
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    __shared__ int s_fallback[kRows];
     for (int q = warp; q < kRows; q += kWarps) {
         const int4 job = jb[q];
         if (job.x == JOB_NONE) continue;
@@ -419,7 +426,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_jobs_kernel(VerifyArgs a) 
         const int4 job = jb[q];
         if (job.x != JOB_RESID || !s_fallback[q]) continue;
         const int j = row0 + q;
-        const int x = block_sample_row<TL>(a, tgt + trow_off(a, j, job.y), j, job.y, scratch);
+        const int x = block_sample_row<TL>(a, reinterpret_cast<const TL*>(a.target) + trow_off(a, j, job.y), j,
+                                           job.y, scratch);
         if (tid == 0) a.corr[j] = x;
     }
 }
@@ -543,8 +551,8 @@ extern "C" dspark_status dspark_verify(const dspark_sample_params* p, const void
     if (cudaLaunchKernel((const void*)rows, dim3(L.nseg, p->gamma, p->B), dim3(kThreads), args, 0, s) != cudaSuccess)
         return DSPARK_ERR_CUDA;
     RowsFn jobs = pick_jobs(p, mma);
-    size_t smem = sizeof(float) * kRows * kSRow + sizeof(float2) * kRows * kChunks + sizeof(RowBlock) +
-                  sizeof(int4) * kRows + sizeof(float) * 64 + (mma ? 0 : sizeof(float) * kRows * (size_t)p->r);
+    size_t smem = sizeof(float4) * kRows * kChunks + align_up(sizeof(RowBlock), 16) + sizeof(int4) * kRows +
+                  sizeof(float) * 64 + (mma ? 0 : sizeof(float) * kRows * (size_t)p->r);
     if (smem > kMaxSmem) return DSPARK_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute((const void*)jobs, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return DSPARK_ERR_CUDA;
