@@ -158,6 +158,53 @@ __device__ __forceinline__ void warp_argmax(float& v, int& idx) {
     }
 }
 
+// ---------------------------------------------------------------- mbarrier + bulk copy
+// Shared-memory mbarriers and the 1-D bulk copy engine (cp.async.bulk): a copy of `bytes`
+// (multiple of 16, both addresses 16-byte aligned) from global to this block's shared memory
+// signals completion on an mbarrier through its transaction count.
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// Bounded wait for the phase with the given parity; false (and DSPARK_ERR_TIMEOUT recorded)
+// if it did not complete within limit_ns.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int32_t* status, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_ns() - t0 > limit_ns) {
+            record_status(status, DSPARK_ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
 // ---------------------------------------------------------------- grid-wide wait
 // All blocks of a co-resident (cooperative) grid meet here.  `target` is the total number of
 // arrivals expected so far (a monotonically growing counter, zeroed before the launch).
@@ -166,10 +213,8 @@ __device__ __forceinline__ void warp_argmax(float& v, int& idx) {
 // Split phase: grid_arrive() then independent work then grid_wait_arrived().
 __device__ __forceinline__ void grid_arrive(WsHeader* h) {
     __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        atomicAdd(&h->arrivals, 1u);
-    }
+    if (threadIdx.x == 0)  // release: this block's writes are visible to whoever sees the arrival
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&h->arrivals) : "memory");
 }
 
 __device__ __forceinline__ bool grid_wait_arrived(WsHeader* h, uint32_t target, uint64_t limit_ns) {

@@ -4,19 +4,19 @@
 // of a tile, a "row block" 16 rows (requests).  The producer computes, for a row block over
 // one tile, z = base + W2 . W1[prev] in registers (tensor-core mma.sync bf16 with the
 // accumulator initialised from the base logits, or a CUDA-core GEMV), turns it into the row's
-// log2-weights (draft sampling, residual or bonus draw) and reduces every chunk to a record
-//   {max log2-weight m_c, sum 2^(l - m_c), in-chunk inverse-CDF candidate, value at it}
-// (greedy: {max value, -, lowest argmax, max value}).  finalize_chunks() turns a row's 32 chunk
-// records into the tile record of the sampling contract (dspark.h): the Gumbel key, the
-// tile's log-mass, and the chunk-level inverse-CDF choice -- all before the winning tile is
-// known, so no per-id data has to stay on chip.
+// log2-weights (draft sampling, residual or bonus draw) and reduces every chunk to
+//   {max log2-weight m_c, sum 2^(l - m_c)}
+// (greedy: {max value, lowest argmax}); the values go to a shared-memory row buffer.
+// finalize_tile() turns a row's 32 chunk statistics into the tile record of the sampling
+// contract (dspark.h): the Gumbel key, the tile's log-mass, the chunk chosen by u1 and the id
+// chosen by u2 inside it -- before the winning tile is known (the draw is speculative per tile).
 #pragma once
 
 #include "common.cuh"
 
 namespace dspark {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kTS = DSPARK_TILE;
 constexpr int kCS = DSPARK_CHUNK;
@@ -25,6 +25,7 @@ constexpr int kRows = 16;
 constexpr int kChunksPerWarp = kChunks / kWarps;
 static_assert(kChunks == 32, "one warp lane per chunk in finalize_chunks");
 static_assert(kCS == 32, "a lane quad holds one chunk: 4 lanes x 8 ids");
+constexpr int kXRow = kTS + 4;  // padded row stride (floats) of the value buffer: conflict-free 16-byte stores
 
 enum RowMode { ROW_OFF = 0, ROW_SAMPLE = 1, ROW_RESID = 2, ROW_BONUS = 3 };
 
@@ -194,11 +195,11 @@ __device__ __forceinline__ void unpack8(const Raw8<TL>& r, float (&x)[8]) {
 }
 
 // --------------------------------------------------------------------------------------------
-// Chunk record from one lane quad (lane tq holds ids id0 .. id0+7 = chunk base + 8 tq).
+// Chunk statistics from one lane quad (lane tq holds ids id0 .. id0+7 = chunk base + 8 tq):
+// T > 0: (max m_c of the log2-weights, sum 2^(l - m_c)); greedy: (max value, lowest argmax).
+// Every lane runs every shuffle (full-warp masks); nothing returns early.
 // --------------------------------------------------------------------------------------------
-__device__ __forceinline__ float4 chunk_record(const float (&l)[8], const float (&val)[8], int id0, float u2,
-                                               int greedy) {
-    const int tq = threadIdx.x & 3;
+__device__ __forceinline__ float2 chunk_stats(const float (&l)[8], int id0, int greedy) {
     if (greedy) {
         float m = l[0];
         int idx = id0;
@@ -217,75 +218,29 @@ __device__ __forceinline__ float4 chunk_record(const float (&l)[8], const float 
                 idx = oi;
             }
         }
-        return make_float4(m, 0.f, __int_as_float(idx), m);
+        return make_float2(m, __int_as_float(idx));
     }
-    // Every lane runs every shuffle below (full-warp masks): a quad without mass is only
-    // masked out at the end, never by an early return.
     float m = l[0];
 #pragma unroll
     for (int e = 1; e < 8; ++e) m = fmaxf(m, l[e]);
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-    const bool empty = m == -CUDART_INF_F;  // quad-uniform
-    const float mref = empty ? 0.f : m;
-    float cum[8];
-    float run = 0.f;
+    const float mref = (m == -CUDART_INF_F) ? 0.f : m;  // an empty quad sums to 0
+    float sum = 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        run += ex2(l[e] - mref);  // 0 for -inf entries
-        cum[e] = run;
-    }
-    // inclusive scan of the lane totals over the quad (ids are in lane order)
-    float incl = run;
-    float t = __shfl_up_sync(0xffffffffu, incl, 1, 4);
-    if (tq >= 1) incl += t;
-    t = __shfl_up_sync(0xffffffffu, incl, 2, 4);
-    if (tq >= 2) incl += t;
-    const float before = incl - run;
-    const float S = __shfl_sync(0xffffffffu, incl, 3, 4);
-    const float target = u2 * S;
-    int first = 0x7fffffff, lastnz = -1;
-    float vfirst = 0.f, vlast = 0.f;
-#pragma unroll
-    for (int e = 7; e >= 0; --e) {
-        if (before + cum[e] > target) {
-            first = id0 + e;
-            vfirst = val[e];
-        }
-        const float w = (e == 0) ? cum[0] : cum[e] - cum[e - 1];
-        if (lastnz < 0 && w > 0.f) {
-            lastnz = id0 + e;
-            vlast = val[e];
-        }
-    }
-    // quad: lowest crossing id; else highest id with mass
-#pragma unroll
-    for (int o = 1; o <= 2; o <<= 1) {
-        const int of = __shfl_xor_sync(0xffffffffu, first, o);
-        const float ovf = __shfl_xor_sync(0xffffffffu, vfirst, o);
-        if (of < first) {
-            first = of;
-            vfirst = ovf;
-        }
-        const int ol = __shfl_xor_sync(0xffffffffu, lastnz, o);
-        const float ovl = __shfl_xor_sync(0xffffffffu, vlast, o);
-        if (ol > lastnz) {
-            lastnz = ol;
-            vlast = ovl;
-        }
-    }
-    if (empty) return make_float4(-CUDART_INF_F, 0.f, __int_as_float(-1), 0.f);
-    const bool hit = first != 0x7fffffff;
-    return make_float4(m, S, __int_as_float(hit ? first : lastnz), hit ? vfirst : vlast);
+    for (int e = 0; e < 8; ++e) sum += ex2(l[e] - mref);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    return make_float2(m, sum);
 }
 
-__device__ __forceinline__ float4 empty_record(int greedy) {
-    return greedy ? make_float4(-CUDART_INF_F, 0.f, __int_as_float(0x7fffffff), -CUDART_INF_F)
-                  : make_float4(-CUDART_INF_F, 0.f, __int_as_float(-1), 0.f);
+__device__ __forceinline__ float2 empty_stats(int greedy) {
+    return greedy ? make_float2(-CUDART_INF_F, __int_as_float(0x7fffffff)) : make_float2(-CUDART_INF_F, 0.f);
 }
 
 // --------------------------------------------------------------------------------------------
-// Producer: chunk records crec[16][32] of a row block over one tile.
+// Producer: for a row block over one tile, the buffered values xbuf[16][kXRow] (z for draft
+// rows, the log2-weight for residual / bonus rows) and the chunk statistics cstat[16][32].
 // --------------------------------------------------------------------------------------------
 struct ProdArgs {
     const void* base;
@@ -302,7 +257,8 @@ struct ProdArgs {
 
 // HAS_T: rows may read target logits (residual / bonus draws of the verify pass).
 template <typename TL, int KS, typename TW, bool HAS_T>
-__device__ __forceinline__ void produce_chunks(const ProdArgs& pa, int tile, const RowBlock& rb, float4* crec) {
+__device__ __forceinline__ void produce_chunks(const ProdArgs& pa, int tile, const RowBlock& rb, float* xbuf,
+                                               float2* cstat) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, tq = lane & 3;
     const int ma = rb.mode[g], mb = rb.mode[g + 8];
@@ -350,8 +306,8 @@ __device__ __forceinline__ void produce_chunks(const ProdArgs& pa, int tile, con
         const int cb = tile0 + kCS * c;
         if (cb >= pa.V) {
             if (tq == 0) {
-                crec[g * kChunks + c] = empty_record(pa.greedy);
-                crec[(g + 8) * kChunks + c] = empty_record(pa.greedy);
+                cstat[g * kChunks + c] = empty_stats(pa.greedy);
+                cstat[(g + 8) * kChunks + c] = empty_stats(pa.greedy);
             }
             continue;
         }
@@ -399,7 +355,8 @@ __device__ __forceinline__ void produce_chunks(const ProdArgs& pa, int tile, con
                 }
             }
         }
-        // per-row log2-weights (greedy: the values themselves)
+        // per-row log2-weights (greedy: the values themselves); buffered: z for draft rows, the
+        // log2-weight (greedy: the value) for residual / bonus rows
         float la[8], lb[8];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -415,10 +372,7 @@ __device__ __forceinline__ void produce_chunks(const ProdArgs& pa, int tile, con
                 unpack8<TL>(xt_[HAS_T ? k : 0][h], t);
                 if (mode == ROW_BONUS) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        l[e] = pa.greedy ? t[e] : t[e] * pa.scale2;
-                        x[e] = t[e];
-                    }
+                    for (int e = 0; e < 8; ++e) l[e] = pa.greedy ? t[e] : t[e] * pa.scale2;
                 } else {
                     const float lse2 = rb.lse2[row], dl2 = rb.dl2[row];
 #pragma unroll
@@ -427,34 +381,132 @@ __device__ __forceinline__ void produce_chunks(const ProdArgs& pa, int tile, con
                         l[e] = w > 0.f ? lg2(w) : -CUDART_INF_F;
                     }
                 }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = l[e];
             } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) l[e] = -CUDART_INF_F;
+                for (int e = 0; e < 8; ++e) l[e] = x[e] = -CUDART_INF_F;
             }
+            float4* dst = reinterpret_cast<float4*>(xbuf + row * kXRow + kCS * c + 8 * tq);
+            dst[0] = make_float4(x[0], x[1], x[2], x[3]);
+            dst[1] = make_float4(x[4], x[5], x[6], x[7]);
         }
-        const float4 ra = chunk_record(la, xa, id0, rb.u2[g], pa.greedy);
-        const float4 rbk = chunk_record(lb, xb, id0, rb.u2[g + 8], pa.greedy);
+        const float2 sa = chunk_stats(la, id0, pa.greedy);
+        const float2 sb = chunk_stats(lb, id0, pa.greedy);
         if (tq == 0) {
-            crec[g * kChunks + c] = ra;
-            crec[(g + 8) * kChunks + c] = rbk;
+            cstat[g * kChunks + c] = sa;
+            cstat[(g + 8) * kChunks + c] = sb;
         }
     }
 }
 
 // --------------------------------------------------------------------------------------------
-// Tile record from a row's 32 chunk records (one warp, lane = chunk).
-// T > 0: {key = ln(mass_t) - ln E_t, ln(mass_t), candidate id, value at it};
+// Draft-sampling producer (tensor-core path): every row is a draft row (rows past B read row
+// brow[0] and are never finalised), so there is no per-lane mode logic; greedy, the W2 source
+// and "tile fully inside the vocabulary" are compile-time.  Writes z to xbuf and the chunk
+// statistics of z * scale2 (greedy: of z) to cstat.
+// --------------------------------------------------------------------------------------------
+__device__ __forceinline__ void mma4(float& d0, float& d1, float& d2, float& d3, const uint32_t a0, const uint32_t a1,
+                                     const uint32_t a2, const uint32_t a3, const uint32_t b0, const uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <typename TL, int KS, bool GREEDY, bool W2SMEM, bool FULL>
+__device__ __forceinline__ void produce_sample(const TL* base, const uint16_t* W1, const uint16_t* W2, const uint4* w2s,
+                                               int V, bool vec, int tile, const RowBlock& rb, float* xbuf,
+                                               float2* cstat, float scale2) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, tq = lane & 3;
+    const long long oA = rb.brow[g] >= 0 ? rb.brow[g] : rb.brow[0];
+    const long long oB = rb.brow[g + 8] >= 0 ? rb.brow[g + 8] : rb.brow[0];
+    const TL* rowA = base + oA;
+    const TL* rowB = base + oB;
+    const int tile0 = tile * kTS;
+    Raw8<TL> ra[kChunksPerWarp], rbv[kChunksPerWarp];
+#pragma unroll
+    for (int k = 0; k < kChunksPerWarp; ++k) {
+        const int v0 = tile0 + kCS * (warp + kWarps * k) + 8 * tq;
+        load_raw8<TL>(rowA, v0, V, FULL || vec, ra[k]);
+        load_raw8<TL>(rowB, v0, V, FULL || vec, rbv[k]);
+    }
+    Frag<KS> fa, fb;
+    load_frag_global<KS>(W1, rb.prev[g], tq, fa);
+    load_frag_global<KS>(W1, rb.prev[g + 8], tq, fb);
+#pragma unroll
+    for (int k = 0; k < kChunksPerWarp; ++k) {
+        const int c = warp + kWarps * k;
+        const int cb = tile0 + kCS * c;
+        if (!FULL && cb >= V) {
+            if (tq == 0) {
+                cstat[g * kChunks + c] = empty_stats(GREEDY);
+                cstat[(g + 8) * kChunks + c] = empty_stats(GREEDY);
+            }
+            continue;
+        }
+        float xa[8], xb[8];
+        unpack8<TL>(ra[k], xa);
+        unpack8<TL>(rbv[k], xb);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            const int vl = kCS * c + 8 * (g >> 1) + 2 * nt + (g & 1);  // id (in tile) this lane feeds as column g
+            Frag<KS> fw;
+            if (FULL || tile0 + vl < V) {
+                if constexpr (W2SMEM) load_frag_smem<KS>(w2s, vl, tq, fw);
+                else load_frag_global<KS>(W2, tile0 + vl, tq, fw);
+            } else {
+                frag_zero<KS>(fw);
+            }
+#pragma unroll
+            for (int s = 0; s < KS; ++s)
+                mma4(xa[2 * nt], xa[2 * nt + 1], xb[2 * nt], xb[2 * nt + 1], fa.w[2 * s], fb.w[2 * s], fa.w[2 * s + 1],
+                     fb.w[2 * s + 1], fw.w[2 * s], fw.w[2 * s + 1]);
+        }
+        float4* dA = reinterpret_cast<float4*>(xbuf + g * kXRow + kCS * c + 8 * tq);
+        float4* dB = reinterpret_cast<float4*>(xbuf + (g + 8) * kXRow + kCS * c + 8 * tq);
+        dA[0] = make_float4(xa[0], xa[1], xa[2], xa[3]);
+        dA[1] = make_float4(xa[4], xa[5], xa[6], xa[7]);
+        dB[0] = make_float4(xb[0], xb[1], xb[2], xb[3]);
+        dB[1] = make_float4(xb[4], xb[5], xb[6], xb[7]);
+        if constexpr (!GREEDY) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                xa[e] *= scale2;
+                xb[e] *= scale2;
+            }
+        }
+        const float2 sa = chunk_stats(xa, cb + 8 * tq, GREEDY);
+        const float2 sb = chunk_stats(xb, cb + 8 * tq, GREEDY);
+        if (tq == 0) {
+            cstat[g * kChunks + c] = sa;
+            cstat[(g + 8) * kChunks + c] = sb;
+        }
+    }
+}
+
+// --------------------------------------------------------------------------------------------
+// Tile record of one row (one warp, lane = chunk) from its 32 chunk statistics and its
+// buffered values xrow (weights 2^(x * lscale): lscale = log2(e)/T for z, 1 for log2-weights).
+// T > 0: {key = ln(mass_t) - ln E_t, ln(mass_t), candidate id, buffered value at it}: the chunk
+// by u1 over the chunk masses, the id by u2 inside that chunk;
 // greedy: {max, NaN, argmax id, max}.  A tile without mass gets key -inf and candidate -1.
 // --------------------------------------------------------------------------------------------
-__device__ __forceinline__ float4 finalize_chunks(float4 cr, bool valid, int greedy, float u1, float lnE) {
+__device__ __forceinline__ float4 finalize_tile(const float* xrow, float2 cs, int tile, int V, int greedy, float lscale,
+                                                float u1, float u2, float lnE) {
+    const int lane = threadIdx.x & 31;
+    const int tile0 = tile * kTS;
+    const bool valid = tile0 + kCS * lane < V;
     if (greedy) {
-        float m = valid ? cr.x : -CUDART_INF_F;
-        int idx = valid ? __float_as_int(cr.z) : 0x7fffffff;
+        float m = valid ? cs.x : -CUDART_INF_F;
+        int idx = valid ? __float_as_int(cs.y) : 0x7fffffff;
         warp_argmax(m, idx);
         return make_float4(m, CUDART_NAN_F, __int_as_float(idx), m);
     }
-    const float mc = valid ? cr.x : -CUDART_INF_F;
-    const float sc = valid ? cr.y : 0.f;
+    const float mc = valid ? cs.x : -CUDART_INF_F;
+    const float sc = valid ? cs.y : 0.f;
     const float mt = warp_max(mc);
     if (mt == -CUDART_INF_F) return make_float4(-CUDART_INF_F, -CUDART_INF_F, __int_as_float(-1), 0.f);
     const float w = (sc > 0.f) ? sc * ex2(mc - mt) : 0.f;
@@ -462,8 +514,7 @@ __device__ __forceinline__ float4 finalize_chunks(float4 cr, bool valid, int gre
     const float St = __shfl_sync(0xffffffffu, P, 31);
     if (!(St > 0.f)) return make_float4(-CUDART_INF_F, -CUDART_INF_F, __int_as_float(-1), 0.f);
     const float lmass = (mt + lg2(St)) * kLn2;
-    const float target = u1 * St;
-    const unsigned hit = __ballot_sync(0xffffffffu, P > target);
+    const unsigned hit = __ballot_sync(0xffffffffu, P > u1 * St);
     int cstar;
     if (hit) {
         cstar = __ffs(hit) - 1;
@@ -471,56 +522,121 @@ __device__ __forceinline__ float4 finalize_chunks(float4 cr, bool valid, int gre
         const unsigned nz = __ballot_sync(0xffffffffu, w > 0.f);
         cstar = nz ? 31 - __clz(nz) : 0;
     }
-    const int cand = __shfl_sync(0xffffffffu, __float_as_int(cr.z), cstar);
-    const float val = __shfl_sync(0xffffffffu, cr.w, cstar);
-    return make_float4(lmass - lnE, lmass, __int_as_float(cand), val);
+    // id by u2 inside chunk cstar (masses relative to its own maximum)
+    const float mcs = __shfl_sync(0xffffffffu, mc, cstar);
+    const int vl = kCS * cstar + lane;
+    const float xv = xrow[vl];
+    const float e = (tile0 + vl < V) ? ex2(xv * lscale - mcs) : 0.f;
+    const float Q = warp_incl_scan(e);
+    const float Sc = __shfl_sync(0xffffffffu, Q, 31);
+    const unsigned hit2 = __ballot_sync(0xffffffffu, Q > u2 * Sc);
+    int xl;
+    if (hit2) {
+        xl = __ffs(hit2) - 1;
+    } else {
+        const unsigned nz = __ballot_sync(0xffffffffu, e > 0.f);
+        xl = nz ? 31 - __clz(nz) : 0;
+    }
+    const float xc = __shfl_sync(0xffffffffu, xv, xl);
+    return make_float4(lmass - lnE, lmass, __int_as_float(tile0 + kCS * cstar + xl), xc);
 }
 
-// Reduction of a request's tile records (one warp): the highest key wins, lowest tile on ties.
-struct TileWinner {
-    int cand;
-    float val;
-    float key;
-    float lse;
+// Running reduction of tile records: the highest key wins (lowest tile on ties); the tiles'
+// log-masses are merged into a log-sum-exp on the fly.
+struct TileAcc {
+    float key, val, m, s;
+    int tile, cand;
 };
-__device__ inline TileWinner reduce_tiles(const float4* rec, int nt, bool want_lse) {
-    const int lane = threadIdx.x & 31;
-    float bk = -CUDART_INF_F, bz = 0.f, lmax = -CUDART_INF_F;
-    int bt = 0x7fffffff, bc = -1;
-    for (int t = lane; t < nt; t += 32) {
-        const float4 q = __ldcg(rec + t);
-        if (bt == 0x7fffffff || q.x > bk) {  // t ascends: equal keys keep the lower tile
-            bk = q.x;
-            bt = t;
-            bc = __float_as_int(q.z);
-            bz = q.w;
-        }
-        lmax = fmaxf(lmax, q.y);
+__device__ __forceinline__ TileAcc tile_acc_init() {
+    return TileAcc{-CUDART_INF_F, 0.f, -CUDART_INF_F, 0.f, 0x7fffffff, -1};
+}
+__device__ __forceinline__ void tile_acc_add(TileAcc& a, const float4 q, int t, bool want_lse) {
+    if (a.tile == 0x7fffffff || q.x > a.key || (q.x == a.key && t < a.tile)) {
+        a.key = q.x;
+        a.tile = t;
+        a.cand = __float_as_int(q.z);
+        a.val = q.w;
     }
+    if (want_lse && q.y != -CUDART_INF_F) {
+        const float l2 = q.y * kLog2e;
+        if (l2 > a.m) {
+            a.s = (a.m == -CUDART_INF_F) ? 1.f : a.s * ex2(a.m - l2) + 1.f;
+            a.m = l2;
+        } else {
+            a.s += ex2(l2 - a.m);
+        }
+    }
+}
+// Merge over `width` consecutive lanes (a power of two <= 32); every lane of the warp calls it.
+__device__ __forceinline__ void tile_acc_shfl_merge(TileAcc& a, int width, bool want_lse) {
+    for (int o = 1; o < width; o <<= 1) {
+        TileAcc b;
+        b.key = __shfl_xor_sync(0xffffffffu, a.key, o);
+        b.tile = __shfl_xor_sync(0xffffffffu, a.tile, o);
+        b.cand = __shfl_xor_sync(0xffffffffu, a.cand, o);
+        b.val = __shfl_xor_sync(0xffffffffu, a.val, o);
+        b.m = __shfl_xor_sync(0xffffffffu, a.m, o);
+        b.s = __shfl_xor_sync(0xffffffffu, a.s, o);
+        if (b.tile != 0x7fffffff && (a.tile == 0x7fffffff || b.key > a.key || (b.key == a.key && b.tile < a.tile))) {
+            a.key = b.key;
+            a.tile = b.tile;
+            a.cand = b.cand;
+            a.val = b.val;
+        }
+        if (want_lse) {
+            const float M = fmaxf(a.m, b.m);
+            a.s = (M == -CUDART_INF_F) ? 0.f
+                                       : (a.m == -CUDART_INF_F ? 0.f : a.s * ex2(a.m - M)) +
+                                             (b.m == -CUDART_INF_F ? 0.f : b.s * ex2(b.m - M));
+            a.m = M;
+        }
+    }
+}
+// ln of the merged log-sum-exp (natural units).
+__device__ __forceinline__ float tile_acc_lse(const TileAcc& a) {
+    return a.m == -CUDART_INF_F ? -CUDART_INF_F : (a.m + lg2(a.s)) * kLn2;
+}
+
+// Reduction of one request's tile records rec[0..nt) by `width` consecutive lanes starting at a
+// multiple of `width` (sub = lane index within the group); records are loaded in batches of 8
+// per lane before they are used, so a batch costs one memory round trip.
+__device__ __forceinline__ TileAcc reduce_tiles_group(const float4* rec, int nt, int sub, int width, bool want_lse) {
+    constexpr int kBatch = 8;
+    TileAcc acc = tile_acc_init();
+    for (int t0 = sub; t0 < nt; t0 += width * kBatch) {
+        float4 q[kBatch];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-        const int ot = __shfl_xor_sync(0xffffffffu, bt, o);
-        const int oc = __shfl_xor_sync(0xffffffffu, bc, o);
-        const float oz = __shfl_xor_sync(0xffffffffu, bz, o);
-        const bool take = (ot != 0x7fffffff) && (bt == 0x7fffffff || ok > bk || (ok == bk && ot < bt));
-        if (take) {
-            bk = ok;
-            bt = ot;
-            bc = oc;
-            bz = oz;
+        for (int k = 0; k < kBatch; ++k) {
+            const int t = t0 + width * k;
+            q[k] = t < nt ? __ldcg(rec + t) : make_float4(-CUDART_INF_F, -CUDART_INF_F, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const int t = t0 + width * k;  // ascending: equal keys keep the lower tile
+            if (t < nt && (acc.tile == 0x7fffffff || q[k].x > acc.key)) {
+                acc.key = q[k].x;
+                acc.tile = t;
+                acc.cand = __float_as_int(q[k].z);
+                acc.val = q[k].w;
+            }
+        }
+        if (want_lse) {
+            float bm = -CUDART_INF_F;
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) bm = fmaxf(bm, q[k].y);  // padding is -inf
+            if (bm != -CUDART_INF_F) {
+                const float bm2 = bm * kLog2e;
+                float bs = 0.f;
+#pragma unroll
+                for (int k = 0; k < kBatch; ++k) bs += ex2(fmaf(q[k].y, kLog2e, -bm2));
+                const float M = fmaxf(acc.m, bm2);
+                acc.s = (acc.m == -CUDART_INF_F ? 0.f : acc.s * ex2(acc.m - M)) + bs * ex2(bm2 - M);
+                acc.m = M;
+            }
         }
     }
-    TileWinner wv{bc, bz, bk, CUDART_NAN_F};
-    if (want_lse) {
-        const float M = warp_max(lmax);
-        float s = 0.f;
-        if (M != -CUDART_INF_F)
-            for (int t = lane; t < nt; t += 32) s += ex2((__ldcg(&rec[t].y) - M) * kLog2e);
-        s = warp_sum(s);
-        wv.lse = (M == -CUDART_INF_F) ? -CUDART_INF_F : M + logf(s);
-    }
-    return wv;
+    tile_acc_shfl_merge(acc, width, want_lse);
+    return acc;
 }
 
 }  // namespace dspark

@@ -39,15 +39,16 @@ struct SampleArgs {
     float* zat;
     WsHeader* hdr;
     int32_t* cur_tok;
-    float4* part;  // [B][nt] tile records
+    float4* part;  // [2][B][nt] tile records, by step parity
     uint64_t limit_ns;
+    int redundant;  // every block reduces every request (one grid-wide wait per step)
     int w2_smem;
     int vec_ok;  // base rows start on 16-byte boundaries: 8-wide loads and L2 prefetch allowed
 };
 
 size_t sample_smem_bytes(int B, int r, bool mma, bool w2_smem) {
-    size_t b = sizeof(float4) * kRows * kChunks + align_up(sizeof(RowBlock), 16) + align_up(sizeof(int) * (size_t)B, 16) +
-               sizeof(float4) * (size_t)B;
+    size_t b = sizeof(float) * kRows * kXRow + sizeof(float2) * kRows * kChunks + align_up(sizeof(RowBlock), 16) +
+               align_up(sizeof(int) * (size_t)B, 16) + sizeof(float4) * (size_t)B;
     if (mma) {
         if (w2_smem) b += (size_t)kTS * r * 2;
     } else {
@@ -79,12 +80,13 @@ __device__ void prefetch_rows(const SampleArgs& a, int tile, int row0, int step)
     prefetch_l2(p, (uint32_t)(n * sizeof(TL)));
 }
 
-template <typename TL, int KS, typename TW>
+template <typename TL, int KS, typename TW, bool GREEDY>
 __global__ void __launch_bounds__(kThreads, 1) sample_kernel(SampleArgs a) {
     constexpr bool kMMA = KS > 0;
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    float4* crec = reinterpret_cast<float4*>(smem_raw);
-    RowBlock* rb = reinterpret_cast<RowBlock*>(crec + kRows * kChunks);
+    float* xbuf = reinterpret_cast<float*>(smem_raw);                  // [kRows][kXRow]: z
+    float2* cstat = reinterpret_cast<float2*>(xbuf + kRows * kXRow);   // [kRows][kChunks]
+    RowBlock* rb = reinterpret_cast<RowBlock*>(cstat + kRows * kChunks);
     int* prev = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(rb) + align_up(sizeof(RowBlock), 16));
     float4* rnd = reinterpret_cast<float4*>(reinterpret_cast<unsigned char*>(prev) + align_up(sizeof(int) * (size_t)a.B, 16));
     unsigned char* wreg = reinterpret_cast<unsigned char*>(rnd + a.B);
@@ -114,23 +116,18 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(SampleArgs a) {
     if (!a.greedy) step_randoms(a, 0, rnd);
 
     uint32_t target = 0;
+    const size_t part_stride = (size_t)a.B * a.nt;
     for (int step = 0; step < a.gamma; ++step) {
-        for (int j = tid; j < a.B; j += kThreads) {
-            int p;
-            if (step == 0) {
-                p = a.anchor[j];
-                if (p < 0 || p >= a.V) {
+        float4* part = a.part + (size_t)(step & 1) * part_stride;
+        if (step == 0 || !a.redundant) {
+            for (int j = tid; j < a.B; j += kThreads) {
+                int p = step == 0 ? a.anchor[j] : __ldcg(a.cur_tok + j);
+                if (p < 0 || p >= a.V) {  // a bad anchor, or a row whose tiles all had no mass
                     record_status(&a.hdr->status, DSPARK_ERR_TOKEN_RANGE);
                     p = min(max(p, 0), a.V - 1);
                 }
-            } else {
-                p = __ldcg(a.cur_tok + j);
-                if (p < 0 || p >= a.V) {  // only when every tile of a row had no mass (non-finite logits)
-                    record_status(&a.hdr->status, DSPARK_ERR_TOKEN_RANGE);
-                    p = min(max(p, 0), a.V - 1);
-                }
+                prev[j] = p;
             }
-            prev[j] = p;
         }
         __syncthreads();
         for (int tile = blockIdx.x; tile < a.nt; tile += a.G) {
@@ -150,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(SampleArgs a) {
                     rb->u2[tid] = q.y;
                     rb->lnE[tid] = q.z;
                 }
-                // next row block of this step (or the first of the next step is prefetched at the wait)
+                // the next row block of this step (the first of the next step is prefetched at the wait)
                 if (row0 + kRows < a.B) prefetch_rows<TL>(a, tile, row0 + kRows, step);
                 if constexpr (!kMMA) {
                     __syncthreads();
@@ -162,62 +159,109 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(SampleArgs a) {
                     }
                 }
                 __syncthreads();
-                produce_chunks<TL, KS, TW, false>(pa, tile, *rb, crec);
+                if constexpr (kMMA) {
+                    const TL* base = reinterpret_cast<const TL*>(a.base);
+                    const uint16_t* W1 = reinterpret_cast<const uint16_t*>(a.W1);
+                    const uint16_t* W2 = reinterpret_cast<const uint16_t*>(a.W2);
+                    const bool full = (tile + 1) * kTS <= a.V && a.vec_ok;
+                    if (pa.w2s) {
+                        if (full) produce_sample<TL, KS, GREEDY, true, true>(base, W1, W2, pa.w2s, a.V, true, tile, *rb, xbuf, cstat, a.scale2);
+                        else produce_sample<TL, KS, GREEDY, true, false>(base, W1, W2, pa.w2s, a.V, a.vec_ok, tile, *rb, xbuf, cstat, a.scale2);
+                    } else {
+                        if (full) produce_sample<TL, KS, GREEDY, false, true>(base, W1, W2, nullptr, a.V, true, tile, *rb, xbuf, cstat, a.scale2);
+                        else produce_sample<TL, KS, GREEDY, false, false>(base, W1, W2, nullptr, a.V, a.vec_ok, tile, *rb, xbuf, cstat, a.scale2);
+                    }
+                } else {
+                    produce_chunks<TL, KS, TW, false>(pa, tile, *rb, xbuf, cstat);
+                }
                 __syncthreads();
                 for (int rl = warp; rl < kRows; rl += kWarps) {
                     const int j = row0 + rl;
                     if (j >= a.B) continue;
-                    const bool valid = tile * kTS + kCS * lane < a.V;
-                    const float4 rec = finalize_chunks(crec[rl * kChunks + lane], valid, a.greedy, rb->u1[rl], rb->lnE[rl]);
-                    if (lane == 0) a.part[(size_t)j * a.nt + tile] = rec;
+                    const float4 rec = finalize_tile(xbuf + rl * kXRow, cstat[rl * kChunks + lane], tile, a.V,
+                                                     GREEDY, a.scale2, rb->u1[rl], rb->u2[rl], rb->lnE[rl]);
+                    if (lane == 0) part[(size_t)j * a.nt + tile] = rec;
                 }
                 __syncthreads();
             }
         }
+        // Everything of the next step that does not depend on its tokens happens while the
+        // last blocks arrive: its random draws and the L2 prefetch of its first row block.
         target += (uint32_t)a.G;
-        if (!grid_wait(a.hdr, target, a.limit_ns)) return;
-        for (int j = blockIdx.x + a.G * warp; j < a.B; j += a.G * kWarps) {
-            const TileWinner w = reduce_tiles(a.part + (size_t)j * a.nt, a.nt, !a.greedy);
-            if (lane == 0) {
-                a.cur_tok[j] = w.cand;
-                const size_t o = (size_t)j * a.gamma + step;
-                a.tokens[o] = w.cand;
-                a.draft_lse[o] = a.greedy ? CUDART_NAN_F : w.lse;
-                a.zat[o] = w.val;
-            }
-        }
+        grid_arrive(a.hdr);
         if (step + 1 < a.gamma) {
-            // everything of the next step that does not depend on its tokens happens while the
-            // last blocks arrive
-            target += (uint32_t)a.G;
-            grid_arrive(a.hdr);
             prefetch_rows<TL>(a, blockIdx.x, 0, step + 1);
             if (!a.greedy) step_randoms(a, step + 1, rnd);
-            if (!grid_wait_arrived(a.hdr, target, a.limit_ns)) return;
+        }
+        if (!grid_wait_arrived(a.hdr, target, a.limit_ns)) return;
+        if (a.redundant) {
+            // every block reduces every request: width = threads per request (power of two)
+            int width = kThreads / a.B;
+            width = width >= 32 ? 32 : (width >= 16 ? 16 : (width >= 8 ? 8 : (width >= 4 ? 4 : (width >= 2 ? 2 : 1))));
+            const int per_pass = kThreads / width;
+            for (int jb = 0; jb < a.B; jb += per_pass) {  // uniform trip count: every lane reaches the shuffles
+                const int j = jb + tid / width, sub = tid % width;
+                const TileAcc w = reduce_tiles_group(part + (size_t)min(j, a.B - 1) * a.nt, a.nt, sub, width, !GREEDY);
+                if (sub == 0 && j < a.B) {
+                    prev[j] = w.cand;
+                    if ((int)blockIdx.x == j % a.G) {
+                        const size_t o = (size_t)j * a.gamma + step;
+                        a.tokens[o] = w.cand;
+                        a.draft_lse[o] = a.greedy ? CUDART_NAN_F : tile_acc_lse(w);
+                        a.zat[o] = w.val;
+                    }
+                }
+            }
+            __syncthreads();
+            for (int j = tid; j < a.B; j += kThreads)
+                if (prev[j] < 0 || prev[j] >= a.V) {  // only when every tile of a row had no mass
+                    record_status(&a.hdr->status, DSPARK_ERR_TOKEN_RANGE);
+                    prev[j] = min(max(prev[j], 0), a.V - 1);
+                }
+        } else {
+            for (int j = blockIdx.x + a.G * warp; j < a.B; j += a.G * kWarps) {
+                const TileAcc w = reduce_tiles_group(part + (size_t)j * a.nt, a.nt, lane, 32, !GREEDY);
+                if (lane == 0) {
+                    a.cur_tok[j] = w.cand;
+                    const size_t o = (size_t)j * a.gamma + step;
+                    a.tokens[o] = w.cand;
+                    a.draft_lse[o] = a.greedy ? CUDART_NAN_F : tile_acc_lse(w);
+                    a.zat[o] = w.val;
+                }
+            }
+            if (step + 1 < a.gamma) {
+                target += (uint32_t)a.G;
+                if (!grid_wait(a.hdr, target, a.limit_ns)) return;
+            }
         }
     }
 }
 
 using KernelFn = void (*)(SampleArgs);
 
-template <typename TL>
+template <typename TL, bool G>
 KernelFn pick_mma(int r) {
     switch (r) {
-        case 16: return sample_kernel<TL, 1, uint16_t>;
-        case 32: return sample_kernel<TL, 2, uint16_t>;
-        case 64: return sample_kernel<TL, 4, uint16_t>;
-        case 128: return sample_kernel<TL, 8, uint16_t>;
-        case 256: return sample_kernel<TL, 16, uint16_t>;
+        case 16: return sample_kernel<TL, 1, uint16_t, G>;
+        case 32: return sample_kernel<TL, 2, uint16_t, G>;
+        case 64: return sample_kernel<TL, 4, uint16_t, G>;
+        case 128: return sample_kernel<TL, 8, uint16_t, G>;
+        case 256: return sample_kernel<TL, 16, uint16_t, G>;
         default: return nullptr;
     }
 }
 
-KernelFn pick_kernel(const dspark_sample_params* p, bool mma) {
+template <bool G>
+KernelFn pick_kernel_g(const dspark_sample_params* p, bool mma) {
     const bool lb = p->logits_dtype == DSPARK_BF16;
-    if (mma) return lb ? pick_mma<__nv_bfloat16>(p->r) : pick_mma<float>(p->r);
+    if (mma) return lb ? pick_mma<__nv_bfloat16, G>(p->r) : pick_mma<float, G>(p->r);
     const bool wb = p->w_dtype == DSPARK_BF16;
-    if (lb) return wb ? sample_kernel<__nv_bfloat16, 0, __nv_bfloat16> : sample_kernel<__nv_bfloat16, 0, float>;
-    return wb ? sample_kernel<float, 0, __nv_bfloat16> : sample_kernel<float, 0, float>;
+    if (lb) return wb ? sample_kernel<__nv_bfloat16, 0, __nv_bfloat16, G> : sample_kernel<__nv_bfloat16, 0, float, G>;
+    return wb ? sample_kernel<float, 0, __nv_bfloat16, G> : sample_kernel<float, 0, float, G>;
+}
+
+KernelFn pick_kernel(const dspark_sample_params* p, bool mma) {
+    return p->temperature == 0.f ? pick_kernel_g<true>(p, mma) : pick_kernel_g<false>(p, mma);
 }
 
 }  // namespace
@@ -240,7 +284,7 @@ dspark_status validate_sample_params(const dspark_sample_params* p) {
 size_t sample_workspace_bytes(const dspark_sample_params* p) {
     const size_t nt = (size_t)(p->V + kTS - 1) / kTS;
     return kHeaderBytes + align_up(sizeof(int32_t) * (size_t)p->B, 256) +
-           align_up(sizeof(float4) * (size_t)p->B * nt, 256);
+           align_up(2 * sizeof(float4) * (size_t)p->B * nt, 256);
 }
 
 }  // namespace dspark
@@ -306,6 +350,7 @@ extern "C" dspark_status dspark_markov_sample_block(const dspark_sample_params* 
     a.cur_tok = reinterpret_cast<int32_t*>(ws + kHeaderBytes);
     a.part = reinterpret_cast<float4*>(ws + kHeaderBytes + align_up(sizeof(int32_t) * (size_t)p->B, 256));
     a.limit_ns = wait_limit_ns();
+    a.redundant = (size_t)p->B * nt <= 8192 && p->B <= kThreads;
     a.w2_smem = w2_smem;
     const size_t esz = p->logits_dtype == DSPARK_BF16 ? 2 : 4;
     a.vec_ok = ((uintptr_t)base_logits % 16 == 0) && (((size_t)p->V * esz) % 16 == 0);

@@ -332,8 +332,9 @@ __device__ int block_sample_row(const VerifyArgs& a, const TL* row, int j, int p
 template <typename TL, int KS, typename TW>
 __global__ void __launch_bounds__(kThreads, 1) verify_jobs_kernel(VerifyArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    float4* crec = reinterpret_cast<float4*>(smem_raw);  // [kRows][kChunks]
-    RowBlock* rb = reinterpret_cast<RowBlock*>(crec + kRows * kChunks);
+    float* xbuf = reinterpret_cast<float*>(smem_raw);                 // [kRows][kXRow]: log2-weights
+    float2* cstat = reinterpret_cast<float2*>(xbuf + kRows * kXRow);  // [kRows][kChunks]
+    RowBlock* rb = reinterpret_cast<RowBlock*>(cstat + kRows * kChunks);
     int4* jb = reinterpret_cast<int4*>(reinterpret_cast<unsigned char*>(rb) + align_up(sizeof(RowBlock), 16));
     float* scratch = reinterpret_cast<float*>(jb + kRows);  // fallback scratch [64]
     float* w1s = scratch + 64;                              // CUDA-core path: [kRows][r]
@@ -393,13 +394,13 @@ __global__ void __launch_bounds__(kThreads, 1) verify_jobs_kernel(VerifyArgs a) 
         }
         __syncthreads();
     }
-    produce_chunks<TL, KS, TW, true>(pa, tile, *rb, crec);
+    produce_chunks<TL, KS, TW, true>(pa, tile, *rb, xbuf, cstat);
     __syncthreads();
     for (int q = warp; q < kRows; q += kWarps) {
         if (rb->mode[q] == ROW_OFF) continue;
         const int j = row0 + q;
-        const bool valid = tile * kTS + kCS * lane < a.V;
-        const float4 rec = finalize_chunks(crec[q * kChunks + lane], valid, a.greedy, rb->u1[q], rb->lnE[q]);
+        const float4 rec = finalize_tile(xbuf + q * kXRow, cstat[q * kChunks + lane], tile, a.V, a.greedy, 1.f,
+                                         rb->u1[q], rb->u2[q], rb->lnE[q]);
         if (lane == 0) a.jobpart[(size_t)j * a.nt + tile] = rec;
     }
     __syncthreads();
@@ -415,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_jobs_kernel(VerifyArgs a) 
         const int4 job = jb[q];
         if (job.x == JOB_NONE) continue;
         const int j = row0 + q;
-        const TileWinner w = reduce_tiles(a.jobpart + (size_t)j * a.nt, a.nt, false);
+        const TileAcc w = reduce_tiles_group(a.jobpart + (size_t)j * a.nt, a.nt, lane, 32, false);
         if (lane == 0) {
             s_fallback[q] = (w.cand < 0);
             if (w.cand >= 0) a.corr[j] = w.cand;
@@ -551,8 +552,8 @@ extern "C" dspark_status dspark_verify(const dspark_sample_params* p, const void
     if (cudaLaunchKernel((const void*)rows, dim3(L.nseg, p->gamma, p->B), dim3(kThreads), args, 0, s) != cudaSuccess)
         return DSPARK_ERR_CUDA;
     RowsFn jobs = pick_jobs(p, mma);
-    size_t smem = sizeof(float4) * kRows * kChunks + align_up(sizeof(RowBlock), 16) + sizeof(int4) * kRows +
-                  sizeof(float) * 64 + (mma ? 0 : sizeof(float) * kRows * (size_t)p->r);
+    size_t smem = sizeof(float) * kRows * kXRow + sizeof(float2) * kRows * kChunks + align_up(sizeof(RowBlock), 16) +
+                  sizeof(int4) * kRows + sizeof(float) * 64 + (mma ? 0 : sizeof(float) * kRows * (size_t)p->r);
     if (smem > kMaxSmem) return DSPARK_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute((const void*)jobs, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return DSPARK_ERR_CUDA;
