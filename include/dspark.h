@@ -197,6 +197,32 @@ dspark_status dspark_schedule_verify_len(int B, int gamma, const float* conf, in
                                          int32_t* offsets, float* objective, void* workspace, size_t ws_bytes,
                                          dspark_stream_t stream);
 
+/*
+ * Draft sampling without any allocation by the caller.  (No counterpart on the pages: this is a
+ * convenience of this library.)  Some callers cannot call cudaMalloc at all -- for instance a
+ * plug-in running inside a serving process whose device memory is owned by someone else's
+ * pool, or a loop that must not allocate after start-up because an allocation can synchronise
+ * the device -- and so cannot provide the workspace that dspark_markov_sample_block needs.
+ * This variant runs the same kernel with its scratch in a fixed array that the library keeps
+ * in device memory (a file-scope __device__ array of DSPARK_NOALLOC_SCRATCH_BYTES, present on
+ * every GPU that loads the library until the process exits).  The caller still passes every
+ * input and output, exactly as for dspark_markov_sample_block.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *     with that device current; make that first call before any stream capture.
+ *   - A call whose scratch would exceed the array (dspark_sample_workspace_size(p) >
+ *     DSPARK_NOALLOC_SCRATCH_BYTES) returns DSPARK_ERR_UNSUPPORTED and enqueues nothing.
+ *   - All calls share the one array and it keeps the last call's contents; each call clears
+ *     the part that must start at zero.  Calls that can overlap on the GPU (other streams,
+ *     other host threads) race on the array: serialise them.
+ *   - Device-side errors land in the shared array's status word, which is not exposed; use
+ *     dspark_markov_sample_block when the device status is needed.
+ */
+#define DSPARK_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+dspark_status dspark_markov_sample_block_noalloc(const dspark_sample_params* p, const void* base_logits,
+                                                 const void* W1, const void* W2, const int32_t* anchor,
+                                                 int32_t* tokens, float* draft_lse, float* draft_logit_at_tok,
+                                                 dspark_stream_t stream);
+
 /* Reads the device status word of `workspace` after synchronising `stream`
  * (DSPARK_OK when no device-side error was recorded).  `workspace` is a device pointer;
  * `out` is a host pointer. */

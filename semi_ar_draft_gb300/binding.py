@@ -45,6 +45,8 @@ def lib():
         L.dspark_sample_workspace_size.restype = sz
         L.dspark_markov_sample_block.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.dspark_markov_sample_block.restype = i32
+        L.dspark_markov_sample_block_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.dspark_markov_sample_block_noalloc.restype = i32
         L.dspark_verify_workspace_size.argtypes = [P, i32]
         L.dspark_verify_workspace_size.restype = sz
         L.dspark_verify.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, sz, vp]
@@ -119,6 +121,16 @@ def dspark_markov_sample_block(p, base_logits, W1, W2, anchor, tokens, draft_lse
                                           _ptr(tokens), _ptr(draft_lse), _ptr(draft_logit_at_tok), _ptr(workspace),
                                           workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "dspark_markov_sample_block")
+
+
+def dspark_markov_sample_block_noalloc(p, base_logits, W1, W2, anchor, tokens, draft_lse, draft_logit_at_tok,
+                                       stream=None):
+    """Draft sampling with the library's own fixed device scratch (no workspace argument): for
+    callers that cannot allocate device memory.  Calls must not overlap on the GPU."""
+    st = lib().dspark_markov_sample_block_noalloc(C.byref(p), _ptr(base_logits), _ptr(W1), _ptr(W2), _ptr(anchor),
+                                                  _ptr(tokens), _ptr(draft_lse), _ptr(draft_logit_at_tok),
+                                                  _stream(stream))
+    _check(st, "dspark_markov_sample_block_noalloc")
 
 
 def dspark_verify_workspace_size(p: SampleParams, gamma_t: int) -> int:

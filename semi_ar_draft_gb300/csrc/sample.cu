@@ -17,6 +17,7 @@
 // When each block owns a single tile and the W2 rows of it fit, they are staged in shared
 // memory once for all gamma steps.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 
 #include "host_util.h"
@@ -361,4 +362,33 @@ extern "C" dspark_status dspark_markov_sample_block(const dspark_sample_params* 
     if (cudaLaunchCooperativeKernel((const void*)fn, dim3(G), dim3(kThreads), args, smem, s) != cudaSuccess)
         return DSPARK_ERR_CUDA;
     return DSPARK_OK;
+}
+
+// ------------------------------------------------------------------------------------------
+// No-allocation variant: the scratch of dspark_markov_sample_block lives in this file-scope
+// device array.  Host code must not use the array's name as an address (it names a host-side
+// stand-in); the device address is looked up once per device with cudaGetSymbolAddress.
+// ------------------------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DSPARK_NOALLOC_SCRATCH_BYTES];
+static std::atomic<void*> g_noalloc_addr[64];
+
+extern "C" dspark_status dspark_markov_sample_block_noalloc(const dspark_sample_params* p, const void* base_logits,
+                                                           const void* W1, const void* W2, const int32_t* anchor,
+                                                           int32_t* tokens, float* draft_lse,
+                                                           float* draft_logit_at_tok, dspark_stream_t stream) {
+    const dspark_status st = validate_sample_params(p);
+    if (st != DSPARK_OK) return st;
+    const size_t need = sample_workspace_bytes(p);
+    if (need > DSPARK_NOALLOC_SCRATCH_BYTES) return DSPARK_ERR_UNSUPPORTED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DSPARK_ERR_CUDA;
+    void* scratch = g_noalloc_addr[dev].load();
+    if (!scratch) {  // first call on this device: this device is current
+        if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess || !scratch) return DSPARK_ERR_CUDA;
+        g_noalloc_addr[dev].store(scratch);
+    }
+    // Same kernel and launch as the workspace entry point; it zeroes the scratch header
+    // (status word and grid-wait counter) before the launch.
+    return dspark_markov_sample_block(p, base_logits, W1, W2, anchor, tokens, draft_lse, draft_logit_at_tok, scratch,
+                                      DSPARK_NOALLOC_SCRATCH_BYTES, stream);
 }
