@@ -63,6 +63,19 @@ __device__ __forceinline__ void lse_merge8(const float (&x)[8], float& m, float&
     m = mn;
 }
 
+// The same for 16 values (one rescale per 16).
+__device__ __forceinline__ void lse_merge16(const float (&x)[16], float& m, float& s) {
+    float gm = fmaxf(fmaxf(x[0], x[1]), x[2]);
+#pragma unroll
+    for (int e = 3; e < 16; e += 2) gm = fmaxf(fmaxf(gm, x[e]), e + 1 < 16 ? x[e + 1] : x[e]);
+    const float mn = fmaxf(m, gm * kLog2e);
+    if (mn == -CUDART_INF_F) return;
+    s = (m == -CUDART_INF_F) ? 0.f : s * ex2(m - mn);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) s += ex2(fmaf(x[e], kLog2e, -mn));
+    m = mn;
+}
+
 __device__ __forceinline__ float2 merge_pair(float2 a, float2 b) {
     const float m = fmaxf(a.x, b.x);
     if (m == -CUDART_INF_F) return make_float2(m, 0.f);
@@ -187,21 +200,45 @@ __global__ void __launch_bounds__(kTVThreads, 1) tv_kernel(TVArgs a) {
 }
 
 // ------------------------------------------------------------------------------------------
-// bf16 fast path: the block's segment of each row streams through a ring of shared-memory
-// slots filled by the bulk-copy engine (one slot = kCE ids of d and of t), so both passes read
-// shared memory and the copies of the next rows proceed while a row is being finished.
-// Chunk q of this block (row iteration q / nch, chunk q % nch) lives in slot q % kNS; slot
-// reuse is ordered by a block barrier after the slot's second pass.  Every wait is bounded;
-// after a timeout the block keeps pace with its cluster (the cluster barriers have no
-// timeout) but stops waiting on copies.
+// bf16 fast path, warp-specialised.  Each block owns a 1/cs segment of every row of its
+// cluster; the segment streams through a ring of kNS shared-memory slots (kCE ids of d and t
+// per slot) filled by the bulk-copy engine:
+//   - one producer warp issues the copies; a slot is refilled once all 16 consumer warps have
+//     released it (per-slot "empty" mbarrier, one arrival per warp);
+//   - 16 consumer warps wait on the slot's "full" mbarrier (transaction count), take the
+//     softmax statistics in pass 1 and the sum of minima in pass 2 -- both from shared memory;
+//   - the per-row statistics and sums go to the other blocks of the cluster by DSMEM stores
+//     followed by remote mbarrier arrivals (no cluster-wide barrier inside the row loop).
+// Every wait is bounded; a timeout raises a block-wide abort flag after which no thread waits
+// any more, while every consumer still executes the same sequence of named barriers, and the
+// whole cluster meets once more before exiting.
 // ------------------------------------------------------------------------------------------
-constexpr int kCE = 4096;  // ids per array per slot
-constexpr int kNS = 13;    // slots: 13 x 16 KB
-constexpr size_t kTmaSmem = (size_t)kNS * 2 * kCE * 2 + kNS * sizeof(uint64_t);
+constexpr int kCE = 4096;                       // ids per array per slot
+constexpr int kNS = 13;                         // ring slots (13 x 16 KB)
+constexpr int kWSCons = 512;                    // consumer threads (16 warps)
+constexpr int kWSWarps = kWSCons / 32;
+constexpr int kWSThreads = kWSCons + 32;        // + one producer warp
+constexpr int kMaxCS = 8;
+static_assert(kCE == 8 * kWSCons, "one 16-byte group of each array per consumer thread per slot");
+
+constexpr int kRB = 1;  // rows per batch: one statistics exchange and one sum exchange per batch
+
+struct TVWSmem {
+    uint16_t slots[kNS][2][kCE];
+    uint64_t full[kNS];
+    uint64_t empty[kNS];
+    uint64_t xbar_st[2];   // batch statistics from every block of the cluster (count = cs)
+    uint64_t xbar_sum[2];  // batch sums, at cluster rank 0 only (count = cs)
+    float4 xst[2][kMaxCS][kRB];
+    float xsum[2][kMaxCS][kRB];
+    float4 red4[kWSWarps][kRB];
+    float red1[kWSWarps][kRB];
+    int abort;
+};
+constexpr size_t kTmaSmem = sizeof(TVWSmem);
 
 struct TVTArgs {
-    long long rows;
-    int V, gamma, segsz, nch, nclusters, cs;
+    int rows, V, gamma, segsz, nch, nclusters, cs;
     const __nv_bfloat16* d;
     const __nv_bfloat16* t;
     const uint8_t* keep;
@@ -212,156 +249,213 @@ struct TVTArgs {
     uint64_t limit_ns;
 };
 
-__global__ void __launch_bounds__(kTVThreads, 1) tv_tma_kernel(TVTArgs a) {
+__device__ __forceinline__ void unpack_bf16x8(const uint4 w, float (&x)[8]) {
+    x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
+    x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z); x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
+}
+
+// Warp-wide combine of (max, sum 2^(x - max)) pairs: the max first, then one rescale per lane.
+__device__ __forceinline__ float2 warp_lse_pair(float m, float s) {
+    const float M = warp_max(m);
+    const float sc = (m == -CUDART_INF_F) ? 0.f : s * ex2(m - M);
+    return make_float2(M, warp_sum(sc));
+}
+
+__global__ void __launch_bounds__(kWSThreads, 1) tv_tma_kernel(TVTArgs a) {
     cg::cluster_group cluster = cg::this_cluster();
     const int crank = (int)cluster.block_rank();
     const int cid = blockIdx.x / a.cs;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    uint16_t* slots = reinterpret_cast<uint16_t*>(smem_raw);  // [kNS][2][kCE]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + (size_t)kNS * 2 * kCE * 2);
-    __shared__ float4 xch[2];
-    __shared__ float xsum[2];
-    __shared__ float4 red4[kTVWarps];
-    __shared__ float red1[kTVWarps];
-    __shared__ float2 s_norm;
-    __shared__ int s_ok;
+    TVWSmem& S = *reinterpret_cast<TVWSmem*>(smem_raw);
+    volatile int* abort = &S.abort;
     const int seg_lo = crank * a.segsz;
     const int seg_len = max(0, min(a.V - seg_lo, a.segsz));
-    const long long niters = (a.rows - cid + a.nclusters - 1) / a.nclusters;
-    const long long Q = niters * a.nch;
-    auto chunk_len = [&](int k) { return max(0, min(kCE, seg_len - k * kCE)); };
-    auto issue = [&](long long q) {  // thread 0 only
-        const int slot = (int)(q % kNS);
-        const long long it = q / a.nch;
-        const int k = (int)(q % a.nch);
-        const int len = chunk_len(k);
-        const long long row = cid + it * a.nclusters;
-        uint16_t* dst = slots + (size_t)slot * 2 * kCE;
-        if (len == 0) {  // keep the phase sequence: an arrival without bytes
-            mbar_arrive_expect_tx(&bars[slot], 0);
-            return;
-        }
-        mbar_arrive_expect_tx(&bars[slot], (uint32_t)(2 * len * 2));
-        const size_t off = (size_t)row * a.V + seg_lo + (size_t)k * kCE;
-        bulk_g2s(dst, a.d + off, (uint32_t)(len * 2), &bars[slot]);
-        bulk_g2s(dst + kCE, a.t + off, (uint32_t)(len * 2), &bars[slot]);
-    };
+    const int nch = a.nch, cs = a.cs;
+    const int nrows = (a.rows - cid + a.nclusters - 1) / a.nclusters;  // rows of this cluster
+    const int nbatch = (nrows + kRB - 1) / kRB;
+    const int Q = nrows * nch;  // chunks: row-major over this cluster's rows
     if (tid == 0) {
-        for (int i = 0; i < kNS; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < kNS; ++i) {
+            mbar_init(&S.full[i], 1);
+            mbar_init(&S.empty[i], kWSWarps);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&S.xbar_st[i], cs);
+            mbar_init(&S.xbar_sum[i], cs);
+        }
+        S.abort = 0;
         mbar_init_fence();
-        s_ok = 1;
     }
-    __syncthreads();
-    if (tid == 0)
-        for (long long q = 0; q < min(Q, (long long)kNS); ++q) issue(q);
+    cluster.sync();  // barriers of every block exist before any remote arrival
 
-    for (long long it = 0; it < niters; ++it) {
-        const int par = (int)(it & 1);
-        const long long row = cid + it * a.nclusters;
-        // ---- pass 1: softmax statistics of the segment of d and t
-        float md = -CUDART_INF_F, sd = 0.f, mt = -CUDART_INF_F, st = 0.f;
-        for (int k = 0; k < a.nch; ++k) {
-            const long long q = it * a.nch + k;
-            const int slot = (int)(q % kNS);
-            if (tid == 0 && s_ok) s_ok = mbar_wait_bounded(&bars[slot], (uint32_t)((q / kNS) & 1), &a.hdr->status, a.limit_ns);
-            __syncthreads();
-            if (s_ok) mbar_try_wait(&bars[slot], (uint32_t)((q / kNS) & 1));  // completed: acquire for this thread
-            const int len = chunk_len(k);
-            if (s_ok && 8 * tid < len) {
-                const uint16_t* sd_ = slots + (size_t)slot * 2 * kCE + 8 * tid;
-                const uint4 wd = *reinterpret_cast<const uint4*>(sd_);
-                const uint4 wt = *reinterpret_cast<const uint4*>(sd_ + kCE);
-                float xd[8], xt[8];
-                xd[0] = bf16_lo(wd.x); xd[1] = bf16_hi(wd.x); xd[2] = bf16_lo(wd.y); xd[3] = bf16_hi(wd.y);
-                xd[4] = bf16_lo(wd.z); xd[5] = bf16_hi(wd.z); xd[6] = bf16_lo(wd.w); xd[7] = bf16_hi(wd.w);
-                xt[0] = bf16_lo(wt.x); xt[1] = bf16_hi(wt.x); xt[2] = bf16_lo(wt.y); xt[3] = bf16_hi(wt.y);
-                xt[4] = bf16_lo(wt.z); xt[5] = bf16_hi(wt.z); xt[6] = bf16_lo(wt.w); xt[7] = bf16_hi(wt.w);
-                lse_merge8(xd, md, sd);
-                lse_merge8(xt, mt, st);
+    if (warp == kWSWarps) {
+        // ---------------- producer warp
+        if (lane == 0) {
+            int slot = 0, k = 0, ri = 0;
+            for (int q = 0; q < Q; ++q) {
+                // the (q / kNS)-th use of the slot waits for the release of its previous use
+                if (q >= kNS && !mbar_wait_or_abort(&S.empty[slot], (uint32_t)((q / kNS - 1) & 1), abort,
+                                                    &a.hdr->status, a.limit_ns, false))
+                    break;
+                const int len = max(0, min(kCE, seg_len - k * kCE));
+                mbar_arrive_expect_tx(&S.full[slot], (uint32_t)(4 * len));
+                if (len > 0) {
+                    const size_t off = (size_t)(cid + ri * a.nclusters) * a.V + seg_lo + (size_t)k * kCE;
+                    bulk_g2s(&S.slots[slot][0][0], a.d + off, (uint32_t)(2 * len), &S.full[slot]);
+                    bulk_g2s(&S.slots[slot][1][0], a.t + off, (uint32_t)(2 * len), &S.full[slot]);
+                }
+                if (++k == nch) {
+                    k = 0;
+                    ++ri;
+                }
+                if (++slot == kNS) slot = 0;
             }
         }
-        {
-            float2 pd = make_float2(md, sd), pt = make_float2(mt, st);
+        __syncwarp();
+    } else {
+        // ---------------- 16 consumer warps
+        const int my0 = 8 * tid;  // this thread's ids in a slot: my0 .. my0 + 7 (conflict-free 16-byte reads)
+        int slot = 0;             // slot of the next chunk to read in pass 1
+        uint32_t phase = 0;
+        for (int b = 0; b < nbatch; ++b) {
+            const int par = b & 1;
+            const int r0 = b * kRB, nr = min(kRB, nrows - r0);
+            const int slot_b = slot;  // first slot of the batch, for pass 2
+            // ---- pass 1 over the batch's rows
+            float md[kRB], sd[kRB], mt[kRB], st[kRB];
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                pd = merge_pair(pd, make_float2(__shfl_xor_sync(0xffffffffu, pd.x, o), __shfl_xor_sync(0xffffffffu, pd.y, o)));
-                pt = merge_pair(pt, make_float2(__shfl_xor_sync(0xffffffffu, pt.x, o), __shfl_xor_sync(0xffffffffu, pt.y, o)));
+            for (int r = 0; r < kRB; ++r) {
+                md[r] = mt[r] = -CUDART_INF_F;
+                sd[r] = st[r] = 0.f;
             }
-            if (lane == 0) red4[warp] = make_float4(pd.x, pd.y, pt.x, pt.y);
-            __syncthreads();
+#pragma unroll
+            for (int r = 0; r < kRB; ++r) {
+                if (r >= nr) break;
+                int len = seg_len;
+                for (int k = 0; k < nch; ++k) {
+                    const bool ok = mbar_wait_or_abort(&S.full[slot], phase, abort, &a.hdr->status, a.limit_ns, false);
+                    if (ok && my0 < len) {
+                        float xd[8], xt[8];
+                        unpack_bf16x8(*reinterpret_cast<const uint4*>(&S.slots[slot][0][my0]), xd);
+                        unpack_bf16x8(*reinterpret_cast<const uint4*>(&S.slots[slot][1][my0]), xt);
+                        lse_merge8(xd, md[r], sd[r]);
+                        lse_merge8(xt, mt[r], st[r]);
+                    }
+                    len -= kCE;
+                    if (++slot == kNS) {
+                        slot = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // ---- batch statistics -> every block of the cluster
+#pragma unroll
+            for (int r = 0; r < kRB; ++r) {
+                const float2 wd = warp_lse_pair(md[r], sd[r]);
+                const float2 wt = warp_lse_pair(mt[r], st[r]);
+                if (lane == 0) S.red4[warp][r] = make_float4(wd.x, wd.y, wt.x, wt.y);
+            }
+            named_barrier(1, kWSCons);
             if (warp == 0) {
-                float4 q = lane < kTVWarps ? red4[lane] : make_float4(-CUDART_INF_F, 0.f, -CUDART_INF_F, 0.f);
-                float2 qd = make_float2(q.x, q.y), qt = make_float2(q.z, q.w);
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    qd = merge_pair(qd, make_float2(__shfl_xor_sync(0xffffffffu, qd.x, o), __shfl_xor_sync(0xffffffffu, qd.y, o)));
-                    qt = merge_pair(qt, make_float2(__shfl_xor_sync(0xffffffffu, qt.x, o), __shfl_xor_sync(0xffffffffu, qt.y, o)));
+                for (int r = 0; r < kRB; ++r) {
+                    const float4 q = lane < kWSWarps ? S.red4[lane][r] : make_float4(-CUDART_INF_F, 0.f, -CUDART_INF_F, 0.f);
+                    const float2 cd = warp_lse_pair(q.x, q.y);
+                    const float2 ct = warp_lse_pair(q.z, q.w);
+                    if (lane < cs) st_cluster_f32x4(map_to_rank(&S.xst[par][crank][r], lane), make_float4(cd.x, cd.y, ct.x, ct.y));
                 }
-                if (lane == 0) xch[par] = make_float4(qd.x, qd.y, qt.x, qt.y);
+                if (lane < cs) mbar_arrive_remote(map_to_rank(&S.xbar_st[par], lane));
             }
-        }
-        cluster.sync();
-        if (tid == 0) {
-            float2 gd = make_float2(-CUDART_INF_F, 0.f), gt = make_float2(-CUDART_INF_F, 0.f);
-            for (int rnk = 0; rnk < a.cs; ++rnk) {
-                const float4 q = cluster.map_shared_rank(&xch[par], rnk)[0];
-                gd = merge_pair(gd, make_float2(q.x, q.y));
-                gt = merge_pair(gt, make_float2(q.z, q.w));
-            }
-            s_norm = make_float2(gd.x + lg2(gd.y), gt.x + lg2(gt.y));
-        }
-        __syncthreads();
-        const float Ld2 = s_norm.x, Lt2 = s_norm.y;
-        // ---- pass 2: sum of min(p, q) over the segment, then the slot is refilled
-        float acc = 0.f;
-        for (int k = 0; k < a.nch; ++k) {
-            const long long q = it * a.nch + k;
-            const int slot = (int)(q % kNS);
-            const int len = chunk_len(k);
-            if (s_ok && 8 * tid < len) {
-                const uint16_t* sd_ = slots + (size_t)slot * 2 * kCE + 8 * tid;
-                const uint4 wd = *reinterpret_cast<const uint4*>(sd_);
-                const uint4 wt = *reinterpret_cast<const uint4*>(sd_ + kCE);
-                const uint32_t dw[4] = {wd.x, wd.y, wd.z, wd.w}, tw[4] = {wt.x, wt.y, wt.z, wt.w};
+            mbar_wait_or_abort(&S.xbar_st[par], (uint32_t)((b >> 1) & 1), abort, &a.hdr->status, a.limit_ns, true);
+            float Ld2[kRB], Lt2[kRB];
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    acc += ex2(fminf(fmaf(bf16_lo(dw[h]), kLog2e, -Ld2), fmaf(bf16_lo(tw[h]), kLog2e, -Lt2)));
-                    acc += ex2(fminf(fmaf(bf16_hi(dw[h]), kLog2e, -Ld2), fmaf(bf16_hi(tw[h]), kLog2e, -Lt2)));
+            for (int r = 0; r < kRB; ++r) {
+                float Md = -CUDART_INF_F, Mt = -CUDART_INF_F;
+                for (int c = 0; c < cs; ++c) {
+                    Md = fmaxf(Md, S.xst[par][c][r].x);
+                    Mt = fmaxf(Mt, S.xst[par][c][r].z);
+                }
+                float Sd = 0.f, St = 0.f;
+                for (int c = 0; c < cs; ++c) {
+                    const float4 q = S.xst[par][c][r];
+                    if (q.x != -CUDART_INF_F) Sd += q.y * ex2(q.x - Md);
+                    if (q.z != -CUDART_INF_F) St += q.w * ex2(q.z - Mt);
+                }
+                Ld2[r] = Md + lg2(Sd);
+                Lt2[r] = Mt + lg2(St);
+            }
+            // ---- pass 2: sum of min(p, q); each warp releases each slot after reading it
+            float acc[kRB];
+            {
+                int slot2 = slot_b;
+                const bool live = !*abort;
+#pragma unroll
+                for (int r = 0; r < kRB; ++r) {
+                    acc[r] = 0.f;
+                    if (r >= nr) break;
+                    int len2 = seg_len;
+                    for (int k = 0; k < nch; ++k) {
+                        if (live && my0 < len2) {
+                            const uint4 wd = *reinterpret_cast<const uint4*>(&S.slots[slot2][0][my0]);
+                            const uint4 wt = *reinterpret_cast<const uint4*>(&S.slots[slot2][1][my0]);
+                            const uint32_t dw[4] = {wd.x, wd.y, wd.z, wd.w}, tw[4] = {wt.x, wt.y, wt.z, wt.w};
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                acc[r] += ex2(fminf(fmaf(bf16_lo(dw[h]), kLog2e, -Ld2[r]), fmaf(bf16_lo(tw[h]), kLog2e, -Lt2[r])));
+                                acc[r] += ex2(fminf(fmaf(bf16_hi(dw[h]), kLog2e, -Ld2[r]), fmaf(bf16_hi(tw[h]), kLog2e, -Lt2[r])));
+                            }
+                        }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_local(&S.empty[slot2]);
+                        len2 -= kCE;
+                        if (++slot2 == kNS) slot2 = 0;
+                    }
                 }
             }
-            __syncthreads();  // every thread has read the slot: the copy engine may overwrite it
-            if (tid == 0 && q + kNS < Q) issue(q + kNS);
-        }
-        acc = warp_sum(acc);
-        if (lane == 0) red1[warp] = acc;
-        __syncthreads();
-        if (warp == 0) {
-            float q = lane < kTVWarps ? red1[lane] : 0.f;
-            q = warp_sum(q);
-            if (lane == 0) xsum[par] = q;
-        }
-        cluster.sync();
-        if (crank == 0 && tid == 0) {
-            float tot = 0.f;
-            for (int rnk = 0; rnk < a.cs; ++rnk) tot += cluster.map_shared_rank(&xsum[par], rnk)[0];
-            a.acc[row] = fminf(fmaxf(tot, 0.f), 1.f);
-            const long long blk = row / a.gamma;
-            const int i = (int)(row % a.gamma);
-            float mval = a.keep[blk] ? 1.f : 0.f;
-            if (a.posv)
-                for (int k = 0; k <= i; ++k) mval = a.posv[blk * a.gamma + k] ? mval : 0.f;
-            a.mask[row] = mval;
+#pragma unroll
+            for (int r = 0; r < kRB; ++r) {
+                const float w = warp_sum(acc[r]);
+                if (lane == 0) S.red1[warp][r] = w;
+            }
+            named_barrier(2, kWSCons);
+            if (warp == 0) {
+#pragma unroll
+                for (int r = 0; r < kRB; ++r) {
+                    const float q = warp_sum(lane < kWSWarps ? S.red1[lane][r] : 0.f);
+                    if (lane == 0) {
+                        const uint32_t dst = map_to_rank(&S.xsum[par][crank][r], 0);
+                        asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst), "f"(q) : "memory");
+                    }
+                }
+                if (lane == 0) mbar_arrive_remote(map_to_rank(&S.xbar_sum[par], 0));
+            }
+            if (crank == 0 && tid == 0) {
+                mbar_wait_or_abort(&S.xbar_sum[par], (uint32_t)((b >> 1) & 1), abort, &a.hdr->status, a.limit_ns, true);
+                for (int r = 0; r < nr; ++r) {
+                    float tot = 0.f;
+                    for (int c = 0; c < cs; ++c) tot += S.xsum[par][c][r];
+                    const int row = cid + (r0 + r) * a.nclusters;
+                    a.acc[row] = fminf(fmaxf(tot, 0.f), 1.f);
+                    const int blk = row / a.gamma, i = row % a.gamma;
+                    float mval = a.keep[blk] ? 1.f : 0.f;
+                    if (a.posv)
+                        for (int kk = 0; kk <= i; ++kk) mval = a.posv[(size_t)blk * a.gamma + kk] ? mval : 0.f;
+                    a.mask[row] = mval;
+                }
+            }
         }
     }
-    // after a timeout, copies may still be in flight: wait for them (bounded) before leaving
-    if (tid == 0 && !s_ok) {
-        for (long long q = max(0LL, Q - kNS); q < Q; ++q) {
-            const int slot = (int)(q % kNS);
-            mbar_wait_bounded(&bars[slot], (uint32_t)((q / kNS) & 1), &a.hdr->status, a.limit_ns);
+    // Copies still in flight after an abort: wait for them (bounded) before the block can leave.
+    if (tid == 0 && *abort) {
+        const uint64_t t0 = global_ns();
+        for (int q = max(0, Q - kNS); q < Q; ++q) {
+            const int sl = q % kNS;
+            while (!mbar_try_wait(&S.full[sl], (uint32_t)((q / kNS) & 1)) && global_ns() - t0 < a.limit_ns) {
+            }
         }
     }
-    cluster.sync();
+    cluster.sync();  // no block leaves while a peer may still write into its shared memory
 }
 
 // tau[s,a] = 1 + sum_i prod_{k<=i} acc * mask (one thread per block of gamma positions).
@@ -406,35 +500,53 @@ extern "C" dspark_status dspark_accept_rate_tv(int S, int A, int gamma, int V, i
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const bool tma = dtype == DSPARK_BF16 && V % 8 == 0 && (uintptr_t)draft_logits % 16 == 0 &&
-                     (uintptr_t)target_logits % 16 == 0 && V >= 4 * 8;
+                     (uintptr_t)target_logits % 16 == 0 && V >= 16;
+    int best_cs = 0, best_n = 0;
     if (tma) {
-        // cluster of 4 (8 when it packs the SMs as well): each block owns a quarter (eighth) row
         static bool attr_set = false;
         if (!attr_set) {
             if (cudaFuncSetAttribute((const void*)tv_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kTmaSmem) != cudaSuccess)
                 return DSPARK_ERR_CUDA;
-            cudaFuncSetAttribute((const void*)tv_tma_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
             attr_set = true;
         }
+        if (rows > (long long)INT32_MAX / 8) return DSPARK_ERR_UNSUPPORTED;
+        cfg.blockDim = dim3(kWSThreads);
         cfg.dynamicSmemBytes = kTmaSmem;
-        int cs = 4, nclusters = 0;
-        attr[0].val.clusterDim.x = cs;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(cs);
-        if (cudaOccupancyMaxActiveClusters(&nclusters, (const void*)tv_tma_kernel, &cfg) != cudaSuccess ||
-            nclusters < 1)
-            return DSPARK_ERR_CUDA;
+        // cluster of 8 when it keeps at least as many SMs busy as clusters of 4
+        // A batch of kRB row segments must fit the ring with slots to spare for the next batch's
+        // copies, so only cluster sizes with at most (kNS - 3) / kRB chunks per segment qualify.
+        for (int cs = kMaxCS; cs >= 1; cs >>= 1) {
+            if (V < 8 * cs) continue;
+            const int seg = (int)align_up((size_t)((V + cs - 1) / cs), 8);
+            if (kRB * ((seg + kCE - 1) / kCE) > kNS - 3) continue;
+            attr[0].val.clusterDim.x = cs;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(cs);
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, (const void*)tv_tma_kernel, &cfg) != cudaSuccess) {
+                cudaGetLastError();
+                continue;
+            }
+            if (n * cs > best_n * best_cs) {
+                best_cs = cs;
+                best_n = n;
+            }
+        }
+    }
+    if (tma && best_cs > 0) {  // (no cluster size fits the ring for very large vocabularies: streaming kernel)
+        int nclusters = best_n;
         if ((long long)nclusters > rows) nclusters = (int)rows;
+        attr[0].val.clusterDim.x = best_cs;
         TVTArgs a;
-        a.rows = rows;
+        a.rows = (int)rows;
         a.V = V;
         a.gamma = gamma;
-        a.segsz = (int)align_up((size_t)((V + cs - 1) / cs), 8);
+        a.segsz = (int)align_up((size_t)((V + best_cs - 1) / best_cs), 8);
         a.nch = (a.segsz + kCE - 1) / kCE;
         a.nclusters = nclusters;
-        a.cs = cs;
+        a.cs = best_cs;
         a.d = static_cast<const __nv_bfloat16*>(draft_logits);
         a.t = static_cast<const __nv_bfloat16*>(target_logits);
         a.keep = block_keep;
@@ -443,10 +555,11 @@ extern "C" dspark_status dspark_accept_rate_tv(int S, int A, int gamma, int V, i
         a.mask = eval_mask;
         a.hdr = static_cast<WsHeader*>(workspace);
         a.limit_ns = wait_limit_ns();
-        cfg.gridDim = dim3(nclusters * cs);
+        cfg.gridDim = dim3(nclusters * best_cs);
         if (cudaLaunchKernelEx(&cfg, tv_tma_kernel, a) != cudaSuccess) return DSPARK_ERR_CUDA;
     } else {
         void (*fn)(TVArgs) = dtype == DSPARK_BF16 ? tv_kernel<__nv_bfloat16> : tv_kernel<float>;
+        cfg.blockDim = dim3(kTVThreads);
         cfg.dynamicSmemBytes = 0;
         int cs = 4;
         int nclusters = 0;

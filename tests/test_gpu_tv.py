@@ -40,6 +40,11 @@ def test_small(V, dtype):
     check(W.make_tv_workload(2, 5, 3, V, device="cuda", dtype=dtype, data_seed=V, truncate=True, drop=0.3))
 
 
+def test_vocabulary_beyond_the_copy_ring():
+    # 262144 ids: a row segment no longer fits the shared-memory ring; the streaming path runs
+    check(W.make_tv_workload(1, 2, 2, 262144, device="cuda", data_seed=5))
+
+
 def test_identical_rows_give_one():
     tv = W.make_tv_workload(1, 3, 2, 5000, device="cuda")
     t = tv.tensors
