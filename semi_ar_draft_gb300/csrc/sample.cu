@@ -26,6 +26,8 @@
 namespace dspark {
 namespace {
 
+constexpr int kMaxStagedTiles = 160;  // tiles a request's log-masses are reduced over by one warp
+
 struct SampleArgs {
     int B, gamma, V, r, nt, G;
     int greedy;
@@ -40,7 +42,9 @@ struct SampleArgs {
     float* zat;
     WsHeader* hdr;
     int32_t* cur_tok;
-    float4* part;  // [2][B][nt] tile records, by step parity
+    float4* part;  // [3][B][nt] tile records, by step mod 2 (general kernel) or mod 3 (staged kernel)
+    unsigned long long* slots;  // [gamma][B] packed (key, id) maxima of the staged kernel; zeroed per call
+    int w1_l2;                  // staged kernel: pull W1 rows of each tile into L2 at the start
     uint64_t limit_ns;
     int redundant;  // every block reduces every request (one grid-wide wait per step)
     int w2_smem;
@@ -84,7 +88,7 @@ __device__ void prefetch_rows(const SampleArgs& a, int tile, int row0, int step)
 template <typename TL, int KS, typename TW, bool GREEDY>
 __global__ void __launch_bounds__(kThreads, 1) sample_kernel(SampleArgs a) {
     constexpr bool kMMA = KS > 0;
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+    extern __shared__ __align__(128) unsigned char smem_raw[];
     float* xbuf = reinterpret_cast<float*>(smem_raw);                  // [kRows][kXRow]: z
     float2* cstat = reinterpret_cast<float2*>(xbuf + kRows * kXRow);   // [kRows][kChunks]
     RowBlock* rb = reinterpret_cast<RowBlock*>(cstat + kRows * kChunks);
@@ -238,6 +242,268 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(SampleArgs a) {
     }
 }
 
+using KernelFnS = void (*)(SampleArgs);
+// ------------------------------------------------------------------------------------------
+// Staged variant (bf16 logits, tensor-core bias, one tile per block).
+//   - The base rows of each row block and the W1 rows of its previous tokens are copied into
+//     shared memory by the bulk-copy engine one row block ahead (double buffer; the base rows of
+//     a step's first row block are requested while the previous step finishes, its W1 rows as
+//     soon as the tokens are known).  z is never stored: the finalize recomputes the one chunk
+//     the draw selects with the producer's MMA sequence.
+//   - Exchange: each tile's record is folded into one 64-bit word per request and step with an
+//     atomic max (order-preserving key bits above the complemented candidate id: the highest
+//     key wins, the lowest id on ties); after the grid-wide wait every block reads the B words.
+//     The owner of request j (block j mod G) writes the token, and later, while it waits at
+//     the next step's grid barrier, LSE(z/T) over the tiles' log-masses and z at the token
+//     (records in three rotating buffers, so none is rewritten before its owner read it).
+// ------------------------------------------------------------------------------------------
+struct StagedLayout {
+    size_t stage, w1s, cstat, prev, rnd, bars, w2s, total;
+};
+
+__host__ __device__ inline StagedLayout staged_layout(int B, int r, bool w2_smem) {
+    StagedLayout L;
+    size_t o = 0;
+    L.stage = o;
+    o += sizeof(uint16_t) * 2 * kRows * kStageRow;
+    L.w1s = o;
+    o += align_up(sizeof(uint16_t) * 2 * kRows * (size_t)(r + 8), 16);
+    L.cstat = o;
+    o += sizeof(float2) * kRows * kChunks;
+    L.prev = o;
+    o += align_up(sizeof(int) * (size_t)B, 16);
+    L.rnd = o;
+    o += sizeof(float4) * (size_t)B;
+    L.bars = o;
+    o += 16;
+    L.w2s = o;
+    if (w2_smem) o += (size_t)kTS * r * 2;
+    L.total = o;
+    return L;
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void red_max_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Order-preserving 32-bit image of a float (-0 taken as +0) above the complemented id.
+__device__ __forceinline__ unsigned long long pack_key(float key, int cand) {
+    const uint32_t b = __float_as_uint(__fadd_rn(key, 0.f));
+    const uint32_t o = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    return ((unsigned long long)o << 32) | (uint32_t)(~cand);
+}
+__device__ __forceinline__ float unpack_key(unsigned long long w) {
+    const uint32_t o = (uint32_t)(w >> 32);
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+
+// Base rows of row block `cnt` (step cnt / nrb) over this block's tile (warp 0): the bytes are
+// announced without an arrival; issue_w1() adds the arrival.
+__device__ __forceinline__ void issue_base(const SampleArgs& a, int cnt, int nrb, uint16_t* dst, uint64_t* bar) {
+    const int lane = threadIdx.x & 31;
+    const int step = cnt / nrb, row0 = (cnt % nrb) * kRows;
+    const int tile0 = blockIdx.x * kTS;
+    const int nvalid = min(kTS, a.V - tile0);
+    const int nrows = min(kRows, a.B - row0);
+    if (lane == 0) mbar_expect_tx(bar, (uint32_t)(nrows * nvalid * 2));
+    __syncwarp();
+    if (lane < nrows) {
+        const __nv_bfloat16* src =
+            reinterpret_cast<const __nv_bfloat16*>(a.base) + ((size_t)(row0 + lane) * a.gamma + step) * (size_t)a.V + tile0;
+        bulk_g2s(dst + (size_t)lane * kStageRow, src, (uint32_t)(nvalid * 2), bar);
+    }
+}
+
+// W1 rows of the previous tokens of rows row0 .. row0 + 15 (warp 0; rows past B repeat row0).
+__device__ __forceinline__ void issue_w1(const SampleArgs& a, int row0, const int* prev, uint16_t* dst, uint64_t* bar) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t rowb = (uint32_t)a.r * 2u;
+    if (lane == 0) mbar_arrive_expect_tx(bar, kRows * rowb);
+    __syncwarp();
+    if (lane < kRows) {
+        const int j = row0 + lane;
+        const int tok = prev[j < a.B ? j : row0];
+        bulk_g2s(dst + (size_t)lane * (a.r + 8), reinterpret_cast<const uint16_t*>(a.W1) + (size_t)tok * a.r, rowb, bar);
+    }
+}
+
+// LSE(z/T) and z at the token of step s for the requests this block owns (a warp per request).
+__device__ void owner_lse(const SampleArgs& a, int s, const int* prev) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float4* part = a.part + (size_t)(s % 3) * a.B * a.nt;
+    for (int k = warp;; k += kWarps) {
+        const int j = blockIdx.x + a.G * k;
+        if (j >= a.B) break;
+        const float4* rec = part + (size_t)j * a.nt;
+        float y[kMaxStagedTiles / 32];
+        float m = -CUDART_INF_F;
+#pragma unroll
+        for (int i = 0; i < kMaxStagedTiles / 32; ++i) {
+            const int t = lane + 32 * i;
+            y[i] = t < a.nt ? __ldcg(&rec[t].y) : -CUDART_INF_F;
+            m = fmaxf(m, y[i]);
+        }
+        m = warp_max(m);
+        float lse = -CUDART_INF_F;
+        if (m != -CUDART_INF_F) {
+            const float m2 = m * kLog2e;
+            float sum = 0.f;
+#pragma unroll
+            for (int i = 0; i < kMaxStagedTiles / 32; ++i) sum += ex2(fmaf(y[i], kLog2e, -m2));
+            sum = warp_sum(sum);
+            lse = (m2 + lg2(sum)) * kLn2;
+        }
+        if (lane == 0) {
+            const size_t o = (size_t)j * a.gamma + s;
+            a.draft_lse[o] = lse;
+            a.zat[o] = __ldcg(&rec[prev[j] / kTS].w);
+        }
+    }
+}
+
+template <int KS, bool GREEDY>
+__global__ void __launch_bounds__(kThreads, 1) sample_staged_kernel(SampleArgs a) {
+    constexpr int r = 16 * KS, w1st = r + 8;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const StagedLayout L = staged_layout(a.B, r, a.w2_smem);
+    uint16_t* stage = reinterpret_cast<uint16_t*>(smem_raw + L.stage);  // [2][kRows][kStageRow] bf16 bits
+    uint16_t* w1s = reinterpret_cast<uint16_t*>(smem_raw + L.w1s);      // [2][kRows][w1st]
+    float2* cstat = reinterpret_cast<float2*>(smem_raw + L.cstat);      // [kRows][kChunks]
+    int* prev = reinterpret_cast<int*>(smem_raw + L.prev);              // [B] previous tokens
+    float4* rnd = reinterpret_cast<float4*>(smem_raw + L.rnd);          // [B] (u1, u2, ln E)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + L.bars);
+    uint4* w2s = reinterpret_cast<uint4*>(smem_raw + L.w2s);
+    __shared__ int s_ok;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tile = blockIdx.x, tile0 = tile * kTS;
+    const bool full = tile0 + kTS <= a.V;
+    const int nrb = (a.B + kRows - 1) / kRows;
+    const int total = a.gamma * nrb;
+    const uint16_t* W2 = reinterpret_cast<const uint16_t*>(a.W2);
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        mbar_init_fence();
+    }
+    for (int j = tid; j < a.B; j += kThreads) {
+        int p = a.anchor[j];
+        if (p < 0 || p >= a.V) {
+            record_status(&a.hdr->status, DSPARK_ERR_TOKEN_RANGE);
+            p = min(max(p, 0), a.V - 1);
+        }
+        prev[j] = p;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        issue_base(a, 0, nrb, stage, &bars[0]);
+        issue_w1(a, 0, prev, w1s, &bars[0]);
+    } else if (warp == 1 && a.w1_l2) {  // W1 rows of this tile into L2: later gathers hit there
+        const uint32_t bytes = (uint32_t)min(kTS, a.V - tile0) * (uint32_t)r * 2u;
+        const unsigned char* w1 = reinterpret_cast<const unsigned char*>(a.W1) + (size_t)tile0 * r * 2;
+        for (uint32_t off = (uint32_t)lane * 4096u; off < bytes; off += 32u * 4096u)
+            prefetch_l2(w1 + off, min(4096u, bytes - off));
+    }
+    if (a.w2_smem) stage_w2_tile<KS>(W2, tile0, a.V, w2s);
+    if (!GREEDY) step_randoms(a, 0, rnd);
+
+    uint32_t target = 0;
+    int cnt = 0;
+    for (int step = 0; step < a.gamma; ++step) {
+        float4* part = a.part + (size_t)(step % 3) * a.B * a.nt;
+        unsigned long long* slot = a.slots + (size_t)step * a.B;
+        for (int rbi = 0; rbi < nrb; ++rbi, ++cnt) {
+            const int buf = cnt & 1, row0 = rbi * kRows;
+            const uint32_t par = (uint32_t)((cnt >> 1) & 1);
+            if (tid == 0) s_ok = mbar_wait_bounded(&bars[buf], par, &a.hdr->status, a.limit_ns);
+            __syncthreads();
+            if (!s_ok) return;  // the copy engine did not deliver in time (status recorded); nothing else in flight
+            mbar_try_wait(&bars[buf], par);  // completed: acquire for this thread
+            if (warp == 0 && cnt + 1 < total) {  // the other buffer was released at the end of the last row block
+                uint64_t* nbar = &bars[buf ^ 1];
+                issue_base(a, cnt + 1, nrb, stage + (size_t)(buf ^ 1) * kRows * kStageRow, nbar);
+                if (rbi + 1 < nrb) issue_w1(a, row0 + kRows, prev, w1s + (size_t)(buf ^ 1) * kRows * w1st, nbar);
+            }
+            const uint16_t* sbuf = stage + (size_t)buf * kRows * kStageRow;
+            const uint16_t* wbuf = w1s + (size_t)buf * kRows * w1st;
+            if (a.w2_smem) {
+                if (full) produce_staged<KS, GREEDY, true, true>(sbuf, wbuf, w1st, W2, w2s, a.V, tile, cstat, a.scale2);
+                else produce_staged<KS, GREEDY, true, false>(sbuf, wbuf, w1st, W2, w2s, a.V, tile, cstat, a.scale2);
+            } else {
+                if (full) produce_staged<KS, GREEDY, false, true>(sbuf, wbuf, w1st, W2, nullptr, a.V, tile, cstat, a.scale2);
+                else produce_staged<KS, GREEDY, false, false>(sbuf, wbuf, w1st, W2, nullptr, a.V, tile, cstat, a.scale2);
+            }
+            __syncthreads();
+            for (int rl = warp; rl < kRows; rl += kWarps) {
+                const int j = row0 + rl;
+                if (j >= a.B) continue;
+                const float4 q = GREEDY ? make_float4(0.f, 0.f, 0.f, 0.f) : rnd[j];
+                float4 rec;
+                if (a.w2_smem)
+                    rec = finalize_staged<KS, GREEDY, true>(sbuf + rl * kStageRow, cstat[rl * kChunks + lane], tile,
+                                                            a.V, a.scale2, q.x, q.y, q.z, wbuf + rl * w1st, W2, w2s);
+                else
+                    rec = finalize_staged<KS, GREEDY, false>(sbuf + rl * kStageRow, cstat[rl * kChunks + lane], tile,
+                                                             a.V, a.scale2, q.x, q.y, q.z, wbuf + rl * w1st, W2,
+                                                             nullptr);
+                if (lane == 0) {
+                    if (!GREEDY) part[(size_t)j * a.nt + tile] = rec;
+                    red_max_u64(slot + j, pack_key(rec.x, __float_as_int(rec.z)));
+                }
+            }
+            __syncthreads();
+        }
+        target += (uint32_t)a.G;
+        grid_arrive(a.hdr);
+        if (!GREEDY && step >= 1) owner_lse(a, step - 1, prev);
+        if (!GREEDY && step + 1 < a.gamma) step_randoms(a, step + 1, rnd);
+        if (!grid_wait_arrived(a.hdr, target, a.limit_ns)) {
+            // the next step's base rows may be in flight: arrive for them and wait (bounded)
+            if (tid == 0 && cnt < total) {
+                mbar_arrive_local(&bars[cnt & 1]);
+                mbar_wait_bounded(&bars[cnt & 1], (uint32_t)((cnt >> 1) & 1), &a.hdr->status, a.limit_ns);
+            }
+            return;
+        }
+        for (int j = tid; j < a.B; j += kThreads) {
+            const unsigned long long w = __ldcg(slot + j);
+            const int cand = ~(int)(uint32_t)w;
+            int p = cand;
+            if (p < 0 || p >= a.V) {  // a row whose tiles all had no mass
+                record_status(&a.hdr->status, DSPARK_ERR_TOKEN_RANGE);
+                p = min(max(p, 0), a.V - 1);
+            }
+            prev[j] = p;
+            if (j % a.G == (int)blockIdx.x) {
+                const size_t o = (size_t)j * a.gamma + step;
+                a.tokens[o] = cand;
+                if (GREEDY) {
+                    a.draft_lse[o] = CUDART_NAN_F;
+                    a.zat[o] = unpack_key(w);
+                }
+            }
+        }
+        __syncthreads();
+        if (warp == 0 && cnt < total) issue_w1(a, 0, prev, w1s + (size_t)(cnt & 1) * kRows * w1st, &bars[cnt & 1]);
+    }
+    if (!GREEDY) owner_lse(a, a.gamma - 1, prev);
+}
+
+template <bool G>
+KernelFnS pick_staged(int r) {
+    switch (r) {
+        case 16: return sample_staged_kernel<1, G>;
+        case 32: return sample_staged_kernel<2, G>;
+        case 64: return sample_staged_kernel<4, G>;
+        case 128: return sample_staged_kernel<8, G>;
+        case 256: return sample_staged_kernel<16, G>;
+        default: return nullptr;
+    }
+}
+
 using KernelFn = void (*)(SampleArgs);
 
 template <typename TL, bool G>
@@ -282,10 +548,14 @@ dspark_status validate_sample_params(const dspark_sample_params* p) {
     return DSPARK_OK;
 }
 
+size_t sample_slot_bytes(const dspark_sample_params* p) {
+    return align_up(sizeof(unsigned long long) * (size_t)p->B * p->gamma, 256);
+}
+
 size_t sample_workspace_bytes(const dspark_sample_params* p) {
     const size_t nt = (size_t)(p->V + kTS - 1) / kTS;
-    return kHeaderBytes + align_up(sizeof(int32_t) * (size_t)p->B, 256) +
-           align_up(2 * sizeof(float4) * (size_t)p->B * nt, 256);
+    return kHeaderBytes + sample_slot_bytes(p) + align_up(sizeof(int32_t) * (size_t)p->B, 256) +
+           align_up(3 * sizeof(float4) * (size_t)p->B * nt, 256);
 }
 
 }  // namespace dspark
@@ -312,12 +582,25 @@ extern "C" dspark_status dspark_markov_sample_block(const dspark_sample_params* 
     const int nt = (p->V + kTS - 1) / kTS;
     int sms = 0;
     if (device_sm_count(&sms) != cudaSuccess) return DSPARK_ERR_CUDA;
-    KernelFn fn = pick_kernel(p, mma);
+    const size_t esz = p->logits_dtype == DSPARK_BF16 ? 2 : 4;
+    const bool vec_ok = ((uintptr_t)base_logits % 16 == 0) && (((size_t)p->V * esz) % 16 == 0);
+    // staged path: bf16 logits, tensor-core bias, one tile per block (one block per SM)
+    bool staged = mma && p->logits_dtype == DSPARK_BF16 && vec_ok && ((uintptr_t)W1 % 16 == 0) && nt <= sms &&
+                  nt <= kMaxStagedTiles;
+    bool w2_staged = (size_t)kTS * p->r * 2 <= 128 * 1024;
+    if (staged && staged_layout(p->B, p->r, w2_staged).total > kMaxSmem) w2_staged = false;
+    if (staged && staged_layout(p->B, p->r, false).total > kMaxSmem) staged = false;
+    KernelFn fn = staged ? (p->temperature == 0.f ? pick_staged<true>(p->r) : pick_staged<false>(p->r))
+                         : pick_kernel(p, mma);
     bool w2_smem = mma && (size_t)kTS * p->r * 2 <= 128 * 1024 && nt <= sms;
     size_t smem = sample_smem_bytes(p->B, p->r, mma, w2_smem);
     if (smem > kMaxSmem && w2_smem) {
         w2_smem = false;
         smem = sample_smem_bytes(p->B, p->r, mma, false);
+    }
+    if (staged) {
+        w2_smem = w2_staged;
+        smem = staged_layout(p->B, p->r, w2_smem).total;
     }
     if (smem > kMaxSmem) return DSPARK_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
@@ -328,6 +611,7 @@ extern "C" dspark_status dspark_markov_sample_block(const dspark_sample_params* 
         return DSPARK_ERR_CUDA;
     const int G = std::min(nt, sms * per_sm);
     if (G < nt) w2_smem = false;  // a block owning several tiles cannot keep one tile's W2
+    if (staged && G < nt) return DSPARK_ERR_CUDA;  // (cannot happen: nt <= SMs and one block per SM)
 
     SampleArgs a;
     a.B = p->B;
@@ -348,16 +632,19 @@ extern "C" dspark_status dspark_markov_sample_block(const dspark_sample_params* 
     a.zat = draft_logit_at_tok;
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     a.hdr = reinterpret_cast<WsHeader*>(ws);
-    a.cur_tok = reinterpret_cast<int32_t*>(ws + kHeaderBytes);
-    a.part = reinterpret_cast<float4*>(ws + kHeaderBytes + align_up(sizeof(int32_t) * (size_t)p->B, 256));
+    a.slots = reinterpret_cast<unsigned long long*>(ws + kHeaderBytes);
+    a.cur_tok = reinterpret_cast<int32_t*>(ws + kHeaderBytes + sample_slot_bytes(p));
+    a.part = reinterpret_cast<float4*>(ws + kHeaderBytes + sample_slot_bytes(p) +
+                                       align_up(sizeof(int32_t) * (size_t)p->B, 256));
+    a.w1_l2 = (size_t)p->V * p->r * 2 <= ((size_t)64 << 20);
     a.limit_ns = wait_limit_ns();
     a.redundant = (size_t)p->B * nt <= 8192 && p->B <= kThreads;
     a.w2_smem = w2_smem;
-    const size_t esz = p->logits_dtype == DSPARK_BF16 ? 2 : 4;
-    a.vec_ok = ((uintptr_t)base_logits % 16 == 0) && (((size_t)p->V * esz) % 16 == 0);
+    a.vec_ok = vec_ok;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(workspace, 0, kHeaderBytes, s) != cudaSuccess) return DSPARK_ERR_CUDA;
+    if (cudaMemsetAsync(workspace, 0, kHeaderBytes + (staged ? sample_slot_bytes(p) : 0), s) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
     void* args[] = {&a};
     if (cudaLaunchCooperativeKernel((const void*)fn, dim3(G), dim3(kThreads), args, smem, s) != cudaSuccess)
         return DSPARK_ERR_CUDA;

@@ -111,3 +111,11 @@ def test_full_b512_r64_sampled_requests():
     wl = W.b512_sched(device="cuda")
     tally, _ = run_and_compare(wl, requests=[0, 300, 511])
     tally.check_fraction()
+
+
+@pytest.mark.parametrize("T", [0.0, 1.0])
+def test_vocabulary_beyond_one_tile_per_sm(T):
+    # 160000 ids = 157 tiles: more tiles than SMs, so blocks own several tiles (no shared-memory staging)
+    wl = W.make_sample_workload("wide", 4, 2, 160000, 64, T, device="cuda", data_seed=12, philox_seed=3, planted=2)
+    tally, _ = run_and_compare(wl)
+    tally.check_fraction()
