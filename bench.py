@@ -99,7 +99,13 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def wait_first(self, timeout_s: float = 5.0):
+        """Block until nvidia-smi has printed its first sample (so the timed window is covered)."""
+        t_end = time.perf_counter() + timeout_s
+        while self.proc and not self.lines and time.perf_counter() < t_end:
+            time.sleep(0.02)
 
     def __exit__(self, *exc):
         if self.proc:
@@ -109,10 +115,13 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, t0: float, t1: float):
+        """Median SM clock and throttle reasons over the samples taken inside [t0, t1]."""
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ts, ln in self.lines:
+            if not (t0 <= ts <= t1):
+                continue
             p = [x.strip() for x in ln.split(",")]
             if len(p) < 9:
                 continue
@@ -184,16 +193,22 @@ def reference_arm(args, rank, world):
     B, g = wl.B, wl.gamma
     for _ in range(args.warmup):
         pass  # the oracle has no warm-up state
-    per_step = max(5.0, 60.0 / max(args.steps, 1))
+    # each step is a bounded sample (whole requests) of the batch; the run stops after ~2 minutes
+    budget_s = 120.0
+    per_step = min(5.0, budget_s / max(args.steps, 1))
     vals = []
     samples = []
+    t_start = time.perf_counter()
     for _ in range(args.steps):
         cb = run_cpu_baseline(host, seconds=per_step)
         vals.append(cb["value"])
         samples.append(cb["sample"])
+        if time.perf_counter() - t_start > budget_s and len(vals) >= 3:
+            break
     v = statistics.median(vals)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "draft tokens/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": B * g / v * 1e3, "higher_is_better": True,
+            "steps": len(vals), "steps_requested": args.steps, "warmup": args.warmup, "ms_per_step": B * g / v * 1e3,
+            "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "B": B, "gamma": g, "V": wl.V, "r": wl.r, "T": wl.T},
             "cpu_baseline": {"value": v, "unit": "draft tokens/s", "cores": 1, "kind": "oracle", "sample": samples[0]},
@@ -204,7 +219,7 @@ def reference_arm(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -283,13 +298,16 @@ def main():
         pg.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        clk.wait_first()
         wall0 = time.perf_counter()
         evs = []
         for _ in range(args.steps):
             flush.zero_()
             evs.append(step())
         torch.cuda.synchronize()
-        wall = time.perf_counter() - wall0
+        wall1 = time.perf_counter()
+        wall = wall1 - wall0
+        time.sleep(0.25)  # let the sample that covers the end of the window arrive
     for ev in evs:
         for k, n in enumerate(names):
             per[n].append(ev[k].elapsed_time(ev[k + 1]))
@@ -352,7 +370,7 @@ def main():
         "e2e": {"value": round(world * B * g / (t_e2e * 1e-3), 1), "unit": "draft tokens/s", "ms_per_step": round(t_e2e, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 6 * args.steps,
-        "clocks": clk.summary(),
+        "clocks": clk.summary(wall0, wall1 + 0.2),
         "wall_s_timed": round(wall, 3),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
