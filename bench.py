@@ -175,10 +175,10 @@ def run_cpu_baseline(wl_host, seconds: float = 15.0):
                       f"single-threaded C oracle, {el:.1f} s"}
 
 
-def host_workload(device):
+def host_workload(device, data_seed=0):
     from semi_ar_draft_gb300 import workloads as W
 
-    wl = W.b32_r64(device=device)
+    wl = W.b32_r64(device=device, data_seed=data_seed)
     t = wl.tensors
     return wl, (W.np_view(t["base"]), W.np_view(t["W1"]), W.np_view(t["W2"]), t["anchor"].cpu().numpy(),
                 W.np_view(t["target"]), t["conf"].cpu().numpy())
@@ -230,7 +230,7 @@ def main():
 
     import torch
 
-    from semi_ar_draft_gb300 import api, binding
+    from semi_ar_draft_gb300 import api, binding, shard
     from semi_ar_draft_gb300 import build as B_
 
     B_.build()
@@ -242,7 +242,9 @@ def main():
 
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
-    wl, host = host_workload(dev)
+    # weak scaling: rank k runs its own shard (requests k*B .. k*B+B-1 of the job's batch):
+    # its own seeded inputs and its own Philox key; no collective touches the data path
+    wl, host = host_workload(dev, data_seed=rank)
     t = wl.tensors
     B, g, V = wl.B, wl.gamma, wl.V
     budget = B * g
@@ -262,7 +264,7 @@ def main():
     acc = torch.empty((1, B, g), device=dev)
     emask = torch.empty((1, B, g), device=dev)
     tau = torch.empty((1, B), device=dev)
-    p = api.make_params(base, W1, wl.T, wl.seed)
+    p = api.make_params(base, W1, wl.T, shard.rank_seed(wl.seed, rank))
     ws_s = binding.workspace(binding.dspark_schedule_workspace_size(B, g), dev)
     ws_a = binding.workspace(binding.dspark_sample_workspace_size(p), dev)
     ws_v = binding.workspace(binding.dspark_verify_workspace_size(p, g), dev)
@@ -312,12 +314,8 @@ def main():
         for k, n in enumerate(names):
             per[n].append(ev[k].elapsed_time(ev[k + 1]))
         step_ms.append(ev[0].elapsed_time(ev[4]))
-    t_step = sum(step_ms) / len(step_ms)
-    if pg:
-        tt = torch.tensor([t_step], device=dev)
-        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-        t_step = float(tt.item())
-    value = world * B * g / (t_step * 1e-3)
+    t_step = shard.max_over_ranks(sum(step_ms) / len(step_ms), pg, dev)
+    value = shard.job_throughput(B * g, world, t_step * 1e-3)
 
     # e2e: the same step through the C ABI with host inputs copied in and results read back
     pin = {k: v.cpu().pin_memory() for k, v in (("base", base), ("target", target), ("conf", conf), ("anchor", anchor))}
@@ -340,11 +338,7 @@ def main():
         torch.cuda.synchronize()
         if it >= max(args.warmup, 3):
             e2e_ms.append(e0.elapsed_time(e1))
-    t_e2e = sum(e2e_ms) / len(e2e_ms)
-    if pg:
-        tt = torch.tensor([t_e2e], device=dev)
-        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-        t_e2e = float(tt.item())
+    t_e2e = shard.max_over_ranks(sum(e2e_ms) / len(e2e_ms), pg, dev)
 
     avg = {n: sum(v) / len(v) for n, v in per.items()}
     algo = algorithmic_bytes(wl, n_rej)
@@ -367,7 +361,7 @@ def main():
                      "traffic": profiled_traffic(dom), "algorithmic_bytes": algo[dom]},
         "kernels": kernels,
         "n_rejected": n_rej,
-        "e2e": {"value": round(world * B * g / (t_e2e * 1e-3), 1), "unit": "draft tokens/s", "ms_per_step": round(t_e2e, 4),
+        "e2e": {"value": round(shard.job_throughput(B * g, world, t_e2e * 1e-3), 1), "unit": "draft tokens/s", "ms_per_step": round(t_e2e, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 6 * args.steps,
         "clocks": clk.summary(wall0, wall1 + 0.2),

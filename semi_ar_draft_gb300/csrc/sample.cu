@@ -16,6 +16,11 @@
 //     step's token, LSE(z/T) and z at the token; bounded grid-wide wait; next step.
 // When each block owns a single tile and the W2 rows of it fit, they are staged in shared
 // memory once for all gamma steps.
+// Two kernels implement this: sample_staged_kernel (bf16 logits, tensor-core bias, one tile
+// per block: base and W1 rows staged by the bulk-copy engine, tile winners exchanged through
+// one packed atomic max per request and step, one grid-wide wait per step) and sample_kernel
+// (every other case: fp32 logits, CUDA-core GEMV bias, vocabularies with more tiles than
+// co-resident blocks; records reduced redundantly or by owner blocks).
 #include <algorithm>
 #include <atomic>
 #include <cmath>

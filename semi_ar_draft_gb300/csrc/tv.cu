@@ -7,11 +7,14 @@
 // eval_mask = cumprod of (keep && pos_valid) (P1 section 3.6), tau = 1 + sum_i prod_{k<=i}
 // acc_k * mask_k (P1 section 3.10).
 //
-// Design: a thread-block cluster of kCS blocks owns one row at a time (persistent over rows);
-// each block streams its 1/kCS segment of d and t once to get (max, sum) of both softmaxes,
-// the blocks exchange those through distributed shared memory, then each block re-reads its
-// segment (an L2 hit: the rows in flight stay far below the L2 size) for the sum of minima,
-// and block 0 of the cluster sums the partial results and writes acc and eval_mask.
+// Design: a thread-block cluster owns one row at a time (persistent over rows); each block of
+// it takes a 1/cs segment of d and t, gets (max, sum) of both softmaxes over the segment, the
+// blocks exchange those through distributed shared memory, each block then forms its part of
+// the sum of minima, and block 0 of the cluster adds the parts and writes acc and eval_mask.
+// Two kernels implement it: tv_tma_kernel (bf16 rows on 16-byte boundaries that fit the copy
+// ring: the segment is read from HBM once, into a shared-memory ring filled by the bulk-copy
+// engine, and both passes read shared memory) and tv_kernel (any other case: the second pass
+// re-reads the segment, an L2 hit since the rows in flight stay far below the L2 size).
 #include <cooperative_groups.h>
 
 #include <algorithm>
