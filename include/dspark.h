@@ -57,8 +57,8 @@ enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 };
 
 /* Random-draw purposes (the fourth Philox counter word). */
 enum {
-    DSPARK_P_SAMPLE_TILE = 1,   /* draft sampling: one uniform per vocabulary tile */
-    DSPARK_P_SAMPLE_INTILE = 2, /* draft sampling: the in-tile inverse-CDF uniform */
+    DSPARK_P_SAMPLE_CHUNK = 1,   /* draft sampling: one uniform per vocabulary chunk (n = chunk index) */
+    DSPARK_P_SAMPLE_INCHUNK = 2, /* draft sampling: the in-chunk inverse-CDF uniform (n = 0) */
     DSPARK_P_ACCEPT = 3,        /* verify: the acceptance uniform u_i */
     DSPARK_P_RESID_TILE = 4,    /* verify: residual draw, per tile */
     DSPARK_P_RESID_INTILE = 5,  /* verify: residual draw, in tile */
@@ -66,24 +66,30 @@ enum {
     DSPARK_P_BONUS_INTILE = 7   /* verify: bonus draw, in tile */
 };
 
-/* Vocabulary tile and chunk of the sampler (see "Sampling contract" below). */
+/* Vocabulary tile and chunk of the samplers (see "Sampling contracts" below). */
 #define DSPARK_TILE 1024
 #define DSPARK_CHUNK 32
 
 /*
- * Sampling contract (the pages never show the body of sample_tokens, P2 section 3.4;
- * any exact categorical draw is lossless, bit-parity needs one fixed definition):
+ * Sampling contracts (the pages never show the body of sample_tokens, P2 section 3.4;
+ * any exact categorical draw is lossless, bit-parity needs one fixed definition).
  *   T == 0: x = argmax_v z_v, lowest index on ties.
- *   T  > 0: s = z / T.  Tiles of DSPARK_TILE consecutive ids, chunks of DSPARK_CHUNK consecutive
- *           ids inside a tile; LSE of a set = log sum e^{s_v} over it.
- *           t* = argmax_t (LSE_t - ln E_t), E_t = -ln U(seed, j, i, SAMPLE_TILE, t), lowest t on ties;
- *           c* = smallest chunk c of t* with sum_{c' <= c} e^{LSE_c' - LSE_t*} > U(.., SAMPLE_INTILE, 0);
- *           x  = smallest id v of c* with sum_{w in c*, w <= v} e^{s_w - LSE_c*} > U(.., SAMPLE_INTILE, 1);
- *           where rounding leaves no crossing: the last chunk (id) with nonzero mass.
- *   This is softmax(s) exactly: Gumbel-max over tiles picks t with probability proportional to
- *   e^{LSE_t}; the two inverse CDFs, on independent uniforms, pick c and then v proportionally to
- *   their masses.  Residual and bonus draws in dspark_verify use the same contract on their own
- *   weights and purposes.
+ *   Draft sampling (T > 0), chunk-Gumbel: s = z / T; chunks of DSPARK_CHUNK consecutive ids
+ *     over the whole vocabulary (the last may be short); LSE_c = log sum_{v in c} e^{s_v};
+ *       c* = argmax_c (LSE_c - ln E_c), E_c = -ln U(seed, j, i, SAMPLE_CHUNK, c), lowest c on ties
+ *            (chunks without mass never win);
+ *       x  = smallest id v of c* with sum_{w in c*, w <= v} e^{s_w - LSE_c*} > U(.., SAMPLE_INCHUNK, 0),
+ *            or, where rounding leaves no crossing, the last id of c* with nonzero mass.
+ *     Gumbel-max over chunks picks c with probability proportional to e^{LSE_c}; the in-chunk
+ *     uniform is independent of the race, so v follows e^{s_v} inside c: the draw is softmax(s).
+ *   Correction draws of dspark_verify (residual, bonus), tile-Gumbel: tiles of DSPARK_TILE ids,
+ *     chunks of DSPARK_CHUNK ids inside a tile, weights w_v, LSE of a set = log sum w over it;
+ *       t* = argmax_t (LSE_t - ln E_t), E_t = -ln U(.., *_TILE, t), lowest t on ties;
+ *       c* = smallest chunk c of t* with sum_{c' <= c} e^{LSE_c' - LSE_t*} > U(.., *_INTILE, 0);
+ *       x  = smallest id v of c* with sum_{w in c*, w <= v} e^{log w_v - LSE_c*} > U(.., *_INTILE, 1);
+ *       where rounding leaves no crossing: the last chunk (id) with nonzero mass.
+ *     Gumbel-max over tiles picks t proportionally to e^{LSE_t}; the two inverse CDFs, on
+ *     independent uniforms, pick c and then v proportionally to their masses.
  */
 
 typedef struct {
@@ -102,7 +108,7 @@ typedef struct {
  * P1 section 3.7; P4 section 3.3):
  *   prev_1 = anchor[j];  for i = 1..gamma:
  *     z_{j,i} = base[j, i-1, :] + W2 . W1[prev_i]      (bias_v = sum_k W1[prev_i, k] W2[v, k])
- *     x_{j,i} ~ sampling contract on z_{j,i} / T;  prev_{i+1} = x_{j,i}
+ *     x_{j,i} ~ draft sampling contract on z_{j,i} / T;  prev_{i+1} = x_{j,i}
  * Arguments
  *   base_logits [B, gamma, V] (logits_dtype); W1 [V, r], W2 [V, r] (w_dtype; W2 is the
  *   nn.Linear(r, V).weight layout, i.e. the page's r x V matrix transposed in memory;

@@ -22,7 +22,7 @@ import numpy as np
 
 F32, BF16 = 0, 1
 TILE, CHUNK = 1024, 32  # the library's vocabulary tile and chunk sizes
-P_SAMPLE_TILE, P_SAMPLE_INTILE, P_ACCEPT = 1, 2, 3
+P_SAMPLE_CHUNK, P_SAMPLE_INCHUNK, P_ACCEPT = 1, 2, 3
 P_RESID_TILE, P_RESID_INTILE, P_BONUS_TILE, P_BONUS_INTILE, P_ELEM_GUMBEL = 4, 5, 6, 7, 8
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -57,6 +57,8 @@ def lib():
         L.oracle_argmax.restype = i32
         L.oracle_tile_gumbel.argtypes = [vp, i32, i32, i32, u64, i32, i32, i32, i32, vp, vp]
         L.oracle_tile_gumbel.restype = i32
+        L.oracle_chunk_gumbel.argtypes = [vp, i32, i32, u64, i32, i32, i32, i32, vp, vp]
+        L.oracle_chunk_gumbel.restype = i32
         L.oracle_gumbel_elem.argtypes = [vp, i32, u64, i32, i32, vp]
         L.oracle_gumbel_elem.restype = i32
         L.oracle_sample_request.argtypes = [i32, i32, i32, i32, i32, dbl, u64, i32, i32, vp, vp, vp, i32, i32,
@@ -135,11 +137,21 @@ def argmax(z: np.ndarray):
     return int(x), float(m[0])
 
 
-def tile_gumbel(lw: np.ndarray, TS: int, seed: int, j: int, i: int, p_tile=P_SAMPLE_TILE, p_intile=P_SAMPLE_INTILE,
+def tile_gumbel(lw: np.ndarray, TS: int, seed: int, j: int, i: int, p_tile=P_RESID_TILE, p_intile=P_RESID_INTILE,
                 CS: int = CHUNK):
+    """The tile-Gumbel draw of the residual / bonus corrections.  Returns (x, margin, lse)."""
     lw = np.ascontiguousarray(lw, dtype=np.float64)
     m, lse = np.zeros(1), np.zeros(1)
     x = lib().oracle_tile_gumbel(_p(lw), lw.shape[0], TS, CS, seed, j, i, p_tile, p_intile, _p(m), _p(lse))
+    return int(x), float(m[0]), float(lse[0])
+
+
+def chunk_gumbel(lw: np.ndarray, seed: int, j: int, i: int, CS: int = CHUNK, p_chunk=P_SAMPLE_CHUNK,
+                 p_inchunk=P_SAMPLE_INCHUNK):
+    """The chunk-Gumbel draw of the draft sampler.  Returns (x, margin, lse)."""
+    lw = np.ascontiguousarray(lw, dtype=np.float64)
+    m, lse = np.zeros(1), np.zeros(1)
+    x = lib().oracle_chunk_gumbel(_p(lw), lw.shape[0], CS, seed, j, i, p_chunk, p_inchunk, _p(m), _p(lse))
     return int(x), float(m[0]), float(lse[0])
 
 

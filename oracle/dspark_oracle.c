@@ -37,8 +37,8 @@
 #define OR_BF16 1
 
 /* Purposes: the fourth Philox counter word.  Which random draw is which. */
-#define OR_P_SAMPLE_TILE 1
-#define OR_P_SAMPLE_INTILE 2
+#define OR_P_SAMPLE_CHUNK 1
+#define OR_P_SAMPLE_INCHUNK 2
 #define OR_P_ACCEPT 3
 #define OR_P_RESID_TILE 4
 #define OR_P_RESID_INTILE 5
@@ -232,6 +232,62 @@ int oracle_tile_gumbel(const double* lw, int V, int TS, int CS, uint64_t seed, i
     return clo + k;
 }
 
+/* ------------------------------------------------------------------ */
+/* Chunk-Gumbel categorical sampler over log-weights lw[0..V): the     */
+/* draft sampler's contract (the body of sample_tokens is not shown,   */
+/* P2 section 3.4; any exact categorical draw is lossless).            */
+/*   chunks of CS consecutive ids over the whole vocabulary (the last  */
+/*   one may be short); LSE_c = log sum_{v in c} e^lw_v;               */
+/*   c* = argmax_c LSE_c - ln E_c, E_c = -ln U(.., p_chunk, c), lowest */
+/*   c on ties; chunks without mass never win;                         */
+/*   x  = smallest id of c* whose in-order cumulative mass             */
+/*   sum_{w<=v} e^(lw_w - LSE_c*) exceeds u = U(.., p_inchunk, 0);     */
+/*   where rounding leaves no crossing, the last id with mass.         */
+/* Gumbel-max over chunks gives P(c) proportional to e^LSE_c; u is     */
+/* independent of the race, so P(v | c) is proportional to e^lw_v and  */
+/* the product is softmax(lw).  Returns x (-1 when nothing has mass);  */
+/* *lse_all = log-sum-exp of all lw; *margin = min(chunk-key gap,      */
+/* distance of u to the id CDF boundaries around x).                   */
+/* ------------------------------------------------------------------ */
+int oracle_chunk_gumbel(const double* lw, int V, int CS, uint64_t seed, int j, int i, int p_chunk, int p_inchunk,
+                        double* margin, double* lse_all) {
+    int nc = (V + CS - 1) / CS;
+    double* lse_c = (double*)malloc(sizeof(double) * (size_t)nc);
+    for (int c = 0; c < nc; ++c) {
+        int lo = c * CS, n = (lo + CS <= V) ? CS : V - lo;
+        lse_c[c] = logsumexp(lw + lo, n);
+    }
+    if (lse_all) *lse_all = logsumexp(lse_c, nc);
+    int best = -1;
+    double best_key = -INFINITY, second_key = -INFINITY;
+    for (int c = 0; c < nc; ++c) {
+        if (lse_c[c] == -INFINITY) continue;
+        double key = lse_c[c] - log(neg_log_u(oracle_uniform(seed, (uint32_t)j, (uint32_t)i, (uint32_t)p_chunk, (uint32_t)c)));
+        if (best < 0 || key > best_key) {
+            if (best >= 0) second_key = best_key;
+            best_key = key;
+            best = c;
+        } else if (key > second_key) {
+            second_key = key;
+        }
+    }
+    if (best < 0) {
+        free(lse_c);
+        if (margin) *margin = 0.0;
+        return -1;
+    }
+    double u = oracle_uniform(seed, (uint32_t)j, (uint32_t)i, (uint32_t)p_inchunk, 0u);
+    int lo = best * CS, n = (lo + CS <= V) ? CS : V - lo;
+    double m_id;
+    int k = inverse_cdf(lw + lo, n, lse_c[best], u, &m_id);
+    if (margin) {
+        double m_chunk = best_key - second_key; /* +inf when a single chunk has mass */
+        *margin = m_chunk < m_id ? m_chunk : m_id;
+    }
+    free(lse_c);
+    return lo + k;
+}
+
 /* Second sampler (reference for the chi-square test): per-element Gumbel-max,
  * x = argmax_v lw_v - ln E_v with E_v = -ln U(.., p_elem, v). */
 int oracle_gumbel_elem(const double* lw, int V, uint64_t seed, int j, int i, double* margin) {
@@ -279,7 +335,7 @@ void oracle_sample_request(int V, int r, int gamma, int TS, int CS, double T, ui
             lse = NAN;
         } else {
             for (int v = 0; v < V; ++v) s[v] = z[v] / T;
-            x = oracle_tile_gumbel(s, V, TS, CS, seed, j, i, OR_P_SAMPLE_TILE, OR_P_SAMPLE_INTILE, &mg, &lse);
+            x = oracle_chunk_gumbel(s, V, CS, seed, j, i, OR_P_SAMPLE_CHUNK, OR_P_SAMPLE_INCHUNK, &mg, &lse);
         }
         tokens[step] = x;
         draft_lse[step] = lse;
@@ -541,20 +597,22 @@ int oracle_theta_schedule(int gamma, const double* c, const double* sps, double*
 /* ------------------------------------------------------------------ */
 /* Trial loops for the chi-square pins (thin drivers of the above).    */
 /* ------------------------------------------------------------------ */
-/* variant 0: tile-Gumbel with tile size TS and chunk size CS; 1: per-element Gumbel-max.
+/* variant 0: tile-Gumbel with tile size TS and chunk size CS (the residual / bonus draws of
+ * verify); 1: per-element Gumbel-max; 2: chunk-Gumbel with chunk size CS (the draft sampler).
  * Trial n uses request index j = n, position i = 1. */
 void oracle_trials_sampler(int V, int TS, int CS, const double* lw, uint64_t seed, long ntrials, int variant,
                            int64_t* counts) {
     for (int v = 0; v < V; ++v) counts[v] = 0;
     for (long n = 0; n < ntrials; ++n) {
-        int x = variant == 0 ? oracle_tile_gumbel(lw, V, TS, CS, seed, (int)n, 1, OR_P_SAMPLE_TILE, OR_P_SAMPLE_INTILE, NULL, NULL)
-                             : oracle_gumbel_elem(lw, V, seed, (int)n, 1, NULL);
+        int x = variant == 0   ? oracle_tile_gumbel(lw, V, TS, CS, seed, (int)n, 1, OR_P_RESID_TILE, OR_P_RESID_INTILE, NULL, NULL)
+                : variant == 1 ? oracle_gumbel_elem(lw, V, seed, (int)n, 1, NULL)
+                               : oracle_chunk_gumbel(lw, V, CS, seed, (int)n, 1, OR_P_SAMPLE_CHUNK, OR_P_SAMPLE_INCHUNK, NULL, NULL);
         counts[x] += 1;
     }
 }
 
 /* One speculative position per trial on V-sized fp32 logits (r = 0, one
- * position, no bonus row): draft x ~ softmax(zd/T) by the tile sampler, verify
+ * position, no bonus row): draft x ~ softmax(zd/T) by the chunk sampler, verify
  * against softmax(zt/T); counts the emitted token (x if accepted, else the
  * residual draw) and the number of acceptances. */
 void oracle_trials_spec_one(int V, int TS, int CS, double T, const float* zd, const float* zt, uint64_t seed, long ntrials,
@@ -565,7 +623,7 @@ void oracle_trials_spec_one(int V, int TS, int CS, double T, const float* zd, co
     *n_accept = 0;
     for (int v = 0; v < V; ++v) emitted[v] = 0;
     for (long n = 0; n < ntrials; ++n) {
-        int32_t x = oracle_tile_gumbel(s, V, TS, CS, seed, (int)n, 1, OR_P_SAMPLE_TILE, OR_P_SAMPLE_INTILE, NULL, NULL);
+        int32_t x = oracle_chunk_gumbel(s, V, CS, seed, (int)n, 1, OR_P_SAMPLE_CHUNK, OR_P_SAMPLE_INCHUNK, NULL, NULL);
         float lse_f = (float)lse_d, zx_f = zd[x];
         int32_t corr;
         int nacc = oracle_verify_request(V, 0, 1, 1, TS, CS, T, seed, OR_F32, OR_F32, OR_F32, zd, NULL, NULL, 0, (int)n,

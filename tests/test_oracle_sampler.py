@@ -65,10 +65,44 @@ def test_single_chunk_is_inverse_cdf():
     p = special.softmax(lw)
     cdf = np.cumsum(p)
     for j in range(200):
+        # tile contract (residual / bonus draws): one tile, one chunk
         x, m, lse = O.tile_gumbel(lw, 8, 5, j, 2, CS=8)
-        u2 = O.uniform(5, j, 2, O.P_SAMPLE_INTILE, 1)
+        u2 = O.uniform(5, j, 2, O.P_RESID_INTILE, 1)
         assert x == int(np.searchsorted(cdf, u2, side="right"))
         assert abs(lse - special.logsumexp(lw)) < 1e-12
+        # chunk contract (draft sampler): a vocabulary of one chunk
+        x, m, lse = O.chunk_gumbel(lw, 5, j, 2, CS=8)
+        u = O.uniform(5, j, 2, O.P_SAMPLE_INCHUNK, 0)
+        assert x == int(np.searchsorted(cdf, u, side="right"))
+        assert abs(lse - special.logsumexp(lw)) < 1e-12
+
+
+def test_chunk_race_then_inverse_cdf():
+    # 12 ids in chunks of 4: the chunk with the largest LSE_c - ln(-ln u_c) wins, the id is the
+    # in-order inverse CDF of u inside it; the short last chunk (V = 14) takes part too
+    rng = np.random.default_rng(15)
+    for V in (12, 14):
+        lw = rng.normal(0, 1.0, V)
+        nc = (V + 3) // 4
+        lse_c = np.array([special.logsumexp(lw[4 * c:4 * c + 4]) for c in range(nc)])
+        for j in range(300):
+            x, m, lse = O.chunk_gumbel(lw, 7, j, 3, CS=4)
+            keys = [lse_c[c] - np.log(-np.log(O.uniform(7, j, 3, O.P_SAMPLE_CHUNK, c))) for c in range(nc)]
+            c = int(np.argmax(keys))
+            u = O.uniform(7, j, 3, O.P_SAMPLE_INCHUNK, 0)
+            pc = special.softmax(lw[4 * c:4 * c + 4])
+            k = int(np.searchsorted(np.cumsum(pc), u, side="right"))
+            assert x == 4 * c + k
+            assert m <= sorted(keys)[-1] - sorted(keys)[-2] + 1e-12
+
+
+def test_chunk_sampler_skips_zero_mass():
+    lw = np.array([-np.inf, -np.inf, 0.3, 1.0, -np.inf, -np.inf, -np.inf, -2.0, -np.inf])
+    for j in range(300):
+        x, m, lse = O.chunk_gumbel(lw, 9, j, 1, CS=2)
+        assert np.isfinite(lw[x])
+    assert abs(lse - special.logsumexp(lw)) < 1e-12
+    assert O.chunk_gumbel(np.full(5, -np.inf), 1, 0, 1, CS=2)[0] == -1
 
 
 def test_two_level_inverse_cdf_within_a_tile():
@@ -79,8 +113,8 @@ def test_two_level_inverse_cdf_within_a_tile():
     cmass = p.reshape(3, 4).sum(1)
     for j in range(300):
         x, m, lse = O.tile_gumbel(lw, 12, 6, j, 3, CS=4)
-        u1 = O.uniform(6, j, 3, O.P_SAMPLE_INTILE, 0)
-        u2 = O.uniform(6, j, 3, O.P_SAMPLE_INTILE, 1)
+        u1 = O.uniform(6, j, 3, O.P_RESID_INTILE, 0)
+        u2 = O.uniform(6, j, 3, O.P_RESID_INTILE, 1)
         c = int(np.searchsorted(np.cumsum(cmass), u1, side="right"))
         k = int(np.searchsorted(np.cumsum(p[4 * c:4 * c + 4] / cmass[c]), u2, side="right"))
         assert x == 4 * c + k
@@ -100,7 +134,8 @@ def _chi2_p(counts, probs):
 
 
 @pytest.mark.parametrize("T", [0.7, 1.0])
-@pytest.mark.parametrize("TS,CS,variant", [(2, 1, 0), (3, 2, 0), (8, 8, 0), (8, 3, 0), (4, 2, 0), (8, 8, 1)])
+@pytest.mark.parametrize("TS,CS,variant", [(2, 1, 0), (3, 2, 0), (8, 8, 0), (8, 3, 0), (4, 2, 0), (8, 8, 1),
+                                           (0, 1, 2), (0, 2, 2), (0, 3, 2), (0, 8, 2)])
 def test_samplers_chi_square(T, TS, CS, variant):
     rng = np.random.default_rng(10)
     z = rng.normal(0, 1.2, 8)
@@ -113,9 +148,10 @@ def test_chi_square_detects_a_wrong_law():
     # the same test must reject a sampler drawing from a slightly different law
     rng = np.random.default_rng(10)
     lw = rng.normal(0, 1.2, 8)
-    counts = O.trials_sampler(lw, 4, 77, 1_000_000, 0, CS=2)
     wrong = special.softmax(lw * 1.02)
-    assert _chi2_p(counts, wrong) < 1e-6
+    for variant in (0, 2):
+        counts = O.trials_sampler(lw, 4, 77, 1_000_000, variant, CS=2)
+        assert _chi2_p(counts, wrong) < 1e-6
 
 
 def test_sample_request_greedy_chain():
@@ -147,7 +183,7 @@ def test_sample_request_carries_token_and_lse():
     prev = 7
     for i in range(gamma):
         z = base[0, i].astype(np.float64) + W2.astype(np.float64) @ W1[prev].astype(np.float64)
-        x, m, l = O.tile_gumbel(z / T, 16, 99, 0, i + 1, CS=4)
+        x, m, l = O.chunk_gumbel(z / T, 99, 0, i + 1, CS=4)
         assert tok[i] == x and abs(lse[i] - special.logsumexp(z / T)) < 1e-12
         assert abs(zx[i] - z[x]) < 1e-12
         prev = x

@@ -57,7 +57,7 @@ def test_residual_support_is_where_target_exceeds_draft():
     tgt = zt.reshape(1, 1, 8)
     seen = set()
     for j in range(3000):
-        x, _, _ = O.tile_gumbel(zd.astype(np.float64) / T, 8, 3, j, 1, CS=4)
+        x, _, _ = O.chunk_gumbel(zd.astype(np.float64) / T, 3, j, 1, CS=4)
         n, corr, mm, fb = O.verify_request(base, None, None, 0, j, np.array([x], np.int32), np.array([lse_d]),
                                            np.array([zd[x]]), tgt, 1, T, 3, 8, row=0, CS=4)
         if n == 0:
