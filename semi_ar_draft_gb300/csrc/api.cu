@@ -1,7 +1,10 @@
 // api.cu -- status strings, device status read-back, the wait bound, and the grid-wait self test.
 #include <atomic>
+#include <mutex>
+#include <vector>
 
 #include "common.cuh"
+
 #include "host_util.h"
 
 namespace dspark {
@@ -32,6 +35,89 @@ cudaError_t device_sm_count(int* sms) {
 }
 
 uint64_t wait_limit_ns() { return g_wait_limit_ns.load(); }
+
+
+namespace {
+struct KernelPrep {
+    int dev;
+    const void* fn;
+    size_t smem_set;  // largest dynamic shared memory granted so far
+    size_t smem;
+    int threads;
+    int per_sm;
+};
+std::mutex g_prep_mu;
+std::vector<KernelPrep> g_prep;
+}  // namespace
+
+namespace {
+struct ClusterOcc {
+    int dev;
+    const void* fn;
+    int cs, threads;
+    size_t smem;
+    int n;
+};
+std::vector<ClusterOcc> g_cocc;
+}  // namespace
+
+cudaError_t max_active_clusters(const void* fn, int cs, int threads, size_t smem, int* n) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_prep_mu);
+    for (const ClusterOcc& c : g_cocc)
+        if (c.dev == dev && c.fn == fn && c.cs == cs && c.threads == threads && c.smem == smem) {
+            *n = c.n;
+            return cudaSuccess;
+        }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(cs);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int k = 0;
+    if (cudaOccupancyMaxActiveClusters(&k, fn, &cfg) != cudaSuccess) {
+        cudaGetLastError();  // an unsupported shape: remember it as zero
+        k = 0;
+    }
+    g_cocc.push_back(ClusterOcc{dev, fn, cs, threads, smem, k});
+    *n = k;
+    return cudaSuccess;
+}
+
+cudaError_t prepare_kernel(const void* fn, size_t smem, int threads, int* per_sm) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_prep_mu);
+    size_t granted = 0;
+    for (const KernelPrep& k : g_prep)
+        if (k.dev == dev && k.fn == fn) {
+            if (k.smem == smem && k.threads == threads) {
+                *per_sm = k.per_sm;
+                return cudaSuccess;
+            }
+            granted = granted > k.smem_set ? granted : k.smem_set;
+        }
+    if (smem > granted) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        granted = smem;
+    }
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem);
+    if (e != cudaSuccess) return e;
+    g_prep.push_back(KernelPrep{dev, fn, granted, smem, threads, n});
+    *per_sm = n;
+    return cudaSuccess;
+}
 
 }  // namespace dspark
 

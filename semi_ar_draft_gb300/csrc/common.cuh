@@ -119,10 +119,33 @@ __device__ __forceinline__ float u01(uint32_t x) { return ((float)(x >> 9) + 0.5
 __device__ __forceinline__ float uniform(uint64_t seed, uint32_t j, uint32_t i, uint32_t purpose, uint32_t n) {
     return u01(philox_word(seed, j, i, purpose, n));
 }
-// ln E with E = -ln u, accurate for u near 1 (1 - u is exact for these u).
+// ln E with E = -ln u, for the exponential variates of the Gumbel races (absolute error a few
+// 1e-7, far inside the decision margin).  u < 1/2: E = -log2(u) ln 2 by the hardware log2.
+// u >= 1/2 (E small, where a variate is most likely to win): t = u - 1 is exact and
+// E = -log1p(t) = -2 atanh(s), s = t / (2 + t) in [-1/3, 0), summed as the odd series
+// 2 (s + s^3/3 + s^5/5 + ...) to s^19 (truncation below 2e-10 relative at |s| = 1/3), so E keeps
+// its relative precision down to E ~ 2^-24.  Then ln E = log2(E) ln 2 by the hardware log2.
 __device__ __forceinline__ float log_neg_log_u(float u) {
-    const float e = (u < 0.5f) ? -logf(u) : -log1pf(-(1.0f - u));
-    return logf(e);
+    float e;
+    if (u < 0.5f) {
+        e = -lg2(u) * 0.69314718055994531f;
+    } else {
+        const float t = u - 1.0f;
+        const float sv = __fdividef(t, 2.0f + t);
+        const float s2 = sv * sv;
+        float q = 1.0f / 19.0f;
+        q = fmaf(q, s2, 1.0f / 17.0f);
+        q = fmaf(q, s2, 1.0f / 15.0f);
+        q = fmaf(q, s2, 1.0f / 13.0f);
+        q = fmaf(q, s2, 1.0f / 11.0f);
+        q = fmaf(q, s2, 1.0f / 9.0f);
+        q = fmaf(q, s2, 1.0f / 7.0f);
+        q = fmaf(q, s2, 1.0f / 5.0f);
+        q = fmaf(q, s2, 1.0f / 3.0f);
+        q = fmaf(q, s2, 1.0f);
+        e = -2.0f * sv * q;
+    }
+    return lg2(e) * 0.69314718055994531f;
 }
 
 // ---------------------------------------------------------------- reductions
@@ -181,6 +204,25 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                      smem_addr(dst)),
                  "l"(src), "r"(bytes), "r"(smem_addr(bar))
                  : "memory");
+}
+// L2 eviction-priority policies (createpolicy): data read once goes first, data read again stays.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+// bulk_g2s with an L2 eviction policy for the source lines.
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+        : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t done;

@@ -55,6 +55,10 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t a0, const
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
+// The same with an L2 eviction policy for the prefetched lines.
+__device__ __forceinline__ void prefetch_l2_hint(const void* p, uint32_t bytes, uint64_t pol) {
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(p), "r"(bytes), "l"(pol) : "memory");
+}
 
 // --------------------------------------------------------------------------------------------
 // Tensor-core bias: mma.sync m16n8k16, rows = 16 requests (A = W1[prev]), columns = 8 ids
@@ -131,16 +135,37 @@ __device__ __forceinline__ void load_frag_smem(const uint4* w2s, int vl, int tq,
     }
 }
 
-// Stage W2 rows [tile0, tile0 + kTS) into shared memory (swizzled); rows past V are zero.
+// Stage W2 rows [tile0, tile0 + kTS) into shared memory (swizzled; threads 0 .. nthreads-1
+// take part); rows past V are zero.
 template <int KS>
-__device__ void stage_w2_tile(const uint16_t* W2, int tile0, int V, uint4* dst) {
+__device__ void stage_w2_tile(const uint16_t* W2, int tile0, int V, uint4* dst, int nthreads) {
     constexpr int units = w2_units<KS>();
     constexpr int mask = w2_mask<KS>();
-    for (int idx = threadIdx.x; idx < kTS * units; idx += blockDim.x) {
+    for (int idx = threadIdx.x; idx < kTS * units; idx += nthreads) {
         const int vl = idx / units, u = idx % units;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (tile0 + vl < V) v = __ldg(reinterpret_cast<const uint4*>(W2 + (size_t)(tile0 + vl) * (16 * KS)) + u);
         dst[vl * units + (u ^ (vl & mask))] = v;
+    }
+}
+
+// The same staging with every 16-byte copy in flight at once (cp.async, L2 -> shared memory,
+// no register round trip); the caller waits with cp_async_wait_all() and a barrier.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n cp.async.wait_group 0;" ::: "memory");
+}
+template <int KS>
+__device__ void stage_w2_tile_async(const uint16_t* W2, int tile0, int V, uint4* dst, int nthreads) {
+    constexpr int units = w2_units<KS>();
+    constexpr int mask = w2_mask<KS>();
+    for (int idx = threadIdx.x; idx < kTS * units; idx += nthreads) {
+        const int vl = idx / units, u = idx % units;
+        uint4* d = dst + vl * units + (u ^ (vl & mask));
+        if (tile0 + vl < V) cp_async16(d, reinterpret_cast<const uint4*>(W2 + (size_t)(tile0 + vl) * (16 * KS)) + u);
+        else *d = make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
@@ -551,6 +576,41 @@ __device__ __forceinline__ void load_frag_row(const uint16_t* row, int tq, Frag<
     }
 }
 
+// As mma_chunk, with the A fragments (W1 rows g and g + 8) read from shared memory as they are
+// used instead of being held in registers for the whole row block.
+template <int KS, bool W2SMEM>
+__device__ __forceinline__ void mma_chunk_rows(float (&xa)[8], float (&xb)[8], const uint16_t* w1a, const uint16_t* w1b,
+                                               const uint16_t* W2, const uint4* w2s, int tile0, int c, int V, int g,
+                                               int tq, bool full) {
+    constexpr int r = 16 * KS;
+    if constexpr (KS == 1) {
+        Frag<1> fa, fb;
+        load_frag_row<1>(w1a, tq, fa);
+        load_frag_row<1>(w1b, tq, fb);
+        mma_chunk<1, W2SMEM>(xa, xb, fa, fb, W2, w2s, tile0, c, V, g, tq, full);
+    } else {
+        constexpr int units = w2_units<KS>();
+        constexpr int mask = w2_mask<KS>();
+#pragma unroll
+        for (int q = 0; q < KS / 2; ++q) {  // two k-steps per 16-byte unit of the lane's weights
+            const uint4 a = reinterpret_cast<const uint4*>(w1a + tq * (r / 4))[q];
+            const uint4 b = reinterpret_cast<const uint4*>(w1b + tq * (r / 4))[q];
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                const int vl = kCS * c + 8 * (g >> 1) + 2 * nt + (g & 1);
+                uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                if (full || tile0 + vl < V) {
+                    const int u = tq * (KS / 2) + q;
+                    if constexpr (W2SMEM) w = w2s[(size_t)vl * units + (u ^ (vl & mask))];
+                    else w = __ldg(reinterpret_cast<const uint4*>(W2 + (size_t)(tile0 + vl) * r + tq * (r / 4)) + q);
+                }
+                mma4(xa[2 * nt], xa[2 * nt + 1], xb[2 * nt], xb[2 * nt + 1], a.x, b.x, a.y, b.y, w.x, w.y);
+                mma4(xa[2 * nt], xa[2 * nt + 1], xb[2 * nt], xb[2 * nt + 1], a.z, b.z, a.w, b.w, w.z, w.w);
+            }
+        }
+    }
+}
+
 // T > 0 chunk statistics straight from z: the maximum of the log2-weights z * scale2 is the
 // scaled maximum of z (scale2 > 0), the sum uses one fused multiply-add per id.
 __device__ __forceinline__ float2 chunk_stats_scaled(const float (&z)[8], float scale2) {
@@ -610,6 +670,151 @@ __device__ __forceinline__ void produce_staged(const uint16_t* stage, const uint
             cstat[(g + 8) * kChunks + c] = sb;
         }
     }
+}
+
+// --------------------------------------------------------------------------------------------
+// Chunk-Gumbel draft sampling (dspark.h): every chunk's record is formed where its z values sit,
+// in the lane quad that holds them (lane tq: ids 8 tq .. 8 tq + 7 of the chunk):
+//   T > 0: {key = LSE_c - ln E_c, LSE_c, candidate by the in-chunk inverse CDF of u, z at it}
+//          (natural-log units; a chunk without mass: {-inf, -inf, -1, 0});
+//   greedy: {max z, NaN, lowest argmax, max z}.
+// --------------------------------------------------------------------------------------------
+__device__ __forceinline__ float4 chunk_record_cg(const float (&z)[8], int id0, float scale2, float lnE, float u) {
+    const int lane = threadIdx.x & 31, tq = lane & 3;
+    float m = z[0];
+#pragma unroll
+    for (int e = 1; e < 8; ++e) m = fmaxf(m, z[e]);
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    const float m2 = m * scale2;
+    const float mref = (m2 == -CUDART_INF_F) ? 0.f : m2;
+    float cum[8];
+    float run = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        run += ex2(fmaf(z[e], scale2, -mref));
+        cum[e] = run;
+    }
+    // in-order prefix over the quad, summed left to right so that a lane's end is exactly the
+    // next lane's start (the crossing lane is then unique)
+    const float r0 = __shfl_sync(0xffffffffu, run, 0, 4);
+    const float r1 = __shfl_sync(0xffffffffu, run, 1, 4);
+    const float r2 = __shfl_sync(0xffffffffu, run, 2, 4);
+    const float r3 = __shfl_sync(0xffffffffu, run, 3, 4);
+    const float b2 = r0 + r1, b3 = b2 + r2, S = b3 + r3;
+    const float before = tq == 0 ? 0.f : (tq == 1 ? r0 : (tq == 2 ? b2 : b3));
+    const float target = u * S;
+    // the lane holding the first crossing: cumulative mass reaches past target inside it
+    const bool mine = before <= target && before + run > target;  // before + run == next lane's start
+    int e_star = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) e_star += (before + cum[e] <= target) ? 1 : 0;
+    e_star = min(e_star, 7);
+    const unsigned quad = (unsigned)(lane & ~3);
+    const unsigned bal = (__ballot_sync(0xffffffffu, mine) >> quad) & 0xFu;
+    int src = bal ? (__ffs(bal) - 1) : 0;
+    int my_e = e_star;
+    if (__any_sync(0xffffffffu, bal == 0u && S > 0.f)) {
+        // rounding left no crossing in some quad: there, the last id with mass
+        int lz = -1;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (ex2(fmaf(z[e], scale2, -mref)) > 0.f) lz = e;
+        const unsigned nzb = (__ballot_sync(0xffffffffu, lz >= 0) >> quad) & 0xFu;
+        if (!bal) {
+            src = nzb ? 31 - __clz(nzb) : 0;
+            my_e = max(lz, 0);
+        }
+    }
+    float zsel = z[0];
+#pragma unroll
+    for (int e = 1; e < 8; ++e)
+        if (my_e == e) zsel = z[e];
+    const int e_src = __shfl_sync(0xffffffffu, my_e, src, 4);
+    const float z_src = __shfl_sync(0xffffffffu, zsel, src, 4);
+    if (!(S > 0.f)) return make_float4(-CUDART_INF_F, -CUDART_INF_F, __int_as_float(-1), 0.f);
+    const float lmass = (m2 + lg2(S)) * kLn2;
+    return make_float4(lmass - lnE, lmass, __int_as_float(id0 - 8 * tq + 8 * src + e_src), z_src);
+}
+
+template <int KS, bool GREEDY, bool W2SMEM, bool FULL>
+__device__ __forceinline__ void produce_cg(const uint16_t* stage, const uint16_t* w1rows, int w1stride,
+                                           const uint16_t* W2, const uint4* w2s, int V, int tile, float4* crec,
+                                           float scale2, const float* lnEt, const float* urow, int nv) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, tq = lane & 3;
+    const int tile0 = tile * kTS;
+    const uint16_t* w1a = w1rows + g * w1stride;
+    const uint16_t* w1b = w1rows + (g + 8) * w1stride;
+    const uint16_t* srowA = stage + g * kStageRow;
+    const uint16_t* srowB = stage + (g + 8) * kStageRow;
+    // rows past the valid ones compute on stale data and are never reduced: clamp their table reads
+    const int ga = min(g, nv - 1), gb = min(g + 8, nv - 1);
+    float uA = 0.f, uB = 0.f;
+    if constexpr (!GREEDY) {
+        uA = urow[ga];
+        uB = urow[gb];
+    }
+#pragma unroll 1
+    for (int k = 0; k < kChunksPerWarp; ++k) {
+        const int c = warp + kWarps * k;
+        const int cb = tile0 + kCS * c;
+        if (!FULL && cb >= V) {
+            if (tq == 0) {
+                const float4 e = GREEDY ? make_float4(-CUDART_INF_F, CUDART_NAN_F, __int_as_float(0x7fffffff), -CUDART_INF_F)
+                                        : make_float4(-CUDART_INF_F, -CUDART_INF_F, __int_as_float(-1), 0.f);
+                crec[g * kChunks + c] = e;
+                crec[(g + 8) * kChunks + c] = e;
+            }
+            continue;
+        }
+        float xa[8], xb[8];
+        load_staged8(srowA, kCS * c + 8 * tq, tile0, V, FULL, xa);
+        load_staged8(srowB, kCS * c + 8 * tq, tile0, V, FULL, xb);
+        mma_chunk_rows<KS, W2SMEM>(xa, xb, w1a, w1b, W2, w2s, tile0, c, V, g, tq, FULL);
+        float4 ra, rbk;
+        if constexpr (GREEDY) {
+            const float2 sa = chunk_stats(xa, cb + 8 * tq, 1);
+            const float2 sb = chunk_stats(xb, cb + 8 * tq, 1);
+            ra = make_float4(sa.x, CUDART_NAN_F, sa.y, sa.x);
+            rbk = make_float4(sb.x, CUDART_NAN_F, sb.y, sb.x);
+        } else {
+            ra = chunk_record_cg(xa, cb + 8 * tq, scale2, lnEt[ga * kChunks + c], uA);
+            rbk = chunk_record_cg(xb, cb + 8 * tq, scale2, lnEt[gb * kChunks + c], uB);
+        }
+        if (tq == 0) {
+            crec[g * kChunks + c] = ra;
+            crec[(g + 8) * kChunks + c] = rbk;
+        }
+    }
+}
+
+// A row's tile record from its 32 chunk records (one warp, lane = chunk): the highest key
+// (lowest chunk on ties) with its candidate and z; T > 0 also the tile's log-mass.
+__device__ __forceinline__ float4 reduce_row_chunks(const float4* crow, bool greedy) {
+    const int lane = threadIdx.x & 31;
+    const float4 q = crow[lane];
+    float key = q.x;
+    int who = lane;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const float ok = __shfl_xor_sync(0xffffffffu, key, o);
+        const int ow = __shfl_xor_sync(0xffffffffu, who, o);
+        if (ok > key || (ok == key && ow < who)) {
+            key = ok;
+            who = ow;
+        }
+    }
+    const float cand = __shfl_sync(0xffffffffu, q.z, who);
+    const float zv = __shfl_sync(0xffffffffu, q.w, who);
+    if (greedy) return make_float4(key, CUDART_NAN_F, cand, zv);
+    const float mt = warp_max(q.y);
+    float lm = -CUDART_INF_F;
+    if (mt != -CUDART_INF_F) {
+        const float sum = warp_sum(q.y == -CUDART_INF_F ? 0.f : ex2((q.y - mt) * kLog2e));
+        lm = mt + lg2(sum) * kLn2;
+    }
+    return make_float4(key, lm, cand, zv);
 }
 
 // Tile record of one staged row (one warp).  Greedy: from the chunk statistics alone.  T > 0:
@@ -706,6 +911,62 @@ __device__ __forceinline__ float4 finalize_staged(const uint16_t* srow, float2 c
     const bool ok = first != 0x7fffffff;
     (void)g;
     return make_float4(lmass - lnE, lmass, __int_as_float(ok ? first : lastnz), ok ? vfirst : vlast);
+}
+
+// --------------------------------------------------------------------------------------------
+// Tile record of one row under the chunk-Gumbel contract (one warp, lane = chunk) from its 32
+// chunk statistics and its buffered z values xrow (weights 2^(x * lscale)):
+// {max over chunks of LSE_c - ln E_c, the tile's log-mass, the candidate of the winning chunk by
+// the in-chunk inverse CDF of u, z at it}; greedy: {max, NaN, argmax id, max}.  The chunk
+// variates are drawn here (one Philox call per lane, draw n = global chunk index).
+// --------------------------------------------------------------------------------------------
+__device__ __forceinline__ float4 finalize_tile_cg(const float* xrow, float2 cs, int tile, int V, int greedy,
+                                                   float lscale, float u, uint64_t seed, uint32_t j, uint32_t i) {
+    const int lane = threadIdx.x & 31;
+    const int tile0 = tile * kTS;
+    const bool valid = tile0 + kCS * lane < V;
+    if (greedy) {
+        float m = valid ? cs.x : -CUDART_INF_F;
+        int idx = valid ? __float_as_int(cs.y) : 0x7fffffff;
+        warp_argmax(m, idx);
+        return make_float4(m, CUDART_NAN_F, __int_as_float(idx), m);
+    }
+    const float mc = valid ? cs.x : -CUDART_INF_F;
+    const float sc = valid ? cs.y : 0.f;
+    const float lnE = log_neg_log_u(uniform(seed, j, i, DSPARK_P_SAMPLE_CHUNK, (uint32_t)(tile * kChunks + lane)));
+    float key = (sc > 0.f) ? (mc + lg2(sc)) * kLn2 - lnE : -CUDART_INF_F;
+    int who = lane;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const float ok = __shfl_xor_sync(0xffffffffu, key, o);
+        const int ow = __shfl_xor_sync(0xffffffffu, who, o);
+        if (ok > key || (ok == key && ow < who)) {
+            key = ok;
+            who = ow;
+        }
+    }
+    const float mt = warp_max(mc);
+    if (mt == -CUDART_INF_F || key == -CUDART_INF_F)
+        return make_float4(-CUDART_INF_F, -CUDART_INF_F, __int_as_float(-1), 0.f);
+    const float St = warp_sum((sc > 0.f) ? sc * ex2(mc - mt) : 0.f);
+    const float lmass = (mt + lg2(St)) * kLn2;
+    // id by u inside chunk `who` (masses relative to its own maximum)
+    const float mcs = __shfl_sync(0xffffffffu, mc, who);
+    const int vl = kCS * who + lane;
+    const float xv = xrow[vl];
+    const float e = (tile0 + vl < V) ? ex2(xv * lscale - mcs) : 0.f;
+    const float Q = warp_incl_scan(e);
+    const float Sc = __shfl_sync(0xffffffffu, Q, 31);
+    const unsigned hit = __ballot_sync(0xffffffffu, Q > u * Sc);
+    int xl;
+    if (hit) {
+        xl = __ffs(hit) - 1;
+    } else {
+        const unsigned nz = __ballot_sync(0xffffffffu, e > 0.f);
+        xl = nz ? 31 - __clz(nz) : 0;
+    }
+    const float zv = __shfl_sync(0xffffffffu, xv, xl);
+    return make_float4(key, lmass, __int_as_float(tile0 + kCS * who + xl), zv);
 }
 
 // --------------------------------------------------------------------------------------------

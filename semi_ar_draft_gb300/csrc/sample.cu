@@ -31,7 +31,9 @@
 namespace dspark {
 namespace {
 
-constexpr int kMaxStagedTiles = 160;  // tiles a request's log-masses are reduced over by one warp
+constexpr int kMaxStagedTiles = 160;
+constexpr int kSlotStride = 16;   // 64-bit words between two requests' maxima
+constexpr int kCountStride = 32;  // 32-bit words between two row blocks' arrival counters  // tiles a request's log-masses are reduced over by one warp
 
 struct SampleArgs {
     int B, gamma, V, r, nt, G;
@@ -48,7 +50,9 @@ struct SampleArgs {
     WsHeader* hdr;
     int32_t* cur_tok;
     float4* part;  // [3][B][nt] tile records, by step mod 2 (general kernel) or mod 3 (staged kernel)
-    unsigned long long* slots;  // [gamma][B] packed (key, id) maxima of the staged kernel; zeroed per call
+    unsigned long long* slots;  // [gamma][B] packed (key, id) maxima of the staged kernel, kSlotStride words
+                                // apart (one 128-byte line each, so the atomics spread over L2); zeroed per call
+    unsigned* rb_count;         // [nrb] grid-wide arrival counters per row block (staged kernel), kCountStride apart
     int w1_l2;                  // staged kernel: pull W1 rows of each tile into L2 at the start
     uint64_t limit_ns;
     int redundant;  // every block reduces every request (one grid-wide wait per step)
@@ -67,16 +71,12 @@ size_t sample_smem_bytes(int B, int r, bool mma, bool w2_smem) {
     return b;
 }
 
-// The step's random draws of every request that do not depend on the drafted tokens:
-// (u1, u2) of SAMPLE_INTILE (one Philox call, words 0 and 1) and ln E of this block's first tile.
+// The step's in-chunk uniform of every request (SAMPLE_INCHUNK, draw 0), in .y; the chunk
+// variates are drawn in the finalize.
 __device__ void step_randoms(const SampleArgs& a, int step, float4* rnd) {
     const uint32_t i = (uint32_t)step + 1u;
-    for (int j = threadIdx.x; j < a.B; j += kThreads) {
-        const uint4 w = philox10(make_uint4(0u, i, (uint32_t)j, DSPARK_P_SAMPLE_INTILE), (uint32_t)a.seed,
-                                 (uint32_t)(a.seed >> 32));
-        const float lnE = log_neg_log_u(uniform(a.seed, (uint32_t)j, i, DSPARK_P_SAMPLE_TILE, blockIdx.x));
-        rnd[j] = make_float4(u01(w.x), u01(w.y), lnE, 0.f);
-    }
+    for (int j = threadIdx.x; j < a.B; j += kThreads)
+        rnd[j] = make_float4(0.f, uniform(a.seed, (uint32_t)j, i, DSPARK_P_SAMPLE_INCHUNK, 0u), 0.f, 0.f);
 }
 
 // L2 prefetch of the base rows of row block [row0, row0 + 16) at `step` over this block's tile.
@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(SampleArgs a) {
     if constexpr (kMMA) {
         if (a.w2_smem) {
             stage_w2_tile<KS>(reinterpret_cast<const uint16_t*>(a.W2), blockIdx.x * kTS, a.V,
-                              reinterpret_cast<uint4*>(wreg));
+                              reinterpret_cast<uint4*>(wreg), kThreads);
             pa.w2s = reinterpret_cast<const uint4*>(wreg);
         }
     }
@@ -149,10 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(SampleArgs a) {
                     rb->mode[tid] = ok ? ROW_SAMPLE : ROW_OFF;
                     rb->brow[tid] = ok ? ((long long)j * a.gamma + step) * (long long)a.V : -1;
                     rb->trow[tid] = -1;
-                    float4 q = ok && !a.greedy ? rnd[j] : make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (ok && !a.greedy && tile != blockIdx.x)  // blocks owning several tiles: per-tile variate
-                        q.z = log_neg_log_u(uniform(a.seed, (uint32_t)j, (uint32_t)step + 1u, DSPARK_P_SAMPLE_TILE,
-                                                    (uint32_t)tile));
+                    const float4 q = ok && !a.greedy ? rnd[j] : make_float4(0.f, 0.f, 0.f, 0.f);
                     rb->u1[tid] = q.x;
                     rb->u2[tid] = q.y;
                     rb->lnE[tid] = q.z;
@@ -188,8 +185,9 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(SampleArgs a) {
                 for (int rl = warp; rl < kRows; rl += kWarps) {
                     const int j = row0 + rl;
                     if (j >= a.B) continue;
-                    const float4 rec = finalize_tile(xbuf + rl * kXRow, cstat[rl * kChunks + lane], tile, a.V,
-                                                     GREEDY, a.scale2, rb->u1[rl], rb->u2[rl], rb->lnE[rl]);
+                    const float4 rec = finalize_tile_cg(xbuf + rl * kXRow, cstat[rl * kChunks + lane], tile, a.V,
+                                                        GREEDY, a.scale2, rb->u2[rl], a.seed, (uint32_t)j,
+                                                        (uint32_t)step + 1u);
                     if (lane == 0) part[(size_t)j * a.nt + tile] = rec;
                 }
                 __syncthreads();
@@ -263,8 +261,13 @@ using KernelFnS = void (*)(SampleArgs);
 //     (records in three rotating buffers, so none is rewritten before its owner read it).
 // ------------------------------------------------------------------------------------------
 struct StagedLayout {
-    size_t stage, w1s, cstat, prev, rnd, bars, w2s, total;
+    size_t stage, w1s, crec, prev, urow, lnEt, bars, w2s, total;
+    int lnE_rows;  // rows of the chunk-variate table: B (filled once per step) or 16 (per row block)
 };
+
+constexpr int kStepTableRows = 64;             // up to this many requests the per-step variate table is kept
+constexpr int kHelperWarps = 4;                         // copy issuer, arriver, two exchangers
+constexpr int kStagedThreads = kThreads + 32 * kHelperWarps;
 
 __host__ __device__ inline StagedLayout staged_layout(int B, int r, bool w2_smem) {
     StagedLayout L;
@@ -273,22 +276,21 @@ __host__ __device__ inline StagedLayout staged_layout(int B, int r, bool w2_smem
     o += sizeof(uint16_t) * 2 * kRows * kStageRow;
     L.w1s = o;
     o += align_up(sizeof(uint16_t) * 2 * kRows * (size_t)(r + 8), 16);
-    L.cstat = o;
-    o += sizeof(float2) * kRows * kChunks;
+    L.crec = o;
+    o += sizeof(float4) * 2 * kRows * kChunks;
     L.prev = o;
-    o += align_up(sizeof(int) * (size_t)B, 16);
-    L.rnd = o;
-    o += sizeof(float4) * (size_t)B;
+    o += align_up(sizeof(int) * 2 * (size_t)B, 16);
+    L.lnE_rows = B <= kStepTableRows ? B : kRows;
+    L.urow = o;
+    o += align_up(sizeof(float) * (size_t)B, 16);
+    L.lnEt = o;
+    o += sizeof(float) * kChunks * (size_t)L.lnE_rows;
     L.bars = o;
-    o += 16;
+    o += 64;  // full[2], empty[2]; flags: abort, ok, reduced count, bases issued, W1 rows done [2]
     L.w2s = o;
     if (w2_smem) o += (size_t)kTS * r * 2;
     L.total = o;
     return L;
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void red_max_u64(unsigned long long* p, unsigned long long v) {
@@ -306,43 +308,169 @@ __device__ __forceinline__ float unpack_key(unsigned long long w) {
     return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
 }
 
-// Base rows of row block `cnt` (step cnt / nrb) over this block's tile (warp 0): the bytes are
-// announced without an arrival; issue_w1() adds the arrival.
+// Base rows of row block `cnt` (step cnt / nrb) over this block's tile (one warp): one of the two
+// arrivals of the buffer's full barrier, with the bytes; load_w1_rows() gives the other.
 __device__ __forceinline__ void issue_base(const SampleArgs& a, int cnt, int nrb, uint16_t* dst, uint64_t* bar) {
     const int lane = threadIdx.x & 31;
     const int step = cnt / nrb, row0 = (cnt % nrb) * kRows;
     const int tile0 = blockIdx.x * kTS;
     const int nvalid = min(kTS, a.V - tile0);
     const int nrows = min(kRows, a.B - row0);
-    if (lane == 0) mbar_expect_tx(bar, (uint32_t)(nrows * nvalid * 2));
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nrows * nvalid * 2));
     __syncwarp();
     if (lane < nrows) {
         const __nv_bfloat16* src =
             reinterpret_cast<const __nv_bfloat16*>(a.base) + ((size_t)(row0 + lane) * a.gamma + step) * (size_t)a.V + tile0;
-        bulk_g2s(dst + (size_t)lane * kStageRow, src, (uint32_t)(nvalid * 2), bar);
+        bulk_g2s_hint(dst + (size_t)lane * kStageRow, src, (uint32_t)(nvalid * 2), bar, l2_policy_evict_first());
     }
 }
 
-// W1 rows of the previous tokens of rows row0 .. row0 + 15 (warp 0; rows past B repeat row0).
-__device__ __forceinline__ void issue_w1(const SampleArgs& a, int row0, const int* prev, uint16_t* dst, uint64_t* bar) {
+// W1 rows of the previous tokens of row block `cnt` (rows past B repeat its first row) into its
+// stage buffer with plain loads by one warp: a batch of loads is in flight before its stores.
+template <int KS>
+__device__ void load_w1_rows(const SampleArgs& a, int cnt, int nrb, const int* toks, uint16_t* w1s) {
+    constexpr int r = 16 * KS, w1st = r + 8, units = r / 8, per_rb = kRows * units, kBatch = 8;
     const int lane = threadIdx.x & 31;
-    const uint32_t rowb = (uint32_t)a.r * 2u;
-    if (lane == 0) mbar_arrive_expect_tx(bar, kRows * rowb);
-    __syncwarp();
-    if (lane < kRows) {
-        const int j = row0 + lane;
-        const int tok = prev[j < a.B ? j : row0];
-        bulk_g2s(dst + (size_t)lane * (a.r + 8), reinterpret_cast<const uint16_t*>(a.W1) + (size_t)tok * a.r, rowb, bar);
+    const uint4* W1 = reinterpret_cast<const uint4*>(a.W1);
+    const int row0 = (cnt % nrb) * kRows;
+    uint4* dst = reinterpret_cast<uint4*>(w1s + (size_t)(cnt & 1) * kRows * w1st);
+    for (int b0 = 0; b0 < per_rb; b0 += 32 * kBatch) {
+        uint4 v[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const int idx = b0 + k * 32 + lane, row = idx / units, u = idx % units, j = row0 + row;
+            if (idx < per_rb) v[k] = __ldg(W1 + (size_t)toks[j < a.B ? j : row0] * units + u);
+        }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const int idx = b0 + k * 32 + lane, row = idx / units, u = idx % units;
+            if (idx < per_rb) dst[(size_t)row * (w1st / 8) + u] = v[k];
+        }
     }
 }
 
-// LSE(z/T) and z at the token of step s for the requests this block owns (a warp per request).
-__device__ void owner_lse(const SampleArgs& a, int s, const int* prev) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+__device__ __forceinline__ void st_release_cta(volatile int* p, int v) {
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_addr((const void*)p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_cta(volatile int* p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr((const void*)p)) : "memory");
+    return v;
+}
+
+// In-chunk uniforms of every request for `step` (SAMPLE_INCHUNK, draw 0).
+__device__ void step_uniforms(const SampleArgs& a, int step, float* urow, int nthreads, int t0) {
+    for (int j = t0; j < a.B; j += nthreads)
+        urow[j] = uniform(a.seed, (uint32_t)j, (uint32_t)step + 1u, DSPARK_P_SAMPLE_INCHUNK, 0u);
+}
+
+// ln E_c of this block's 32 chunks for requests row0 .. row0 + nrows - 1 at `step`: one Philox
+// call gives the four chunks 4q .. 4q + 3 (draws n = global chunk index).
+__device__ void chunk_variates(const SampleArgs& a, int step, int row0, int nrows, float* table, int nthreads,
+                               int t0) {
+    const uint32_t i = (uint32_t)step + 1u;
+    for (int idx = t0; idx < nrows * (kChunks / 4); idx += nthreads) {
+        const int rl = idx / (kChunks / 4), q = idx % (kChunks / 4);
+        const uint32_t j = (uint32_t)(row0 + rl);
+        const uint4 w = philox10(make_uint4(blockIdx.x * (kChunks / 4) + (uint32_t)q, i, j, DSPARK_P_SAMPLE_CHUNK),
+                                 (uint32_t)a.seed, (uint32_t)(a.seed >> 32));
+        float4 v;
+        v.x = log_neg_log_u(u01(w.x));
+        v.y = log_neg_log_u(u01(w.y));
+        v.z = log_neg_log_u(u01(w.z));
+        v.w = log_neg_log_u(u01(w.w));
+        reinterpret_cast<float4*>(table + (size_t)rl * kChunks)[q] = v;
+    }
+}
+
+// Helper warps of the staged kernel.  Waits are bounded (a.limit_ns without progress) and
+// give up once the block's abort flag is raised; lane 0 decides, the warp follows.
+__device__ __forceinline__ bool helper_should_stop(volatile int* abort, uint64_t t0, const SampleArgs& a) {
+    int stop = 0;
+    if ((threadIdx.x & 31) == 0) {
+        if (*abort) {
+            stop = 1;
+        } else if (global_ns() - t0 > a.limit_ns) {
+            record_status(&a.hdr->status, DSPARK_ERR_TIMEOUT);
+            *abort = 1;
+            stop = 1;
+        }
+    }
+    return __shfl_sync(0xffffffffu, stop, 0) != 0;
+}
+
+// Copy issuer: the W1 rows of this tile into L2 (kept there), then the base rows of every row
+// block as soon as its stage buffer is released (two row blocks ahead of the compute warps).
+template <int KS>
+__device__ void copy_issuer(const SampleArgs& a, uint16_t* stage, uint64_t* full, uint64_t* empty,
+                            volatile int* abort, volatile int* nb_out) {
+    const int lane = threadIdx.x & 31;
+    const int nrb = (a.B + kRows - 1) / kRows, total = a.gamma * nrb;
+    if (a.w1_l2) {
+        const int tile0 = blockIdx.x * kTS;
+        const uint32_t bytes = (uint32_t)min(kTS, a.V - tile0) * (uint32_t)(16 * KS) * 2u;
+        const unsigned char* w1 = reinterpret_cast<const unsigned char*>(a.W1) + (size_t)tile0 * (16 * KS) * 2;
+        for (uint32_t off = (uint32_t)lane * 4096u; off < bytes; off += 32u * 4096u)
+            prefetch_l2_hint(w1 + off, min(4096u, bytes - off), l2_policy_evict_last());
+    }
+    for (int nb = 0; nb < total; ++nb) {
+        if (nb >= 2) {
+            const uint64_t t0 = global_ns();
+            bool ok = false;
+            while (true) {
+                int done = lane == 0 ? (int)mbar_try_wait(&empty[nb & 1], (uint32_t)(((nb - 2) >> 1) & 1)) : 0;
+                if (__shfl_sync(0xffffffffu, done, 0)) {
+                    ok = true;
+                    break;
+                }
+                if (helper_should_stop(abort, t0, a)) break;
+            }
+            if (!ok) return;
+        }
+        issue_base(a, nb, nrb, stage + (size_t)(nb & 1) * kRows * kStageRow, &full[nb & 1]);
+        if (lane == 0) *nb_out = nb + 1;
+        __syncwarp();
+    }
+}
+
+// Arriver: once the compute warps have issued a row block's maxima, one release-arrival on that
+// row block's grid-wide counter (the release waits for the maxima to be performed in L2: that
+// wait happens here, not in the compute warps).
+__device__ void arriver(const SampleArgs& a, volatile int* reduced, volatile int* abort) {
+    const int lane = threadIdx.x & 31;
+    const int nrb = (a.B + kRows - 1) / kRows, total = a.gamma * nrb;
+    for (int cnt = 0; cnt < total; ++cnt) {
+        const uint64_t t0 = global_ns();
+        bool ok = false;
+        while (true) {
+            int done = lane == 0 ? (ld_acquire_cta(reduced) > cnt ? 1 : 0) : 0;
+            if (__shfl_sync(0xffffffffu, done, 0)) {
+                ok = true;
+                break;
+            }
+            if (helper_should_stop(abort, t0, a)) break;
+        }
+        if (!ok) return;
+        if (lane == 0)
+            asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.rb_count + (size_t)(cnt % nrb) * kCountStride)
+                         : "memory");
+        __syncwarp();
+    }
+}
+
+// Exchanger `par` (0 or 1) serves the row blocks whose index has that parity: for each of their
+// row blocks of step st >= 1 it waits until every block has arrived for (st - 1, row block),
+// turns the packed maxima into the tokens (the owner writes them out), then loads the W1 rows
+// of those tokens into the row block's stage buffer and gives its second arrival.  After the
+// last step it collects that step's tokens too.
+// The LSE(z/T) and z at the token of step s for the requests of row block rbi this block owns
+// (one warp; T > 0).  Runs once every block has arrived for (s, rbi): the records are complete.
+__device__ void owner_lse_rb(const SampleArgs& a, int s, int rbi, const int* toks) {
+    const int lane = threadIdx.x & 31;
     const float4* part = a.part + (size_t)(s % 3) * a.B * a.nt;
-    for (int k = warp;; k += kWarps) {
-        const int j = blockIdx.x + a.G * k;
-        if (j >= a.B) break;
+    const int row0 = rbi * kRows, row1 = min(a.B, row0 + kRows);
+    int j = row0 + (((int)blockIdx.x - row0) % a.G + a.G) % a.G;  // first row >= row0 owned here
+    for (; j < row1; j += a.G) {
         const float4* rec = part + (size_t)j * a.nt;
         float y[kMaxStagedTiles / 32];
         float m = -CUDART_INF_F;
@@ -365,36 +493,125 @@ __device__ void owner_lse(const SampleArgs& a, int s, const int* prev) {
         if (lane == 0) {
             const size_t o = (size_t)j * a.gamma + s;
             a.draft_lse[o] = lse;
-            a.zat[o] = __ldcg(&rec[prev[j] / kTS].w);
+            a.zat[o] = __ldcg(&rec[toks[j] / kTS].w);
         }
     }
 }
 
+template <int KS>
+__device__ void exchanger(const SampleArgs& a, int par, int* prev, uint16_t* w1s, uint64_t* full, uint64_t* empty,
+                          volatile int* abort, volatile int* w1_upto) {
+    const int lane = threadIdx.x & 31;
+    const int nrb = (a.B + kRows - 1) / kRows, total = a.gamma * nrb;
+    auto collect = [&](int rbi, int st) -> bool {  // tokens of step st - 1, row block rbi
+        const uint64_t t0 = global_ns();
+        const unsigned* cnt_p = a.rb_count + (size_t)rbi * kCountStride;
+        while (true) {
+            int st_ok = 0;
+            if (lane == 0) {
+                st_ok = ld_acquire_u32(cnt_p) >= (uint32_t)a.G * (uint32_t)st ? 1 : 0;
+                if (!st_ok && ld_relaxed_s32(&a.hdr->status) == DSPARK_ERR_TIMEOUT) {
+                    *abort = 1;
+                    st_ok = -1;
+                }
+            }
+            st_ok = __shfl_sync(0xffffffffu, st_ok, 0);
+            if (st_ok > 0) break;
+            if (st_ok < 0 || helper_should_stop(abort, t0, a)) return false;
+        }
+        __syncwarp();
+        const int row0 = rbi * kRows, nv = min(kRows, a.B - row0);
+        const unsigned long long* slot = a.slots + (size_t)(st - 1) * a.B * kSlotStride;
+        int* nxt = prev + (size_t)(st & 1) * a.B;
+        if (lane < nv) {
+            const int j = row0 + lane;
+            const unsigned long long w = __ldcg(slot + (size_t)j * kSlotStride);
+            const int cand = ~(int)(uint32_t)w;
+            int p = cand;
+            if (p < 0 || p >= a.V) {  // a row whose chunks all had no mass
+                record_status(&a.hdr->status, DSPARK_ERR_TOKEN_RANGE);
+                p = min(max(p, 0), a.V - 1);
+            }
+            nxt[j] = p;
+            if (j % a.G == (int)blockIdx.x) {
+                const size_t o = (size_t)j * a.gamma + (st - 1);
+                a.tokens[o] = cand;
+                if (a.greedy) {
+                    a.draft_lse[o] = CUDART_NAN_F;
+                    a.zat[o] = unpack_key(w);
+                }
+            }
+        }
+        __syncwarp();
+        return true;
+    };
+    for (int cnt = 0; cnt < total; ++cnt) {
+        const int rbi = cnt % nrb, st = cnt / nrb;
+        if ((rbi & 1) != par) continue;
+        if (st > 0 && !collect(rbi, st)) return;
+        if (cnt >= 2) {  // the stage buffer's W1 rows were read by row block cnt - 2
+            const uint64_t t0 = global_ns();
+            bool ok = false;
+            while (true) {
+                int done = lane == 0 ? (int)mbar_try_wait(&empty[cnt & 1], (uint32_t)(((cnt - 2) >> 1) & 1)) : 0;
+                if (__shfl_sync(0xffffffffu, done, 0)) {
+                    ok = true;
+                    break;
+                }
+                if (helper_should_stop(abort, t0, a)) break;
+            }
+            if (!ok) return;
+        }
+        load_w1_rows<KS>(a, cnt, nrb, prev + (size_t)(st & 1) * a.B, w1s);
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive_local(&full[cnt & 1]);  // release: the W1 rows above are visible to its waiters
+            *w1_upto = cnt + 1;
+        }
+        __syncwarp();
+        if (!a.greedy && st > 0) owner_lse_rb(a, st - 1, rbi, prev + (size_t)(st & 1) * a.B);
+    }
+    for (int rbi = par; rbi < nrb; rbi += 2) {
+        if (!collect(rbi, a.gamma)) return;
+        if (!a.greedy) owner_lse_rb(a, a.gamma - 1, rbi, prev + (size_t)(a.gamma & 1) * a.B);
+    }
+}
+
 template <int KS, bool GREEDY>
-__global__ void __launch_bounds__(kThreads, 1) sample_staged_kernel(SampleArgs a) {
+__global__ void __launch_bounds__(kStagedThreads, 1) sample_staged_kernel(SampleArgs a) {
     constexpr int r = 16 * KS, w1st = r + 8;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const StagedLayout L = staged_layout(a.B, r, a.w2_smem);
     uint16_t* stage = reinterpret_cast<uint16_t*>(smem_raw + L.stage);  // [2][kRows][kStageRow] bf16 bits
     uint16_t* w1s = reinterpret_cast<uint16_t*>(smem_raw + L.w1s);      // [2][kRows][w1st]
-    float2* cstat = reinterpret_cast<float2*>(smem_raw + L.cstat);      // [kRows][kChunks]
-    int* prev = reinterpret_cast<int*>(smem_raw + L.prev);              // [B] previous tokens
-    float4* rnd = reinterpret_cast<float4*>(smem_raw + L.rnd);          // [B] (u1, u2, ln E)
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + L.bars);
+    float4* crec = reinterpret_cast<float4*>(smem_raw + L.crec);        // [2][kRows][kChunks] chunk records
+    int* prev = reinterpret_cast<int*>(smem_raw + L.prev);              // [2][B]: tokens feeding step s at s & 1
+    float* urow = reinterpret_cast<float*>(smem_raw + L.urow);          // [B] in-chunk uniforms
+    float* lnEt = reinterpret_cast<float*>(smem_raw + L.lnEt);          // [lnE_rows][kChunks]
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + L.bars);    // [2] stage buffer filled (2 arrivals)
+    uint64_t* empty = full + 2;                                         // [2] stage buffer released
+    volatile int* flags = reinterpret_cast<volatile int*>(full + 4);
+    volatile int* abort = flags + 0;
+    volatile int* s_ok = flags + 1;
+    volatile int* reduced = flags + 2;  // row blocks whose maxima the compute warps have issued
+    volatile int* nb_issued = flags + 3;
+    volatile int* w1_upto = flags + 4;  // [2]: per exchanger, row blocks whose W1 rows are in
     uint4* w2s = reinterpret_cast<uint4*>(smem_raw + L.w2s);
-    __shared__ int s_ok;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tile = blockIdx.x, tile0 = tile * kTS;
-    const bool full = tile0 + kTS <= a.V;
-    const int nrb = (a.B + kRows - 1) / kRows;
-    const int total = a.gamma * nrb;
+    const bool full_tile = tile0 + kTS <= a.V;
+    const int nrb = (a.B + kRows - 1) / kRows, total = a.gamma * nrb;
+    const bool step_table = L.lnE_rows == a.B;
     const uint16_t* W2 = reinterpret_cast<const uint16_t*>(a.W2);
     if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&full[b], 2);
+            mbar_init(&empty[b], 1);
+        }
+        for (int f = 0; f < 6; ++f) flags[f] = 0;
         mbar_init_fence();
     }
-    for (int j = tid; j < a.B; j += kThreads) {
+    for (int j = tid; j < a.B; j += kStagedThreads) {
         int p = a.anchor[j];
         if (p < 0 || p >= a.V) {
             record_status(&a.hdr->status, DSPARK_ERR_TOKEN_RANGE);
@@ -403,98 +620,83 @@ __global__ void __launch_bounds__(kThreads, 1) sample_staged_kernel(SampleArgs a
         prev[j] = p;
     }
     __syncthreads();
-    if (warp == 0) {
-        issue_base(a, 0, nrb, stage, &bars[0]);
-        issue_w1(a, 0, prev, w1s, &bars[0]);
-    } else if (warp == 1 && a.w1_l2) {  // W1 rows of this tile into L2: later gathers hit there
-        const uint32_t bytes = (uint32_t)min(kTS, a.V - tile0) * (uint32_t)r * 2u;
-        const unsigned char* w1 = reinterpret_cast<const unsigned char*>(a.W1) + (size_t)tile0 * r * 2;
-        for (uint32_t off = (uint32_t)lane * 4096u; off < bytes; off += 32u * 4096u)
-            prefetch_l2(w1 + off, min(4096u, bytes - off));
-    }
-    if (a.w2_smem) stage_w2_tile<KS>(W2, tile0, a.V, w2s);
-    if (!GREEDY) step_randoms(a, 0, rnd);
-
-    uint32_t target = 0;
-    int cnt = 0;
-    for (int step = 0; step < a.gamma; ++step) {
-        float4* part = a.part + (size_t)(step % 3) * a.B * a.nt;
-        unsigned long long* slot = a.slots + (size_t)step * a.B;
-        for (int rbi = 0; rbi < nrb; ++rbi, ++cnt) {
-            const int buf = cnt & 1, row0 = rbi * kRows;
-            const uint32_t par = (uint32_t)((cnt >> 1) & 1);
-            if (tid == 0) s_ok = mbar_wait_bounded(&bars[buf], par, &a.hdr->status, a.limit_ns);
-            __syncthreads();
-            if (!s_ok) return;  // the copy engine did not deliver in time (status recorded); nothing else in flight
-            mbar_try_wait(&bars[buf], par);  // completed: acquire for this thread
-            if (warp == 0 && cnt + 1 < total) {  // the other buffer was released at the end of the last row block
-                uint64_t* nbar = &bars[buf ^ 1];
-                issue_base(a, cnt + 1, nrb, stage + (size_t)(buf ^ 1) * kRows * kStageRow, nbar);
-                if (rbi + 1 < nrb) issue_w1(a, row0 + kRows, prev, w1s + (size_t)(buf ^ 1) * kRows * w1st, nbar);
-            }
-            const uint16_t* sbuf = stage + (size_t)buf * kRows * kStageRow;
-            const uint16_t* wbuf = w1s + (size_t)buf * kRows * w1st;
-            if (a.w2_smem) {
-                if (full) produce_staged<KS, GREEDY, true, true>(sbuf, wbuf, w1st, W2, w2s, a.V, tile, cstat, a.scale2);
-                else produce_staged<KS, GREEDY, true, false>(sbuf, wbuf, w1st, W2, w2s, a.V, tile, cstat, a.scale2);
-            } else {
-                if (full) produce_staged<KS, GREEDY, false, true>(sbuf, wbuf, w1st, W2, nullptr, a.V, tile, cstat, a.scale2);
-                else produce_staged<KS, GREEDY, false, false>(sbuf, wbuf, w1st, W2, nullptr, a.V, tile, cstat, a.scale2);
-            }
-            __syncthreads();
-            for (int rl = warp; rl < kRows; rl += kWarps) {
-                const int j = row0 + rl;
-                if (j >= a.B) continue;
-                const float4 q = GREEDY ? make_float4(0.f, 0.f, 0.f, 0.f) : rnd[j];
-                float4 rec;
-                if (a.w2_smem)
-                    rec = finalize_staged<KS, GREEDY, true>(sbuf + rl * kStageRow, cstat[rl * kChunks + lane], tile,
-                                                            a.V, a.scale2, q.x, q.y, q.z, wbuf + rl * w1st, W2, w2s);
-                else
-                    rec = finalize_staged<KS, GREEDY, false>(sbuf + rl * kStageRow, cstat[rl * kChunks + lane], tile,
-                                                             a.V, a.scale2, q.x, q.y, q.z, wbuf + rl * w1st, W2,
-                                                             nullptr);
-                if (lane == 0) {
-                    if (!GREEDY) part[(size_t)j * a.nt + tile] = rec;
-                    red_max_u64(slot + j, pack_key(rec.x, __float_as_int(rec.z)));
+    if (warp == kWarps) {
+        copy_issuer<KS>(a, stage, full, empty, abort, nb_issued);
+    } else if (warp == kWarps + 1) {
+        arriver(a, reduced, abort);
+    } else if (warp >= kWarps + 2) {
+        exchanger<KS>(a, warp - kWarps - 2, prev, w1s, full, empty, abort, w1_upto + (warp - kWarps - 2));
+    } else {
+        if (a.w2_smem) stage_w2_tile_async<KS>(W2, tile0, a.V, w2s, kThreads);
+        if (!GREEDY && step_table) {  // step 0's draws for every request
+            step_uniforms(a, 0, urow, kThreads, tid);
+            chunk_variates(a, 0, 0, a.B, lnEt, kThreads, tid);
+        }
+        if (a.w2_smem) cp_async_wait_all();
+        named_barrier(1, kThreads);
+        int cnt = 0;
+        bool live = true;
+        for (int step = 0; step < a.gamma && live; ++step) {
+            float4* part = a.part + (size_t)(step % 3) * a.B * a.nt;
+            unsigned long long* slot = a.slots + (size_t)step * a.B * kSlotStride;
+            for (int rbi = 0; rbi < nrb; ++rbi, ++cnt) {
+                const int buf = cnt & 1, row0 = rbi * kRows;
+                const uint32_t par = (uint32_t)((cnt >> 1) & 1);
+                const int nv = min(kRows, a.B - row0);
+                if (!GREEDY && !step_table) {  // the row block's draws
+                    if (rbi == 0) step_uniforms(a, step, urow, kThreads, tid);
+                    chunk_variates(a, step, row0, nv, lnEt, kThreads, tid);
                 }
-            }
-            __syncthreads();
-        }
-        target += (uint32_t)a.G;
-        grid_arrive(a.hdr);
-        if (!GREEDY && step >= 1) owner_lse(a, step - 1, prev);
-        if (!GREEDY && step + 1 < a.gamma) step_randoms(a, step + 1, rnd);
-        if (!grid_wait_arrived(a.hdr, target, a.limit_ns)) {
-            // the next step's base rows may be in flight: arrive for them and wait (bounded)
-            if (tid == 0 && cnt < total) {
-                mbar_arrive_local(&bars[cnt & 1]);
-                mbar_wait_bounded(&bars[cnt & 1], (uint32_t)((cnt >> 1) & 1), &a.hdr->status, a.limit_ns);
-            }
-            return;
-        }
-        for (int j = tid; j < a.B; j += kThreads) {
-            const unsigned long long w = __ldcg(slot + j);
-            const int cand = ~(int)(uint32_t)w;
-            int p = cand;
-            if (p < 0 || p >= a.V) {  // a row whose tiles all had no mass
-                record_status(&a.hdr->status, DSPARK_ERR_TOKEN_RANGE);
-                p = min(max(p, 0), a.V - 1);
-            }
-            prev[j] = p;
-            if (j % a.G == (int)blockIdx.x) {
-                const size_t o = (size_t)j * a.gamma + step;
-                a.tokens[o] = cand;
-                if (GREEDY) {
-                    a.draft_lse[o] = CUDART_NAN_F;
-                    a.zat[o] = unpack_key(w);
+                if (tid == 0) *s_ok = mbar_wait_or_abort(&full[buf], par, abort, &a.hdr->status, a.limit_ns, false);
+                named_barrier(1, kThreads);
+                if (!*s_ok) {
+                    live = false;
+                    break;
                 }
+                mbar_try_wait(&full[buf], par);  // completed: acquire for this thread
+                const uint16_t* sbuf = stage + (size_t)buf * kRows * kStageRow;
+                const uint16_t* wbuf = w1s + (size_t)buf * kRows * w1st;
+                float4* cr = crec + (size_t)buf * kRows * kChunks;
+                const float* lt = lnEt + (step_table ? (size_t)row0 * kChunks : 0);
+                const float* ut = urow + row0;
+                if (a.w2_smem) {
+                    if (full_tile) produce_cg<KS, GREEDY, true, true>(sbuf, wbuf, w1st, W2, w2s, a.V, tile, cr, a.scale2, lt, ut, nv);
+                    else produce_cg<KS, GREEDY, true, false>(sbuf, wbuf, w1st, W2, w2s, a.V, tile, cr, a.scale2, lt, ut, nv);
+                } else {
+                    if (full_tile) produce_cg<KS, GREEDY, false, true>(sbuf, wbuf, w1st, W2, nullptr, a.V, tile, cr, a.scale2, lt, ut, nv);
+                    else produce_cg<KS, GREEDY, false, false>(sbuf, wbuf, w1st, W2, nullptr, a.V, tile, cr, a.scale2, lt, ut, nv);
+                }
+                named_barrier(1, kThreads);
+                if (tid == 0) mbar_arrive_local(&empty[buf]);  // stage and W1 buffer free for row block cnt + 2
+                if (warp < nv) {  // one request per warp
+                    const int j = row0 + warp;
+                    const float4 rec = reduce_row_chunks(cr + warp * kChunks, GREEDY);
+                    if (lane == 0) {
+                        if (!GREEDY) part[(size_t)j * a.nt + tile] = rec;
+                        red_max_u64(slot + (size_t)j * kSlotStride, pack_key(rec.x, __float_as_int(rec.z)));
+                    }
+                }
+                named_barrier(1, kThreads);
+                if (tid == 0) st_release_cta(reduced, cnt + 1);  // the arriver publishes this row block
+            }
+            if (!live) break;
+            if (!GREEDY && step_table && step + 1 < a.gamma) {  // the next step's draws (this step's are read)
+                step_uniforms(a, step + 1, urow, kThreads, tid);
+                chunk_variates(a, step + 1, 0, a.B, lnEt, kThreads, tid);
+                named_barrier(1, kThreads);
             }
         }
-        __syncthreads();
-        if (warp == 0 && cnt < total) issue_w1(a, 0, prev, w1s + (size_t)(cnt & 1) * kRows * w1st, &bars[cnt & 1]);
     }
-    if (!GREEDY) owner_lse(a, a.gamma - 1, prev);
+    __syncthreads();
+    if (tid == 0 && *abort) {  // the (at most two) newest row blocks' copies may still be in flight
+        const int nb = *nb_issued;
+        for (int c = max(0, nb - 2); c < nb; ++c) {
+            const int ex = (c % nrb) & 1;
+            if (w1_upto[ex] <= c) mbar_arrive_local(&full[c & 1]);  // its W1 arrival never came
+            mbar_wait_bounded(&full[c & 1], (uint32_t)((c >> 1) & 1), &a.hdr->status, a.limit_ns);
+        }
+    }
+    (void)total;
 }
 
 template <bool G>
@@ -553,8 +755,10 @@ dspark_status validate_sample_params(const dspark_sample_params* p) {
     return DSPARK_OK;
 }
 
-size_t sample_slot_bytes(const dspark_sample_params* p) {
-    return align_up(sizeof(unsigned long long) * (size_t)p->B * p->gamma, 256);
+size_t sample_slot_bytes(const dspark_sample_params* p) {  // maxima and per-row-block counters
+    const size_t nrb = (size_t)(p->B + kRows - 1) / kRows;
+    return align_up((size_t)kSlotStride * sizeof(unsigned long long) * (size_t)p->B * p->gamma, 256) +
+           align_up((size_t)kCountStride * sizeof(unsigned) * nrb, 256);
 }
 
 size_t sample_workspace_bytes(const dspark_sample_params* p) {
@@ -590,7 +794,8 @@ extern "C" dspark_status dspark_markov_sample_block(const dspark_sample_params* 
     const size_t esz = p->logits_dtype == DSPARK_BF16 ? 2 : 4;
     const bool vec_ok = ((uintptr_t)base_logits % 16 == 0) && (((size_t)p->V * esz) % 16 == 0);
     // staged path: bf16 logits, tensor-core bias, one tile per block (one block per SM)
-    bool staged = mma && p->logits_dtype == DSPARK_BF16 && vec_ok && ((uintptr_t)W1 % 16 == 0) && nt <= sms &&
+    bool staged = mma && p->logits_dtype == DSPARK_BF16 && vec_ok && ((uintptr_t)W1 % 16 == 0) &&
+                  ((uintptr_t)W2 % 16 == 0) && nt <= sms &&
                   nt <= kMaxStagedTiles;
     bool w2_staged = (size_t)kTS * p->r * 2 <= 128 * 1024;
     if (staged && staged_layout(p->B, p->r, w2_staged).total > kMaxSmem) w2_staged = false;
@@ -608,12 +813,9 @@ extern "C" dspark_status dspark_markov_sample_block(const dspark_sample_params* 
         smem = staged_layout(p->B, p->r, w2_smem).total;
     }
     if (smem > kMaxSmem) return DSPARK_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return DSPARK_ERR_CUDA;
+    const int threads = staged ? kStagedThreads : kThreads;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, (const void*)fn, kThreads, smem) != cudaSuccess ||
-        per_sm < 1)
-        return DSPARK_ERR_CUDA;
+    if (prepare_kernel((const void*)fn, smem, threads, &per_sm) != cudaSuccess || per_sm < 1) return DSPARK_ERR_CUDA;
     const int G = std::min(nt, sms * per_sm);
     if (G < nt) w2_smem = false;  // a block owning several tiles cannot keep one tile's W2
     if (staged && G < nt) return DSPARK_ERR_CUDA;  // (cannot happen: nt <= SMs and one block per SM)
@@ -638,6 +840,8 @@ extern "C" dspark_status dspark_markov_sample_block(const dspark_sample_params* 
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     a.hdr = reinterpret_cast<WsHeader*>(ws);
     a.slots = reinterpret_cast<unsigned long long*>(ws + kHeaderBytes);
+    a.rb_count = reinterpret_cast<unsigned*>(
+        ws + kHeaderBytes + align_up((size_t)kSlotStride * sizeof(unsigned long long) * (size_t)p->B * p->gamma, 256));
     a.cur_tok = reinterpret_cast<int32_t*>(ws + kHeaderBytes + sample_slot_bytes(p));
     a.part = reinterpret_cast<float4*>(ws + kHeaderBytes + sample_slot_bytes(p) +
                                        align_up(sizeof(int32_t) * (size_t)p->B, 256));
@@ -651,7 +855,7 @@ extern "C" dspark_status dspark_markov_sample_block(const dspark_sample_params* 
     if (cudaMemsetAsync(workspace, 0, kHeaderBytes + (staged ? sample_slot_bytes(p) : 0), s) != cudaSuccess)
         return DSPARK_ERR_CUDA;
     void* args[] = {&a};
-    if (cudaLaunchCooperativeKernel((const void*)fn, dim3(G), dim3(kThreads), args, smem, s) != cudaSuccess)
+    if (cudaLaunchCooperativeKernel((const void*)fn, dim3(G), dim3(threads), args, smem, s) != cudaSuccess)
         return DSPARK_ERR_CUDA;
     return DSPARK_OK;
 }

@@ -185,8 +185,8 @@ extern "C" dspark_status dspark_schedule_verify_len(int B, int gamma, const floa
     const long long bg = (long long)B * gamma;
     const int budget_c = (long long)budget > bg ? (int)bg : budget;
     const size_t smem = sizeof(uint32_t) * (size_t)bg;
-    if (cudaFuncSetAttribute((const void*)schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
+    int per_sm = 0;
+    if (prepare_kernel((const void*)schedule_kernel, smem, kSchedThreads, &per_sm) != cudaSuccess)
         return DSPARK_ERR_CUDA;
     schedule_kernel<<<1, kSchedThreads, smem, s>>>(B, gamma, conf, budget_c, verify_len, offsets, objective);
     if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;

@@ -66,19 +66,6 @@ __device__ __forceinline__ void lse_merge8(const float (&x)[8], float& m, float&
     m = mn;
 }
 
-// The same for 16 values (one rescale per 16).
-__device__ __forceinline__ void lse_merge16(const float (&x)[16], float& m, float& s) {
-    float gm = fmaxf(fmaxf(x[0], x[1]), x[2]);
-#pragma unroll
-    for (int e = 3; e < 16; e += 2) gm = fmaxf(fmaxf(gm, x[e]), e + 1 < 16 ? x[e + 1] : x[e]);
-    const float mn = fmaxf(m, gm * kLog2e);
-    if (mn == -CUDART_INF_F) return;
-    s = (m == -CUDART_INF_F) ? 0.f : s * ex2(m - mn);
-#pragma unroll
-    for (int e = 0; e < 16; ++e) s += ex2(fmaf(x[e], kLog2e, -mn));
-    m = mn;
-}
-
 __device__ __forceinline__ float2 merge_pair(float2 a, float2 b) {
     const float m = fmaxf(a.x, b.x);
     if (m == -CUDART_INF_F) return make_float2(m, 0.f);
@@ -506,32 +493,22 @@ extern "C" dspark_status dspark_accept_rate_tv(int S, int A, int gamma, int V, i
                      (uintptr_t)target_logits % 16 == 0 && V >= 16;
     int best_cs = 0, best_n = 0;
     if (tma) {
-        static bool attr_set = false;
-        if (!attr_set) {
-            if (cudaFuncSetAttribute((const void*)tv_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kTmaSmem) != cudaSuccess)
-                return DSPARK_ERR_CUDA;
-            attr_set = true;
-        }
+        int per_sm = 0;
+        if (prepare_kernel((const void*)tv_tma_kernel, kTmaSmem, kWSThreads, &per_sm) != cudaSuccess)
+            return DSPARK_ERR_CUDA;
         if (rows > (long long)INT32_MAX / 8) return DSPARK_ERR_UNSUPPORTED;
         cfg.blockDim = dim3(kWSThreads);
         cfg.dynamicSmemBytes = kTmaSmem;
-        // cluster of 8 when it keeps at least as many SMs busy as clusters of 4
-        // A batch of kRB row segments must fit the ring with slots to spare for the next batch's
-        // copies, so only cluster sizes with at most (kNS - 3) / kRB chunks per segment qualify.
+        // the cluster size keeping the most SMs busy; a batch of kRB row segments must fit the
+        // ring with slots to spare for the next batch's copies, so only cluster sizes with at
+        // most (kNS - 3) / kRB chunks per segment qualify
         for (int cs = kMaxCS; cs >= 1; cs >>= 1) {
             if (V < 8 * cs) continue;
             const int seg = (int)align_up((size_t)((V + cs - 1) / cs), 8);
             if (kRB * ((seg + kCE - 1) / kCE) > kNS - 3) continue;
-            attr[0].val.clusterDim.x = cs;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.gridDim = dim3(cs);
             int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, (const void*)tv_tma_kernel, &cfg) != cudaSuccess) {
-                cudaGetLastError();
-                continue;
-            }
+            if (max_active_clusters((const void*)tv_tma_kernel, cs, kWSThreads, kTmaSmem, &n) != cudaSuccess)
+                return DSPARK_ERR_CUDA;
             if (n * cs > best_n * best_cs) {
                 best_cs = cs;
                 best_n = n;
@@ -542,6 +519,8 @@ extern "C" dspark_status dspark_accept_rate_tv(int S, int A, int gamma, int V, i
         int nclusters = best_n;
         if ((long long)nclusters > rows) nclusters = (int)rows;
         attr[0].val.clusterDim.x = best_cs;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
         TVTArgs a;
         a.rows = (int)rows;
         a.V = V;
@@ -567,14 +546,13 @@ extern "C" dspark_status dspark_accept_rate_tv(int S, int A, int gamma, int V, i
         int cs = 4;
         int nclusters = 0;
         for (; cs >= 1; cs >>= 1) {
-            attr[0].val.clusterDim.x = cs;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.gridDim = dim3(cs);
-            if (cudaOccupancyMaxActiveClusters(&nclusters, (const void*)fn, &cfg) == cudaSuccess && nclusters > 0) break;
-            cudaGetLastError();
+            if (max_active_clusters((const void*)fn, cs, kTVThreads, 0, &nclusters) != cudaSuccess) return DSPARK_ERR_CUDA;
+            if (nclusters > 0) break;
         }
         if (cs < 1 || nclusters < 1) return DSPARK_ERR_CUDA;
+        attr[0].val.clusterDim.x = cs;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
         if ((long long)nclusters > rows) nclusters = (int)rows;
         TVArgs a;
         a.rows = rows;

@@ -555,8 +555,8 @@ extern "C" dspark_status dspark_verify(const dspark_sample_params* p, const void
     size_t smem = sizeof(float) * kRows * kXRow + sizeof(float2) * kRows * kChunks + align_up(sizeof(RowBlock), 16) +
                   sizeof(int4) * kRows + sizeof(float) * 64 + (mma ? 0 : sizeof(float) * kRows * (size_t)p->r);
     if (smem > kMaxSmem) return DSPARK_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute((const void*)jobs, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return DSPARK_ERR_CUDA;
+    int per_sm = 0;
+    if (prepare_kernel((const void*)jobs, smem, kThreads, &per_sm) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (cudaLaunchKernel((const void*)jobs, dim3(L.nt, L.nrb), dim3(kThreads), args, smem, s) != cudaSuccess)
         return DSPARK_ERR_CUDA;
     return DSPARK_OK;
