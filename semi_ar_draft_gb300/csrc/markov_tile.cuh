@@ -611,6 +611,52 @@ __device__ __forceinline__ void mma_chunk_rows(float (&xa)[8], float (&xb)[8], c
     }
 }
 
+// Row-block W1 fragments in shared memory, interleaved so that one 16-byte load is a whole A
+// fragment: unit (s, g, tq) [s = k-step, g = 0..7, tq = 0..3] holds the four 32-bit words
+// {W1 row g, row g + 8} x {k0 .. k0 + 1, k0 + 2 .. k0 + 3}, k0 = tq r/4 + 4 s, in MMA order
+// (a0 a1 a2 a3); a quarter-warp reads 8 consecutive units.  unit index = (s * 8 + g) * 4 + tq.
+template <int KS>
+__host__ __device__ constexpr int w1_units() {
+    return KS * 32;
+}
+
+// z of one chunk for rows g and g + 8 in MMA accumulator layout: acc[nt] = {row g: ids
+// 8 tq + 2 nt, +1; row g + 8: the same ids}; acc holds the base values on entry.
+template <int KS, bool W2SMEM, bool FULL>
+__device__ __forceinline__ void mma_chunk_frag(float (&acc)[4][4], const uint4* w1i, const uint16_t* W2,
+                                               const uint4* w2s, int tile0, int c, int V, int g, int tq) {
+    constexpr int r = 16 * KS;
+    constexpr int units = w2_units<KS>();
+    constexpr int mask = w2_mask<KS>();
+#pragma unroll
+    for (int s = 0; s < KS; s += 2) {  // k-steps s and s + 1 share a 16-byte unit of W2
+        const uint4 ua = w1i[(s * 8 + g) * 4 + tq];
+        uint4 ub = make_uint4(0u, 0u, 0u, 0u);
+        if (s + 1 < KS) ub = w1i[((s + 1) * 8 + g) * 4 + tq];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            const int vl = kCS * c + 8 * (g >> 1) + 2 * nt + (g & 1);
+            uint4 w = make_uint4(0u, 0u, 0u, 0u);
+            if (FULL || tile0 + vl < V) {
+                if constexpr (KS == 1) {
+                    const int u = tq >> 1, half = tq & 1;
+                    uint2 v;
+                    if constexpr (W2SMEM) v = reinterpret_cast<const uint2*>(w2s + (size_t)vl * units + (u ^ (vl & mask)))[half];
+                    else v = __ldg(reinterpret_cast<const uint2*>(W2 + (size_t)(tile0 + vl) * r + tq * (r / 4)));
+                    w.x = v.x;
+                    w.y = v.y;
+                } else {
+                    const int u = tq * (KS / 2) + s / 2;
+                    if constexpr (W2SMEM) w = w2s[(size_t)vl * units + (u ^ (vl & mask))];
+                    else w = __ldg(reinterpret_cast<const uint4*>(W2 + (size_t)(tile0 + vl) * r + tq * (r / 4)) + s / 2);
+                }
+            }
+            mma4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3], ua.x, ua.y, ua.z, ua.w, w.x, w.y);
+            if (s + 1 < KS) mma4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3], ub.x, ub.y, ub.z, ub.w, w.z, w.w);
+        }
+    }
+}
+
 // T > 0 chunk statistics straight from z: the maximum of the log2-weights z * scale2 is the
 // scaled maximum of z (scale2 > 0), the sum uses one fused multiply-add per id.
 __device__ __forceinline__ float2 chunk_stats_scaled(const float (&z)[8], float scale2) {
@@ -706,46 +752,67 @@ __device__ __forceinline__ float4 chunk_record_cg(const float (&z)[8], int id0, 
     const float target = u * S;
     // the lane holding the first crossing: cumulative mass reaches past target inside it
     const bool mine = before <= target && before + run > target;  // before + run == next lane's start
-    int e_star = 0;
+    // first id of this lane whose cumulative mass passes target (the last one when rounding
+    // leaves none), and its z
+    const float tl = target - before;
+    int e_star = 7;
+    float z_star = z[7];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) e_star += (before + cum[e] <= target) ? 1 : 0;
-    e_star = min(e_star, 7);
+    for (int e = 6; e >= 0; --e) {  // selects, not branches
+        const bool past = cum[e] > tl;
+        e_star = past ? e : e_star;
+        z_star = past ? z[e] : z_star;
+    }
     const unsigned quad = (unsigned)(lane & ~3);
     const unsigned bal = (__ballot_sync(0xffffffffu, mine) >> quad) & 0xFu;
     int src = bal ? (__ffs(bal) - 1) : 0;
     int my_e = e_star;
+    float zsel = z_star;
     if (__any_sync(0xffffffffu, bal == 0u && S > 0.f)) {
         // rounding left no crossing in some quad: there, the last id with mass
         int lz = -1;
+        float zl = z[0];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            if (ex2(fmaf(z[e], scale2, -mref)) > 0.f) lz = e;
+        for (int e = 0; e < 8; ++e) {
+            const bool has_e = ex2(fmaf(z[e], scale2, -mref)) > 0.f;
+            lz = has_e ? e : lz;
+            zl = has_e ? z[e] : zl;
+        }
         const unsigned nzb = (__ballot_sync(0xffffffffu, lz >= 0) >> quad) & 0xFu;
         if (!bal) {
             src = nzb ? 31 - __clz(nzb) : 0;
             my_e = max(lz, 0);
+            zsel = zl;
         }
     }
-    float zsel = z[0];
-#pragma unroll
-    for (int e = 1; e < 8; ++e)
-        if (my_e == e) zsel = z[e];
     const int e_src = __shfl_sync(0xffffffffu, my_e, src, 4);
     const float z_src = __shfl_sync(0xffffffffu, zsel, src, 4);
-    if (!(S > 0.f)) return make_float4(-CUDART_INF_F, -CUDART_INF_F, __int_as_float(-1), 0.f);
-    const float lmass = (m2 + lg2(S)) * kLn2;
-    return make_float4(lmass - lnE, lmass, __int_as_float(id0 - 8 * tq + 8 * src + e_src), z_src);
+    const bool has = S > 0.f;  // a chunk without mass: {-inf, -inf, -1, 0}
+    const float lmass = has ? (m2 + lg2(S)) * kLn2 : -CUDART_INF_F;
+    return make_float4(lmass - lnE, lmass, __int_as_float(has ? id0 - 8 * tq + 8 * src + e_src : -1), has ? z_src : 0.f);
+}
+
+// Two records of one request merged: the higher key wins (the first on ties: callers pass the
+// lower ids first); T > 0 also the log-sum of the log-masses (natural units).
+__device__ __forceinline__ float log_add(float a, float b) {
+    const float m = fmaxf(a, b);
+    if (m == -CUDART_INF_F) return m;
+    return m + lg2(1.0f + ex2((fminf(a, b) - m) * kLog2e)) * kLn2;
+}
+__device__ __forceinline__ float4 merge_rec(const float4 lo, const float4 hi, bool greedy) {
+    const bool take = hi.x > lo.x;
+    float4 r = take ? hi : lo;
+    if (!greedy) r.y = log_add(lo.y, hi.y);
+    return r;
 }
 
 template <int KS, bool GREEDY, bool W2SMEM, bool FULL>
-__device__ __forceinline__ void produce_cg(const uint16_t* stage, const uint16_t* w1rows, int w1stride,
-                                           const uint16_t* W2, const uint4* w2s, int V, int tile, float4* crec,
-                                           float scale2, const float* lnEt, const float* urow, int nv) {
+__device__ __forceinline__ void produce_cg(const uint16_t* stage, const uint4* w1i, const uint16_t* W2,
+                                           const uint4* w2s, int V, int tile, float4* crec, float scale2,
+                                           const float* lnEt, int ld, const float* urow, int nv) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, tq = lane & 3;
     const int tile0 = tile * kTS;
-    const uint16_t* w1a = w1rows + g * w1stride;
-    const uint16_t* w1b = w1rows + (g + 8) * w1stride;
     const uint16_t* srowA = stage + g * kStageRow;
     const uint16_t* srowB = stage + (g + 8) * kStageRow;
     // rows past the valid ones compute on stale data and are never reduced: clamp their table reads
@@ -755,23 +822,44 @@ __device__ __forceinline__ void produce_cg(const uint16_t* stage, const uint16_t
         uA = urow[ga];
         uB = urow[gb];
     }
+    const float4 empty = GREEDY ? make_float4(-CUDART_INF_F, CUDART_NAN_F, __int_as_float(0x7fffffff), -CUDART_INF_F)
+                                : make_float4(-CUDART_INF_F, -CUDART_INF_F, __int_as_float(-1), 0.f);
+    float4 accA = empty, accB = empty;  // this warp's chunks merged, rows g and g + 8
 #pragma unroll 1
     for (int k = 0; k < kChunksPerWarp; ++k) {
         const int c = warp + kWarps * k;
         const int cb = tile0 + kCS * c;
-        if (!FULL && cb >= V) {
-            if (tq == 0) {
-                const float4 e = GREEDY ? make_float4(-CUDART_INF_F, CUDART_NAN_F, __int_as_float(0x7fffffff), -CUDART_INF_F)
-                                        : make_float4(-CUDART_INF_F, -CUDART_INF_F, __int_as_float(-1), 0.f);
-                crec[g * kChunks + c] = e;
-                crec[(g + 8) * kChunks + c] = e;
+        if (!FULL && cb >= V) continue;
+        float acc[4][4];
+        {
+            const uint4 wa = *reinterpret_cast<const uint4*>(srowA + kCS * c + 8 * tq);
+            const uint4 wb = *reinterpret_cast<const uint4*>(srowB + kCS * c + 8 * tq);
+            const uint32_t pa[4] = {wa.x, wa.y, wa.z, wa.w}, pb[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                acc[nt][0] = bf16_lo(pa[nt]);
+                acc[nt][1] = bf16_hi(pa[nt]);
+                acc[nt][2] = bf16_lo(pb[nt]);
+                acc[nt][3] = bf16_hi(pb[nt]);
             }
-            continue;
+            if (!FULL) {  // ids past V take no part
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        if (cb + 8 * tq + 2 * nt + h >= V) {
+                            acc[nt][h] = -CUDART_INF_F;
+                            acc[nt][2 + h] = -CUDART_INF_F;
+                        }
+            }
         }
+        mma_chunk_frag<KS, W2SMEM, FULL>(acc, w1i, W2, w2s, tile0, c, V, g, tq);
         float xa[8], xb[8];
-        load_staged8(srowA, kCS * c + 8 * tq, tile0, V, FULL, xa);
-        load_staged8(srowB, kCS * c + 8 * tq, tile0, V, FULL, xb);
-        mma_chunk_rows<KS, W2SMEM>(xa, xb, w1a, w1b, W2, w2s, tile0, c, V, g, tq, FULL);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            xa[e] = acc[e >> 1][e & 1];
+            xb[e] = acc[e >> 1][2 + (e & 1)];
+        }
         float4 ra, rbk;
         if constexpr (GREEDY) {
             const float2 sa = chunk_stats(xa, cb + 8 * tq, 1);
@@ -779,42 +867,43 @@ __device__ __forceinline__ void produce_cg(const uint16_t* stage, const uint16_t
             ra = make_float4(sa.x, CUDART_NAN_F, sa.y, sa.x);
             rbk = make_float4(sb.x, CUDART_NAN_F, sb.y, sb.x);
         } else {
-            ra = chunk_record_cg(xa, cb + 8 * tq, scale2, lnEt[ga * kChunks + c], uA);
-            rbk = chunk_record_cg(xb, cb + 8 * tq, scale2, lnEt[gb * kChunks + c], uB);
+            ra = chunk_record_cg(xa, cb + 8 * tq, scale2, lnEt[c * ld + ga], uA);
+            rbk = chunk_record_cg(xb, cb + 8 * tq, scale2, lnEt[c * ld + gb], uB);
         }
-        if (tq == 0) {
-            crec[g * kChunks + c] = ra;
-            crec[(g + 8) * kChunks + c] = rbk;
-        }
+        accA = merge_rec(accA, ra, GREEDY);  // chunks in increasing order: ties keep the lower id
+        accB = merge_rec(accB, rbk, GREEDY);
+    }
+    if (tq == 0) {
+        crec[g * kWarps + warp] = accA;
+        crec[(g + 8) * kWarps + warp] = accB;
     }
 }
 
-// A row's tile record from its 32 chunk records (one warp, lane = chunk): the highest key
-// (lowest chunk on ties) with its candidate and z; T > 0 also the tile's log-mass.
+// A row's tile record from its per-warp records crow[0 .. kWarps) (one warp; lanes 16 .. 31
+// mirror lanes 0 .. 15): the arg-max (the lower warp, i.e. the lower ids, on ties) and the
+// maximum log-mass share one shuffle tree, then the sum of the log-masses' exponentials.
 __device__ __forceinline__ float4 reduce_row_chunks(const float4* crow, bool greedy) {
+    static_assert(kWarps == 16, "one lane per producing warp in a half-warp");
     const int lane = threadIdx.x & 31;
-    const float4 q = crow[lane];
-    float key = q.x;
-    int who = lane;
+    const float4 q = crow[lane & 15];
+    float key = q.x, ym = q.y;
+    int who = lane & 15;
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
+    for (int o = 8; o >= 1; o >>= 1) {
         const float ok = __shfl_xor_sync(0xffffffffu, key, o);
         const int ow = __shfl_xor_sync(0xffffffffu, who, o);
-        if (ok > key || (ok == key && ow < who)) {
-            key = ok;
-            who = ow;
-        }
+        const bool take = ok > key || (ok == key && ow < who);
+        key = take ? ok : key;
+        who = take ? ow : who;
+        if (!greedy) ym = fmaxf(ym, __shfl_xor_sync(0xffffffffu, ym, o));
     }
-    const float cand = __shfl_sync(0xffffffffu, q.z, who);
-    const float zv = __shfl_sync(0xffffffffu, q.w, who);
-    if (greedy) return make_float4(key, CUDART_NAN_F, cand, zv);
-    const float mt = warp_max(q.y);
-    float lm = -CUDART_INF_F;
-    if (mt != -CUDART_INF_F) {
-        const float sum = warp_sum(q.y == -CUDART_INF_F ? 0.f : ex2((q.y - mt) * kLog2e));
-        lm = mt + lg2(sum) * kLn2;
-    }
-    return make_float4(key, lm, cand, zv);
+    const float4 w = crow[who];
+    if (greedy) return make_float4(key, CUDART_NAN_F, w.z, w.w);
+    float sum = (q.y == -CUDART_INF_F) ? 0.f : ex2((q.y - ym) * kLog2e);
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const float lm = (ym == -CUDART_INF_F) ? -CUDART_INF_F : ym + lg2(sum) * kLn2;
+    return make_float4(key, lm, w.z, w.w);
 }
 
 // Tile record of one staged row (one warp).  Greedy: from the chunk statistics alone.  T > 0:

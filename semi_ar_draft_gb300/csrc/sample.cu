@@ -275,9 +275,9 @@ __host__ __device__ inline StagedLayout staged_layout(int B, int r, bool w2_smem
     L.stage = o;
     o += sizeof(uint16_t) * 2 * kRows * kStageRow;
     L.w1s = o;
-    o += align_up(sizeof(uint16_t) * 2 * kRows * (size_t)(r + 8), 16);
+    o += 2 * sizeof(uint4) * (size_t)(2 * r);  // [2] x (r / 16 k-steps x 32 fragment units)
     L.crec = o;
-    o += sizeof(float4) * 2 * kRows * kChunks;
+    o += sizeof(float4) * 2 * kRows * kWarps;
     L.prev = o;
     o += align_up(sizeof(int) * 2 * (size_t)B, 16);
     L.lnE_rows = B <= kStepTableRows ? B : kRows;
@@ -326,25 +326,32 @@ __device__ __forceinline__ void issue_base(const SampleArgs& a, int cnt, int nrb
 }
 
 // W1 rows of the previous tokens of row block `cnt` (rows past B repeat its first row) into its
-// stage buffer with plain loads by one warp: a batch of loads is in flight before its stores.
+// stage buffer as interleaved A fragments (see w1_units), with plain loads by one warp: a batch
+// of loads is in flight before its shared-memory stores.
 template <int KS>
-__device__ void load_w1_rows(const SampleArgs& a, int cnt, int nrb, const int* toks, uint16_t* w1s) {
-    constexpr int r = 16 * KS, w1st = r + 8, units = r / 8, per_rb = kRows * units, kBatch = 8;
+__device__ void load_w1_rows(const SampleArgs& a, int cnt, int nrb, const int* toks, uint4* w1s) {
+    constexpr int r = 16 * KS, nunits = w1_units<KS>(), kBatch = 8;
     const int lane = threadIdx.x & 31;
-    const uint4* W1 = reinterpret_cast<const uint4*>(a.W1);
+    const uint2* W1 = reinterpret_cast<const uint2*>(a.W1);  // 4 bf16 per uint2
     const int row0 = (cnt % nrb) * kRows;
-    uint4* dst = reinterpret_cast<uint4*>(w1s + (size_t)(cnt & 1) * kRows * w1st);
-    for (int b0 = 0; b0 < per_rb; b0 += 32 * kBatch) {
-        uint4 v[kBatch];
+    uint4* dst = w1s + (size_t)(cnt & 1) * nunits;
+    for (int b0 = 0; b0 < nunits; b0 += 32 * kBatch) {
+        uint2 va[kBatch], vb[kBatch];
 #pragma unroll
         for (int k = 0; k < kBatch; ++k) {
-            const int idx = b0 + k * 32 + lane, row = idx / units, u = idx % units, j = row0 + row;
-            if (idx < per_rb) v[k] = __ldg(W1 + (size_t)toks[j < a.B ? j : row0] * units + u);
+            const int idx = b0 + k * 32 + lane;
+            if (idx < nunits) {
+                const int sk = idx >> 5, g = (idx >> 2) & 7, tq = idx & 3;
+                const int k4 = (tq * (r / 4) + 4 * sk) / 4;  // uint2 index inside a row
+                const int ja = row0 + g, jb = row0 + g + 8;
+                va[k] = __ldg(W1 + (size_t)toks[ja < a.B ? ja : row0] * (r / 4) + k4);
+                vb[k] = __ldg(W1 + (size_t)toks[jb < a.B ? jb : row0] * (r / 4) + k4);
+            }
         }
 #pragma unroll
         for (int k = 0; k < kBatch; ++k) {
-            const int idx = b0 + k * 32 + lane, row = idx / units, u = idx % units;
-            if (idx < per_rb) dst[(size_t)row * (w1st / 8) + u] = v[k];
+            const int idx = b0 + k * 32 + lane;
+            if (idx < nunits) dst[idx] = make_uint4(va[k].x, vb[k].x, va[k].y, vb[k].y);
         }
     }
 }
@@ -365,21 +372,21 @@ __device__ void step_uniforms(const SampleArgs& a, int step, float* urow, int nt
 }
 
 // ln E_c of this block's 32 chunks for requests row0 .. row0 + nrows - 1 at `step`: one Philox
-// call gives the four chunks 4q .. 4q + 3 (draws n = global chunk index).
-__device__ void chunk_variates(const SampleArgs& a, int step, int row0, int nrows, float* table, int nthreads,
-                               int t0) {
+// call gives the four chunks 4q .. 4q + 3 (draws n = global chunk index).  The table is
+// chunk-major, table[c * ld + row - row0], so the producer's reads of one chunk for eight rows
+// fall on consecutive banks.
+__device__ void chunk_variates(const SampleArgs& a, int step, int row0, int nrows, float* table, int ld,
+                               int nthreads, int t0) {
     const uint32_t i = (uint32_t)step + 1u;
     for (int idx = t0; idx < nrows * (kChunks / 4); idx += nthreads) {
-        const int rl = idx / (kChunks / 4), q = idx % (kChunks / 4);
+        const int rl = idx % nrows, q = idx / nrows;
         const uint32_t j = (uint32_t)(row0 + rl);
         const uint4 w = philox10(make_uint4(blockIdx.x * (kChunks / 4) + (uint32_t)q, i, j, DSPARK_P_SAMPLE_CHUNK),
                                  (uint32_t)a.seed, (uint32_t)(a.seed >> 32));
-        float4 v;
-        v.x = log_neg_log_u(u01(w.x));
-        v.y = log_neg_log_u(u01(w.y));
-        v.z = log_neg_log_u(u01(w.z));
-        v.w = log_neg_log_u(u01(w.w));
-        reinterpret_cast<float4*>(table + (size_t)rl * kChunks)[q] = v;
+        table[(size_t)(4 * q + 0) * ld + rl] = log_neg_log_u(u01(w.x));
+        table[(size_t)(4 * q + 1) * ld + rl] = log_neg_log_u(u01(w.y));
+        table[(size_t)(4 * q + 2) * ld + rl] = log_neg_log_u(u01(w.z));
+        table[(size_t)(4 * q + 3) * ld + rl] = log_neg_log_u(u01(w.w));
     }
 }
 
@@ -499,7 +506,7 @@ __device__ void owner_lse_rb(const SampleArgs& a, int s, int rbi, const int* tok
 }
 
 template <int KS>
-__device__ void exchanger(const SampleArgs& a, int par, int* prev, uint16_t* w1s, uint64_t* full, uint64_t* empty,
+__device__ void exchanger(const SampleArgs& a, int par, int* prev, uint4* w1s, uint64_t* full, uint64_t* empty,
                           volatile int* abort, volatile int* w1_upto) {
     const int lane = threadIdx.x & 31;
     const int nrb = (a.B + kRows - 1) / kRows, total = a.gamma * nrb;
@@ -517,6 +524,7 @@ __device__ void exchanger(const SampleArgs& a, int par, int* prev, uint16_t* w1s
             }
             st_ok = __shfl_sync(0xffffffffu, st_ok, 0);
             if (st_ok > 0) break;
+            __nanosleep(128);
             if (st_ok < 0 || helper_should_stop(abort, t0, a)) return false;
         }
         __syncwarp();
@@ -579,15 +587,15 @@ __device__ void exchanger(const SampleArgs& a, int par, int* prev, uint16_t* w1s
 
 template <int KS, bool GREEDY>
 __global__ void __launch_bounds__(kStagedThreads, 1) sample_staged_kernel(SampleArgs a) {
-    constexpr int r = 16 * KS, w1st = r + 8;
+    constexpr int r = 16 * KS;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const StagedLayout L = staged_layout(a.B, r, a.w2_smem);
     uint16_t* stage = reinterpret_cast<uint16_t*>(smem_raw + L.stage);  // [2][kRows][kStageRow] bf16 bits
-    uint16_t* w1s = reinterpret_cast<uint16_t*>(smem_raw + L.w1s);      // [2][kRows][w1st]
-    float4* crec = reinterpret_cast<float4*>(smem_raw + L.crec);        // [2][kRows][kChunks] chunk records
+    uint4* w1s = reinterpret_cast<uint4*>(smem_raw + L.w1s);            // [2][w1_units] A fragments
+    float4* crec = reinterpret_cast<float4*>(smem_raw + L.crec);        // [2][kRows][kWarps] per-warp records
     int* prev = reinterpret_cast<int*>(smem_raw + L.prev);              // [2][B]: tokens feeding step s at s & 1
     float* urow = reinterpret_cast<float*>(smem_raw + L.urow);          // [B] in-chunk uniforms
-    float* lnEt = reinterpret_cast<float*>(smem_raw + L.lnEt);          // [lnE_rows][kChunks]
+    float* lnEt = reinterpret_cast<float*>(smem_raw + L.lnEt);          // [kChunks][lnE_rows]
     uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + L.bars);    // [2] stage buffer filled (2 arrivals)
     uint64_t* empty = full + 2;                                         // [2] stage buffer released
     volatile int* flags = reinterpret_cast<volatile int*>(full + 4);
@@ -630,7 +638,7 @@ __global__ void __launch_bounds__(kStagedThreads, 1) sample_staged_kernel(Sample
         if (a.w2_smem) stage_w2_tile_async<KS>(W2, tile0, a.V, w2s, kThreads);
         if (!GREEDY && step_table) {  // step 0's draws for every request
             step_uniforms(a, 0, urow, kThreads, tid);
-            chunk_variates(a, 0, 0, a.B, lnEt, kThreads, tid);
+            chunk_variates(a, 0, 0, a.B, lnEt, a.B, kThreads, tid);
         }
         if (a.w2_smem) cp_async_wait_all();
         named_barrier(1, kThreads);
@@ -645,7 +653,7 @@ __global__ void __launch_bounds__(kStagedThreads, 1) sample_staged_kernel(Sample
                 const int nv = min(kRows, a.B - row0);
                 if (!GREEDY && !step_table) {  // the row block's draws
                     if (rbi == 0) step_uniforms(a, step, urow, kThreads, tid);
-                    chunk_variates(a, step, row0, nv, lnEt, kThreads, tid);
+                    chunk_variates(a, step, row0, nv, lnEt, kRows, kThreads, tid);
                 }
                 if (tid == 0) *s_ok = mbar_wait_or_abort(&full[buf], par, abort, &a.hdr->status, a.limit_ns, false);
                 named_barrier(1, kThreads);
@@ -655,22 +663,23 @@ __global__ void __launch_bounds__(kStagedThreads, 1) sample_staged_kernel(Sample
                 }
                 mbar_try_wait(&full[buf], par);  // completed: acquire for this thread
                 const uint16_t* sbuf = stage + (size_t)buf * kRows * kStageRow;
-                const uint16_t* wbuf = w1s + (size_t)buf * kRows * w1st;
-                float4* cr = crec + (size_t)buf * kRows * kChunks;
-                const float* lt = lnEt + (step_table ? (size_t)row0 * kChunks : 0);
+                const uint4* wbuf = w1s + (size_t)buf * w1_units<KS>();
+                float4* cr = crec + (size_t)buf * kRows * kWarps;
+                const float* lt = lnEt + (step_table ? (size_t)row0 : 0);  // chunk-major, leading dimension ld
+                const int ld = step_table ? a.B : kRows;
                 const float* ut = urow + row0;
                 if (a.w2_smem) {
-                    if (full_tile) produce_cg<KS, GREEDY, true, true>(sbuf, wbuf, w1st, W2, w2s, a.V, tile, cr, a.scale2, lt, ut, nv);
-                    else produce_cg<KS, GREEDY, true, false>(sbuf, wbuf, w1st, W2, w2s, a.V, tile, cr, a.scale2, lt, ut, nv);
+                    if (full_tile) produce_cg<KS, GREEDY, true, true>(sbuf, wbuf, W2, w2s, a.V, tile, cr, a.scale2, lt, ld, ut, nv);
+                    else produce_cg<KS, GREEDY, true, false>(sbuf, wbuf, W2, w2s, a.V, tile, cr, a.scale2, lt, ld, ut, nv);
                 } else {
-                    if (full_tile) produce_cg<KS, GREEDY, false, true>(sbuf, wbuf, w1st, W2, nullptr, a.V, tile, cr, a.scale2, lt, ut, nv);
-                    else produce_cg<KS, GREEDY, false, false>(sbuf, wbuf, w1st, W2, nullptr, a.V, tile, cr, a.scale2, lt, ut, nv);
+                    if (full_tile) produce_cg<KS, GREEDY, false, true>(sbuf, wbuf, W2, nullptr, a.V, tile, cr, a.scale2, lt, ld, ut, nv);
+                    else produce_cg<KS, GREEDY, false, false>(sbuf, wbuf, W2, nullptr, a.V, tile, cr, a.scale2, lt, ld, ut, nv);
                 }
                 named_barrier(1, kThreads);
                 if (tid == 0) mbar_arrive_local(&empty[buf]);  // stage and W1 buffer free for row block cnt + 2
                 if (warp < nv) {  // one request per warp
                     const int j = row0 + warp;
-                    const float4 rec = reduce_row_chunks(cr + warp * kChunks, GREEDY);
+                    const float4 rec = reduce_row_chunks(cr + warp * kWarps, GREEDY);
                     if (lane == 0) {
                         if (!GREEDY) part[(size_t)j * a.nt + tile] = rec;
                         red_max_u64(slot + (size_t)j * kSlotStride, pack_key(rec.x, __float_as_int(rec.z)));
@@ -682,7 +691,7 @@ __global__ void __launch_bounds__(kStagedThreads, 1) sample_staged_kernel(Sample
             if (!live) break;
             if (!GREEDY && step_table && step + 1 < a.gamma) {  // the next step's draws (this step's are read)
                 step_uniforms(a, step + 1, urow, kThreads, tid);
-                chunk_variates(a, step + 1, 0, a.B, lnEt, kThreads, tid);
+                chunk_variates(a, step + 1, 0, a.B, lnEt, a.B, kThreads, tid);
                 named_barrier(1, kThreads);
             }
         }
