@@ -7,14 +7,11 @@
 // eval_mask = cumprod of (keep && pos_valid) (P1 section 3.6), tau = 1 + sum_i prod_{k<=i}
 // acc_k * mask_k (P1 section 3.10).
 //
-// Design: a thread-block cluster owns one row at a time (persistent over rows); each block of
-// it takes a 1/cs segment of d and t, gets (max, sum) of both softmaxes over the segment, the
-// blocks exchange those through distributed shared memory, each block then forms its part of
-// the sum of minima, and block 0 of the cluster adds the parts and writes acc and eval_mask.
-// Two kernels implement it: tv_tma_kernel (bf16 rows on 16-byte boundaries that fit the copy
-// ring: the segment is read from HBM once, into a shared-memory ring filled by the bulk-copy
-// engine, and both passes read shared memory) and tv_kernel (any other case: the second pass
-// re-reads the segment, an L2 hit since the rows in flight stay far below the L2 size).
+// Two kernels: tv_rows_kernel (bf16 rows on 16-byte boundaries: a block streams whole rows twice
+// through a shared-memory ring fed by the bulk-copy engine, pass 1 from HBM and pass 2 from L2)
+// and tv_kernel (any other case: a thread-block cluster shares a row, each block takes a 1/cs
+// segment, the blocks exchange (max, sum) through distributed shared memory, and the second
+// pass re-reads the segment, an L2 hit).
 #include <cooperative_groups.h>
 
 #include <algorithm>
@@ -190,45 +187,35 @@ __global__ void __launch_bounds__(kTVThreads, 1) tv_kernel(TVArgs a) {
 }
 
 // ------------------------------------------------------------------------------------------
-// bf16 fast path, warp-specialised.  Each block owns a 1/cs segment of every row of its
-// cluster; the segment streams through a ring of kNS shared-memory slots (kCE ids of d and t
-// per slot) filled by the bulk-copy engine:
-//   - one producer warp issues the copies; a slot is refilled once all 16 consumer warps have
-//     released it (per-slot "empty" mbarrier, one arrival per warp);
-//   - 16 consumer warps wait on the slot's "full" mbarrier (transaction count), take the
-//     softmax statistics in pass 1 and the sum of minima in pass 2 -- both from shared memory;
-//   - the per-row statistics and sums go to the other blocks of the cluster by DSMEM stores
-//     followed by remote mbarrier arrivals (no cluster-wide barrier inside the row loop).
-// Every wait is bounded; a timeout raises a block-wide abort flag after which no thread waits
-// any more, while every consumer still executes the same sequence of named barriers, and the
-// whole cluster meets once more before exiting.
+// bf16 fast path: one block per row at a time (persistent over rows, no cluster), warp-specialised.
+// A producer warp streams every row twice through a ring of kNS shared-memory slots (kCE ids of
+// d and t per slot) with the bulk-copy engine: pass 1 from HBM with an L2 evict-last policy, so
+// that pass 2, which follows right after, reads the same bytes from L2 (evict-first); a slot
+// is refilled once all 16 consumer warps have released it.  The consumer warps take the softmax
+// statistics of d and t in pass 1, combine them across the block, then form
+// sum_v min(p_v, q_v) = sum_v 2^min(d_v log2e - Ld, t_v log2e - Lt) in pass 2.
+// Every wait is bounded; after a timeout the block-wide abort flag makes the consumers skip the
+// data while keeping the same sequence of named barriers, and in-flight copies are awaited.
 // ------------------------------------------------------------------------------------------
-constexpr int kCE = 4096;                       // ids per array per slot
-constexpr int kNS = 13;                         // ring slots (13 x 16 KB)
-constexpr int kWSCons = 512;                    // consumer threads (16 warps)
+constexpr int kCE = 4096;                 // ids per array per slot
+constexpr int kNS = 13;                   // ring slots (13 x 16 KB)
+constexpr int kWSCons = 512;              // consumer threads (16 warps)
 constexpr int kWSWarps = kWSCons / 32;
-constexpr int kWSThreads = kWSCons + 32;        // + one producer warp
-constexpr int kMaxCS = 8;
+constexpr int kWSThreads = kWSCons + 32;  // + one producer warp
 static_assert(kCE == 8 * kWSCons, "one 16-byte group of each array per consumer thread per slot");
 
-constexpr int kRB = 1;  // rows per batch: one statistics exchange and one sum exchange per batch
-
-struct TVWSmem {
+struct TVRSmem {
     uint16_t slots[kNS][2][kCE];
     uint64_t full[kNS];
     uint64_t empty[kNS];
-    uint64_t xbar_st[2];   // batch statistics from every block of the cluster (count = cs)
-    uint64_t xbar_sum[2];  // batch sums, at cluster rank 0 only (count = cs)
-    float4 xst[2][kMaxCS][kRB];
-    float xsum[2][kMaxCS][kRB];
-    float4 red4[kWSWarps][kRB];
-    float red1[kWSWarps][kRB];
+    float4 red4[kWSWarps];
+    float red1[kWSWarps];
     int abort;
 };
-constexpr size_t kTmaSmem = sizeof(TVWSmem);
+constexpr size_t kRowSmem = sizeof(TVRSmem);
 
-struct TVTArgs {
-    int rows, V, gamma, segsz, nch, nclusters, cs;
+struct TVRArgs {
+    int rows, V, gamma, nch;
     const __nv_bfloat16* d;
     const __nv_bfloat16* t;
     const uint8_t* keep;
@@ -251,182 +238,109 @@ __device__ __forceinline__ float2 warp_lse_pair(float m, float s) {
     return make_float2(M, warp_sum(sc));
 }
 
-__global__ void __launch_bounds__(kWSThreads, 1) tv_tma_kernel(TVTArgs a) {
-    cg::cluster_group cluster = cg::this_cluster();
-    const int crank = (int)cluster.block_rank();
-    const int cid = blockIdx.x / a.cs;
+__global__ void __launch_bounds__(kWSThreads, 1) tv_rows_kernel(TVRArgs a) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    TVWSmem& S = *reinterpret_cast<TVWSmem*>(smem_raw);
+    TVRSmem& S = *reinterpret_cast<TVRSmem*>(smem_raw);
     volatile int* abort = &S.abort;
-    const int seg_lo = crank * a.segsz;
-    const int seg_len = max(0, min(a.V - seg_lo, a.segsz));
-    const int nch = a.nch, cs = a.cs;
-    const int nrows = (a.rows - cid + a.nclusters - 1) / a.nclusters;  // rows of this cluster
-    const int nbatch = (nrows + kRB - 1) / kRB;
-    const int Q = nrows * nch;  // chunks: row-major over this cluster's rows
+    const int nch = a.nch;
+    const int nrows = (a.rows - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;  // rows of this block
+    const int Q = nrows * 2 * nch;  // chunks: per row, pass 1 then pass 2
     if (tid == 0) {
         for (int i = 0; i < kNS; ++i) {
             mbar_init(&S.full[i], 1);
             mbar_init(&S.empty[i], kWSWarps);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&S.xbar_st[i], cs);
-            mbar_init(&S.xbar_sum[i], cs);
-        }
         S.abort = 0;
         mbar_init_fence();
     }
-    cluster.sync();  // barriers of every block exist before any remote arrival
+    __syncthreads();
 
     if (warp == kWSWarps) {
         // ---------------- producer warp
         if (lane == 0) {
-            int slot = 0, k = 0, ri = 0;
+            const uint64_t keep_pol = l2_policy_evict_last(), drop_pol = l2_policy_evict_first();
             for (int q = 0; q < Q; ++q) {
+                const int slot = q % kNS;
                 // the (q / kNS)-th use of the slot waits for the release of its previous use
                 if (q >= kNS && !mbar_wait_or_abort(&S.empty[slot], (uint32_t)((q / kNS - 1) & 1), abort,
                                                     &a.hdr->status, a.limit_ns, false))
                     break;
-                const int len = max(0, min(kCE, seg_len - k * kCE));
+                const int rl = q / (2 * nch), pass = (q / nch) & 1, k = q % nch;
+                const int len = min(kCE, a.V - k * kCE);
+                const size_t off = (size_t)((int)blockIdx.x + rl * (int)gridDim.x) * a.V + (size_t)k * kCE;
+                const uint64_t pol = pass ? drop_pol : keep_pol;
                 mbar_arrive_expect_tx(&S.full[slot], (uint32_t)(4 * len));
-                if (len > 0) {
-                    const size_t off = (size_t)(cid + ri * a.nclusters) * a.V + seg_lo + (size_t)k * kCE;
-                    bulk_g2s(&S.slots[slot][0][0], a.d + off, (uint32_t)(2 * len), &S.full[slot]);
-                    bulk_g2s(&S.slots[slot][1][0], a.t + off, (uint32_t)(2 * len), &S.full[slot]);
-                }
-                if (++k == nch) {
-                    k = 0;
-                    ++ri;
-                }
-                if (++slot == kNS) slot = 0;
+                bulk_g2s_hint(&S.slots[slot][0][0], a.d + off, (uint32_t)(2 * len), &S.full[slot], pol);
+                bulk_g2s_hint(&S.slots[slot][1][0], a.t + off, (uint32_t)(2 * len), &S.full[slot], pol);
             }
         }
         __syncwarp();
     } else {
         // ---------------- 16 consumer warps
         const int my0 = 8 * tid;  // this thread's ids in a slot: my0 .. my0 + 7 (conflict-free 16-byte reads)
-        int slot = 0;             // slot of the next chunk to read in pass 1
-        uint32_t phase = 0;
-        for (int b = 0; b < nbatch; ++b) {
-            const int par = b & 1;
-            const int r0 = b * kRB, nr = min(kRB, nrows - r0);
-            const int slot_b = slot;  // first slot of the batch, for pass 2
-            // ---- pass 1 over the batch's rows
-            float md[kRB], sd[kRB], mt[kRB], st[kRB];
+        int q = 0;
+        for (int rl = 0; rl < nrows; ++rl) {
+            // ---- pass 1: softmax statistics of d and t
+            float md = -CUDART_INF_F, sd = 0.f, mt = -CUDART_INF_F, st = 0.f;
+            for (int k = 0; k < nch; ++k, ++q) {
+                const int slot = q % kNS;
+                const bool ok = mbar_wait_or_abort(&S.full[slot], (uint32_t)((q / kNS) & 1), abort, &a.hdr->status,
+                                                   a.limit_ns, false);
+                float xd[8], xt[8];  // lanes without data merge -inf
+                if (ok && (k + 1 < nch || my0 < a.V - k * kCE)) {
+                    unpack_bf16x8(*reinterpret_cast<const uint4*>(&S.slots[slot][0][my0]), xd);
+                    unpack_bf16x8(*reinterpret_cast<const uint4*>(&S.slots[slot][1][my0]), xt);
+                } else {
 #pragma unroll
-            for (int r = 0; r < kRB; ++r) {
-                md[r] = mt[r] = -CUDART_INF_F;
-                sd[r] = st[r] = 0.f;
-            }
-#pragma unroll
-            for (int r = 0; r < kRB; ++r) {
-                if (r >= nr) break;
-                int len = seg_len;
-                for (int k = 0; k < nch; ++k) {
-                    const bool ok = mbar_wait_or_abort(&S.full[slot], phase, abort, &a.hdr->status, a.limit_ns, false);
-                    if (ok && my0 < len) {
-                        float xd[8], xt[8];
-                        unpack_bf16x8(*reinterpret_cast<const uint4*>(&S.slots[slot][0][my0]), xd);
-                        unpack_bf16x8(*reinterpret_cast<const uint4*>(&S.slots[slot][1][my0]), xt);
-                        lse_merge8(xd, md[r], sd[r]);
-                        lse_merge8(xt, mt[r], st[r]);
-                    }
-                    len -= kCE;
-                    if (++slot == kNS) {
-                        slot = 0;
-                        phase ^= 1u;
-                    }
+                    for (int e = 0; e < 8; ++e) xd[e] = xt[e] = -CUDART_INF_F;
                 }
+                lse_merge8(xd, md, sd);
+                lse_merge8(xt, mt, st);
+                __syncwarp();
+                if (lane == 0) mbar_arrive_local(&S.empty[slot]);
             }
-            // ---- batch statistics -> every block of the cluster
-#pragma unroll
-            for (int r = 0; r < kRB; ++r) {
-                const float2 wd = warp_lse_pair(md[r], sd[r]);
-                const float2 wt = warp_lse_pair(mt[r], st[r]);
-                if (lane == 0) S.red4[warp][r] = make_float4(wd.x, wd.y, wt.x, wt.y);
+            {
+                const float2 wd = warp_lse_pair(md, sd);
+                const float2 wt = warp_lse_pair(mt, st);
+                if (lane == 0) S.red4[warp] = make_float4(wd.x, wd.y, wt.x, wt.y);
             }
             named_barrier(1, kWSCons);
-            if (warp == 0) {
-#pragma unroll
-                for (int r = 0; r < kRB; ++r) {
-                    const float4 q = lane < kWSWarps ? S.red4[lane][r] : make_float4(-CUDART_INF_F, 0.f, -CUDART_INF_F, 0.f);
-                    const float2 cd = warp_lse_pair(q.x, q.y);
-                    const float2 ct = warp_lse_pair(q.z, q.w);
-                    if (lane < cs) st_cluster_f32x4(map_to_rank(&S.xst[par][crank][r], lane), make_float4(cd.x, cd.y, ct.x, ct.y));
-                }
-                if (lane < cs) mbar_arrive_remote(map_to_rank(&S.xbar_st[par], lane));
-            }
-            mbar_wait_or_abort(&S.xbar_st[par], (uint32_t)((b >> 1) & 1), abort, &a.hdr->status, a.limit_ns, true);
-            float Ld2[kRB], Lt2[kRB];
-#pragma unroll
-            for (int r = 0; r < kRB; ++r) {
-                float Md = -CUDART_INF_F, Mt = -CUDART_INF_F;
-                for (int c = 0; c < cs; ++c) {
-                    Md = fmaxf(Md, S.xst[par][c][r].x);
-                    Mt = fmaxf(Mt, S.xst[par][c][r].z);
-                }
-                float Sd = 0.f, St = 0.f;
-                for (int c = 0; c < cs; ++c) {
-                    const float4 q = S.xst[par][c][r];
-                    if (q.x != -CUDART_INF_F) Sd += q.y * ex2(q.x - Md);
-                    if (q.z != -CUDART_INF_F) St += q.w * ex2(q.z - Mt);
-                }
-                Ld2[r] = Md + lg2(Sd);
-                Lt2[r] = Mt + lg2(St);
-            }
-            // ---- pass 2: sum of min(p, q); each warp releases each slot after reading it
-            float acc[kRB];
+            float Ld2, Lt2;
             {
-                int slot2 = slot_b;
-                const bool live = !*abort;
+                const float4 v = lane < kWSWarps ? S.red4[lane] : make_float4(-CUDART_INF_F, 0.f, -CUDART_INF_F, 0.f);
+                const float2 cd = warp_lse_pair(v.x, v.y);
+                const float2 ct = warp_lse_pair(v.z, v.w);
+                Ld2 = cd.x + lg2(cd.y);
+                Lt2 = ct.x + lg2(ct.y);
+            }
+            // ---- pass 2: sum of min(p, q)
+            float acc = 0.f;
+            for (int k = 0; k < nch; ++k, ++q) {
+                const int slot = q % kNS;
+                const bool ok = mbar_wait_or_abort(&S.full[slot], (uint32_t)((q / kNS) & 1), abort, &a.hdr->status,
+                                                   a.limit_ns, false);
+                if (ok && (k + 1 < nch || my0 < a.V - k * kCE)) {
+                    const uint4 wd = *reinterpret_cast<const uint4*>(&S.slots[slot][0][my0]);
+                    const uint4 wt = *reinterpret_cast<const uint4*>(&S.slots[slot][1][my0]);
+                    const uint32_t dw[4] = {wd.x, wd.y, wd.z, wd.w}, tw[4] = {wt.x, wt.y, wt.z, wt.w};
 #pragma unroll
-                for (int r = 0; r < kRB; ++r) {
-                    acc[r] = 0.f;
-                    if (r >= nr) break;
-                    int len2 = seg_len;
-                    for (int k = 0; k < nch; ++k) {
-                        if (live && my0 < len2) {
-                            const uint4 wd = *reinterpret_cast<const uint4*>(&S.slots[slot2][0][my0]);
-                            const uint4 wt = *reinterpret_cast<const uint4*>(&S.slots[slot2][1][my0]);
-                            const uint32_t dw[4] = {wd.x, wd.y, wd.z, wd.w}, tw[4] = {wt.x, wt.y, wt.z, wt.w};
-#pragma unroll
-                            for (int h = 0; h < 4; ++h) {
-                                acc[r] += ex2(fminf(fmaf(bf16_lo(dw[h]), kLog2e, -Ld2[r]), fmaf(bf16_lo(tw[h]), kLog2e, -Lt2[r])));
-                                acc[r] += ex2(fminf(fmaf(bf16_hi(dw[h]), kLog2e, -Ld2[r]), fmaf(bf16_hi(tw[h]), kLog2e, -Lt2[r])));
-                            }
-                        }
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive_local(&S.empty[slot2]);
-                        len2 -= kCE;
-                        if (++slot2 == kNS) slot2 = 0;
+                    for (int h = 0; h < 4; ++h) {
+                        acc += ex2(fminf(fmaf(bf16_lo(dw[h]), kLog2e, -Ld2), fmaf(bf16_lo(tw[h]), kLog2e, -Lt2)));
+                        acc += ex2(fminf(fmaf(bf16_hi(dw[h]), kLog2e, -Ld2), fmaf(bf16_hi(tw[h]), kLog2e, -Lt2)));
                     }
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive_local(&S.empty[slot]);
             }
-#pragma unroll
-            for (int r = 0; r < kRB; ++r) {
-                const float w = warp_sum(acc[r]);
-                if (lane == 0) S.red1[warp][r] = w;
-            }
+            const float w = warp_sum(acc);
+            if (lane == 0) S.red1[warp] = w;
             named_barrier(2, kWSCons);
             if (warp == 0) {
-#pragma unroll
-                for (int r = 0; r < kRB; ++r) {
-                    const float q = warp_sum(lane < kWSWarps ? S.red1[lane][r] : 0.f);
-                    if (lane == 0) {
-                        const uint32_t dst = map_to_rank(&S.xsum[par][crank][r], 0);
-                        asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst), "f"(q) : "memory");
-                    }
-                }
-                if (lane == 0) mbar_arrive_remote(map_to_rank(&S.xbar_sum[par], 0));
-            }
-            if (crank == 0 && tid == 0) {
-                mbar_wait_or_abort(&S.xbar_sum[par], (uint32_t)((b >> 1) & 1), abort, &a.hdr->status, a.limit_ns, true);
-                for (int r = 0; r < nr; ++r) {
-                    float tot = 0.f;
-                    for (int c = 0; c < cs; ++c) tot += S.xsum[par][c][r];
-                    const int row = cid + (r0 + r) * a.nclusters;
-                    a.acc[row] = fminf(fmaxf(tot, 0.f), 1.f);
+                const float v = warp_sum(lane < kWSWarps ? S.red1[lane] : 0.f);
+                if (lane == 0 && !*abort) {
+                    const int row = (int)blockIdx.x + rl * (int)gridDim.x;
+                    a.acc[row] = fminf(fmaxf(v, 0.f), 1.f);
                     const int blk = row / a.gamma, i = row % a.gamma;
                     float mval = a.keep[blk] ? 1.f : 0.f;
                     if (a.posv)
@@ -436,16 +350,16 @@ __global__ void __launch_bounds__(kWSThreads, 1) tv_tma_kernel(TVTArgs a) {
             }
         }
     }
-    // Copies still in flight after an abort: wait for them (bounded) before the block can leave.
+    __syncthreads();
+    // copies still in flight after an abort: wait for them (bounded) before the block leaves
     if (tid == 0 && *abort) {
         const uint64_t t0 = global_ns();
-        for (int q = max(0, Q - kNS); q < Q; ++q) {
-            const int sl = q % kNS;
-            while (!mbar_try_wait(&S.full[sl], (uint32_t)((q / kNS) & 1)) && global_ns() - t0 < a.limit_ns) {
+        for (int qq = max(0, Q - kNS); qq < Q; ++qq) {
+            const int sl = qq % kNS;
+            while (!mbar_try_wait(&S.full[sl], (uint32_t)((qq / kNS) & 1)) && global_ns() - t0 < a.limit_ns) {
             }
         }
     }
-    cluster.sync();  // no block leaves while a peer may still write into its shared memory
 }
 
 // tau[s,a] = 1 + sum_i prod_{k<=i} acc * mask (one thread per block of gamma positions).
@@ -491,44 +405,18 @@ extern "C" dspark_status dspark_accept_rate_tv(int S, int A, int gamma, int V, i
     cfg.numAttrs = 1;
     const bool tma = dtype == DSPARK_BF16 && V % 8 == 0 && (uintptr_t)draft_logits % 16 == 0 &&
                      (uintptr_t)target_logits % 16 == 0 && V >= 16;
-    int best_cs = 0, best_n = 0;
-    if (tma) {
-        int per_sm = 0;
-        if (prepare_kernel((const void*)tv_tma_kernel, kTmaSmem, kWSThreads, &per_sm) != cudaSuccess)
-            return DSPARK_ERR_CUDA;
-        if (rows > (long long)INT32_MAX / 8) return DSPARK_ERR_UNSUPPORTED;
-        cfg.blockDim = dim3(kWSThreads);
-        cfg.dynamicSmemBytes = kTmaSmem;
-        // the cluster size keeping the most SMs busy; a batch of kRB row segments must fit the
-        // ring with slots to spare for the next batch's copies, so only cluster sizes with at
-        // most (kNS - 3) / kRB chunks per segment qualify
-        for (int cs = kMaxCS; cs >= 1; cs >>= 1) {
-            if (V < 8 * cs) continue;
-            const int seg = (int)align_up((size_t)((V + cs - 1) / cs), 8);
-            if (kRB * ((seg + kCE - 1) / kCE) > kNS - 3) continue;
-            int n = 0;
-            if (max_active_clusters((const void*)tv_tma_kernel, cs, kWSThreads, kTmaSmem, &n) != cudaSuccess)
-                return DSPARK_ERR_CUDA;
-            if (n * cs > best_n * best_cs) {
-                best_cs = cs;
-                best_n = n;
-            }
-        }
-    }
-    if (tma && best_cs > 0) {  // (no cluster size fits the ring for very large vocabularies: streaming kernel)
-        int nclusters = best_n;
-        if ((long long)nclusters > rows) nclusters = (int)rows;
-        attr[0].val.clusterDim.x = best_cs;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        TVTArgs a;
+    int per_sm = 0;
+    if (tma && prepare_kernel((const void*)tv_rows_kernel, kRowSmem, kWSThreads, &per_sm) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
+    if (tma && per_sm > 0 && rows <= (long long)INT32_MAX / 2) {
+        int sms = 0;
+        if (device_sm_count(&sms) != cudaSuccess) return DSPARK_ERR_CUDA;
+        const long long G = std::min<long long>(rows, (long long)sms * per_sm);
+        TVRArgs a;
         a.rows = (int)rows;
         a.V = V;
         a.gamma = gamma;
-        a.segsz = (int)align_up((size_t)((V + best_cs - 1) / best_cs), 8);
-        a.nch = (a.segsz + kCE - 1) / kCE;
-        a.nclusters = nclusters;
-        a.cs = best_cs;
+        a.nch = (V + kCE - 1) / kCE;
         a.d = static_cast<const __nv_bfloat16*>(draft_logits);
         a.t = static_cast<const __nv_bfloat16*>(target_logits);
         a.keep = block_keep;
@@ -537,8 +425,8 @@ extern "C" dspark_status dspark_accept_rate_tv(int S, int A, int gamma, int V, i
         a.mask = eval_mask;
         a.hdr = static_cast<WsHeader*>(workspace);
         a.limit_ns = wait_limit_ns();
-        cfg.gridDim = dim3(nclusters * best_cs);
-        if (cudaLaunchKernelEx(&cfg, tv_tma_kernel, a) != cudaSuccess) return DSPARK_ERR_CUDA;
+        tv_rows_kernel<<<(unsigned)G, kWSThreads, kRowSmem, s>>>(a);
+        if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
     } else {
         void (*fn)(TVArgs) = dtype == DSPARK_BF16 ? tv_kernel<__nv_bfloat16> : tv_kernel<float>;
         cfg.blockDim = dim3(kTVThreads);
