@@ -10,7 +10,11 @@ metric = drafted tokens per second = N * B * gamma / step time (replicas: every 
 batch, "weak" scaling).  Inputs are synthetic, seeded, resident in HBM before timing; L2 is
 flushed (256 MB write) before every step, outside the per-step CUDA-event interval.
 
-Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Other workloads of the same path can be timed with --workload (b128_r256: B=128, gamma=16,
+rank 256, T=0.7; b512_sched: B=512, gamma=16, budget 2048 verify tokens); the default line is
+the b32_r64 one.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--workload NAME]
 """
 from __future__ import annotations
 
@@ -30,6 +34,7 @@ if ROOT not in sys.path:
 
 METRIC = "draft tokens/s (sample+verify) at V=151936; achieved HBM GB/s vs peak"
 WORKLOAD = "b32_r64"
+WORKLOADS = ("b32_r64", "b128_r256", "b512_sched")
 KERNEL_SOURCES = {
     "sample": ["sample.cu", "markov_tile.cuh", "common.cuh"],
     "verify": ["verify.cu", "markov_tile.cuh", "common.cuh"],
@@ -138,17 +143,19 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def algorithmic_bytes(wl, n_rejected: int):
+def algorithmic_bytes(wl, n_rejected: int, n_verified: int):
+    """Bytes each call must move (bf16): sample reads every base row and W2 once; verify reads the
+    n_verified scheduled target rows, plus a base and a target row per rejection (and W2 once)."""
     B, g, V, r = wl.B, wl.gamma, wl.V, wl.r
     e = 2  # bf16
     sample = B * g * V * e + V * r * e + B * g * r * e + B * g * 12
-    verify = B * g * V * e + n_rejected * V * (e + e) + (V * r * e if n_rejected else 0) + B * 8
+    verify = n_verified * V * e + n_rejected * V * (e + e) + (V * r * e if n_rejected else 0) + B * 8
     tv = 2 * B * g * V * e + B * g * 8 + B * 4
     schedule = B * g * 4 + (2 * B + 1) * 4
     return {"sample": sample, "verify": verify, "tv": tv, "schedule": schedule}
 
 
-def run_cpu_baseline(wl_host, seconds: float = 15.0):
+def run_cpu_baseline(wl_host, seconds: float = 15.0, wl_name: str = WORKLOAD, T: float = 1.0):
     """The oracle, as it stands, on a bounded sample of the same batch: whole requests of the
     step (sample + verify + their accept-rate rows), plus the scheduler over the batch."""
     import numpy as np
@@ -161,9 +168,9 @@ def run_cpu_baseline(wl_host, seconds: float = 15.0):
     O.schedule(conf, B * g)
     done = 0
     for j in range(B):
-        tok, lse, zat, _ = O.sample_request(base, W1, W2, int(anchor[j]), j, 1.0, 0, 1024)
+        tok, lse, zat, _ = O.sample_request(base, W1, W2, int(anchor[j]), j, T, 0, 1024)
         O.verify_request(base, W1, W2, int(anchor[j]), j, tok, lse.astype(np.float32), zat.astype(np.float32), target,
-                         g, 1.0, 0, 1024)
+                         g, T, 0, 1024)
         for i in range(g):
             O.tv_row(base[j, i], target[j, i])
         done += 1
@@ -171,14 +178,14 @@ def run_cpu_baseline(wl_host, seconds: float = 15.0):
             break
     el = time.perf_counter() - t0
     return {"value": done * g / el, "unit": "draft tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{done} of {B} requests of {WORKLOAD} (sample+verify+tv rows) + schedule over the batch, "
+            "sample": f"{done} of {B} requests of {wl_name} (sample+verify+tv rows) + schedule over the batch, "
                       f"single-threaded C oracle, {el:.1f} s"}
 
 
-def host_workload(device, data_seed=0):
+def host_workload(device, data_seed=0, name=WORKLOAD):
     from semi_ar_draft_gb300 import workloads as W
 
-    wl = W.b32_r64(device=device, data_seed=data_seed)
+    wl = getattr(W, name)(device=device, data_seed=data_seed)
     t = wl.tensors
     return wl, (W.np_view(t["base"]), W.np_view(t["W1"]), W.np_view(t["W2"]), t["anchor"].cpu().numpy(),
                 W.np_view(t["target"]), t["conf"].cpu().numpy())
@@ -189,7 +196,7 @@ def reference_arm(args, rank, world):
         return
     import numpy as np  # noqa: F401
 
-    wl, host = host_workload("cpu")
+    wl, host = host_workload("cpu", name=args.workload)
     B, g = wl.B, wl.gamma
     for _ in range(args.warmup):
         pass  # the oracle has no warm-up state
@@ -200,7 +207,7 @@ def reference_arm(args, rank, world):
     samples = []
     t_start = time.perf_counter()
     for _ in range(args.steps):
-        cb = run_cpu_baseline(host, seconds=per_step)
+        cb = run_cpu_baseline(host, seconds=per_step, wl_name=args.workload, T=wl.T)
         vals.append(cb["value"])
         samples.append(cb["sample"])
         if time.perf_counter() - t_start > budget_s and len(vals) >= 3:
@@ -210,7 +217,7 @@ def reference_arm(args, rank, world):
             "steps": len(vals), "steps_requested": args.steps, "warmup": args.warmup, "ms_per_step": B * g / v * 1e3,
             "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "B": B, "gamma": g, "V": wl.V, "r": wl.r, "T": wl.T},
+            "config": {"workload": args.workload, "B": B, "gamma": g, "V": wl.V, "r": wl.r, "T": wl.T},
             "cpu_baseline": {"value": v, "unit": "draft tokens/s", "cores": 1, "kind": "oracle", "sample": samples[0]},
             "e2e": {"value": v, "unit": "draft tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -223,6 +230,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD, choices=WORKLOADS)
     args = ap.parse_args()
     rank, world, local = dist_env()
     if args.impl == "reference":
@@ -244,10 +252,10 @@ def main():
         pg = dist
     # weak scaling: rank k runs its own shard (requests k*B .. k*B+B-1 of the job's batch):
     # its own seeded inputs and its own Philox key; no collective touches the data path
-    wl, host = host_workload(dev, data_seed=rank)
+    wl, host = host_workload(dev, data_seed=rank, name=args.workload)
     t = wl.tensors
     B, g, V = wl.B, wl.gamma, wl.V
-    budget = B * g
+    budget = wl.budget if wl.budget else B * g
     base, W1, W2, anchor, target, conf = t["base"], t["W1"], t["W2"], t["anchor"], t["target"], t["conf"]
     d4 = base.view(1, B, g, V)
     t4 = target.view(1, B, g, V)
@@ -292,6 +300,7 @@ def main():
     for w in (ws_s, ws_a, ws_v, ws_t):
         assert binding.dspark_get_device_status(w) == 0
     n_rej = int((nacc < Lout).sum().item())
+    n_ver = int(Lout.sum().item())
 
     names = ["schedule", "sample", "verify", "tv"]
     per = {n: [] for n in names}
@@ -341,7 +350,7 @@ def main():
     t_e2e = shard.max_over_ranks(sum(e2e_ms) / len(e2e_ms), pg, dev)
 
     avg = {n: sum(v) / len(v) for n, v in per.items()}
-    algo = algorithmic_bytes(wl, n_rej)
+    algo = algorithmic_bytes(wl, n_rej, n_ver)
     peak, peak_kind = peaks()
     dom = max(["sample", "verify", "tv"], key=lambda n: avg[n])
     achieved = algo[dom] / (avg[dom] * 1e-3) / 1e9
@@ -352,7 +361,7 @@ def main():
         "metric": METRIC, "value": round(value, 1), "unit": "draft tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": round(t_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; shapes and distributions of the workload)",
-        "config": {"workload": WORKLOAD, "B": B, "gamma": g, "V": V, "r": wl.r, "T": wl.T, "budget": budget,
+        "config": {"workload": args.workload, "B": B, "gamma": g, "V": V, "r": wl.r, "T": wl.T, "budget": budget,
                    "parallelism": f"replicas x{world}",
                    "l2": "flushed (256 MB write) before each step; per-step CUDA events exclude the flush",
                    "step": "schedule + sample + verify + tv(eval_mask, tau)"},
@@ -368,7 +377,7 @@ def main():
         "wall_s_timed": round(wall, 3),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = run_cpu_baseline(host)
+        line["cpu_baseline"] = run_cpu_baseline(host, wl_name=args.workload, T=wl.T)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg:

@@ -112,7 +112,7 @@ def b32_r64(device="cpu", data_seed=0, V=VOCAB, B=32) -> SampleWorkload:
 
 def b128_r256(device="cpu", data_seed=0, V=VOCAB, B=128) -> SampleWorkload:
     return make_sample_workload("b128_r256", B, 16, V, 256, 0.7, device=device, data_seed=data_seed,
-                                target_sigma=lambda i: sigma_linear(i, 16))
+                                target_sigma=lambda i: sigma_linear(i, 16), conf=True, budget=B * 16)
 
 
 def b512_sched(device="cpu", data_seed=0, V=VOCAB, B=512, budget=2048) -> SampleWorkload:
