@@ -51,7 +51,7 @@ __device__ int block_excl_scan(int v, int* tot, int* sh) {
 
 __global__ void __launch_bounds__(kSchedThreads, 1)
     schedule_kernel(int B, int gamma, const float* __restrict__ conf, int budget, int32_t* __restrict__ L_out,
-                    int32_t* __restrict__ off_out, float* __restrict__ obj_out) {
+                    int32_t* __restrict__ off_out, float* __restrict__ obj_out, int32_t* __restrict__ status) {
     extern __shared__ uint32_t a_bits[];  // [B * gamma]
     __shared__ int hist[256];
     __shared__ int scan_sh[64];
@@ -59,6 +59,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
     __shared__ int s_rem;
     __shared__ double red_d[kSchedWarps];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) *status = DSPARK_OK;  // one block and no device-side error: the status word is just reset
 
     // survival a_{j,i}: left-to-right fp32 products of clamped confidences
     for (int j = tid; j < B; j += kSchedThreads) {
@@ -181,14 +182,14 @@ extern "C" dspark_status dspark_schedule_verify_len(int B, int gamma, const floa
     if (budget < B) return DSPARK_ERR_BUDGET;
     if (!workspace || ((uintptr_t)workspace & 255u) || ws_bytes < kHeaderBytes) return DSPARK_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(workspace, 0, kHeaderBytes, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     const long long bg = (long long)B * gamma;
     const int budget_c = (long long)budget > bg ? (int)bg : budget;
     const size_t smem = sizeof(uint32_t) * (size_t)bg;
     int per_sm = 0;
     if (prepare_kernel((const void*)schedule_kernel, smem, kSchedThreads, &per_sm) != cudaSuccess)
         return DSPARK_ERR_CUDA;
-    schedule_kernel<<<1, kSchedThreads, smem, s>>>(B, gamma, conf, budget_c, verify_len, offsets, objective);
+    schedule_kernel<<<1, kSchedThreads, smem, s>>>(B, gamma, conf, budget_c, verify_len, offsets, objective,
+                                                   &static_cast<WsHeader*>(workspace)->status);
     if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
     return DSPARK_OK;
 }

@@ -38,6 +38,7 @@ struct VerifyArgs {
     const void* W2;
     const int32_t* anchor;
     const int32_t* tokens;
+    uint64_t limit_ns;  // bound of every wait of the persistent rows kernel
     const float* dlse;
     const float* zat;
     const void* target;
@@ -98,6 +99,73 @@ __device__ float2 block_argmax_pair(float m, int idx, float2* red) {
 }
 
 // ------------------------------------------------------------------------------- launch 1
+// The accept walk of request j by one warp (lane = segment of the rows' partial results, nseg of
+// them): the accept test at every position left to right, n_accepted, the greedy correction,
+// or the job (residual at the rejecting position, or the bonus row) for the second launch.
+template <typename TL>
+__device__ void accept_walk(const VerifyArgs& a, int j, int L, int lane) {
+    int n = L, corr = -1, jtype = JOB_NONE, jpos = 0, jprev = 0;
+    float jlse2 = 0.f;
+    const TL* tgt = reinterpret_cast<const TL*>(a.target);
+    for (int ii = 1; ii <= L; ++ii) {
+        const float2 p = lane < a.nseg ? __ldcg(&a.rowpart[((size_t)j * a.gamma + (ii - 1)) * a.nseg + lane])
+                                       : (a.greedy ? make_float2(-CUDART_INF_F, __int_as_float(0x7fffffff))
+                                                   : make_float2(-CUDART_INF_F, 0.f));
+        const int x = a.tokens[(size_t)j * a.gamma + ii - 1];
+        const bool xok = x >= 0 && x < a.V;
+        int accept;
+        int am = 0;
+        float lse2 = 0.f;
+        if (a.greedy) {
+            float m = p.x;
+            int idx = __float_as_int(p.y);
+            warp_argmax(m, idx);
+            am = idx;
+            accept = xok && (am == x);
+        } else {
+            const float M = warp_max(p.x);
+            const float S = warp_sum(p.x == -CUDART_INF_F ? 0.f : p.y * ex2(p.x - M));
+            lse2 = M + lg2(S);
+            accept = 0;
+            if (lane == 0 && xok) {
+                const float tx = load_logit<TL>(tgt, (size_t)(trow_off(a, j, ii) + x));
+                const float lnp = (tx * a.scale2 - lse2) * kLn2;
+                const float lnq = a.zat[(size_t)j * a.gamma + ii - 1] * a.invT - a.dlse[(size_t)j * a.gamma + ii - 1];
+                const float lnu = logf(uniform(a.seed, (uint32_t)j, (uint32_t)ii, DSPARK_P_ACCEPT, 0u));
+                accept = lnu < lnp - lnq;
+            }
+            accept = __shfl_sync(0xffffffffu, accept, 0);
+        }
+        if (!xok && lane == 0) record_status(&a.hdr->status, DSPARK_ERR_TOKEN_RANGE);
+        if (!accept) {
+            n = ii - 1;
+            if (!xok) break;
+            if (a.greedy) {
+                corr = am;
+            } else {
+                jtype = JOB_RESID;
+                jpos = ii;
+                jlse2 = lse2;
+                jprev = (ii == 1) ? a.anchor[j] : a.tokens[(size_t)j * a.gamma + ii - 2];
+                if (jprev < 0 || jprev >= a.V) {
+                    if (lane == 0) record_status(&a.hdr->status, DSPARK_ERR_TOKEN_RANGE);
+                    jtype = JOB_NONE;
+                }
+            }
+            break;
+        }
+    }
+    if (n == L && req_rows(a, j) > L) {
+        jtype = JOB_BONUS;
+        jpos = L + 1;
+    }
+    if (lane == 0) {
+        a.nacc[j] = n;
+        a.corr[j] = corr;
+        a.job[j] = make_int4(jtype, jpos, jprev, __float_as_int(jlse2));
+    }
+}
+
 template <typename TL>
 __global__ void __launch_bounds__(kThreads) verify_rows_kernel(VerifyArgs a) {
     __shared__ float2 red[kWarps];
@@ -184,58 +252,66 @@ __global__ void __launch_bounds__(kThreads) verify_rows_kernel(VerifyArgs a) {
     if (!s_last || tid >= 32) return;
     __threadfence();
 
-    // ---- accept walk of request j (one warp; lane = segment)
-    const int lane = tid;
+    accept_walk<TL>(a, j, L, tid);
+}
+
+// The accept walk when every row has one segment: lane q takes position q + 1 (32 at a time),
+// so the rows' partials, the tokens, the target logits at the tokens and the draft terms are
+// all read at once; the first rejection is the lowest lane whose test fails.  Same decisions
+// and outputs as accept_walk.
+template <typename TL>
+__device__ void accept_walk_lanes(const VerifyArgs& a, int j, int L, int lane) {
+    const TL* tgt = reinterpret_cast<const TL*>(a.target);
     int n = L, corr = -1, jtype = JOB_NONE, jpos = 0, jprev = 0;
     float jlse2 = 0.f;
-    const TL* tgt = reinterpret_cast<const TL*>(a.target);
-    for (int ii = 1; ii <= L; ++ii) {
-        const float2 p = lane < a.nseg ? __ldcg(&a.rowpart[((size_t)j * a.gamma + (ii - 1)) * a.nseg + lane])
-                                       : (a.greedy ? make_float2(-CUDART_INF_F, __int_as_float(0x7fffffff))
-                                                   : make_float2(-CUDART_INF_F, 0.f));
-        const int x = a.tokens[(size_t)j * a.gamma + ii - 1];
-        const bool xok = x >= 0 && x < a.V;
-        int accept;
-        int am = 0;
+    for (int base = 0; base < L; base += 32) {
+        const int ii = base + lane + 1;  // this lane's position
+        const bool act = ii <= L;
+        int accept = 1, xok = 1, am = 0;
         float lse2 = 0.f;
-        if (a.greedy) {
-            float m = p.x;
-            int idx = __float_as_int(p.y);
-            warp_argmax(m, idx);
-            am = idx;
-            accept = xok && (am == x);
-        } else {
-            const float M = warp_max(p.x);
-            const float S = warp_sum(p.x == -CUDART_INF_F ? 0.f : p.y * ex2(p.x - M));
-            lse2 = M + lg2(S);
-            accept = 0;
-            if (lane == 0 && xok) {
-                const float tx = load_logit<TL>(tgt, (size_t)(trow_off(a, j, ii) + x));
-                const float lnp = (tx * a.scale2 - lse2) * kLn2;
-                const float lnq = a.zat[(size_t)j * a.gamma + ii - 1] * a.invT - a.dlse[(size_t)j * a.gamma + ii - 1];
-                const float lnu = logf(uniform(a.seed, (uint32_t)j, (uint32_t)ii, DSPARK_P_ACCEPT, 0u));
-                accept = lnu < lnp - lnq;
-            }
-            accept = __shfl_sync(0xffffffffu, accept, 0);
-        }
-        if (!xok && lane == 0) record_status(&a.hdr->status, DSPARK_ERR_TOKEN_RANGE);
-        if (!accept) {
-            n = ii - 1;
-            if (!xok) break;
+        if (act) {
+            const float2 p = __ldcg(&a.rowpart[(size_t)j * a.gamma + (ii - 1)]);
+            const int x = a.tokens[(size_t)j * a.gamma + ii - 1];
+            xok = x >= 0 && x < a.V;
             if (a.greedy) {
-                corr = am;
+                am = __float_as_int(p.y);
+                accept = xok && (am == x);
+            } else {
+                lse2 = p.x + lg2(p.y);
+                accept = 0;
+                if (xok) {
+                    const float tx = load_logit<TL>(tgt, (size_t)(trow_off(a, j, ii) + x));
+                    const float lnp = (tx * a.scale2 - lse2) * kLn2;
+                    const float lnq = a.zat[(size_t)j * a.gamma + ii - 1] * a.invT - a.dlse[(size_t)j * a.gamma + ii - 1];
+                    const float lnu = logf(uniform(a.seed, (uint32_t)j, (uint32_t)ii, DSPARK_P_ACCEPT, 0u));
+                    accept = lnu < lnp - lnq;
+                }
+            }
+        }
+        const unsigned rej = __ballot_sync(0xffffffffu, act && !accept);
+        if (!rej) continue;
+        const int f = __ffs(rej) - 1;  // the first rejecting position of this group: base + f + 1
+        const int fx = __shfl_sync(0xffffffffu, xok, f);
+        const int fam = __shfl_sync(0xffffffffu, am, f);
+        const float flse2 = __shfl_sync(0xffffffffu, lse2, f);
+        const int fi = base + f + 1;
+        if (lane == 0 && !fx) record_status(&a.hdr->status, DSPARK_ERR_TOKEN_RANGE);
+        n = fi - 1;
+        if (fx) {
+            if (a.greedy) {
+                corr = fam;
             } else {
                 jtype = JOB_RESID;
-                jpos = ii;
-                jlse2 = lse2;
-                jprev = (ii == 1) ? a.anchor[j] : a.tokens[(size_t)j * a.gamma + ii - 2];
+                jpos = fi;
+                jlse2 = flse2;
+                jprev = (fi == 1) ? a.anchor[j] : a.tokens[(size_t)j * a.gamma + fi - 2];
                 if (jprev < 0 || jprev >= a.V) {
                     if (lane == 0) record_status(&a.hdr->status, DSPARK_ERR_TOKEN_RANGE);
                     jtype = JOB_NONE;
                 }
             }
-            break;
         }
+        break;
     }
     if (n == L && req_rows(a, j) > L) {
         jtype = JOB_BONUS;
@@ -246,6 +322,185 @@ __global__ void __launch_bounds__(kThreads) verify_rows_kernel(VerifyArgs a) {
         a.corr[j] = corr;
         a.job[j] = make_int4(jtype, jpos, jprev, __float_as_int(jlse2));
     }
+}
+
+// ------------------------------------------------------------------------------- launch 1, bf16
+// Persistent variant for bf16 target rows on 16-byte boundaries: one block per SM walks the
+// verified rows (r = blockIdx.x, blockIdx.x + G, ...; row r is position r % gamma + 1 of request
+// r / gamma, verified when that position is <= L_j).  A producer warp streams each row through a
+// ring of kVNS shared-memory slots with the bulk-copy engine; 16 consumer warps reduce it to
+// (max, sum 2^(t * scale2 - max)) (T > 0) or (max, lowest argmax) (T = 0).  The block that
+// completes a request's last row runs the accept walk (rows then have one segment).
+constexpr int kVCE = 8192;  // target ids per slot
+constexpr int kVNS = 13;    // ring slots (13 x 16 KB)
+constexpr int kVThreads = kThreads + 32;
+
+struct VRSmem {
+    uint16_t slots[kVNS][kVCE];
+    uint64_t full[kVNS];
+    uint64_t empty[kVNS];
+    float2 red[2][kWarps];
+    int s_last;
+    int abort;
+    int issued;  // chunks the producer has issued
+};
+
+__device__ __forceinline__ bool verified_row(const VerifyArgs& a, int r, int& j, int& i, int& L) {
+    j = r / a.gamma;
+    i = r % a.gamma + 1;
+    L = req_len(a, j);
+    return L >= 1 && L <= a.gamma && req_rows(a, j) >= L && i <= L;
+}
+
+__global__ void __launch_bounds__(kVThreads, 1) verify_rows_ws_kernel(VerifyArgs a) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    VRSmem& S = *reinterpret_cast<VRSmem*>(smem_raw);
+    volatile int* abort = &S.abort;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nrow_all = a.B * a.gamma;
+    const int nch = (a.V + kVCE - 1) / kVCE;
+    if (tid == 0) {
+        for (int k = 0; k < kVNS; ++k) {
+            mbar_init(&S.full[k], 1);
+            mbar_init(&S.empty[k], kWarps);
+        }
+        S.abort = 0;
+        S.issued = 0;
+        mbar_init_fence();
+        for (int j = blockIdx.x; j < a.B; j += gridDim.x) {  // requests without a valid length: no walk
+            const int L = req_len(a, j);
+            if (!(L >= 1 && L <= a.gamma && req_rows(a, j) >= L)) {
+                record_status(&a.hdr->status, DSPARK_ERR_TOKEN_RANGE);
+                a.nacc[j] = 0;
+                a.corr[j] = -1;
+                a.job[j] = make_int4(JOB_NONE, 0, 0, 0);
+            }
+        }
+    }
+    __syncthreads();
+    const __nv_bfloat16* tgt = reinterpret_cast<const __nv_bfloat16*>(a.target);
+    int q = 0;
+    if (warp == kWarps) {
+        // ---------------- producer warp
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();
+            for (int r = blockIdx.x; r < nrow_all; r += gridDim.x) {
+                int j, i, L;
+                if (!verified_row(a, r, j, i, L)) continue;
+                const __nv_bfloat16* row = tgt + trow_off(a, j, i);
+                for (int k = 0; k < nch; ++k, ++q) {
+                    const int slot = q % kVNS;
+                    if (q >= kVNS && !mbar_wait_or_abort(&S.empty[slot], (uint32_t)((q / kVNS - 1) & 1), abort,
+                                                        &a.hdr->status, a.limit_ns, false))
+                        break;
+                    const int len = min(kVCE, a.V - k * kVCE);
+                    mbar_arrive_expect_tx(&S.full[slot], (uint32_t)(2 * len));
+                    bulk_g2s_hint(&S.slots[slot][0], row + (size_t)k * kVCE, (uint32_t)(2 * len), &S.full[slot], pol);
+                    S.issued = q + 1;
+                }
+                if (*abort) break;
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- 16 consumer warps; thread t takes ids 8t .. 8t+7 and 4096+8t .. 4096+8t+7
+        int par = 0;
+        for (int r = blockIdx.x; r < nrow_all; r += gridDim.x) {
+            int j, i, L;
+            if (!verified_row(a, r, j, i, L)) continue;
+            float m = -CUDART_INF_F, sacc = 0.f;
+            int idx = 0x7fffffff;
+            for (int k = 0; k < nch; ++k, ++q) {
+                const int slot = q % kVNS;
+                const bool ok = mbar_wait_or_abort(&S.full[slot], (uint32_t)((q / kVNS) & 1), abort, &a.hdr->status,
+                                                   a.limit_ns, false);
+                const int len = min(kVCE, a.V - k * kVCE);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int o = h * (kVCE / 2) + 8 * tid;
+                    float x[8];
+                    if (ok && o < len) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(&S.slots[slot][o]);
+                        x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
+                        x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z); x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) x[e] = -CUDART_INF_F;
+                    }
+                    if (a.greedy) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            if (x[e] > m) {  // ids ascend within a thread: the first maximum is kept
+                                m = x[e];
+                                idx = k * kVCE + o + e;
+                            }
+                    } else {
+                        float gm = x[0];
+#pragma unroll
+                        for (int e = 1; e < 8; ++e) gm = fmaxf(gm, x[e]);
+                        const float mn = fmaxf(m, gm * a.scale2);
+                        if (mn != -CUDART_INF_F) {
+                            sacc = (m == -CUDART_INF_F) ? 0.f : sacc * ex2(m - mn);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) sacc += ex2(fmaf(x[e], a.scale2, -mn));
+                            m = mn;
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive_local(&S.empty[slot]);
+            }
+            // block combine -> the row's partial, then the request's counter
+            if (a.greedy) {
+                warp_argmax(m, idx);
+                if (lane == 0) S.red[par][warp] = make_float2(m, __int_as_float(idx));
+            } else {
+                const float M = warp_max(m);
+                const float Sm = warp_sum(m == -CUDART_INF_F ? 0.f : sacc * ex2(m - M));
+                if (lane == 0) S.red[par][warp] = make_float2(M, Sm);
+            }
+            named_barrier(1, kThreads);
+            if (warp == 0) {
+                float2 v = lane < kWarps ? S.red[par][lane]
+                                         : (a.greedy ? make_float2(-CUDART_INF_F, __int_as_float(0x7fffffff))
+                                                     : make_float2(-CUDART_INF_F, 0.f));
+                float2 res;
+                if (a.greedy) {
+                    int id = __float_as_int(v.y);
+                    warp_argmax(v.x, id);
+                    res = make_float2(v.x, __int_as_float(id));
+                } else {
+                    const float M = warp_max(v.x);
+                    const float Sm = warp_sum(v.x == -CUDART_INF_F ? 0.f : v.y * ex2(v.x - M));
+                    res = make_float2(M, Sm);
+                }
+                if (lane == 0) {
+                    if (!*abort) a.rowpart[(size_t)j * a.gamma + (i - 1)] = res;  // one segment per row
+                    __threadfence();
+                    const uint32_t old = atomicAdd(&a.cnt_req[j], 1u);
+                    S.s_last = (old == (uint32_t)(L - 1)) && !*abort;
+                }
+                __syncwarp();
+                if (S.s_last) {  // warp-uniform: every row of request j is in
+                    __threadfence();
+                    accept_walk_lanes<__nv_bfloat16>(a, j, L, lane);
+                }
+            }
+            par ^= 1;
+        }
+    }
+    __syncthreads();
+    // copies still in flight after an abort: wait for them (bounded) before the block leaves
+    if (tid == 0 && *abort) {
+        const int nq = S.issued;
+        const uint64_t t0 = global_ns();
+        for (int qq = max(0, nq - kVNS); qq < nq; ++qq) {
+            const int sl = qq % kVNS;
+            while (!mbar_try_wait(&S.full[sl], (uint32_t)((qq / kVNS) & 1)) && global_ns() - t0 < a.limit_ns) {
+            }
+        }
+    }
+    (void)q;
 }
 
 // ------------------------------------------------------------------------------- launch 2
@@ -526,6 +781,7 @@ extern "C" dspark_status dspark_verify(const dspark_sample_params* p, const void
     a.W2 = W2;
     a.anchor = anchor;
     a.tokens = tokens;
+    a.limit_ns = wait_limit_ns();
     a.dlse = draft_lse;
     a.zat = draft_logit_at_tok;
     a.target = target_logits;
@@ -548,9 +804,23 @@ extern "C" dspark_status dspark_verify(const dspark_sample_params* p, const void
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(workspace, 0, L.zero_bytes, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     void* args[] = {&a};
-    RowsFn rows = p->logits_dtype == DSPARK_BF16 ? verify_rows_kernel<__nv_bfloat16> : verify_rows_kernel<float>;
-    if (cudaLaunchKernel((const void*)rows, dim3(L.nseg, p->gamma, p->B), dim3(kThreads), args, 0, s) != cudaSuccess)
-        return DSPARK_ERR_CUDA;
+    const bool ws_rows = p->logits_dtype == DSPARK_BF16 && a.vec_t;
+    if (ws_rows) {  // persistent streaming kernel: rows have one segment
+        int per_sm = 0, sms = 0;
+        if (prepare_kernel((const void*)verify_rows_ws_kernel, sizeof(VRSmem), kVThreads, &per_sm) != cudaSuccess ||
+            per_sm < 1 || device_sm_count(&sms) != cudaSuccess)
+            return DSPARK_ERR_CUDA;
+        a.nseg = 1;
+        const int G = std::max(1, std::min(p->B * p->gamma, sms * per_sm));
+        if (cudaLaunchKernel((const void*)verify_rows_ws_kernel, dim3(G), dim3(kVThreads), args, sizeof(VRSmem), s) !=
+            cudaSuccess)
+            return DSPARK_ERR_CUDA;
+    } else {
+        RowsFn rows = p->logits_dtype == DSPARK_BF16 ? verify_rows_kernel<__nv_bfloat16> : verify_rows_kernel<float>;
+        if (cudaLaunchKernel((const void*)rows, dim3(L.nseg, p->gamma, p->B), dim3(kThreads), args, 0, s) !=
+            cudaSuccess)
+            return DSPARK_ERR_CUDA;
+    }
     RowsFn jobs = pick_jobs(p, mma);
     size_t smem = sizeof(float) * kRows * kXRow + sizeof(float2) * kRows * kChunks + align_up(sizeof(RowBlock), 16) +
                   sizeof(int4) * kRows + sizeof(float) * 64 + (mma ? 0 : sizeof(float) * kRows * (size_t)p->r);
