@@ -261,12 +261,40 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
 }
 // Bounded wait that also gives up at once when `*abort` is set; records DSPARK_ERR_TIMEOUT
 // and sets *abort on its own timeout.  cluster = acquire at cluster scope.
+// try_wait with a suspend-time hint: the thread sleeps in hardware until the phase completes or
+// about `ns` nanoseconds pass, so a waiting warp issues almost nothing.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t ns) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return done != 0;
+}
+
 __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort, int32_t* status,
                                                    uint64_t limit_ns, bool cluster) {
     auto test = [&]() { return cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
     if (test()) return true;
     const uint64_t t0 = global_ns();
     while (!test()) {
+        if (*abort) return false;
+        if (global_ns() - t0 > limit_ns) {
+            record_status(status, DSPARK_ERR_TIMEOUT);
+            *abort = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
+// mbar_wait_or_abort for a CTA-local barrier with suspended waits (bounded the same way).
+__device__ __forceinline__ bool mbar_wait_hint_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                        int32_t* status, uint64_t limit_ns) {
+    if (mbar_try_wait_hint(bar, parity, 100000u)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait_hint(bar, parity, 100000u)) {
         if (*abort) return false;
         if (global_ns() - t0 > limit_ns) {
             record_status(status, DSPARK_ERR_TIMEOUT);

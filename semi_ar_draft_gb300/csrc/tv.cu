@@ -197,12 +197,12 @@ __global__ void __launch_bounds__(kTVThreads, 1) tv_kernel(TVArgs a) {
 // Every wait is bounded; after a timeout the block-wide abort flag makes the consumers skip the
 // data while keeping the same sequence of named barriers, and in-flight copies are awaited.
 // ------------------------------------------------------------------------------------------
-constexpr int kCE = 4096;                 // ids per array per slot
-constexpr int kNS = 13;                   // ring slots (13 x 16 KB)
+constexpr int kCE = 8192;                 // ids per array per slot
+constexpr int kNS = 6;                    // ring slots (6 x 32 KB)
 constexpr int kWSCons = 512;              // consumer threads (16 warps)
 constexpr int kWSWarps = kWSCons / 32;
 constexpr int kWSThreads = kWSCons + 32;  // + one producer warp
-static_assert(kCE == 8 * kWSCons, "one 16-byte group of each array per consumer thread per slot");
+static_assert(kCE == 16 * kWSCons, "two 16-byte groups of each array per consumer thread per slot");
 
 struct TVRSmem {
     uint16_t slots[kNS][2][kCE];
@@ -229,6 +229,59 @@ struct TVRArgs {
 __device__ __forceinline__ void unpack_bf16x8(const uint4 w, float (&x)[8]) {
     x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
     x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z); x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
+}
+
+// A consumer thread's sixteen ids of a slot: 8 at `my0` and 8 at kCE/2 + my0 (each group a
+// conflict-free 16-byte read across the warp).
+__device__ __forceinline__ void load16(const uint16_t* slot_arr, int my0, float (&x)[16]) {
+    float lo[8], hi[8];
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(slot_arr + my0), lo);
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(slot_arr + kCE / 2 + my0), hi);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        x[e] = lo[e];
+        x[8 + e] = hi[e];
+    }
+}
+
+// Ids at or past the end of the row (the ragged last chunk) read as -inf: no mass, no max.
+__device__ __forceinline__ void mask_tail16(float (&xd)[16], float (&xt)[16], int my0, int tail) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        const int id = (e < 8 ? my0 + e : kCE / 2 + my0 + e - 8);
+        if (id >= tail) xd[e] = xt[e] = -CUDART_INF_F;
+    }
+}
+
+// Online (max, sum 2^(x log2e - max)) over sixteen more values, without branches: the running
+// sum is rescaled by 2^(m_old - m_new) (1 when the maximum did not grow), and the sixteen terms
+// are added as a tree.  While every value so far is -inf the pair stays (-inf, 0).
+__device__ __forceinline__ void lse_step16(const float (&x)[16], float& m, float& s) {
+    float g[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) g[e] = fmaxf(x[e], x[8 + e]);
+    const float gm = fmaxf(fmaxf(fmaxf(g[0], g[1]), fmaxf(g[2], g[3])), fmaxf(fmaxf(g[4], g[5]), fmaxf(g[6], g[7])));
+    const float mn = fmaxf(m, gm * kLog2e);
+    const bool none = mn == -CUDART_INF_F;
+    const float sc = none ? 0.f : ex2(m - mn);  // m = -inf, mn finite: 0
+    const float mo = none ? 0.f : mn;           // x = -inf then gives 2^-inf = 0, never NaN
+    float e[16];
+#pragma unroll
+    for (int h = 0; h < 16; ++h) e[h] = ex2(fmaf(x[h], kLog2e, -mo));
+#pragma unroll
+    for (int h = 0; h < 8; ++h) e[h] += e[8 + h];
+    s = fmaf(s, sc, ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7])));
+    m = mn;
+}
+
+// Sum over sixteen ids of 2^min(d log2e - Ld2, t log2e - Lt2), as a tree.
+__device__ __forceinline__ float minsum16(const float (&xd)[16], const float (&xt)[16], float Ld2, float Lt2) {
+    float e[16];
+#pragma unroll
+    for (int h = 0; h < 16; ++h) e[h] = ex2(fminf(fmaf(xd[h], kLog2e, -Ld2), fmaf(xt[h], kLog2e, -Lt2)));
+#pragma unroll
+    for (int h = 0; h < 8; ++h) e[h] += e[8 + h];
+    return ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
 }
 
 // Warp-wide combine of (max, sum 2^(x - max)) pairs: the max first, then one rescale per lane.
@@ -278,27 +331,32 @@ __global__ void __launch_bounds__(kWSThreads, 1) tv_rows_kernel(TVRArgs a) {
         __syncwarp();
     } else {
         // ---------------- 16 consumer warps
-        const int my0 = 8 * tid;  // this thread's ids in a slot: my0 .. my0 + 7 (conflict-free 16-byte reads)
-        int q = 0;
+        const int my0 = 8 * tid;
+        const int tail = a.V - (nch - 1) * kCE;  // ids in the last chunk of a row
+        int slot = 0;
+        uint32_t phase = 0;
+        // After an abort the waits return at once and the slots hold stale data: the arithmetic
+        // runs on it (shared-memory reads cannot fault) and the result is never stored.
+        auto take = [&](float (&xd)[16], float (&xt)[16], bool last) {
+            mbar_wait_hint_or_abort(&S.full[slot], phase, abort, &a.hdr->status, a.limit_ns);
+            load16(&S.slots[slot][0][0], my0, xd);
+            load16(&S.slots[slot][1][0], my0, xt);
+            if (last) mask_tail16(xd, xt, my0, tail);
+            __syncwarp();
+            if (lane == 0) mbar_arrive_local(&S.empty[slot]);
+            if (++slot == kNS) {
+                slot = 0;
+                phase ^= 1u;
+            }
+        };
         for (int rl = 0; rl < nrows; ++rl) {
-            // ---- pass 1: softmax statistics of d and t
+            // ---- pass 1: softmax statistics of d and t (log2 domain)
             float md = -CUDART_INF_F, sd = 0.f, mt = -CUDART_INF_F, st = 0.f;
-            for (int k = 0; k < nch; ++k, ++q) {
-                const int slot = q % kNS;
-                const bool ok = mbar_wait_or_abort(&S.full[slot], (uint32_t)((q / kNS) & 1), abort, &a.hdr->status,
-                                                   a.limit_ns, false);
-                float xd[8], xt[8];  // lanes without data merge -inf
-                if (ok && (k + 1 < nch || my0 < a.V - k * kCE)) {
-                    unpack_bf16x8(*reinterpret_cast<const uint4*>(&S.slots[slot][0][my0]), xd);
-                    unpack_bf16x8(*reinterpret_cast<const uint4*>(&S.slots[slot][1][my0]), xt);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) xd[e] = xt[e] = -CUDART_INF_F;
-                }
-                lse_merge8(xd, md, sd);
-                lse_merge8(xt, mt, st);
-                __syncwarp();
-                if (lane == 0) mbar_arrive_local(&S.empty[slot]);
+            for (int k = 0; k < nch; ++k) {
+                float xd[16], xt[16];
+                take(xd, xt, k == nch - 1);
+                lse_step16(xd, md, sd);
+                lse_step16(xt, mt, st);
             }
             {
                 const float2 wd = warp_lse_pair(md, sd);
@@ -314,24 +372,12 @@ __global__ void __launch_bounds__(kWSThreads, 1) tv_rows_kernel(TVRArgs a) {
                 Ld2 = cd.x + lg2(cd.y);
                 Lt2 = ct.x + lg2(ct.y);
             }
-            // ---- pass 2: sum of min(p, q)
+            // ---- pass 2: sum of min(p, q) = 2^min(d log2e - Ld2, t log2e - Lt2)
             float acc = 0.f;
-            for (int k = 0; k < nch; ++k, ++q) {
-                const int slot = q % kNS;
-                const bool ok = mbar_wait_or_abort(&S.full[slot], (uint32_t)((q / kNS) & 1), abort, &a.hdr->status,
-                                                   a.limit_ns, false);
-                if (ok && (k + 1 < nch || my0 < a.V - k * kCE)) {
-                    const uint4 wd = *reinterpret_cast<const uint4*>(&S.slots[slot][0][my0]);
-                    const uint4 wt = *reinterpret_cast<const uint4*>(&S.slots[slot][1][my0]);
-                    const uint32_t dw[4] = {wd.x, wd.y, wd.z, wd.w}, tw[4] = {wt.x, wt.y, wt.z, wt.w};
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        acc += ex2(fminf(fmaf(bf16_lo(dw[h]), kLog2e, -Ld2), fmaf(bf16_lo(tw[h]), kLog2e, -Lt2)));
-                        acc += ex2(fminf(fmaf(bf16_hi(dw[h]), kLog2e, -Ld2), fmaf(bf16_hi(tw[h]), kLog2e, -Lt2)));
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive_local(&S.empty[slot]);
+            for (int k = 0; k < nch; ++k) {
+                float xd[16], xt[16];
+                take(xd, xt, k == nch - 1);
+                acc += minsum16(xd, xt, Ld2, Lt2);
             }
             const float w = warp_sum(acc);
             if (lane == 0) S.red1[warp] = w;
