@@ -231,8 +231,30 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 w, float (&x)[8]) {
     x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z); x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
 }
 
+// Packed fp32x2 arithmetic (two lanes per instruction, each rounded as the scalar op).
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float2 up2(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 // A consumer thread's sixteen ids of a slot: 8 at `my0` and 8 at kCE/2 + my0 (each group a
-// conflict-free 16-byte read across the warp).
+// conflict-free 16-byte read across the warp).  x[2i], x[2i+1]: the two values of word i.
 __device__ __forceinline__ void load16(const uint16_t* slot_arr, int my0, float (&x)[16]) {
     float lo[8], hi[8];
     unpack_bf16x8(*reinterpret_cast<const uint4*>(slot_arr + my0), lo);
@@ -253,6 +275,14 @@ __device__ __forceinline__ void mask_tail16(float (&xd)[16], float (&xt)[16], in
     }
 }
 
+// Tree sum of eight packed pairs, then of the two lanes.
+__device__ __forceinline__ float tree_sum8x2(const uint64_t (&v)[8]) {
+    const uint64_t a = add2(add2(v[0], v[1]), add2(v[2], v[3]));
+    const uint64_t b = add2(add2(v[4], v[5]), add2(v[6], v[7]));
+    const float2 r = up2(add2(a, b));
+    return r.x + r.y;
+}
+
 // Online (max, sum 2^(x log2e - max)) over sixteen more values, without branches: the running
 // sum is rescaled by 2^(m_old - m_new) (1 when the maximum did not grow), and the sixteen terms
 // are added as a tree.  While every value so far is -inf the pair stays (-inf, 0).
@@ -260,28 +290,34 @@ __device__ __forceinline__ void lse_step16(const float (&x)[16], float& m, float
     float g[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) g[e] = fmaxf(x[e], x[8 + e]);
-    const float gm = fmaxf(fmaxf(fmaxf(g[0], g[1]), fmaxf(g[2], g[3])), fmaxf(fmaxf(g[4], g[5]), fmaxf(g[6], g[7])));
-    const float mn = fmaxf(m, gm * kLog2e);
+    const float gm = fmaxf(fmaxf(fmaxf(g[0], g[1]), fmaxf(g[2], g[3])), fmaxf(fmaxf(g[4], g[5]), fmaxf(g[6], g[7]))) *
+                     kLog2e;
+    const float mn = fmaxf(m, gm);
     const bool none = mn == -CUDART_INF_F;
     const float sc = none ? 0.f : ex2(m - mn);  // m = -inf, mn finite: 0
     const float mo = none ? 0.f : mn;           // x = -inf then gives 2^-inf = 0, never NaN
-    float e[16];
+    const uint64_t c2 = pk2(kLog2e, kLog2e), nm2 = pk2(-mo, -mo);
+    uint64_t e[8];
 #pragma unroll
-    for (int h = 0; h < 16; ++h) e[h] = ex2(fmaf(x[h], kLog2e, -mo));
-#pragma unroll
-    for (int h = 0; h < 8; ++h) e[h] += e[8 + h];
-    s = fmaf(s, sc, ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7])));
+    for (int h = 0; h < 8; ++h) {
+        const float2 y = up2(fma2(pk2(x[2 * h], x[2 * h + 1]), c2, nm2));
+        e[h] = pk2(ex2(y.x), ex2(y.y));
+    }
+    s = fmaf(s, sc, tree_sum8x2(e));
     m = mn;
 }
 
 // Sum over sixteen ids of 2^min(d log2e - Ld2, t log2e - Lt2), as a tree.
-__device__ __forceinline__ float minsum16(const float (&xd)[16], const float (&xt)[16], float Ld2, float Lt2) {
-    float e[16];
+__device__ __forceinline__ float minsum16(const float (&xd)[16], const float (&xt)[16], uint64_t c2, uint64_t nld2,
+                                          uint64_t nlt2) {
+    uint64_t e[8];
 #pragma unroll
-    for (int h = 0; h < 16; ++h) e[h] = ex2(fminf(fmaf(xd[h], kLog2e, -Ld2), fmaf(xt[h], kLog2e, -Lt2)));
-#pragma unroll
-    for (int h = 0; h < 8; ++h) e[h] += e[8 + h];
-    return ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
+    for (int h = 0; h < 8; ++h) {
+        const float2 yd = up2(fma2(pk2(xd[2 * h], xd[2 * h + 1]), c2, nld2));
+        const float2 yt = up2(fma2(pk2(xt[2 * h], xt[2 * h + 1]), c2, nlt2));
+        e[h] = pk2(ex2(fminf(yd.x, yt.x)), ex2(fminf(yd.y, yt.y)));
+    }
+    return tree_sum8x2(e);
 }
 
 // Warp-wide combine of (max, sum 2^(x - max)) pairs: the max first, then one rescale per lane.
@@ -337,11 +373,10 @@ __global__ void __launch_bounds__(kWSThreads, 1) tv_rows_kernel(TVRArgs a) {
         uint32_t phase = 0;
         // After an abort the waits return at once and the slots hold stale data: the arithmetic
         // runs on it (shared-memory reads cannot fault) and the result is never stored.
-        auto take = [&](float (&xd)[16], float (&xt)[16], bool last) {
+        auto take = [&](float (&xd)[16], float (&xt)[16]) {
             mbar_wait_hint_or_abort(&S.full[slot], phase, abort, &a.hdr->status, a.limit_ns);
             load16(&S.slots[slot][0][0], my0, xd);
             load16(&S.slots[slot][1][0], my0, xt);
-            if (last) mask_tail16(xd, xt, my0, tail);
             __syncwarp();
             if (lane == 0) mbar_arrive_local(&S.empty[slot]);
             if (++slot == kNS) {
@@ -352,9 +387,16 @@ __global__ void __launch_bounds__(kWSThreads, 1) tv_rows_kernel(TVRArgs a) {
         for (int rl = 0; rl < nrows; ++rl) {
             // ---- pass 1: softmax statistics of d and t (log2 domain)
             float md = -CUDART_INF_F, sd = 0.f, mt = -CUDART_INF_F, st = 0.f;
-            for (int k = 0; k < nch; ++k) {
+            for (int k = 0; k < nch - 1; ++k) {
                 float xd[16], xt[16];
-                take(xd, xt, k == nch - 1);
+                take(xd, xt);
+                lse_step16(xd, md, sd);
+                lse_step16(xt, mt, st);
+            }
+            {
+                float xd[16], xt[16];
+                take(xd, xt);
+                mask_tail16(xd, xt, my0, tail);
                 lse_step16(xd, md, sd);
                 lse_step16(xt, mt, st);
             }
@@ -373,11 +415,18 @@ __global__ void __launch_bounds__(kWSThreads, 1) tv_rows_kernel(TVRArgs a) {
                 Lt2 = ct.x + lg2(ct.y);
             }
             // ---- pass 2: sum of min(p, q) = 2^min(d log2e - Ld2, t log2e - Lt2)
+            const uint64_t c2 = pk2(kLog2e, kLog2e), nld2 = pk2(-Ld2, -Ld2), nlt2 = pk2(-Lt2, -Lt2);
             float acc = 0.f;
-            for (int k = 0; k < nch; ++k) {
+            for (int k = 0; k < nch - 1; ++k) {
                 float xd[16], xt[16];
-                take(xd, xt, k == nch - 1);
-                acc += minsum16(xd, xt, Ld2, Lt2);
+                take(xd, xt);
+                acc += minsum16(xd, xt, c2, nld2, nlt2);
+            }
+            {
+                float xd[16], xt[16];
+                take(xd, xt);
+                mask_tail16(xd, xt, my0, tail);
+                acc += minsum16(xd, xt, c2, nld2, nlt2);
             }
             const float w = warp_sum(acc);
             if (lane == 0) S.red1[warp] = w;
