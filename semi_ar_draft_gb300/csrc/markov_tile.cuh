@@ -51,14 +51,6 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t a0, const
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// L2 prefetch of a contiguous byte range (16-byte aligned, multiple of 16 bytes).
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-// The same with an L2 eviction policy for the prefetched lines.
-__device__ __forceinline__ void prefetch_l2_hint(const void* p, uint32_t bytes, uint64_t pol) {
-    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(p), "r"(bytes), "l"(pol) : "memory");
-}
 
 // --------------------------------------------------------------------------------------------
 // Tensor-core bias: mma.sync m16n8k16, rows = 16 requests (A = W1[prev]), columns = 8 ids

@@ -55,3 +55,26 @@ def test_identical_rows_give_one():
 def test_full_tv_4x512x8_sampled_rows():
     tv = W.make_tv_workload(device="cuda", truncate=True)
     check(tv, rows=[(0, 0), (1, 77), (2, 300), (3, 511)])
+
+
+@pytest.mark.parametrize(
+    "S,A,g,V",
+    [
+        (1, 1, 1, 8192),  # one row of one ring slot
+        (1, 1, 8, 151936),  # 8 rows: fewer rows than blocks
+        (1, 3, 7, 20000),  # partial last slots
+        (1, 16, 8, 151936),  # 128 rows
+        (1, 32, 8, 151936),  # 256 rows: a ragged second round of rows
+        (1, 19, 16, 65536),  # 304 rows: two full rounds
+    ],
+)
+def test_batch_shapes(S, A, g, V):
+    check(W.make_tv_workload(S, A, g, V, device="cuda", data_seed=S * 1000 + A * 10 + g, truncate=True, drop=0.2))
+
+
+def test_repeated_calls_are_bit_identical():
+    tv = W.make_tv_workload(1, 16, 8, 151936, device="cuda", data_seed=9)
+    t = tv.tensors
+    a1 = api.accept_rate_tv(t["d"], t["t"], t["keep"])[0].clone()
+    a2 = api.accept_rate_tv(t["d"], t["t"], t["keep"])[0]
+    assert torch.equal(a1, a2)
