@@ -286,7 +286,7 @@ __host__ __device__ inline StagedLayout staged_layout(int B, int r, bool w2_smem
     L.lnEt = o;
     o += sizeof(float) * kChunks * (size_t)L.lnE_rows;
     L.bars = o;
-    o += 64;  // full[2], empty[2]; flags: abort, ok, reduced count, bases issued, W1 rows done [2]
+    o += 64;  // full[2], empty[2], reduced barrier; flags: abort, ok, reduced count, bases issued, W1 rows done [2]
     L.w2s = o;
     if (w2_smem) o += (size_t)kTS * r * 2;
     L.total = o;
@@ -443,14 +443,20 @@ __device__ void copy_issuer(const SampleArgs& a, uint16_t* stage, uint64_t* full
 // Arriver: once the compute warps have issued a row block's maxima, one release-arrival on that
 // row block's grid-wide counter (the release waits for the maxima to be performed in L2: that
 // wait happens here, not in the compute warps).
-__device__ void arriver(const SampleArgs& a, volatile int* reduced, volatile int* abort) {
+__device__ void arriver(const SampleArgs& a, volatile int* reduced, uint64_t* redbar, volatile int* abort) {
     const int lane = threadIdx.x & 31;
     const int nrb = (a.B + kRows - 1) / kRows, total = a.gamma * nrb;
     for (int cnt = 0; cnt < total; ++cnt) {
         const uint64_t t0 = global_ns();
         bool ok = false;
         while (true) {
-            int done = lane == 0 ? (ld_acquire_cta(reduced) > cnt ? 1 : 0) : 0;
+            // the count decides; the barrier (one phase per row block) only wakes this warp, so a
+            // phase that went by unseen costs one suspended wait, never a wrong count
+            int done = 0;
+            if (lane == 0) {
+                done = ld_acquire_cta(reduced) > cnt ? 1 : 0;
+                if (!done) mbar_try_wait_hint(redbar, (uint32_t)(cnt & 1), 4000u);
+            }
             if (__shfl_sync(0xffffffffu, done, 0)) {
                 ok = true;
                 break;
@@ -598,7 +604,8 @@ __global__ void __launch_bounds__(kStagedThreads, 1) sample_staged_kernel(Sample
     float* lnEt = reinterpret_cast<float*>(smem_raw + L.lnEt);          // [kChunks][lnE_rows]
     uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + L.bars);    // [2] stage buffer filled (2 arrivals)
     uint64_t* empty = full + 2;                                         // [2] stage buffer released
-    volatile int* flags = reinterpret_cast<volatile int*>(full + 4);
+    uint64_t* redbar = full + 4;                                        // a phase per row block reduced
+    volatile int* flags = reinterpret_cast<volatile int*>(full + 5);
     volatile int* abort = flags + 0;
     volatile int* s_ok = flags + 1;
     volatile int* reduced = flags + 2;  // row blocks whose maxima the compute warps have issued
@@ -616,6 +623,7 @@ __global__ void __launch_bounds__(kStagedThreads, 1) sample_staged_kernel(Sample
             mbar_init(&full[b], 2);
             mbar_init(&empty[b], 1);
         }
+        mbar_init(redbar, 1);
         for (int f = 0; f < 6; ++f) flags[f] = 0;
         mbar_init_fence();
     }
@@ -631,7 +639,7 @@ __global__ void __launch_bounds__(kStagedThreads, 1) sample_staged_kernel(Sample
     if (warp == kWarps) {
         copy_issuer<KS>(a, stage, full, empty, abort, nb_issued);
     } else if (warp == kWarps + 1) {
-        arriver(a, reduced, abort);
+        arriver(a, reduced, redbar, abort);
     } else if (warp >= kWarps + 2) {
         exchanger<KS>(a, warp - kWarps - 2, prev, w1s, full, empty, abort, w1_upto + (warp - kWarps - 2));
     } else {
@@ -686,7 +694,10 @@ __global__ void __launch_bounds__(kStagedThreads, 1) sample_staged_kernel(Sample
                     }
                 }
                 named_barrier(1, kThreads);
-                if (tid == 0) st_release_cta(reduced, cnt + 1);  // the arriver publishes this row block
+                if (tid == 0) {  // the arriver publishes this row block
+                    st_release_cta(reduced, cnt + 1);
+                    mbar_arrive_local(redbar);
+                }
             }
             if (!live) break;
             if (!GREEDY && step_table && step + 1 < a.gamma) {  // the next step's draws (this step's are read)

@@ -74,6 +74,32 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
     }
     const int K = budget - B;                  // extra slots
     const int ncand = B * (gamma - 1);         // candidates: positions i >= 2
+    if (K >= ncand) {  // the budget covers every position: L_j = gamma, no selection
+        // the same contiguous rows per thread and summation order as the general path below
+        __syncthreads();
+        const int rpt = (B + kSchedThreads - 1) / kSchedThreads;
+        const int r0 = min(B, tid * rpt), r1 = min(B, r0 + rpt);
+        double obj = 0.0;
+        for (int j = r0; j < r1; ++j) {
+            for (int i = 0; i < gamma; ++i) obj += (double)__uint_as_float(a_bits[j * gamma + i]);
+            L_out[j] = gamma;
+            off_out[j] = j * gamma;
+        }
+        if (tid == 0) off_out[B] = B * gamma;
+        if (obj_out) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) obj += __shfl_xor_sync(0xffffffffu, obj, o);
+            if (lane == 0) red_d[warp] = obj;
+            __syncthreads();
+            if (warp == 0) {
+                double q = lane < kSchedWarps ? red_d[lane] : 0.0;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+                if (lane == 0) obj_out[0] = (float)q;
+            }
+        }
+        return;
+    }
     if (tid == 0) {
         s_prefix = 0u;
         s_mask = 0u;
