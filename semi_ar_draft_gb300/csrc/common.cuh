@@ -206,6 +206,21 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                  : "memory");
 }
 // L2 eviction-priority policies (createpolicy): data read once goes first, data read again stays.
+__device__ __forceinline__ void red_max_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Order-preserving 32-bit image of a float (-0 taken as +0) above the complemented id.
+__device__ __forceinline__ unsigned long long pack_key(float key, int cand) {
+    const uint32_t b = __float_as_uint(__fadd_rn(key, 0.f));
+    const uint32_t o = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    return ((unsigned long long)o << 32) | (uint32_t)(~cand);
+}
+__device__ __forceinline__ float unpack_key(unsigned long long w) {
+    const uint32_t o = (uint32_t)(w >> 32);
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+
 // L2 prefetch of a contiguous byte range (16-byte aligned, multiple of 16 bytes).
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");

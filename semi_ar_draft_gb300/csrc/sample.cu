@@ -293,21 +293,6 @@ __host__ __device__ inline StagedLayout staged_layout(int B, int r, bool w2_smem
     return L;
 }
 
-__device__ __forceinline__ void red_max_u64(unsigned long long* p, unsigned long long v) {
-    asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-// Order-preserving 32-bit image of a float (-0 taken as +0) above the complemented id.
-__device__ __forceinline__ unsigned long long pack_key(float key, int cand) {
-    const uint32_t b = __float_as_uint(__fadd_rn(key, 0.f));
-    const uint32_t o = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-    return ((unsigned long long)o << 32) | (uint32_t)(~cand);
-}
-__device__ __forceinline__ float unpack_key(unsigned long long w) {
-    const uint32_t o = (uint32_t)(w >> 32);
-    return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
-}
-
 // Base rows of row block `cnt` (step cnt / nrb) over this block's tile (one warp): one of the two
 // arrivals of the buffer's full barrier, with the bytes; load_w1_rows() gives the other.
 __device__ __forceinline__ void issue_base(const SampleArgs& a, int cnt, int nrb, uint16_t* dst, uint64_t* bar) {
