@@ -226,32 +226,6 @@ struct TVRArgs {
     uint64_t limit_ns;
 };
 
-__device__ __forceinline__ void unpack_bf16x8(const uint4 w, float (&x)[8]) {
-    x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
-    x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z); x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
-}
-
-// Packed fp32x2 arithmetic (two lanes per instruction, each rounded as the scalar op).
-__device__ __forceinline__ uint64_t pk2(float a, float b) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-    return r;
-}
-__device__ __forceinline__ float2 up2(uint64_t v) {
-    float2 r;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
-    return r;
-}
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
 
 // A consumer thread's sixteen ids of a slot: 8 at `my0` and 8 at kCE/2 + my0 (each group a
 // conflict-free 16-byte read across the warp).  x[2i], x[2i+1]: the two values of word i.
@@ -273,38 +247,6 @@ __device__ __forceinline__ void mask_tail16(float (&xd)[16], float (&xt)[16], in
         const int id = (e < 8 ? my0 + e : kCE / 2 + my0 + e - 8);
         if (id >= tail) xd[e] = xt[e] = -CUDART_INF_F;
     }
-}
-
-// Tree sum of eight packed pairs, then of the two lanes.
-__device__ __forceinline__ float tree_sum8x2(const uint64_t (&v)[8]) {
-    const uint64_t a = add2(add2(v[0], v[1]), add2(v[2], v[3]));
-    const uint64_t b = add2(add2(v[4], v[5]), add2(v[6], v[7]));
-    const float2 r = up2(add2(a, b));
-    return r.x + r.y;
-}
-
-// Online (max, sum 2^(x log2e - max)) over sixteen more values, without branches: the running
-// sum is rescaled by 2^(m_old - m_new) (1 when the maximum did not grow), and the sixteen terms
-// are added as a tree.  While every value so far is -inf the pair stays (-inf, 0).
-__device__ __forceinline__ void lse_step16(const float (&x)[16], float& m, float& s) {
-    float g[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) g[e] = fmaxf(x[e], x[8 + e]);
-    const float gm = fmaxf(fmaxf(fmaxf(g[0], g[1]), fmaxf(g[2], g[3])), fmaxf(fmaxf(g[4], g[5]), fmaxf(g[6], g[7]))) *
-                     kLog2e;
-    const float mn = fmaxf(m, gm);
-    const bool none = mn == -CUDART_INF_F;
-    const float sc = none ? 0.f : ex2(m - mn);  // m = -inf, mn finite: 0
-    const float mo = none ? 0.f : mn;           // x = -inf then gives 2^-inf = 0, never NaN
-    const uint64_t c2 = pk2(kLog2e, kLog2e), nm2 = pk2(-mo, -mo);
-    uint64_t e[8];
-#pragma unroll
-    for (int h = 0; h < 8; ++h) {
-        const float2 y = up2(fma2(pk2(x[2 * h], x[2 * h + 1]), c2, nm2));
-        e[h] = pk2(ex2(y.x), ex2(y.y));
-    }
-    s = fmaf(s, sc, tree_sum8x2(e));
-    m = mn;
 }
 
 // Sum over sixteen ids of 2^min(d log2e - Ld2, t log2e - Lt2), as a tree.
@@ -390,15 +332,15 @@ __global__ void __launch_bounds__(kWSThreads, 1) tv_rows_kernel(TVRArgs a) {
             for (int k = 0; k < nch - 1; ++k) {
                 float xd[16], xt[16];
                 take(xd, xt);
-                lse_step16(xd, md, sd);
-                lse_step16(xt, mt, st);
+                lse_step16(xd, kLog2e, md, sd);
+                lse_step16(xt, kLog2e, mt, st);
             }
             {
                 float xd[16], xt[16];
                 take(xd, xt);
                 mask_tail16(xd, xt, my0, tail);
-                lse_step16(xd, md, sd);
-                lse_step16(xt, mt, st);
+                lse_step16(xd, kLog2e, md, sd);
+                lse_step16(xt, kLog2e, mt, st);
             }
             {
                 const float2 wd = warp_lse_pair(md, sd);

@@ -404,52 +404,55 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_rows_ws_kernel(VerifyArgs
         __syncwarp();
     } else {
         // ---------------- 16 consumer warps; thread t takes ids 8t .. 8t+7 and 4096+8t .. 4096+8t+7
-        int par = 0;
+        // After an abort the waits return at once and the slots hold stale data: the arithmetic runs
+        // on it (shared-memory reads cannot fault) and nothing is stored.
+        const int my0 = 8 * tid;
+        const int tail = a.V - (nch - 1) * kVCE;  // ids in the last chunk of a row
+        int par = 0, slot = 0;
+        uint32_t phase = 0;
         for (int r = blockIdx.x; r < nrow_all; r += gridDim.x) {
             int j, i, L;
             if (!verified_row(a, r, j, i, L)) continue;
             float m = -CUDART_INF_F, sacc = 0.f;
             int idx = 0x7fffffff;
-            for (int k = 0; k < nch; ++k, ++q) {
-                const int slot = q % kVNS;
-                const bool ok = mbar_wait_or_abort(&S.full[slot], (uint32_t)((q / kVNS) & 1), abort, &a.hdr->status,
-                                                   a.limit_ns, false);
-                const int len = min(kVCE, a.V - k * kVCE);
+            auto chunk = [&](int k, bool last) {
+                mbar_wait_hint_or_abort(&S.full[slot], phase, abort, &a.hdr->status, a.limit_ns);
+                float x[16];
+                {
+                    float lo[8], hi[8];
+                    unpack_bf16x8(*reinterpret_cast<const uint4*>(&S.slots[slot][my0]), lo);
+                    unpack_bf16x8(*reinterpret_cast<const uint4*>(&S.slots[slot][kVCE / 2 + my0]), hi);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int o = h * (kVCE / 2) + 8 * tid;
-                    float x[8];
-                    if (ok && o < len) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(&S.slots[slot][o]);
-                        x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
-                        x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z); x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) x[e] = -CUDART_INF_F;
-                    }
-                    if (a.greedy) {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            if (x[e] > m) {  // ids ascend within a thread: the first maximum is kept
-                                m = x[e];
-                                idx = k * kVCE + o + e;
-                            }
-                    } else {
-                        float gm = x[0];
-#pragma unroll
-                        for (int e = 1; e < 8; ++e) gm = fmaxf(gm, x[e]);
-                        const float mn = fmaxf(m, gm * a.scale2);
-                        if (mn != -CUDART_INF_F) {
-                            sacc = (m == -CUDART_INF_F) ? 0.f : sacc * ex2(m - mn);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) sacc += ex2(fmaf(x[e], a.scale2, -mn));
-                            m = mn;
-                        }
+                    for (int e = 0; e < 8; ++e) {
+                        x[e] = lo[e];
+                        x[8 + e] = hi[e];
                     }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive_local(&S.empty[slot]);
-            }
+                if (++slot == kVNS) {
+                    slot = 0;
+                    phase ^= 1u;
+                }
+                if (last) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        if ((e < 8 ? my0 + e : kVCE / 2 + my0 + e - 8) >= tail) x[e] = -CUDART_INF_F;
+                }
+                if (a.greedy) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        if (x[e] > m) {  // ids ascend within a thread: the first maximum is kept
+                            m = x[e];
+                            idx = k * kVCE + (e < 8 ? my0 + e : kVCE / 2 + my0 + e - 8);
+                        }
+                } else {
+                    lse_step16(x, a.scale2, m, sacc);
+                }
+            };
+            for (int k = 0; k < nch - 1; ++k) chunk(k, false);
+            chunk(nch - 1, true);
+            q += nch;
             // block combine -> the row's partial, then the request's counter
             if (a.greedy) {
                 warp_argmax(m, idx);
