@@ -376,6 +376,24 @@ def main():
         "clocks": clk.summary(wall0, wall1 + 0.2),
         "wall_s_timed": round(wall, 3),
     }
+    # outside the step: the throughput-aware prefix choice on the same confidences (a per-request
+    # causal search; one launch), timed alone with CUDA events after the step's timing
+    sps = torch.clamp(1.0 - 0.05 * torch.arange(g + 1, dtype=torch.float32, device=dev), min=0.05)
+    ell = torch.empty(B, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        binding.dspark_theta_schedule(B, g, conf, sps, ell)
+    th_ms = []
+    for _ in range(200):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush.zero_()  # the device is busy while the launch below is submitted: the events time the kernel
+        e0.record()
+        binding.dspark_theta_schedule(B, g, conf, sps, ell)
+        e1.record()
+        th_ms.append((e0, e1))
+    torch.cuda.synchronize()
+    th_us = sorted(a.elapsed_time(b_) * 1e3 for a, b_ in th_ms)
+    line["extras"] = {"theta_schedule_us": round(th_us[len(th_us) // 2], 2),
+                      "theta_schedule": f"median of 200 launches over B={B} requests, gamma={g}; not part of the step"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = run_cpu_baseline(host, wl_name=args.workload, T=wl.T)
     if rank == 0:

@@ -204,6 +204,28 @@ dspark_status dspark_schedule_verify_len(int B, int gamma, const float* conf, in
                                          dspark_stream_t stream);
 
 /*
+ * Throughput-aware prefix choice with a causal stop (page "DSpark 深度解读：DeepSeek-V4 如何用
+ * 「半自回归」把推理速度提升 85%", section 5.1, 调度核心: 应该验证多少 token?), per request j:
+ *   a_k = prod_{i<=k} c_{j,i},   Theta_l = (1 + sum_{k<=l} a_k) * SPS(l + 1),   l = 0 .. gamma,
+ * searched from l = 0 upwards; the search stops at the first l with Theta_l < Theta_{l-1} and
+ * chooses l - 1 (gamma when it never stops).  The page's worked example prints conditional
+ * confidences as a_1, a_2; its Theta_2 holds only with a_2 = c_1 c_2, so a_k is the running
+ * product.  Everything is computed in IEEE single precision, one rounding per multiply and per
+ * add in the order above (no fused operations), so the choice is reproducible bit for bit.
+ * Arguments (device memory)
+ *   conf [B, gamma] float: conditional confidences, used as given (no clamping);
+ *   sps [gamma + 1] float: SPS(1) .. SPS(gamma + 1), the throughput profile for a verify of
+ *   l + 1 tokens, shared by the batch.
+ * Outputs (device memory)
+ *   ell [B] int32 in [0, gamma]; theta [B, gamma + 1] float or NULL: Theta_0 .. Theta_l as far as
+ *   the search evaluated them, NaN after.
+ * Host errors: DSPARK_ERR_INVALID_ARG for B < 1, gamma < 1 or a NULL conf / sps / ell.
+ * No workspace and no device-side errors.
+ */
+dspark_status dspark_theta_schedule(int B, int gamma, const float* conf, const float* sps, int32_t* ell,
+                                    float* theta, dspark_stream_t stream);
+
+/*
  * Draft sampling without any allocation by the caller.  (No counterpart on the pages: this is a
  * convenience of this library.)  Some callers cannot call cudaMalloc at all -- for instance a
  * plug-in running inside a serving process whose device memory is owned by someone else's

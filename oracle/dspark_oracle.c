@@ -577,17 +577,21 @@ int oracle_schedule(int B, int gamma, const float* conf, int budget, int32_t* L,
  *   Theta_l = (1 + sum_{k<=l} a_k) * SPS(l + 1),  a_k = prod_{i<=k} c_i,
  * searched causally from l = 0, stopping at the first l with
  * Theta_l < Theta_{l-1}; returns that l - 1 (or the last l).  theta_out
- * receives Theta_0..Theta_gamma as far as they were evaluated (NaN after). */
+ * receives Theta_0..Theta_gamma as far as they were evaluated (NaN after).
+ * The comparisons decide an integer, so they are taken in the precision of
+ * the CUDA path (the pages fix none): IEEE single, one rounding per multiply
+ * and per add in this order (compiled without contraction).  c and sps are
+ * single-precision values (narrowed exactly when given as such). */
 int oracle_theta_schedule(int gamma, const double* c, const double* sps, double* theta_out) {
-    double a = 1.0, acc = 0.0, prev = -INFINITY;
+    float a = 1.0f, acc = 0.0f, prev = -INFINITY;
     for (int l = 0; l <= gamma; ++l) theta_out[l] = NAN;
     for (int l = 0; l <= gamma; ++l) {
         if (l > 0) {
-            a *= c[l - 1];
-            acc += a;
+            a = a * (float)c[l - 1];
+            acc = acc + a;
         }
-        double th = (1.0 + acc) * sps[l];
-        theta_out[l] = th;
+        const float th = (1.0f + acc) * (float)sps[l];
+        theta_out[l] = (double)th;
         if (l > 0 && th < prev) return l - 1;
         prev = th;
     }

@@ -61,6 +61,16 @@ def accept_rate_tv(d, t, keep, pos_valid=None, want_tau=True, ws=None, out=None,
     return out[0], out[1], out[2], ws
 
 
+def theta_schedule(conf, sps, with_theta=False, stream=None):
+    """conf [B,gamma] f32, sps [gamma+1] f32 (device).  Returns (ell [B] int32, theta [B,gamma+1] f32 or None)."""
+    B, gamma = conf.shape
+    dev = conf.device
+    ell = torch.empty(B, dtype=torch.int32, device=dev)
+    theta = torch.empty((B, gamma + 1), dtype=torch.float32, device=dev) if with_theta else None
+    b.dspark_theta_schedule(B, gamma, conf, sps, ell, theta, stream)
+    return ell, theta
+
+
 def schedule_verify_len(conf, budget, ws=None, out=None, stream=None):
     """conf [B,gamma] f32.  Returns (verify_len [B], offsets [B+1], objective [1], workspace)."""
     B, gamma = conf.shape

@@ -59,6 +59,8 @@ def lib():
         L.dspark_schedule_workspace_size.restype = sz
         L.dspark_schedule_verify_len.argtypes = [i32, i32, vp, i32, vp, vp, vp, vp, sz, vp]
         L.dspark_schedule_verify_len.restype = i32
+        L.dspark_theta_schedule.argtypes = [i32, i32, vp, vp, vp, vp, vp]
+        L.dspark_theta_schedule.restype = i32
         L.dspark_get_device_status.argtypes = [vp, vp, C.POINTER(C.c_int32)]
         L.dspark_get_device_status.restype = i32
         L.dspark_set_wait_limit_ns.argtypes = [u64]
@@ -168,6 +170,12 @@ def dspark_schedule_verify_len(B, gamma, conf, budget, verify_len, offsets, obje
                                           _ptr(offsets), _ptr(objective), _ptr(workspace),
                                           workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "dspark_schedule_verify_len")
+
+
+def dspark_theta_schedule(B, gamma, conf, sps, ell, theta=None, stream=None):
+    st = lib().dspark_theta_schedule(int(B), int(gamma), _ptr(conf), _ptr(sps), _ptr(ell), _ptr(theta),
+                                     _stream(stream))
+    _check(st, "dspark_theta_schedule")
 
 
 def dspark_get_device_status(workspace, stream=None) -> int:

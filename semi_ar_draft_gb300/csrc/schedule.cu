@@ -189,6 +189,34 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
     }
 }
 
+// Throughput-aware prefix choice, one request per thread, in IEEE single precision with explicit
+// round-to-nearest operations (no contraction), in the order of the definition.
+__global__ void theta_kernel(int B, int gamma, const float* __restrict__ conf, const float* __restrict__ sps,
+                             int32_t* __restrict__ ell, float* __restrict__ theta) {
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= B) return;
+    float a = 1.f, acc = 0.f, prev = -CUDART_INF_F;
+    int out = gamma;
+    bool stopped = false;
+    for (int l = 0; l <= gamma; ++l) {
+        float th = CUDART_NAN_F;
+        if (!stopped) {
+            if (l > 0) {
+                a = __fmul_rn(a, conf[(size_t)j * gamma + l - 1]);
+                acc = __fadd_rn(acc, a);
+            }
+            th = __fmul_rn(__fadd_rn(1.f, acc), sps[l]);
+            if (l > 0 && th < prev) {
+                out = l - 1;
+                stopped = true;
+            }
+            prev = th;
+        }
+        if (theta) theta[(size_t)j * (gamma + 1) + l] = th;
+    }
+    ell[j] = out;
+}
+
 }  // namespace
 }  // namespace dspark
 
@@ -216,6 +244,15 @@ extern "C" dspark_status dspark_schedule_verify_len(int B, int gamma, const floa
         return DSPARK_ERR_CUDA;
     schedule_kernel<<<1, kSchedThreads, smem, s>>>(B, gamma, conf, budget_c, verify_len, offsets, objective,
                                                    &static_cast<WsHeader*>(workspace)->status);
+    if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+    return DSPARK_OK;
+}
+
+extern "C" dspark_status dspark_theta_schedule(int B, int gamma, const float* conf, const float* sps, int32_t* ell,
+                                               float* theta, dspark_stream_t stream) {
+    if (B < 1 || gamma < 1 || !conf || !sps || !ell) return DSPARK_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    theta_kernel<<<(unsigned)((B + 127) / 128), 128, 0, s>>>(B, gamma, conf, sps, ell, theta);
     if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
     return DSPARK_OK;
 }

@@ -74,6 +74,8 @@ def test_host_validation_needs_no_gpu(L):
     assert L.dspark_markov_sample_block(C.byref(ok), fake, fake, fake, fake, fake, fake, fake, vp(0x1001), 1 << 20, None) == 6
     # scheduler: budget < B, too many cells
     assert L.dspark_schedule_verify_len(8, 4, fake, 7, fake, fake, None, fake, 1 << 20, None) == 5
+    assert L.dspark_theta_schedule(0, 4, fake, fake, fake, None, None) == 1  # B < 1
+    assert L.dspark_theta_schedule(8, 4, fake, None, fake, None, None) == 1  # no SPS profile
     assert L.dspark_schedule_verify_len(4096, 8, fake, 8192, fake, fake, None, fake, 1 << 20, None) == 2
     # TV: bad dtype
     assert L.dspark_accept_rate_tv(1, 1, 1, 8, 7, fake, fake, fake, None, fake, fake, None, fake, 1 << 20, None) == 1
