@@ -392,8 +392,28 @@ def main():
         th_ms.append((e0, e1))
     torch.cuda.synchronize()
     th_us = sorted(a.elapsed_time(b_) * 1e3 for a, b_ in th_ms)
+    # teacher-forced block logits of the same batch (the drafted tokens as the true ones), fp32 out
+    zt = torch.empty((B, g, V), dtype=torch.float32, device=dev)
+    ws_z = binding.workspace(binding.dspark_markov_block_logits_workspace_size(p), dev)
+    for _ in range(3):
+        binding.dspark_markov_block_logits(p, base, W1, W2, anchor, tok, zt, ws_z)
+    bl = []
+    for _ in range(50):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush.zero_()
+        e0.record()
+        binding.dspark_markov_block_logits(p, base, W1, W2, anchor, tok, zt, ws_z)
+        e1.record()
+        bl.append((e0, e1))
+    torch.cuda.synchronize()
+    bl_us = sorted(a.elapsed_time(b_) * 1e3 for a, b_ in bl)[len(bl) // 2]
+    bl_bytes = B * g * V * base.element_size() + V * wl.r * W2.element_size() + B * g * V * 4
     line["extras"] = {"theta_schedule_us": round(th_us[len(th_us) // 2], 2),
-                      "theta_schedule": f"median of 200 launches over B={B} requests, gamma={g}; not part of the step"}
+                      "theta_schedule": f"median of 200 launches over B={B} requests, gamma={g}; not part of the step",
+                      "block_logits_us": round(bl_us, 2),
+                      "block_logits_frac_of_peak": round(bl_bytes / (bl_us * 1e-6) / 1e9 / peak, 4),
+                      "block_logits": f"teacher-forced z [B,gamma,V] fp32 of the batch, median of 50 launches, "
+                                      f"{bl_bytes} algorithmic bytes (base + W2 read, z written); not part of the step"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = run_cpu_baseline(host, wl_name=args.workload, T=wl.T)
     if rank == 0:

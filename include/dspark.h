@@ -204,6 +204,24 @@ dspark_status dspark_schedule_verify_len(int B, int gamma, const float* conf, in
                                          dspark_stream_t stream);
 
 /*
+ * Teacher-forced block logits of the Markov head (page "03 · DSpark 建模：Markov 与 Confidence",
+ * build_markov_head / VanillaMarkov, Eq. 5; apply_block_logits): at training time every position's
+ * bias comes from its true previous token, all positions at once:
+ *   z[j, i, :] = base[j, i, :] + W2 W1[prev_{j,i}],  prev_{j,0} = anchor[j],  prev_{j,i} = tokens[j, i-1].
+ * The same bias and add as dspark_markov_sample_block (params p: B, gamma, V, r, dtypes; T and
+ * seed are not used), without the draw.
+ * Arguments (device memory): base_logits [B, gamma, V] (logits_dtype); W1 [V, r], W2 [V, r]
+ * (w_dtype); anchor [B] int32; tokens [B, gamma] int32 (the true tokens; column gamma-1 is not read).
+ * Output: z_out [B, gamma, V] float32 (caller-owned).
+ * Workspace: dspark_markov_block_logits_workspace_size(p) bytes, 256-byte aligned.  A previous token
+ * outside [0, V) is clamped and recorded as DSPARK_ERR_TOKEN_RANGE in the workspace status.
+ */
+size_t dspark_markov_block_logits_workspace_size(const dspark_sample_params* p);
+dspark_status dspark_markov_block_logits(const dspark_sample_params* p, const void* base_logits, const void* W1,
+                                         const void* W2, const int32_t* anchor, const int32_t* tokens, float* z_out,
+                                         void* workspace, size_t ws_bytes, dspark_stream_t stream);
+
+/*
  * Throughput-aware prefix choice with a causal stop (page "DSpark 深度解读：DeepSeek-V4 如何用
  * 「半自回归」把推理速度提升 85%", section 5.1, 调度核心: 应该验证多少 token?), per request j:
  *   a_k = prod_{i<=k} c_{j,i},   Theta_l = (1 + sum_{k<=l} a_k) * SPS(l + 1),   l = 0 .. gamma,

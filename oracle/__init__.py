@@ -130,6 +130,18 @@ def markov_logits(base_row: np.ndarray, W1: np.ndarray | None, W2: np.ndarray | 
     return z
 
 
+def block_logits(base: np.ndarray, W1, W2, anchor, tokens) -> np.ndarray:
+    """Teacher-forced z[j, i] = markov_logits(base[j, i], W1, W2, prev_{j,i}) with prev_{j,0} = anchor[j] and
+    prev_{j,i} = tokens[j, i - 1] (P1 section on build_markov_head, apply_block_logits), in fp64."""
+    B, gamma, V = base.shape
+    z = np.empty((B, gamma, V))
+    for j in range(B):
+        for i in range(gamma):
+            prev = int(anchor[j]) if i == 0 else int(tokens[j, i - 1])
+            z[j, i] = markov_logits(base[j, i], W1, W2, prev)
+    return z
+
+
 def argmax(z: np.ndarray):
     z = np.ascontiguousarray(z, dtype=np.float64)
     m = np.zeros(1)

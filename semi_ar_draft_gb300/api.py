@@ -61,6 +61,16 @@ def accept_rate_tv(d, t, keep, pos_valid=None, want_tau=True, ws=None, out=None,
     return out[0], out[1], out[2], ws
 
 
+def markov_block_logits(base, W1, W2, anchor, tokens, stream=None):
+    """Teacher-forced z = base + W2 W1[prev] at every position.  base [B,gamma,V]; returns z [B,gamma,V] f32."""
+    p = make_params(base, W1, 1.0, 0)
+    B, gamma, V = base.shape
+    z = torch.empty((B, gamma, V), dtype=torch.float32, device=base.device)
+    ws = b.workspace(b.dspark_markov_block_logits_workspace_size(p), base.device)
+    b.dspark_markov_block_logits(p, base, W1, W2, anchor, tokens, z, ws, stream)
+    return z, ws
+
+
 def theta_schedule(conf, sps, with_theta=False, stream=None):
     """conf [B,gamma] f32, sps [gamma+1] f32 (device).  Returns (ell [B] int32, theta [B,gamma+1] f32 or None)."""
     B, gamma = conf.shape

@@ -59,6 +59,10 @@ def lib():
         L.dspark_schedule_workspace_size.restype = sz
         L.dspark_schedule_verify_len.argtypes = [i32, i32, vp, i32, vp, vp, vp, vp, sz, vp]
         L.dspark_schedule_verify_len.restype = i32
+        L.dspark_markov_block_logits_workspace_size.argtypes = [C.POINTER(SampleParams)]
+        L.dspark_markov_block_logits_workspace_size.restype = sz
+        L.dspark_markov_block_logits.argtypes = [C.POINTER(SampleParams), vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.dspark_markov_block_logits.restype = i32
         L.dspark_theta_schedule.argtypes = [i32, i32, vp, vp, vp, vp, vp]
         L.dspark_theta_schedule.restype = i32
         L.dspark_get_device_status.argtypes = [vp, vp, C.POINTER(C.c_int32)]
@@ -170,6 +174,17 @@ def dspark_schedule_verify_len(B, gamma, conf, budget, verify_len, offsets, obje
                                           _ptr(offsets), _ptr(objective), _ptr(workspace),
                                           workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "dspark_schedule_verify_len")
+
+
+def dspark_markov_block_logits_workspace_size(p) -> int:
+    return int(lib().dspark_markov_block_logits_workspace_size(C.byref(p)))
+
+
+def dspark_markov_block_logits(p, base, W1, W2, anchor, tokens, z_out, workspace, stream=None):
+    st = lib().dspark_markov_block_logits(C.byref(p), _ptr(base), _ptr(W1), _ptr(W2), _ptr(anchor), _ptr(tokens),
+                                          _ptr(z_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                          _stream(stream))
+    _check(st, "dspark_markov_block_logits")
 
 
 def dspark_theta_schedule(B, gamma, conf, sps, ell, theta=None, stream=None):

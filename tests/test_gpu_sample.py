@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import oracle as O
-from parity import Tally, compare_block
+from parity import Tally, close, compare_block
 from semi_ar_draft_gb300 import api, binding
 from semi_ar_draft_gb300 import workloads as W
 
@@ -119,3 +119,52 @@ def test_vocabulary_beyond_one_tile_per_sm(T):
     wl = W.make_sample_workload("wide", 4, 2, 160000, 64, T, device="cuda", data_seed=12, philox_seed=3, planted=2)
     tally, _ = run_and_compare(wl)
     tally.check_fraction()
+
+
+# ---------------------------------------------------------------- teacher-forced block logits
+def _block_logits_check(wl, tokens):
+    t = wl.tensors
+    z, ws = api.markov_block_logits(t["base"], t["W1"], t["W2"], t["anchor"], tokens)
+    torch.cuda.synchronize()
+    assert binding.dspark_get_device_status(ws) == 0
+    base = W.np_view(t["base"])
+    W1 = None if t["W1"] is None else W.np_view(t["W1"])
+    W2 = None if t["W2"] is None else W.np_view(t["W2"])
+    anchor, toks = t["anchor"].cpu().numpy(), tokens.cpu().numpy()
+    ref = O.block_logits(base, W1, W2, anchor, toks)
+    # Tolerance from the arithmetic: the kernel adds r products (bf16 or fp32 operands, exact in
+    # fp32) in fp32, so its error scales with the summed magnitude S = |base| + sum_k |W2[v,k] W1[prev,k]|
+    # (about sqrt(r) 2^-24 S, at most 1e-6 S for r <= 256), not with |z|, which cancellation can
+    # make small.  Plus the usual 1e-5 relative term.
+    S = np.abs(base.astype(np.float64))
+    if W1 is not None:
+        prev = np.concatenate([anchor[:, None], toks[:, :-1]], axis=1).astype(np.int64)
+        aW1 = np.abs(W1.astype(np.float64))[prev]  # [B, gamma, r]
+        S = S + np.einsum("bgk,vk->bgv", aW1, np.abs(W2.astype(np.float64)))
+    got = z.cpu().numpy().astype(np.float64)
+    bad = np.abs(got - ref) > 1e-5 * np.abs(ref) + 1e-6 * S
+    assert not bad.any(), f"block logits: {int(bad.sum())} values off; first {got[bad][:5]} vs {ref[bad][:5]}"
+
+
+@pytest.mark.parametrize("B,gamma,V,r", [(3, 5, 5000, 64), (2, 7, 4096, 16), (1, 3, 2048, 256), (32, 8, 151936, 64)])
+def test_block_logits_tensor_core(B, gamma, V, r):
+    wl = W.make_sample_workload("blk", B, gamma, V, r, 1.0, device="cuda", data_seed=B * 10 + r, w_std=0.3)
+    g = torch.Generator(device="cpu").manual_seed(B + gamma)
+    tokens = torch.randint(0, V, (B, gamma), generator=g, dtype=torch.int32).cuda()
+    _block_logits_check(wl, tokens)
+
+
+@pytest.mark.parametrize("wdt,r", [(torch.float32, 24), (torch.bfloat16, 24), (torch.float32, 0)])
+def test_block_logits_cuda_core(wdt, r):
+    wl = W.make_sample_workload("blkc", 4, 4, 3001, r, 1.0, device="cuda", data_seed=5, logits_dtype=torch.float32,
+                                w_dtype=wdt, w_std=0.3)
+    tokens = torch.randint(0, 3001, (4, 4), dtype=torch.int32).cuda()
+    _block_logits_check(wl, tokens)
+
+
+def test_block_logits_token_out_of_range_sets_status():
+    wl = W.make_sample_workload("blkbad", 2, 3, 2048, 16, 1.0, device="cuda")
+    t = wl.tensors
+    tokens = torch.tensor([[1, 5000, 3], [4, 5, 6]], dtype=torch.int32, device="cuda")
+    _, ws = api.markov_block_logits(t["base"], t["W1"], t["W2"], t["anchor"], tokens)
+    assert binding.dspark_get_device_status(ws) == 7  # DSPARK_ERR_TOKEN_RANGE

@@ -172,6 +172,36 @@ def test_sample_request_greedy_chain():
             prev = tok[i]
 
 
+def test_block_logits_with_the_drafts_own_tokens_replays_the_draft():
+    # teacher forcing with the greedy draft's own tokens must give back, at every position, the
+    # draft's argmax and its z at the token (the previous-token rule against the sampler's carry)
+    rng = np.random.default_rng(8)
+    B, gamma, V, r = 3, 5, 96, 4
+    base = rng.normal(0, 2, (B, gamma, V)).astype(np.float32)
+    W1 = rng.normal(0, 0.7, (V, r)).astype(np.float32)
+    W2 = rng.normal(0, 0.7, (V, r)).astype(np.float32)
+    anchor = np.array([5, 17, 95], np.int32)
+    toks = np.zeros((B, gamma), np.int32)
+    zats = np.zeros((B, gamma))
+    for j in range(B):
+        tok, _, zx, _ = O.sample_request(base, W1, W2, anchor[j], j, 0.0, 0, 1024)
+        toks[j], zats[j] = tok, zx
+    z = O.block_logits(base, W1, W2, anchor, toks)
+    assert z.shape == (B, gamma, V)
+    for j in range(B):
+        for i in range(gamma):
+            assert int(np.argmax(z[j, i])) == toks[j, i]
+            assert z[j, i, toks[j, i]] == zats[j, i]
+    # a different token at position i changes only position i + 1's bias
+    t2 = toks.copy()
+    t2[1, 2] = (t2[1, 2] + 1) % V
+    z2 = O.block_logits(base, W1, W2, anchor, t2)
+    changed = np.argwhere(np.any(z2 != z, axis=-1))
+    assert changed.tolist() == [[1, 3]]
+    # no Markov head: z is the base row
+    assert np.array_equal(O.block_logits(base, None, None, anchor, toks), base.astype(np.float64))
+
+
 def test_sample_request_carries_token_and_lse():
     rng = np.random.default_rng(6)
     B, gamma, V, r = 1, 5, 50, 4
