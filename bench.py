@@ -408,7 +408,21 @@ def main():
     torch.cuda.synchronize()
     bl_us = sorted(a.elapsed_time(b_) * 1e3 for a, b_ in bl)[len(bl) // 2]
     bl_bytes = B * g * V * base.element_size() + V * wl.r * W2.element_size() + B * g * V * 4
-    line["extras"] = {"theta_schedule_us": round(th_us[len(th_us) // 2], 2),
+    # the training-side L1 term on this step's accept rates (one block)
+    l1b = torch.empty_like(acc)
+    l1s = torch.empty(2, dtype=torch.float64, device=dev)
+    l1t = []
+    for _ in range(50):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush.zero_()
+        e0.record()
+        binding.dspark_tv_l1_loss(1, B, g, acc, emask, 4.0, l1b, l1s)
+        e1.record()
+        l1t.append((e0, e1))
+    torch.cuda.synchronize()
+    l1_us = sorted(a.elapsed_time(b_) * 1e3 for a, b_ in l1t)[len(l1t) // 2]
+    line["extras"] = {"tv_l1_loss_us": round(l1_us, 2),
+                      "theta_schedule_us": round(th_us[len(th_us) // 2], 2),
                       "theta_schedule": f"median of 200 launches over B={B} requests, gamma={g}; not part of the step",
                       "block_logits_us": round(bl_us, 2),
                       "block_logits_frac_of_peak": round(bl_bytes / (bl_us * 1e-6) / 1e9 / peak, 4),

@@ -204,6 +204,23 @@ dspark_status dspark_schedule_verify_len(int B, int gamma, const float* conf, in
                                          dspark_stream_t stream);
 
 /*
+ * Training-side L1 term on the accept rates (page "03 · DSpark 建模：Markov 与 Confidence",
+ * section 3.9, the three weighted loss terms; the L1 / TV loss l1_dist = sum_v |softmax(d) -
+ * softmax(t)|, with the position weights w_k = exp(-(k-1)/loss_decay_gamma)).  Per position
+ * (s, a, k), k = 1..gamma:
+ *   l1 = 2 (1 - accept_rate)          (sum |p - q| = 2 (1 - sum min(p, q)))
+ *   sums[0] = sum w_k eval_mask l1,   sums[1] = sum w_k eval_mask
+ * The two sums are returned apart so that ranks can add them before dividing.  Another page writes
+ * the weight as e^(-k/gamma); the page that cites the loss code writes k-1, which is used here.
+ * Arguments (device memory): accept_rate, eval_mask [S, A, gamma] float (dspark_accept_rate_tv's
+ * outputs); decay_gamma > 0 (the pages use 4).
+ * Outputs (device memory): l1 [S, A, gamma] float or NULL; sums [2] double.
+ * The sums are added in a fixed order: the same inputs give the same bits.
+ */
+dspark_status dspark_tv_l1_loss(int S, int A, int gamma, const float* accept_rate, const float* eval_mask,
+                                float decay_gamma, float* l1, double* sums, dspark_stream_t stream);
+
+/*
  * Teacher-forced block logits of the Markov head (page "03 · DSpark 建模：Markov 与 Confidence",
  * build_markov_head / VanillaMarkov, Eq. 5; apply_block_logits): at training time every position's
  * bias comes from its true previous token, all positions at once:

@@ -245,6 +245,17 @@ def eval_mask_tau(acc: np.ndarray, keep: int, pos_valid: np.ndarray | None):
 
 
 # ----------------------------------------------------------------- schedulers
+def tv_l1_loss(acc: np.ndarray, mask: np.ndarray, decay: float = 4.0):
+    """L1 term on accept rates (P1 section 3.9): l1 = 2 (1 - acc) per position, weights
+    w_k = exp(-(k-1)/decay) for positions k = 1..gamma (the last axis); returns (l1, sum w mask l1,
+    sum w mask) in fp64."""
+    acc = np.asarray(acc, dtype=np.float64)
+    mask = np.asarray(mask, dtype=np.float64)
+    l1 = 2.0 * (1.0 - acc)
+    w = np.exp(-np.arange(acc.shape[-1]) / decay)
+    return l1, float(np.sum(w * mask * l1)), float(np.sum(w * mask))
+
+
 def schedule(conf: np.ndarray, budget: int):
     conf = np.ascontiguousarray(conf, dtype=np.float32)
     B, gamma = conf.shape

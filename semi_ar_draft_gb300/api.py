@@ -71,6 +71,15 @@ def markov_block_logits(base, W1, W2, anchor, tokens, stream=None):
     return z, ws
 
 
+def tv_l1_loss(accept_rate, eval_mask, decay_gamma=4.0, stream=None):
+    """accept_rate, eval_mask [S,A,gamma] f32.  Returns (l1 [S,A,gamma] f32, sums [2] f64: weighted numerator, denominator)."""
+    S, A, gamma = accept_rate.shape
+    l1 = torch.empty_like(accept_rate)
+    sums = torch.empty(2, dtype=torch.float64, device=accept_rate.device)
+    b.dspark_tv_l1_loss(S, A, gamma, accept_rate, eval_mask, decay_gamma, l1, sums, stream)
+    return l1, sums
+
+
 def theta_schedule(conf, sps, with_theta=False, stream=None):
     """conf [B,gamma] f32, sps [gamma+1] f32 (device).  Returns (ell [B] int32, theta [B,gamma+1] f32 or None)."""
     B, gamma = conf.shape

@@ -63,6 +63,8 @@ def lib():
         L.dspark_markov_block_logits_workspace_size.restype = sz
         L.dspark_markov_block_logits.argtypes = [C.POINTER(SampleParams), vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.dspark_markov_block_logits.restype = i32
+        L.dspark_tv_l1_loss.argtypes = [i32, i32, i32, vp, vp, C.c_float, vp, vp, vp]
+        L.dspark_tv_l1_loss.restype = i32
         L.dspark_theta_schedule.argtypes = [i32, i32, vp, vp, vp, vp, vp]
         L.dspark_theta_schedule.restype = i32
         L.dspark_get_device_status.argtypes = [vp, vp, C.POINTER(C.c_int32)]
@@ -185,6 +187,12 @@ def dspark_markov_block_logits(p, base, W1, W2, anchor, tokens, z_out, workspace
                                           _ptr(z_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                           _stream(stream))
     _check(st, "dspark_markov_block_logits")
+
+
+def dspark_tv_l1_loss(S, A, gamma, accept_rate, eval_mask, decay_gamma, l1, sums, stream=None):
+    st = lib().dspark_tv_l1_loss(int(S), int(A), int(gamma), _ptr(accept_rate), _ptr(eval_mask), float(decay_gamma),
+                                 _ptr(l1), _ptr(sums), _stream(stream))
+    _check(st, "dspark_tv_l1_loss")
 
 
 def dspark_theta_schedule(B, gamma, conf, sps, ell, theta=None, stream=None):

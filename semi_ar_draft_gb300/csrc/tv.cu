@@ -411,6 +411,50 @@ __global__ void tau_kernel(long long nblk, int gamma, const float* acc, const fl
     tau[b] = 1.f + expected;
 }
 
+// Training-side L1 term over the accept rates of a batch: l1 = sum_v |p - q| = 2 (1 - accept) per
+// position (accept = sum_v min(p, q)), position weights w_k = exp(-(k-1)/decay) for k = 1..gamma,
+// numerator sum w mask l1 and denominator sum w mask.  One block; every thread adds its elements in
+// index order in fp64 and the block adds the threads in a fixed tree, so the sums are deterministic.
+constexpr int kL1Threads = 512;
+__global__ void __launch_bounds__(kL1Threads) tv_l1_kernel(long long n, int gamma, const float* __restrict__ acc,
+                                                           const float* __restrict__ mask, double decay,
+                                                           float* __restrict__ l1, double* __restrict__ sums) {
+    __shared__ double red[2][kL1Threads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    double num = 0.0, den = 0.0;
+    for (long long e = tid; e < n; e += kL1Threads) {
+        const int k = (int)(e % gamma);  // position k + 1
+        const float d = 2.f * (1.f - acc[e]);
+        if (l1) l1[e] = d;
+        const double w = exp(-(double)k / decay) * (double)mask[e];
+        num += w * (double)d;
+        den += w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        num += __shfl_xor_sync(0xffffffffu, num, o);
+        den += __shfl_xor_sync(0xffffffffu, den, o);
+    }
+    if (lane == 0) {
+        red[0][warp] = num;
+        red[1][warp] = den;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        num = lane < kL1Threads / 32 ? red[0][lane] : 0.0;
+        den = lane < kL1Threads / 32 ? red[1][lane] : 0.0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            num += __shfl_xor_sync(0xffffffffu, num, o);
+            den += __shfl_xor_sync(0xffffffffu, den, o);
+        }
+        if (lane == 0) {
+            sums[0] = num;
+            sums[1] = den;
+        }
+    }
+}
+
 }  // namespace
 }  // namespace dspark
 
@@ -502,5 +546,16 @@ extern "C" dspark_status dspark_accept_rate_tv(int S, int A, int gamma, int V, i
         tau_kernel<<<(unsigned)((nblk + 255) / 256), 256, 0, s>>>(nblk, gamma, accept_rate, eval_mask, tau);
         if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
     }
+    return DSPARK_OK;
+}
+
+extern "C" dspark_status dspark_tv_l1_loss(int S, int A, int gamma, const float* accept_rate, const float* eval_mask,
+                                           float decay_gamma, float* l1, double* sums, dspark_stream_t stream) {
+    if (S < 1 || A < 1 || gamma < 1 || !accept_rate || !eval_mask || !sums) return DSPARK_ERR_INVALID_ARG;
+    if (!(decay_gamma > 0.f)) return DSPARK_ERR_INVALID_ARG;
+    const long long n = (long long)S * A * gamma;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    tv_l1_kernel<<<1, kL1Threads, 0, s>>>(n, gamma, accept_rate, eval_mask, (double)decay_gamma, l1, sums);
+    if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
     return DSPARK_OK;
 }

@@ -78,3 +78,17 @@ def test_repeated_calls_are_bit_identical():
     a1 = api.accept_rate_tv(t["d"], t["t"], t["keep"])[0].clone()
     a2 = api.accept_rate_tv(t["d"], t["t"], t["keep"])[0]
     assert torch.equal(a1, a2)
+
+
+def test_l1_loss_epilogue():
+    tv = W.make_tv_workload(2, 64, 8, 20000, device="cuda", data_seed=3, truncate=True, drop=0.2)
+    t = tv.tensors
+    acc, mask, _, _ = api.accept_rate_tv(t["d"], t["t"], t["keep"], t["pos_valid"])
+    l1, sums = api.tv_l1_loss(acc, mask, 4.0)
+    torch.cuda.synchronize()
+    r_l1, r_num, r_den = O.tv_l1_loss(acc.cpu().numpy(), mask.cpu().numpy(), 4.0)
+    assert np.abs(l1.cpu().numpy() - r_l1).max() < 1e-6  # 2 (1 - acc) in fp32
+    # each l1 is rounded to fp32 (2^-24 relative) before the fp64 sums: 1e-6 relative covers it
+    close(sums.cpu().numpy(), [r_num, r_den], rtol=1e-6, atol=1e-9, what="weighted L1 sums")
+    l1b, sums_b = api.tv_l1_loss(acc, mask, 4.0)
+    assert torch.equal(sums, sums_b) and torch.equal(l1, l1b)

@@ -1,6 +1,7 @@
 """Pins of the oracle's accept-rate target (P1 section 3.9 "Accept rate 3D";
 P2 section 3.5) and of eval_mask / tau (P1 sections 3.6 and 3.10)."""
 import numpy as np
+import pytest
 from scipy import special
 
 import oracle as O
@@ -67,3 +68,31 @@ def test_eval_mask_cumprod_and_tau():
     assert np.array_equal(m, np.zeros(4)) and tau == 1.0
     m, tau = O.eval_mask_tau(np.ones(8), 1, None)
     assert tau == 9.0
+
+
+def test_l1_term_is_the_sum_of_absolute_differences():
+    # the oracle's route (2 (1 - sum min(p, q)) from the TV row) against the page's definition
+    # sum_v |softmax(d) - softmax(t)| written out directly
+    rng = np.random.default_rng(11)
+    for V in (7, 100, 3000):
+        d = rng.normal(0, 2, V).astype(np.float32)
+        t = (0.6 * d + rng.normal(0, 1.5, V)).astype(np.float32)
+        acc, _ = O.tv_row(d, t)
+        p = np.exp(d.astype(np.float64) - d.max())
+        p /= p.sum()
+        q = np.exp(t.astype(np.float64) - t.max())
+        q /= q.sum()
+        l1, _, _ = O.tv_l1_loss(np.array([[[acc]]]), np.ones((1, 1, 1)))
+        assert abs(l1[0, 0, 0] - np.abs(p - q).sum()) < 1e-12
+
+
+def test_l1_position_weights():
+    gamma, decay = 8, 4.0
+    for k in range(gamma):  # one live position: the sums are 2 w_k (accept 0) and w_k
+        mask = np.zeros((1, 1, gamma))
+        mask[0, 0, k] = 1.0
+        _, num, den = O.tv_l1_loss(np.zeros((1, 1, gamma)), mask, decay)
+        assert den == pytest.approx(np.exp(-1.0 / decay) ** k, rel=1e-14)
+        assert num == pytest.approx(2.0 * den, rel=1e-14)
+    _, num, den = O.tv_l1_loss(np.ones((3, 5, gamma)), np.ones((3, 5, gamma)), decay)
+    assert num == 0.0 and den == pytest.approx(15 * sum(np.exp(-np.arange(gamma) / decay)))
