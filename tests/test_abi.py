@@ -79,6 +79,16 @@ def test_host_validation_needs_no_gpu(L):
     assert L.dspark_schedule_verify_len(4096, 8, fake, 8192, fake, fake, None, fake, 1 << 20, None) == 2
     # TV: bad dtype
     assert L.dspark_accept_rate_tv(1, 1, 1, 8, 7, fake, fake, fake, None, fake, fake, None, fake, 1 << 20, None) == 1
+    # L1 term: no sums buffer, decay not positive
+    assert L.dspark_tv_l1_loss(1, 4, 8, fake, fake, C.c_float(4.0), None, None, None) == 1
+    assert L.dspark_tv_l1_loss(1, 4, 8, fake, fake, C.c_float(0.0), None, fake, None) == 1
+    # teacher-forced block logits: bad params, r > 0 without weights, tokens missing, workspace
+    assert L.dspark_markov_block_logits(C.byref(bad), fake, None, None, fake, fake, fake, fake, 1 << 20, None) == 1
+    assert L.dspark_markov_block_logits(C.byref(ok), fake, None, None, fake, fake, fake, fake, 1 << 20, None) == 1
+    assert L.dspark_markov_block_logits(C.byref(ok), fake, fake, fake, fake, None, fake, fake, 1 << 20, None) == 1
+    assert L.dspark_markov_block_logits(C.byref(ok), fake, fake, fake, fake, fake, fake, fake, 16, None) == 6
+    assert b.dspark_markov_block_logits_workspace_size(ok) >= 256
+    assert b.dspark_markov_block_logits_workspace_size(bad) == 0
     # verify: dense layout needs gamma_t >= 1
     assert L.dspark_verify(C.byref(ok), fake, fake, fake, fake, fake, fake, fake, fake, 0, None, None, fake, fake,
                            fake, 1 << 20, None) == 1
