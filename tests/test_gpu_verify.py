@@ -143,3 +143,33 @@ def test_end_to_end_b32_r64():
 
 def test_end_to_end_b128_r256_sampled():
     end_to_end(W.b128_r256(device="cuda"), [3, 64, 126])
+
+
+def test_end_to_end_b512_scheduled_lengths_sampled():
+    # the b512 configuration as the bench runs it: lengths from the scheduler, then sample and verify
+    wl = W.b512_sched(device="cuda")
+    t = wl.tensors
+    L, _, _, _ = api.schedule_verify_len(t["conf"], wl.budget)
+    base, W1, W2, anchor, target = host(wl)
+    tok, lse, zat, _ = api.markov_sample_block(t["base"], t["W1"], t["W2"], t["anchor"], wl.T, wl.seed)
+    n, corr, ws = api.verify(t["base"], t["W1"], t["W2"], t["anchor"], tok, lse, zat, t["target"], wl.T, wl.seed,
+                             verify_len=L)
+    torch.cuda.synchronize()
+    assert binding.dspark_get_device_status(ws) == 0
+    L = L.cpu().numpy()
+    assert L.sum() <= wl.budget and L.min() >= 1
+    g_tok, g_lse, g_zat = tok.cpu().numpy(), lse.cpu().numpy(), zat.cpu().numpy()
+    n, corr = n.cpu().numpy(), corr.cpu().numpy()
+    tally = Tally()
+    for j in (0, 137, 300, 511):
+        ref = O.sample_request(base, W1, W2, int(anchor[j]), j, wl.T, wl.seed, TS)
+        if compare_block(tally, g_tok[j], g_lse[j], g_zat[j], ref, wl.T, j) < wl.gamma:
+            continue
+        rn, rc, rm, _ = O.verify_request(base, W1, W2, int(anchor[j]), j, ref[0], ref[1].astype(np.float32),
+                                         ref[2].astype(np.float32), target, int(L[j]), wl.T, wl.seed, TS)
+        assert n[j] <= L[j]
+        tally.total += 1
+        if (n[j], corr[j]) != (rn, rc):
+            assert rm < MARGIN, f"request {j}: ({n[j]}, {corr[j]}) vs ({rn}, {rc}) margin {rm}"
+            tally.excluded += 1
+    tally.check_fraction()
