@@ -11,7 +11,12 @@
 // with an 8-bit-digit radix select for the K-th largest, ties at the threshold are taken in
 // index order with a block-wide prefix count, and L_j / offsets / objective follow from
 // block scans.  All decisions are integer or exact fp32, so the result is bit-identical to a
-// sequential implementation of the same definition.
+// sequential implementation of the same definition.  When the budget covers every position the
+// selection is skipped (L_j = gamma).
+//
+// The file also holds dspark_theta_schedule, the throughput-aware prefix choice with a causal
+// stop (P4 "DSpark 深度解读：DeepSeek-V4 如何用「半自回归」把推理速度提升 85%" section 5.1):
+// one request per thread, decisions in IEEE single precision.
 #include "common.cuh"
 #include "host_util.h"
 

@@ -11,7 +11,8 @@
 // through a shared-memory ring fed by the bulk-copy engine, pass 1 from HBM and pass 2 from L2)
 // and tv_kernel (any other case: a thread-block cluster shares a row, each block takes a 1/cs
 // segment, the blocks exchange (max, sum) through distributed shared memory, and the second
-// pass re-reads the segment, an L2 hit).
+// pass re-reads the segment, an L2 hit).  tau_kernel follows them; tv_l1_kernel is the separate
+// training-side L1 term (dspark_tv_l1_loss, P1 section 3.9) on the accept rates.
 #include <cooperative_groups.h>
 
 #include <algorithm>
