@@ -72,7 +72,7 @@ def lib():
         L.oracle_eval_mask_tau.restype = dbl
         L.oracle_schedule.argtypes = [i32, i32, vp, i32, vp, vp, vp, vp]
         L.oracle_schedule.restype = i32
-        L.oracle_theta_schedule.argtypes = [i32, vp, vp, vp]
+        L.oracle_theta_schedule.argtypes = [i32, vp, vp, vp, vp]
         L.oracle_theta_schedule.restype = i32
         L.oracle_trials_sampler.argtypes = [i32, i32, i32, vp, u64, i64, i32, vp]
         L.oracle_trials_spec_one.argtypes = [i32, i32, i32, dbl, vp, vp, u64, i64, vp, vp]
@@ -268,13 +268,19 @@ def schedule(conf: np.ndarray, budget: int):
     return L, off, float(obj[0]), float(mg[0])
 
 
-def theta_schedule(c, sps):
+def theta_schedule(c, sps, with_margin: bool = False):
+    """Throughput-aware prefix choice in fp64 (P4 section 5.1): returns (ell, Theta_0..Theta_gamma
+    as far as the causal search evaluated them, NaN after) and, with_margin, the smallest relative
+    gap between two Theta values the search compared."""
     c = np.ascontiguousarray(c, dtype=np.float64)
     sps = np.ascontiguousarray(sps, dtype=np.float64)
     gamma = c.shape[0]
     assert sps.shape[0] >= gamma + 1
     th = np.zeros(gamma + 1)
-    ell = lib().oracle_theta_schedule(gamma, _p(c), _p(sps), _p(th))
+    mg = np.zeros(1)
+    ell = lib().oracle_theta_schedule(gamma, _p(c), _p(sps), _p(th), _p(mg))
+    if with_margin:
+        return int(ell), th, float(mg[0])
     return int(ell), th
 
 

@@ -505,28 +505,37 @@ double oracle_eval_mask_tau(int gamma, int keep, const uint8_t* pos_valid, const
 /* <= K; the SLA constraint is read as sum_j L_j <= budget; survival is */
 /* a product of conditional confidences, P2 section 3.8.3).             */
 /*   c is clamped to [0,1] (NaN -> 0); a_{j,i} = prod_{k<=i} c_{j,k}     */
-/*   formed left to right in fp32.  Every request verifies one token;   */
+/*   formed left to right in double.  Every request verifies one token; */
 /*   the remaining budget - B slots go to the largest a_{j,i}, i >= 2,  */
 /*   ordered by (a desc, j asc, i asc).  Because c <= 1, a is           */
 /*   non-increasing along i, so the chosen set is prefix-closed and the */
 /*   greedy choice is optimal (concave gains).  budget < B: returns -1. */
-/*   *margin = fp32 gap between the last taken and the first left key.  */
+/*   *margin = a of the last taken key minus a of the first key left    */
+/*   out (infinite when nothing is left out or nothing is taken).       */
 /* ------------------------------------------------------------------ */
-static int cmp_desc_key(const void* pa, const void* pb) {
-    const uint64_t a = *(const uint64_t*)pa, b = *(const uint64_t*)pb;
-    return (a < b) - (a > b);
+typedef struct {
+    double a;
+    long idx; /* j * gamma + i */
+} sched_key;
+
+static int cmp_sched_key(const void* pa, const void* pb) {
+    const sched_key* x = (const sched_key*)pa;
+    const sched_key* y = (const sched_key*)pb;
+    if (x->a > y->a) return -1;
+    if (x->a < y->a) return 1;
+    return (x->idx > y->idx) - (x->idx < y->idx);
 }
 
 int oracle_schedule(int B, int gamma, const float* conf, int budget, int32_t* L, int32_t* offsets,
                     double* objective, double* margin) {
     if (budget < B) return -1;
-    float* a = (float*)malloc(sizeof(float) * (size_t)B * gamma);
+    double* a = (double*)malloc(sizeof(double) * (size_t)B * gamma);
     for (int j = 0; j < B; ++j) {
-        float run = 1.0f;
+        double run = 1.0;
         for (int i = 0; i < gamma; ++i) {
-            float c = conf[(size_t)j * gamma + i];
-            if (!(c >= 0.0f)) c = 0.0f; /* also NaN */
-            if (c > 1.0f) c = 1.0f;
+            double c = (double)conf[(size_t)j * gamma + i];
+            if (!(c >= 0.0)) c = 0.0; /* also NaN */
+            if (c > 1.0) c = 1.0;
             run = run * c;
             a[(size_t)j * gamma + i] = run;
         }
@@ -534,37 +543,22 @@ int oracle_schedule(int B, int gamma, const float* conf, int budget, int32_t* L,
     long extra = (long)budget - B;
     long cand = (long)B * (gamma - 1);
     if (extra > cand) extra = cand;
-    /* key = (bits(a) << 32) | ~index : descending key order is (a desc, index asc) */
-    uint64_t* keys = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)(cand > 0 ? cand : 1));
+    sched_key* keys = (sched_key*)malloc(sizeof(sched_key) * (size_t)(cand > 0 ? cand : 1));
     long nk = 0;
     for (int j = 0; j < B; ++j)
         for (int i = 1; i < gamma; ++i) {
-            uint32_t bits;
-            memcpy(&bits, &a[(size_t)j * gamma + i], 4);
-            uint32_t idx = (uint32_t)((size_t)j * gamma + i);
-            keys[nk++] = ((uint64_t)bits << 32) | (uint64_t)(~idx);
+            keys[nk].a = a[(size_t)j * gamma + i];
+            keys[nk].idx = (long)j * gamma + i;
+            ++nk;
         }
-    qsort(keys, (size_t)nk, sizeof(uint64_t), cmp_desc_key);
+    qsort(keys, (size_t)nk, sizeof(sched_key), cmp_sched_key);
     for (int j = 0; j < B; ++j) L[j] = 1;
-    for (long k = 0; k < extra; ++k) {
-        uint32_t idx = ~(uint32_t)(keys[k] & 0xffffffffu);
-        L[idx / (uint32_t)gamma] += 1;
-    }
-    if (margin) {
-        if (extra > 0 && extra < nk) {
-            uint32_t b1 = (uint32_t)(keys[extra - 1] >> 32), b2 = (uint32_t)(keys[extra] >> 32);
-            float f1, f2;
-            memcpy(&f1, &b1, 4);
-            memcpy(&f2, &b2, 4);
-            *margin = (double)f1 - (double)f2;
-        } else {
-            *margin = INFINITY;
-        }
-    }
+    for (long k = 0; k < extra; ++k) L[keys[k].idx / gamma] += 1;
+    if (margin) *margin = (extra > 0 && extra < nk) ? keys[extra - 1].a - keys[extra].a : INFINITY;
     double obj = 0.0;
     offsets[0] = 0;
     for (int j = 0; j < B; ++j) {
-        for (int i = 0; i < L[j]; ++i) obj += (double)a[(size_t)j * gamma + i];
+        for (int i = 0; i < L[j]; ++i) obj += a[(size_t)j * gamma + i];
         offsets[j + 1] = offsets[j] + L[j];
     }
     if (objective) *objective = obj;
@@ -576,25 +570,34 @@ int oracle_schedule(int B, int gamma, const float* conf, int budget, int32_t* L,
 /* Throughput-aware prefix choice (P4 section 5.1):
  *   Theta_l = (1 + sum_{k<=l} a_k) * SPS(l + 1),  a_k = prod_{i<=k} c_i,
  * searched causally from l = 0, stopping at the first l with
- * Theta_l < Theta_{l-1}; returns that l - 1 (or the last l).  theta_out
- * receives Theta_0..Theta_gamma as far as they were evaluated (NaN after).
- * The comparisons decide an integer, so they are taken in the precision of
- * the CUDA path (the pages fix none): IEEE single, one rounding per multiply
- * and per add in this order (compiled without contraction).  c and sps are
- * single-precision values (narrowed exactly when given as such). */
-int oracle_theta_schedule(int gamma, const double* c, const double* sps, double* theta_out) {
-    float a = 1.0f, acc = 0.0f, prev = -INFINITY;
+ * Theta_l < Theta_{l-1}; returns that l - 1 (or gamma when it never stops).
+ * theta_out receives Theta_0..Theta_gamma as far as they were evaluated (NaN
+ * after).  Computed in double.  *margin = the smallest relative gap
+ * |Theta_l - Theta_{l-1}| / max(|Theta_l|, |Theta_{l-1}|) over the
+ * comparisons the search made (infinite when gamma = 0): a comparison whose
+ * gap is below rounding could go either way in a lower precision. */
+int oracle_theta_schedule(int gamma, const double* c, const double* sps, double* theta_out, double* margin) {
+    double a = 1.0, acc = 0.0, prev = -INFINITY, mg = INFINITY;
     for (int l = 0; l <= gamma; ++l) theta_out[l] = NAN;
     for (int l = 0; l <= gamma; ++l) {
         if (l > 0) {
-            a = a * (float)c[l - 1];
+            a = a * c[l - 1];
             acc = acc + a;
         }
-        const float th = (1.0f + acc) * (float)sps[l];
-        theta_out[l] = (double)th;
-        if (l > 0 && th < prev) return l - 1;
+        const double th = (1.0 + acc) * sps[l];
+        theta_out[l] = th;
+        if (l > 0) {
+            const double den = fmax(fabs(th), fabs(prev));
+            const double gap = den > 0.0 ? fabs(th - prev) / den : 0.0;
+            if (gap < mg) mg = gap;
+            if (th < prev) {
+                if (margin) *margin = mg;
+                return l - 1;
+            }
+        }
         prev = th;
     }
+    if (margin) *margin = mg;
     return gamma;
 }
 

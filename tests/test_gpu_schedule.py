@@ -1,47 +1,67 @@
-"""Parity of dspark_schedule_verify_len (CUDA) with the oracle: bit-exact L and offsets."""
+"""Parity of dspark_schedule_verify_len and dspark_theta_schedule (CUDA, fp32) with the fp64
+oracle: L, offsets and the chosen prefix are bit-exact except where the oracle's decision margin
+is below 1e-5 (counted, under 0.01% of decisions); objective and Theta within 1e-5 relative."""
 import numpy as np
 import pytest
 import torch
 
 import oracle as O
-from parity import close
+from parity import MARGIN, Tally, close
 from semi_ar_draft_gb300 import api, binding
 from semi_ar_draft_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
 
-def check(conf, budget):
+def check(conf, budget, tally=None):
+    """One call against the oracle.  The selection decisions are the B (gamma - 1) candidate
+    positions i >= 2; a survival pair straddling the budget boundary within rounding can be taken
+    in the other order (one decision, two requests' L off by one), which is allowed only when the
+    oracle's boundary margin is below 1e-5."""
+    tally = tally if tally is not None else Tally()
+    B, g = conf.shape
     L, off, obj, _ = api.schedule_verify_len(conf, budget)
-    rL, roff, robj, _ = O.schedule(conf.cpu().numpy(), budget)
-    assert np.array_equal(L.cpu().numpy(), rL)
-    assert np.array_equal(off.cpu().numpy(), roff)
+    rL, roff, robj, mg = O.schedule(conf.cpu().numpy(), budget)
+    L, off = L.cpu().numpy(), off.cpu().numpy()
+    tally.total += B * max(g - 1, 1)
+    if not np.array_equal(L, rL):
+        assert mg < MARGIN, (mg, np.nonzero(L != rL))
+        tally.excluded += (int(np.abs(L - rL).sum()) + 1) // 2
+    # whatever was chosen is a valid selection of the same size
+    assert L.min() >= 1 and L.max() <= g and L.sum() == rL.sum()
+    assert off[0] == 0 and np.array_equal(np.diff(off), L)
     close(obj.cpu().numpy(), [robj], what="objective")
+    return tally
 
 
 @pytest.mark.parametrize("B,g", [(1, 1), (1, 16), (3, 5), (37, 7), (512, 16), (1024, 16), (2000, 8)])
 def test_random_budgets(B, g):
     gen = torch.Generator(device="cuda").manual_seed(B * 31 + g)
     conf = torch.rand((B, g), generator=gen, device="cuda")
+    tally = Tally()
     for budget in sorted({B, B + 1, (B * g) // 2, B * g - 1, B * g, B * g + 5}):
         if budget >= B:
-            check(conf, budget)
+            check(conf, budget, tally)
+    tally.check_fraction()
 
 
 def test_config_b512_budget_2048():
     wl = W.b512_sched(device="cuda", V=1024)  # confidences only
-    check(wl.tensors["conf"], 2048)
+    check(wl.tensors["conf"], 2048).check_fraction()
 
 
 def test_ties_nan_and_clamp():
+    # exact ties in both precisions (powers of two, ones): both sides break them by (j, i)
     conf = torch.ones((6, 5), device="cuda")
-    check(conf, 13)
+    check(conf, 13).check_fraction()
     conf[1, 2] = float("nan")
     conf[3, 1] = 1.7
     conf[4, 0] = -0.2
-    check(conf, 17)
+    check(conf, 17).check_fraction()
     q = torch.full((40, 8), 0.5, device="cuda")  # many exact ties across rows
-    check(q, 100)
+    rL, *_ = O.schedule(q.cpu().numpy(), 100)
+    L, *_ = api.schedule_verify_len(q, 100)
+    assert np.array_equal(L.cpu().numpy(), rL)
 
 
 def test_budget_below_b_is_rejected():
@@ -58,13 +78,20 @@ def _theta_check(c, sps):
     ell, theta = api.theta_schedule(conf, prof, with_theta=True)
     torch.cuda.synchronize()
     ell, theta = ell.cpu().numpy(), theta.cpu().numpy()
+    tally = Tally()
     for j in range(conf.shape[0]):
-        # the oracle on the same float32 values, widened exactly
-        r_ell, r_th = O.theta_schedule(conf[j].cpu().numpy().astype(np.float64), prof.cpu().numpy().astype(np.float64))
-        assert ell[j] == r_ell, j
+        # the fp64 oracle on the same float32 values, widened exactly
+        r_ell, r_th, mg = O.theta_schedule(conf[j].cpu().numpy().astype(np.float64),
+                                           prof.cpu().numpy().astype(np.float64), with_margin=True)
+        tally.total += 1
+        if ell[j] != r_ell:
+            assert mg < MARGIN, (j, ell[j], r_ell, mg)
+            tally.excluded += 1
+            continue
         assert np.array_equal(np.isnan(theta[j]), np.isnan(r_th)), j
         ok = ~np.isnan(r_th)
-        assert np.array_equal(theta[j][ok], r_th[ok].astype(np.float32)), j  # same IEEE single operations
+        close(theta[j][ok], r_th[ok], atol=0.0, what=f"Theta of request {j}")
+    tally.check_fraction()
 
 
 def test_theta_worked_example_on_gpu():

@@ -12,18 +12,14 @@ import oracle as O
 GOLD = os.path.join(os.path.dirname(__file__), "golden", "theta_worked_example.txt")
 
 
-def _survival_f32(conf):
-    c = np.clip(np.nan_to_num(conf.astype(np.float32), nan=0.0), 0, 1).astype(np.float32)
-    a = np.empty_like(c)
-    run = np.ones(c.shape[0], np.float32)
-    for i in range(c.shape[1]):
-        run = (run * c[:, i]).astype(np.float32)
-        a[:, i] = run
-    return a
+def _survival(conf):
+    # prefix products of the clamped conditional confidences, in double (the definition)
+    c = np.clip(np.nan_to_num(conf.astype(np.float64), nan=0.0), 0, 1)
+    return np.cumprod(c, axis=1)
 
 
 def _brute(conf, budget):
-    a = _survival_f32(conf).astype(np.float64)
+    a = _survival(conf)
     B, g = a.shape
     best, arg, nbest = -1.0, None, 0
     for L in itertools.product(range(1, g + 1), repeat=B):
@@ -72,6 +68,58 @@ def test_schedule_ties_are_prefix_closed():
     conf[1, 0] = np.nan  # NaN confidence reads as 0
     L, *_ = O.schedule(conf, 9)
     assert list(L) == [4, 1, 4]
+
+
+def test_schedule_survival_is_double_precision():
+    # two requests whose second-position survivals c1*c2 are equal once rounded to fp32 but differ
+    # in double: with one extra verify slot the larger true product must win, not the lower index
+    rng = np.random.default_rng(0)
+    x = rng.uniform(0.5, 1.0, (200000, 2)).astype(np.float32)
+    p32 = (x[:, 0] * x[:, 1]).astype(np.float32)
+    p64 = x[:, 0].astype(np.float64) * x[:, 1].astype(np.float64)
+    order = np.argsort(p32, kind="stable")
+    found = None
+    for k in range(len(order) - 1):
+        a, b = order[k], order[k + 1]
+        if p32[a] == p32[b] and p64[a] != p64[b]:
+            lo, hi = (a, b) if p64[a] < p64[b] else (b, a)
+            found = (lo, hi)
+            break
+    assert found is not None
+    lo, hi = found
+    conf = np.stack([x[lo], x[hi]]).astype(np.float32)  # row 0 has the smaller true product
+    L, off, obj, mg = O.schedule(conf, 3)
+    assert list(L) == [1, 2]
+    assert mg == p64[hi] - p64[lo] and 0 < mg < 1e-7
+    assert abs(obj - (float(conf[0, 0]) + float(conf[1, 0]) + p64[hi])) < 1e-15
+
+
+def test_schedule_margin_is_the_boundary_gap():
+    conf = np.array([[1.0, 0.9, 0.5], [1.0, 0.6, 0.5]], np.float32)
+    # candidates (a desc): 0.9 (j0,i2), 0.6 (j1,i2), 0.45 (j0,i3), 0.3 (j1,i3); budget 3 takes one
+    L, off, obj, mg = O.schedule(conf, 3)
+    assert list(L) == [2, 1]
+    assert abs(mg - (0.9 - 0.6)) < 1e-7
+    L, off, obj, mg = O.schedule(conf, 6)  # everything taken: nothing left to compare
+    assert list(L) == [3, 3] and mg == np.inf
+
+
+def test_theta_margin_and_double_precision():
+    # the worked example: the search compares Theta_1 with Theta_0 and Theta_2 with Theta_1
+    ell, th, mg = O.theta_schedule(np.array([0.8, 0.7, 0.1]), np.array([1.0, 0.95, 0.52, 0.48]), with_margin=True)
+    t0, t1, t2 = 1.0, 1.8 * 0.95, 2.36 * 0.52
+    assert ell == 1
+    assert abs(mg - min((t1 - t0) / t1, (t1 - t2) / t1)) < 1e-12
+    # Theta_1 = 1.25 (0.8 - 1e-12) lies 1.25e-12 below Theta_0 = 1: the search stops at once.  In
+    # single precision the two would round to the same value and the search would go on.
+    ell, th, mg = O.theta_schedule(np.array([0.25, 0.0]), np.array([1.0, 0.8 - 1e-12, 0.1]), with_margin=True)
+    assert ell == 0 and np.isnan(th[2])
+    assert abs(mg - 1.25e-12) < 1e-15
+    # a search that never stops reports the smallest gap it saw; gamma = 0 compares nothing
+    ell, th, mg = O.theta_schedule(np.array([0.5, 0.5]), np.array([1.0, 1.0, 1.0]), with_margin=True)
+    assert ell == 2 and abs(mg - 0.25 / 1.75) < 1e-12
+    ell, th, mg = O.theta_schedule(np.zeros(0), np.array([2.0]), with_margin=True)
+    assert ell == 0 and th[0] == 2.0 and mg == np.inf
 
 
 def test_theta_worked_example():
