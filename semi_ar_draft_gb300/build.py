@@ -10,7 +10,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libdspark.so")
-SOURCES = ["api.cu", "sample.cu", "verify.cu", "tv.cu", "schedule.cu", "logits.cu"]
+SOURCES = ["api.cu", "sample.cu", "sample_tc.cu", "verify.cu", "tv.cu", "schedule.cu", "logits.cu"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc" if os.path.exists("/usr/local/cuda/bin/nvcc") else "nvcc")
 FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
          "-I", INCLUDE, "-I", CSRC]

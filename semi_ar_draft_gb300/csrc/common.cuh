@@ -209,6 +209,44 @@ __device__ __forceinline__ float log_neg_log_u(float u) {
     return lg2(e) * 0.69314718055994531f;
 }
 
+// The same value without a branch: both formulas are evaluated (same operations, same
+// results) and the one for u's range is selected, so lanes of a warp do not diverge.
+__device__ __forceinline__ float log_neg_log_u_nb(float u) {
+    const float e_log = -lg2(u) * 0.69314718055994531f;
+    const float t = u - 1.0f;
+    const float sv = __fdividef(t, 2.0f + t);
+    const float s2 = sv * sv;
+    float q = 1.0f / 19.0f;
+    q = fmaf(q, s2, 1.0f / 17.0f);
+    q = fmaf(q, s2, 1.0f / 15.0f);
+    q = fmaf(q, s2, 1.0f / 13.0f);
+    q = fmaf(q, s2, 1.0f / 11.0f);
+    q = fmaf(q, s2, 1.0f / 9.0f);
+    q = fmaf(q, s2, 1.0f / 7.0f);
+    q = fmaf(q, s2, 1.0f / 5.0f);
+    q = fmaf(q, s2, 1.0f / 3.0f);
+    q = fmaf(q, s2, 1.0f);
+    const float e = u < 0.5f ? e_log : -2.0f * sv * q;
+    return lg2(e) * 0.69314718055994531f;
+}
+
+// max of three (one instruction on this architecture)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+// max of 32 values as a tree of three-input maxima (depth 4)
+__device__ __forceinline__ float max32(const float (&z)[32]) {
+    float a[11];
+#pragma unroll
+    for (int k = 0; k < 10; ++k) a[k] = fmax3(z[3 * k], z[3 * k + 1], z[3 * k + 2]);
+    a[10] = fmaxf(z[30], z[31]);
+    const float b0 = fmax3(a[0], a[1], a[2]), b1 = fmax3(a[3], a[4], a[5]), b2 = fmax3(a[6], a[7], a[8]);
+    const float b3 = fmaxf(a[9], a[10]);
+    return fmaxf(fmax3(b0, b1, b2), b3);
+}
+
 // ---------------------------------------------------------------- reductions
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll

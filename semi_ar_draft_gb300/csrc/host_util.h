@@ -24,4 +24,20 @@ dspark_status validate_sample_params(const dspark_sample_params* p);
 size_t sample_workspace_bytes(const dspark_sample_params* p);
 bool markov_use_mma(const dspark_sample_params* p);
 
+// Byte offsets inside the draft-sampling workspace (dspark_sample_workspace_size bytes):
+// packed maxima [gamma][B] (one 128-byte line each), per-row-block arrival counters, and the
+// per-tile records; the first `zeroed` bytes (header, maxima, counters) are cleared per call.
+struct SampleWsLayout {
+    size_t slots, counts, part, zeroed;
+};
+SampleWsLayout sample_ws_layout(const dspark_sample_params* p);
+
+// Tensor-core draft sampler (sample_tc.cu): bf16 logits and weights of rank 64, at least
+// kTcMinBatch requests, V % 8 == 0, 16-byte aligned tensors, one vocabulary tile per SM.
+constexpr int kTcMinBatch = 64;
+bool sample_tc_eligible(const dspark_sample_params* p, const void* base, const void* W1, const void* W2, int sms);
+dspark_status launch_sample_tc(const dspark_sample_params* p, const void* base_logits, const void* W1, const void* W2,
+                               const int32_t* anchor, int32_t* tokens, float* draft_lse, float* draft_logit_at_tok,
+                               const SampleWsLayout& L, void* workspace, cudaStream_t s);
+
 }  // namespace dspark

@@ -772,6 +772,15 @@ size_t sample_workspace_bytes(const dspark_sample_params* p) {
            align_up(3 * sizeof(float4) * (size_t)p->B * nt, 256);
 }
 
+SampleWsLayout sample_ws_layout(const dspark_sample_params* p) {
+    SampleWsLayout L;
+    L.slots = kHeaderBytes;
+    L.counts = kHeaderBytes + align_up((size_t)kSlotStride * sizeof(unsigned long long) * (size_t)p->B * p->gamma, 256);
+    L.zeroed = kHeaderBytes + sample_slot_bytes(p);
+    L.part = L.zeroed + align_up(sizeof(int32_t) * (size_t)p->B, 256);
+    return L;
+}
+
 }  // namespace dspark
 
 using namespace dspark;
@@ -796,6 +805,9 @@ extern "C" dspark_status dspark_markov_sample_block(const dspark_sample_params* 
     const int nt = (p->V + kTS - 1) / kTS;
     int sms = 0;
     if (device_sm_count(&sms) != cudaSuccess) return DSPARK_ERR_CUDA;
+    if (sample_tc_eligible(p, base_logits, W1, W2, sms))
+        return launch_sample_tc(p, base_logits, W1, W2, anchor, tokens, draft_lse, draft_logit_at_tok,
+                                sample_ws_layout(p), workspace, reinterpret_cast<cudaStream_t>(stream));
     const size_t esz = p->logits_dtype == DSPARK_BF16 ? 2 : 4;
     const bool vec_ok = ((uintptr_t)base_logits % 16 == 0) && (((size_t)p->V * esz) % 16 == 0);
     // staged path: bf16 logits, tensor-core bias, one tile per block (one block per SM)
@@ -843,13 +855,12 @@ extern "C" dspark_status dspark_markov_sample_block(const dspark_sample_params* 
     a.draft_lse = draft_lse;
     a.zat = draft_logit_at_tok;
     unsigned char* ws = static_cast<unsigned char*>(workspace);
+    const SampleWsLayout WL = sample_ws_layout(p);
     a.hdr = reinterpret_cast<WsHeader*>(ws);
-    a.slots = reinterpret_cast<unsigned long long*>(ws + kHeaderBytes);
-    a.rb_count = reinterpret_cast<unsigned*>(
-        ws + kHeaderBytes + align_up((size_t)kSlotStride * sizeof(unsigned long long) * (size_t)p->B * p->gamma, 256));
-    a.cur_tok = reinterpret_cast<int32_t*>(ws + kHeaderBytes + sample_slot_bytes(p));
-    a.part = reinterpret_cast<float4*>(ws + kHeaderBytes + sample_slot_bytes(p) +
-                                       align_up(sizeof(int32_t) * (size_t)p->B, 256));
+    a.slots = reinterpret_cast<unsigned long long*>(ws + WL.slots);
+    a.rb_count = reinterpret_cast<unsigned*>(ws + WL.counts);
+    a.cur_tok = reinterpret_cast<int32_t*>(ws + WL.zeroed);
+    a.part = reinterpret_cast<float4*>(ws + WL.part);
     a.w1_l2 = (size_t)p->V * p->r * 2 <= ((size_t)64 << 20);
     a.limit_ns = wait_limit_ns();
     a.redundant = (size_t)p->B * nt <= 8192 && p->B <= kThreads;

@@ -1,0 +1,696 @@
+// sample_tc.cu -- Markov-head block sampling on the fifth-generation tensor cores (tcgen05), for
+// batches of many requests with bf16 logits and weights of rank 64.
+//
+// Method (P2 "从 DFlash 到 dLLM Self-Spec（三）" section 3.4, VanillaMarkov and the
+// sample_block_tokens loop; P1 "03 · DSpark 建模：Markov 与 Confidence" section 3.7): for
+// i = 1..gamma, z = base_i + W2 . W1[prev]; draw x_i from softmax(z / T) by the chunk-Gumbel
+// contract of dspark.h; prev = x_i.
+//
+// One persistent cooperative kernel; CTA b owns vocabulary tile b (1024 ids) for all gamma steps.
+// Requests go in row blocks of 128 (one TMEM lane each); a unit is one (step, row block).
+//   - W2 rows of the tile (1024 x 64 bf16, 128 KB) are copied into shared memory once by a tiled
+//     tensor copy (128-byte swizzle, the K-major MMA layout) and stay there.
+//   - z of a unit, D[128 requests x 1024 ids], is computed entirely on the tensor cores, as eight
+//     accumulators of 128 fp32 TMEM columns (four rotating slots = all 512 columns):
+//       bias: D = W1[prev] . W2_tile^T, four kind::f16 MMAs of M = 128, N = 128, K = 16, with A =
+//             the 128 W1 rows of the previous tokens (written into shared memory, swizzled, by the
+//             exchange warps) and B = 128 resident W2 rows;
+//       base: D += base . I, the base logits of the unit (bf16, streamed by 3-D tiled copies of
+//             64 ids x 128 requests, 128-byte swizzle, through a four-slot ring) as the A operand
+//             and a 16 x 16 identity as B: four MMAs of N = 16, K = 16 per copy, each adding 16
+//             ids' base values in fp32.  The copies do not depend on the tokens, so those of the
+//             next step run ahead of the exchange.
+//   - Epilogue: two warpgroups, one per parity of accumulator.  Thread = request: it reads its
+//     lane's 32 columns of a chunk from TMEM (the next chunk's load in flight meanwhile) and forms
+//     the chunk record of the contract with no shuffles: max, the weights 2^(z s - max), their
+//     prefix sums in four blocks of eight, the in-chunk inverse-CDF candidate (the count of prefix
+//     values not above u times the sum), and the key LSE_c - ln E_c (E_c from Philox: one call per
+//     accumulator gives its four chunks).  Each warpgroup keeps the best key and the log-mass of
+//     its half of the tile and, at the end of a unit, folds the key into the request's 64-bit word
+//     with one atomic max (key bits above the complemented id: highest key, then lowest id, wins)
+//     and stores the log-mass.
+//   - An arriver warp then performs one release-add on the row block's arrival counter.  The
+//     exchange warps of every CTA wait for all G arrivals of (step - 1, row block), read the
+//     words (the token), write the W1 rows of the tokens as the next A operand, and the owner of
+//     request j (CTA j mod G) writes the token, LSE(z/T) over the log-masses and z at the token.
+// Every wait is bounded (DSPARK_ERR_TIMEOUT in the status word); on a timeout the kernel drains
+// its copies and MMAs in flight, frees its tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "host_util.h"
+#include "tc05.cuh"
+
+namespace dspark {
+namespace {
+
+constexpr int kTcTile = 1024;                 // ids per CTA (one vocabulary tile)
+constexpr int kTcRows = 128;                  // requests per row block = MMA M = TMEM lanes
+constexpr int kTcN = 128;                     // ids per accumulator = MMA N of the bias
+constexpr int kTcAccs = kTcTile / kTcN;       // accumulators per unit
+constexpr int kTcTmemSlots = 4;               // 4 x 128 fp32 columns = all 512 TMEM columns
+constexpr int kTcBox = 64;                    // ids per base copy (128 bytes: one swizzle span)
+constexpr int kTcBoxes = kTcTile / kTcBox;    // base copies per unit
+constexpr int kTcStages = 4;                  // base copy ring
+constexpr int kTcRank = 64;                   // K of the bias (W1 / W2 row = 128 bytes)
+constexpr int kTcThreads = 512;
+constexpr int kTcMaxTiles = 160;              // vocabulary tiles (CTAs) at most: 2 log-mass records each per request
+constexpr int kTcSlotStride = 16;             // 64-bit words between two requests' maxima (one 128-byte line)
+constexpr int kTcCountStride = 32;            // 32-bit words between two row blocks' arrival counters
+constexpr uint32_t kBoxBytes = kTcBox * kTcRows * 2;       // 16 KB
+constexpr uint32_t kABytes = kTcRows * kTcRank * 2;        // 16 KB
+constexpr uint32_t kW2Bytes = kTcTile * kTcRank * 2;       // 128 KB
+constexpr uint32_t kIdBytes = 16 * 128;                    // 16 x 16 identity, rows of a 128-byte swizzled tile
+
+// shared memory (offsets from the 1024-byte aligned base)
+constexpr uint32_t kSmW2 = 0;
+constexpr uint32_t kSmA = kSmW2 + kW2Bytes;                 // [2]
+constexpr uint32_t kSmId = kSmA + 2 * kABytes;
+constexpr uint32_t kSmBase = kSmId + kIdBytes;              // [kTcStages]
+constexpr uint32_t kSmBars = kSmBase + kTcStages * kBoxBytes;
+constexpr int kNumBars = 5 + 2 * kTcStages + 2 * kTcTmemSlots + 2;
+constexpr uint32_t kSmFlags = kSmBars + 8 * kNumBars;
+constexpr uint32_t kSmTotal = kSmFlags + 64;
+constexpr size_t kTcSmemBytes = kSmTotal;  // the dynamic base is 1024-byte aligned (checked at entry)
+static_assert(kSmBase % 1024 == 0, "base stages are 1024-byte aligned");
+static_assert(kTcSmemBytes <= 227 * 1024, "shared memory of the tensor-core sampler");
+
+struct TcArgs {
+    int B, gamma, V, nt, nrb, G;
+    int part_ld;          // floats per request row of the log-mass records (2 per tile)
+    float scale2;         // log2(e) / T (1 when greedy)
+    uint64_t seed;
+    const uint16_t* base;  // bf16 bits [B, gamma, V]
+    const uint16_t* W1;    // bf16 bits [V, 64]
+    const uint16_t* W2;    // bf16 bits [V, 64]
+    const int32_t* anchor;
+    int32_t* tokens;
+    float* draft_lse;
+    float* zat;
+    WsHeader* hdr;
+    unsigned long long* slots;  // [gamma][B] packed maxima, kTcSlotStride words apart (zeroed per call)
+    unsigned* rb_count;         // [nrb] arrival counters, kTcCountStride apart (zeroed per call)
+    float* part;                // [3][B][part_ld] per-half-tile log-masses (natural log)
+    uint64_t limit_ns;
+};
+
+__device__ __forceinline__ bool bar_red_or(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ int ld_acq_cta(const int* p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+    return v;
+}
+__device__ __forceinline__ void add_rel_cta(int* p, int v) {
+    asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+
+// One lane waits (bounded, abort-aware), the warp follows; every lane then takes its own acquire.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, const TcArgs& a) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait_hint_or_abort(bar, parity, abort, &a.hdr->status, a.limit_ns) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) mbar_try_wait(bar, parity);
+    return ok != 0;
+}
+
+// Running state of one request over the chunks of a half tile.
+struct ChunkState {
+    float bkey;  // best key so far (T > 0: LSE_c - ln E_c; greedy: max z)
+    int bcand;   // its candidate id
+    float mt, st;  // log2-mass of the chunks seen: 2^mt * st
+};
+
+// Chunk record of one request over 32 ids in registers (T > 0), folded into the state.  Chunks
+// arrive in increasing id order, so a strictly greater key is needed to replace the best (ties
+// keep the lower chunk).  ids past V (MASK) are -inf.  No early exit and one warp vote: every lane
+// of the warp runs this in step.
+template <bool MASK>
+__device__ __forceinline__ void chunk_sample(const uint32_t (&v)[32], int id0, int V, float scale2, float u, float lnE,
+                                             ChunkState& cs) {
+    float z[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) z[e] = (MASK && id0 + e >= V) ? -CUDART_INF_F : __uint_as_float(v[e]);
+    const float m = max32(z);
+    const bool has = m != -CUDART_INF_F;
+    const float m2 = has ? m * scale2 : 0.f;  // no ids: weights 2^-inf = 0, never NaN
+    float p[32];
+    const uint64_t s2 = pk2(scale2, scale2), nm2 = pk2(-m2, -m2);
+#pragma unroll
+    for (int h = 0; h < 16; ++h) {
+        const float2 y = up2(fma2(pk2(z[2 * h], z[2 * h + 1]), s2, nm2));
+        p[2 * h] = ex2(y.x);
+        p[2 * h + 1] = ex2(y.y);
+    }
+    // inclusive prefix sums in four blocks of eight (four independent chains), then block offsets
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+#pragma unroll
+        for (int k = 1; k < 8; ++k) p[8 * b + k] += p[8 * b + k - 1];
+    const float o1 = p[7], o2 = o1 + p[15], o3 = o2 + p[23];
+    const float S = o3 + p[31];
+    const float t = u * S;
+    const float t1 = t - o1, t2 = t - o2, t3 = t - o3;
+    int cnt = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        cnt += (p[k] <= t ? 1 : 0) + (p[8 + k] <= t1 ? 1 : 0) + (p[16 + k] <= t2 ? 1 : 0) + (p[24 + k] <= t3 ? 1 : 0);
+    if (__any_sync(0xffffffffu, cnt == 32)) {  // rounding left no crossing: the last id with weight
+        if (cnt == 32) {
+            int last = 0;
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float before = k == 0 ? 0.f : p[8 * b + k - 1];
+                    last = p[8 * b + k] > before ? 8 * b + k : last;
+                }
+            cnt = last;
+        }
+    }
+    if (has && S > 0.f) {
+        const float l2 = m2 + lg2(S);
+        const float key = l2 * kLn2 - lnE;
+        if (key > cs.bkey) {
+            cs.bkey = key;
+            cs.bcand = id0 + cnt;
+        }
+        const float nm = fmaxf(cs.mt, l2);
+        cs.st = cs.st * ex2(cs.mt - nm) + ex2(l2 - nm);
+        cs.mt = nm;
+    }
+}
+
+// Greedy: the chunk's maximum and its lowest argmax.
+template <bool MASK>
+__device__ __forceinline__ void chunk_greedy(const uint32_t (&v)[32], int id0, int V, ChunkState& cs) {
+    float z[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) z[e] = (MASK && id0 + e >= V) ? -CUDART_INF_F : __uint_as_float(v[e]);
+    const float m = max32(z);
+    int x = 31;
+#pragma unroll
+    for (int e = 31; e >= 0; --e) x = z[e] == m ? e : x;
+    if (m > cs.bkey) {
+        cs.bkey = m;
+        cs.bcand = id0 + x;
+    }
+}
+
+// The four chunks of one accumulator for this thread's request: TMEM loads double-buffered, the
+// next chunk's in flight while the current one is reduced.
+template <bool GREEDY, bool MASK>
+__device__ __forceinline__ void accumulator_chunks(uint32_t taddr, int id0, int V, float scale2, float u,
+                                                   const float (&lnE)[4], ChunkState& cs) {
+    uint32_t va[32], vb[32];
+    tmem_ld32(taddr, va);
+    tmem_wait_ld(va);
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+        uint32_t(&cur)[32] = (cc & 1) ? vb : va;
+        uint32_t(&nxt)[32] = (cc & 1) ? va : vb;
+        if (cc < 3) tmem_ld32(taddr + 32u * (uint32_t)(cc + 1), nxt);
+        if (!MASK || id0 + 32 * cc < V) {  // (uniform) a chunk wholly past V has no ids
+            if (GREEDY) chunk_greedy<MASK>(cur, id0 + 32 * cc, V, cs);
+            else chunk_sample<MASK>(cur, id0 + 32 * cc, V, scale2, u, lnE[cc], cs);
+        }
+        if (cc < 3) tmem_wait_ld(nxt);
+    }
+}
+
+// ln E_c of four consecutive chunks 4q .. 4q + 3 (one Philox call, draws n = global chunk index).
+__device__ __forceinline__ void chunk_variates4(uint64_t seed, uint32_t j, uint32_t i, uint32_t q, float (&lnE)[4]) {
+    const uint4 w = philox10(make_uint4(q, i, j, DSPARK_P_SAMPLE_CHUNK), (uint32_t)seed, (uint32_t)(seed >> 32));
+    lnE[0] = log_neg_log_u_nb(u01(w.x));
+    lnE[1] = log_neg_log_u_nb(u01(w.y));
+    lnE[2] = log_neg_log_u_nb(u01(w.z));
+    lnE[3] = log_neg_log_u_nb(u01(w.w));
+}
+
+template <bool GREEDY>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    sample_tc_kernel(const __grid_constant__ CUtensorMap tm_base, const __grid_constant__ CUtensorMap tm_w2,
+                     const TcArgs a) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    if (smem_addr(smem_raw) & 1023u) {  // the swizzled tiles need 1024-byte alignment (uniform exit)
+        if (threadIdx.x == 0) record_status(&a.hdr->status, DSPARK_ERR_UNSUPPORTED);
+        return;
+    }
+    unsigned char* sm = smem_raw;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kSmBars);
+    uint64_t* w2_full = bars;
+    uint64_t* a_full = bars + 1;                       // [2]
+    uint64_t* a_empty = bars + 3;                      // [2]
+    uint64_t* b_full = bars + 5;                       // [kTcStages]
+    uint64_t* b_empty = b_full + kTcStages;            // [kTcStages]
+    uint64_t* t_full = b_empty + kTcStages;            // [kTcTmemSlots]
+    uint64_t* t_empty = t_full + kTcTmemSlots;         // [kTcTmemSlots]
+    uint64_t* done_bar = t_empty + kTcTmemSlots;
+    uint64_t* drain_bar = done_bar + 1;
+    int* flags = reinterpret_cast<int*>(sm + kSmFlags);
+    volatile int* abort = flags;
+    int* wg_done = flags + 1;          // warpgroup-units finished (two per unit)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(flags + 2);
+    volatile int* nb_issued = flags + 3;
+    volatile int* n_mma = flags + 4;   // MMAs issued (drained before the tensor memory is freed)
+    volatile int* w2_armed = flags + 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tile = blockIdx.x, tile0 = tile * kTcTile;
+    const int total = a.gamma * a.nrb;
+
+    if (tid == 0) {
+        mbar_init(w2_full, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&a_full[b], 4);
+            mbar_init(&a_empty[b], 1);
+        }
+        for (int b = 0; b < kTcStages; ++b) {
+            mbar_init(&b_full[b], 1);
+            mbar_init(&b_empty[b], 1);
+        }
+        for (int b = 0; b < kTcTmemSlots; ++b) {
+            mbar_init(&t_full[b], 1);
+            mbar_init(&t_empty[b], 4);
+        }
+        mbar_init(done_bar, 1);
+        mbar_init(drain_bar, 1);
+        for (int f = 0; f < 16; ++f) flags[f] = 0;
+        mbar_init_fence();
+    }
+    if (tid < 128) {  // the identity B operand: row n holds 1.0 at k = n (units 0 and 1 of its row)
+        const int n = tid >> 3, u = tid & 7;
+        const int k = n & 7;  // bf16 1.0 = 0x3F80 at element k of unit n / 8
+        const uint32_t one = (u < 2 && (n >> 3) == u) ? ((k & 1) ? 0x3F800000u : 0x00003F80u) : 0u;
+        const int wd = k >> 1;
+        *reinterpret_cast<uint4*>(sm + kSmId + sw128_offset(n, u)) =
+            make_uint4(wd == 0 ? one : 0u, wd == 1 ? one : 0u, wd == 2 ? one : 0u, wd == 3 ? one : 0u);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- tensor copies
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_base);
+            tma_prefetch_desc(&tm_w2);
+            const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
+            mbar_arrive_expect_tx(w2_full, kW2Bytes);
+            for (int q = 0; q < kTcTile / 256; ++q)
+                tma_load_2d(sm + kSmW2 + q * 256 * 128, &tm_w2, 0, tile0 + 256 * q, w2_full, keep);
+            *w2_armed = 1;
+            const int nbox = total * kTcBoxes;
+            for (int g = 0; g < nbox; ++g) {
+                const int st = g % kTcStages, use = g / kTcStages;
+                if (use > 0 && !mbar_wait_hint_or_abort(&b_empty[st], (uint32_t)((use - 1) & 1), abort,
+                                                        &a.hdr->status, a.limit_ns))
+                    break;
+                const int u = g / kTcBoxes, k = g % kTcBoxes;
+                const int s = u / a.nrb, rb = u % a.nrb;
+                mbar_arrive_expect_tx(&b_full[st], kBoxBytes);
+                tma_load_3d(sm + kSmBase + st * kBoxBytes, &tm_base, tile0 + kTcBox * k, s, rb * kTcRows, &b_full[st],
+                            stream);
+                *nb_issued = g + 1;
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            constexpr uint32_t idesc_bias = umma_idesc_bf16(kTcRows, kTcN);
+            constexpr uint32_t idesc_base = umma_idesc_bf16(kTcRows, 16);
+            const uint32_t w2s = smem_addr(sm + kSmW2);
+            const uint64_t id_desc = umma_desc_sw128(smem_addr(sm + kSmId), 1024);
+            bool ok = mbar_wait_hint_or_abort(w2_full, 0, abort, &a.hdr->status, a.limit_ns);
+            for (int u = 0; u < total && ok; ++u) {
+                const int ab = u & 1;
+                if (!mbar_wait_hint_or_abort(&a_full[ab], (uint32_t)((u >> 1) & 1), abort, &a.hdr->status, a.limit_ns))
+                    break;
+                const uint32_t as = smem_addr(sm + kSmA + ab * kABytes);
+                for (int acc = 0; acc < kTcAccs && ok; ++acc) {
+                    const int ga = u * kTcAccs + acc, sl = ga % kTcTmemSlots, use = ga / kTcTmemSlots;
+                    if (use > 0 && !mbar_wait_hint_or_abort(&t_empty[sl], (uint32_t)((use - 1) & 1), abort,
+                                                            &a.hdr->status, a.limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem + (uint32_t)(sl * kTcN);
+                    const uint32_t bs = w2s + (uint32_t)(acc * kTcN * 128);
+#pragma unroll
+                    for (int k = 0; k < kTcRank / 16; ++k)
+                        umma_bf16(d, umma_desc_sw128(as + 32 * k, 1024), umma_desc_sw128(bs + 32 * k, 1024), idesc_bias,
+                                  k > 0 ? 1u : 0u);
+                    *n_mma = 1;
+                    for (int bh = 0; bh < 2; ++bh) {
+                        const int g = u * kTcBoxes + 2 * acc + bh, bst = g % kTcStages;
+                        if (!mbar_wait_hint_or_abort(&b_full[bst], (uint32_t)((g / kTcStages) & 1), abort,
+                                                     &a.hdr->status, a.limit_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t bsrc = smem_addr(sm + kSmBase + bst * kBoxBytes);
+#pragma unroll
+                        for (int i = 0; i < kTcBox / 16; ++i)  // D[:, 16i..] += base[:, 16i..] . I
+                            umma_bf16(d + (uint32_t)(64 * bh + 16 * i), umma_desc_sw128(bsrc + 32 * i, 1024), id_desc,
+                                      idesc_base, 1u);
+                        umma_commit(&b_empty[bst]);  // the copy slot is free once these have read it
+                    }
+                    if (!ok) break;
+                    umma_commit(&t_full[sl]);
+                }
+                if (ok) umma_commit(&a_empty[ab]);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ---------------------------------------------------------------- arriver
+        if (lane == 0) {
+            for (int u = 0; u < total; ++u) {
+                const uint64_t t0 = global_ns();
+                bool ok = true;
+                int c;
+                while ((c = ld_acq_cta(wg_done)) < 2 * (u + 1)) {
+                    // one arrival per finished warpgroup-unit, so phase c completes at the next one;
+                    // the count decides, the barrier only wakes this thread
+                    mbar_try_wait_hint(done_bar, (uint32_t)(c & 1), 20000u);
+                    if (*abort) {
+                        ok = false;
+                        break;
+                    }
+                    if (global_ns() - t0 > a.limit_ns) {
+                        record_status(&a.hdr->status, DSPARK_ERR_TIMEOUT);
+                        *abort = 1;
+                        ok = false;
+                        break;
+                    }
+                }
+                if (!ok) break;
+                asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.rb_count + (size_t)(u % a.nrb) *
+                                                                                             kTcCountStride)
+                             : "memory");
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 4 && warp < 8) {
+        // ---------------------------------------------------------------- exchange
+        const int row = tid - 128;
+        bool live = true;
+        auto collect = [&](int s, int rb, int& tok) -> bool {  // the token drawn at step s - 1 (s >= 1)
+            int ok = 1;
+            if (row == 0) {
+                const unsigned* cp = a.rb_count + (size_t)rb * kTcCountStride;
+                const uint64_t t0 = global_ns();
+                while (ld_acquire_u32(cp) < (uint32_t)a.G * (uint32_t)s) {
+                    if (*abort || ld_relaxed_s32(&a.hdr->status) == DSPARK_ERR_TIMEOUT) {
+                        *abort = 1;
+                        ok = 0;
+                        break;
+                    }
+                    if (global_ns() - t0 > a.limit_ns) {
+                        record_status(&a.hdr->status, DSPARK_ERR_TIMEOUT);
+                        *abort = 1;
+                        ok = 0;
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+            }
+            if (bar_red_or(3, 128, ok == 0)) return false;
+            const int j = rb * kTcRows + row;
+            tok = 0;
+            if (j < a.B) {
+                const unsigned long long w = __ldcg(a.slots + ((size_t)(s - 1) * a.B + j) * kTcSlotStride);
+                const int cand = ~(int)(uint32_t)w;
+                tok = cand;
+                if (tok < 0 || tok >= a.V) {  // a request whose chunks all had no mass
+                    record_status(&a.hdr->status, DSPARK_ERR_TOKEN_RANGE);
+                    tok = min(max(tok, 0), a.V - 1);
+                }
+                if (j % a.G == (int)blockIdx.x) {
+                    const size_t o = (size_t)j * a.gamma + (s - 1);
+                    a.tokens[o] = cand;
+                    if (GREEDY) {
+                        a.draft_lse[o] = CUDART_NAN_F;
+                        a.zat[o] = unpack_key(w);
+                    }
+                }
+            }
+            return true;
+        };
+        // LSE(z/T) over the half-tile log-masses and z at the token of the rows this CTA owns
+        // (T > 0), a warp per owned row: one load of all records, warp reductions, and the
+        // 64-term dot product of z at the token split over the lanes.
+        auto owner_stats = [&](int s, int rb, int tok) {
+            if (GREEDY) return;
+            const int j = rb * kTcRows + row;
+            unsigned own = __ballot_sync(0xffffffffu, j < a.B && j % a.G == (int)blockIdx.x);
+            const int n = 2 * a.nt;
+            while (own) {
+                const int src = __ffs(own) - 1;
+                own &= own - 1;
+                const int jj = j - lane + src;
+                const int tk = __shfl_sync(0xffffffffu, tok, src);
+                const float* rec = a.part + ((size_t)(s % 3) * a.B + jj) * a.part_ld;
+                float y[kTcMaxTiles * 2 / 32];
+                float m = -CUDART_INF_F;
+#pragma unroll
+                for (int q = 0; q < kTcMaxTiles * 2 / 32; ++q) {
+                    const int idx = lane + 32 * q;
+                    y[q] = idx < n ? __ldcg(rec + idx) * kLog2e : -CUDART_INF_F;
+                    m = fmaxf(m, y[q]);
+                }
+                m = warp_max(m);
+                float sum = 0.f;
+                if (m != -CUDART_INF_F) {
+#pragma unroll
+                    for (int q = 0; q < kTcMaxTiles * 2 / 32; ++q) sum += ex2(y[q] - m);
+                }
+                sum = warp_sum(sum);
+                // z at the token: base + W2[tok] . W1[prev], prev = the token before step s
+                const size_t o = (size_t)jj * a.gamma + s;
+                int prev = s == 0 ? a.anchor[jj] : a.tokens[o - 1];
+                prev = min(max(prev, 0), a.V - 1);
+                const uint32_t w1 = __ldg(reinterpret_cast<const uint32_t*>(a.W1 + (size_t)prev * kTcRank) + lane);
+                const uint32_t w2 = __ldg(reinterpret_cast<const uint32_t*>(a.W2 + (size_t)tk * kTcRank) + lane);
+                const float bias = warp_sum(fmaf(bf16_lo(w1), bf16_lo(w2), bf16_hi(w1) * bf16_hi(w2)));
+                if (lane == 0) {
+                    a.draft_lse[o] = m == -CUDART_INF_F ? -CUDART_INF_F : (m + lg2(sum)) * kLn2;
+                    a.zat[o] = bf16_bits_to_f32(__ldg(a.base + o * (size_t)a.V + tk)) + bias;
+                }
+            }
+        };
+        for (int u = 0; u < total && live; ++u) {
+            const int s = u / a.nrb, rb = u % a.nrb;
+            const int j = rb * kTcRows + row;
+            int tok = 0;
+            if (s == 0) {
+                if (j < a.B) {
+                    tok = a.anchor[j];
+                    if (tok < 0 || tok >= a.V) {
+                        record_status(&a.hdr->status, DSPARK_ERR_TOKEN_RANGE);
+                        tok = min(max(tok, 0), a.V - 1);
+                    }
+                }
+            } else if (!collect(s, rb, tok)) {
+                live = false;
+                break;
+            }
+            uint4 w[8];  // the W1 row, loaded before the A buffer is free
+            if (j < a.B) {
+                const uint4* src = reinterpret_cast<const uint4*>(a.W1 + (size_t)tok * kTcRank);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) w[q] = __ldg(src + q);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) w[q] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            // the A buffer was last read by the MMAs of unit u - 2
+            if (u >= 2 && !warp_wait(&a_empty[u & 1], (uint32_t)(((u >> 1) - 1) & 1), abort, a)) live = false;
+            if (live) {
+                unsigned char* ad = sm + kSmA + (u & 1) * kABytes;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(ad + sw128_offset(row, q)) = w[q];
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive_local(&a_full[u & 1]);
+            }
+            if (bar_red_or(3, 128, !live)) break;
+            if (s > 0) owner_stats(s - 1, rb, tok);
+        }
+        // the last step's tokens
+        for (int rb = 0; rb < a.nrb && live; ++rb) {
+            int tok = 0;
+            if (!collect(a.gamma, rb, tok)) break;
+            owner_stats(a.gamma - 1, rb, tok);
+        }
+    } else if (warp >= 8) {
+        // ---------------------------------------------------------------- epilogue
+        const int h = (warp - 8) >> 2;                 // accumulators of parity h
+        const int row = (warp & 3) * 32 + lane;        // TMEM lane = request within the row block
+        const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const bool full_tile = tile0 + kTcTile <= a.V;
+        bool live = true;
+        for (int u = 0; u < total && live; ++u) {
+            const int s = u / a.nrb, rb = u % a.nrb;
+            const int j = rb * kTcRows + row;
+            const bool valid = j < a.B;
+            const uint32_t i = (uint32_t)s + 1u;
+            const float uin = (!GREEDY && valid) ? uniform(a.seed, (uint32_t)j, i, DSPARK_P_SAMPLE_INCHUNK, 0u) : 0.f;
+            ChunkState cs{-CUDART_INF_F, -1, -CUDART_INF_F, 0.f};
+            bool ok = true;
+            for (int ah = 0; ah < kTcAccs / 2; ++ah) {
+                const int acc = 2 * ah + h;
+                const int ga = u * kTcAccs + acc, sl = ga % kTcTmemSlots;
+                float lnE[4] = {0.f, 0.f, 0.f, 0.f};
+                if (!GREEDY) chunk_variates4(a.seed, (uint32_t)j, i, (uint32_t)(tile * (kTcTile / 128) + acc), lnE);
+                if (!warp_wait(&t_full[sl], (uint32_t)((ga / kTcTmemSlots) & 1), abort, a)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tl + (uint32_t)(sl * kTcN);
+                const int id0 = tile0 + kTcN * acc;
+                if (full_tile) accumulator_chunks<GREEDY, false>(taddr, id0, a.V, a.scale2, uin, lnE, cs);
+                else accumulator_chunks<GREEDY, true>(taddr, id0, a.V, a.scale2, uin, lnE, cs);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_local(&t_empty[sl]);
+            }
+            if (ok && valid) {
+                if (!GREEDY) a.part[((size_t)(s % 3) * a.B + j) * a.part_ld + 2 * tile + h] =
+                    (cs.mt == -CUDART_INF_F) ? -CUDART_INF_F : (cs.mt + lg2(cs.st)) * kLn2;
+                red_max_u64(a.slots + ((size_t)s * a.B + j) * kTcSlotStride, pack_key(cs.bkey, cs.bcand));
+            }
+            if (bar_red_or(1 + h, 128, !ok)) {
+                live = false;
+                break;
+            }
+            if (row == 0) {  // this warpgroup's maxima are issued: the arriver publishes the unit
+                add_rel_cta(wg_done, 1);
+                mbar_arrive_local(done_bar);
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && *abort) {  // copies in flight land before the shared memory goes away
+        if (*w2_armed) mbar_wait_bounded(w2_full, 0, &a.hdr->status, a.limit_ns);
+        const int nb = *nb_issued;
+        for (int g = max(0, nb - kTcStages); g < nb; ++g)
+            mbar_wait_bounded(&b_full[g % kTcStages], (uint32_t)((g / kTcStages) & 1), &a.hdr->status, a.limit_ns);
+    }
+    if (warp == 1) {
+        if (lane == 0 && *n_mma) {  // every MMA issued has completed
+            umma_commit(drain_bar);
+            mbar_wait_bounded(drain_bar, 0, &a.hdr->status, a.limit_ns);
+        }
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+}  // namespace
+
+bool sample_tc_eligible(const dspark_sample_params* p, const void* base, const void* W1, const void* W2, int sms) {
+    const int nt = (p->V + kTcTile - 1) / kTcTile;
+    return p->logits_dtype == DSPARK_BF16 && p->w_dtype == DSPARK_BF16 && p->r == kTcRank && p->B >= kTcMinBatch &&
+           p->V % 8 == 0 && ((uintptr_t)base % 16) == 0 && ((uintptr_t)W1 % 16) == 0 && ((uintptr_t)W2 % 16) == 0 &&
+           nt <= sms && nt <= kTcMaxTiles && tensor_map_encoder() != nullptr;
+}
+
+dspark_status launch_sample_tc(const dspark_sample_params* p, const void* base_logits, const void* W1, const void* W2,
+                               const int32_t* anchor, int32_t* tokens, float* draft_lse, float* draft_logit_at_tok,
+                               const SampleWsLayout& L, void* workspace, cudaStream_t s) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return DSPARK_ERR_UNSUPPORTED;
+    const int nt = (p->V + kTcTile - 1) / kTcTile;
+    CUtensorMap m_base, m_w2;
+    {
+        cuuint64_t dims[3] = {(cuuint64_t)p->V, (cuuint64_t)p->gamma, (cuuint64_t)p->B};
+        cuuint64_t strides[2] = {(cuuint64_t)p->V * 2, (cuuint64_t)p->gamma * p->V * 2};
+        cuuint32_t box[3] = {kTcBox, 1, kTcRows};
+        cuuint32_t es[3] = {1, 1, 1};
+        if (enc(&m_base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base_logits), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return DSPARK_ERR_UNSUPPORTED;
+    }
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)kTcRank, (cuuint64_t)p->V};
+        cuuint64_t strides[1] = {(cuuint64_t)kTcRank * 2};
+        cuuint32_t box[2] = {kTcRank, 256};
+        cuuint32_t es[2] = {1, 1};
+        if (enc(&m_w2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W2), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return DSPARK_ERR_UNSUPPORTED;
+    }
+    const bool greedy = p->temperature == 0.f;
+    const void* fn = greedy ? (const void*)sample_tc_kernel<true> : (const void*)sample_tc_kernel<false>;
+    int per_sm = 0;
+    if (prepare_kernel(fn, kTcSmemBytes, kTcThreads, &per_sm) != cudaSuccess || per_sm < 1) return DSPARK_ERR_CUDA;
+
+    TcArgs a;
+    a.B = p->B;
+    a.gamma = p->gamma;
+    a.V = p->V;
+    a.nt = nt;
+    a.nrb = (p->B + kTcRows - 1) / kTcRows;
+    a.G = nt;
+    a.part_ld = 2 * nt;
+    a.scale2 = greedy ? 1.f : kLog2e / p->temperature;
+    a.seed = p->seed;
+    a.base = static_cast<const uint16_t*>(base_logits);
+    a.W1 = static_cast<const uint16_t*>(W1);
+    a.W2 = static_cast<const uint16_t*>(W2);
+    a.anchor = anchor;
+    a.tokens = tokens;
+    a.draft_lse = draft_lse;
+    a.zat = draft_logit_at_tok;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    a.hdr = reinterpret_cast<WsHeader*>(ws);
+    a.slots = reinterpret_cast<unsigned long long*>(ws + L.slots);
+    a.rb_count = reinterpret_cast<unsigned*>(ws + L.counts);
+    a.part = reinterpret_cast<float*>(ws + L.part);
+    a.limit_ns = wait_limit_ns();
+    if (cudaMemsetAsync(workspace, 0, L.zeroed, s) != cudaSuccess) return DSPARK_ERR_CUDA;
+    void* args[] = {(void*)&m_base, (void*)&m_w2, (void*)&a};
+    if (cudaLaunchCooperativeKernel(fn, dim3(nt), dim3(kTcThreads), args, kTcSmemBytes, s) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
+    return DSPARK_OK;
+}
+
+}  // namespace dspark

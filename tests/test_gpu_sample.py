@@ -108,9 +108,53 @@ def test_full_b128_r256_sampled_requests():
 
 
 def test_full_b512_r64_sampled_requests():
+    # the tensor-core sampler: requests from every 128-request row block, first and last lanes
     wl = W.b512_sched(device="cuda")
-    tally, _ = run_and_compare(wl, requests=[0, 300, 511])
+    tally, _ = run_and_compare(wl, requests=[0, 1, 31, 32, 127, 128, 200, 255, 256, 300, 383, 384, 450, 510, 511])
     tally.check_fraction()
+
+
+# ---------------------------------------------------------------- tensor-core sampler (B >= 64, r = 64)
+@pytest.mark.parametrize("T", [0.0, 0.8])
+def test_tc_ragged_vocab_and_row_block(T):
+    # V = 5000: four full 1024-id tiles and a ragged one whose last 64-id copy is partly past V;
+    # B = 200: one full 128-request row block and a partial one
+    wl = W.make_sample_workload("tc", 200, 3, 5000, 64, T, device="cuda", data_seed=31, philox_seed=4, planted=3,
+                                w_std=0.3)
+    tally, _ = run_and_compare(wl)
+    tally.check_fraction()
+
+
+@pytest.mark.parametrize("B,gamma,V,T", [(64, 2, 2048, 0.7), (300, 5, 4096, 1.0), (128, 6, 3000, 0.0),
+                                         (129, 4, 1032, 1.3)])
+def test_tc_shapes(B, gamma, V, T):
+    wl = W.make_sample_workload("tcs", B, gamma, V, 64, T, device="cuda", data_seed=B + V, philox_seed=B,
+                                planted=2, w_std=0.4)
+    tally, _ = run_and_compare(wl)
+    tally.check_fraction()
+
+
+def test_tc_bias_matters_and_deterministic():
+    wl = W.make_sample_workload("tcb", 128, 4, 4096, 64, 0.0, device="cuda", data_seed=8, w_std=0.5)
+    tally, (tok, _, _) = run_and_compare(wl)
+    t = wl.tensors
+    no_bias = torch.argmax(t["base"].float(), dim=-1).to(torch.int32)
+    assert (tok != no_bias).float().mean().item() > 0.5
+    wl = W.make_sample_workload("tcd", 160, 4, 3000, 64, 1.0, device="cuda", data_seed=2)
+    t = wl.tensors
+    a = api.markov_sample_block(t["base"], t["W1"], t["W2"], t["anchor"], 1.0, 5)[0].clone()
+    b = api.markov_sample_block(t["base"], t["W1"], t["W2"], t["anchor"], 1.0, 5)[0].clone()
+    c = api.markov_sample_block(t["base"], t["W1"], t["W2"], t["anchor"], 1.0, 6)[0].clone()
+    assert torch.equal(a, b) and not torch.equal(a, c)
+
+
+def test_tc_anchor_out_of_range_sets_status():
+    wl = W.make_sample_workload("tcbad", 96, 2, 2048, 64, 1.0, device="cuda")
+    t = wl.tensors
+    anchor = t["anchor"].clone()
+    anchor[70] = 5000
+    _, _, _, ws = api.markov_sample_block(t["base"], t["W1"], t["W2"], anchor, 1.0, 0)
+    assert binding.dspark_get_device_status(ws) == 7
 
 
 @pytest.mark.parametrize("T", [0.0, 1.0])
