@@ -8,18 +8,19 @@
 //
 // One persistent cooperative kernel; CTA b owns vocabulary tile b (1024 ids) for all gamma steps.
 // Requests go in row blocks of 128 (one TMEM lane each); a unit is one (step, row block).
-//   - W2 rows of the tile (1024 x 64 bf16, 128 KB) are copied into shared memory once by a tiled
-//     tensor copy (128-byte swizzle, the K-major MMA layout) and stay there.
 //   - z of a unit, D[128 requests x 1024 ids], is computed entirely on the tensor cores, as eight
-//     accumulators of 128 fp32 TMEM columns (four rotating slots = all 512 columns):
-//       bias: D = W1[prev] . W2_tile^T, four kind::f16 MMAs of M = 128, N = 128, K = 16, with A =
+//     accumulators of 128 ids in fp32 TMEM columns (four rotating slots = all 512 columns):
+//       bias: D = W1[prev] . W2_rows^T, four kind::f16 MMAs of M = 128, N = 128, K = 16, with A =
 //             the 128 W1 rows of the previous tokens (written into shared memory, swizzled, by the
-//             exchange warps) and B = 128 resident W2 rows;
-//       base: D += base . I, the base logits of the unit (bf16, streamed by 3-D tiled copies of
-//             64 ids x 128 requests, 128-byte swizzle, through a four-slot ring) as the A operand
-//             and a 16 x 16 identity as B: four MMAs of N = 16, K = 16 per copy, each adding 16
-//             ids' base values in fp32.  The copies do not depend on the tokens, so those of the
-//             next step run ahead of the exchange.
+//             exchange warps) and B = the accumulator's 128 W2 rows;
+//       base: D += base . I, the accumulator's base logits (bf16, two 3-D copies of 64 ids x 128
+//             requests) as the A operand and a 16 x 16 identity as B: four MMAs of N = 16, K = 16
+//             per copy, each adding 16 ids' base values in fp32.
+//     The operands of each accumulator (its W2 rows, re-read from L2 where W2 is kept with an
+//     evict-last policy, and its base copies, evict-first) arrive by tiled tensor copies (128-byte
+//     swizzle, the K-major MMA layout) in one 48 KB stage of a four-stage ring.  With the four TMEM
+//     accumulators that is eight accumulators of lookahead, so the copies of the next units (they do
+//     not depend on the tokens) run well ahead of the epilogue.
 //   - Epilogue: two warpgroups, one per parity of accumulator.  Thread = request: it reads its
 //     lane's 32 columns of a chunk from TMEM (the next chunk's load in flight meanwhile) and forms
 //     the chunk record of the contract with no shuffles: max, the weights 2^(z s - max), their
@@ -52,34 +53,34 @@ constexpr int kTcN = 128;                     // ids per accumulator = MMA N of 
 constexpr int kTcAccs = kTcTile / kTcN;       // accumulators per unit
 constexpr int kTcTmemSlots = 4;               // 4 x 128 fp32 columns = all 512 TMEM columns
 constexpr int kTcBox = 64;                    // ids per base copy (128 bytes: one swizzle span)
-constexpr int kTcBoxes = kTcTile / kTcBox;    // base copies per unit
-constexpr int kTcStages = 4;                  // base copy ring
+constexpr int kTcStages = 4;                  // operand ring: one accumulator's W2 rows and base copies per stage
 constexpr int kTcRank = 64;                   // K of the bias (W1 / W2 row = 128 bytes)
 constexpr int kTcThreads = 512;
-constexpr int kTcMaxTiles = 160;              // vocabulary tiles (CTAs) at most: 2 log-mass records each per request
+constexpr int kTcMaxTiles = 160;              // vocabulary tiles (CTAs) at most
+constexpr int kTcEpiGroups = 2;               // epilogue warpgroups (one partial record each per tile and request)
 constexpr int kTcSlotStride = 16;             // 64-bit words between two requests' maxima (one 128-byte line)
 constexpr int kTcCountStride = 32;            // 32-bit words between two row blocks' arrival counters
 constexpr uint32_t kBoxBytes = kTcBox * kTcRows * 2;       // 16 KB
 constexpr uint32_t kABytes = kTcRows * kTcRank * 2;        // 16 KB
-constexpr uint32_t kW2Bytes = kTcTile * kTcRank * 2;       // 128 KB
+constexpr uint32_t kW2SubBytes = kTcN * kTcRank * 2;      // W2 rows of one accumulator: 16 KB
+constexpr uint32_t kStageBytes = kW2SubBytes + 2 * kBoxBytes;  // 48 KB
 constexpr uint32_t kIdBytes = 16 * 128;                    // 16 x 16 identity, rows of a 128-byte swizzled tile
 
 // shared memory (offsets from the 1024-byte aligned base)
-constexpr uint32_t kSmW2 = 0;
-constexpr uint32_t kSmA = kSmW2 + kW2Bytes;                 // [2]
+constexpr uint32_t kSmRing = 0;                             // [kTcStages] {W2 rows, base box 0, base box 1}
+constexpr uint32_t kSmA = kSmRing + kTcStages * kStageBytes;  // [2]
 constexpr uint32_t kSmId = kSmA + 2 * kABytes;
-constexpr uint32_t kSmBase = kSmId + kIdBytes;              // [kTcStages]
-constexpr uint32_t kSmBars = kSmBase + kTcStages * kBoxBytes;
-constexpr int kNumBars = 5 + 2 * kTcStages + 2 * kTcTmemSlots + 2;
+constexpr uint32_t kSmBars = kSmId + kIdBytes;
+constexpr int kNumBars = 4 + 2 * kTcStages + 2 * kTcTmemSlots + 2;
 constexpr uint32_t kSmFlags = kSmBars + 8 * kNumBars;
 constexpr uint32_t kSmTotal = kSmFlags + 64;
 constexpr size_t kTcSmemBytes = kSmTotal;  // the dynamic base is 1024-byte aligned (checked at entry)
-static_assert(kSmBase % 1024 == 0, "base stages are 1024-byte aligned");
+static_assert(kStageBytes % 1024 == 0 && kSmA % 1024 == 0, "operand tiles are 1024-byte aligned");
 static_assert(kTcSmemBytes <= 227 * 1024, "shared memory of the tensor-core sampler");
 
 struct TcArgs {
     int B, gamma, V, nt, nrb, G;
-    int part_ld;          // floats per request row of the log-mass records (2 per tile)
+    int part_ld;          // floats per request row of the log-mass records (kTcEpiGroups per tile)
     float scale2;         // log2(e) / T (1 when greedy)
     uint64_t seed;
     const uint16_t* base;  // bf16 bits [B, gamma, V]
@@ -92,7 +93,7 @@ struct TcArgs {
     WsHeader* hdr;
     unsigned long long* slots;  // [gamma][B] packed maxima, kTcSlotStride words apart (zeroed per call)
     unsigned* rb_count;         // [nrb] arrival counters, kTcCountStride apart (zeroed per call)
-    float* part;                // [3][B][part_ld] per-half-tile log-masses (natural log)
+    float* part;                // [3][B][part_ld] partial log-masses (natural log), one per tile and warpgroup
     uint64_t limit_ns;
 };
 
@@ -127,67 +128,76 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 struct ChunkState {
     float bkey;  // best key so far (T > 0: LSE_c - ln E_c; greedy: max z)
     int bcand;   // its candidate id
-    float mt, st;  // log2-mass of the chunks seen: 2^mt * st
+    float mt, st;  // mass of the chunks seen = 2^mt * st; mt = the largest scaled chunk maximum so far
 };
 
 // Chunk record of one request over 32 ids in registers (T > 0), folded into the state.  Chunks
 // arrive in increasing id order, so a strictly greater key is needed to replace the best (ties
-// keep the lower chunk).  ids past V (MASK) are -inf.  No early exit and one warp vote: every lane
-// of the warp runs this in step.
+// keep the lower chunk).  ids past V (MASK) are -inf.  The weights are taken relative to the
+// running maximum mt (not the chunk's own), which folds the chunk into the mass with one
+// exponential; a chunk more than 2^126 below the running maximum then has no weight, and it
+// cannot win the race (its key is ~87 nats below the leader's, beyond any Gumbel variate).
+// The inverse CDF runs on prefix sums in four blocks of eight ids, kept as two packed pairs of
+// blocks (0, 1) and (2, 3).  No early exit and one warp vote: every lane of the warp runs this
+// in step.
 template <bool MASK>
 __device__ __forceinline__ void chunk_sample(const uint32_t (&v)[32], int id0, int V, float scale2, float u, float lnE,
                                              ChunkState& cs) {
     float z[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) z[e] = (MASK && id0 + e >= V) ? -CUDART_INF_F : __uint_as_float(v[e]);
-    const float m = max32(z);
-    const bool has = m != -CUDART_INF_F;
-    const float m2 = has ? m * scale2 : 0.f;  // no ids: weights 2^-inf = 0, never NaN
-    float p[32];
-    const uint64_t s2 = pk2(scale2, scale2), nm2 = pk2(-m2, -m2);
+    const float nm = fmaxf(cs.mt, max32(z) * scale2);
+    const float ref = nm == -CUDART_INF_F ? 0.f : nm;  // no ids at all: weights 2^-inf = 0, never NaN
+    const uint64_t s2 = pk2(scale2, scale2), nr = pk2(-ref, -ref);
+    uint64_t q[8], r[8];  // q[k] = ids (k, 8 + k), r[k] = ids (16 + k, 24 + k)
 #pragma unroll
-    for (int h = 0; h < 16; ++h) {
-        const float2 y = up2(fma2(pk2(z[2 * h], z[2 * h + 1]), s2, nm2));
-        p[2 * h] = ex2(y.x);
-        p[2 * h + 1] = ex2(y.y);
+    for (int k = 0; k < 8; ++k) {
+        const float2 x = up2(fma2(pk2(z[k], z[8 + k]), s2, nr));
+        const float2 y = up2(fma2(pk2(z[16 + k], z[24 + k]), s2, nr));
+        q[k] = pk2(ex2(x.x), ex2(x.y));
+        r[k] = pk2(ex2(y.x), ex2(y.y));
     }
-    // inclusive prefix sums in four blocks of eight (four independent chains), then block offsets
 #pragma unroll
-    for (int b = 0; b < 4; ++b)
+    for (int k = 1; k < 8; ++k) {  // inclusive prefix inside each block of eight
+        q[k] = add2(q[k], q[k - 1]);
+        r[k] = add2(r[k], r[k - 1]);
+    }
+    const float2 qe = up2(q[7]), re = up2(r[7]);
+    const float o1 = qe.x, o2 = o1 + qe.y, o3 = o2 + re.x;
+    const float S = o3 + re.y;
+    const float t = u * S, t1 = t - o1, t2 = t - o2, t3 = t - o3;
+    uint32_t neg = 0;  // minus the number of prefix values not above the target: the crossing index
 #pragma unroll
-        for (int k = 1; k < 8; ++k) p[8 * b + k] += p[8 * b + k - 1];
-    const float o1 = p[7], o2 = o1 + p[15], o3 = o2 + p[23];
-    const float S = o3 + p[31];
-    const float t = u * S;
-    const float t1 = t - o1, t2 = t - o2, t3 = t - o3;
-    int cnt = 0;
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        cnt += (p[k] <= t ? 1 : 0) + (p[8 + k] <= t1 ? 1 : 0) + (p[16 + k] <= t2 ? 1 : 0) + (p[24 + k] <= t3 ? 1 : 0);
+    for (int k = 0; k < 8; ++k) {
+        const float2 a = up2(q[k]), b = up2(r[k]);
+        neg += le_mask(a.x, t) + le_mask(a.y, t1) + le_mask(b.x, t2) + le_mask(b.y, t3);
+    }
+    int cnt = -(int)neg;
     if (__any_sync(0xffffffffu, cnt == 32)) {  // rounding left no crossing: the last id with weight
         if (cnt == 32) {
             int last = 0;
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float before = k == 0 ? 0.f : p[8 * b + k - 1];
-                    last = p[8 * b + k] > before ? 8 * b + k : last;
-                }
+            for (int k = 0; k < 8; ++k) {
+                const float2 a = up2(q[k]), b = up2(r[k]);
+                const float2 pa = k ? up2(q[k - 1]) : make_float2(0.f, 0.f);
+                const float2 pb = k ? up2(r[k - 1]) : make_float2(0.f, 0.f);
+                last = a.x > pa.x ? max(last, k) : last;
+                last = a.y > pa.y ? max(last, 8 + k) : last;
+                last = b.x > pb.x ? max(last, 16 + k) : last;
+                last = b.y > pb.y ? max(last, 24 + k) : last;
+            }
             cnt = last;
         }
     }
-    if (has && S > 0.f) {
-        const float l2 = m2 + lg2(S);
-        const float key = l2 * kLn2 - lnE;
+    if (S > 0.f) {
+        const float key = (ref + lg2(S)) * kLn2 - lnE;
         if (key > cs.bkey) {
             cs.bkey = key;
             cs.bcand = id0 + cnt;
         }
-        const float nm = fmaxf(cs.mt, l2);
-        cs.st = cs.st * ex2(cs.mt - nm) + ex2(l2 - nm);
-        cs.mt = nm;
     }
+    cs.st = cs.st * ex2(cs.mt - ref) + S;  // (st = 0 while mt = -inf: 0 * 0)
+    cs.mt = nm == -CUDART_INF_F ? cs.mt : nm;
 }
 
 // Greedy: the chunk's maximum and its lowest argmax.
@@ -230,10 +240,10 @@ __device__ __forceinline__ void accumulator_chunks(uint32_t taddr, int id0, int 
 // ln E_c of four consecutive chunks 4q .. 4q + 3 (one Philox call, draws n = global chunk index).
 __device__ __forceinline__ void chunk_variates4(uint64_t seed, uint32_t j, uint32_t i, uint32_t q, float (&lnE)[4]) {
     const uint4 w = philox10(make_uint4(q, i, j, DSPARK_P_SAMPLE_CHUNK), (uint32_t)seed, (uint32_t)(seed >> 32));
-    lnE[0] = log_neg_log_u_nb(u01(w.x));
-    lnE[1] = log_neg_log_u_nb(u01(w.y));
-    lnE[2] = log_neg_log_u_nb(u01(w.z));
-    lnE[3] = log_neg_log_u_nb(u01(w.w));
+    lnE[0] = log_neg_log_u_2(u01(w.x));
+    lnE[1] = log_neg_log_u_2(u01(w.y));
+    lnE[2] = log_neg_log_u_2(u01(w.z));
+    lnE[3] = log_neg_log_u_2(u01(w.w));
 }
 
 template <bool GREEDY>
@@ -247,10 +257,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     unsigned char* sm = smem_raw;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kSmBars);
-    uint64_t* w2_full = bars;
-    uint64_t* a_full = bars + 1;                       // [2]
-    uint64_t* a_empty = bars + 3;                      // [2]
-    uint64_t* b_full = bars + 5;                       // [kTcStages]
+    uint64_t* a_full = bars;                           // [2]
+    uint64_t* a_empty = bars + 2;                      // [2]
+    uint64_t* b_full = bars + 4;                       // [kTcStages]
     uint64_t* b_empty = b_full + kTcStages;            // [kTcStages]
     uint64_t* t_full = b_empty + kTcStages;            // [kTcTmemSlots]
     uint64_t* t_empty = t_full + kTcTmemSlots;         // [kTcTmemSlots]
@@ -262,13 +271,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(flags + 2);
     volatile int* nb_issued = flags + 3;
     volatile int* n_mma = flags + 4;   // MMAs issued (drained before the tensor memory is freed)
-    volatile int* w2_armed = flags + 5;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tile = blockIdx.x, tile0 = tile * kTcTile;
     const int total = a.gamma * a.nrb;
 
     if (tid == 0) {
-        mbar_init(w2_full, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&a_full[b], 4);
             mbar_init(&a_empty[b], 1);
@@ -310,22 +317,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tma_prefetch_desc(&tm_base);
             tma_prefetch_desc(&tm_w2);
             const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
-            mbar_arrive_expect_tx(w2_full, kW2Bytes);
-            for (int q = 0; q < kTcTile / 256; ++q)
-                tma_load_2d(sm + kSmW2 + q * 256 * 128, &tm_w2, 0, tile0 + 256 * q, w2_full, keep);
-            *w2_armed = 1;
-            const int nbox = total * kTcBoxes;
-            for (int g = 0; g < nbox; ++g) {
-                const int st = g % kTcStages, use = g / kTcStages;
+            const int nacc = total * kTcAccs;
+            for (int ga = 0; ga < nacc; ++ga) {  // one stage per accumulator: its W2 rows and base copies
+                const int st = ga % kTcStages, use = ga / kTcStages;
                 if (use > 0 && !mbar_wait_hint_or_abort(&b_empty[st], (uint32_t)((use - 1) & 1), abort,
                                                         &a.hdr->status, a.limit_ns))
                     break;
-                const int u = g / kTcBoxes, k = g % kTcBoxes;
+                const int u = ga / kTcAccs, acc = ga % kTcAccs;
                 const int s = u / a.nrb, rb = u % a.nrb;
-                mbar_arrive_expect_tx(&b_full[st], kBoxBytes);
-                tma_load_3d(sm + kSmBase + st * kBoxBytes, &tm_base, tile0 + kTcBox * k, s, rb * kTcRows, &b_full[st],
-                            stream);
-                *nb_issued = g + 1;
+                unsigned char* dst = sm + kSmRing + st * kStageBytes;
+                mbar_arrive_expect_tx(&b_full[st], kStageBytes);
+                tma_load_2d(dst, &tm_w2, 0, tile0 + kTcN * acc, &b_full[st], keep);  // W2 stays in L2
+                tma_load_3d(dst + kW2SubBytes, &tm_base, tile0 + kTcN * acc, s, rb * kTcRows, &b_full[st], stream);
+                tma_load_3d(dst + kW2SubBytes + kBoxBytes, &tm_base, tile0 + kTcN * acc + kTcBox, s, rb * kTcRows,
+                            &b_full[st], stream);
+                *nb_issued = ga + 1;
             }
         }
         __syncwarp();
@@ -334,9 +340,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_bias = umma_idesc_bf16(kTcRows, kTcN);
             constexpr uint32_t idesc_base = umma_idesc_bf16(kTcRows, 16);
-            const uint32_t w2s = smem_addr(sm + kSmW2);
             const uint64_t id_desc = umma_desc_sw128(smem_addr(sm + kSmId), 1024);
-            bool ok = mbar_wait_hint_or_abort(w2_full, 0, abort, &a.hdr->status, a.limit_ns);
+            bool ok = true;
             for (int u = 0; u < total && ok; ++u) {
                 const int ab = u & 1;
                 if (!mbar_wait_hint_or_abort(&a_full[ab], (uint32_t)((u >> 1) & 1), abort, &a.hdr->status, a.limit_ns))
@@ -349,29 +354,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         ok = false;
                         break;
                     }
+                    const int st = ga % kTcStages;
+                    if (!mbar_wait_hint_or_abort(&b_full[st], (uint32_t)((ga / kTcStages) & 1), abort, &a.hdr->status,
+                                                 a.limit_ns)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
                     const uint32_t d = tmem + (uint32_t)(sl * kTcN);
-                    const uint32_t bs = w2s + (uint32_t)(acc * kTcN * 128);
+                    const uint32_t stage = smem_addr(sm + kSmRing + st * kStageBytes);
 #pragma unroll
-                    for (int k = 0; k < kTcRank / 16; ++k)
-                        umma_bf16(d, umma_desc_sw128(as + 32 * k, 1024), umma_desc_sw128(bs + 32 * k, 1024), idesc_bias,
-                                  k > 0 ? 1u : 0u);
+                    for (int k = 0; k < kTcRank / 16; ++k)  // D = W1[prev] . W2_rows^T
+                        umma_bf16(d, umma_desc_sw128(as + 32 * k, 1024), umma_desc_sw128(stage + 32 * k, 1024),
+                                  idesc_bias, k > 0 ? 1u : 0u);
                     *n_mma = 1;
+#pragma unroll
                     for (int bh = 0; bh < 2; ++bh) {
-                        const int g = u * kTcBoxes + 2 * acc + bh, bst = g % kTcStages;
-                        if (!mbar_wait_hint_or_abort(&b_full[bst], (uint32_t)((g / kTcStages) & 1), abort,
-                                                     &a.hdr->status, a.limit_ns)) {
-                            ok = false;
-                            break;
-                        }
-                        const uint32_t bsrc = smem_addr(sm + kSmBase + bst * kBoxBytes);
+                        const uint32_t bsrc = stage + kW2SubBytes + bh * kBoxBytes;
 #pragma unroll
                         for (int i = 0; i < kTcBox / 16; ++i)  // D[:, 16i..] += base[:, 16i..] . I
                             umma_bf16(d + (uint32_t)(64 * bh + 16 * i), umma_desc_sw128(bsrc + 32 * i, 1024), id_desc,
                                       idesc_base, 1u);
-                        umma_commit(&b_empty[bst]);  // the copy slot is free once these have read it
                     }
-                    if (!ok) break;
+                    umma_commit(&b_empty[st]);  // the stage is free once these have read it
                     umma_commit(&t_full[sl]);
                 }
                 if (ok) umma_commit(&a_empty[ab]);
@@ -385,7 +390,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint64_t t0 = global_ns();
                 bool ok = true;
                 int c;
-                while ((c = ld_acq_cta(wg_done)) < 2 * (u + 1)) {
+                while ((c = ld_acq_cta(wg_done)) < kTcEpiGroups * (u + 1)) {
                     // one arrival per finished warpgroup-unit, so phase c completes at the next one;
                     // the count decides, the barrier only wakes this thread
                     mbar_try_wait_hint(done_bar, (uint32_t)(c & 1), 20000u);
@@ -460,17 +465,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (GREEDY) return;
             const int j = rb * kTcRows + row;
             unsigned own = __ballot_sync(0xffffffffu, j < a.B && j % a.G == (int)blockIdx.x);
-            const int n = 2 * a.nt;
+            const int n = kTcEpiGroups * a.nt;
             while (own) {
                 const int src = __ffs(own) - 1;
                 own &= own - 1;
                 const int jj = j - lane + src;
                 const int tk = __shfl_sync(0xffffffffu, tok, src);
                 const float* rec = a.part + ((size_t)(s % 3) * a.B + jj) * a.part_ld;
-                float y[kTcMaxTiles * 2 / 32];
+                float y[kTcMaxTiles * kTcEpiGroups / 32];
                 float m = -CUDART_INF_F;
 #pragma unroll
-                for (int q = 0; q < kTcMaxTiles * 2 / 32; ++q) {
+                for (int q = 0; q < kTcMaxTiles * kTcEpiGroups / 32; ++q) {
                     const int idx = lane + 32 * q;
                     y[q] = idx < n ? __ldcg(rec + idx) * kLog2e : -CUDART_INF_F;
                     m = fmaxf(m, y[q]);
@@ -479,7 +484,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 float sum = 0.f;
                 if (m != -CUDART_INF_F) {
 #pragma unroll
-                    for (int q = 0; q < kTcMaxTiles * 2 / 32; ++q) sum += ex2(y[q] - m);
+                    for (int q = 0; q < kTcMaxTiles * kTcEpiGroups / 32; ++q) sum += ex2(y[q] - m);
                 }
                 sum = warp_sum(sum);
                 // z at the token: base + W2[tok] . W1[prev], prev = the token before step s
@@ -573,7 +578,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (lane == 0) mbar_arrive_local(&t_empty[sl]);
             }
             if (ok && valid) {
-                if (!GREEDY) a.part[((size_t)(s % 3) * a.B + j) * a.part_ld + 2 * tile + h] =
+                if (!GREEDY) a.part[((size_t)(s % 3) * a.B + j) * a.part_ld + kTcEpiGroups * tile + h] =
                     (cs.mt == -CUDART_INF_F) ? -CUDART_INF_F : (cs.mt + lg2(cs.st)) * kLn2;
                 red_max_u64(a.slots + ((size_t)s * a.B + j) * kTcSlotStride, pack_key(cs.bkey, cs.bcand));
             }
@@ -592,7 +597,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (tid == 0 && *abort) {  // copies in flight land before the shared memory goes away
-        if (*w2_armed) mbar_wait_bounded(w2_full, 0, &a.hdr->status, a.limit_ns);
         const int nb = *nb_issued;
         for (int g = max(0, nb - kTcStages); g < nb; ++g)
             mbar_wait_bounded(&b_full[g % kTcStages], (uint32_t)((g / kTcStages) & 1), &a.hdr->status, a.limit_ns);
@@ -651,7 +655,7 @@ dspark_status launch_sample_tc(const dspark_sample_params* p, const void* base_l
     {
         cuuint64_t dims[2] = {(cuuint64_t)kTcRank, (cuuint64_t)p->V};
         cuuint64_t strides[1] = {(cuuint64_t)kTcRank * 2};
-        cuuint32_t box[2] = {kTcRank, 256};
+        cuuint32_t box[2] = {kTcRank, kTcN};
         cuuint32_t es[2] = {1, 1};
         if (enc(&m_w2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W2), dims, strides, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -670,7 +674,7 @@ dspark_status launch_sample_tc(const dspark_sample_params* p, const void* base_l
     a.nt = nt;
     a.nrb = (p->B + kTcRows - 1) / kTcRows;
     a.G = nt;
-    a.part_ld = 2 * nt;
+    a.part_ld = kTcEpiGroups * nt;
     a.scale2 = greedy ? 1.f : kLog2e / p->temperature;
     a.seed = p->seed;
     a.base = static_cast<const uint16_t*>(base_logits);
