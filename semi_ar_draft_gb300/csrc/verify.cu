@@ -326,14 +326,17 @@ __device__ void accept_walk_lanes(const VerifyArgs& a, int j, int L, int lane) {
 
 // ------------------------------------------------------------------------------- launch 1, bf16
 // Persistent variant for bf16 target rows on 16-byte boundaries: one block per SM walks the
-// verified rows (r = blockIdx.x, blockIdx.x + G, ...; row r is position r % gamma + 1 of request
-// r / gamma, verified when that position is <= L_j).  A producer warp streams each row through a
-// ring of kVNS shared-memory slots with the bulk-copy engine; 16 consumer warps reduce it to
-// (max, sum 2^(t * scale2 - max)) (T > 0) or (max, lowest argmax) (T = 0).  The block that
-// completes a request's last row runs the accept walk (rows then have one segment).
+// verified rows, numbered v = 0 .. sum_j L_j - 1 in request order (v = blockIdx.x, blockIdx.x + G,
+// ...), so every block gets the same number of rows whatever the lengths; each block finds the
+// request of row v by binary search in the prefix sums of L_j it forms first in shared memory.
+// A producer warp streams each row through a ring of kVNS shared-memory slots with the bulk-copy
+// engine; 16 consumer warps reduce it to (max, sum 2^(t * scale2 - max)) (T > 0) or (max, lowest
+// argmax) (T = 0).  The block that completes a request's last row runs the accept walk (rows then
+// have one segment).
 constexpr int kVCE = 8192;  // target ids per slot
-constexpr int kVNS = 13;    // ring slots (13 x 16 KB)
+constexpr int kVNS = 8;     // ring slots (8 x 16 KB)
 constexpr int kVThreads = kThreads + 32;
+constexpr int kVMaxB = 4096;  // requests (the prefix of their lengths is kept in shared memory)
 
 struct VRSmem {
     uint16_t slots[kVNS][kVCE];
@@ -343,13 +346,66 @@ struct VRSmem {
     int s_last;
     int abort;
     int issued;  // chunks the producer has issued
+    int nver;    // verified rows of the call
+    int voff[kVMaxB + 1];  // exclusive prefix of the valid L_j (0 for a request with an invalid length)
 };
 
-__device__ __forceinline__ bool verified_row(const VerifyArgs& a, int r, int& j, int& i, int& L) {
-    j = r / a.gamma;
-    i = r % a.gamma + 1;
-    L = req_len(a, j);
-    return L >= 1 && L <= a.gamma && req_rows(a, j) >= L && i <= L;
+__device__ __forceinline__ int valid_len(const VerifyArgs& a, int j) {
+    const int L = req_len(a, j);
+    return (L >= 1 && L <= a.gamma && req_rows(a, j) >= L) ? L : 0;
+}
+
+// Verified row v -> request j, position i (1-based) and that request's length L.
+__device__ __forceinline__ void verified_row(const VerifyArgs& a, const int* voff, int v, int& j, int& i, int& L) {
+    int lo = 0, hi = a.B - 1;  // the last j with voff[j] <= v
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (voff[mid] <= v) lo = mid;
+        else hi = mid - 1;
+    }
+    j = lo;
+    i = v - voff[j] + 1;
+    L = voff[j + 1] - voff[j];
+}
+
+// Exclusive prefix of the valid lengths into S.voff (all threads of the block take part).
+__device__ void length_prefix(const VerifyArgs& a, VRSmem& S) {
+    const int tid = threadIdx.x, nth = blockDim.x;
+    const int per = (a.B + nth - 1) / nth;  // consecutive requests per thread
+    const int j0 = tid * per;
+    int sum = 0;
+    for (int j = j0; j < min(a.B, j0 + per); ++j) sum += valid_len(a, j);
+    // block-wide exclusive scan of the per-thread sums (warp scans, then the warp totals)
+    const int lane = tid & 31, warp = tid >> 5, nw = nth >> 5;
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    __shared__ int wsum[32];
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < nw ? wsum[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += t;
+        }
+        wsum[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    int run = incl - sum + (warp > 0 ? wsum[warp - 1] : 0);
+    for (int j = j0; j < min(a.B, j0 + per); ++j) {
+        S.voff[j] = run;
+        run += valid_len(a, j);
+    }
+    if (tid == nth - 1) {
+        S.voff[a.B] = run;
+        S.nver = run;
+    }
+    __syncthreads();
 }
 
 __global__ void __launch_bounds__(kVThreads, 1) verify_rows_ws_kernel(VerifyArgs a) {
@@ -357,8 +413,9 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_rows_ws_kernel(VerifyArgs
     VRSmem& S = *reinterpret_cast<VRSmem*>(smem_raw);
     volatile int* abort = &S.abort;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nrow_all = a.B * a.gamma;
     const int nch = (a.V + kVCE - 1) / kVCE;
+    length_prefix(a, S);
+    const int nver = S.nver;
     if (tid == 0) {
         for (int k = 0; k < kVNS; ++k) {
             mbar_init(&S.full[k], 1);
@@ -384,9 +441,9 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_rows_ws_kernel(VerifyArgs
         // ---------------- producer warp
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
-            for (int r = blockIdx.x; r < nrow_all; r += gridDim.x) {
+            for (int v = blockIdx.x; v < nver; v += gridDim.x) {
                 int j, i, L;
-                if (!verified_row(a, r, j, i, L)) continue;
+                verified_row(a, S.voff, v, j, i, L);
                 const __nv_bfloat16* row = tgt + trow_off(a, j, i);
                 for (int k = 0; k < nch; ++k, ++q) {
                     const int slot = q % kVNS;
@@ -410,9 +467,9 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_rows_ws_kernel(VerifyArgs
         const int tail = a.V - (nch - 1) * kVCE;  // ids in the last chunk of a row
         int par = 0, slot = 0;
         uint32_t phase = 0;
-        for (int r = blockIdx.x; r < nrow_all; r += gridDim.x) {
+        for (int v = blockIdx.x; v < nver; v += gridDim.x) {
             int j, i, L;
-            if (!verified_row(a, r, j, i, L)) continue;
+            verified_row(a, S.voff, v, j, i, L);
             float m = -CUDART_INF_F, sacc = 0.f;
             int idx = 0x7fffffff;
             auto chunk = [&](int k, bool last) {
@@ -516,7 +573,10 @@ __device__ int block_sample_row(const VerifyArgs& a, const TL* row, int j, int p
     float2* red = reinterpret_cast<float2*>(sh);  // sh[0..15]
     float* cmass = sh + 16;                       // sh[16..47]
     float* misc = sh + 48;                        // sh[48..63]
-    constexpr int per = kTS / kThreads;           // 4 ids per thread, in id order
+    constexpr int per = kTS / kThreads;           // ids per thread, in id order
+    constexpr int tpc = kCS / per;                // threads per 32-id chunk
+    static_assert(kCS % per == 0 && tpc <= 32 && (tpc & (tpc - 1)) == 0, "a chunk's threads share a warp");
+    static_assert(kTS / kCS <= 32, "chunk masses of a tile fit sh[16..47]");
     float best_key = -CUDART_INF_F, best_m = 0.f;
     int best_t = 0;
     for (int t = 0; t < a.nt; ++t) {
@@ -550,17 +610,16 @@ __device__ int block_sample_row(const VerifyArgs& a, const TL* row, int j, int p
     __syncthreads();
     const int t = __float_as_int(misc[0]);
     const float mt = misc[1];
-    // chunk masses of tile t (8 threads per 32-id chunk)
+    // chunk masses of tile t (tpc consecutive threads per 32-id chunk)
     float tot = 0.f;
 #pragma unroll
     for (int e = 0; e < per; ++e) {
         const int v = t * kTS + per * tid + e;
         tot += v < a.V ? ex2(load_logit<TL>(row, (size_t)v) * a.scale2 - mt) : 0.f;
     }
-    tot += __shfl_xor_sync(0xffffffffu, tot, 1);
-    tot += __shfl_xor_sync(0xffffffffu, tot, 2);
-    tot += __shfl_xor_sync(0xffffffffu, tot, 4);
-    if ((tid & 7) == 0) cmass[tid >> 3] = tot;
+#pragma unroll
+    for (int o = 1; o < tpc; o <<= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    if ((tid & (tpc - 1)) == 0) cmass[tid / tpc] = tot;
     __syncthreads();
     const uint4 w = philox10(make_uint4(0u, (uint32_t)pos, (uint32_t)j, DSPARK_P_RESID_INTILE), (uint32_t)a.seed,
                              (uint32_t)(a.seed >> 32));
@@ -807,7 +866,7 @@ extern "C" dspark_status dspark_verify(const dspark_sample_params* p, const void
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(workspace, 0, L.zero_bytes, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     void* args[] = {&a};
-    const bool ws_rows = p->logits_dtype == DSPARK_BF16 && a.vec_t;
+    const bool ws_rows = p->logits_dtype == DSPARK_BF16 && a.vec_t && p->B <= kVMaxB;
     if (ws_rows) {  // persistent streaming kernel: rows have one segment
         int per_sm = 0, sms = 0;
         if (prepare_kernel((const void*)verify_rows_ws_kernel, sizeof(VRSmem), kVThreads, &per_sm) != cudaSuccess ||

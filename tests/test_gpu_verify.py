@@ -173,3 +173,29 @@ def test_end_to_end_b512_scheduled_lengths_sampled():
             assert rm < MARGIN, f"request {j}: ({n[j]}, {corr[j]}) vs ({rn}, {rc}) margin {rm}"
             tally.excluded += 1
     tally.check_fraction()
+
+
+def test_residual_without_mass_falls_back_to_p():
+    # Position 1's target row is the draft's own z = base + W2 W1[anchor], and the draft LSE passed
+    # in is 30 nats below the true one: q(x) then exceeds p(x) by a factor e^30 at every id, so the
+    # accept test rejects at position 1 and max(0, p - q) has no mass anywhere; the correction is
+    # drawn from p instead (the oracle's fallback flag), with the status word left OK.
+    wl = W.make_sample_workload("fb", 6, 2, 3000, 16, 1.0, device="cuda", data_seed=17, philox_seed=9,
+                                logits_dtype=torch.float32, w_std=0.3)
+    t = wl.tensors
+    base, W1, W2, anchor, _ = host(wl)
+    tok, lse, zat = oracle_drafts(wl)
+    def f64(x):  # bf16 bit patterns (uint16) or float32 -> float64
+        return ((x.astype(np.uint32) << 16).view(np.float32) if x.dtype == np.uint16 else x).astype(np.float64)
+
+    z1 = f64(base[:, 0]) + f64(W1)[anchor] @ f64(W2).T
+    target = np.array(W.np_view(t["target"]), copy=True)
+    target[:, 0] = z1.astype(np.float32)
+    t["target"].copy_(torch.from_numpy(target).to("cuda"))
+    lse_low = (lse - 30.0).astype(np.float32)
+    n, corr = verify_both(wl, tok, lse_low, zat)
+    assert (n == 0).all()
+    for j in range(wl.B):
+        _, rc, _, fb = O.verify_request(base, W1, W2, int(anchor[j]), j, tok[j], lse_low[j], zat[j], target, wl.gamma,
+                                        wl.T, wl.seed, TS)
+        assert fb == 1, j
