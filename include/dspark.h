@@ -215,7 +215,12 @@ dspark_status dspark_schedule_verify_len(int B, int gamma, const float* conf, in
  * Arguments (device memory): accept_rate, eval_mask [S, A, gamma] float (dspark_accept_rate_tv's
  * outputs); decay_gamma > 0 (the pages use 4).
  * Outputs (device memory): l1 [S, A, gamma] float or NULL; sums [2] double.
+ * Host errors: DSPARK_ERR_INVALID_ARG (sizes < 1, NULL accept_rate / eval_mask / sums,
+ * decay_gamma <= 0), DSPARK_ERR_UNSUPPORTED when gamma > 1024.
  * The sums are added in a fixed order: the same inputs give the same bits.
+ * Precision: l1 is formed from the fp32 accept rate, so its absolute error is twice the accept
+ * rate's (at most 2 (1e-5 accept + 2^-24) against an exact sum |p - q|); as the accept rate tends
+ * to 1 that error is a growing fraction of the small l1 itself.
  */
 dspark_status dspark_tv_l1_loss(int S, int A, int gamma, const float* accept_rate, const float* eval_mask,
                                 float decay_gamma, float* l1, double* sums, dspark_stream_t stream);
@@ -271,7 +276,10 @@ dspark_status dspark_theta_schedule(int B, int gamma, const float* conf, const f
  * every GPU that loads the library until the process exits).  The caller still passes every
  * input and output, exactly as for dspark_markov_sample_block.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
- *     with that device current; make that first call before any stream capture.
+ *     with that device current; make that first call before any stream capture.  The address
+ *     is kept for the life of the process: after cudaDeviceReset (or anything else that unloads
+ *     the library's module from the device) it is stale, so reload the library before calling
+ *     this entry point again.
  *   - A call whose scratch would exceed the array (dspark_sample_workspace_size(p) >
  *     DSPARK_NOALLOC_SCRATCH_BYTES) returns DSPARK_ERR_UNSUPPORTED and enqueues nothing.
  *   - All calls share the one array and it keeps the last call's contents; each call clears

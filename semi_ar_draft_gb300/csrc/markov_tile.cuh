@@ -508,100 +508,11 @@ __device__ __forceinline__ void produce_sample(const TL* base, const uint16_t* W
 // Staged draft sampling (bf16 logits, tensor-core path).  The base logits of a row block over
 // the block's tile are copied into shared memory by the bulk-copy engine one row block ahead;
 // rows are padded to kStageRow ids so the 16-byte reads of a quarter-warp (rows g, g+1, four
-// 8-id groups each) fall on distinct bank groups.  The producer keeps only chunk statistics;
-// the finalize recomputes the one chosen chunk with the same MMA sequence (bit-identical z).
+// 8-id groups each) fall on distinct bank groups.  The producer forms every chunk's record of
+// the chunk-Gumbel contract in the registers that hold its z (produce_cg below); z is never
+// stored.
 // --------------------------------------------------------------------------------------------
 constexpr int kStageRow = kTS + 32;  // ids per staged row (2112 bytes)
-
-template <int KS, bool W2SMEM>
-__device__ __forceinline__ void mma_chunk(float (&xa)[8], float (&xb)[8], const Frag<KS>& fa, const Frag<KS>& fb,
-                                          const uint16_t* W2, const uint4* w2s, int tile0, int c, int V, int g, int tq,
-                                          bool full) {
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-        const int vl = kCS * c + 8 * (g >> 1) + 2 * nt + (g & 1);  // id (in tile) this lane feeds as column g
-        Frag<KS> fw;
-        if (full || tile0 + vl < V) {
-            if constexpr (W2SMEM) load_frag_smem<KS>(w2s, vl, tq, fw);
-            else load_frag_global<KS>(W2, tile0 + vl, tq, fw);
-        } else {
-            frag_zero<KS>(fw);
-        }
-#pragma unroll
-        for (int s = 0; s < KS; ++s)
-            mma4(xa[2 * nt], xa[2 * nt + 1], xb[2 * nt], xb[2 * nt + 1], fa.w[2 * s], fb.w[2 * s], fa.w[2 * s + 1],
-                 fb.w[2 * s + 1], fw.w[2 * s], fw.w[2 * s + 1]);
-    }
-}
-
-// 8 staged bf16 ids (16-byte aligned) to fp32; ids >= V read as -inf when the tile is partial.
-__device__ __forceinline__ void load_staged8(const uint16_t* srow, int id_in_tile, int tile0, int V, bool full,
-                                             float (&x)[8]) {
-    const uint4 w = *reinterpret_cast<const uint4*>(srow + id_in_tile);
-    x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
-    x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z); x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
-    if (!full) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            if (tile0 + id_in_tile + e >= V) x[e] = -CUDART_INF_F;
-    }
-}
-
-// A-operand fragment of one W1 row held in shared memory (same K permutation as above).
-template <int KS>
-__device__ __forceinline__ void load_frag_row(const uint16_t* row, int tq, Frag<KS>& f) {
-    constexpr int r = 16 * KS;
-    const uint16_t* p = row + tq * (r / 4);
-    if constexpr (KS == 1) {
-        const uint2 u = *reinterpret_cast<const uint2*>(p);
-        f.w[0] = u.x;
-        f.w[1] = u.y;
-    } else {
-#pragma unroll
-        for (int q = 0; q < KS / 2; ++q) {
-            const uint4 u = reinterpret_cast<const uint4*>(p)[q];
-            f.w[4 * q + 0] = u.x;
-            f.w[4 * q + 1] = u.y;
-            f.w[4 * q + 2] = u.z;
-            f.w[4 * q + 3] = u.w;
-        }
-    }
-}
-
-// As mma_chunk, with the A fragments (W1 rows g and g + 8) read from shared memory as they are
-// used instead of being held in registers for the whole row block.
-template <int KS, bool W2SMEM>
-__device__ __forceinline__ void mma_chunk_rows(float (&xa)[8], float (&xb)[8], const uint16_t* w1a, const uint16_t* w1b,
-                                               const uint16_t* W2, const uint4* w2s, int tile0, int c, int V, int g,
-                                               int tq, bool full) {
-    constexpr int r = 16 * KS;
-    if constexpr (KS == 1) {
-        Frag<1> fa, fb;
-        load_frag_row<1>(w1a, tq, fa);
-        load_frag_row<1>(w1b, tq, fb);
-        mma_chunk<1, W2SMEM>(xa, xb, fa, fb, W2, w2s, tile0, c, V, g, tq, full);
-    } else {
-        constexpr int units = w2_units<KS>();
-        constexpr int mask = w2_mask<KS>();
-#pragma unroll
-        for (int q = 0; q < KS / 2; ++q) {  // two k-steps per 16-byte unit of the lane's weights
-            const uint4 a = reinterpret_cast<const uint4*>(w1a + tq * (r / 4))[q];
-            const uint4 b = reinterpret_cast<const uint4*>(w1b + tq * (r / 4))[q];
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                const int vl = kCS * c + 8 * (g >> 1) + 2 * nt + (g & 1);
-                uint4 w = make_uint4(0u, 0u, 0u, 0u);
-                if (full || tile0 + vl < V) {
-                    const int u = tq * (KS / 2) + q;
-                    if constexpr (W2SMEM) w = w2s[(size_t)vl * units + (u ^ (vl & mask))];
-                    else w = __ldg(reinterpret_cast<const uint4*>(W2 + (size_t)(tile0 + vl) * r + tq * (r / 4)) + q);
-                }
-                mma4(xa[2 * nt], xa[2 * nt + 1], xb[2 * nt], xb[2 * nt + 1], a.x, b.x, a.y, b.y, w.x, w.y);
-                mma4(xa[2 * nt], xa[2 * nt + 1], xb[2 * nt], xb[2 * nt + 1], a.z, b.z, a.w, b.w, w.z, w.w);
-            }
-        }
-    }
-}
 
 // Row-block W1 fragments in shared memory, interleaved so that one 16-byte load is a whole A
 // fragment: unit (s, g, tq) [s = k-step, g = 0..7, tq = 0..3] holds the four 32-bit words
@@ -645,67 +556,6 @@ __device__ __forceinline__ void mma_chunk_frag(float (&acc)[4][4], const uint4* 
             }
             mma4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3], ua.x, ua.y, ua.z, ua.w, w.x, w.y);
             if (s + 1 < KS) mma4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3], ub.x, ub.y, ub.z, ub.w, w.z, w.w);
-        }
-    }
-}
-
-// T > 0 chunk statistics straight from z: the maximum of the log2-weights z * scale2 is the
-// scaled maximum of z (scale2 > 0), the sum uses one fused multiply-add per id.
-__device__ __forceinline__ float2 chunk_stats_scaled(const float (&z)[8], float scale2) {
-    float m = z[0];
-#pragma unroll
-    for (int e = 1; e < 8; ++e) m = fmaxf(m, z[e]);
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-    m *= scale2;
-    const float mref = (m == -CUDART_INF_F) ? 0.f : m;  // an empty quad sums to 0
-    float sum = 0.f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) sum += ex2(fmaf(z[e], scale2, -mref));
-    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-    return make_float2(m, sum);
-}
-
-// w1rows: the row block's 16 W1 rows (of the previous tokens) in shared memory, w1stride apart.
-template <int KS, bool GREEDY, bool W2SMEM, bool FULL>
-__device__ __forceinline__ void produce_staged(const uint16_t* stage, const uint16_t* w1rows, int w1stride,
-                                               const uint16_t* W2, const uint4* w2s, int V, int tile, float2* cstat,
-                                               float scale2) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, tq = lane & 3;
-    const int tile0 = tile * kTS;
-    Frag<KS> fa, fb;
-    load_frag_row<KS>(w1rows + g * w1stride, tq, fa);
-    load_frag_row<KS>(w1rows + (g + 8) * w1stride, tq, fb);
-    const uint16_t* srowA = stage + g * kStageRow;
-    const uint16_t* srowB = stage + (g + 8) * kStageRow;
-#pragma unroll
-    for (int k = 0; k < kChunksPerWarp; ++k) {
-        const int c = warp + kWarps * k;
-        const int cb = tile0 + kCS * c;
-        if (!FULL && cb >= V) {
-            if (tq == 0) {
-                cstat[g * kChunks + c] = empty_stats(GREEDY);
-                cstat[(g + 8) * kChunks + c] = empty_stats(GREEDY);
-            }
-            continue;
-        }
-        float xa[8], xb[8];
-        load_staged8(srowA, kCS * c + 8 * tq, tile0, V, FULL, xa);
-        load_staged8(srowB, kCS * c + 8 * tq, tile0, V, FULL, xb);
-        mma_chunk<KS, W2SMEM>(xa, xb, fa, fb, W2, w2s, tile0, c, V, g, tq, FULL);
-        float2 sa, sb;
-        if constexpr (GREEDY) {
-            sa = chunk_stats(xa, cb + 8 * tq, 1);
-            sb = chunk_stats(xb, cb + 8 * tq, 1);
-        } else {
-            sa = chunk_stats_scaled(xa, scale2);
-            sb = chunk_stats_scaled(xb, scale2);
-        }
-        if (tq == 0) {
-            cstat[g * kChunks + c] = sa;
-            cstat[(g + 8) * kChunks + c] = sb;
         }
     }
 }
@@ -898,102 +748,6 @@ __device__ __forceinline__ float4 reduce_row_chunks(const float4* crow, bool gre
     return make_float4(key, lm, w.z, w.w);
 }
 
-// Tile record of one staged row (one warp).  Greedy: from the chunk statistics alone.  T > 0:
-// the chunk by u1 over the chunk masses, then that chunk's z recomputed with the producer's MMA
-// sequence (every lane quad holds the same 32 values: lane tq has ids 8 tq .. 8 tq + 7) and the
-// id by u2 inside it.
-template <int KS, bool GREEDY, bool W2SMEM>
-__device__ __forceinline__ float4 finalize_staged(const uint16_t* srow, float2 cs, int tile, int V, float scale2,
-                                                  float u1, float u2, float lnE, const uint16_t* w1row,
-                                                  const uint16_t* W2, const uint4* w2s) {
-    const int lane = threadIdx.x & 31;
-    const int g = lane >> 2, tq = lane & 3;
-    const int tile0 = tile * kTS;
-    const bool valid = tile0 + kCS * lane < V;
-    if constexpr (GREEDY) {
-        float m = valid ? cs.x : -CUDART_INF_F;
-        int idx = valid ? __float_as_int(cs.y) : 0x7fffffff;
-        warp_argmax(m, idx);
-        return make_float4(m, CUDART_NAN_F, __int_as_float(idx), m);
-    }
-    const float mc = valid ? cs.x : -CUDART_INF_F;
-    const float sc = valid ? cs.y : 0.f;
-    const float mt = warp_max(mc);
-    if (mt == -CUDART_INF_F) return make_float4(-CUDART_INF_F, -CUDART_INF_F, __int_as_float(-1), 0.f);
-    const float w = (sc > 0.f) ? sc * ex2(mc - mt) : 0.f;
-    const float P = warp_incl_scan(w);
-    const float St = __shfl_sync(0xffffffffu, P, 31);
-    if (!(St > 0.f)) return make_float4(-CUDART_INF_F, -CUDART_INF_F, __int_as_float(-1), 0.f);
-    const float lmass = (mt + lg2(St)) * kLn2;
-    const unsigned hit = __ballot_sync(0xffffffffu, P > u1 * St);
-    int cstar;
-    if (hit) {
-        cstar = __ffs(hit) - 1;
-    } else {
-        const unsigned nz = __ballot_sync(0xffffffffu, w > 0.f);
-        cstar = nz ? 31 - __clz(nz) : 0;
-    }
-    const float mcs = __shfl_sync(0xffffffffu, mc, cstar);  // the producer's chunk maximum (log2 units)
-    // recompute z of chunk cstar: both MMA row halves carry this row
-    Frag<KS> fa;
-    load_frag_row<KS>(w1row, tq, fa);
-    const bool full = tile0 + kTS <= V;
-    float xa[8], xb[8];
-    load_staged8(srow, kCS * cstar + 8 * tq, tile0, V, full, xa);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) xb[e] = xa[e];
-    mma_chunk<KS, W2SMEM>(xa, xb, fa, fa, W2, w2s, tile0, cstar, V, g, tq, full);
-    // id by u2 inside the chunk: masses 2^(z*scale2 - m_c), in id order across the lane quad
-    float cum[8];
-    float run = 0.f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        run += ex2(fmaf(xa[e], scale2, -mcs));
-        cum[e] = run;
-    }
-    float incl = run;
-    float t = __shfl_up_sync(0xffffffffu, incl, 1, 4);
-    if (tq >= 1) incl += t;
-    t = __shfl_up_sync(0xffffffffu, incl, 2, 4);
-    if (tq >= 2) incl += t;
-    const float before = incl - run;
-    const float Sc = __shfl_sync(0xffffffffu, incl, 3, 4);
-    const float target = u2 * Sc;
-    const int id0 = tile0 + kCS * cstar + 8 * tq;
-    int first = 0x7fffffff, lastnz = -1;
-    float vfirst = 0.f, vlast = 0.f;
-#pragma unroll
-    for (int e = 7; e >= 0; --e) {
-        if (before + cum[e] > target) {
-            first = id0 + e;
-            vfirst = xa[e];
-        }
-        const float we = (e == 0) ? cum[0] : cum[e] - cum[e - 1];
-        if (lastnz < 0 && we > 0.f) {
-            lastnz = id0 + e;
-            vlast = xa[e];
-        }
-    }
-#pragma unroll
-    for (int o = 1; o <= 2; o <<= 1) {
-        const int of = __shfl_xor_sync(0xffffffffu, first, o);
-        const float ovf = __shfl_xor_sync(0xffffffffu, vfirst, o);
-        if (of < first) {
-            first = of;
-            vfirst = ovf;
-        }
-        const int ol = __shfl_xor_sync(0xffffffffu, lastnz, o);
-        const float ovl = __shfl_xor_sync(0xffffffffu, vlast, o);
-        if (ol > lastnz) {
-            lastnz = ol;
-            vlast = ovl;
-        }
-    }
-    const bool ok = first != 0x7fffffff;
-    (void)g;
-    return make_float4(lmass - lnE, lmass, __int_as_float(ok ? first : lastnz), ok ? vfirst : vlast);
-}
-
 // --------------------------------------------------------------------------------------------
 // Tile record of one row under the chunk-Gumbel contract (one warp, lane = chunk) from its 32
 // chunk statistics and its buffered z values xrow (weights 2^(x * lscale)):
@@ -1112,23 +866,6 @@ struct TileAcc {
 };
 __device__ __forceinline__ TileAcc tile_acc_init() {
     return TileAcc{-CUDART_INF_F, 0.f, -CUDART_INF_F, 0.f, 0x7fffffff, -1};
-}
-__device__ __forceinline__ void tile_acc_add(TileAcc& a, const float4 q, int t, bool want_lse) {
-    if (a.tile == 0x7fffffff || q.x > a.key || (q.x == a.key && t < a.tile)) {
-        a.key = q.x;
-        a.tile = t;
-        a.cand = __float_as_int(q.z);
-        a.val = q.w;
-    }
-    if (want_lse && q.y != -CUDART_INF_F) {
-        const float l2 = q.y * kLog2e;
-        if (l2 > a.m) {
-            a.s = (a.m == -CUDART_INF_F) ? 1.f : a.s * ex2(a.m - l2) + 1.f;
-            a.m = l2;
-        } else {
-            a.s += ex2(l2 - a.m);
-        }
-    }
 }
 // Merge over `width` consecutive lanes (a power of two <= 32); every lane of the warp calls it.
 __device__ __forceinline__ void tile_acc_shfl_merge(TileAcc& a, int width, bool want_lse) {

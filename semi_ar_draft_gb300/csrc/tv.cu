@@ -417,17 +417,21 @@ __global__ void tau_kernel(long long nblk, int gamma, const float* acc, const fl
 // numerator sum w mask l1 and denominator sum w mask.  One block; every thread adds its elements in
 // index order in fp64 and the block adds the threads in a fixed tree, so the sums are deterministic.
 constexpr int kL1Threads = 512;
+constexpr int kL1MaxGamma = 1024;  // positions per block (the sampling calls accept gamma <= 1024 too)
 __global__ void __launch_bounds__(kL1Threads) tv_l1_kernel(long long n, int gamma, const float* __restrict__ acc,
                                                            const float* __restrict__ mask, double decay,
                                                            float* __restrict__ l1, double* __restrict__ sums) {
     __shared__ double red[2][kL1Threads / 32];
+    __shared__ double wtab[kL1MaxGamma];  // w_k = exp(-(k - 1) / decay), one per position
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int k = tid; k < gamma; k += kL1Threads) wtab[k] = exp(-(double)k / decay);
+    __syncthreads();
     double num = 0.0, den = 0.0;
     for (long long e = tid; e < n; e += kL1Threads) {
         const int k = (int)(e % gamma);  // position k + 1
         const float d = 2.f * (1.f - acc[e]);
         if (l1) l1[e] = d;
-        const double w = exp(-(double)k / decay) * (double)mask[e];
+        const double w = wtab[k] * (double)mask[e];
         num += w * (double)d;
         den += w;
     }
@@ -554,6 +558,7 @@ extern "C" dspark_status dspark_tv_l1_loss(int S, int A, int gamma, const float*
                                            float decay_gamma, float* l1, double* sums, dspark_stream_t stream) {
     if (S < 1 || A < 1 || gamma < 1 || !accept_rate || !eval_mask || !sums) return DSPARK_ERR_INVALID_ARG;
     if (!(decay_gamma > 0.f)) return DSPARK_ERR_INVALID_ARG;
+    if (gamma > kL1MaxGamma) return DSPARK_ERR_UNSUPPORTED;
     const long long n = (long long)S * A * gamma;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     tv_l1_kernel<<<1, kL1Threads, 0, s>>>(n, gamma, accept_rate, eval_mask, (double)decay_gamma, l1, sums);

@@ -80,15 +80,31 @@ def test_repeated_calls_are_bit_identical():
     assert torch.equal(a1, a2)
 
 
-def test_l1_loss_epilogue():
-    tv = W.make_tv_workload(2, 64, 8, 20000, device="cuda", data_seed=3, truncate=True, drop=0.2)
+@pytest.mark.parametrize("rho", [0.8, 0.99999])
+def test_l1_loss_epilogue(rho):
+    # The oracle's side is built from its own accept rates on the raw logits (tv_row) and its own
+    # eval mask, never from the CUDA path's outputs.  rho = 0.99999: nearly identical rows, accept
+    # rates close to 1, where l1 = 2 (1 - accept) is a small difference of fp32 values.
+    tv = W.make_tv_workload(2, 64, 8, 20000, device="cuda", data_seed=3, truncate=True, drop=0.2, rho=rho)
     t = tv.tensors
+    S, A, g = tv.S, tv.A, tv.gamma
     acc, mask, _, _ = api.accept_rate_tv(t["d"], t["t"], t["keep"], t["pos_valid"])
     l1, sums = api.tv_l1_loss(acc, mask, 4.0)
     torch.cuda.synchronize()
-    r_l1, r_num, r_den = O.tv_l1_loss(acc.cpu().numpy(), mask.cpu().numpy(), 4.0)
-    assert np.abs(l1.cpu().numpy() - r_l1).max() < 1e-6  # 2 (1 - acc) in fp32
-    # each l1 is rounded to fp32 (2^-24 relative) before the fp64 sums: 1e-6 relative covers it
-    close(sums.cpu().numpy(), [r_num, r_den], rtol=1e-6, atol=1e-9, what="weighted L1 sums")
+    keep, pv = t["keep"].cpu().numpy(), t["pos_valid"].cpu().numpy()
+    d_all, t_all = W.np_view(t["d"]), W.np_view(t["t"])
+    r_acc = np.array([[[O.tv_row(d_all[s_, a, i], t_all[s_, a, i])[0] for i in range(g)] for a in range(A)]
+                      for s_ in range(S)])
+    r_mask = np.array([[O.eval_mask_tau(r_acc[s_, a], int(keep[s_, a]), pv[s_, a])[0] for a in range(A)]
+                       for s_ in range(S)])
+    r_l1, r_num, r_den = O.tv_l1_loss(r_acc, r_mask, 4.0)
+    # bound from the arithmetic: l1 = 2 (1 - accept) carries twice the accept rate's absolute error,
+    # which the TV parity bound holds to 1e-5 accept + 2^-24 (the fp32 spacing near 1)
+    bound = 2 * (1e-5 * r_acc + 2.0 ** -24)
+    assert (np.abs(l1.cpu().numpy() - r_l1) <= bound).all()
+    assert np.array_equal(mask.cpu().numpy(), r_mask.astype(np.float32))
+    w = np.exp(-np.arange(g) / 4.0)
+    close(sums.cpu().numpy()[1:], [r_den], rtol=1e-12, atol=1e-12, what="weighted mask sum")
+    assert abs(float(sums[0]) - r_num) <= float(np.sum(w * r_mask * bound)) + 1e-9
     l1b, sums_b = api.tv_l1_loss(acc, mask, 4.0)
     assert torch.equal(sums, sums_b) and torch.equal(l1, l1b)

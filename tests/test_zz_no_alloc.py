@@ -37,7 +37,7 @@ def test_noalloc_matches_workspace_entry_point_twice(T):
             close(lse.cpu().numpy(), ref_lse, what="draft_lse")
         else:
             assert np.isnan(lse.cpu().numpy()).all()
-        close(zat.cpu().numpy(), ref_zat, atol=1e-5, what="z_at_tok")
+        close(zat.cpu().numpy(), ref_zat, what="z_at_tok")
 
 
 def test_noalloc_rejects_oversized_scratch():
