@@ -101,13 +101,18 @@ typedef struct {
     uint64_t seed;     /* Philox key */
     int logits_dtype;  /* dtype of base (and target) logits: DSPARK_F32 or DSPARK_BF16 */
     int w_dtype;       /* dtype of W1 and W2 */
+    float softcap;     /* final-logit softcap s of the draft model (P1 section 3.12, compute_logits:
+                          s tanh(logits / s)): every base logit b is replaced by s tanh(b / s) before
+                          the Markov bias is added (+-inf -> +-s); 0 = none.  Target logits are taken
+                          as given (the target model applies its own cap). */
 } dspark_sample_params;
 
 /*
  * Markov-head block sampling (P2 section 3.4, VanillaMarkov and sample_block_tokens;
  * P1 section 3.7; P4 section 3.3):
  *   prev_1 = anchor[j];  for i = 1..gamma:
- *     z_{j,i} = base[j, i-1, :] + W2 . W1[prev_i]      (bias_v = sum_k W1[prev_i, k] W2[v, k])
+ *     z_{j,i} = cap(base[j, i-1, :]) + W2 . W1[prev_i]  (bias_v = sum_k W1[prev_i, k] W2[v, k];
+ *                                                        cap = the softcap of p, or the identity)
  *     x_{j,i} ~ draft sampling contract on z_{j,i} / T;  prev_{i+1} = x_{j,i}
  * Arguments
  *   base_logits [B, gamma, V] (logits_dtype); W1 [V, r], W2 [V, r] (w_dtype; W2 is the

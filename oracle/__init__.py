@@ -52,7 +52,7 @@ def lib():
         L.oracle_philox_word.restype = u32
         L.oracle_uniform.argtypes = [u64, u32, u32, u32, u32]
         L.oracle_uniform.restype = dbl
-        L.oracle_markov_logits.argtypes = [i32, i32, i32, i32, vp, vp, vp, i32, vp]
+        L.oracle_markov_logits.argtypes = [i32, i32, i32, i32, vp, vp, vp, i32, dbl, vp]
         L.oracle_argmax.argtypes = [vp, i32, vp]
         L.oracle_argmax.restype = i32
         L.oracle_tile_gumbel.argtypes = [vp, i32, i32, i32, u64, i32, i32, i32, i32, vp, vp]
@@ -62,9 +62,9 @@ def lib():
         L.oracle_gumbel_elem.argtypes = [vp, i32, u64, i32, i32, vp]
         L.oracle_gumbel_elem.restype = i32
         L.oracle_sample_request.argtypes = [i32, i32, i32, i32, i32, dbl, u64, i32, i32, vp, vp, vp, i32, i32,
-                                            vp, vp, vp, vp]
+                                            vp, vp, vp, vp, dbl]
         L.oracle_verify_request.argtypes = [i32, i32, i32, i32, i32, i32, dbl, u64, i32, i32, i32, vp, vp, vp,
-                                            i32, i32, vp, vp, vp, vp, i32, vp, vp, vp]
+                                            i32, i32, vp, vp, vp, vp, i32, vp, vp, vp, dbl]
         L.oracle_verify_request.restype = i32
         L.oracle_tv_row.argtypes = [i32, i32, vp, vp, vp]
         L.oracle_tv_row.restype = dbl
@@ -119,18 +119,21 @@ def uniform(seed: int, j: int, i: int, purpose: int, n: int) -> float:
 
 
 # ----------------------------------------------------------------- sampler
-def markov_logits(base_row: np.ndarray, W1: np.ndarray | None, W2: np.ndarray | None, prev: int) -> np.ndarray:
+def markov_logits(base_row: np.ndarray, W1: np.ndarray | None, W2: np.ndarray | None, prev: int,
+                  softcap: float = 0.0) -> np.ndarray:
+    """z = cap(base) + W2 W1[prev] in fp64; cap(b) = s tanh(b / s) with s = softcap > 0, else b."""
     V = base_row.shape[-1]
     r = 0 if W1 is None else W1.shape[1]
     z = np.zeros(V, dtype=np.float64)
     w_dt = _dtype_code(W1) if r else F32
     w1 = _p(W1) if r else None
     w2 = _p(W2) if r else None
-    lib().oracle_markov_logits(V, r, _dtype_code(base_row), w_dt, _p(base_row), w1, w2, int(prev), _p(z))
+    lib().oracle_markov_logits(V, r, _dtype_code(base_row), w_dt, _p(base_row), w1, w2, int(prev), float(softcap),
+                               _p(z))
     return z
 
 
-def block_logits(base: np.ndarray, W1, W2, anchor, tokens) -> np.ndarray:
+def block_logits(base: np.ndarray, W1, W2, anchor, tokens, softcap: float = 0.0) -> np.ndarray:
     """Teacher-forced z[j, i] = markov_logits(base[j, i], W1, W2, prev_{j,i}) with prev_{j,0} = anchor[j] and
     prev_{j,i} = tokens[j, i - 1] (P1 section on build_markov_head, apply_block_logits), in fp64."""
     B, gamma, V = base.shape
@@ -138,7 +141,7 @@ def block_logits(base: np.ndarray, W1, W2, anchor, tokens) -> np.ndarray:
     for j in range(B):
         for i in range(gamma):
             prev = int(anchor[j]) if i == 0 else int(tokens[j, i - 1])
-            z[j, i] = markov_logits(base[j, i], W1, W2, prev)
+            z[j, i] = markov_logits(base[j, i], W1, W2, prev, softcap)
     return z
 
 
@@ -175,7 +178,7 @@ def gumbel_elem(lw: np.ndarray, seed: int, j: int, i: int):
 
 
 def sample_request(base: np.ndarray, W1, W2, anchor: int, j: int, T: float, seed: int, TS: int, row=None,
-                   CS: int = CHUNK):
+                   CS: int = CHUNK, softcap: float = 0.0):
     """One request of dspark_markov_sample_block.  base: [B, gamma, V]; j is the
     request index (random stream); `row` selects the data block (default j)."""
     B, gamma, V = base.shape
@@ -186,7 +189,7 @@ def sample_request(base: np.ndarray, W1, W2, anchor: int, j: int, T: float, seed
     w_dt = _dtype_code(W1) if r else F32
     lib().oracle_sample_request(V, r, gamma, TS, CS, float(T), seed, _dtype_code(base), w_dt, _p(blk),
                                 _p(W1) if r else None, _p(W2) if r else None, int(anchor), int(j),
-                                _p(tok), _p(lse), _p(zx), _p(mg))
+                                _p(tok), _p(lse), _p(zx), _p(mg), float(softcap))
     return tok, lse, zx, mg
 
 
@@ -202,7 +205,7 @@ def sample_block(base, W1, W2, anchor, T, seed, TS, requests=None, CS: int = CHU
 
 # ----------------------------------------------------------------- verify
 def verify_request(base, W1, W2, anchor: int, j: int, tokens, draft_lse, z_at_tok, target, L: int,
-                   T: float, seed: int, TS: int, row=None, CS: int = CHUNK):
+                   T: float, seed: int, TS: int, row=None, CS: int = CHUNK, softcap: float = 0.0):
     """One request of dspark_verify.  base [B,gamma,V], target [B,gamma_t,V];
     tokens/draft_lse/z_at_tok: this request's gamma entries (int32 / float32);
     j is the request index (random stream); `row` selects the data (default j)."""
@@ -222,7 +225,7 @@ def verify_request(base, W1, W2, anchor: int, j: int, tokens, draft_lse, z_at_to
     n = lib().oracle_verify_request(V, r, gamma, gamma_t, TS, CS, float(T), seed, _dtype_code(base), w_dt,
                                     _dtype_code(target), _p(bblk), _p(W1) if r else None,
                                     _p(W2) if r else None, int(anchor), int(j), _p(tok), _p(dl), _p(zx),
-                                    _p(tblk), int(L), _p(corr), _p(mm), _p(fb))
+                                    _p(tblk), int(L), _p(corr), _p(mm), _p(fb), float(softcap))
     return int(n), int(corr[0]), float(mm[0]), int(fb[0])
 
 

@@ -109,12 +109,16 @@ static double load_val(const void* p, int dtype, size_t idx) {
 /* bias.                                                                */
 /* ------------------------------------------------------------------ */
 void oracle_markov_logits(int V, int r, int logits_dtype, int w_dtype, const void* base_row,
-                          const void* W1, const void* W2, int prev, double* z_out) {
+                          const void* W1, const void* W2, int prev, double softcap, double* z_out) {
     for (int v = 0; v < V; ++v) {
         double bias = 0.0;
         for (int k = 0; k < r; ++k)
             bias += load_val(W1, w_dtype, (size_t)prev * r + k) * load_val(W2, w_dtype, (size_t)v * r + k);
-        z_out[v] = load_val(base_row, logits_dtype, (size_t)v) + bias;
+        double b = load_val(base_row, logits_dtype, (size_t)v);
+        /* final-logit softcap of the draft model's logits (P1 section 3.12): s tanh(b / s), before
+         * the Markov bias is added; softcap = 0: none */
+        if (softcap > 0.0) b = softcap * tanh(b / softcap);
+        z_out[v] = b + bias;
     }
 }
 
@@ -319,7 +323,7 @@ int oracle_gumbel_elem(const double* lw, int V, uint64_t seed, int j, int i, dou
 /* ------------------------------------------------------------------ */
 void oracle_sample_request(int V, int r, int gamma, int TS, int CS, double T, uint64_t seed, int logits_dtype,
                            int w_dtype, const void* base_req, const void* W1, const void* W2, int anchor, int j,
-                           int32_t* tokens, double* draft_lse, double* z_at_tok, double* margin) {
+                           int32_t* tokens, double* draft_lse, double* z_at_tok, double* margin, double softcap) {
     double* z = (double*)malloc(sizeof(double) * (size_t)V);
     double* s = (double*)malloc(sizeof(double) * (size_t)V);
     size_t esz = (logits_dtype == OR_F32) ? 4 : 2;
@@ -327,7 +331,7 @@ void oracle_sample_request(int V, int r, int gamma, int TS, int CS, double T, ui
     for (int step = 0; step < gamma; ++step) {
         int i = step + 1; /* 1-based block position */
         const char* row = (const char*)base_req + (size_t)step * (size_t)V * esz;
-        oracle_markov_logits(V, r, logits_dtype, w_dtype, row, W1, W2, prev, z);
+        oracle_markov_logits(V, r, logits_dtype, w_dtype, row, W1, W2, prev, softcap, z);
         int x;
         double mg, lse;
         if (T == 0.0) {
@@ -373,7 +377,7 @@ int oracle_verify_request(int V, int r, int gamma, int gamma_t, int TS, int CS, 
                           int logits_dtype, int w_dtype, int target_dtype, const void* base_req, const void* W1,
                           const void* W2, int anchor, int j, const int32_t* tokens, const float* draft_lse,
                           const float* z_at_tok, const void* target_req, int L, int32_t* correction,
-                          double* min_margin, int* resid_fallback) {
+                          double* min_margin, int* resid_fallback, double softcap) {
     size_t tsz = (target_dtype == OR_F32) ? 4 : 2;
     size_t bsz = (logits_dtype == OR_F32) ? 4 : 2;
     (void)gamma; /* the per-request blocks are already sliced */
@@ -413,7 +417,7 @@ int oracle_verify_request(int V, int r, int gamma, int gamma_t, int TS, int CS, 
                 int prev = (step == 0) ? anchor : tokens[step - 1];
                 const char* brow = (const char*)base_req + (size_t)step * (size_t)V * bsz;
                 double* z = (double*)malloc(sizeof(double) * (size_t)V);
-                oracle_markov_logits(V, r, logits_dtype, w_dtype, brow, W1, W2, prev, z);
+                oracle_markov_logits(V, r, logits_dtype, w_dtype, brow, W1, W2, prev, softcap, z);
                 double lse_t = logsumexp(lw, V); /* lw still holds t/T of this row */
                 int any = 0;
                 for (int v = 0; v < V; ++v) {
@@ -634,7 +638,7 @@ void oracle_trials_spec_one(int V, int TS, int CS, double T, const float* zd, co
         float lse_f = (float)lse_d, zx_f = zd[x];
         int32_t corr;
         int nacc = oracle_verify_request(V, 0, 1, 1, TS, CS, T, seed, OR_F32, OR_F32, OR_F32, zd, NULL, NULL, 0, (int)n,
-                                         &x, &lse_f, &zx_f, zt, 1, &corr, NULL, NULL);
+                                         &x, &lse_f, &zx_f, zt, 1, &corr, NULL, NULL, 0.0);
         if (nacc == 1) {
             emitted[x] += 1;
             *n_accept += 1;
@@ -660,14 +664,14 @@ void oracle_trials_spec_block(int V, int r, int gamma, int TS, int CS, double T,
     float* zx_f = (float*)malloc(sizeof(float) * (size_t)gamma);
     for (int k = 0; k <= gamma; ++k) hist[k] = 0;
     for (long n = 0; n < ntrials; ++n) {
-        oracle_sample_request(V, r, gamma, TS, CS, T, seed, OR_F32, OR_F32, base_req, W1, W2, anchor, (int)n, tok, lse, zx, mg);
+        oracle_sample_request(V, r, gamma, TS, CS, T, seed, OR_F32, OR_F32, base_req, W1, W2, anchor, (int)n, tok, lse, zx, mg, 0.0);
         for (int i = 0; i < gamma; ++i) {
             lse_f[i] = (float)lse[i];
             zx_f[i] = (float)zx[i];
         }
         int32_t corr;
         int nacc = oracle_verify_request(V, r, gamma, gamma, TS, CS, T, seed, OR_F32, OR_F32, OR_F32, base_req, W1, W2,
-                                         anchor, (int)n, tok, lse_f, zx_f, target_req, gamma, &corr, NULL, NULL);
+                                         anchor, (int)n, tok, lse_f, zx_f, target_req, gamma, &corr, NULL, NULL, 0.0);
         hist[nacc] += 1;
     }
     free(tok); free(lse); free(zx); free(mg); free(lse_f); free(zx_f);

@@ -11,15 +11,15 @@ def _wdt(W1):
     return b.F32 if W1 is None else b.dtype_code(W1.dtype)
 
 
-def make_params(base: torch.Tensor, W1, T: float, seed: int) -> b.SampleParams:
+def make_params(base: torch.Tensor, W1, T: float, seed: int, softcap: float = 0.0) -> b.SampleParams:
     B, gamma, V = base.shape
     r = 0 if W1 is None else W1.shape[1]
-    return b.params(B, gamma, V, r, T, seed, b.dtype_code(base.dtype), _wdt(W1))
+    return b.params(B, gamma, V, r, T, seed, b.dtype_code(base.dtype), _wdt(W1), softcap)
 
 
-def markov_sample_block(base, W1, W2, anchor, T, seed, ws=None, out=None, stream=None):
+def markov_sample_block(base, W1, W2, anchor, T, seed, ws=None, out=None, stream=None, softcap=0.0):
     """Returns (tokens [B,gamma] int32, draft_lse [B,gamma] f32, z_at_tok [B,gamma] f32, workspace)."""
-    p = make_params(base, W1, T, seed)
+    p = make_params(base, W1, T, seed, softcap)
     B, gamma, _ = base.shape
     dev = base.device
     if out is None:
@@ -32,9 +32,9 @@ def markov_sample_block(base, W1, W2, anchor, T, seed, ws=None, out=None, stream
 
 
 def verify(base, W1, W2, anchor, tokens, draft_lse, z_at_tok, target, T, seed, verify_len=None,
-           target_row_offsets=None, ws=None, out=None, stream=None):
+           target_row_offsets=None, ws=None, out=None, stream=None, softcap=0.0):
     """Returns (n_accepted [B] int32, correction_token [B] int32, workspace)."""
-    p = make_params(base, W1, T, seed)
+    p = make_params(base, W1, T, seed, softcap)
     B = base.shape[0]
     gamma_t = 0 if target_row_offsets is not None else target.shape[1]
     dev = base.device
@@ -61,9 +61,9 @@ def accept_rate_tv(d, t, keep, pos_valid=None, want_tau=True, ws=None, out=None,
     return out[0], out[1], out[2], ws
 
 
-def markov_block_logits(base, W1, W2, anchor, tokens, stream=None):
+def markov_block_logits(base, W1, W2, anchor, tokens, stream=None, softcap=0.0):
     """Teacher-forced z = base + W2 W1[prev] at every position.  base [B,gamma,V]; returns z [B,gamma,V] f32."""
-    p = make_params(base, W1, 1.0, 0)
+    p = make_params(base, W1, 1.0, 0, softcap)
     B, gamma, V = base.shape
     z = torch.empty((B, gamma, V), dtype=torch.float32, device=base.device)
     ws = b.workspace(b.dspark_markov_block_logits_workspace_size(p), base.device)

@@ -27,7 +27,7 @@ class DsparkError(RuntimeError):
 
 class SampleParams(C.Structure):
     _fields_ = [("B", C.c_int), ("gamma", C.c_int), ("V", C.c_int), ("r", C.c_int), ("temperature", C.c_float),
-                ("seed", C.c_uint64), ("logits_dtype", C.c_int), ("w_dtype", C.c_int)]
+                ("seed", C.c_uint64), ("logits_dtype", C.c_int), ("w_dtype", C.c_int), ("softcap", C.c_float)]
 
 
 _L = None
@@ -113,9 +113,9 @@ def _check(st: int, where: str):
         raise DsparkError(st, where)
 
 
-def params(B, gamma, V, r, temperature, seed, logits_dtype, w_dtype) -> SampleParams:
+def params(B, gamma, V, r, temperature, seed, logits_dtype, w_dtype, softcap=0.0) -> SampleParams:
     return SampleParams(int(B), int(gamma), int(V), int(r), float(temperature), int(seed) & (2 ** 64 - 1),
-                        int(logits_dtype), int(w_dtype))
+                        int(logits_dtype), int(w_dtype), float(softcap))
 
 
 # ------------------------------------------------------------------ entry points (same names as the C ABI)

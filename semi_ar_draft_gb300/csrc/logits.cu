@@ -24,6 +24,7 @@ struct BLArgs {
     const int32_t* tokens;
     float* z;
     int vec_b;
+    float softcap;  // draft softcap of the base logits (0: none)
     WsHeader* hdr;
 };
 
@@ -79,6 +80,8 @@ __global__ void __launch_bounds__(kThreads, 1) block_logits_kernel(BLArgs a) {
     pa.scale2 = 1.f;
     pa.vec_b = a.vec_b;
     pa.vec_t = 0;
+    pa.softcap = a.softcap;
+    pa.inv_softcap = a.softcap > 0.f ? 1.f / a.softcap : 0.f;
     produce_chunks<TL, KS, TW, false>(pa, tile, *rb, xbuf, cstat);
     __syncthreads();
     const int n = min(kTS, a.V - tile0);
@@ -147,6 +150,7 @@ extern "C" dspark_status dspark_markov_block_logits(const dspark_sample_params* 
     a.z = z_out;
     const size_t esz = p->logits_dtype == DSPARK_BF16 ? 2 : 4;
     a.vec_b = ((size_t)p->V * esz) % 16 == 0 && (uintptr_t)base_logits % 16 == 0;
+    a.softcap = p->softcap;
     a.hdr = static_cast<WsHeader*>(workspace);
     const size_t smem = sizeof(float) * kRows * kXRow + sizeof(float2) * kRows * kChunks +
                         align_up(sizeof(RowBlock), 16) + (mma ? 0 : sizeof(float) * kRows * (size_t)p->r);

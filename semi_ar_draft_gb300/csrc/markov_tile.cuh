@@ -29,6 +29,14 @@ constexpr int kXRow = kTS + 4;  // padded row stride (floats) of the value buffe
 
 enum RowMode { ROW_OFF = 0, ROW_SAMPLE = 1, ROW_RESID = 2, ROW_BONUS = 3 };
 
+// Final-logit softcap of the draft model (page "03 · DSpark 建模：Markov 与 Confidence", section
+// 3.12: compute_logits returns s tanh(logits / s)): applied to base logits as they are loaded,
+// before the Markov bias; ids past V keep the -inf of their padding.  s = 0: none.
+__device__ __forceinline__ void softcap8(float (&x)[8], int id0, int V, float s, float inv_s) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = id0 + e < V ? s * tanhf(x[e] * inv_s) : -CUDART_INF_F;
+}
+
 // Per-row inputs of a row block, staged in shared memory by the caller.
 struct RowBlock {
     int prev[kRows];         // W1 row (previous token)
@@ -270,6 +278,7 @@ struct ProdArgs {
     int greedy;
     float scale2;       // log2(e) / T
     int vec_b, vec_t;   // 16-byte aligned rows: 8-wide loads allowed
+    float softcap, inv_softcap;  // draft softcap of the base logits (0: none)
 };
 
 // HAS_T: rows may read target logits (residual / bonus draws of the verify pass).
@@ -335,6 +344,10 @@ __device__ __forceinline__ void produce_chunks(const ProdArgs& pa, int tile, con
         if (need_z) {
             if (za) unpack8<TL>(xb_[k][0], xa);
             if (zb) unpack8<TL>(xb_[k][1], xb);
+            if (pa.softcap > 0.f) {
+                softcap8(xa, id0, pa.V, pa.softcap, pa.inv_softcap);
+                softcap8(xb, id0, pa.V, pa.softcap, pa.inv_softcap);
+            }
             if constexpr (KS > 0) {
                 const uint16_t* W2 = reinterpret_cast<const uint16_t*>(pa.W2);
 #pragma unroll
@@ -435,7 +448,7 @@ __device__ __forceinline__ void mma4(float& d0, float& d1, float& d2, float& d3,
 template <typename TL, int KS, bool GREEDY, bool W2SMEM, bool FULL>
 __device__ __forceinline__ void produce_sample(const TL* base, const uint16_t* W1, const uint16_t* W2, const uint4* w2s,
                                                int V, bool vec, int tile, const RowBlock& rb, float* xbuf,
-                                               float2* cstat, float scale2) {
+                                               float2* cstat, float scale2, float softcap, float inv_softcap) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, tq = lane & 3;
     const long long oA = rb.brow[g] >= 0 ? rb.brow[g] : rb.brow[0];
@@ -467,6 +480,10 @@ __device__ __forceinline__ void produce_sample(const TL* base, const uint16_t* W
         float xa[8], xb[8];
         unpack8<TL>(ra[k], xa);
         unpack8<TL>(rbv[k], xb);
+        if (softcap > 0.f) {
+            softcap8(xa, cb + 8 * tq, V, softcap, inv_softcap);
+            softcap8(xb, cb + 8 * tq, V, softcap, inv_softcap);
+        }
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
             const int vl = kCS * c + 8 * (g >> 1) + 2 * nt + (g & 1);  // id (in tile) this lane feeds as column g
@@ -651,7 +668,8 @@ __device__ __forceinline__ float4 merge_rec(const float4 lo, const float4 hi, bo
 template <int KS, bool GREEDY, bool W2SMEM, bool FULL>
 __device__ __forceinline__ void produce_cg(const uint16_t* stage, const uint4* w1i, const uint16_t* W2,
                                            const uint4* w2s, int V, int tile, float4* crec, float scale2,
-                                           const float* lnEt, int ld, const float* urow, int nv) {
+                                           const float* lnEt, int ld, const float* urow, int nv, float softcap,
+                                           float inv_softcap) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, tq = lane & 3;
     const int tile0 = tile * kTS;
@@ -683,6 +701,12 @@ __device__ __forceinline__ void produce_cg(const uint16_t* stage, const uint4* w
                 acc[nt][1] = bf16_hi(pa[nt]);
                 acc[nt][2] = bf16_lo(pb[nt]);
                 acc[nt][3] = bf16_hi(pb[nt]);
+            }
+            if (softcap > 0.f) {  // (ids past V are set to -inf just below)
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) acc[nt][h] = softcap * tanhf(acc[nt][h] * inv_softcap);
             }
             if (!FULL) {  // ids past V take no part
 #pragma unroll

@@ -58,6 +58,7 @@ struct SampleArgs {
     int redundant;  // every block reduces every request (one grid-wide wait per step)
     int w2_smem;
     int vec_ok;  // base rows start on 16-byte boundaries: 8-wide loads and L2 prefetch allowed
+    float softcap, inv_softcap;  // draft softcap of the base logits (0: none)
 };
 
 size_t sample_smem_bytes(int B, int r, bool mma, bool w2_smem) {
@@ -115,6 +116,8 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(SampleArgs a) {
     pa.scale2 = a.scale2;
     pa.vec_b = a.vec_ok;
     pa.vec_t = 0;
+    pa.softcap = a.softcap;
+    pa.inv_softcap = a.inv_softcap;
     if constexpr (kMMA) {
         if (a.w2_smem) {
             stage_w2_tile<KS>(reinterpret_cast<const uint16_t*>(a.W2), blockIdx.x * kTS, a.V,
@@ -172,11 +175,11 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(SampleArgs a) {
                     const uint16_t* W2 = reinterpret_cast<const uint16_t*>(a.W2);
                     const bool full = (tile + 1) * kTS <= a.V && a.vec_ok;
                     if (pa.w2s) {
-                        if (full) produce_sample<TL, KS, GREEDY, true, true>(base, W1, W2, pa.w2s, a.V, true, tile, *rb, xbuf, cstat, a.scale2);
-                        else produce_sample<TL, KS, GREEDY, true, false>(base, W1, W2, pa.w2s, a.V, a.vec_ok, tile, *rb, xbuf, cstat, a.scale2);
+                        if (full) produce_sample<TL, KS, GREEDY, true, true>(base, W1, W2, pa.w2s, a.V, true, tile, *rb, xbuf, cstat, a.scale2, a.softcap, a.inv_softcap);
+                        else produce_sample<TL, KS, GREEDY, true, false>(base, W1, W2, pa.w2s, a.V, a.vec_ok, tile, *rb, xbuf, cstat, a.scale2, a.softcap, a.inv_softcap);
                     } else {
-                        if (full) produce_sample<TL, KS, GREEDY, false, true>(base, W1, W2, nullptr, a.V, true, tile, *rb, xbuf, cstat, a.scale2);
-                        else produce_sample<TL, KS, GREEDY, false, false>(base, W1, W2, nullptr, a.V, a.vec_ok, tile, *rb, xbuf, cstat, a.scale2);
+                        if (full) produce_sample<TL, KS, GREEDY, false, true>(base, W1, W2, nullptr, a.V, true, tile, *rb, xbuf, cstat, a.scale2, a.softcap, a.inv_softcap);
+                        else produce_sample<TL, KS, GREEDY, false, false>(base, W1, W2, nullptr, a.V, a.vec_ok, tile, *rb, xbuf, cstat, a.scale2, a.softcap, a.inv_softcap);
                     }
                 } else {
                     produce_chunks<TL, KS, TW, false>(pa, tile, *rb, xbuf, cstat);
@@ -662,11 +665,11 @@ __global__ void __launch_bounds__(kStagedThreads, 1) sample_staged_kernel(Sample
                 const int ld = step_table ? a.B : kRows;
                 const float* ut = urow + row0;
                 if (a.w2_smem) {
-                    if (full_tile) produce_cg<KS, GREEDY, true, true>(sbuf, wbuf, W2, w2s, a.V, tile, cr, a.scale2, lt, ld, ut, nv);
-                    else produce_cg<KS, GREEDY, true, false>(sbuf, wbuf, W2, w2s, a.V, tile, cr, a.scale2, lt, ld, ut, nv);
+                    if (full_tile) produce_cg<KS, GREEDY, true, true>(sbuf, wbuf, W2, w2s, a.V, tile, cr, a.scale2, lt, ld, ut, nv, a.softcap, a.inv_softcap);
+                    else produce_cg<KS, GREEDY, true, false>(sbuf, wbuf, W2, w2s, a.V, tile, cr, a.scale2, lt, ld, ut, nv, a.softcap, a.inv_softcap);
                 } else {
-                    if (full_tile) produce_cg<KS, GREEDY, false, true>(sbuf, wbuf, W2, nullptr, a.V, tile, cr, a.scale2, lt, ld, ut, nv);
-                    else produce_cg<KS, GREEDY, false, false>(sbuf, wbuf, W2, nullptr, a.V, tile, cr, a.scale2, lt, ld, ut, nv);
+                    if (full_tile) produce_cg<KS, GREEDY, false, true>(sbuf, wbuf, W2, nullptr, a.V, tile, cr, a.scale2, lt, ld, ut, nv, a.softcap, a.inv_softcap);
+                    else produce_cg<KS, GREEDY, false, false>(sbuf, wbuf, W2, nullptr, a.V, tile, cr, a.scale2, lt, ld, ut, nv, a.softcap, a.inv_softcap);
                 }
                 named_barrier(1, kThreads);
                 if (tid == 0) mbar_arrive_local(&empty[buf]);  // stage and W1 buffer free for row block cnt + 2
@@ -754,6 +757,7 @@ dspark_status validate_sample_params(const dspark_sample_params* p) {
     if (!p) return DSPARK_ERR_INVALID_ARG;
     if (p->B < 1 || p->gamma < 1 || p->V < 1 || p->r < 0) return DSPARK_ERR_INVALID_ARG;
     if (!(p->temperature >= 0.f) || std::isinf(p->temperature)) return DSPARK_ERR_INVALID_ARG;
+    if (!(p->softcap >= 0.f) || std::isinf(p->softcap)) return DSPARK_ERR_INVALID_ARG;
     if (p->logits_dtype != DSPARK_F32 && p->logits_dtype != DSPARK_BF16) return DSPARK_ERR_INVALID_ARG;
     if (p->r > 0 && p->w_dtype != DSPARK_F32 && p->w_dtype != DSPARK_BF16) return DSPARK_ERR_INVALID_ARG;
     if (p->B > 4096 || p->r > 1024 || p->gamma > 1024) return DSPARK_ERR_UNSUPPORTED;
@@ -866,6 +870,8 @@ extern "C" dspark_status dspark_markov_sample_block(const dspark_sample_params* 
     a.redundant = (size_t)p->B * nt <= 8192 && p->B <= kThreads;
     a.w2_smem = w2_smem;
     a.vec_ok = vec_ok;
+    a.softcap = p->softcap;
+    a.inv_softcap = p->softcap > 0.f ? 1.f / p->softcap : 0.f;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(workspace, 0, kHeaderBytes + (staged ? sample_slot_bytes(p) : 0), s) != cudaSuccess)

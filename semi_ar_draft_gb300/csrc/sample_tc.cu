@@ -630,7 +630,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 bool sample_tc_eligible(const dspark_sample_params* p, const void* base, const void* W1, const void* W2, int sms) {
     const int nt = (p->V + kTcTile - 1) / kTcTile;
+    // (the base logits are added on the tensor cores: a softcap of them needs the other samplers)
     return p->logits_dtype == DSPARK_BF16 && p->w_dtype == DSPARK_BF16 && p->r == kTcRank && p->B >= kTcMinBatch &&
+           p->softcap == 0.f &&
            p->V % 8 == 0 && ((uintptr_t)base % 16) == 0 && ((uintptr_t)W1 % 16) == 0 && ((uintptr_t)W2 % 16) == 0 &&
            nt <= sms && nt <= kTcMaxTiles && tensor_map_encoder() != nullptr;
 }

@@ -53,6 +53,7 @@ struct VerifyArgs {
     int4* job;          // [B] {type, position (1-based), prev token, lse2 bits of the target row}
     float4* jobpart;    // [B][nt]
     int vec_b, vec_t;
+    float softcap;  // draft softcap of the base logits (0: none)
 };
 
 __device__ __forceinline__ int req_len(const VerifyArgs& a, int j) { return a.vlen ? a.vlen[j] : a.gamma; }
@@ -703,6 +704,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_jobs_kernel(VerifyArgs a) 
     pa.scale2 = a.scale2;
     pa.vec_b = a.vec_b;
     pa.vec_t = a.vec_t;
+    pa.softcap = a.softcap;
+    pa.inv_softcap = a.softcap > 0.f ? 1.f / a.softcap : 0.f;
     if constexpr (KS == 0) {
         const TW* W1 = reinterpret_cast<const TW*>(a.W1);
         for (int idx = tid; idx < kRows * a.r; idx += kThreads) {
@@ -862,6 +865,7 @@ extern "C" dspark_status dspark_verify(const dspark_sample_params* p, const void
     const bool rows16 = ((size_t)p->V * esz) % 16 == 0;
     a.vec_b = rows16 && ((uintptr_t)base_logits % 16 == 0);
     a.vec_t = rows16 && ((uintptr_t)target_logits % 16 == 0);
+    a.softcap = p->softcap;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(workspace, 0, L.zero_bytes, s) != cudaSuccess) return DSPARK_ERR_CUDA;

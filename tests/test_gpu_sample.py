@@ -12,9 +12,10 @@ pytestmark = pytest.mark.gpu
 TS = 1024
 
 
-def run_and_compare(wl, requests=None, tally=None):
+def run_and_compare(wl, requests=None, tally=None, softcap=0.0):
     t = wl.tensors
-    tok, lse, zat, ws = api.markov_sample_block(t["base"], t["W1"], t["W2"], t["anchor"], wl.T, wl.seed)
+    tok, lse, zat, ws = api.markov_sample_block(t["base"], t["W1"], t["W2"], t["anchor"], wl.T, wl.seed,
+                                                softcap=softcap)
     torch.cuda.synchronize()
     assert binding.dspark_get_device_status(ws) == 0
     base = W.np_view(t["base"])
@@ -25,7 +26,7 @@ def run_and_compare(wl, requests=None, tally=None):
     tally = tally or Tally()
     reqs = range(wl.B) if requests is None else requests
     for j in reqs:
-        ref = O.sample_request(base, W1, W2, int(anchor[j]), int(j), wl.T, wl.seed, TS)
+        ref = O.sample_request(base, W1, W2, int(anchor[j]), int(j), wl.T, wl.seed, TS, softcap=softcap)
         compare_block(tally, g_tok[j], g_lse[j], g_zat[j], ref, wl.T, j)
     return tally, (tok, lse, zat)
 
@@ -212,3 +213,37 @@ def test_block_logits_token_out_of_range_sets_status():
     tokens = torch.tensor([[1, 5000, 3], [4, 5, 6]], dtype=torch.int32, device="cuda")
     _, ws = api.markov_block_logits(t["base"], t["W1"], t["W2"], t["anchor"], tokens)
     assert binding.dspark_get_device_status(ws) == 7  # DSPARK_ERR_TOKEN_RANGE
+
+
+# ---------------------------------------------------------------- final-logit softcap (page "03 · DSpark 建模", 3.12)
+@pytest.mark.parametrize("T", [0.0, 1.0])
+@pytest.mark.parametrize("B,logits_dtype", [(20, torch.bfloat16), (96, torch.bfloat16), (5, torch.float32)])
+def test_softcap(T, B, logits_dtype):
+    # staged sampler (bf16, 20 requests), the 96-request case (eligible for the tensor-core sampler
+    # without a cap, so it shows the cap routes elsewhere) and the general fp32 kernel; cap 4 against
+    # base logits ~N(0, 3) with planted peaks of +8: most of the mass sits where the cap bends
+    wl = W.make_sample_workload("cap", B, 3, 5000, 64, T, device="cuda", data_seed=B + 3, philox_seed=7, planted=3,
+                                logits_dtype=logits_dtype, w_std=0.3)
+    tally, _ = run_and_compare(wl, softcap=4.0)
+    tally.check_fraction()
+
+
+def test_softcap_block_logits():
+    wl = W.make_sample_workload("capb", 3, 4, 3000, 64, 1.0, device="cuda", data_seed=11, w_std=0.3)
+    t = wl.tensors
+    tokens = torch.randint(0, 3000, (3, 4), dtype=torch.int32).cuda()
+    z, ws = api.markov_block_logits(t["base"], t["W1"], t["W2"], t["anchor"], tokens, softcap=2.5)
+    torch.cuda.synchronize()
+    assert binding.dspark_get_device_status(ws) == 0
+    ref = O.block_logits(W.np_view(t["base"]), W.np_view(t["W1"]), W.np_view(t["W2"]), t["anchor"].cpu().numpy(),
+                         tokens.cpu().numpy(), softcap=2.5)
+    close(z.cpu().numpy(), ref, rtol=1e-5, atol=2e-6, what="capped block logits")
+
+
+def test_softcap_rejects_bad_values():
+    wl = W.make_sample_workload("capbad", 2, 2, 1024, 16, 1.0, device="cuda")
+    t = wl.tensors
+    for bad in (-1.0, float("inf"), float("nan")):
+        with pytest.raises(binding.DsparkError) as e:
+            api.markov_sample_block(t["base"], t["W1"], t["W2"], t["anchor"], 1.0, 0, softcap=bad)
+        assert e.value.status == 1

@@ -19,19 +19,19 @@ def host(wl):
             None if t["W2"] is None else W.np_view(t["W2"]), t["anchor"].cpu().numpy(), W.np_view(t["target"]))
 
 
-def oracle_drafts(wl):
+def oracle_drafts(wl, softcap=0.0):
     base, W1, W2, anchor, _ = host(wl)
     B, g = wl.B, wl.gamma
     tok = np.zeros((B, g), np.int32)
     lse = np.zeros((B, g), np.float32)
     zat = np.zeros((B, g), np.float32)
     for j in range(B):
-        rt, rl, rz, _ = O.sample_request(base, W1, W2, int(anchor[j]), j, wl.T, wl.seed, TS)
+        rt, rl, rz, _ = O.sample_request(base, W1, W2, int(anchor[j]), j, wl.T, wl.seed, TS, softcap=softcap)
         tok[j], lse[j], zat[j] = rt, rl.astype(np.float32), rz.astype(np.float32)
     return tok, lse, zat
 
 
-def verify_both(wl, tok, lse, zat, vlen=None, csr=False):
+def verify_both(wl, tok, lse, zat, vlen=None, csr=False, softcap=0.0):
     t = wl.tensors
     base, W1, W2, anchor, target = host(wl)
     dev = "cuda"
@@ -50,7 +50,7 @@ def verify_both(wl, tok, lse, zat, vlen=None, csr=False):
                                  wl.seed, verify_len=vl, target_row_offsets=torch.from_numpy(off).to(dev))
     else:
         n, corr, ws = api.verify(t["base"], t["W1"], t["W2"], t["anchor"], gt_tok, gt_lse, gt_zat, t["target"],
-                                 wl.T, wl.seed, verify_len=vl)
+                                 wl.T, wl.seed, verify_len=vl, softcap=softcap)
     torch.cuda.synchronize()
     assert binding.dspark_get_device_status(ws) == 0
     n, corr = n.cpu().numpy(), corr.cpu().numpy()
@@ -59,7 +59,7 @@ def verify_both(wl, tok, lse, zat, vlen=None, csr=False):
         Lj = wl.gamma if vlen is None else int(vlen[j])
         tgt = target if not csr else target[:, : wl.gamma_t]
         rn, rc, rm, _ = O.verify_request(base, W1, W2, int(anchor[j]), j, tok[j], lse[j], zat[j], tgt, Lj, wl.T,
-                                         wl.seed, TS)
+                                         wl.seed, TS, softcap=softcap)
         tally.total += 1
         if (n[j], corr[j]) != (rn, rc):
             assert rm < MARGIN, f"request {j}: gpu (n={n[j]}, corr={corr[j]}) vs oracle ({rn}, {rc}) margin {rm}"
@@ -199,3 +199,11 @@ def test_residual_without_mass_falls_back_to_p():
         _, rc, _, fb = O.verify_request(base, W1, W2, int(anchor[j]), j, tok[j], lse_low[j], zat[j], target, wl.gamma,
                                         wl.T, wl.seed, TS)
         assert fb == 1, j
+
+
+@pytest.mark.parametrize("T", [0.0, 1.0])
+def test_softcap_residuals(T):
+    # the draft's capped logits are rebuilt at every rejecting position (the target is taken as given)
+    wl = W.make_sample_workload("vcap", 21, 4, 5000, 64, T, device="cuda", data_seed=5, philox_seed=3,
+                                target_sigma=0.7, planted=2, w_std=0.3)
+    verify_both(wl, *oracle_drafts(wl, softcap=3.0), softcap=3.0)

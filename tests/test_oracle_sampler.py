@@ -217,3 +217,57 @@ def test_sample_request_carries_token_and_lse():
         assert tok[i] == x and abs(lse[i] - special.logsumexp(z / T)) < 1e-12
         assert abs(zx[i] - z[x]) < 1e-12
         prev = x
+
+
+# ---------------------------------------------------------------- final-logit softcap (page "03 · DSpark 建模", 3.12)
+def test_softcap_limits_and_bounds():
+    rng = np.random.default_rng(5)
+    V, r = 64, 4
+    base = (rng.normal(0, 20, V)).astype(np.float32)
+    W1 = rng.normal(0, 1.0, (V, r)).astype(np.float32)
+    W2 = rng.normal(0, 1.0, (V, r)).astype(np.float32)
+    prev = 7
+    plain = O.markov_logits(base, W1, W2, prev)
+    bias = plain - base.astype(np.float64)
+    # a cap far above every logit leaves them unchanged
+    assert np.allclose(O.markov_logits(base, W1, W2, prev, softcap=1e30), plain, rtol=1e-15, atol=0)
+    for s in (0.5, 3.0, 30.0):
+        capped = O.markov_logits(base, None, None, 0, softcap=s)  # rank 0: the capped base alone
+        assert np.all(np.abs(capped) <= s)  # (tanh reaches 1 in double for large arguments)
+        order = np.argsort(base, kind="stable")
+        assert np.all(np.diff(capped[order]) >= 0)  # monotone in the base logit
+        neg = O.markov_logits(-base, None, None, 0, softcap=s)
+        assert np.array_equal(neg, -capped)  # odd
+        # the bias is added after the cap: with the Markov head the difference is the bias itself
+        assert np.allclose(O.markov_logits(base, W1, W2, prev, softcap=s) - capped, bias, rtol=0, atol=1e-12)
+    # with the bias added after the cap, z itself leaves [-s, s] when the bias is large
+    z = O.markov_logits(base, W1, W2, prev, softcap=0.5)
+    assert np.abs(z).max() > 0.5
+    # closed form: base = s atanh(q) is capped to s q
+    s = 4.0
+    q = np.array([-0.9, -0.25, 0.0, 0.25, 0.5, 0.9])
+    b = (s * np.arctanh(q)).astype(np.float32)
+    got = O.markov_logits(b, None, None, 0, softcap=s)
+    want = s * np.tanh(np.arctanh(q) + (b.astype(np.float64) / s - np.arctanh(q)))  # exact for the rounded b
+    assert np.allclose(got, want, rtol=0, atol=1e-12) and np.allclose(got, s * q, rtol=0, atol=1e-6)
+
+
+def test_softcap_greedy_draft_is_the_capped_argmax():
+    rng = np.random.default_rng(9)
+    B, g, V, r = 1, 3, 300, 4
+    base = rng.normal(0, 5, (B, g, V)).astype(np.float32)
+    base[0, :, 17] = 40.0  # towers over the rest uncapped ...
+    base[0, :, 200] = 39.0
+    W1 = rng.normal(0, 0.01, (V, r)).astype(np.float32)
+    W2 = rng.normal(0, 0.01, (V, r)).astype(np.float32)
+    W1[3] = [1.0, 0.0, 0.0, 0.0]  # the anchor's row: bias_v = W2[v, 0] at position 1
+    W2[17, 0], W2[200, 0] = 0.0, 0.5  # ... while a cap of 2 flattens the top and the bias then decides
+    tok, lse, zx, mg = O.sample_request(base, W1, W2, 3, 0, 0.0, 0, 64, softcap=2.0)
+    prev = 3
+    for i in range(g):
+        z = O.markov_logits(base[0, i], W1, W2, prev, softcap=2.0)
+        assert tok[i] == int(np.argmax(z)) and zx[i] == z[tok[i]]
+        prev = int(tok[i])
+    assert tok[0] == 200  # capped: 2 tanh(19.5) + 0.5 > 2 tanh(20)
+    tok0, *_ = O.sample_request(base, W1, W2, 3, 0, 0.0, 0, 64)
+    assert tok0[0] == 17  # without the cap the tower wins: 40 > 39 + 0.5
