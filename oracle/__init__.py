@@ -64,7 +64,9 @@ def lib():
         L.oracle_sample_request.argtypes = [i32, i32, i32, i32, i32, dbl, u64, i32, i32, vp, vp, vp, i32, i32,
                                             vp, vp, vp, vp, dbl]
         L.oracle_verify_request.argtypes = [i32, i32, i32, i32, i32, i32, dbl, u64, i32, i32, i32, vp, vp, vp,
-                                            i32, i32, vp, vp, vp, vp, i32, vp, vp, vp, dbl]
+                                            i32, i32, vp, vp, vp, vp, i32, vp, vp, vp, dbl, vp]
+        L.oracle_sample_request_head.argtypes = [i32, i32, i32, i32, i32, dbl, u64, i32, i32, vp, vp, vp, i32, i32,
+                                                 i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, dbl]
         L.oracle_verify_request.restype = i32
         L.oracle_tv_row.argtypes = [i32, i32, vp, vp, vp]
         L.oracle_tv_row.restype = dbl
@@ -193,6 +195,30 @@ def sample_request(base: np.ndarray, W1, W2, anchor: int, j: int, T: float, seed
     return tok, lse, zx, mg
 
 
+HEAD_VANILLA, HEAD_GATED, HEAD_RNN = 0, 1, 2
+
+
+def sample_request_head(base: np.ndarray, W1, W2, anchor: int, j: int, T: float, seed: int, TS: int, kind: int,
+                        hidden: np.ndarray, Wg, Wc=None, Wo=None, CS: int = CHUNK, softcap: float = 0.0):
+    """One request of the Gated / RNN head sampler (P1 section 3.7).  hidden [B, gamma, d] (the request's
+    rows are used) and the head weights share W1's dtype.  Returns (tokens, lse, z_at_tok, margins,
+    head vectors [gamma, r])."""
+    B, gamma, V = base.shape
+    r = W1.shape[1]
+    d = hidden.shape[-1]
+    blk = np.ascontiguousarray(base[j])
+    hrow = np.ascontiguousarray(hidden[j])
+    tok = np.zeros(gamma, dtype=np.int32)
+    lse, zx, mg = np.zeros(gamma), np.zeros(gamma), np.zeros(gamma)
+    u = np.zeros((gamma, r))
+    w_dt = _dtype_code(W1)
+    lib().oracle_sample_request_head(V, r, gamma, TS, CS, float(T), seed, _dtype_code(base), w_dt, _p(blk), _p(W1),
+                                     _p(W2), int(anchor), int(j), int(kind), int(d), _p(hrow), _p(Wg),
+                                     _p(Wc) if Wc is not None else None, _p(Wo) if Wo is not None else None,
+                                     _p(tok), _p(lse), _p(zx), _p(mg), _p(u), float(softcap))
+    return tok, lse, zx, mg, u
+
+
 def sample_block(base, W1, W2, anchor, T, seed, TS, requests=None, CS: int = CHUNK):
     """Oracle of dspark_markov_sample_block for the listed requests (default all)."""
     B, gamma, V = base.shape
@@ -205,7 +231,7 @@ def sample_block(base, W1, W2, anchor, T, seed, TS, requests=None, CS: int = CHU
 
 # ----------------------------------------------------------------- verify
 def verify_request(base, W1, W2, anchor: int, j: int, tokens, draft_lse, z_at_tok, target, L: int,
-                   T: float, seed: int, TS: int, row=None, CS: int = CHUNK, softcap: float = 0.0):
+                   T: float, seed: int, TS: int, row=None, CS: int = CHUNK, softcap: float = 0.0, head_vec=None):
     """One request of dspark_verify.  base [B,gamma,V], target [B,gamma_t,V];
     tokens/draft_lse/z_at_tok: this request's gamma entries (int32 / float32);
     j is the request index (random stream); `row` selects the data (default j)."""
@@ -221,11 +247,13 @@ def verify_request(base, W1, W2, anchor: int, j: int, tokens, draft_lse, z_at_to
     corr = np.zeros(1, dtype=np.int32)
     mm = np.zeros(1)
     fb = np.zeros(1, dtype=np.int32)
+    hv = None if head_vec is None else np.ascontiguousarray(head_vec, dtype=np.float64)
     w_dt = _dtype_code(W1) if r else F32
     n = lib().oracle_verify_request(V, r, gamma, gamma_t, TS, CS, float(T), seed, _dtype_code(base), w_dt,
                                     _dtype_code(target), _p(bblk), _p(W1) if r else None,
                                     _p(W2) if r else None, int(anchor), int(j), _p(tok), _p(dl), _p(zx),
-                                    _p(tblk), int(L), _p(corr), _p(mm), _p(fb), float(softcap))
+                                    _p(tblk), int(L), _p(corr), _p(mm), _p(fb), float(softcap),
+                                    _p(hv) if hv is not None else None)
     return int(n), int(corr[0]), float(mm[0]), int(fb[0])
 
 

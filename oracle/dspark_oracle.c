@@ -373,11 +373,119 @@ void oracle_sample_request(int V, int r, int gamma, int TS, int CS, double T, ui
 /*   *min_margin over all decisions; *resid_fallback = 1 when the       */
 /*   residual had no mass and p was used instead.                       */
 /* ------------------------------------------------------------------ */
+/* Gated and RNN Markov heads (P1 section 3.7, 三种 Markov head; P4    */
+/* section 3.3): the vector u_k that W2 multiplies at draft step k,    */
+/* from e = W1[x_{k-1}] (r), the backbone hidden state h_k (d) and,    */
+/* for the RNN head, the state s_{k-1} (r, updated in place to s_k).   */
+/*   gated: gate = sigmoid(Wg [h; e]),  u = gate * e                   */
+/*          (Wg: r x (d + r), columns h then e)                        */
+/*   rnn:   z = [s; e; h] (2r + d),  g = sigmoid(Wg z),                */
+/*          s <- g * s + (1 - g) * tanh(Wc z),  u = tanh(Wo z)         */
+/*          (Wg, Wc, Wo: r x (2r + d)); the bias uses z_k, which holds */
+/*          s_{k-1}.  The initial state is zero (the pages give none). */
+/* sigmoid(a) = 1 / (1 + exp(-a)).                                     */
+/* ------------------------------------------------------------------ */
+enum { OR_HEAD_VANILLA = 0, OR_HEAD_GATED = 1, OR_HEAD_RNN = 2 };
+
+static double sigmoid(double a) { return 1.0 / (1.0 + exp(-a)); }
+
+void oracle_head_vector(int kind, int r, int d, int dtype, const void* Wg, const void* Wc, const void* Wo,
+                        const double* e, const void* h_row, double* s, double* u) {
+    if (kind == OR_HEAD_GATED) {
+        for (int i = 0; i < r; ++i) {
+            double a = 0.0;
+            for (int c = 0; c < d; ++c) a += load_val(Wg, dtype, (size_t)i * (d + r) + c) * load_val(h_row, dtype, c);
+            for (int c = 0; c < r; ++c) a += load_val(Wg, dtype, (size_t)i * (d + r) + d + c) * e[c];
+            u[i] = sigmoid(a) * e[i];
+        }
+        return;
+    }
+    if (kind == OR_HEAD_RNN) {
+        const int w = 2 * r + d;
+        double* z = (double*)malloc(sizeof(double) * (size_t)w);
+        double* s_new = (double*)malloc(sizeof(double) * (size_t)r);
+        for (int c = 0; c < r; ++c) z[c] = s[c];
+        for (int c = 0; c < r; ++c) z[r + c] = e[c];
+        for (int c = 0; c < d; ++c) z[2 * r + c] = load_val(h_row, dtype, c);
+        for (int i = 0; i < r; ++i) {
+            double ag = 0.0, ac = 0.0, ao = 0.0;
+            for (int c = 0; c < w; ++c) {
+                ag += load_val(Wg, dtype, (size_t)i * w + c) * z[c];
+                ac += load_val(Wc, dtype, (size_t)i * w + c) * z[c];
+                ao += load_val(Wo, dtype, (size_t)i * w + c) * z[c];
+            }
+            const double g = sigmoid(ag);
+            s_new[i] = g * s[i] + (1.0 - g) * tanh(ac);
+            u[i] = tanh(ao);
+        }
+        for (int i = 0; i < r; ++i) s[i] = s_new[i];
+        free(z);
+        free(s_new);
+        return;
+    }
+    for (int i = 0; i < r; ++i) u[i] = e[i]; /* vanilla: u = W1[x] */
+}
+
+/* z_v = cap(base_v) + sum_i W2[v, i] u_i (the Markov logits with an explicit head vector). */
+void oracle_head_logits(int V, int r, int logits_dtype, int w_dtype, const void* base_row, const double* u,
+                        const void* W2, double softcap, double* z_out) {
+    for (int v = 0; v < V; ++v) {
+        double bias = 0.0;
+        for (int k = 0; k < r; ++k) bias += load_val(W2, w_dtype, (size_t)v * r + k) * u[k];
+        double b = load_val(base_row, logits_dtype, (size_t)v);
+        if (softcap > 0.0) b = softcap * tanh(b / softcap);
+        z_out[v] = b + bias;
+    }
+}
+
+/* One request of the head sampler: as oracle_sample_request with the bias W2 u_k of the head
+ * (hidden_req [gamma, d] in the head dtype); u_out [gamma, r] receives the head vectors. */
+void oracle_sample_request_head(int V, int r, int gamma, int TS, int CS, double T, uint64_t seed, int logits_dtype,
+                                int w_dtype, const void* base_req, const void* W1, const void* W2, int anchor, int j,
+                                int kind, int d, const void* hidden_req, const void* Wg, const void* Wc,
+                                const void* Wo, int32_t* tokens, double* draft_lse, double* z_at_tok, double* margin,
+                                double* u_out, double softcap) {
+    double* z = (double*)malloc(sizeof(double) * (size_t)V);
+    double* sv = (double*)malloc(sizeof(double) * (size_t)V);
+    double* e = (double*)malloc(sizeof(double) * (size_t)(r > 0 ? r : 1));
+    double* st = (double*)calloc((size_t)(r > 0 ? r : 1), sizeof(double));
+    size_t esz = (logits_dtype == OR_F32) ? 4 : 2, hsz = (w_dtype == OR_F32) ? 4 : 2;
+    int prev = anchor;
+    for (int step = 0; step < gamma; ++step) {
+        int i = step + 1;
+        for (int c = 0; c < r; ++c) e[c] = load_val(W1, w_dtype, (size_t)prev * r + c);
+        const char* hrow = (const char*)hidden_req + (size_t)step * (size_t)d * hsz;
+        double* u = u_out + (size_t)step * r;
+        oracle_head_vector(kind, r, d, w_dtype, Wg, Wc, Wo, e, hrow, st, u);
+        const char* row = (const char*)base_req + (size_t)step * (size_t)V * esz;
+        oracle_head_logits(V, r, logits_dtype, w_dtype, row, u, W2, softcap, z);
+        int x;
+        double mg, lse;
+        if (T == 0.0) {
+            x = oracle_argmax(z, V, &mg);
+            lse = NAN;
+        } else {
+            for (int v = 0; v < V; ++v) sv[v] = z[v] / T;
+            x = oracle_chunk_gumbel(sv, V, CS, seed, j, i, OR_P_SAMPLE_CHUNK, OR_P_SAMPLE_INCHUNK, &mg, &lse);
+        }
+        tokens[step] = x;
+        draft_lse[step] = lse;
+        z_at_tok[step] = z[x];
+        margin[step] = mg;
+        prev = x;
+    }
+    free(z);
+    free(sv);
+    free(e);
+    free(st);
+}
+
+/* ------------------------------------------------------------------ */
 int oracle_verify_request(int V, int r, int gamma, int gamma_t, int TS, int CS, double T, uint64_t seed,
                           int logits_dtype, int w_dtype, int target_dtype, const void* base_req, const void* W1,
                           const void* W2, int anchor, int j, const int32_t* tokens, const float* draft_lse,
                           const float* z_at_tok, const void* target_req, int L, int32_t* correction,
-                          double* min_margin, int* resid_fallback, double softcap) {
+                          double* min_margin, int* resid_fallback, double softcap, const double* head_vec) {
     size_t tsz = (target_dtype == OR_F32) ? 4 : 2;
     size_t bsz = (logits_dtype == OR_F32) ? 4 : 2;
     (void)gamma; /* the per-request blocks are already sliced */
@@ -417,7 +525,10 @@ int oracle_verify_request(int V, int r, int gamma, int gamma_t, int TS, int CS, 
                 int prev = (step == 0) ? anchor : tokens[step - 1];
                 const char* brow = (const char*)base_req + (size_t)step * (size_t)V * bsz;
                 double* z = (double*)malloc(sizeof(double) * (size_t)V);
-                oracle_markov_logits(V, r, logits_dtype, w_dtype, brow, W1, W2, prev, softcap, z);
+                if (head_vec) /* a Gated / RNN head: the draft's own head vector of this position */
+                    oracle_head_logits(V, r, logits_dtype, w_dtype, brow, head_vec + (size_t)step * r, W2, softcap, z);
+                else
+                    oracle_markov_logits(V, r, logits_dtype, w_dtype, brow, W1, W2, prev, softcap, z);
                 double lse_t = logsumexp(lw, V); /* lw still holds t/T of this row */
                 int any = 0;
                 for (int v = 0; v < V; ++v) {
@@ -638,7 +749,7 @@ void oracle_trials_spec_one(int V, int TS, int CS, double T, const float* zd, co
         float lse_f = (float)lse_d, zx_f = zd[x];
         int32_t corr;
         int nacc = oracle_verify_request(V, 0, 1, 1, TS, CS, T, seed, OR_F32, OR_F32, OR_F32, zd, NULL, NULL, 0, (int)n,
-                                         &x, &lse_f, &zx_f, zt, 1, &corr, NULL, NULL, 0.0);
+                                         &x, &lse_f, &zx_f, zt, 1, &corr, NULL, NULL, 0.0, NULL);
         if (nacc == 1) {
             emitted[x] += 1;
             *n_accept += 1;
@@ -671,7 +782,7 @@ void oracle_trials_spec_block(int V, int r, int gamma, int TS, int CS, double T,
         }
         int32_t corr;
         int nacc = oracle_verify_request(V, r, gamma, gamma, TS, CS, T, seed, OR_F32, OR_F32, OR_F32, base_req, W1, W2,
-                                         anchor, (int)n, tok, lse_f, zx_f, target_req, gamma, &corr, NULL, NULL, 0.0);
+                                         anchor, (int)n, tok, lse_f, zx_f, target_req, gamma, &corr, NULL, NULL, 0.0, NULL);
         hist[nacc] += 1;
     }
     free(tok); free(lse); free(zx); free(mg); free(lse_f); free(zx_f);
