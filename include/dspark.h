@@ -132,6 +132,45 @@ dspark_status dspark_markov_sample_block(const dspark_sample_params* p, const vo
                                          dspark_stream_t stream);
 
 /*
+ * Gated and RNN Markov heads (P1 section 3.7; P4 section 3.3, the table of the three heads).
+ * Both replace the vector that W2 multiplies: the vanilla head uses e = W1[prev]; with the
+ * backbone's hidden state h_{j,i} [d] of position i these use
+ *   DSPARK_HEAD_GATED: u = sigmoid(Wg [h; e]) * e              Wg [r, d + r], columns [h | e]
+ *   DSPARK_HEAD_RNN:   z = [s; e; h]  (s_{j,0} = 0 per request, one state per request)
+ *                      g = sigmoid(Wg z),  s <- g * s + (1 - g) * tanh(Wc z),  u = tanh(Wo z)
+ *                                                              Wg, Wc, Wo [r, 2r + d], columns [s | e | h]
+ * and z_{j,i} = cap(base[j, i-1, :]) + W2 u.  The RNN step forms u from the state before the update.
+ * The gate is a logistic sigmoid and the state starts at zero (the pages show neither).
+ */
+enum { DSPARK_HEAD_VANILLA = 0, DSPARK_HEAD_GATED = 1, DSPARK_HEAD_RNN = 2 };
+typedef struct {
+    int kind;           /* DSPARK_HEAD_GATED or DSPARK_HEAD_RNN */
+    int d;              /* hidden size (>= 1) */
+    const void* hidden; /* [B, gamma, d] (w_dtype): the hidden state feeding position i (row i-1) */
+    const void* Wg;     /* gated: [r, d + r]; rnn: [r, 2r + d]  (w_dtype) */
+    const void* Wc;     /* rnn only: [r, 2r + d] (w_dtype); NULL for gated */
+    const void* Wo;     /* rnn only: [r, 2r + d] (w_dtype); NULL for gated */
+} dspark_head;
+
+/*
+ * dspark_markov_sample_block with a Gated or RNN head: the same draw, contracts and outputs,
+ * with W2 u in place of W2 W1[prev].  Needs r >= 1.  head_vec [B, gamma, r] float (or NULL)
+ * receives the u of every position, for dspark_verify_head.  The head vectors of a step are
+ * computed in fp32 on CUDA cores inside the persistent kernel (B r (r + d) multiply-adds per step
+ * for the gated head, 3 B r (2r + d) for the RNN head).
+ * Host errors: as dspark_markov_sample_block, plus DSPARK_ERR_INVALID_ARG for a bad kind, d < 1,
+ * r < 1 or a NULL hidden / weight, and DSPARK_ERR_UNSUPPORTED when the per-request head state
+ * does not fit one block's shared memory (B r (1 gated, 3 rnn) floats next to the sampler's own).
+ * Workspace: dspark_sample_head_workspace_size(p, head) bytes.
+ */
+size_t dspark_sample_head_workspace_size(const dspark_sample_params* p, const dspark_head* head);
+dspark_status dspark_markov_sample_block_head(const dspark_sample_params* p, const dspark_head* head,
+                                              const void* base_logits, const void* W1, const void* W2,
+                                              const int32_t* anchor, int32_t* tokens, float* draft_lse,
+                                              float* draft_logit_at_tok, float* head_vec, void* workspace,
+                                              size_t ws_bytes, dspark_stream_t stream);
+
+/*
  * Lossless verification by rejection sampling (P3 "Speculative Decoding": the target checks
  * the drafted positions in parallel, accepts left to right, truncates at the first failure
  * and resamples from the target, so the output law is the target's; the verify tokens of all
@@ -167,6 +206,18 @@ dspark_status dspark_verify(const dspark_sample_params* p, const void* base_logi
                             const float* draft_logit_at_tok, const void* target_logits, int gamma_t,
                             const int32_t* verify_len, const int32_t* target_row_offsets, int32_t* n_accepted,
                             int32_t* correction_token, void* workspace, size_t ws_bytes, dspark_stream_t stream);
+
+/*
+ * dspark_verify for drafts of a Gated or RNN head: the residual's q_k is rebuilt from
+ * head_vec [B, gamma, r] float (dspark_markov_sample_block_head's output) as
+ * cap(base) + W2 head_vec[j, k-1] instead of W1[prev].  W1 is not read and may be NULL; every
+ * other argument, output and error is that of dspark_verify.  Workspace: dspark_verify_workspace_size.
+ */
+dspark_status dspark_verify_head(const dspark_sample_params* p, const void* base_logits, const float* head_vec,
+                                 const void* W2, const int32_t* anchor, const int32_t* tokens, const float* draft_lse,
+                                 const float* draft_logit_at_tok, const void* target_logits, int gamma_t,
+                                 const int32_t* verify_len, const int32_t* target_row_offsets, int32_t* n_accepted,
+                                 int32_t* correction_token, void* workspace, size_t ws_bytes, dspark_stream_t stream);
 
 /*
  * Training-side accept-rate targets (P1 section 3.9 "Accept rate 3D", P2 section 3.5) and the

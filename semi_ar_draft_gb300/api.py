@@ -47,6 +47,40 @@ def verify(base, W1, W2, anchor, tokens, draft_lse, z_at_tok, target, T, seed, v
     return out[0], out[1], ws
 
 
+def markov_sample_block_head(base, W1, W2, anchor, T, seed, kind, hidden, Wg, Wc=None, Wo=None, ws=None,
+                             out=None, stream=None, softcap=0.0):
+    """Gated / RNN head sampling.  Returns (tokens, draft_lse, z_at_tok, head_vec [B,gamma,r] f32, workspace)."""
+    p = make_params(base, W1, T, seed, softcap)
+    B, gamma, _ = base.shape
+    dev = base.device
+    h = b.head(kind, hidden, Wg, Wc, Wo)
+    if out is None:
+        out = (torch.empty((B, gamma), dtype=torch.int32, device=dev), torch.empty((B, gamma), device=dev),
+               torch.empty((B, gamma), device=dev), torch.empty((B, gamma, W1.shape[1]), device=dev))
+    if ws is None:
+        ws = b.workspace(b.dspark_sample_head_workspace_size(p, h), dev)
+    b.dspark_markov_sample_block_head(p, h, base, W1, W2, anchor, out[0], out[1], out[2], out[3], ws, stream)
+    return out[0], out[1], out[2], out[3], ws
+
+
+def verify_head(base, head_vec, W2, anchor, tokens, draft_lse, z_at_tok, target, T, seed, verify_len=None,
+                target_row_offsets=None, ws=None, out=None, stream=None, softcap=0.0):
+    """dspark_verify for Gated / RNN drafts: q is rebuilt from head_vec [B,gamma,r] f32.
+    Returns (n_accepted, correction_token, workspace)."""
+    B, gamma, V = base.shape
+    r = head_vec.shape[-1]
+    p = b.params(B, gamma, V, r, T, seed, b.dtype_code(base.dtype), b.dtype_code(W2.dtype), softcap)
+    gamma_t = 0 if target_row_offsets is not None else target.shape[1]
+    dev = base.device
+    if out is None:
+        out = (torch.empty(B, dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev))
+    if ws is None:
+        ws = b.workspace(b.dspark_verify_workspace_size(p, gamma_t), dev)
+    b.dspark_verify_head(p, base, head_vec, W2, anchor, tokens, draft_lse, z_at_tok, target, gamma_t, verify_len,
+                         target_row_offsets, out[0], out[1], ws, stream)
+    return out[0], out[1], ws
+
+
 def accept_rate_tv(d, t, keep, pos_valid=None, want_tau=True, ws=None, out=None, stream=None):
     """d, t [S,A,gamma,V]; keep [S,A] uint8.  Returns (accept_rate, eval_mask, tau or None, workspace)."""
     S, A, gamma, V = d.shape

@@ -25,6 +25,14 @@ class DsparkError(RuntimeError):
         self.status = status
 
 
+HEAD_VANILLA, HEAD_GATED, HEAD_RNN = 0, 1, 2
+
+
+class Head(C.Structure):
+    _fields_ = [("kind", C.c_int), ("d", C.c_int), ("hidden", C.c_void_p), ("Wg", C.c_void_p), ("Wc", C.c_void_p),
+                ("Wo", C.c_void_p)]
+
+
 class SampleParams(C.Structure):
     _fields_ = [("B", C.c_int), ("gamma", C.c_int), ("V", C.c_int), ("r", C.c_int), ("temperature", C.c_float),
                 ("seed", C.c_uint64), ("logits_dtype", C.c_int), ("w_dtype", C.c_int), ("softcap", C.c_float)]
@@ -47,6 +55,13 @@ def lib():
         L.dspark_markov_sample_block.restype = i32
         L.dspark_markov_sample_block_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp]
         L.dspark_markov_sample_block_noalloc.restype = i32
+        H = C.POINTER(Head)
+        L.dspark_sample_head_workspace_size.argtypes = [P, H]
+        L.dspark_sample_head_workspace_size.restype = sz
+        L.dspark_markov_sample_block_head.argtypes = [P, H, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.dspark_markov_sample_block_head.restype = i32
+        L.dspark_verify_head.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, sz, vp]
+        L.dspark_verify_head.restype = i32
         L.dspark_verify_workspace_size.argtypes = [P, i32]
         L.dspark_verify_workspace_size.restype = sz
         L.dspark_verify.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, sz, vp]
@@ -139,6 +154,34 @@ def dspark_markov_sample_block_noalloc(p, base_logits, W1, W2, anchor, tokens, d
                                                   _ptr(tokens), _ptr(draft_lse), _ptr(draft_logit_at_tok),
                                                   _stream(stream))
     _check(st, "dspark_markov_sample_block_noalloc")
+
+
+def head(kind, hidden, Wg, Wc=None, Wo=None) -> Head:
+    """A dspark_head over device tensors (kept alive by the caller): hidden [B, gamma, d]."""
+    return Head(int(kind), int(hidden.shape[-1]), _ptr(hidden), _ptr(Wg), _ptr(Wc), _ptr(Wo))
+
+
+def dspark_sample_head_workspace_size(p: SampleParams, h: Head) -> int:
+    return int(lib().dspark_sample_head_workspace_size(C.byref(p), C.byref(h)))
+
+
+def dspark_markov_sample_block_head(p, h, base_logits, W1, W2, anchor, tokens, draft_lse, draft_logit_at_tok,
+                                    head_vec, workspace, stream=None):
+    st = lib().dspark_markov_sample_block_head(C.byref(p), C.byref(h), _ptr(base_logits), _ptr(W1), _ptr(W2),
+                                               _ptr(anchor), _ptr(tokens), _ptr(draft_lse), _ptr(draft_logit_at_tok),
+                                               _ptr(head_vec), _ptr(workspace),
+                                               workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "dspark_markov_sample_block_head")
+
+
+def dspark_verify_head(p, base_logits, head_vec, W2, anchor, tokens, draft_lse, draft_logit_at_tok, target_logits,
+                       gamma_t, verify_len, target_row_offsets, n_accepted, correction_token, workspace, stream=None):
+    st = lib().dspark_verify_head(C.byref(p), _ptr(base_logits), _ptr(head_vec), _ptr(W2), _ptr(anchor),
+                                  _ptr(tokens), _ptr(draft_lse), _ptr(draft_logit_at_tok), _ptr(target_logits),
+                                  int(gamma_t), _ptr(verify_len), _ptr(target_row_offsets), _ptr(n_accepted),
+                                  _ptr(correction_token), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "dspark_verify_head")
 
 
 def dspark_verify_workspace_size(p: SampleParams, gamma_t: int) -> int:

@@ -59,9 +59,19 @@ struct SampleArgs {
     int w2_smem;
     int vec_ok;  // base rows start on 16-byte boundaries: 8-wide loads and L2 prefetch allowed
     float softcap, inv_softcap;  // draft softcap of the base logits (0: none)
+    // Gated / RNN heads (general kernel): the vector u that W2 multiplies replaces W1[prev]
+    int head;              // DSPARK_HEAD_*
+    int hd;                // backbone hidden size d
+    const float* hpre;     // [B][gamma][m r] hidden-state parts of the pre-activations (m = 1 gated, 3 rnn)
+    const void* Wg;
+    const void* Wc;
+    const void* Wo;        // head weights (w_dtype): gated [r][d + r]; rnn [r][2r + d] each
+    float* head_out;       // [B][gamma][r] the head vectors, or null
 };
 
-size_t sample_smem_bytes(int B, int r, bool mma, bool w2_smem) {
+// Shared memory of the general kernel; a Gated / RNN head adds u [B][r] and, for the RNN head,
+// two state buffers [2][B][r] (fp32).
+size_t sample_smem_bytes(int B, int r, bool mma, bool w2_smem, int head = DSPARK_HEAD_VANILLA) {
     size_t b = sizeof(float) * kRows * kXRow + sizeof(float2) * kRows * kChunks + align_up(sizeof(RowBlock), 16) +
                align_up(sizeof(int) * (size_t)B, 16) + sizeof(float4) * (size_t)B;
     if (mma) {
@@ -69,7 +79,80 @@ size_t sample_smem_bytes(int B, int r, bool mma, bool w2_smem) {
     } else {
         b += sizeof(float) * kRows * (size_t)r;
     }
+    if (head != DSPARK_HEAD_VANILLA) b += sizeof(float) * (size_t)B * r * (head == DSPARK_HEAD_RNN ? 3 : 1);
     return b;
+}
+
+// Head vectors of every request for `step` (all threads of the block; every block computes the
+// same values in the same order, so all tiles use identical u):
+//   gated: u_i = sigmoid(hpre_i + sum_c Wg[i][d + c] e_c) e_i,  e = W1[prev]
+//   rnn:   a_t = hpre_t + sum_c Wt[i][c] s_c + sum_c Wt[i][r + c] e_c  (t = g, c, o),
+//          s'_i = sigmoid(a_g) s_i + (1 - sigmoid(a_g)) tanh(a_c),  u_i = tanh(a_o)
+// (page "03 · DSpark 建模：Markov 与 Confidence", section 3.7; z = [s; W1[x]; h], the h part in hpre).
+template <typename TW>
+__device__ void head_vectors(const SampleArgs& a, int step, const int* prev, float* hu, const float* hs_cur,
+                             float* hs_next) {
+    const int r = a.r, d = a.hd;
+    const TW* W1 = reinterpret_cast<const TW*>(a.W1);
+    const int m = a.head == DSPARK_HEAD_RNN ? 3 : 1;
+    for (int idx = threadIdx.x; idx < a.B * r; idx += kThreads) {
+        const int j = idx / r, i = idx % r;
+        const TW* e = W1 + (size_t)prev[j] * r;
+        const float* hp = a.hpre + ((size_t)j * a.gamma + step) * (size_t)(m * r);
+        float u;
+        if (a.head == DSPARK_HEAD_GATED) {
+            const TW* wr = reinterpret_cast<const TW*>(a.Wg) + (size_t)i * (d + r) + d;
+            float acc = hp[i];
+            for (int c = 0; c < r; ++c) acc = fmaf(load_logit<TW>(wr, c), load_logit<TW>(e, c), acc);
+            u = load_logit<TW>(e, i) / (1.f + expf(-acc));
+        } else {
+            const int w = 2 * r + d;
+            const TW* wg = reinterpret_cast<const TW*>(a.Wg) + (size_t)i * w;
+            const TW* wc = reinterpret_cast<const TW*>(a.Wc) + (size_t)i * w;
+            const TW* wo = reinterpret_cast<const TW*>(a.Wo) + (size_t)i * w;
+            const float* sj = hs_cur + (size_t)j * r;
+            float ag = hp[i], ac = hp[r + i], ao = hp[2 * r + i];
+            for (int c = 0; c < r; ++c) {
+                const float sc = sj[c];
+                ag = fmaf(load_logit<TW>(wg, c), sc, ag);
+                ac = fmaf(load_logit<TW>(wc, c), sc, ac);
+                ao = fmaf(load_logit<TW>(wo, c), sc, ao);
+            }
+            for (int c = 0; c < r; ++c) {
+                const float ec = load_logit<TW>(e, c);
+                ag = fmaf(load_logit<TW>(wg, r + c), ec, ag);
+                ac = fmaf(load_logit<TW>(wc, r + c), ec, ac);
+                ao = fmaf(load_logit<TW>(wo, r + c), ec, ao);
+            }
+            const float g = 1.f / (1.f + expf(-ag));
+            hs_next[(size_t)j * r + i] = g * sj[i] + (1.f - g) * tanhf(ac);
+            u = tanhf(ao);
+        }
+        hu[(size_t)j * r + i] = u;
+        if (a.head_out && j % a.G == (int)blockIdx.x) a.head_out[((size_t)j * a.gamma + step) * r + i] = u;
+    }
+}
+
+// The hidden-state parts of the head pre-activations, for every (request, position): one block
+// per (j, i), a warp per output, the d products split over the lanes.
+//   gated: out[i] = sum_c Wg[i][c] h_c;  rnn: out[t r + i] = sum_c Wt[i][2r + c] h_c (t = g, c, o).
+template <typename TW>
+__global__ void __launch_bounds__(256) head_hidden_kernel(int r, int d, int head, const TW* __restrict__ hidden,
+                                                          const TW* __restrict__ Wg, const TW* __restrict__ Wc,
+                                                          const TW* __restrict__ Wo, float* __restrict__ out) {
+    const int row = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m = head == DSPARK_HEAD_RNN ? 3 : 1;
+    const TW* h = hidden + (size_t)row * d;
+    const int stride = head == DSPARK_HEAD_RNN ? 2 * r + d : d + r;
+    const int off = head == DSPARK_HEAD_RNN ? 2 * r : 0;
+    for (int t = warp; t < m * r; t += 8) {
+        const TW* W = (t < r) ? Wg : (t < 2 * r ? Wc : Wo);
+        const TW* wr = W + (size_t)(t % r) * stride + off;
+        float acc = 0.f;
+        for (int c = lane; c < d; c += 32) acc = fmaf(load_logit<TW>(wr, c), load_logit<TW>(h, c), acc);
+        acc = warp_sum(acc);
+        if (lane == 0) out[(size_t)row * (m * r) + t] = acc;
+    }
 }
 
 // The step's in-chunk uniform of every request (SAMPLE_INCHUNK, draw 0), in .y; the chunk
@@ -101,7 +184,14 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(SampleArgs a) {
     int* prev = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(rb) + align_up(sizeof(RowBlock), 16));
     float4* rnd = reinterpret_cast<float4*>(reinterpret_cast<unsigned char*>(prev) + align_up(sizeof(int) * (size_t)a.B, 16));
     unsigned char* wreg = reinterpret_cast<unsigned char*>(rnd + a.B);
+    // after the W1-row staging of the CUDA-core path: the head vectors and the RNN state
+    float* hu = reinterpret_cast<float*>(wreg + sizeof(float) * kRows * (size_t)a.r);
+    float* hs = hu + (size_t)a.B * a.r;  // [2][B][r]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if constexpr (!kMMA) {
+        if (a.head == DSPARK_HEAD_RNN)
+            for (int idx = tid; idx < a.B * a.r; idx += kThreads) hs[idx] = 0.f;  // s_0 = 0
+    }
 
     ProdArgs pa;
     pa.base = a.base;
@@ -143,6 +233,14 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(SampleArgs a) {
             }
         }
         __syncthreads();
+        if constexpr (!kMMA) {
+            if (a.head != DSPARK_HEAD_VANILLA) {
+                float* s_cur = hs + (size_t)(step & 1) * a.B * a.r;
+                float* s_nxt = hs + (size_t)((step + 1) & 1) * a.B * a.r;
+                head_vectors<TW>(a, step, prev, hu, s_cur, s_nxt);
+                __syncthreads();
+            }
+        }
         for (int tile = blockIdx.x; tile < a.nt; tile += a.G) {
             for (int row0 = 0; row0 < a.B; row0 += kRows) {
                 if (tid < kRows) {
@@ -165,7 +263,10 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(SampleArgs a) {
                     const TW* W1 = reinterpret_cast<const TW*>(a.W1);
                     for (int idx = tid; idx < kRows * a.r; idx += kThreads) {
                         const int q = idx / a.r, k = idx % a.r;
-                        w1s[idx] = (rb->brow[q] >= 0) ? load_logit<TW>(W1, (size_t)rb->prev[q] * a.r + k) : 0.f;
+                        w1s[idx] = (rb->brow[q] >= 0)
+                                       ? (a.head != DSPARK_HEAD_VANILLA ? hu[(size_t)(row0 + q) * a.r + k]
+                                                                        : load_logit<TW>(W1, (size_t)rb->prev[q] * a.r + k))
+                                       : 0.f;
                     }
                 }
                 __syncthreads();
@@ -794,28 +895,26 @@ extern "C" size_t dspark_sample_workspace_size(const dspark_sample_params* p) {
     return sample_workspace_bytes(p);
 }
 
-extern "C" dspark_status dspark_markov_sample_block(const dspark_sample_params* p, const void* base_logits,
-                                                    const void* W1, const void* W2, const int32_t* anchor,
-                                                    int32_t* tokens, float* draft_lse, float* draft_logit_at_tok,
-                                                    void* workspace, size_t ws_bytes, dspark_stream_t stream) {
-    dspark_status st = validate_sample_params(p);
-    if (st != DSPARK_OK) return st;
-    if (!base_logits || !anchor || !tokens || !draft_lse || !draft_logit_at_tok) return DSPARK_ERR_INVALID_ARG;
-    if (p->r > 0 && (!W1 || !W2)) return DSPARK_ERR_INVALID_ARG;
-    if (!workspace || ((uintptr_t)workspace & 255u) || ws_bytes < sample_workspace_bytes(p))
-        return DSPARK_ERR_WORKSPACE;
+namespace {
 
-    const bool mma = markov_use_mma(p);
+// The launch shared by the vanilla and the head entry points (arguments already validated).
+// head: null for the vanilla head; hpre: the head's precomputed hidden-state parts.
+dspark_status sample_block_launch(const dspark_sample_params* p, const dspark_head* head, const float* hpre,
+                                  float* head_vec, const void* base_logits, const void* W1, const void* W2,
+                                  const int32_t* anchor, int32_t* tokens, float* draft_lse,
+                                  float* draft_logit_at_tok, void* workspace, dspark_stream_t stream) {
+    const int hk = head ? head->kind : DSPARK_HEAD_VANILLA;
+    const bool mma = hk == DSPARK_HEAD_VANILLA && markov_use_mma(p);
     const int nt = (p->V + kTS - 1) / kTS;
     int sms = 0;
     if (device_sm_count(&sms) != cudaSuccess) return DSPARK_ERR_CUDA;
-    if (sample_tc_eligible(p, base_logits, W1, W2, sms))
+    if (hk == DSPARK_HEAD_VANILLA && sample_tc_eligible(p, base_logits, W1, W2, sms))
         return launch_sample_tc(p, base_logits, W1, W2, anchor, tokens, draft_lse, draft_logit_at_tok,
                                 sample_ws_layout(p), workspace, reinterpret_cast<cudaStream_t>(stream));
     const size_t esz = p->logits_dtype == DSPARK_BF16 ? 2 : 4;
     const bool vec_ok = ((uintptr_t)base_logits % 16 == 0) && (((size_t)p->V * esz) % 16 == 0);
     // staged path: bf16 logits, tensor-core bias, one tile per block (one block per SM)
-    bool staged = mma && p->logits_dtype == DSPARK_BF16 && vec_ok && ((uintptr_t)W1 % 16 == 0) &&
+    bool staged = mma && hk == DSPARK_HEAD_VANILLA && p->logits_dtype == DSPARK_BF16 && vec_ok && ((uintptr_t)W1 % 16 == 0) &&
                   ((uintptr_t)W2 % 16 == 0) && nt <= sms &&
                   nt <= kMaxStagedTiles;
     bool w2_staged = (size_t)kTS * p->r * 2 <= 128 * 1024;
@@ -824,10 +923,10 @@ extern "C" dspark_status dspark_markov_sample_block(const dspark_sample_params* 
     KernelFn fn = staged ? (p->temperature == 0.f ? pick_staged<true>(p->r) : pick_staged<false>(p->r))
                          : pick_kernel(p, mma);
     bool w2_smem = mma && (size_t)kTS * p->r * 2 <= 128 * 1024 && nt <= sms;
-    size_t smem = sample_smem_bytes(p->B, p->r, mma, w2_smem);
+    size_t smem = sample_smem_bytes(p->B, p->r, mma, w2_smem, hk);
     if (smem > kMaxSmem && w2_smem) {
         w2_smem = false;
-        smem = sample_smem_bytes(p->B, p->r, mma, false);
+        smem = sample_smem_bytes(p->B, p->r, mma, false, hk);
     }
     if (staged) {
         w2_smem = w2_staged;
@@ -872,6 +971,13 @@ extern "C" dspark_status dspark_markov_sample_block(const dspark_sample_params* 
     a.vec_ok = vec_ok;
     a.softcap = p->softcap;
     a.inv_softcap = p->softcap > 0.f ? 1.f / p->softcap : 0.f;
+    a.head = hk;
+    a.hd = head ? head->d : 0;
+    a.hpre = hpre;
+    a.Wg = head ? head->Wg : nullptr;
+    a.Wc = head ? head->Wc : nullptr;
+    a.Wo = head ? head->Wo : nullptr;
+    a.head_out = head_vec;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(workspace, 0, kHeaderBytes + (staged ? sample_slot_bytes(p) : 0), s) != cudaSuccess)
@@ -880,6 +986,77 @@ extern "C" dspark_status dspark_markov_sample_block(const dspark_sample_params* 
     if (cudaLaunchCooperativeKernel((const void*)fn, dim3(G), dim3(threads), args, smem, s) != cudaSuccess)
         return DSPARK_ERR_CUDA;
     return DSPARK_OK;
+}
+
+dspark_status validate_head(const dspark_sample_params* p, const dspark_head* h) {
+    if (!h || p->r < 1 || h->d < 1 || !h->hidden || !h->Wg) return DSPARK_ERR_INVALID_ARG;
+    if (h->kind == DSPARK_HEAD_RNN) {
+        if (!h->Wc || !h->Wo) return DSPARK_ERR_INVALID_ARG;
+    } else if (h->kind != DSPARK_HEAD_GATED) {
+        return DSPARK_ERR_INVALID_ARG;
+    }
+    if (h->d > (1 << 20)) return DSPARK_ERR_UNSUPPORTED;
+    return DSPARK_OK;
+}
+
+size_t head_hpre_bytes(const dspark_sample_params* p, const dspark_head* h) {
+    const size_t m = h->kind == DSPARK_HEAD_RNN ? 3 : 1;
+    return align_up(sizeof(float) * (size_t)p->B * p->gamma * m * p->r, 256);
+}
+
+}  // namespace
+
+extern "C" dspark_status dspark_markov_sample_block(const dspark_sample_params* p, const void* base_logits,
+                                                    const void* W1, const void* W2, const int32_t* anchor,
+                                                    int32_t* tokens, float* draft_lse, float* draft_logit_at_tok,
+                                                    void* workspace, size_t ws_bytes, dspark_stream_t stream) {
+    dspark_status st = validate_sample_params(p);
+    if (st != DSPARK_OK) return st;
+    if (!base_logits || !anchor || !tokens || !draft_lse || !draft_logit_at_tok) return DSPARK_ERR_INVALID_ARG;
+    if (p->r > 0 && (!W1 || !W2)) return DSPARK_ERR_INVALID_ARG;
+    if (!workspace || ((uintptr_t)workspace & 255u) || ws_bytes < sample_workspace_bytes(p))
+        return DSPARK_ERR_WORKSPACE;
+    return sample_block_launch(p, nullptr, nullptr, nullptr, base_logits, W1, W2, anchor, tokens, draft_lse,
+                               draft_logit_at_tok, workspace, stream);
+}
+
+extern "C" size_t dspark_sample_head_workspace_size(const dspark_sample_params* p, const dspark_head* head) {
+    if (validate_sample_params(p) != DSPARK_OK || validate_head(p, head) != DSPARK_OK) return 0;
+    return sample_workspace_bytes(p) + head_hpre_bytes(p, head);
+}
+
+extern "C" dspark_status dspark_markov_sample_block_head(const dspark_sample_params* p, const dspark_head* head,
+                                                         const void* base_logits, const void* W1, const void* W2,
+                                                         const int32_t* anchor, int32_t* tokens, float* draft_lse,
+                                                         float* draft_logit_at_tok, float* head_vec, void* workspace,
+                                                         size_t ws_bytes, dspark_stream_t stream) {
+    dspark_status st = validate_sample_params(p);
+    if (st != DSPARK_OK) return st;
+    if ((st = validate_head(p, head)) != DSPARK_OK) return st;
+    if (!base_logits || !anchor || !tokens || !draft_lse || !draft_logit_at_tok || !W1 || !W2)
+        return DSPARK_ERR_INVALID_ARG;
+    const size_t base_ws = sample_workspace_bytes(p);
+    if (!workspace || ((uintptr_t)workspace & 255u) || ws_bytes < base_ws + head_hpre_bytes(p, head))
+        return DSPARK_ERR_WORKSPACE;
+    if (sample_smem_bytes(p->B, p->r, false, false, head->kind) > kMaxSmem) return DSPARK_ERR_UNSUPPORTED;
+    float* hpre = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + base_ws);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const unsigned rows = (unsigned)((size_t)p->B * p->gamma);
+    if (p->w_dtype == DSPARK_BF16) {
+        head_hidden_kernel<__nv_bfloat16><<<rows, 256, 0, s>>>(
+            p->r, head->d, head->kind, static_cast<const __nv_bfloat16*>(head->hidden),
+            static_cast<const __nv_bfloat16*>(head->Wg), static_cast<const __nv_bfloat16*>(head->Wc),
+            static_cast<const __nv_bfloat16*>(head->Wo), hpre);
+    } else {
+        head_hidden_kernel<float><<<rows, 256, 0, s>>>(p->r, head->d, head->kind,
+                                                       static_cast<const float*>(head->hidden),
+                                                       static_cast<const float*>(head->Wg),
+                                                       static_cast<const float*>(head->Wc),
+                                                       static_cast<const float*>(head->Wo), hpre);
+    }
+    if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+    return sample_block_launch(p, head, hpre, head_vec, base_logits, W1, W2, anchor, tokens, draft_lse,
+                               draft_logit_at_tok, workspace, stream);
 }
 
 // ------------------------------------------------------------------------------------------

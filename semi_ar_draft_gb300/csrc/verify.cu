@@ -54,6 +54,7 @@ struct VerifyArgs {
     float4* jobpart;    // [B][nt]
     int vec_b, vec_t;
     float softcap;  // draft softcap of the base logits (0: none)
+    const float* head_vec;  // [B][gamma][r] head vectors of a Gated / RNN head, or null (W1[prev])
 };
 
 __device__ __forceinline__ int req_len(const VerifyArgs& a, int j) { return a.vlen ? a.vlen[j] : a.gamma; }
@@ -710,7 +711,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_jobs_kernel(VerifyArgs a) 
         const TW* W1 = reinterpret_cast<const TW*>(a.W1);
         for (int idx = tid; idx < kRows * a.r; idx += kThreads) {
             const int q = idx / a.r, k = idx % a.r;
-            w1s[idx] = (rb->brow[q] >= 0) ? load_logit<TW>(W1, (size_t)rb->prev[q] * a.r + k) : 0.f;
+            w1s[idx] = rb->brow[q] < 0 ? 0.f
+                       : a.head_vec ? a.head_vec[((size_t)(row0 + q) * a.gamma + jb[q].y - 1) * a.r + k]
+                                    : load_logit<TW>(W1, (size_t)rb->prev[q] * a.r + k);
         }
         __syncthreads();
     }
@@ -809,23 +812,26 @@ extern "C" size_t dspark_verify_workspace_size(const dspark_sample_params* p, in
     return layout(p).total;
 }
 
-extern "C" dspark_status dspark_verify(const dspark_sample_params* p, const void* base_logits, const void* W1,
-                                       const void* W2, const int32_t* anchor, const int32_t* tokens,
-                                       const float* draft_lse, const float* draft_logit_at_tok,
-                                       const void* target_logits, int gamma_t, const int32_t* verify_len,
-                                       const int32_t* target_row_offsets, int32_t* n_accepted,
-                                       int32_t* correction_token, void* workspace, size_t ws_bytes,
-                                       dspark_stream_t stream) {
+namespace {
+
+// Shared by dspark_verify and dspark_verify_head (head_vec non-null: the CUDA-core bias path
+// reads the head vectors instead of W1 rows).
+dspark_status verify_impl(const dspark_sample_params* p, const void* base_logits, const void* W1,
+                          const float* head_vec, const void* W2, const int32_t* anchor, const int32_t* tokens,
+                          const float* draft_lse, const float* draft_logit_at_tok, const void* target_logits,
+                          int gamma_t, const int32_t* verify_len, const int32_t* target_row_offsets,
+                          int32_t* n_accepted, int32_t* correction_token, void* workspace, size_t ws_bytes,
+                          dspark_stream_t stream) {
     dspark_status st = validate_sample_params(p);
     if (st != DSPARK_OK) return st;
     if (!base_logits || !anchor || !tokens || !draft_lse || !draft_logit_at_tok || !target_logits || !n_accepted ||
         !correction_token)
         return DSPARK_ERR_INVALID_ARG;
-    if (p->r > 0 && (!W1 || !W2)) return DSPARK_ERR_INVALID_ARG;
+    if (p->r > 0 && ((!W1 && !head_vec) || !W2)) return DSPARK_ERR_INVALID_ARG;
     if (!target_row_offsets && gamma_t < 1) return DSPARK_ERR_INVALID_ARG;
     const Layout L = layout(p);
     if (!workspace || ((uintptr_t)workspace & 255u) || ws_bytes < L.total) return DSPARK_ERR_WORKSPACE;
-    const bool mma = markov_use_mma(p);
+    const bool mma = !head_vec && markov_use_mma(p);
 
     VerifyArgs a;
     a.B = p->B;
@@ -866,6 +872,7 @@ extern "C" dspark_status dspark_verify(const dspark_sample_params* p, const void
     a.vec_b = rows16 && ((uintptr_t)base_logits % 16 == 0);
     a.vec_t = rows16 && ((uintptr_t)target_logits % 16 == 0);
     a.softcap = p->softcap;
+    a.head_vec = head_vec;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(workspace, 0, L.zero_bytes, s) != cudaSuccess) return DSPARK_ERR_CUDA;
@@ -896,4 +903,31 @@ extern "C" dspark_status dspark_verify(const dspark_sample_params* p, const void
     if (cudaLaunchKernel((const void*)jobs, dim3(L.nt, L.nrb), dim3(kThreads), args, smem, s) != cudaSuccess)
         return DSPARK_ERR_CUDA;
     return DSPARK_OK;
+}
+
+}  // namespace
+
+extern "C" dspark_status dspark_verify(const dspark_sample_params* p, const void* base_logits, const void* W1,
+                                       const void* W2, const int32_t* anchor, const int32_t* tokens,
+                                       const float* draft_lse, const float* draft_logit_at_tok,
+                                       const void* target_logits, int gamma_t, const int32_t* verify_len,
+                                       const int32_t* target_row_offsets, int32_t* n_accepted,
+                                       int32_t* correction_token, void* workspace, size_t ws_bytes,
+                                       dspark_stream_t stream) {
+    return verify_impl(p, base_logits, W1, nullptr, W2, anchor, tokens, draft_lse, draft_logit_at_tok,
+                       target_logits, gamma_t, verify_len, target_row_offsets, n_accepted, correction_token,
+                       workspace, ws_bytes, stream);
+}
+
+extern "C" dspark_status dspark_verify_head(const dspark_sample_params* p, const void* base_logits,
+                                            const float* head_vec, const void* W2, const int32_t* anchor,
+                                            const int32_t* tokens, const float* draft_lse,
+                                            const float* draft_logit_at_tok, const void* target_logits, int gamma_t,
+                                            const int32_t* verify_len, const int32_t* target_row_offsets,
+                                            int32_t* n_accepted, int32_t* correction_token, void* workspace,
+                                            size_t ws_bytes, dspark_stream_t stream) {
+    if (!p || p->r < 1 || !head_vec) return DSPARK_ERR_INVALID_ARG;
+    return verify_impl(p, base_logits, nullptr, head_vec, W2, anchor, tokens, draft_lse, draft_logit_at_tok,
+                       target_logits, gamma_t, verify_len, target_row_offsets, n_accepted, correction_token,
+                       workspace, ws_bytes, stream);
 }

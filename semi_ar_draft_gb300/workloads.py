@@ -17,6 +17,8 @@ Workloads (all synthetic; the pages run trained models that are not available):
               N(0,1) in bf16 (correlation 0.8), 10% of anchors with keep=0
   b512_sched  B=512, gamma=16, V=151936, r=64, T=1, bf16 base ~N(0,3), target =
               base + N(0,1), confidences Beta(8,2) x 0.93^(i-1), budget 2048
+  heads       (make_head_inputs) hidden states [B, gamma, d] ~N(0,1) and Gated / RNN head
+              weights ~N(0, w_std) in the sampler's weight dtype
 """
 from __future__ import annotations
 
@@ -118,6 +120,24 @@ def b128_r256(device="cpu", data_seed=0, V=VOCAB, B=128) -> SampleWorkload:
 def b512_sched(device="cpu", data_seed=0, V=VOCAB, B=512, budget=2048) -> SampleWorkload:
     return make_sample_workload("b512_sched", B, 16, V, 64, 1.0, device=device, data_seed=data_seed,
                                 conf=True, budget=budget)
+
+
+HEAD_GATED, HEAD_RNN = 1, 2
+
+
+def make_head_inputs(wl: SampleWorkload, kind: int, d: int, *, data_seed: int = 0, w_std: float = 0.2,
+                     h_std: float = 1.0, device=None) -> dict:
+    """Hidden states [B, gamma, d] and the head's weights for workload ``wl`` (its r and
+    weight dtype): gated Wg [r, d + r]; rnn Wg, Wc, Wo [r, 2r + d]."""
+    device = device if device is not None else wl.tensors["base"].device
+    g = _gen(device, 7919 + data_seed)
+    r = wl.r
+    cols = d + r if kind == HEAD_GATED else 2 * r + d
+    out = {"hidden": _normal((wl.B, wl.gamma, d), h_std, g, device).to(wl.w_dtype)}
+    names = ["Wg"] if kind == HEAD_GATED else ["Wg", "Wc", "Wo"]
+    for n in names:
+        out[n] = _normal((r, cols), w_std, g, device).to(wl.w_dtype)
+    return out
 
 
 @dataclass

@@ -94,6 +94,37 @@ def test_host_validation_needs_no_gpu(L):
                            fake, 1 << 20, None) == 1
 
 
+def test_head_host_validation_needs_no_gpu(L):
+    from semi_ar_draft_gb300 import binding as b
+
+    vp = C.c_void_p
+    fake = vp(0x1000)
+    ok = b.params(4, 8, 100, 8, 1.0, 0, 0, 0)
+    gated = b.Head(b.HEAD_GATED, 16, 0x1000, 0x1000, None, None)
+    rnn = b.Head(b.HEAD_RNN, 16, 0x1000, 0x1000, 0x1000, 0x1000)
+    size_g = b.dspark_sample_head_workspace_size(ok, gated)
+    size_r = b.dspark_sample_head_workspace_size(ok, rnn)
+    # the head adds the hidden-state pre-activations: 4 x 8 x (1 or 3) x 8 floats
+    assert size_g >= b.dspark_sample_workspace_size(ok) + 4 * 8 * 8 * 4
+    assert size_r >= b.dspark_sample_workspace_size(ok) + 3 * 4 * 8 * 8 * 4
+    for bad in [b.Head(7, 16, 0x1000, 0x1000, None, None),        # unknown kind
+                b.Head(b.HEAD_GATED, 0, 0x1000, 0x1000, None, None),  # d < 1
+                b.Head(b.HEAD_GATED, 16, None, 0x1000, None, None),    # no hidden state
+                b.Head(b.HEAD_RNN, 16, 0x1000, 0x1000, None, 0x1000)]:  # rnn without Wc
+        assert b.dspark_sample_head_workspace_size(ok, bad) == 0
+        assert L.dspark_markov_sample_block_head(C.byref(ok), C.byref(bad), fake, fake, fake, fake, fake, fake, fake,
+                                                 None, fake, 1 << 20, None) == 1
+    r0 = b.params(4, 8, 100, 0, 1.0, 0, 0, 0)  # a head needs r >= 1
+    assert L.dspark_markov_sample_block_head(C.byref(r0), C.byref(gated), fake, fake, fake, fake, fake, fake, fake,
+                                             None, fake, 1 << 20, None) == 1
+    # workspace one byte short of the head's size
+    assert L.dspark_markov_sample_block_head(C.byref(ok), C.byref(rnn), fake, fake, fake, fake, fake, fake, fake,
+                                             None, fake, size_r - 1, None) == 6
+    # verify_head: head vectors required
+    assert L.dspark_verify_head(C.byref(ok), fake, None, fake, fake, fake, fake, fake, fake, 8, None, None, fake, fake,
+                                fake, 1 << 20, None) == 1
+
+
 def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     import importlib
 
