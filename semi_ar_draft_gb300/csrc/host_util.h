@@ -32,7 +32,7 @@ struct SampleWsLayout {
 };
 SampleWsLayout sample_ws_layout(const dspark_sample_params* p);
 
-// Tensor-core draft sampler (sample_tc.cu): bf16 logits and weights of rank 64, at least
+// Tensor-core draft sampler (sample_tc.cu): bf16 logits and weights of rank 64, 128 or 256, at least
 // kTcMinBatch requests, V % 8 == 0, 16-byte aligned tensors, one vocabulary tile per SM.
 constexpr int kTcMinBatch = 64;
 bool sample_tc_eligible(const dspark_sample_params* p, const void* base, const void* W1, const void* W2, int sms);

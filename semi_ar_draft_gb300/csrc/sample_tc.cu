@@ -1,5 +1,5 @@
 // sample_tc.cu -- Markov-head block sampling on the fifth-generation tensor cores (tcgen05), for
-// batches of many requests with bf16 logits and weights of rank 64.
+// batches of many requests with bf16 logits and weights of rank 64, 128 or 256.
 //
 // Method (P2 "从 DFlash 到 dLLM Self-Spec（三）" section 3.4, VanillaMarkov and the
 // sample_block_tokens loop; P1 "03 · DSpark 建模：Markov 与 Confidence" section 3.7): for
@@ -9,18 +9,21 @@
 // One persistent cooperative kernel; CTA b owns vocabulary tile b (1024 ids) for all gamma steps.
 // Requests go in row blocks of 128 (one TMEM lane each); a unit is one (step, row block).
 //   - z of a unit, D[128 requests x 1024 ids], is computed entirely on the tensor cores, as eight
-//     accumulators of 128 ids in fp32 TMEM columns (four rotating slots = all 512 columns):
-//       bias: D = W1[prev] . W2_rows^T, four kind::f16 MMAs of M = 128, N = 128, K = 16, with A =
-//             the 128 W1 rows of the previous tokens (written into shared memory, swizzled, by the
-//             exchange warps) and B = the accumulator's 128 W2 rows;
+//     accumulators of 128 ids in fp32 TMEM columns (four rotating slots of 128 columns at rank 64;
+//     three at ranks 128 and 256, where the A operand takes the remaining columns):
+//       bias: D = W1[prev] . W2_rows^T, kind::f16 MMAs of M = 128, N = 128, K = 16 over the rank,
+//             with A = the 128 W1 rows of the previous tokens (written by the exchange warps into
+//             shared memory, swizzled, at rank 64, or into tensor memory at ranks 128 and 256) and
+//             B = the accumulator's W2 rows (R / 64 swizzled K-chunks);
 //       base: D += base . I, the accumulator's base logits (bf16, two 3-D copies of 64 ids x 128
 //             requests) as the A operand and a 16 x 16 identity as B: four MMAs of N = 16, K = 16
 //             per copy, each adding 16 ids' base values in fp32.
 //     The operands of each accumulator (its W2 rows, re-read from L2 where W2 is kept with an
 //     evict-last policy, and its base copies, evict-first) arrive by tiled tensor copies (128-byte
-//     swizzle, the K-major MMA layout) in one 48 KB stage of a four-stage ring.  With the four TMEM
-//     accumulators that is eight accumulators of lookahead, so the copies of the next units (they do
-//     not depend on the tokens) run well ahead of the epilogue.
+//     swizzle, the K-major MMA layout) in one stage of a ring, one accumulator per stage (rank 64:
+//     four stages of 48 KB; rank 128: three of 64 KB; rank 256: two of 96 KB).  With the TMEM
+//     accumulators the copies of the next units (they do not depend on the tokens) run ahead of
+//     the epilogue.
 //   - Epilogue: two warpgroups, one per parity of accumulator.  Thread = request: it reads its
 //     lane's 32 columns of a chunk from TMEM (the next chunk's load in flight meanwhile) and forms
 //     the chunk record of the contract with no shuffles: max, the weights 2^(z s - max), their
@@ -51,32 +54,49 @@ constexpr int kTcTile = 1024;                 // ids per CTA (one vocabulary til
 constexpr int kTcRows = 128;                  // requests per row block = MMA M = TMEM lanes
 constexpr int kTcN = 128;                     // ids per accumulator = MMA N of the bias
 constexpr int kTcAccs = kTcTile / kTcN;       // accumulators per unit
-constexpr int kTcTmemSlots = 4;               // 4 x 128 fp32 columns = all 512 TMEM columns
 constexpr int kTcBox = 64;                    // ids per base copy (128 bytes: one swizzle span)
-constexpr int kTcStages = 4;                  // operand ring: one accumulator's W2 rows and base copies per stage
-constexpr int kTcRank = 64;                   // K of the bias (W1 / W2 row = 128 bytes)
 constexpr int kTcThreads = 512;
 constexpr int kTcMaxTiles = 160;              // vocabulary tiles (CTAs) at most
 constexpr int kTcEpiGroups = 2;               // epilogue warpgroups (one partial record each per tile and request)
 constexpr int kTcSlotStride = 16;             // 64-bit words between two requests' maxima (one 128-byte line)
 constexpr int kTcCountStride = 32;            // 32-bit words between two row blocks' arrival counters
-constexpr uint32_t kBoxBytes = kTcBox * kTcRows * 2;       // 16 KB
-constexpr uint32_t kABytes = kTcRows * kTcRank * 2;        // 16 KB
-constexpr uint32_t kW2SubBytes = kTcN * kTcRank * 2;      // W2 rows of one accumulator: 16 KB
-constexpr uint32_t kStageBytes = kW2SubBytes + 2 * kBoxBytes;  // 48 KB
 constexpr uint32_t kIdBytes = 16 * 128;                    // 16 x 16 identity, rows of a 128-byte swizzled tile
 
-// shared memory (offsets from the 1024-byte aligned base)
-constexpr uint32_t kSmRing = 0;                             // [kTcStages] {W2 rows, base box 0, base box 1}
-constexpr uint32_t kSmA = kSmRing + kTcStages * kStageBytes;  // [2]
-constexpr uint32_t kSmId = kSmA + 2 * kABytes;
-constexpr uint32_t kSmBars = kSmId + kIdBytes;
-constexpr int kNumBars = 4 + 2 * kTcStages + 2 * kTcTmemSlots + 2;
-constexpr uint32_t kSmFlags = kSmBars + 8 * kNumBars;
-constexpr uint32_t kSmTotal = kSmFlags + 64;
-constexpr size_t kTcSmemBytes = kSmTotal;  // the dynamic base is 1024-byte aligned (checked at entry)
-static_assert(kStageBytes % 1024 == 0 && kSmA % 1024 == 0, "operand tiles are 1024-byte aligned");
-static_assert(kTcSmemBytes <= 227 * 1024, "shared memory of the tensor-core sampler");
+// Layout for rank R.  Operands are split in K-chunks of 64 (128 bytes per row: one swizzle span).
+// One ring stage holds everything one accumulator (128 ids) needs: its W2 rows as R / 64 tiles of
+// 128 ids x one K-chunk (four MMAs of N = 128, K = 16 each) and its base logits as two copies of
+// 64 ids x 128 requests (four identity MMAs of N = 16 each).  One wait and one release per
+// accumulator keep the MMA thread's own instruction stream short: it shares its scheduler with
+// the epilogue warps, so every instruction it issues costs it several cycles.
+// Shared-memory offsets are from the 1024-byte aligned base.
+template <int R>
+struct TcCfg {
+    static_assert(R == 64 || R == 128 || R == 256, "ranks of the tensor-core sampler");
+    static constexpr int kKChunks = R / 64;
+    static constexpr uint32_t kTileBytes = 16384;                // one tiled copy: 128 rows x 128 bytes
+    static constexpr uint32_t kStageBytes = (kKChunks + 2) * kTileBytes;
+    // A (the W1 rows) sits in shared memory at rank 64; at ranks 128 and 256 it sits in tensor memory
+    // (written by the exchange threads, lane = request), which leaves shared memory to the ring, and
+    // the accumulators keep three 128-column slots.
+    static constexpr bool kATmem = R >= 128;
+    static constexpr int kSlots = kATmem ? 3 : 4;                // accumulator slots of 128 TMEM columns
+    static constexpr uint32_t kACol = kSlots * kTcN;              // first TMEM column of A (tensor-memory A)
+    static constexpr uint32_t kACols = R / 2;                     // columns of one A operand (two bf16 each)
+    static constexpr uint32_t kAChunkBytes = kTcRows * 128;      // one K-chunk of a shared-memory A: 16 KB
+    static constexpr uint32_t kABytes = kATmem ? 0 : kAChunkBytes * kKChunks;
+    static constexpr int kABufs = R == 256 ? 1 : 2;              // A operands in flight
+    static_assert(!kATmem || kACol + kABufs * kACols <= 512, "tensor memory of the A operands");
+    static constexpr int kStages = R == 64 ? 4 : (R == 128 ? 3 : 2);
+    static constexpr uint32_t kSmRing = 0;                       // [kStages] {W2 K-chunks, base copy 0, 1}
+    static constexpr uint32_t kSmA = kSmRing + kStages * kStageBytes;  // [kABufs] {A K-chunks}
+    static constexpr uint32_t kSmId = kSmA + kABufs * kABytes;
+    static constexpr uint32_t kSmBars = kSmId + kIdBytes;
+    static constexpr int kNumBars = 2 * kABufs + 2 * kStages + 2 * kSlots + 2;
+    static constexpr uint32_t kSmFlags = kSmBars + 8 * kNumBars;
+    static constexpr size_t kSmemBytes = kSmFlags + 64;  // the dynamic base is 1024-byte aligned (checked at entry)
+    static_assert(kSmA % 1024 == 0, "operand tiles are 1024-byte aligned");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory of the tensor-core sampler");
+};
 
 struct TcArgs {
     int B, gamma, V, nt, nrb, G;
@@ -84,8 +104,8 @@ struct TcArgs {
     float scale2;         // log2(e) / T (1 when greedy)
     uint64_t seed;
     const uint16_t* base;  // bf16 bits [B, gamma, V]
-    const uint16_t* W1;    // bf16 bits [V, 64]
-    const uint16_t* W2;    // bf16 bits [V, 64]
+    const uint16_t* W1;    // bf16 bits [V, R]
+    const uint16_t* W2;    // bf16 bits [V, R]
     const int32_t* anchor;
     int32_t* tokens;
     float* draft_lse;
@@ -246,10 +266,14 @@ __device__ __forceinline__ void chunk_variates4(uint64_t seed, uint32_t j, uint3
     lnE[3] = log_neg_log_u_2(u01(w.w));
 }
 
-template <bool GREEDY>
+template <int R, bool GREEDY>
 __global__ void __launch_bounds__(kTcThreads, 1)
     sample_tc_kernel(const __grid_constant__ CUtensorMap tm_base, const __grid_constant__ CUtensorMap tm_w2,
                      const TcArgs a) {
+    using C = TcCfg<R>;
+    constexpr int kStages = C::kStages, kABufs = C::kABufs;
+    constexpr uint32_t kSmRing = C::kSmRing, kSmA = C::kSmA, kSmId = C::kSmId, kSmBars = C::kSmBars,
+                       kSmFlags = C::kSmFlags, kStageBytes = C::kStageBytes, kABytes = C::kABytes;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     if (smem_addr(smem_raw) & 1023u) {  // the swizzled tiles need 1024-byte alignment (uniform exit)
         if (threadIdx.x == 0) record_status(&a.hdr->status, DSPARK_ERR_UNSUPPORTED);
@@ -257,13 +281,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     unsigned char* sm = smem_raw;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kSmBars);
-    uint64_t* a_full = bars;                           // [2]
-    uint64_t* a_empty = bars + 2;                      // [2]
-    uint64_t* b_full = bars + 4;                       // [kTcStages]
-    uint64_t* b_empty = b_full + kTcStages;            // [kTcStages]
-    uint64_t* t_full = b_empty + kTcStages;            // [kTcTmemSlots]
-    uint64_t* t_empty = t_full + kTcTmemSlots;         // [kTcTmemSlots]
-    uint64_t* done_bar = t_empty + kTcTmemSlots;
+    uint64_t* a_full = bars;                           // [kABufs]
+    uint64_t* a_empty = bars + kABufs;                 // [kABufs]
+    uint64_t* b_full = bars + 2 * kABufs;              // [kStages]
+    uint64_t* b_empty = b_full + kStages;              // [kStages]
+    constexpr int kSlots = C::kSlots;
+    uint64_t* t_full = b_empty + kStages;              // [kSlots]
+    uint64_t* t_empty = t_full + kSlots;               // [kSlots]
+    uint64_t* done_bar = t_empty + kSlots;
     uint64_t* drain_bar = done_bar + 1;
     int* flags = reinterpret_cast<int*>(sm + kSmFlags);
     volatile int* abort = flags;
@@ -276,15 +301,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int total = a.gamma * a.nrb;
 
     if (tid == 0) {
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kABufs; ++b) {
             mbar_init(&a_full[b], 4);
             mbar_init(&a_empty[b], 1);
         }
-        for (int b = 0; b < kTcStages; ++b) {
+        for (int b = 0; b < kStages; ++b) {
             mbar_init(&b_full[b], 1);
             mbar_init(&b_empty[b], 1);
         }
-        for (int b = 0; b < kTcTmemSlots; ++b) {
+        for (int b = 0; b < kSlots; ++b) {
             mbar_init(&t_full[b], 1);
             mbar_init(&t_empty[b], 4);
         }
@@ -317,21 +342,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tma_prefetch_desc(&tm_base);
             tma_prefetch_desc(&tm_w2);
             const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
-            const int nacc = total * kTcAccs;
-            for (int ga = 0; ga < nacc; ++ga) {  // one stage per accumulator: its W2 rows and base copies
-                const int st = ga % kTcStages, use = ga / kTcStages;
+            const int nstage = total * kTcAccs;
+            for (int gs = 0; gs < nstage; ++gs) {  // one stage per accumulator: its W2 rows and base copies
+                const int st = gs % kStages, use = gs / kStages;
                 if (use > 0 && !mbar_wait_hint_or_abort(&b_empty[st], (uint32_t)((use - 1) & 1), abort,
                                                         &a.hdr->status, a.limit_ns))
                     break;
-                const int u = ga / kTcAccs, acc = ga % kTcAccs;
+                const int u = gs / kTcAccs, acc = gs % kTcAccs;
                 const int s = u / a.nrb, rb = u % a.nrb;
+                const int id0 = tile0 + kTcN * acc;
                 unsigned char* dst = sm + kSmRing + st * kStageBytes;
                 mbar_arrive_expect_tx(&b_full[st], kStageBytes);
-                tma_load_2d(dst, &tm_w2, 0, tile0 + kTcN * acc, &b_full[st], keep);  // W2 stays in L2
-                tma_load_3d(dst + kW2SubBytes, &tm_base, tile0 + kTcN * acc, s, rb * kTcRows, &b_full[st], stream);
-                tma_load_3d(dst + kW2SubBytes + kBoxBytes, &tm_base, tile0 + kTcN * acc + kTcBox, s, rb * kTcRows,
-                            &b_full[st], stream);
-                *nb_issued = ga + 1;
+#pragma unroll
+                for (int kc = 0; kc < C::kKChunks; ++kc)  // W2 stays in L2
+                    tma_load_2d(dst + kc * C::kTileBytes, &tm_w2, 64 * kc, id0, &b_full[st], keep);
+#pragma unroll
+                for (int bx = 0; bx < 2; ++bx)
+                    tma_load_3d(dst + (C::kKChunks + bx) * C::kTileBytes, &tm_base, id0 + kTcBox * bx, s, rb * kTcRows,
+                                &b_full[st], stream);
+                *nb_issued = gs + 1;
             }
         }
         __syncwarp();
@@ -340,42 +369,54 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_bias = umma_idesc_bf16(kTcRows, kTcN);
             constexpr uint32_t idesc_base = umma_idesc_bf16(kTcRows, 16);
+            // descriptors advance by address / 16 in their low bits: 1024 per 16 KB stage, 2 per K-step
             const uint64_t id_desc = umma_desc_sw128(smem_addr(sm + kSmId), 1024);
+            const uint64_t ring_desc = umma_desc_sw128(smem_addr(sm + kSmRing), 1024);
+            const uint64_t a_desc = umma_desc_sw128(smem_addr(sm + kSmA), 1024);
             bool ok = true;
             for (int u = 0; u < total && ok; ++u) {
-                const int ab = u & 1;
-                if (!mbar_wait_hint_or_abort(&a_full[ab], (uint32_t)((u >> 1) & 1), abort, &a.hdr->status, a.limit_ns))
+                const int ab = u % kABufs;
+                if (!mbar_wait_hint_or_abort(&a_full[ab], (uint32_t)((u / kABufs) & 1), abort, &a.hdr->status,
+                                             a.limit_ns))
                     break;
-                const uint32_t as = smem_addr(sm + kSmA + ab * kABytes);
                 for (int acc = 0; acc < kTcAccs && ok; ++acc) {
-                    const int ga = u * kTcAccs + acc, sl = ga % kTcTmemSlots, use = ga / kTcTmemSlots;
+                    const int ga = u * kTcAccs + acc, sl = ga % kSlots, use = ga / kSlots;
                     if (use > 0 && !mbar_wait_hint_or_abort(&t_empty[sl], (uint32_t)((use - 1) & 1), abort,
                                                             &a.hdr->status, a.limit_ns)) {
                         ok = false;
                         break;
                     }
-                    const int st = ga % kTcStages;
-                    if (!mbar_wait_hint_or_abort(&b_full[st], (uint32_t)((ga / kTcStages) & 1), abort, &a.hdr->status,
+                    const int st = ga % kStages;
+                    if (!mbar_wait_hint_or_abort(&b_full[st], (uint32_t)((ga / kStages) & 1), abort, &a.hdr->status,
                                                  a.limit_ns)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t d = tmem + (uint32_t)(sl * kTcN);
-                    const uint32_t stage = smem_addr(sm + kSmRing + st * kStageBytes);
+                    const uint64_t sd = ring_desc + (uint64_t)(st * (int)(kStageBytes >> 4));
 #pragma unroll
-                    for (int k = 0; k < kTcRank / 16; ++k)  // D = W1[prev] . W2_rows^T
-                        umma_bf16(d, umma_desc_sw128(as + 32 * k, 1024), umma_desc_sw128(stage + 32 * k, 1024),
-                                  idesc_bias, k > 0 ? 1u : 0u);
+                    for (int kc = 0; kc < C::kKChunks; ++kc)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {  // D = W1[prev] . W2_rows^T
+                            const uint64_t bd = sd + (uint64_t)(kc * (int)(C::kTileBytes >> 4) + 2 * k);
+                            if constexpr (C::kATmem)
+                                umma_bf16_ts(d, tmem + C::kACol + (uint32_t)ab * C::kACols + 32u * kc + 8u * k, bd,
+                                             idesc_bias, (kc | k) > 0 ? 1u : 0u);
+                            else
+                                umma_bf16(d,
+                                          a_desc + (uint64_t)(ab * (int)(C::kABytes >> 4) +
+                                                              kc * (int)(C::kAChunkBytes >> 4) + 2 * k),
+                                          bd, idesc_bias, (kc | k) > 0 ? 1u : 0u);
+                        }
                     *n_mma = 1;
 #pragma unroll
-                    for (int bh = 0; bh < 2; ++bh) {
-                        const uint32_t bsrc = stage + kW2SubBytes + bh * kBoxBytes;
+                    for (int bx = 0; bx < 2; ++bx)
 #pragma unroll
-                        for (int i = 0; i < kTcBox / 16; ++i)  // D[:, 16i..] += base[:, 16i..] . I
-                            umma_bf16(d + (uint32_t)(64 * bh + 16 * i), umma_desc_sw128(bsrc + 32 * i, 1024), id_desc,
+                        for (int i = 0; i < kTcBox / 16; ++i)  // D[:, 64 bx + 16 i ..] += base[:, 16 i ..] . I
+                            umma_bf16(d + (uint32_t)(kTcBox * bx + 16 * i),
+                                      sd + (uint64_t)((C::kKChunks + bx) * (int)(C::kTileBytes >> 4) + 2 * i), id_desc,
                                       idesc_base, 1u);
-                    }
                     umma_commit(&b_empty[st]);  // the stage is free once these have read it
                     umma_commit(&t_full[sl]);
                 }
@@ -491,9 +532,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const size_t o = (size_t)jj * a.gamma + s;
                 int prev = s == 0 ? a.anchor[jj] : a.tokens[o - 1];
                 prev = min(max(prev, 0), a.V - 1);
-                const uint32_t w1 = __ldg(reinterpret_cast<const uint32_t*>(a.W1 + (size_t)prev * kTcRank) + lane);
-                const uint32_t w2 = __ldg(reinterpret_cast<const uint32_t*>(a.W2 + (size_t)tk * kTcRank) + lane);
-                const float bias = warp_sum(fmaf(bf16_lo(w1), bf16_lo(w2), bf16_hi(w1) * bf16_hi(w2)));
+                const uint32_t* w1r = reinterpret_cast<const uint32_t*>(a.W1 + (size_t)prev * R);
+                const uint32_t* w2r = reinterpret_cast<const uint32_t*>(a.W2 + (size_t)tk * R);
+                float bias = 0.f;
+#pragma unroll
+                for (int q = 0; q < R / 64; ++q) {
+                    const uint32_t w1 = __ldg(w1r + lane + 32 * q), w2 = __ldg(w2r + lane + 32 * q);
+                    bias = fmaf(bf16_lo(w1), bf16_lo(w2), fmaf(bf16_hi(w1), bf16_hi(w2), bias));
+                }
+                bias = warp_sum(bias);
                 if (lane == 0) {
                     a.draft_lse[o] = m == -CUDART_INF_F ? -CUDART_INF_F : (m + lg2(sum)) * kLn2;
                     a.zat[o] = bf16_bits_to_f32(__ldg(a.base + o * (size_t)a.V + tk)) + bias;
@@ -516,24 +563,61 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 live = false;
                 break;
             }
-            uint4 w[8];  // the W1 row, loaded before the A buffer is free
-            if (j < a.B) {
-                const uint4* src = reinterpret_cast<const uint4*>(a.W1 + (size_t)tok * kTcRank);
+            // the W1 row (R / 8 units of 16 bytes) in batches of at most 16 units; the first batch is
+            // loaded before the A buffer is free
+            constexpr int kQ = R / 8, kQB = kQ < 16 ? kQ : 16;
+            const uint4* src = reinterpret_cast<const uint4*>(a.W1 + (size_t)tok * R);
+            uint4 w[kQB];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) w[q] = __ldg(src + q);
-            } else {
+            for (int q = 0; q < kQB; ++q) w[q] = j < a.B ? __ldg(src + q) : make_uint4(0u, 0u, 0u, 0u);
+            // the A buffer was last read by the MMAs of unit u - kABufs
+            if (u >= kABufs && !warp_wait(&a_empty[u % kABufs], (uint32_t)(((u / kABufs) - 1) & 1), abort, a))
+                live = false;
+            if (live && C::kATmem) {  // this thread's TMEM lane, 8 columns per unit of 16 bytes
+                tc_fence_after();
+                const uint32_t ta = tmem + ((uint32_t)(row & ~31) << 16) + C::kACol + (uint32_t)(u % kABufs) * C::kACols;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) w[q] = make_uint4(0u, 0u, 0u, 0u);
-            }
-            // the A buffer was last read by the MMAs of unit u - 2
-            if (u >= 2 && !warp_wait(&a_empty[u & 1], (uint32_t)(((u >> 1) - 1) & 1), abort, a)) live = false;
-            if (live) {
-                unsigned char* ad = sm + kSmA + (u & 1) * kABytes;
+                for (int b0 = 0; b0 < kQ; b0 += kQB) {
+                    if (b0 > 0) {
 #pragma unroll
-                for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(ad + sw128_offset(row, q)) = w[q];
+                        for (int q = 0; q < kQB; ++q)
+                            w[q] = j < a.B ? __ldg(src + b0 + q) : make_uint4(0u, 0u, 0u, 0u);
+                    }
+#pragma unroll
+                    for (int h8 = 0; h8 < kQB / 8; ++h8) {  // 32 columns at a time
+                        uint32_t v[32];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            v[4 * q] = w[8 * h8 + q].x;
+                            v[4 * q + 1] = w[8 * h8 + q].y;
+                            v[4 * q + 2] = w[8 * h8 + q].z;
+                            v[4 * q + 3] = w[8 * h8 + q].w;
+                        }
+                        tmem_st32(ta + 4u * (uint32_t)(b0 + 8 * h8), v);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_local(&a_full[u % kABufs]);
+            } else if (live) {
+                unsigned char* ad = sm + kSmA + (u % kABufs) * kABytes;
+#pragma unroll
+                for (int b0 = 0; b0 < kQ; b0 += kQB) {
+                    if (b0 > 0) {
+#pragma unroll
+                        for (int q = 0; q < kQB; ++q)
+                            w[q] = j < a.B ? __ldg(src + b0 + q) : make_uint4(0u, 0u, 0u, 0u);
+                    }
+#pragma unroll
+                    for (int q = 0; q < kQB; ++q) {  // unit q of the row: K-chunk q / 8, unit q % 8 of it
+                        const int qq = b0 + q;
+                        *reinterpret_cast<uint4*>(ad + (qq >> 3) * C::kAChunkBytes + sw128_offset(row, qq & 7)) = w[q];
+                    }
+                }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) mbar_arrive_local(&a_full[u & 1]);
+                if (lane == 0) mbar_arrive_local(&a_full[u % kABufs]);
             }
             if (bar_red_or(3, 128, !live)) break;
             if (s > 0) owner_stats(s - 1, rb, tok);
@@ -561,10 +645,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bool ok = true;
             for (int ah = 0; ah < kTcAccs / 2; ++ah) {
                 const int acc = 2 * ah + h;
-                const int ga = u * kTcAccs + acc, sl = ga % kTcTmemSlots;
+                const int ga = u * kTcAccs + acc, sl = ga % kSlots;
                 float lnE[4] = {0.f, 0.f, 0.f, 0.f};
                 if (!GREEDY) chunk_variates4(a.seed, (uint32_t)j, i, (uint32_t)(tile * (kTcTile / 128) + acc), lnE);
-                if (!warp_wait(&t_full[sl], (uint32_t)((ga / kTcTmemSlots) & 1), abort, a)) {
+                if (!warp_wait(&t_full[sl], (uint32_t)((ga / kSlots) & 1), abort, a)) {
                     ok = false;
                     break;
                 }
@@ -598,8 +682,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     if (tid == 0 && *abort) {  // copies in flight land before the shared memory goes away
         const int nb = *nb_issued;
-        for (int g = max(0, nb - kTcStages); g < nb; ++g)
-            mbar_wait_bounded(&b_full[g % kTcStages], (uint32_t)((g / kTcStages) & 1), &a.hdr->status, a.limit_ns);
+        for (int g = max(0, nb - kStages); g < nb; ++g)
+            mbar_wait_bounded(&b_full[g % kStages], (uint32_t)((g / kStages) & 1), &a.hdr->status, a.limit_ns);
     }
     if (warp == 1) {
         if (lane == 0 && *n_mma) {  // every MMA issued has completed
@@ -631,7 +715,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 bool sample_tc_eligible(const dspark_sample_params* p, const void* base, const void* W1, const void* W2, int sms) {
     const int nt = (p->V + kTcTile - 1) / kTcTile;
     // (the base logits are added on the tensor cores: a softcap of them needs the other samplers)
-    return p->logits_dtype == DSPARK_BF16 && p->w_dtype == DSPARK_BF16 && p->r == kTcRank && p->B >= kTcMinBatch &&
+    return p->logits_dtype == DSPARK_BF16 && p->w_dtype == DSPARK_BF16 &&
+           (p->r == 64 || p->r == 128 || p->r == 256) && p->B >= kTcMinBatch &&
            p->softcap == 0.f &&
            p->V % 8 == 0 && ((uintptr_t)base % 16) == 0 && ((uintptr_t)W1 % 16) == 0 && ((uintptr_t)W2 % 16) == 0 &&
            nt <= sms && nt <= kTcMaxTiles && tensor_map_encoder() != nullptr;
@@ -655,9 +740,10 @@ dspark_status launch_sample_tc(const dspark_sample_params* p, const void* base_l
             return DSPARK_ERR_UNSUPPORTED;
     }
     {
-        cuuint64_t dims[2] = {(cuuint64_t)kTcRank, (cuuint64_t)p->V};
-        cuuint64_t strides[1] = {(cuuint64_t)kTcRank * 2};
-        cuuint32_t box[2] = {kTcRank, kTcN};
+        // W2 [V, r]: boxes of one K-chunk (64) x the 128 ids of an accumulator
+        cuuint64_t dims[2] = {(cuuint64_t)p->r, (cuuint64_t)p->V};
+        cuuint64_t strides[1] = {(cuuint64_t)p->r * 2};
+        cuuint32_t box[2] = {64, kTcN};
         cuuint32_t es[2] = {1, 1};
         if (enc(&m_w2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W2), dims, strides, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -665,9 +751,25 @@ dspark_status launch_sample_tc(const dspark_sample_params* p, const void* base_l
             return DSPARK_ERR_UNSUPPORTED;
     }
     const bool greedy = p->temperature == 0.f;
-    const void* fn = greedy ? (const void*)sample_tc_kernel<true> : (const void*)sample_tc_kernel<false>;
+    const void* fn = nullptr;
+    size_t smem = 0;
+    switch (p->r) {
+        case 64:
+            fn = greedy ? (const void*)sample_tc_kernel<64, true> : (const void*)sample_tc_kernel<64, false>;
+            smem = TcCfg<64>::kSmemBytes;
+            break;
+        case 128:
+            fn = greedy ? (const void*)sample_tc_kernel<128, true> : (const void*)sample_tc_kernel<128, false>;
+            smem = TcCfg<128>::kSmemBytes;
+            break;
+        case 256:
+            fn = greedy ? (const void*)sample_tc_kernel<256, true> : (const void*)sample_tc_kernel<256, false>;
+            smem = TcCfg<256>::kSmemBytes;
+            break;
+        default: return DSPARK_ERR_UNSUPPORTED;
+    }
     int per_sm = 0;
-    if (prepare_kernel(fn, kTcSmemBytes, kTcThreads, &per_sm) != cudaSuccess || per_sm < 1) return DSPARK_ERR_CUDA;
+    if (prepare_kernel(fn, smem, kTcThreads, &per_sm) != cudaSuccess || per_sm < 1) return DSPARK_ERR_CUDA;
 
     TcArgs a;
     a.B = p->B;
@@ -694,7 +796,7 @@ dspark_status launch_sample_tc(const dspark_sample_params* p, const void* base_l
     a.limit_ns = wait_limit_ns();
     if (cudaMemsetAsync(workspace, 0, L.zeroed, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     void* args[] = {(void*)&m_base, (void*)&m_w2, (void*)&a};
-    if (cudaLaunchCooperativeKernel(fn, dim3(nt), dim3(kTcThreads), args, kTcSmemBytes, s) != cudaSuccess)
+    if (cudaLaunchCooperativeKernel(fn, dim3(nt), dim3(kTcThreads), args, smem, s) != cudaSuccess)
         return DSPARK_ERR_CUDA;
     return DSPARK_OK;
 }

@@ -103,8 +103,9 @@ def test_full_b32_r64():
 
 
 def test_full_b128_r256_sampled_requests():
+    # the tensor-core sampler at rank 256: first and last lanes of each 32-lane TMEM quarter
     wl = W.b128_r256(device="cuda")
-    tally, _ = run_and_compare(wl, requests=[0, 45, 127])
+    tally, _ = run_and_compare(wl, requests=[0, 31, 32, 45, 63, 64, 96, 127])
     tally.check_fraction()
 
 
@@ -133,6 +134,24 @@ def test_tc_shapes(B, gamma, V, T):
                                 planted=2, w_std=0.4)
     tally, _ = run_and_compare(wl)
     tally.check_fraction()
+
+
+@pytest.mark.parametrize("r", [128, 256])
+@pytest.mark.parametrize("B,gamma,V,T", [(200, 3, 5000, 0.8), (128, 4, 3000, 0.0), (64, 2, 2048, 1.3)])
+def test_tc_higher_ranks(r, B, gamma, V, T):
+    # ranks 128 and 256: K-chunked operands, two ring stages per accumulator (N = 64); ragged
+    # vocabularies and a partial row block
+    wl = W.make_sample_workload("tcr", B, gamma, V, r, T, device="cuda", data_seed=r + B, philox_seed=7, planted=2,
+                                w_std=0.25)
+    tally, _ = run_and_compare(wl)
+    tally.check_fraction()
+
+
+def test_tc_rank256_bias_matters():
+    wl = W.make_sample_workload("tcb256", 128, 3, 4096, 256, 0.0, device="cuda", data_seed=9, w_std=0.3)
+    tally, (tok, _, _) = run_and_compare(wl)
+    no_bias = torch.argmax(wl.tensors["base"].float(), dim=-1).to(torch.int32)
+    assert (tok != no_bias).float().mean().item() > 0.5
 
 
 def test_tc_bias_matters_and_deterministic():
