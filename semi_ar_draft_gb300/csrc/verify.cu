@@ -650,7 +650,7 @@ __device__ int block_sample_row(const VerifyArgs& a, const TL* row, int j, int p
 
 template <typename TL, int KS, typename TW>
 __global__ void __launch_bounds__(kThreads, 1) verify_jobs_kernel(VerifyArgs a) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+    extern __shared__ __align__(128) unsigned char smem_raw[];
     float* xbuf = reinterpret_cast<float*>(smem_raw);                 // [kRows][kXRow]: log2-weights
     float2* cstat = reinterpret_cast<float2*>(xbuf + kRows * kXRow);  // [kRows][kChunks]
     RowBlock* rb = reinterpret_cast<RowBlock*>(cstat + kRows * kChunks);
