@@ -53,7 +53,6 @@ struct SampleArgs {
     unsigned long long* slots;  // [gamma][B] packed (key, id) maxima of the staged kernel, kSlotStride words
                                 // apart (one 128-byte line each, so the atomics spread over L2); zeroed per call
     unsigned* rb_count;         // [nrb] grid-wide arrival counters per row block (staged kernel), kCountStride apart
-    int w1_l2;                  // staged kernel: pull W1 rows of each tile into L2 at the start
     uint64_t limit_ns;
     int redundant;  // every block reduces every request (one grid-wide wait per step)
     int w2_smem;
@@ -495,20 +494,13 @@ __device__ __forceinline__ bool helper_should_stop(volatile int* abort, uint64_t
     return __shfl_sync(0xffffffffu, stop, 0) != 0;
 }
 
-// Copy issuer: the W1 rows of this tile into L2 (kept there), then the base rows of every row
-// block as soon as its stage buffer is released (two row blocks ahead of the compute warps).
+// Copy issuer: the base rows of every row block as soon as its stage buffer is released (two row
+// blocks ahead of the compute warps).
 template <int KS>
 __device__ void copy_issuer(const SampleArgs& a, uint16_t* stage, uint64_t* full, uint64_t* empty,
                             volatile int* abort, volatile int* nb_out) {
     const int lane = threadIdx.x & 31;
     const int nrb = (a.B + kRows - 1) / kRows, total = a.gamma * nrb;
-    if (a.w1_l2) {
-        const int tile0 = blockIdx.x * kTS;
-        const uint32_t bytes = (uint32_t)min(kTS, a.V - tile0) * (uint32_t)(16 * KS) * 2u;
-        const unsigned char* w1 = reinterpret_cast<const unsigned char*>(a.W1) + (size_t)tile0 * (16 * KS) * 2;
-        for (uint32_t off = (uint32_t)lane * 4096u; off < bytes; off += 32u * 4096u)
-            prefetch_l2_hint(w1 + off, min(4096u, bytes - off), l2_policy_evict_last());
-    }
     for (int nb = 0; nb < total; ++nb) {
         if (nb >= 2) {
             const uint64_t t0 = global_ns();
@@ -964,7 +956,6 @@ dspark_status sample_block_launch(const dspark_sample_params* p, const dspark_he
     a.rb_count = reinterpret_cast<unsigned*>(ws + WL.counts);
     a.cur_tok = reinterpret_cast<int32_t*>(ws + WL.zeroed);
     a.part = reinterpret_cast<float4*>(ws + WL.part);
-    a.w1_l2 = (size_t)p->V * p->r * 2 <= ((size_t)64 << 20);
     a.limit_ns = wait_limit_ns();
     a.redundant = (size_t)p->B * nt <= 8192 && p->B <= kThreads;
     a.w2_smem = w2_smem;
