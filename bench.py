@@ -456,7 +456,30 @@ def main():
         l1t.append((e0, e1))
     torch.cuda.synchronize()
     l1_us = sorted(a.elapsed_time(b_) * 1e3 for a, b_ in l1t)[len(l1t) // 2]
+    # the draft sampler with a final-logit softcap (s tanh(b / s) on every base logit; s = 30): the
+    # same call as the step's, on the sampler that supports the cap
+    pc = api.make_params(base, W1, wl.T, wl.seed, softcap=30.0)
+    ws_c = binding.workspace(binding.dspark_sample_workspace_size(pc), dev)
+    tok_c = torch.empty_like(tok)
+    lse_c = torch.empty((B, g), device=dev)
+    zat_c = torch.empty((B, g), device=dev)
+    for _ in range(3):
+        binding.dspark_markov_sample_block(pc, base, W1, W2, anchor, tok_c, lse_c, zat_c, ws_c)
+    sc = []
+    for _ in range(20):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush.zero_()
+        e0.record()
+        binding.dspark_markov_sample_block(pc, base, W1, W2, anchor, tok_c, lse_c, zat_c, ws_c)
+        e1.record()
+        sc.append((e0, e1))
+    torch.cuda.synchronize()
+    sc_us = sorted(a.elapsed_time(b_) * 1e3 for a, b_ in sc)[len(sc) // 2]
     line["extras"] = {"tv_l1_loss_us": round(l1_us, 2),
+                      "sample_softcap_us": round(sc_us, 2),
+                      "sample_softcap_frac_of_peak": round(algo["sample"] / (sc_us * 1e-6) / 1e9 / peak, 4),
+                      "sample_softcap": "the step's sampling call with softcap 30 (tanh on every base logit), median "
+                                        "of 20 launches; the same algorithmic bytes as the step's sampler",
                       "theta_schedule_us": round(th_us[len(th_us) // 2], 2),
                       "theta_schedule": f"median of 200 launches over B={B} requests, gamma={g}; not part of the step",
                       "block_logits_us": round(bl_us, 2),
