@@ -20,7 +20,7 @@ from . import workloads as W
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kernel", choices=["sample", "verify", "tv"], required=True)
+    ap.add_argument("--kernel", choices=["sample", "verify", "tv", "logits"], required=True)
     ap.add_argument("--B", type=int, default=512)
     ap.add_argument("--gamma", type=int, default=4)
     ap.add_argument("--V", type=int, default=W.VOCAB)
@@ -41,6 +41,8 @@ def main():
         tok, lse, zat, ws = api.markov_sample_block(t["base"], t["W1"], t["W2"], t["anchor"], args.T, wl.seed)
         if args.kernel == "sample":
             run = lambda: api.markov_sample_block(t["base"], t["W1"], t["W2"], t["anchor"], args.T, wl.seed)  # noqa: E731
+        elif args.kernel == "logits":  # teacher-forced block logits with the drafted tokens as the true ones
+            run = lambda: api.markov_block_logits(t["base"], t["W1"], t["W2"], t["anchor"], tok)  # noqa: E731
         else:
             run = lambda: api.verify(t["base"], t["W1"], t["W2"], t["anchor"], tok, lse, zat, t["target"], args.T,  # noqa: E731
                                      wl.seed)
