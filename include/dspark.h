@@ -60,36 +60,32 @@ enum {
     DSPARK_P_SAMPLE_CHUNK = 1,   /* draft sampling: one uniform per vocabulary chunk (n = chunk index) */
     DSPARK_P_SAMPLE_INCHUNK = 2, /* draft sampling: the in-chunk inverse-CDF uniform (n = 0) */
     DSPARK_P_ACCEPT = 3,        /* verify: the acceptance uniform u_i */
-    DSPARK_P_RESID_TILE = 4,    /* verify: residual draw, per tile */
-    DSPARK_P_RESID_INTILE = 5,  /* verify: residual draw, in tile */
-    DSPARK_P_BONUS_TILE = 6,    /* verify: bonus draw from the next target row, per tile */
-    DSPARK_P_BONUS_INTILE = 7   /* verify: bonus draw, in tile */
+    DSPARK_P_RESID_CHUNK = 4,   /* verify: residual draw, one uniform per vocabulary chunk (n = chunk index) */
+    DSPARK_P_RESID_INCHUNK = 5, /* verify: residual draw, the in-chunk inverse-CDF uniform (n = 0) */
+    DSPARK_P_BONUS_CHUNK = 6,   /* verify: bonus draw from the next target row, per chunk */
+    DSPARK_P_BONUS_INCHUNK = 7  /* verify: bonus draw, in chunk */
 };
 
-/* Vocabulary tile and chunk of the samplers (see "Sampling contracts" below). */
+/* The chunk of the sampling contract below; the kernels split the vocabulary into tiles of
+ * DSPARK_TILE ids (a whole number of chunks), which does not change the draw. */
 #define DSPARK_TILE 1024
 #define DSPARK_CHUNK 32
 
 /*
- * Sampling contracts (the pages never show the body of sample_tokens, P2 section 3.4;
- * any exact categorical draw is lossless, bit-parity needs one fixed definition).
+ * Sampling contract (the pages never show the body of sample_tokens, P2 section 3.4; any exact
+ * categorical draw is lossless, bit-parity needs one fixed definition).  Every draw of the library
+ * -- the draft tokens and verify's residual and bonus corrections -- is the same chunk-Gumbel draw
+ * with its own pair of purposes (CHUNK, INCHUNK):
  *   T == 0: x = argmax_v z_v, lowest index on ties.
- *   Draft sampling (T > 0), chunk-Gumbel: s = z / T; chunks of DSPARK_CHUNK consecutive ids
- *     over the whole vocabulary (the last may be short); LSE_c = log sum_{v in c} e^{s_v};
- *       c* = argmax_c (LSE_c - ln E_c), E_c = -ln U(seed, j, i, SAMPLE_CHUNK, c), lowest c on ties
+ *   T > 0, over log-weights s_v (draft: z / T; residual: log max(0, p - q); bonus: t / T):
+ *     chunks of DSPARK_CHUNK consecutive ids over the whole vocabulary (the last may be short);
+ *     LSE_c = log sum_{v in c} e^{s_v};
+ *       c* = argmax_c (LSE_c - ln E_c), E_c = -ln U(seed, j, i, CHUNK, c), lowest c on ties
  *            (chunks without mass never win);
- *       x  = smallest id v of c* with sum_{w in c*, w <= v} e^{s_w - LSE_c*} > U(.., SAMPLE_INCHUNK, 0),
+ *       x  = smallest id v of c* with sum_{w in c*, w <= v} e^{s_w - LSE_c*} > U(.., INCHUNK, 0),
  *            or, where rounding leaves no crossing, the last id of c* with nonzero mass.
  *     Gumbel-max over chunks picks c with probability proportional to e^{LSE_c}; the in-chunk
  *     uniform is independent of the race, so v follows e^{s_v} inside c: the draw is softmax(s).
- *   Correction draws of dspark_verify (residual, bonus), tile-Gumbel: tiles of DSPARK_TILE ids,
- *     chunks of DSPARK_CHUNK ids inside a tile, weights w_v, LSE of a set = log sum w over it;
- *       t* = argmax_t (LSE_t - ln E_t), E_t = -ln U(.., *_TILE, t), lowest t on ties;
- *       c* = smallest chunk c of t* with sum_{c' <= c} e^{LSE_c' - LSE_t*} > U(.., *_INTILE, 0);
- *       x  = smallest id v of c* with sum_{w in c*, w <= v} e^{log w_v - LSE_c*} > U(.., *_INTILE, 1);
- *       where rounding leaves no crossing: the last chunk (id) with nonzero mass.
- *     Gumbel-max over tiles picks t proportionally to e^{LSE_t}; the two inverse CDFs, on
- *     independent uniforms, pick c and then v proportionally to their masses.
  */
 
 typedef struct {

@@ -23,7 +23,7 @@ import numpy as np
 F32, BF16 = 0, 1
 TILE, CHUNK = 1024, 32  # the library's vocabulary tile and chunk sizes
 P_SAMPLE_CHUNK, P_SAMPLE_INCHUNK, P_ACCEPT = 1, 2, 3
-P_RESID_TILE, P_RESID_INTILE, P_BONUS_TILE, P_BONUS_INTILE, P_ELEM_GUMBEL = 4, 5, 6, 7, 8
+P_RESID_CHUNK, P_RESID_INCHUNK, P_BONUS_CHUNK, P_BONUS_INCHUNK, P_ELEM_GUMBEL = 4, 5, 6, 7, 8
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "dspark_oracle.c")
@@ -55,8 +55,6 @@ def lib():
         L.oracle_markov_logits.argtypes = [i32, i32, i32, i32, vp, vp, vp, i32, dbl, vp]
         L.oracle_argmax.argtypes = [vp, i32, vp]
         L.oracle_argmax.restype = i32
-        L.oracle_tile_gumbel.argtypes = [vp, i32, i32, i32, u64, i32, i32, i32, i32, vp, vp]
-        L.oracle_tile_gumbel.restype = i32
         L.oracle_chunk_gumbel.argtypes = [vp, i32, i32, u64, i32, i32, i32, i32, vp, vp]
         L.oracle_chunk_gumbel.restype = i32
         L.oracle_gumbel_elem.argtypes = [vp, i32, u64, i32, i32, vp]
@@ -76,7 +74,7 @@ def lib():
         L.oracle_schedule.restype = i32
         L.oracle_theta_schedule.argtypes = [i32, vp, vp, vp, vp]
         L.oracle_theta_schedule.restype = i32
-        L.oracle_trials_sampler.argtypes = [i32, i32, i32, vp, u64, i64, i32, vp]
+        L.oracle_trials_sampler.argtypes = [i32, i32, vp, u64, i64, i32, vp]
         L.oracle_trials_spec_one.argtypes = [i32, i32, i32, dbl, vp, vp, u64, i64, vp, vp]
         L.oracle_trials_spec_block.argtypes = [i32, i32, i32, i32, i32, dbl, vp, vp, vp, i32, vp, u64, i64, vp]
         _lib = L
@@ -154,18 +152,10 @@ def argmax(z: np.ndarray):
     return int(x), float(m[0])
 
 
-def tile_gumbel(lw: np.ndarray, TS: int, seed: int, j: int, i: int, p_tile=P_RESID_TILE, p_intile=P_RESID_INTILE,
-                CS: int = CHUNK):
-    """The tile-Gumbel draw of the residual / bonus corrections.  Returns (x, margin, lse)."""
-    lw = np.ascontiguousarray(lw, dtype=np.float64)
-    m, lse = np.zeros(1), np.zeros(1)
-    x = lib().oracle_tile_gumbel(_p(lw), lw.shape[0], TS, CS, seed, j, i, p_tile, p_intile, _p(m), _p(lse))
-    return int(x), float(m[0]), float(lse[0])
-
-
 def chunk_gumbel(lw: np.ndarray, seed: int, j: int, i: int, CS: int = CHUNK, p_chunk=P_SAMPLE_CHUNK,
                  p_inchunk=P_SAMPLE_INCHUNK):
-    """The chunk-Gumbel draw of the draft sampler.  Returns (x, margin, lse)."""
+    """The chunk-Gumbel draw (the draft sampler's purposes by default; verify's corrections use the
+    RESID / BONUS purposes).  Returns (x, margin, lse)."""
     lw = np.ascontiguousarray(lw, dtype=np.float64)
     m, lse = np.zeros(1), np.zeros(1)
     x = lib().oracle_chunk_gumbel(_p(lw), lw.shape[0], CS, seed, j, i, p_chunk, p_inchunk, _p(m), _p(lse))
@@ -316,10 +306,12 @@ def theta_schedule(c, sps, with_margin: bool = False):
 
 
 # ----------------------------------------------------------------- trial drivers
-def trials_sampler(lw, TS, seed, ntrials, variant=0, CS: int = CHUNK):
+def trials_sampler(lw, seed, ntrials, variant=0, CS: int = CHUNK):
+    """Draw counts over ntrials (trial n = request n): variant 0 = chunk-Gumbel with the correction
+    purposes, 1 = per-element Gumbel-max, 2 = chunk-Gumbel with the sampling purposes."""
     lw = np.ascontiguousarray(lw, dtype=np.float64)
     counts = np.zeros(lw.shape[0], dtype=np.int64)
-    lib().oracle_trials_sampler(lw.shape[0], TS, CS, _p(lw), seed, int(ntrials), int(variant), _p(counts))
+    lib().oracle_trials_sampler(lw.shape[0], CS, _p(lw), seed, int(ntrials), int(variant), _p(counts))
     return counts
 
 

@@ -40,10 +40,10 @@
 #define OR_P_SAMPLE_CHUNK 1
 #define OR_P_SAMPLE_INCHUNK 2
 #define OR_P_ACCEPT 3
-#define OR_P_RESID_TILE 4
-#define OR_P_RESID_INTILE 5
-#define OR_P_BONUS_TILE 6
-#define OR_P_BONUS_INTILE 7
+#define OR_P_RESID_CHUNK 4
+#define OR_P_RESID_INCHUNK 5
+#define OR_P_BONUS_CHUNK 6
+#define OR_P_BONUS_INCHUNK 7
 #define OR_P_ELEM_GUMBEL 8
 
 /* ------------------------------------------------------------------ */
@@ -145,29 +145,12 @@ static double logsumexp(const double* lw, int n) {
     return m + log(s);
 }
 
-/* Exponential variate E = -ln U for the race between tiles. */
+/* Exponential variate E = -ln U for the race between chunks. */
 static double neg_log_u(double u) { return -log(u); }
 
-/* ------------------------------------------------------------------ */
-/* Tile-Gumbel categorical sampler over log-weights lw[0..V).          */
-/* The pages never show the body of sample_tokens (P2 section 3.4);    */
-/* this is the exact categorical draw fixed for bit-parity:            */
-/*   tiles of TS consecutive ids, chunks of CS consecutive ids inside  */
-/*   a tile; LSE of a set = log sum e^lw over it;                      */
-/*   t* = argmax_t LSE_t - ln E_t, E_t = -ln U(.., p_tile, t)          */
-/*   (lowest t on ties; tiles without mass never win);                 */
-/*   c* = smallest chunk of t* whose in-order cumulative mass          */
-/*   sum_{c'<=c} e^(LSE_c' - LSE_t*) exceeds u1 = U(.., p_intile, 0);  */
-/*   x  = smallest id of c* whose in-order cumulative mass             */
-/*   sum_{w<=v} e^(lw_w - LSE_c*) exceeds u2 = U(.., p_intile, 1);     */
-/*   where rounding leaves no crossing, the last chunk (id) with mass. */
-/* Gumbel-max over tiles gives P(t) proportional to e^LSE_t; the two   */
-/* inverse CDFs (independent uniforms) give P(c | t) proportional to   */
-/* e^LSE_c and P(v | c) proportional to e^lw_v: the product is         */
-/* softmax(lw).  Returns x; *lse_all = log-sum-exp of all lw;          */
-/* *margin = min(tile-key gap, distance of u1 to the chunk CDF         */
-/* boundaries around c*, distance of u2 to the id CDF boundaries).     */
-/* ------------------------------------------------------------------ */
+/* In-order inverse CDF of u over n log-weights normalised by lse: the smallest k whose cumulative
+ * mass exceeds u; where rounding leaves no crossing, the last k with mass.  *margin = distance of u
+ * to the CDF boundaries around k. */
 static int inverse_cdf(const double* lw, int n, double lse, double u, double* margin) {
     double cum = 0.0, prev_cum = 0.0;
     int last_nz = -1;
@@ -186,60 +169,11 @@ static int inverse_cdf(const double* lw, int n, double lse, double u, double* ma
     return last_nz;
 }
 
-int oracle_tile_gumbel(const double* lw, int V, int TS, int CS, uint64_t seed, int j, int i, int p_tile, int p_intile,
-                       double* margin, double* lse_all) {
-    int nt = (V + TS - 1) / TS;
-    double* lse_t = (double*)malloc(sizeof(double) * (size_t)nt);
-    for (int t = 0; t < nt; ++t) {
-        int lo = t * TS, n = (lo + TS <= V) ? TS : V - lo;
-        lse_t[t] = logsumexp(lw + lo, n);
-    }
-    if (lse_all) *lse_all = logsumexp(lse_t, nt);
-    int best = -1;
-    double best_key = -INFINITY, second_key = -INFINITY;
-    for (int t = 0; t < nt; ++t) {
-        if (lse_t[t] == -INFINITY) continue;
-        double key = lse_t[t] - log(neg_log_u(oracle_uniform(seed, (uint32_t)j, (uint32_t)i, (uint32_t)p_tile, (uint32_t)t)));
-        if (best < 0 || key > best_key) {
-            if (best >= 0) second_key = best_key;
-            best_key = key;
-            best = t;
-        } else if (key > second_key) {
-            second_key = key;
-        }
-    }
-    if (best < 0) { /* no mass anywhere */
-        free(lse_t);
-        if (margin) *margin = 0.0;
-        return -1;
-    }
-    double m_tile = best_key - second_key; /* +inf when a single tile has mass */
-    double u1 = oracle_uniform(seed, (uint32_t)j, (uint32_t)i, (uint32_t)p_intile, 0u);
-    double u2 = oracle_uniform(seed, (uint32_t)j, (uint32_t)i, (uint32_t)p_intile, 1u);
-    int lo = best * TS, n = (lo + TS <= V) ? TS : V - lo;
-    int nc = (n + CS - 1) / CS;
-    double* lse_c = (double*)malloc(sizeof(double) * (size_t)nc);
-    for (int c = 0; c < nc; ++c) {
-        int clo = lo + c * CS, cn = (c * CS + CS <= n) ? CS : n - c * CS;
-        lse_c[c] = logsumexp(lw + clo, cn);
-    }
-    double m_chunk, m_id;
-    int c = inverse_cdf(lse_c, nc, lse_t[best], u1, &m_chunk);
-    int clo = lo + c * CS, cn = (c * CS + CS <= n) ? CS : n - c * CS;
-    int k = inverse_cdf(lw + clo, cn, lse_c[c], u2, &m_id);
-    if (margin) {
-        double mg = m_tile < m_chunk ? m_tile : m_chunk;
-        *margin = mg < m_id ? mg : m_id;
-    }
-    free(lse_t);
-    free(lse_c);
-    return clo + k;
-}
-
 /* ------------------------------------------------------------------ */
 /* Chunk-Gumbel categorical sampler over log-weights lw[0..V): the     */
-/* draft sampler's contract (the body of sample_tokens is not shown,   */
-/* P2 section 3.4; any exact categorical draw is lossless).            */
+/* contract of every draw, the draft sampler's and verify's residual   */
+/* and bonus corrections (the body of sample_tokens is not shown, P2   */
+/* section 3.4; any exact categorical draw is lossless).               */
 /*   chunks of CS consecutive ids over the whole vocabulary (the last  */
 /*   one may be short); LSE_c = log sum_{v in c} e^lw_v;               */
 /*   c* = argmax_c LSE_c - ln E_c, E_c = -ln U(.., p_chunk, c), lowest */
@@ -540,10 +474,10 @@ int oracle_verify_request(int V, int r, int gamma, int gamma_t, int TS, int CS, 
                 }
                 double mg;
                 if (any) {
-                    *correction = oracle_tile_gumbel(z, V, TS, CS, seed, j, i, OR_P_RESID_TILE, OR_P_RESID_INTILE, &mg, NULL);
+                    *correction = oracle_chunk_gumbel(z, V, CS, seed, j, i, OR_P_RESID_CHUNK, OR_P_RESID_INCHUNK, &mg, NULL);
                 } else { /* p == q everywhere yet a float rejection: fall back to p */
                     if (resid_fallback) *resid_fallback = 1;
-                    *correction = oracle_tile_gumbel(lw, V, TS, CS, seed, j, i, OR_P_RESID_TILE, OR_P_RESID_INTILE, &mg, NULL);
+                    *correction = oracle_chunk_gumbel(lw, V, CS, seed, j, i, OR_P_RESID_CHUNK, OR_P_RESID_INCHUNK, &mg, NULL);
                 }
                 if (mg < mm) mm = mg;
                 free(z);
@@ -560,7 +494,7 @@ int oracle_verify_request(int V, int r, int gamma, int gamma_t, int TS, int CS, 
             *correction = oracle_argmax(tl, V, &mg);
         } else {
             for (int v = 0; v < V; ++v) lw[v] = tl[v] / T;
-            *correction = oracle_tile_gumbel(lw, V, TS, CS, seed, j, i, OR_P_BONUS_TILE, OR_P_BONUS_INTILE, &mg, NULL);
+            *correction = oracle_chunk_gumbel(lw, V, CS, seed, j, i, OR_P_BONUS_CHUNK, OR_P_BONUS_INCHUNK, &mg, NULL);
         }
         if (mg < mm) mm = mg;
     }
@@ -719,14 +653,14 @@ int oracle_theta_schedule(int gamma, const double* c, const double* sps, double*
 /* ------------------------------------------------------------------ */
 /* Trial loops for the chi-square pins (thin drivers of the above).    */
 /* ------------------------------------------------------------------ */
-/* variant 0: tile-Gumbel with tile size TS and chunk size CS (the residual / bonus draws of
- * verify); 1: per-element Gumbel-max; 2: chunk-Gumbel with chunk size CS (the draft sampler).
- * Trial n uses request index j = n, position i = 1. */
-void oracle_trials_sampler(int V, int TS, int CS, const double* lw, uint64_t seed, long ntrials, int variant,
+/* variant 0: chunk-Gumbel with chunk size CS and the residual purposes (verify's corrections);
+ * 1: per-element Gumbel-max; 2: chunk-Gumbel with chunk size CS and the sampling purposes (the
+ * draft sampler).  Trial n uses request index j = n, position i = 1. */
+void oracle_trials_sampler(int V, int CS, const double* lw, uint64_t seed, long ntrials, int variant,
                            int64_t* counts) {
     for (int v = 0; v < V; ++v) counts[v] = 0;
     for (long n = 0; n < ntrials; ++n) {
-        int x = variant == 0   ? oracle_tile_gumbel(lw, V, TS, CS, seed, (int)n, 1, OR_P_RESID_TILE, OR_P_RESID_INTILE, NULL, NULL)
+        int x = variant == 0   ? oracle_chunk_gumbel(lw, V, CS, seed, (int)n, 1, OR_P_RESID_CHUNK, OR_P_RESID_INCHUNK, NULL, NULL)
                 : variant == 1 ? oracle_gumbel_elem(lw, V, seed, (int)n, 1, NULL)
                                : oracle_chunk_gumbel(lw, V, CS, seed, (int)n, 1, OR_P_SAMPLE_CHUNK, OR_P_SAMPLE_INCHUNK, NULL, NULL);
         counts[x] += 1;

@@ -7,9 +7,9 @@
 // log2-weights (draft sampling, residual or bonus draw) and reduces every chunk to
 //   {max log2-weight m_c, sum 2^(l - m_c)}
 // (greedy: {max value, lowest argmax}); the values go to a shared-memory row buffer.
-// finalize_tile() turns a row's 32 chunk statistics into the tile record of the sampling
-// contract (dspark.h): the Gumbel key, the tile's log-mass, the chunk chosen by u1 and the id
-// chosen by u2 inside it -- before the winning tile is known (the draw is speculative per tile).
+// finalize_tile_cg() turns a row's 32 chunk statistics into the tile record of the chunk-Gumbel
+// contract (dspark.h): the best chunk key of the tile, the tile's log-mass, and the in-chunk
+// inverse-CDF candidate of the winning chunk -- before the winning tile is known.
 #pragma once
 
 #include "common.cuh"
@@ -777,10 +777,12 @@ __device__ __forceinline__ float4 reduce_row_chunks(const float4* crow, bool gre
 // chunk statistics and its buffered z values xrow (weights 2^(x * lscale)):
 // {max over chunks of LSE_c - ln E_c, the tile's log-mass, the candidate of the winning chunk by
 // the in-chunk inverse CDF of u, z at it}; greedy: {max, NaN, argmax id, max}.  The chunk
-// variates are drawn here (one Philox call per lane, draw n = global chunk index).
+// variates are drawn here (one Philox call per lane, draw n = global chunk index, purpose p_chunk:
+// the draft draw's or a verify correction's).
 // --------------------------------------------------------------------------------------------
 __device__ __forceinline__ float4 finalize_tile_cg(const float* xrow, float2 cs, int tile, int V, int greedy,
-                                                   float lscale, float u, uint64_t seed, uint32_t j, uint32_t i) {
+                                                   float lscale, float u, uint64_t seed, uint32_t j, uint32_t i,
+                                                   uint32_t p_chunk) {
     const int lane = threadIdx.x & 31;
     const int tile0 = tile * kTS;
     const bool valid = tile0 + kCS * lane < V;
@@ -792,7 +794,7 @@ __device__ __forceinline__ float4 finalize_tile_cg(const float* xrow, float2 cs,
     }
     const float mc = valid ? cs.x : -CUDART_INF_F;
     const float sc = valid ? cs.y : 0.f;
-    const float lnE = log_neg_log_u(uniform(seed, j, i, DSPARK_P_SAMPLE_CHUNK, (uint32_t)(tile * kChunks + lane)));
+    const float lnE = log_neg_log_u(uniform(seed, j, i, p_chunk, (uint32_t)(tile * kChunks + lane)));
     float key = (sc > 0.f) ? (mc + lg2(sc)) * kLn2 - lnE : -CUDART_INF_F;
     int who = lane;
 #pragma unroll
@@ -826,60 +828,6 @@ __device__ __forceinline__ float4 finalize_tile_cg(const float* xrow, float2 cs,
     }
     const float zv = __shfl_sync(0xffffffffu, xv, xl);
     return make_float4(key, lmass, __int_as_float(tile0 + kCS * who + xl), zv);
-}
-
-// --------------------------------------------------------------------------------------------
-// Tile record of one row (one warp, lane = chunk) from its 32 chunk statistics and its
-// buffered values xrow (weights 2^(x * lscale): lscale = log2(e)/T for z, 1 for log2-weights).
-// T > 0: {key = ln(mass_t) - ln E_t, ln(mass_t), candidate id, buffered value at it}: the chunk
-// by u1 over the chunk masses, the id by u2 inside that chunk;
-// greedy: {max, NaN, argmax id, max}.  A tile without mass gets key -inf and candidate -1.
-// --------------------------------------------------------------------------------------------
-__device__ __forceinline__ float4 finalize_tile(const float* xrow, float2 cs, int tile, int V, int greedy, float lscale,
-                                                float u1, float u2, float lnE) {
-    const int lane = threadIdx.x & 31;
-    const int tile0 = tile * kTS;
-    const bool valid = tile0 + kCS * lane < V;
-    if (greedy) {
-        float m = valid ? cs.x : -CUDART_INF_F;
-        int idx = valid ? __float_as_int(cs.y) : 0x7fffffff;
-        warp_argmax(m, idx);
-        return make_float4(m, CUDART_NAN_F, __int_as_float(idx), m);
-    }
-    const float mc = valid ? cs.x : -CUDART_INF_F;
-    const float sc = valid ? cs.y : 0.f;
-    const float mt = warp_max(mc);
-    if (mt == -CUDART_INF_F) return make_float4(-CUDART_INF_F, -CUDART_INF_F, __int_as_float(-1), 0.f);
-    const float w = (sc > 0.f) ? sc * ex2(mc - mt) : 0.f;
-    const float P = warp_incl_scan(w);
-    const float St = __shfl_sync(0xffffffffu, P, 31);
-    if (!(St > 0.f)) return make_float4(-CUDART_INF_F, -CUDART_INF_F, __int_as_float(-1), 0.f);
-    const float lmass = (mt + lg2(St)) * kLn2;
-    const unsigned hit = __ballot_sync(0xffffffffu, P > u1 * St);
-    int cstar;
-    if (hit) {
-        cstar = __ffs(hit) - 1;
-    } else {
-        const unsigned nz = __ballot_sync(0xffffffffu, w > 0.f);
-        cstar = nz ? 31 - __clz(nz) : 0;
-    }
-    // id by u2 inside chunk cstar (masses relative to its own maximum)
-    const float mcs = __shfl_sync(0xffffffffu, mc, cstar);
-    const int vl = kCS * cstar + lane;
-    const float xv = xrow[vl];
-    const float e = (tile0 + vl < V) ? ex2(xv * lscale - mcs) : 0.f;
-    const float Q = warp_incl_scan(e);
-    const float Sc = __shfl_sync(0xffffffffu, Q, 31);
-    const unsigned hit2 = __ballot_sync(0xffffffffu, Q > u2 * Sc);
-    int xl;
-    if (hit2) {
-        xl = __ffs(hit2) - 1;
-    } else {
-        const unsigned nz = __ballot_sync(0xffffffffu, e > 0.f);
-        xl = nz ? 31 - __clz(nz) : 0;
-    }
-    const float xc = __shfl_sync(0xffffffffu, xv, xl);
-    return make_float4(lmass - lnE, lmass, __int_as_float(tile0 + kCS * cstar + xl), xc);
 }
 
 // Running reduction of tile records: the highest key wins (lowest tile on ties); the tiles'

@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(SampleArgs a) {
                     if (j >= a.B) continue;
                     const float4 rec = finalize_tile_cg(xbuf + rl * kXRow, cstat[rl * kChunks + lane], tile, a.V,
                                                         GREEDY, a.scale2, rb->u2[rl], a.seed, (uint32_t)j,
-                                                        (uint32_t)step + 1u);
+                                                        (uint32_t)step + 1u, DSPARK_P_SAMPLE_CHUNK);
                     if (lane == 0) part[(size_t)j * a.nt + tile] = rec;
                 }
                 __syncthreads();

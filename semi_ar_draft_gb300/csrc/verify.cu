@@ -566,84 +566,56 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_rows_ws_kernel(VerifyArgs
 }
 
 // ------------------------------------------------------------------------------- launch 2
-// Whole-block draw from softmax(target row / T) with the RESID purposes and the sampling
-// contract (tile by Gumbel race, chunk by u1, id by u2): the fallback when a residual
+// Whole-block draw from softmax(target row / T) with the RESID purposes and the chunk-Gumbel
+// contract (a warp per chunk: lane = id; the chunk's key LSE_c - ln E_c, its in-chunk inverse-CDF
+// candidate; the best key over the block, the lowest chunk on ties): the fallback when a residual
 // max(0, p - q) has no mass at all.  sh: 64 floats of shared scratch.
 template <typename TL>
 __device__ int block_sample_row(const VerifyArgs& a, const TL* row, int j, int pos, float* sh) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    float2* red = reinterpret_cast<float2*>(sh);  // sh[0..15]
-    float* cmass = sh + 16;                       // sh[16..47]
-    float* misc = sh + 48;                        // sh[48..63]
-    constexpr int per = kTS / kThreads;           // ids per thread, in id order
-    constexpr int tpc = kCS / per;                // threads per 32-id chunk
-    static_assert(kCS % per == 0 && tpc <= 32 && (tpc & (tpc - 1)) == 0, "a chunk's threads share a warp");
-    static_assert(kTS / kCS <= 32, "chunk masses of a tile fit sh[16..47]");
-    float best_key = -CUDART_INF_F, best_m = 0.f;
-    int best_t = 0;
-    for (int t = 0; t < a.nt; ++t) {
-        float x[per];
-        float m = -CUDART_INF_F;
-#pragma unroll
-        for (int e = 0; e < per; ++e) {
-            const int v = t * kTS + per * tid + e;
-            x[e] = v < a.V ? load_logit<TL>(row, (size_t)v) * a.scale2 : -CUDART_INF_F;
-            m = fmaxf(m, x[e]);
+    const float u = uniform(a.seed, (uint32_t)j, (uint32_t)pos, DSPARK_P_RESID_INCHUNK, 0u);
+    const int nc = (a.V + kCS - 1) / kCS;
+    float bkey = -CUDART_INF_F;
+    int bcand = 0x7fffffff;
+    for (int c = warp; c < nc; c += kWarps) {  // ascending chunks per warp: ties keep the lower one
+        const int v = kCS * c + lane;
+        const float x = v < a.V ? load_logit<TL>(row, (size_t)v) * a.scale2 : -CUDART_INF_F;
+        const float m = warp_max(x);
+        if (m == -CUDART_INF_F) continue;  // (warp-uniform) a chunk without mass never wins
+        const float e = v < a.V ? ex2(x - m) : 0.f;
+        const float Q = warp_incl_scan(e);
+        const float S = __shfl_sync(0xffffffffu, Q, 31);
+        const float key = (m + lg2(S)) * kLn2 - log_neg_log_u(uniform(a.seed, (uint32_t)j, (uint32_t)pos,
+                                                                         DSPARK_P_RESID_CHUNK, (uint32_t)c));
+        const unsigned hit = __ballot_sync(0xffffffffu, Q > u * S);
+        const unsigned nz = __ballot_sync(0xffffffffu, e > 0.f);
+        const int k = hit ? __ffs(hit) - 1 : (nz ? 31 - __clz(nz) : 0);
+        if (key > bkey) {
+            bkey = key;
+            bcand = kCS * c + k;
         }
-        float sum = 0.f;
-        if (m != -CUDART_INF_F)
+    }
+    if (lane == 0) {
+        sh[warp] = bkey;
+        sh[16 + warp] = __int_as_float(bcand);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        float k = lane < kWarps ? sh[lane] : -CUDART_INF_F;
+        int x = lane < kWarps ? __float_as_int(sh[16 + lane]) : 0x7fffffff;
 #pragma unroll
-            for (int e = 0; e < per; ++e) sum += ex2(x[e] - m);
-        const float2 ms = block_lse_pair(m, sum, red);
-        if (tid == 0 && ms.y > 0.f) {
-            const float key = (ms.x + lg2(ms.y)) * kLn2 -
-                              log_neg_log_u(uniform(a.seed, (uint32_t)j, (uint32_t)pos, DSPARK_P_RESID_TILE, (uint32_t)t));
-            if (key > best_key) {
-                best_key = key;
-                best_t = t;
-                best_m = ms.x;
+        for (int o = 16; o >= 1; o >>= 1) {
+            const float ok = __shfl_xor_sync(0xffffffffu, k, o);
+            const int ox = __shfl_xor_sync(0xffffffffu, x, o);
+            if (ok > k || (ok == k && ox < x)) {
+                k = ok;
+                x = ox;
             }
         }
-    }
-    if (tid == 0) {
-        misc[0] = __int_as_float(best_t);
-        misc[1] = best_m;
+        if (lane == 0) sh[32] = __int_as_float(x == 0x7fffffff ? -1 : x);
     }
     __syncthreads();
-    const int t = __float_as_int(misc[0]);
-    const float mt = misc[1];
-    // chunk masses of tile t (tpc consecutive threads per 32-id chunk)
-    float tot = 0.f;
-#pragma unroll
-    for (int e = 0; e < per; ++e) {
-        const int v = t * kTS + per * tid + e;
-        tot += v < a.V ? ex2(load_logit<TL>(row, (size_t)v) * a.scale2 - mt) : 0.f;
-    }
-#pragma unroll
-    for (int o = 1; o < tpc; o <<= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-    if ((tid & (tpc - 1)) == 0) cmass[tid / tpc] = tot;
-    __syncthreads();
-    const uint4 w = philox10(make_uint4(0u, (uint32_t)pos, (uint32_t)j, DSPARK_P_RESID_INTILE), (uint32_t)a.seed,
-                             (uint32_t)(a.seed >> 32));
-    if (warp == 0) {  // chunk by u1
-        const float cw = cmass[lane];
-        const float P = warp_incl_scan(cw);
-        const float S = __shfl_sync(0xffffffffu, P, 31);
-        const unsigned hit = __ballot_sync(0xffffffffu, P > u01(w.x) * S);
-        const unsigned nz = __ballot_sync(0xffffffffu, cw > 0.f);
-        const int c = hit ? __ffs(hit) - 1 : (nz ? 31 - __clz(nz) : 0);
-        // id by u2 inside chunk c, masses relative to the same tile maximum
-        const int v = t * kTS + kCS * c + lane;
-        const float e = v < a.V ? ex2(load_logit<TL>(row, (size_t)v) * a.scale2 - mt) : 0.f;
-        const float Q = warp_incl_scan(e);
-        const float Sc = __shfl_sync(0xffffffffu, Q, 31);
-        const unsigned hit2 = __ballot_sync(0xffffffffu, Q > u01(w.y) * Sc);
-        const unsigned nz2 = __ballot_sync(0xffffffffu, e > 0.f);
-        const int k = hit2 ? __ffs(hit2) - 1 : (nz2 ? 31 - __clz(nz2) : 0);
-        if (lane == 0) misc[2] = __int_as_float(t * kTS + kCS * c + k);
-    }
-    __syncthreads();
-    const int x = __float_as_int(misc[2]);
+    const int x = __float_as_int(sh[32]);
     __syncthreads();
     return x;
 }
@@ -672,21 +644,16 @@ __global__ void __launch_bounds__(kThreads, 1) verify_jobs_kernel(VerifyArgs a) 
         rb->prev[tid] = resid ? q.z : 0;
         rb->brow[tid] = resid ? ((long long)j * a.gamma + q.y - 1) * (long long)a.V : -1;
         rb->trow[tid] = (resid || bonus) ? trow_off(a, j, q.y) : -1;
-        float u1 = 0.f, u2 = 0.f, lnE = 0.f, dl2 = 0.f;
-        if (resid || bonus) {
-            const uint32_t pt = resid ? DSPARK_P_RESID_TILE : DSPARK_P_BONUS_TILE;
-            const uint32_t pi = resid ? DSPARK_P_RESID_INTILE : DSPARK_P_BONUS_INTILE;
-            const uint4 w = philox10(make_uint4(0u, (uint32_t)q.y, (uint32_t)j, pi), (uint32_t)a.seed,
-                                     (uint32_t)(a.seed >> 32));
-            u1 = u01(w.x);
-            u2 = u01(w.y);
-            lnE = log_neg_log_u(uniform(a.seed, (uint32_t)j, (uint32_t)q.y, pt, (uint32_t)tile));
+        float u = 0.f, dl2 = 0.f;
+        if (resid || bonus) {  // the in-chunk uniform of the correction's chunk-Gumbel draw
+            u = uniform(a.seed, (uint32_t)j, (uint32_t)q.y, resid ? DSPARK_P_RESID_INCHUNK : DSPARK_P_BONUS_INCHUNK,
+                        0u);
             if (resid) dl2 = a.dlse[(size_t)j * a.gamma + q.y - 1] * kLog2e;
             atomicOr(&s_any, 1);
         }
-        rb->u1[tid] = u1;
-        rb->u2[tid] = u2;
-        rb->lnE[tid] = lnE;
+        rb->u1[tid] = 0.f;
+        rb->u2[tid] = u;
+        rb->lnE[tid] = 0.f;
         rb->lse2[tid] = __int_as_float(q.w);
         rb->dl2[tid] = dl2;
     }
@@ -722,8 +689,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_jobs_kernel(VerifyArgs a) 
     for (int q = warp; q < kRows; q += kWarps) {
         if (rb->mode[q] == ROW_OFF) continue;
         const int j = row0 + q;
-        const float4 rec = finalize_tile(xbuf + q * kXRow, cstat[q * kChunks + lane], tile, a.V, a.greedy, 1.f,
-                                         rb->u1[q], rb->u2[q], rb->lnE[q]);
+        const float4 rec = finalize_tile_cg(xbuf + q * kXRow, cstat[q * kChunks + lane], tile, a.V, a.greedy, 1.f,
+                                            rb->u2[q], a.seed, (uint32_t)j, (uint32_t)jb[q].y,
+                                            rb->mode[q] == ROW_RESID ? DSPARK_P_RESID_CHUNK : DSPARK_P_BONUS_CHUNK);
         if (lane == 0) a.jobpart[(size_t)j * a.nt + tile] = rec;
     }
     __syncthreads();

@@ -65,16 +65,13 @@ def test_single_chunk_is_inverse_cdf():
     p = special.softmax(lw)
     cdf = np.cumsum(p)
     for j in range(200):
-        # tile contract (residual / bonus draws): one tile, one chunk
-        x, m, lse = O.tile_gumbel(lw, 8, 5, j, 2, CS=8)
-        u2 = O.uniform(5, j, 2, O.P_RESID_INTILE, 1)
-        assert x == int(np.searchsorted(cdf, u2, side="right"))
-        assert abs(lse - special.logsumexp(lw)) < 1e-12
-        # chunk contract (draft sampler): a vocabulary of one chunk
-        x, m, lse = O.chunk_gumbel(lw, 5, j, 2, CS=8)
-        u = O.uniform(5, j, 2, O.P_SAMPLE_INCHUNK, 0)
-        assert x == int(np.searchsorted(cdf, u, side="right"))
-        assert abs(lse - special.logsumexp(lw)) < 1e-12
+        # a vocabulary of one chunk: the draft draw and the corrections' draw (their own purposes)
+        for pc, pin in ((O.P_SAMPLE_CHUNK, O.P_SAMPLE_INCHUNK), (O.P_RESID_CHUNK, O.P_RESID_INCHUNK),
+                        (O.P_BONUS_CHUNK, O.P_BONUS_INCHUNK)):
+            x, m, lse = O.chunk_gumbel(lw, 5, j, 2, CS=8, p_chunk=pc, p_inchunk=pin)
+            u = O.uniform(5, j, 2, pin, 0)
+            assert x == int(np.searchsorted(cdf, u, side="right"))
+            assert abs(lse - special.logsumexp(lw)) < 1e-12
 
 
 def test_chunk_race_then_inverse_cdf():
@@ -105,27 +102,21 @@ def test_chunk_sampler_skips_zero_mass():
     assert O.chunk_gumbel(np.full(5, -np.inf), 1, 0, 1, CS=2)[0] == -1
 
 
-def test_two_level_inverse_cdf_within_a_tile():
-    # one tile of 12 ids in chunks of 4: chunk by u1 over chunk masses, id by u2 within it
+def test_corrections_race_with_their_own_purposes():
+    # the residual draw races chunks on E_c = -ln U(RESID_CHUNK, c) and draws inside the winner with
+    # U(RESID_INCHUNK, 0): the same contract as the draft draw with the other purposes
     rng = np.random.default_rng(14)
     lw = rng.normal(0, 1.0, 12)
-    p = special.softmax(lw)
-    cmass = p.reshape(3, 4).sum(1)
+    lw[5] = -np.inf
+    lse_c = np.array([special.logsumexp(lw[4 * c:4 * c + 4]) for c in range(3)])
     for j in range(300):
-        x, m, lse = O.tile_gumbel(lw, 12, 6, j, 3, CS=4)
-        u1 = O.uniform(6, j, 3, O.P_RESID_INTILE, 0)
-        u2 = O.uniform(6, j, 3, O.P_RESID_INTILE, 1)
-        c = int(np.searchsorted(np.cumsum(cmass), u1, side="right"))
-        k = int(np.searchsorted(np.cumsum(p[4 * c:4 * c + 4] / cmass[c]), u2, side="right"))
-        assert x == 4 * c + k
-
-
-def test_tile_lse_output_and_no_mass_tiles():
-    lw = np.array([-np.inf, -np.inf, 0.3, 1.0, -np.inf, -np.inf, -np.inf, -2.0])
-    for j in range(300):
-        x, m, lse = O.tile_gumbel(lw, 4, 9, j, 1, CS=2)
-        assert np.isfinite(lw[x])  # zero-weight entries are never drawn
-    assert abs(lse - special.logsumexp(lw)) < 1e-12
+        x, m, lse = O.chunk_gumbel(lw, 6, j, 3, CS=4, p_chunk=O.P_RESID_CHUNK, p_inchunk=O.P_RESID_INCHUNK)
+        keys = [lse_c[c] - np.log(-np.log(O.uniform(6, j, 3, O.P_RESID_CHUNK, c))) for c in range(3)]
+        c = int(np.argmax(keys))
+        u = O.uniform(6, j, 3, O.P_RESID_INCHUNK, 0)
+        k = int(np.searchsorted(np.cumsum(special.softmax(lw[4 * c:4 * c + 4])), u, side="right"))
+        assert x == 4 * c + k and np.isfinite(lw[x])
+        assert abs(lse - special.logsumexp(lw)) < 1e-12
 
 
 def _chi2_p(counts, probs):
@@ -134,13 +125,12 @@ def _chi2_p(counts, probs):
 
 
 @pytest.mark.parametrize("T", [0.7, 1.0])
-@pytest.mark.parametrize("TS,CS,variant", [(2, 1, 0), (3, 2, 0), (8, 8, 0), (8, 3, 0), (4, 2, 0), (8, 8, 1),
-                                           (0, 1, 2), (0, 2, 2), (0, 3, 2), (0, 8, 2)])
-def test_samplers_chi_square(T, TS, CS, variant):
+@pytest.mark.parametrize("CS,variant", [(1, 0), (2, 0), (3, 0), (8, 0), (8, 1), (1, 2), (2, 2), (3, 2), (8, 2)])
+def test_samplers_chi_square(T, CS, variant):
     rng = np.random.default_rng(10)
     z = rng.normal(0, 1.2, 8)
     lw = z / T
-    counts = O.trials_sampler(lw, TS, 1234 + TS + 7 * CS, 1_000_000, variant, CS=CS)
+    counts = O.trials_sampler(lw, 1234 + 7 * CS + (5, 8, 0)[variant], 1_000_000, variant, CS=CS)
     assert _chi2_p(counts, special.softmax(lw)) > 1e-3
 
 
@@ -150,7 +140,7 @@ def test_chi_square_detects_a_wrong_law():
     lw = rng.normal(0, 1.2, 8)
     wrong = special.softmax(lw * 1.02)
     for variant in (0, 2):
-        counts = O.trials_sampler(lw, 4, 77, 1_000_000, variant, CS=2)
+        counts = O.trials_sampler(lw, 77, 1_000_000, variant, CS=2)
         assert _chi2_p(counts, wrong) < 1e-6
 
 
