@@ -40,4 +40,33 @@ dspark_status launch_sample_tc(const dspark_sample_params* p, const void* base_l
                                const int32_t* anchor, int32_t* tokens, float* draft_lse, float* draft_logit_at_tok,
                                const SampleWsLayout& L, void* workspace, cudaStream_t s);
 
+// Tensor-core residual / bonus draws of verify (sample_tc.cu): bf16 logits and weights of rank 64,
+// V % 64 == 0, at least kTcMinBatch requests, 16-byte aligned tensors, no softcap, vanilla head.
+// One CTA per vocabulary tile walks row blocks of 128 jobs; each job's base and target rows are
+// gathered four at a time by tensor copies.
+constexpr size_t kVtcLine = 128;  // bytes between two jobs' packed words / two row blocks' counters
+struct VerifyTcArgs {
+    int B, gamma, V, nt, nrb, greedy;
+    float scale2;                 // log2(e) / T (1 when greedy)
+    uint64_t seed;
+    const void* base;             // bf16 [B, gamma, V]
+    const void* target;           // bf16 target rows: dense [B, gamma_t, V] or CSR [target_rows, V]
+    long long target_rows;
+    int gamma_t;                  // dense layout: rows per request (0 with offsets)
+    const int32_t* toff;          // CSR row offsets [B + 1] or null
+    const void* W1;               // bf16 [V, 64]
+    const void* W2;               // bf16 [V, 64]
+    const int4* job;              // [B] {type, 1-based position, prev token, log2-sum-exp bits of the target row}
+    const float* dlse;            // [B, gamma] draft LSE (natural)
+    int32_t* corr;                // [B] corrections (written for RESID / BONUS jobs)
+    int32_t* fb;                  // [B] set where a residual has no mass (zeroed per call)
+    unsigned long long* words;    // [B] packed maxima, kVtcLine apart (zeroed per call)
+    unsigned* rb_count;           // [nrb] arrival counters, kVtcLine apart (zeroed per call)
+    void* hdr;                    // the workspace header (status word)
+    uint64_t limit_ns;
+};
+bool verify_tc_eligible(const dspark_sample_params* p, const void* base, const void* target, const void* W1,
+                        const void* W2);
+dspark_status launch_verify_tc(const VerifyTcArgs& a, cudaStream_t s);
+
 }  // namespace dspark

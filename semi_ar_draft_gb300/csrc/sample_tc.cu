@@ -258,8 +258,9 @@ __device__ __forceinline__ void accumulator_chunks(uint32_t taddr, int id0, int 
 }
 
 // ln E_c of four consecutive chunks 4q .. 4q + 3 (one Philox call, draws n = global chunk index).
-__device__ __forceinline__ void chunk_variates4(uint64_t seed, uint32_t j, uint32_t i, uint32_t q, float (&lnE)[4]) {
-    const uint4 w = philox10(make_uint4(q, i, j, DSPARK_P_SAMPLE_CHUNK), (uint32_t)seed, (uint32_t)(seed >> 32));
+__device__ __forceinline__ void chunk_variates4(uint64_t seed, uint32_t j, uint32_t i, uint32_t q, float (&lnE)[4],
+                                                uint32_t purpose = DSPARK_P_SAMPLE_CHUNK) {
+    const uint4 w = philox10(make_uint4(q, i, j, purpose), (uint32_t)seed, (uint32_t)(seed >> 32));
     lnE[0] = log_neg_log_u_2(u01(w.x));
     lnE[1] = log_neg_log_u_2(u01(w.y));
     lnE[2] = log_neg_log_u_2(u01(w.z));
@@ -798,6 +799,530 @@ dspark_status launch_sample_tc(const dspark_sample_params* p, const void* base_l
     void* args[] = {(void*)&m_base, (void*)&m_w2, (void*)&a};
     if (cudaLaunchCooperativeKernel(fn, dim3(nt), dim3(kTcThreads), args, smem, s) != cudaSuccess)
         return DSPARK_ERR_CUDA;
+    return DSPARK_OK;
+}
+
+// ==========================================================================================
+// Verify's residual and bonus draws on the tensor cores (dspark_verify, the correction draw of
+// the chunk-Gumbel contract).  Method (P3 "Speculative Decoding"; P2 section 3.4): at the first
+// rejection k of request j the correction is drawn from norm(max(0, p - q)), p = softmax(t/T) of
+// target row k and q = softmax(z/T) with z = base[j, k-1] + W2 . W1[prev] rebuilt here; after a
+// fully accepted block the bonus token is drawn from softmax(t/T) of row L_j + 1.
+//
+// One CTA per vocabulary tile (1024 ids) walks row blocks of 128 jobs (one TMEM lane each); the
+// row blocks are independent.  Per accumulator of 128 ids one ring stage holds its W2 rows (one
+// tiled copy) and each job's base and target rows, fetched by tile::gather4 copies (32 lanes x 4
+// rows per 64-id box: every job sits at its own position).  z = base + W1[prev] . W2_rows^T is
+// formed on the tensor cores exactly as in the sampler; the epilogue (thread = job) reads z from
+// TMEM and t from the stage, forms the weights (residual: max(0, 2^(t s - lse2) - 2^(z s - dl2));
+// bonus: 2^(t s - max of the chunk)) and the chunk records, and folds the best into the job's
+// 64-bit word with one atomic max.  The last CTA to finish a row block writes the corrections;
+// a residual with no mass at all is flagged for the whole-row fallback draw from p.
+// ==========================================================================================
+namespace {
+
+enum { VJOB_NONE = 0, VJOB_RESID = 1, VJOB_BONUS = 2 };  // the job types the rows kernel emits
+constexpr uint32_t kVtTile = 16384;                        // 128 rows x 128 bytes
+constexpr uint32_t kVtStageBytes = 5 * kVtTile;            // {W2 rows, base box 0, 1, target box 0, 1}
+constexpr int kVtStages = 2;
+constexpr int kVtSlots = 4;
+constexpr uint32_t kVtSmA = kVtStages * kVtStageBytes;     // [2] A operands (W1 rows of the prevs)
+constexpr uint32_t kVtSmId = kVtSmA + 2 * kVtTile;
+constexpr uint32_t kVtSmBars = kVtSmId + kIdBytes;
+constexpr int kVtNumBars = 4 + 2 * kVtStages + 2 * kVtSlots + 2;
+constexpr uint32_t kVtSmFlags = kVtSmBars + 8 * kVtNumBars;
+constexpr size_t kVtSmemBytes = kVtSmFlags + 64;
+static_assert(kVtSmemBytes <= 227 * 1024, "shared memory of the tensor-core verify kernel");
+constexpr int kVtLineWords = (int)(kVtcLine / 8);
+constexpr int kVtLineInts = (int)(kVtcLine / 4);
+
+__device__ __forceinline__ long long vt_target_row(const VerifyTcArgs& a, int j, int i) {  // i 1-based
+    return a.toff ? (long long)a.toff[j] + i - 1 : (long long)j * a.gamma_t + i - 1;
+}
+
+// The chunk record of one job over 32 ids (t: target values, z: TMEM bits of z; mode: the job's
+// type).  Every lane of the warp calls it for the same chunk (its one vote stays warp-uniform).
+template <bool GREEDY, bool MASK>
+__device__ __forceinline__ void chunk_job(const float (&t)[32], const uint32_t (&zv)[32], int mode, int id0, int V,
+                                          float scale2, float lse2, float dl2, float u, float lnE, float& bkey,
+                                          int& bcand) {
+    if (GREEDY) {  // bonus jobs only: the argmax of the target row, lowest id on ties
+        float m = -CUDART_INF_F;
+        int x = 0;
+#pragma unroll
+        for (int e = 31; e >= 0; --e) {
+            const float v = (MASK && id0 + e >= V) ? -CUDART_INF_F : t[e];
+            if (v >= m) {
+                m = v;
+                x = e;
+            }
+        }
+        if (mode == VJOB_BONUS && m > bkey) {
+            bkey = m;
+            bcand = id0 + x;
+        }
+        return;
+    }
+    uint64_t q[8], r[8];  // weights: q[k] = ids (k, 8 + k), r[k] = ids (16 + k, 24 + k)
+    float ref = 0.f;
+    if (mode == VJOB_RESID) {
+        const uint64_t s2 = pk2(scale2, scale2), nl = pk2(-lse2, -lse2), nd = pk2(-dl2, -dl2);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float2 pa = up2(fma2(pk2(t[k], t[8 + k]), s2, nl));
+            const float2 qa = up2(fma2(pk2(__uint_as_float(zv[k]), __uint_as_float(zv[8 + k])), s2, nd));
+            const float2 pb = up2(fma2(pk2(t[16 + k], t[24 + k]), s2, nl));
+            const float2 qb = up2(fma2(pk2(__uint_as_float(zv[16 + k]), __uint_as_float(zv[24 + k])), s2, nd));
+            float w0 = fmaxf(ex2(pa.x) - ex2(qa.x), 0.f), w1 = fmaxf(ex2(pa.y) - ex2(qa.y), 0.f);
+            float w2 = fmaxf(ex2(pb.x) - ex2(qb.x), 0.f), w3 = fmaxf(ex2(pb.y) - ex2(qb.y), 0.f);
+            if (MASK) {
+                w0 = id0 + k < V ? w0 : 0.f;
+                w1 = id0 + 8 + k < V ? w1 : 0.f;
+                w2 = id0 + 16 + k < V ? w2 : 0.f;
+                w3 = id0 + 24 + k < V ? w3 : 0.f;
+            }
+            q[k] = pk2(w0, w1);
+            r[k] = pk2(w2, w3);
+        }
+    } else if (mode == VJOB_BONUS) {
+        float x[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[e] = (MASK && id0 + e >= V) ? -CUDART_INF_F : t[e];
+        const float m = max32(x) * scale2;
+        ref = m == -CUDART_INF_F ? 0.f : m;
+        const uint64_t s2 = pk2(scale2, scale2), nr = pk2(-ref, -ref);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float2 xa = up2(fma2(pk2(x[k], x[8 + k]), s2, nr));
+            const float2 xb = up2(fma2(pk2(x[16 + k], x[24 + k]), s2, nr));
+            q[k] = pk2(ex2(xa.x), ex2(xa.y));
+            r[k] = pk2(ex2(xb.x), ex2(xb.y));
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) q[k] = r[k] = pk2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 1; k < 8; ++k) {  // inclusive prefix inside each block of eight
+        q[k] = add2(q[k], q[k - 1]);
+        r[k] = add2(r[k], r[k - 1]);
+    }
+    const float2 qe = up2(q[7]), re = up2(r[7]);
+    const float o1 = qe.x, o2 = o1 + qe.y, o3 = o2 + re.x;
+    const float S = o3 + re.y;
+    const float tt = u * S, t1 = tt - o1, t2 = tt - o2, t3 = tt - o3;
+    uint32_t neg = 0;  // minus the number of prefix values not above the target: the crossing index
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float2 qa = up2(q[k]), rb = up2(r[k]);
+        neg += le_mask(qa.x, tt) + le_mask(qa.y, t1) + le_mask(rb.x, t2) + le_mask(rb.y, t3);
+    }
+    int cnt = -(int)neg;
+    if (__any_sync(0xffffffffu, cnt == 32)) {  // rounding left no crossing: the last id with weight
+        if (cnt == 32) {
+            int last = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float2 qa = up2(q[k]), rb = up2(r[k]);
+                const float2 pa = k ? up2(q[k - 1]) : make_float2(0.f, 0.f);
+                const float2 pb = k ? up2(r[k - 1]) : make_float2(0.f, 0.f);
+                last = qa.x > pa.x ? max(last, k) : last;
+                last = qa.y > pa.y ? max(last, 8 + k) : last;
+                last = rb.x > pb.x ? max(last, 16 + k) : last;
+                last = rb.y > pb.y ? max(last, 24 + k) : last;
+            }
+            cnt = last;
+        }
+    }
+    if (S > 0.f) {
+        const float key = (ref + lg2(S)) * kLn2 - lnE;
+        if (key > bkey) {
+            bkey = key;
+            bcand = id0 + cnt;
+        }
+    }
+}
+
+template <bool GREEDY>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    verify_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_base,
+                     const __grid_constant__ CUtensorMap tm_tgt, const VerifyTcArgs a) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(a.hdr);
+    if (smem_addr(smem_raw) & 1023u) {  // the swizzled tiles need 1024-byte alignment (uniform exit)
+        if (threadIdx.x == 0) record_status(&hdr->status, DSPARK_ERR_UNSUPPORTED);
+        return;
+    }
+    unsigned char* sm = smem_raw;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kVtSmBars);
+    uint64_t* a_full = bars;                    // [2]
+    uint64_t* a_empty = bars + 2;               // [2]
+    uint64_t* b_full = bars + 4;                // [kVtStages]
+    uint64_t* b_empty = b_full + kVtStages;     // [kVtStages]: the epilogue has read the stage's target rows
+    uint64_t* t_full = b_empty + kVtStages;     // [kVtSlots]
+    uint64_t* t_empty = t_full + kVtSlots;      // [kVtSlots]
+    uint64_t* done_bar = t_empty + kVtSlots;
+    uint64_t* drain_bar = done_bar + 1;
+    int* flags = reinterpret_cast<int*>(sm + kVtSmFlags);
+    volatile int* abort = flags;
+    int* wg_done = flags + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(flags + 2);
+    volatile int* nb_issued = flags + 3;
+    volatile int* n_mma = flags + 4;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tile = blockIdx.x, tile0 = tile * kTcTile;
+    const int total = a.nrb;
+    const uint64_t lim = a.limit_ns;
+
+    if (tid == 0) {
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&a_full[b], 4);
+            mbar_init(&a_empty[b], 1);
+        }
+        for (int b = 0; b < kVtStages; ++b) {
+            mbar_init(&b_full[b], 1);
+            mbar_init(&b_empty[b], 4);
+        }
+        for (int b = 0; b < kVtSlots; ++b) {
+            mbar_init(&t_full[b], 1);
+            mbar_init(&t_empty[b], 4);
+        }
+        mbar_init(done_bar, 1);
+        mbar_init(drain_bar, 1);
+        for (int f = 0; f < 16; ++f) flags[f] = 0;
+        mbar_init_fence();
+    }
+    if (tid < 128) {  // the identity B operand: row n holds 1.0 at k = n (units 0 and 1 of its row)
+        const int n = tid >> 3, u = tid & 7;
+        const int k = n & 7;
+        const uint32_t one = (u < 2 && (n >> 3) == u) ? ((k & 1) ? 0x3F800000u : 0x00003F80u) : 0u;
+        const int wd = k >> 1;
+        *reinterpret_cast<uint4*>(sm + kVtSmId + sw128_offset(n, u)) =
+            make_uint4(wd == 0 ? one : 0u, wd == 1 ? one : 0u, wd == 2 ? one : 0u, wd == 3 ? one : 0u);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- copies (all 32 lanes)
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_w2);
+            tma_prefetch_desc(&tm_base);
+            tma_prefetch_desc(&tm_tgt);
+        }
+        const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
+        bool live = true;
+        for (int u = 0; u < total && live; ++u) {
+            int br[4], tr[4];  // rows 4 lane .. 4 lane + 3 of the row block: their base and target rows
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int j = u * kTcRows + 4 * lane + k;
+                const int4 q = j < a.B ? a.job[j] : make_int4(VJOB_NONE, 0, 0, 0);
+                const bool resid = q.x == VJOB_RESID, bonus = q.x == VJOB_BONUS;
+                long long b = resid && q.y >= 1 && q.y <= a.gamma ? (long long)j * a.gamma + q.y - 1 : 0;
+                long long t = (resid || bonus) && q.y >= 1 ? vt_target_row(a, j, q.y) : 0;
+                br[k] = (int)b;
+                tr[k] = (t >= 0 && t < a.target_rows) ? (int)t : 0;  // (the rows kernel checked the counts)
+            }
+            for (int acc = 0; acc < kTcAccs; ++acc) {
+                const int ga = u * kTcAccs + acc, st = ga % kVtStages, use = ga / kVtStages;
+                int ok = 1;
+                if (lane == 0 && use > 0)
+                    ok = mbar_wait_hint_or_abort(&b_empty[st], (uint32_t)((use - 1) & 1), abort, &hdr->status, lim) ? 1 : 0;
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                    live = false;
+                    break;
+                }
+                const int id0 = tile0 + kTcN * acc;
+                const int nbox = (id0 < a.V) + (id0 + kTcBox < a.V);  // boxes inside V (V % 64 == 0)
+                unsigned char* dst = sm + st * kVtStageBytes;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&b_full[st], kVtTile + 2u * (uint32_t)nbox * kVtTile);
+                    tma_load_2d(dst, &tm_w2, 0, id0, &b_full[st], keep);  // W2 stays in L2
+                }
+                __syncwarp();
+                for (int bx = 0; bx < nbox; ++bx) {
+                    tma_gather4(dst + (1 + bx) * kVtTile + 512 * lane, &tm_base, id0 + kTcBox * bx, br[0], br[1],
+                                br[2], br[3], &b_full[st], stream);
+                    tma_gather4(dst + (3 + bx) * kVtTile + 512 * lane, &tm_tgt, id0 + kTcBox * bx, tr[0], tr[1],
+                                tr[2], tr[3], &b_full[st], stream);
+                }
+                if (lane == 0) *nb_issued = ga + 1;
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            constexpr uint32_t idesc_bias = umma_idesc_bf16(kTcRows, kTcN);
+            constexpr uint32_t idesc_base = umma_idesc_bf16(kTcRows, 16);
+            const uint64_t id_desc = umma_desc_sw128(smem_addr(sm + kVtSmId), 1024);
+            const uint64_t ring_desc = umma_desc_sw128(smem_addr(sm), 1024);
+            const uint64_t a_desc = umma_desc_sw128(smem_addr(sm + kVtSmA), 1024);
+            bool ok = true;
+            for (int u = 0; u < total && ok; ++u) {
+                const int ab = u & 1;
+                if (!mbar_wait_hint_or_abort(&a_full[ab], (uint32_t)((u >> 1) & 1), abort, &hdr->status, lim)) break;
+                for (int acc = 0; acc < kTcAccs && ok; ++acc) {
+                    const int ga = u * kTcAccs + acc, sl = ga % kVtSlots, use = ga / kVtSlots, st = ga % kVtStages;
+                    if ((use > 0 && !mbar_wait_hint_or_abort(&t_empty[sl], (uint32_t)((use - 1) & 1), abort,
+                                                             &hdr->status, lim)) ||
+                        !mbar_wait_hint_or_abort(&b_full[st], (uint32_t)((ga / kVtStages) & 1), abort, &hdr->status,
+                                                 lim)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem + (uint32_t)(sl * kTcN);
+                    const uint64_t sd = ring_desc + (uint64_t)(st * (int)(kVtStageBytes >> 4));
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)  // D = W1[prev] . W2_rows^T
+                        umma_bf16(d, a_desc + (uint64_t)(ab * (int)(kVtTile >> 4) + 2 * k), sd + 2 * k, idesc_bias,
+                                  k > 0 ? 1u : 0u);
+                    *n_mma = 1;
+#pragma unroll
+                    for (int bx = 0; bx < 2; ++bx)
+#pragma unroll
+                        for (int i = 0; i < kTcBox / 16; ++i)  // D[:, 64 bx + 16 i ..] += base[:, 16 i ..] . I
+                            umma_bf16(d + (uint32_t)(kTcBox * bx + 16 * i),
+                                      sd + (uint64_t)((1 + bx) * (int)(kVtTile >> 4) + 2 * i), id_desc, idesc_base, 1u);
+                    umma_commit(&t_full[sl]);  // (the stage stays until the epilogue has read its target rows)
+                }
+                if (ok) umma_commit(&a_empty[ab]);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ---------------------------------------------------------------- finisher
+        for (int u = 0; u < total; ++u) {
+            int ok = 1, last = 0;
+            if (lane == 0) {
+                const uint64_t t0 = global_ns();
+                int c;
+                while ((c = ld_acq_cta(wg_done)) < kTcEpiGroups * (u + 1)) {
+                    mbar_try_wait_hint(done_bar, (uint32_t)(c & 1), 20000u);
+                    if (*abort) {
+                        ok = 0;
+                        break;
+                    }
+                    if (global_ns() - t0 > lim) {
+                        record_status(&hdr->status, DSPARK_ERR_TIMEOUT);
+                        *abort = 1;
+                        ok = 0;
+                        break;
+                    }
+                }
+                if (ok) {  // this tile's maxima of row block u are in: count it; the last tile finishes
+                    unsigned old;
+                    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                                 : "=r"(old)
+                                 : "l"(a.rb_count + (size_t)u * kVtLineInts)
+                                 : "memory");
+                    last = old == (unsigned)(a.nt - 1);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (!ok) break;
+            if (last) {
+                __syncwarp();  // lane 0's acquire above orders the other CTAs' maxima before these reads
+                __threadfence();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int j = u * kTcRows + 4 * lane + k;
+                    if (j >= a.B) continue;
+                    const int4 q = a.job[j];
+                    if (q.x != VJOB_RESID && q.x != VJOB_BONUS) continue;
+                    const unsigned long long w = __ldcg(a.words + (size_t)j * kVtLineWords);
+                    const int cand = ~(int)(uint32_t)w;
+                    if (cand >= 0 && cand < a.V) a.corr[j] = cand;
+                    else if (q.x == VJOB_RESID) a.fb[j] = 1;  // no residual mass anywhere: draw from p instead
+                }
+            }
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ---------------------------------------------------------------- A operands (thread = job)
+        const int row = tid - 128;
+        bool live = true;
+        for (int u = 0; u < total && live; ++u) {
+            const int j = u * kTcRows + row;
+            const int4 q = j < a.B ? a.job[j] : make_int4(VJOB_NONE, 0, 0, 0);
+            const int prev = (q.x == VJOB_RESID) ? min(max(q.z, 0), a.V - 1) : 0;
+            uint4 w[8];
+            const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.W1) + (size_t)prev * 64);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) w[k] = __ldg(src + k);
+            int ok = 1;
+            if (u >= 2 && lane == 0)
+                ok = mbar_wait_hint_or_abort(&a_empty[u & 1], (uint32_t)(((u >> 1) - 1) & 1), abort, &hdr->status, lim)
+                         ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (ok) {
+                if (u >= 2) mbar_try_wait(&a_empty[u & 1], (uint32_t)(((u >> 1) - 1) & 1));  // (this lane's acquire)
+                unsigned char* ad = sm + kVtSmA + (u & 1) * kVtTile;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) *reinterpret_cast<uint4*>(ad + sw128_offset(row, k)) = w[k];
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive_local(&a_full[u & 1]);
+            } else {
+                live = false;
+            }
+        }
+    } else if (warp >= 8) {
+        // ---------------------------------------------------------------- epilogue (thread = job)
+        const int h = (warp - 8) >> 2;
+        const int row = (warp & 3) * 32 + lane;
+        const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const bool full_tile = tile0 + kTcTile <= a.V;
+        bool live = true;
+        for (int u = 0; u < total && live; ++u) {
+            const int j = u * kTcRows + row;
+            const int4 q = j < a.B ? a.job[j] : make_int4(VJOB_NONE, 0, 0, 0);
+            const int mode = (q.x == VJOB_RESID || q.x == VJOB_BONUS) ? q.x : VJOB_NONE;
+            const uint32_t pos = (uint32_t)q.y;
+            const uint32_t p_chunk = mode == VJOB_RESID ? DSPARK_P_RESID_CHUNK : DSPARK_P_BONUS_CHUNK;
+            const float uin = (!GREEDY && mode != VJOB_NONE)
+                                  ? uniform(a.seed, (uint32_t)j, pos,
+                                            mode == VJOB_RESID ? DSPARK_P_RESID_INCHUNK : DSPARK_P_BONUS_INCHUNK, 0u)
+                                  : 0.f;
+            const float lse2 = __int_as_float(q.w);
+            const float dl2 = mode == VJOB_RESID ? a.dlse[(size_t)j * a.gamma + q.y - 1] * kLog2e : 0.f;
+            float bkey = -CUDART_INF_F;
+            int bcand = -1;
+            bool ok = true;
+            for (int ah = 0; ah < kTcAccs / 2; ++ah) {
+                const int acc = 2 * ah + h;
+                const int ga = u * kTcAccs + acc, sl = ga % kVtSlots, st = ga % kVtStages;
+                float lnE[4] = {0.f, 0.f, 0.f, 0.f};
+                if (!GREEDY && mode != VJOB_NONE)
+                    chunk_variates4(a.seed, (uint32_t)j, pos, (uint32_t)(tile * (kTcTile / 128) + acc), lnE, p_chunk);
+                int okw = 1;
+                if (lane == 0)
+                    okw = mbar_wait_hint_or_abort(&t_full[sl], (uint32_t)((ga / kVtSlots) & 1), abort, &hdr->status, lim)
+                              ? 1 : 0;
+                if (!__shfl_sync(0xffffffffu, okw, 0)) {
+                    ok = false;
+                    break;
+                }
+                mbar_try_wait(&t_full[sl], (uint32_t)((ga / kVtSlots) & 1));  // (this lane's acquire)
+                // the stage's copies (its target rows are read below) completed before the MMAs
+                // that committed t_full; each lane takes the copies' barrier phase too, so the
+                // tensor-copy writes are ordered before its reads (the phase cannot move on: the
+                // stage is refilled only after this warpgroup releases it)
+                mbar_try_wait(&b_full[st], (uint32_t)((ga / kVtStages) & 1));
+                tc_fence_after();
+                const uint32_t taddr = tl + (uint32_t)(sl * kTcN);
+                const unsigned char* tg = sm + st * kVtStageBytes + 3 * kVtTile;  // target boxes 0, 1
+                const int id0 = tile0 + kTcN * acc;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t zv[32];
+                    tmem_ld32(taddr + 32u * (uint32_t)cc, zv);
+                    float t[32];
+                    const unsigned char* box = tg + (cc >> 1) * kVtTile;
+#pragma unroll
+                    for (int uu = 0; uu < 4; ++uu) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(box + sw128_offset(row, (cc & 1) * 4 + uu));
+                        float f[8];
+                        unpack_bf16x8(v, f);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) t[8 * uu + e] = f[e];
+                    }
+                    tmem_wait_ld(zv);
+                    const int idc = id0 + 32 * cc;
+                    if (full_tile)
+                        chunk_job<GREEDY, false>(t, zv, mode, idc, a.V, a.scale2, lse2, dl2, uin, lnE[cc], bkey, bcand);
+                    else if (idc < a.V)  // (uniform) a chunk wholly past V has no ids
+                        chunk_job<GREEDY, true>(t, zv, mode, idc, a.V, a.scale2, lse2, dl2, uin, lnE[cc], bkey, bcand);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive_local(&t_empty[sl]);
+                    mbar_arrive_local(&b_empty[st]);
+                }
+            }
+            if (ok && mode != VJOB_NONE && bcand >= 0)
+                red_max_u64(a.words + (size_t)j * kVtLineWords, pack_key(bkey, bcand));
+            if (bar_red_or(1 + h, 128, !ok)) {
+                live = false;
+                break;
+            }
+            if (row == 0) {
+                add_rel_cta(wg_done, 1);
+                mbar_arrive_local(done_bar);
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && *abort) {  // copies in flight land before the shared memory goes away
+        const int nb = *nb_issued;
+        for (int g = max(0, nb - kVtStages); g < nb; ++g)
+            mbar_wait_bounded(&b_full[g % kVtStages], (uint32_t)((g / kVtStages) & 1), &hdr->status, lim);
+    }
+    if (warp == 1) {
+        if (lane == 0 && *n_mma) {
+            umma_commit(drain_bar);
+            mbar_wait_bounded(drain_bar, 0, &hdr->status, lim);
+        }
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+bool verify_tc_eligible(const dspark_sample_params* p, const void* base, const void* target, const void* W1,
+                        const void* W2) {
+    return p->logits_dtype == DSPARK_BF16 && p->w_dtype == DSPARK_BF16 && p->r == 64 && p->B >= kTcMinBatch &&
+           p->softcap == 0.f && p->V % 64 == 0 && ((uintptr_t)base % 16) == 0 && ((uintptr_t)target % 16) == 0 &&
+           ((uintptr_t)W1 % 16) == 0 && ((uintptr_t)W2 % 16) == 0 && tensor_map_encoder() != nullptr;
+}
+
+dspark_status launch_verify_tc(const VerifyTcArgs& a, cudaStream_t s) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return DSPARK_ERR_UNSUPPORTED;
+    CUtensorMap m_w2, m_base, m_tgt;
+    {
+        cuuint64_t dims[2] = {64, (cuuint64_t)a.V};
+        cuuint64_t strides[1] = {64 * 2};
+        cuuint32_t box[2] = {64, kTcN};
+        cuuint32_t es[2] = {1, 1};
+        if (enc(&m_w2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.W2), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return DSPARK_ERR_UNSUPPORTED;
+    }
+    // base and target as 2-D [rows, V]: gather4 boxes of 64 ids x one row
+    auto rows_map = [&](CUtensorMap* m, const void* ptr, long long rows) {
+        cuuint64_t dims[2] = {(cuuint64_t)a.V, (cuuint64_t)rows};
+        cuuint64_t strides[1] = {(cuuint64_t)a.V * 2};
+        cuuint32_t box[2] = {kTcBox, 1};
+        cuuint32_t es[2] = {1, 1};
+        return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    if (a.target_rows < 1 || a.target_rows > (long long)INT32_MAX || (long long)a.B * a.gamma > (long long)INT32_MAX ||
+        !rows_map(&m_base, a.base, (long long)a.B * a.gamma) || !rows_map(&m_tgt, a.target, a.target_rows))
+        return DSPARK_ERR_UNSUPPORTED;
+    const void* fn = a.greedy ? (const void*)verify_tc_kernel<true> : (const void*)verify_tc_kernel<false>;
+    int per_sm = 0;
+    if (prepare_kernel(fn, kVtSmemBytes, kTcThreads, &per_sm) != cudaSuccess || per_sm < 1) return DSPARK_ERR_CUDA;
+    void* args[] = {(void*)&m_w2, (void*)&m_base, (void*)&m_tgt, (void*)&a};
+    if (cudaLaunchKernel(fn, dim3(a.nt), dim3(kTcThreads), args, kVtSmemBytes, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     return DSPARK_OK;
 }
 

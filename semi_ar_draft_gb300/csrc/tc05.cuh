@@ -145,6 +145,19 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, int
         : "memory");
 }
 
+// Four rows (r0..r3) x the box's columns from c0 of a 2-D tensor map whose box is one row high,
+// written as four consecutive 128-byte rows at dst (swizzled like a tiled copy: with a 512-byte
+// aligned dst inside a 1024-byte aligned tile they are rows 4k..4k+3 of the K-major layout).
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, int c0, int r0, int r1, int r2, int r3,
+                                            uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_addr(bar)),
+        "l"(policy)
+        : "memory");
+}
+
 // Byte offset of 16-byte unit u (0..7) of row q inside a K-major 128-byte-swizzled tile.
 __host__ __device__ __forceinline__ uint32_t sw128_offset(int q, int u) {
     return (uint32_t)((q >> 3) * 1024 + (q & 7) * 128 + ((u ^ (q & 7)) << 4));

@@ -620,6 +620,18 @@ __device__ int block_sample_row(const VerifyArgs& a, const TL* row, int j, int p
     return x;
 }
 
+// After the tensor-core jobs kernel: the whole-row draw from p for the residuals it found without
+// mass (one block per request; the others return at once).
+template <typename TL>
+__global__ void __launch_bounds__(kThreads) verify_fallback_kernel(VerifyArgs a, const int32_t* fb) {
+    const int j = blockIdx.x;
+    if (!fb[j]) return;  // (uniform per block)
+    __shared__ float sh[64];
+    const int4 q = a.job[j];
+    const int x = block_sample_row<TL>(a, reinterpret_cast<const TL*>(a.target) + trow_off(a, j, q.y), j, q.y, sh);
+    if (threadIdx.x == 0) a.corr[j] = x;
+}
+
 template <typename TL, int KS, typename TW>
 __global__ void __launch_bounds__(kThreads, 1) verify_jobs_kernel(VerifyArgs a) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -748,7 +760,8 @@ RowsFn pick_jobs(const dspark_sample_params* p, bool mma) {
 
 struct Layout {
     int nt, nseg, segsz, nrb;
-    size_t off_cnt_req, off_cnt_rb, zero_bytes, off_rowpart, off_job, off_jobpart, total;
+    size_t off_cnt_req, off_cnt_rb, off_tc_words, off_tc_count, off_fb, zero_bytes, off_rowpart, off_job, off_jobpart,
+        total;
 };
 
 Layout layout(const dspark_sample_params* p) {
@@ -761,7 +774,12 @@ Layout layout(const dspark_sample_params* p) {
     L.nrb = (p->B + kRows - 1) / kRows;
     L.off_cnt_req = kHeaderBytes;
     L.off_cnt_rb = L.off_cnt_req + sizeof(uint32_t) * (size_t)p->B;
-    L.zero_bytes = align_up(L.off_cnt_rb + sizeof(uint32_t) * (size_t)L.nrb, 256);
+    // the tensor-core jobs kernel: a packed word per job and an arrival counter per 128 jobs, one
+    // 128-byte line each, and the fallback flags
+    L.off_tc_words = align_up(L.off_cnt_rb + sizeof(uint32_t) * (size_t)L.nrb, 256);
+    L.off_tc_count = L.off_tc_words + kVtcLine * (size_t)p->B;
+    L.off_fb = L.off_tc_count + kVtcLine * (size_t)((p->B + 127) / 128);
+    L.zero_bytes = align_up(L.off_fb + sizeof(int32_t) * (size_t)p->B, 256);
     L.off_rowpart = L.zero_bytes;
     L.off_job = L.off_rowpart + align_up(sizeof(float2) * (size_t)p->B * p->gamma * L.nseg, 256);
     L.off_jobpart = L.off_job + align_up(sizeof(int4) * (size_t)p->B, 256);
@@ -861,6 +879,40 @@ dspark_status verify_impl(const dspark_sample_params* p, const void* base_logits
         if (cudaLaunchKernel((const void*)rows, dim3(L.nseg, p->gamma, p->B), dim3(kThreads), args, 0, s) !=
             cudaSuccess)
             return DSPARK_ERR_CUDA;
+    }
+    // the tensor-core draws: dense target rows (the CSR layout's row count is not known on the host)
+    if (!head_vec && ws_rows && !target_row_offsets && verify_tc_eligible(p, base_logits, target_logits, W1, W2)) {
+        VerifyTcArgs t;
+        t.B = p->B;
+        t.gamma = p->gamma;
+        t.V = p->V;
+        t.nt = L.nt;
+        t.nrb = (p->B + 127) / 128;
+        t.greedy = a.greedy;
+        t.scale2 = a.scale2;
+        t.seed = p->seed;
+        t.base = base_logits;
+        t.target = target_logits;
+        t.gamma_t = gamma_t;
+        t.toff = nullptr;
+        t.target_rows = (long long)p->B * gamma_t;
+        t.W1 = W1;
+        t.W2 = W2;
+        t.job = a.job;
+        t.dlse = draft_lse;
+        t.corr = correction_token;
+        t.fb = reinterpret_cast<int32_t*>(ws + L.off_fb);
+        t.words = reinterpret_cast<unsigned long long*>(ws + L.off_tc_words);
+        t.rb_count = reinterpret_cast<unsigned*>(ws + L.off_tc_count);
+        t.hdr = a.hdr;
+        t.limit_ns = a.limit_ns;
+        if (t.target_rows >= 1) {
+            st = launch_verify_tc(t, s);
+            if (st != DSPARK_OK) return st;
+            verify_fallback_kernel<__nv_bfloat16><<<p->B, kThreads, 0, s>>>(a, t.fb);
+            if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+            return DSPARK_OK;
+        }
     }
     RowsFn jobs = pick_jobs(p, mma);
     size_t smem = sizeof(float) * kRows * kXRow + sizeof(float2) * kRows * kChunks + align_up(sizeof(RowBlock), 16) +

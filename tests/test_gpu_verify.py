@@ -207,3 +207,54 @@ def test_softcap_residuals(T):
     wl = W.make_sample_workload("vcap", 21, 4, 5000, 64, T, device="cuda", data_seed=5, philox_seed=3,
                                 target_sigma=0.7, planted=2, w_std=0.3)
     verify_both(wl, *oracle_drafts(wl, softcap=3.0), softcap=3.0)
+
+
+# ---------------------------------------------------------------- tensor-core residual / bonus draws
+# (bf16, rank 64, B >= 64, V % 64 == 0, dense target rows: one CTA per tile walks row blocks of 128
+# jobs whose base and target rows are gathered by tensor copies)
+@pytest.mark.parametrize("B,gamma,V,T", [(200, 4, 4096, 1.0), (64, 3, 3008, 0.7), (96, 4, 5056, 1.3),
+                                         (129, 2, 2048, 0.8)])
+def test_tc_jobs(B, gamma, V, T):
+    wl = W.make_sample_workload("vtc", B, gamma, V, 64, T, device="cuda", data_seed=B + V, philox_seed=5,
+                                target_sigma=0.7, planted=2, w_std=0.3)
+    n, corr = verify_both(wl, *oracle_drafts(wl))
+    assert (n < gamma).mean() > 0.3  # residual draws were exercised
+
+
+def test_tc_jobs_verify_len_and_bonus():
+    wl = W.make_sample_workload("vtcb", 150, 5, 3008, 64, 1.0, device="cuda", data_seed=23, target_sigma=0.1,
+                                gamma_t=6, w_std=0.3)
+    tok, lse, zat = oracle_drafts(wl)
+    vlen = np.random.default_rng(4).integers(1, 6, wl.B)
+    n, corr = verify_both(wl, tok, lse, zat, vlen=vlen)
+    assert (n == vlen).sum() > 10 and (corr >= 0).all()  # bonus draws from row L_j + 1
+
+
+def test_tc_jobs_greedy_bonus():
+    wl = W.make_sample_workload("vtcg", 100, 3, 2048, 64, 0.0, device="cuda", data_seed=31, target_sigma=0.01,
+                                gamma_t=4, w_std=0.3)
+    n, corr = verify_both(wl, *oracle_drafts(wl))
+    assert (n == 3).any()
+
+
+def test_tc_jobs_residual_without_mass_falls_back_to_p():
+    # as test_residual_without_mass_falls_back_to_p, on the tensor-core path (bf16, B = 64)
+    wl = W.make_sample_workload("vtcfb", 64, 2, 3008, 64, 1.0, device="cuda", data_seed=17, philox_seed=9,
+                                w_std=0.3)
+    t = wl.tensors
+    base, W1, W2, anchor, _ = host(wl)
+    tok, lse, zat = oracle_drafts(wl)
+
+    def f64(x):
+        return ((x.astype(np.uint32) << 16).view(np.float32) if x.dtype == np.uint16 else x).astype(np.float64)
+
+    z1 = f64(base[:, 0]) + f64(W1)[anchor] @ f64(W2).T
+    t["target"][:, 0] = torch.from_numpy(z1.astype(np.float32)).to("cuda").to(torch.bfloat16)
+    target = W.np_view(t["target"])
+    lse_low = (lse - 30.0).astype(np.float32)
+    n, corr = verify_both(wl, tok, lse_low, zat)
+    assert (n == 0).all()
+    for j in range(0, wl.B, 7):
+        _, rc, _, fb = O.verify_request(base, W1, W2, int(anchor[j]), j, tok[j], lse_low[j], zat[j], target, wl.gamma,
+                                        wl.T, wl.seed, TS)
+        assert fb == 1, j
