@@ -811,10 +811,12 @@ dspark_status launch_sample_tc(const dspark_sample_params* p, const void* base_l
 //
 // One CTA per vocabulary tile (1024 ids) walks row blocks of 128 jobs (one TMEM lane each); the
 // row blocks are independent.  Per accumulator of 128 ids one ring stage holds its W2 rows (one
-// tiled copy) and each job's base and target rows, fetched by tile::gather4 copies (32 lanes x 4
-// rows per 64-id box: every job sits at its own position).  z = base + W1[prev] . W2_rows^T is
-// formed on the tensor cores exactly as in the sampler; the epilogue (thread = job) reads z from
-// TMEM and t from the stage, forms the weights (residual: max(0, 2^(t s - lse2) - 2^(z s - dl2));
+// tiled copy) and each job's base and target rows (every job sits at its own position), copied
+// by four warps in 16-byte pieces straight into the swizzled layout (tensor-copy gathers of four
+// rows per instruction stream at 1.8 TB/s on this part: no faster).  z = base + W1[prev] . W2_rows^T is
+// formed on the tensor cores exactly as in the sampler, and the target rows are moved into the
+// neighbouring TMEM columns by the same identity MMAs, so a stage is free as soon as its MMAs have
+// read it; the epilogue (thread = job) reads z and t from TMEM, forms the weights (residual: max(0, 2^(t s - lse2) - 2^(z s - dl2));
 // bonus: 2^(t s - max of the chunk)) and the chunk records, and folds the best into the job's
 // 64-bit word with one atomic max.  The last CTA to finish a row block writes the corrections;
 // a residual with no mass at all is flagged for the whole-row fallback draw from p.
@@ -825,13 +827,14 @@ enum { VJOB_NONE = 0, VJOB_RESID = 1, VJOB_BONUS = 2 };  // the job types the ro
 constexpr uint32_t kVtTile = 16384;                        // 128 rows x 128 bytes
 constexpr uint32_t kVtStageBytes = 5 * kVtTile;            // {W2 rows, base box 0, 1, target box 0, 1}
 constexpr int kVtStages = 2;
-constexpr int kVtSlots = 4;
+constexpr int kVtSlots = 2;  // accumulator pairs {z, t}: 2 x 256 TMEM columns
 constexpr uint32_t kVtSmA = kVtStages * kVtStageBytes;     // [2] A operands (W1 rows of the prevs)
 constexpr uint32_t kVtSmId = kVtSmA + 2 * kVtTile;
 constexpr uint32_t kVtSmBars = kVtSmId + kIdBytes;
 constexpr int kVtNumBars = 4 + 2 * kVtStages + 2 * kVtSlots + 2;
 constexpr uint32_t kVtSmFlags = kVtSmBars + 8 * kVtNumBars;
-constexpr size_t kVtSmemBytes = kVtSmFlags + 64;
+constexpr uint32_t kVtSmRows = kVtSmFlags + 64;            // [2][128] the unit's base and target rows (-1: none)
+constexpr size_t kVtSmemBytes = kVtSmRows + 2 * kTcRows * 4;
 static_assert(kVtSmemBytes <= 227 * 1024, "shared memory of the tensor-core verify kernel");
 constexpr int kVtLineWords = (int)(kVtcLine / 8);
 constexpr int kVtLineInts = (int)(kVtcLine / 4);
@@ -945,8 +948,7 @@ __device__ __forceinline__ void chunk_job(const float (&t)[32], const uint32_t (
 
 template <bool GREEDY>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    verify_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_base,
-                     const __grid_constant__ CUtensorMap tm_tgt, const VerifyTcArgs a) {
+    verify_tc_kernel(const __grid_constant__ CUtensorMap tm_w2, const VerifyTcArgs a) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     WsHeader* hdr = reinterpret_cast<WsHeader*>(a.hdr);
     if (smem_addr(smem_raw) & 1023u) {  // the swizzled tiles need 1024-byte alignment (uniform exit)
@@ -958,7 +960,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t* a_full = bars;                    // [2]
     uint64_t* a_empty = bars + 2;               // [2]
     uint64_t* b_full = bars + 4;                // [kVtStages]
-    uint64_t* b_empty = b_full + kVtStages;     // [kVtStages]: the epilogue has read the stage's target rows
+    uint64_t* b_empty = b_full + kVtStages;     // [kVtStages]
     uint64_t* t_full = b_empty + kVtStages;     // [kVtSlots]
     uint64_t* t_empty = t_full + kVtSlots;      // [kVtSlots]
     uint64_t* done_bar = t_empty + kVtSlots;
@@ -980,8 +982,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&a_empty[b], 1);
         }
         for (int b = 0; b < kVtStages; ++b) {
-            mbar_init(&b_full[b], 1);
-            mbar_init(&b_empty[b], 4);
+            mbar_init(&b_full[b], 5);  // the W2 copy's arrival with its bytes + one per copying warp
+            mbar_init(&b_empty[b], 1);
         }
         for (int b = 0; b < kVtSlots; ++b) {
             mbar_init(&t_full[b], 1);
@@ -1011,50 +1013,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ---------------------------------------------------------------- copies (all 32 lanes)
+        // ---------------------------------------------------------------- W2 copies
         if (lane == 0) {
             tma_prefetch_desc(&tm_w2);
-            tma_prefetch_desc(&tm_base);
-            tma_prefetch_desc(&tm_tgt);
-        }
-        const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
-        bool live = true;
-        for (int u = 0; u < total && live; ++u) {
-            int br[4], tr[4];  // rows 4 lane .. 4 lane + 3 of the row block: their base and target rows
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int j = u * kTcRows + 4 * lane + k;
-                const int4 q = j < a.B ? a.job[j] : make_int4(VJOB_NONE, 0, 0, 0);
-                const bool resid = q.x == VJOB_RESID, bonus = q.x == VJOB_BONUS;
-                long long b = resid && q.y >= 1 && q.y <= a.gamma ? (long long)j * a.gamma + q.y - 1 : 0;
-                long long t = (resid || bonus) && q.y >= 1 ? vt_target_row(a, j, q.y) : 0;
-                br[k] = (int)b;
-                tr[k] = (t >= 0 && t < a.target_rows) ? (int)t : 0;  // (the rows kernel checked the counts)
-            }
-            for (int acc = 0; acc < kTcAccs; ++acc) {
-                const int ga = u * kTcAccs + acc, st = ga % kVtStages, use = ga / kVtStages;
-                int ok = 1;
-                if (lane == 0 && use > 0)
-                    ok = mbar_wait_hint_or_abort(&b_empty[st], (uint32_t)((use - 1) & 1), abort, &hdr->status, lim) ? 1 : 0;
-                if (!__shfl_sync(0xffffffffu, ok, 0)) {
-                    live = false;
+            const uint64_t keep = l2_policy_evict_last();
+            const int nacc = total * kTcAccs;
+            for (int ga = 0; ga < nacc; ++ga) {
+                const int st = ga % kVtStages, use = ga / kVtStages;
+                if (use > 0 &&
+                    !mbar_wait_hint_or_abort(&b_empty[st], (uint32_t)((use - 1) & 1), abort, &hdr->status, lim))
                     break;
-                }
-                const int id0 = tile0 + kTcN * acc;
-                const int nbox = (id0 < a.V) + (id0 + kTcBox < a.V);  // boxes inside V (V % 64 == 0)
-                unsigned char* dst = sm + st * kVtStageBytes;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&b_full[st], kVtTile + 2u * (uint32_t)nbox * kVtTile);
-                    tma_load_2d(dst, &tm_w2, 0, id0, &b_full[st], keep);  // W2 stays in L2
-                }
-                __syncwarp();
-                for (int bx = 0; bx < nbox; ++bx) {
-                    tma_gather4(dst + (1 + bx) * kVtTile + 512 * lane, &tm_base, id0 + kTcBox * bx, br[0], br[1],
-                                br[2], br[3], &b_full[st], stream);
-                    tma_gather4(dst + (3 + bx) * kVtTile + 512 * lane, &tm_tgt, id0 + kTcBox * bx, tr[0], tr[1],
-                                tr[2], tr[3], &b_full[st], stream);
-                }
-                if (lane == 0) *nb_issued = ga + 1;
+                mbar_arrive_expect_tx(&b_full[st], kVtTile);
+                tma_load_2d(sm + st * kVtStageBytes, &tm_w2, 0, tile0 + kTcN * (ga % kTcAccs), &b_full[st], keep);
+                *nb_issued = ga + 1;
             }
         }
         __syncwarp();
@@ -1080,7 +1051,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t d = tmem + (uint32_t)(sl * kTcN);
+                    const uint32_t d = tmem + (uint32_t)(sl * 2 * kTcN), dt = d + (uint32_t)kTcN;
                     const uint64_t sd = ring_desc + (uint64_t)(st * (int)(kVtStageBytes >> 4));
 #pragma unroll
                     for (int k = 0; k < 4; ++k)  // D = W1[prev] . W2_rows^T
@@ -1093,7 +1064,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         for (int i = 0; i < kTcBox / 16; ++i)  // D[:, 64 bx + 16 i ..] += base[:, 16 i ..] . I
                             umma_bf16(d + (uint32_t)(kTcBox * bx + 16 * i),
                                       sd + (uint64_t)((1 + bx) * (int)(kVtTile >> 4) + 2 * i), id_desc, idesc_base, 1u);
-                    umma_commit(&t_full[sl]);  // (the stage stays until the epilogue has read its target rows)
+#pragma unroll
+                    for (int bx = 0; bx < 2; ++bx)
+#pragma unroll
+                        for (int i = 0; i < kTcBox / 16; ++i)  // T[:, 64 bx + 16 i ..] = target[:, 16 i ..] . I
+                            umma_bf16(dt + (uint32_t)(kTcBox * bx + 16 * i),
+                                      sd + (uint64_t)((3 + bx) * (int)(kVtTile >> 4) + 2 * i), id_desc, idesc_base, 0u);
+                    umma_commit(&b_empty[st]);  // the stage is free once these have read it
+                    umma_commit(&t_full[sl]);
                 }
                 if (ok) umma_commit(&a_empty[ab]);
             }
@@ -1148,33 +1126,95 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
         }
     } else if (warp >= 4 && warp < 8) {
-        // ---------------------------------------------------------------- A operands (thread = job)
-        const int row = tid - 128;
+        // ---------------------------------------------------------------- job rows and A operands
+        // Per unit: the table of the jobs' base and target rows, then the A operand (thread = job).
+        // Per accumulator: warp w copies rows 32 w .. 32 w + 31 of both arrays, 16 lanes per row
+        // (one 256-byte segment, 16-byte pieces into the swizzled slots); the copies of the next
+        // accumulator are in flight while the previous ones complete and are handed over.
+        const int row = tid - 128, cw = warp - 4;
+        int* s_br = reinterpret_cast<int*>(sm + kVtSmRows);
+        int* s_tr = s_br + kTcRows;
+        const uint16_t* basep = static_cast<const uint16_t*>(a.base);
+        const uint16_t* tgtp = static_cast<const uint16_t*>(a.target);
+        // A warp whose bounded wait gave up stays in the loop without doing work until the four warps
+        // agree, at the next unit start (a barrier reduction), to leave together: the named barriers
+        // are never left with a warp missing.
+        int pend = -1;  // stage whose copies are in flight and not yet handed over
         bool live = true;
-        for (int u = 0; u < total && live; ++u) {
-            const int j = u * kTcRows + row;
-            const int4 q = j < a.B ? a.job[j] : make_int4(VJOB_NONE, 0, 0, 0);
-            const int prev = (q.x == VJOB_RESID) ? min(max(q.z, 0), a.V - 1) : 0;
-            uint4 w[8];
-            const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.W1) + (size_t)prev * 64);
+        const int nacc = total * kTcAccs;
+        for (int ga = 0; ga < nacc; ++ga) {
+            const int u = ga / kTcAccs, acc = ga % kTcAccs, st = ga % kVtStages, use = ga / kVtStages;
+            if (acc == 0) {
+                // every copier has issued the previous unit's copies (its table reads); all alive?
+                if (bar_red_or(4, 128, !live)) break;
+                const int j = u * kTcRows + row;
+                const int4 q = j < a.B ? a.job[j] : make_int4(VJOB_NONE, 0, 0, 0);
+                const bool resid = q.x == VJOB_RESID, bonus = q.x == VJOB_BONUS;
+                const long long t = (resid || bonus) && q.y >= 1 ? vt_target_row(a, j, q.y) : -1;
+                s_br[row] = resid && q.y >= 1 && q.y <= a.gamma ? j * a.gamma + q.y - 1 : -1;
+                s_tr[row] = (t >= 0 && t < a.target_rows) ? (int)t : -1;
+                // the A operand of the unit: the W1 row of the job's previous token
+                const int prev = resid ? min(max(q.z, 0), a.V - 1) : 0;
+                uint4 w[8];
+                const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.W1) + (size_t)prev * 64);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) w[k] = __ldg(src + k);
+                for (int k = 0; k < 8; ++k) w[k] = __ldg(src + k);
+                int ok = 1;
+                if (u >= 2 && lane == 0)
+                    ok = mbar_wait_hint_or_abort(&a_empty[u & 1], (uint32_t)(((u >> 1) - 1) & 1), abort, &hdr->status,
+                                                 lim) ? 1 : 0;
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (ok) {
+                    if (u >= 2) mbar_try_wait(&a_empty[u & 1], (uint32_t)(((u >> 1) - 1) & 1));  // (this lane's acquire)
+                    unsigned char* ad = sm + kVtSmA + (u & 1) * kVtTile;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) *reinterpret_cast<uint4*>(ad + sw128_offset(row, k)) = w[k];
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                }
+                if (bar_red_or(4, 128, !ok)) {  // the table is complete (or the kernel is giving up)
+                    live = false;
+                    break;
+                }
+                if (lane == 0) mbar_arrive_local(&a_full[u & 1]);
+            }
+            if (!live) continue;
             int ok = 1;
-            if (u >= 2 && lane == 0)
-                ok = mbar_wait_hint_or_abort(&a_empty[u & 1], (uint32_t)(((u >> 1) - 1) & 1), abort, &hdr->status, lim)
-                         ? 1 : 0;
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (ok) {
-                if (u >= 2) mbar_try_wait(&a_empty[u & 1], (uint32_t)(((u >> 1) - 1) & 1));  // (this lane's acquire)
-                unsigned char* ad = sm + kVtSmA + (u & 1) * kVtTile;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) *reinterpret_cast<uint4*>(ad + sw128_offset(row, k)) = w[k];
+            if (use > 0 && lane == 0)
+                ok = mbar_wait_hint_or_abort(&b_empty[st], (uint32_t)((use - 1) & 1), abort, &hdr->status, lim) ? 1 : 0;
+            if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                live = false;
+                continue;
+            }
+            if (use > 0) mbar_try_wait(&b_empty[st], (uint32_t)((use - 1) & 1));  // (this lane's acquire)
+            const int id0 = tile0 + kTcN * acc;
+            const int unit = lane & 15, box = unit >> 3;
+            if (id0 + kTcBox * box < a.V) {  // (V % 64 == 0: a box is wholly inside or outside)
+                unsigned char* stg = sm + st * kVtStageBytes;
+#pragma unroll 4
+                for (int i = 0; i < 16; ++i) {
+                    const int rr = 32 * cw + 2 * i + (lane >> 4);
+                    const uint32_t off = sw128_offset(rr, unit & 7);
+                    const int br = s_br[rr], tr = s_tr[rr];
+                    if (br >= 0)
+                        cp_async_16(stg + (1 + box) * kVtTile + off, basep + (size_t)br * a.V + id0 + 8 * unit);
+                    if (tr >= 0)
+                        cp_async_16(stg + (3 + box) * kVtTile + off, tgtp + (size_t)tr * a.V + id0 + 8 * unit);
+                }
+            }
+            cp_async_commit();
+            if (pend >= 0) {  // the previous accumulator's rows have landed: hand its stage over
+                cp_async_wait_group<1>();
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) mbar_arrive_local(&a_full[u & 1]);
-            } else {
-                live = false;
+                if (lane == 0) mbar_arrive_local(&b_full[pend]);
             }
+            pend = st;
+        }
+        cp_async_wait_group<0>();  // nothing of this thread's lands after the block leaves
+        if (pend >= 0 && live) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive_local(&b_full[pend]);
         }
     } else if (warp >= 8) {
         // ---------------------------------------------------------------- epilogue (thread = job)
@@ -1213,30 +1253,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     break;
                 }
                 mbar_try_wait(&t_full[sl], (uint32_t)((ga / kVtSlots) & 1));  // (this lane's acquire)
-                // the stage's copies (its target rows are read below) completed before the MMAs
-                // that committed t_full; each lane takes the copies' barrier phase too, so the
-                // tensor-copy writes are ordered before its reads (the phase cannot move on: the
-                // stage is refilled only after this warpgroup releases it)
-                mbar_try_wait(&b_full[st], (uint32_t)((ga / kVtStages) & 1));
                 tc_fence_after();
-                const uint32_t taddr = tl + (uint32_t)(sl * kTcN);
-                const unsigned char* tg = sm + st * kVtStageBytes + 3 * kVtTile;  // target boxes 0, 1
+                const uint32_t taddr = tl + (uint32_t)(sl * 2 * kTcN);  // z; t in the next 128 columns
                 const int id0 = tile0 + kTcN * acc;
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t zv[32];
+                    uint32_t zv[32], tv[32];
                     tmem_ld32(taddr + 32u * (uint32_t)cc, zv);
-                    float t[32];
-                    const unsigned char* box = tg + (cc >> 1) * kVtTile;
-#pragma unroll
-                    for (int uu = 0; uu < 4; ++uu) {
-                        const uint4 v = *reinterpret_cast<const uint4*>(box + sw128_offset(row, (cc & 1) * 4 + uu));
-                        float f[8];
-                        unpack_bf16x8(v, f);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) t[8 * uu + e] = f[e];
-                    }
+                    tmem_ld32(taddr + (uint32_t)kTcN + 32u * (uint32_t)cc, tv);
                     tmem_wait_ld(zv);
+                    tmem_wait_ld(tv);
+                    float t[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) t[e] = __uint_as_float(tv[e]);
                     const int idc = id0 + 32 * cc;
                     if (full_tile)
                         chunk_job<GREEDY, false>(t, zv, mode, idc, a.V, a.scale2, lse2, dl2, uin, lnE[cc], bkey, bcand);
@@ -1245,10 +1274,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive_local(&t_empty[sl]);
-                    mbar_arrive_local(&b_empty[st]);
-                }
+                if (lane == 0) mbar_arrive_local(&t_empty[sl]);
             }
             if (ok && mode != VJOB_NONE && bcand >= 0)
                 red_max_u64(a.words + (size_t)j * kVtLineWords, pack_key(bkey, bcand));
@@ -1294,7 +1320,7 @@ bool verify_tc_eligible(const dspark_sample_params* p, const void* base, const v
 dspark_status launch_verify_tc(const VerifyTcArgs& a, cudaStream_t s) {
     auto enc = tensor_map_encoder();
     if (!enc) return DSPARK_ERR_UNSUPPORTED;
-    CUtensorMap m_w2, m_base, m_tgt;
+    CUtensorMap m_w2;
     {
         cuuint64_t dims[2] = {64, (cuuint64_t)a.V};
         cuuint64_t strides[1] = {64 * 2};
@@ -1305,23 +1331,12 @@ dspark_status launch_verify_tc(const VerifyTcArgs& a, cudaStream_t s) {
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return DSPARK_ERR_UNSUPPORTED;
     }
-    // base and target as 2-D [rows, V]: gather4 boxes of 64 ids x one row
-    auto rows_map = [&](CUtensorMap* m, const void* ptr, long long rows) {
-        cuuint64_t dims[2] = {(cuuint64_t)a.V, (cuuint64_t)rows};
-        cuuint64_t strides[1] = {(cuuint64_t)a.V * 2};
-        cuuint32_t box[2] = {kTcBox, 1};
-        cuuint32_t es[2] = {1, 1};
-        return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-    };
-    if (a.target_rows < 1 || a.target_rows > (long long)INT32_MAX || (long long)a.B * a.gamma > (long long)INT32_MAX ||
-        !rows_map(&m_base, a.base, (long long)a.B * a.gamma) || !rows_map(&m_tgt, a.target, a.target_rows))
+    if (a.target_rows < 1 || a.target_rows > (long long)INT32_MAX || (long long)a.B * a.gamma > (long long)INT32_MAX)
         return DSPARK_ERR_UNSUPPORTED;
     const void* fn = a.greedy ? (const void*)verify_tc_kernel<true> : (const void*)verify_tc_kernel<false>;
     int per_sm = 0;
     if (prepare_kernel(fn, kVtSmemBytes, kTcThreads, &per_sm) != cudaSuccess || per_sm < 1) return DSPARK_ERR_CUDA;
-    void* args[] = {(void*)&m_w2, (void*)&m_base, (void*)&m_tgt, (void*)&a};
+    void* args[] = {(void*)&m_w2, (void*)&a};
     if (cudaLaunchKernel(fn, dim3(a.nt), dim3(kTcThreads), args, kVtSmemBytes, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     return DSPARK_OK;
 }

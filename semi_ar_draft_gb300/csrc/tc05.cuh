@@ -145,17 +145,16 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, int
         : "memory");
 }
 
-// Four rows (r0..r3) x the box's columns from c0 of a 2-D tensor map whose box is one row high,
-// written as four consecutive 128-byte rows at dst (swizzled like a tiled copy: with a 512-byte
-// aligned dst inside a 1024-byte aligned tile they are rows 4k..4k+3 of the K-major layout).
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, int c0, int r0, int r1, int r2, int r3,
-                                            uint64_t* bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_addr(bar)),
-        "l"(policy)
-        : "memory");
+// 16-byte copies by threads (through L2 only), in groups: commit closes a group; wait_group<N>
+// returns once at most N of this thread's groups are still in flight.  The copied data is seen by
+// the tensor cores after the thread's fence.proxy.async and a barrier arrival.
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Byte offset of 16-byte unit u (0..7) of row q inside a K-major 128-byte-swizzled tile.
