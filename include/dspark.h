@@ -365,6 +365,11 @@ dspark_status dspark_selftest_grid_wait(int nblocks, int missing, void* workspac
 
 const char* dspark_status_string(dspark_status s);
 
+/* Number of kernels the library has enqueued in this process so far (all devices and streams;
+ * an entry point that returns an error may have enqueued some).  For counting launches around a
+ * region: read it before and after. */
+uint64_t dspark_kernel_launches(void);
+
 #ifdef __cplusplus
 }
 #endif

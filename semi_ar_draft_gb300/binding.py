@@ -90,6 +90,8 @@ def lib():
         L.dspark_selftest_grid_wait.restype = i32
         L.dspark_status_string.argtypes = [i32]
         L.dspark_status_string.restype = C.c_char_p
+        L.dspark_kernel_launches.argtypes = []
+        L.dspark_kernel_launches.restype = u64
         _L = L
     return _L
 
@@ -259,6 +261,10 @@ def dspark_selftest_grid_wait(nblocks, missing, workspace, stream=None):
     st = lib().dspark_selftest_grid_wait(int(nblocks), int(missing), _ptr(workspace),
                                          workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "dspark_selftest_grid_wait")
+
+
+def dspark_kernel_launches() -> int:
+    return int(lib().dspark_kernel_launches())
 
 
 def dspark_status_string(s: int) -> str:

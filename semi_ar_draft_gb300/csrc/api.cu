@@ -11,6 +11,7 @@ namespace dspark {
 
 namespace {
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+std::atomic<uint64_t> g_launches{0};
 int g_sm_count[64] = {0};
 
 __global__ void selftest_grid_wait_kernel(WsHeader* hdr, uint32_t expected, uint64_t limit_ns, int32_t* passed) {
@@ -35,6 +36,8 @@ cudaError_t device_sm_count(int* sms) {
 }
 
 uint64_t wait_limit_ns() { return g_wait_limit_ns.load(); }
+
+void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
 
 namespace {
@@ -153,8 +156,11 @@ extern "C" dspark_status dspark_selftest_grid_wait(int nblocks, int missing, voi
     if (cudaLaunchCooperativeKernel((const void*)selftest_grid_wait_kernel, dim3(nblocks), dim3(64), args, 0, s) !=
         cudaSuccess)
         return DSPARK_ERR_CUDA;
+    note_launch();
     return DSPARK_OK;
 }
+
+extern "C" uint64_t dspark_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 extern "C" const char* dspark_status_string(dspark_status s) {
     switch (s) {

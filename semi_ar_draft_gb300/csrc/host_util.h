@@ -40,6 +40,9 @@ dspark_status launch_sample_tc(const dspark_sample_params* p, const void* base_l
                                const int32_t* anchor, int32_t* tokens, float* draft_lse, float* draft_logit_at_tok,
                                const SampleWsLayout& L, void* workspace, cudaStream_t s);
 
+// Counts the kernels the library enqueues (dspark_kernel_launches reads the total).
+void note_launch(int n = 1);
+
 // Tensor-core residual / bonus draws of verify (sample_tc.cu): bf16 logits and weights of rank 64,
 // V % 64 == 0, at least kTcMinBatch requests, 16-byte aligned tensors, no softcap, vanilla head.
 // One CTA per vocabulary tile walks row blocks of 128 jobs; each job's base and target rows are

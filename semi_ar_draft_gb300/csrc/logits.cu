@@ -165,5 +165,6 @@ extern "C" dspark_status dspark_markov_block_logits(const dspark_sample_params* 
     void* args[] = {&a};
     if (cudaLaunchKernel((const void*)fn, dim3(nt, (unsigned)nrb), dim3(kThreads), args, smem, s) != cudaSuccess)
         return DSPARK_ERR_CUDA;
+    note_launch();
     return DSPARK_OK;
 }

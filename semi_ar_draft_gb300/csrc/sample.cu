@@ -976,6 +976,7 @@ dspark_status sample_block_launch(const dspark_sample_params* p, const dspark_he
     void* args[] = {&a};
     if (cudaLaunchCooperativeKernel((const void*)fn, dim3(G), dim3(threads), args, smem, s) != cudaSuccess)
         return DSPARK_ERR_CUDA;
+    note_launch();
     return DSPARK_OK;
 }
 
@@ -1046,6 +1047,7 @@ extern "C" dspark_status dspark_markov_sample_block_head(const dspark_sample_par
                                                        static_cast<const float*>(head->Wo), hpre);
     }
     if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+    note_launch();
     return sample_block_launch(p, head, hpre, head_vec, base_logits, W1, W2, anchor, tokens, draft_lse,
                                draft_logit_at_tok, workspace, stream);
 }

@@ -799,6 +799,7 @@ dspark_status launch_sample_tc(const dspark_sample_params* p, const void* base_l
     void* args[] = {(void*)&m_base, (void*)&m_w2, (void*)&a};
     if (cudaLaunchCooperativeKernel(fn, dim3(nt), dim3(kTcThreads), args, smem, s) != cudaSuccess)
         return DSPARK_ERR_CUDA;
+    note_launch();
     return DSPARK_OK;
 }
 
@@ -1338,6 +1339,7 @@ dspark_status launch_verify_tc(const VerifyTcArgs& a, cudaStream_t s) {
     if (prepare_kernel(fn, kVtSmemBytes, kTcThreads, &per_sm) != cudaSuccess || per_sm < 1) return DSPARK_ERR_CUDA;
     void* args[] = {(void*)&m_w2, (void*)&a};
     if (cudaLaunchKernel(fn, dim3(a.nt), dim3(kTcThreads), args, kVtSmemBytes, s) != cudaSuccess) return DSPARK_ERR_CUDA;
+    note_launch();
     return DSPARK_OK;
 }
 

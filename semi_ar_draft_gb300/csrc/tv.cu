@@ -512,6 +512,7 @@ extern "C" dspark_status dspark_accept_rate_tv(int S, int A, int gamma, int V, i
         a.hdr = static_cast<WsHeader*>(workspace);
         a.limit_ns = wait_limit_ns();
         tv_rows_kernel<<<(unsigned)G, kWSThreads, kRowSmem, s>>>(a);
+        note_launch();
         if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
     } else {
         void (*fn)(TVArgs) = dtype == DSPARK_BF16 ? tv_kernel<__nv_bfloat16> : tv_kernel<float>;
@@ -545,10 +546,12 @@ extern "C" dspark_status dspark_accept_rate_tv(int S, int A, int gamma, int V, i
         a.vec_ok = ((size_t)V * esz) % 16 == 0 && (uintptr_t)draft_logits % 16 == 0 && (uintptr_t)target_logits % 16 == 0;
         cfg.gridDim = dim3(nclusters * cs);
         if (cudaLaunchKernelEx(&cfg, fn, a) != cudaSuccess) return DSPARK_ERR_CUDA;
+        note_launch();
     }
     if (tau) {
         const long long nblk = (long long)S * A;
         tau_kernel<<<(unsigned)((nblk + 255) / 256), 256, 0, s>>>(nblk, gamma, accept_rate, eval_mask, tau);
+        note_launch();
         if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
     }
     return DSPARK_OK;
@@ -562,6 +565,7 @@ extern "C" dspark_status dspark_tv_l1_loss(int S, int A, int gamma, const float*
     const long long n = (long long)S * A * gamma;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     tv_l1_kernel<<<1, kL1Threads, 0, s>>>(n, gamma, accept_rate, eval_mask, (double)decay_gamma, l1, sums);
+    note_launch();
     if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
     return DSPARK_OK;
 }

@@ -874,11 +874,13 @@ dspark_status verify_impl(const dspark_sample_params* p, const void* base_logits
         if (cudaLaunchKernel((const void*)verify_rows_ws_kernel, dim3(G), dim3(kVThreads), args, sizeof(VRSmem), s) !=
             cudaSuccess)
             return DSPARK_ERR_CUDA;
+        note_launch();
     } else {
         RowsFn rows = p->logits_dtype == DSPARK_BF16 ? verify_rows_kernel<__nv_bfloat16> : verify_rows_kernel<float>;
         if (cudaLaunchKernel((const void*)rows, dim3(L.nseg, p->gamma, p->B), dim3(kThreads), args, 0, s) !=
             cudaSuccess)
             return DSPARK_ERR_CUDA;
+        note_launch();
     }
     // the tensor-core draws: dense target rows (the CSR layout's row count is not known on the host)
     if (!head_vec && ws_rows && !target_row_offsets && verify_tc_eligible(p, base_logits, target_logits, W1, W2)) {
@@ -911,6 +913,7 @@ dspark_status verify_impl(const dspark_sample_params* p, const void* base_logits
             if (st != DSPARK_OK) return st;
             verify_fallback_kernel<__nv_bfloat16><<<p->B, kThreads, 0, s>>>(a, t.fb);
             if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+            note_launch();
             return DSPARK_OK;
         }
     }
@@ -922,6 +925,7 @@ dspark_status verify_impl(const dspark_sample_params* p, const void* base_logits
     if (prepare_kernel((const void*)jobs, smem, kThreads, &per_sm) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (cudaLaunchKernel((const void*)jobs, dim3(L.nt, L.nrb), dim3(kThreads), args, smem, s) != cudaSuccess)
         return DSPARK_ERR_CUDA;
+    note_launch();
     return DSPARK_OK;
 }
 

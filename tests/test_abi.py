@@ -125,6 +125,17 @@ def test_head_host_validation_needs_no_gpu(L):
                                 fake, 1 << 20, None) == 1
 
 
+def test_kernel_launch_counter(L):
+    from semi_ar_draft_gb300 import binding as b
+
+    # readable without a GPU; host-validation failures enqueue nothing and do not count
+    n0 = b.dspark_kernel_launches()
+    bad = b.params(0, 8, 100, 0, 1.0, 0, 0, 0)
+    fake = C.c_void_p(0x1000)
+    assert L.dspark_markov_sample_block(C.byref(bad), fake, None, None, fake, fake, fake, fake, fake, 1 << 20, None) == 1
+    assert b.dspark_kernel_launches() == n0 >= 0
+
+
 def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     import importlib
 
