@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(kTVThreads, 1) tv_kernel(TVArgs a) {
 // ------------------------------------------------------------------------------------------
 // bf16 fast path: one block per row at a time (persistent over rows, no cluster), warp-specialised.
 // A producer warp streams every row twice through a ring of kNS shared-memory slots (kCE ids of
-// d and t per slot) with the bulk-copy engine: pass 1 from HBM with an L2 evict-last policy, so
+// d and t per slot, 32 per consumer thread) with the bulk-copy engine: pass 1 from HBM with an L2 evict-last policy, so
 // that pass 2, which follows right after, reads the same bytes from L2 (evict-first); a slot
 // is refilled once all 16 consumer warps have released it.  The consumer warps take the softmax
 // statistics of d and t in pass 1, combine them across the block, then form
@@ -198,12 +198,13 @@ __global__ void __launch_bounds__(kTVThreads, 1) tv_kernel(TVArgs a) {
 // Every wait is bounded; after a timeout the block-wide abort flag makes the consumers skip the
 // data while keeping the same sequence of named barriers, and in-flight copies are awaited.
 // ------------------------------------------------------------------------------------------
-constexpr int kCE = 8192;                 // ids per array per slot
-constexpr int kNS = 6;                    // ring slots (6 x 32 KB)
+constexpr int kCE = 16384;                // ids per array per slot
+constexpr int kNS = 3;                    // ring slots (3 x 64 KB)
 constexpr int kWSCons = 512;              // consumer threads (16 warps)
 constexpr int kWSWarps = kWSCons / 32;
 constexpr int kWSThreads = kWSCons + 32;  // + one producer warp
-static_assert(kCE == 16 * kWSCons, "two 16-byte groups of each array per consumer thread per slot");
+constexpr int kGrp = kCE / 4;             // ids between a thread's 16-byte groups
+static_assert(kCE == 32 * kWSCons, "four 16-byte groups of each array per consumer thread per slot");
 
 struct TVRSmem {
     uint16_t slots[kNS][2][kCE];
@@ -228,39 +229,88 @@ struct TVRArgs {
 };
 
 
-// A consumer thread's sixteen ids of a slot: 8 at `my0` and 8 at kCE/2 + my0 (each group a
-// conflict-free 16-byte read across the warp).  x[2i], x[2i+1]: the two values of word i.
-__device__ __forceinline__ void load16(const uint16_t* slot_arr, int my0, float (&x)[16]) {
-    float lo[8], hi[8];
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(slot_arr + my0), lo);
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(slot_arr + kCE / 2 + my0), hi);
+// A consumer thread's 32 ids of one array in a slot, as 16 bf16 pairs: four 16-byte groups at
+// my0 + g kGrp (each a conflict-free 16-byte read across the warp).  Word k holds ids
+// (k / 4) kGrp + my0 + 2 (k % 4) + {0, 1} in its low and high halves.
+__device__ __forceinline__ void load32w(const uint16_t* arr, int my0, uint32_t (&w)[16]) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        x[e] = lo[e];
-        x[8 + e] = hi[e];
+    for (int g = 0; g < 4; ++g) {
+        const uint4 v = *reinterpret_cast<const uint4*>(arr + g * kGrp + my0);
+        w[4 * g] = v.x;
+        w[4 * g + 1] = v.y;
+        w[4 * g + 2] = v.z;
+        w[4 * g + 3] = v.w;
     }
 }
 
-// Ids at or past the end of the row (the ragged last chunk) read as -inf: no mass, no max.
-__device__ __forceinline__ void mask_tail16(float (&xd)[16], float (&xt)[16], int my0, int tail) {
+// Ids at or past the end of the row (the ragged last chunk) read as bf16 -inf: no mass, no max.
+// The row length is a multiple of 8, so a 16-byte group is wholly inside or outside.
+__device__ __forceinline__ void mask_tail32(uint32_t (&w)[16], int my0, int tail) {
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-        const int id = (e < 8 ? my0 + e : kCE / 2 + my0 + e - 8);
-        if (id >= tail) xd[e] = xt[e] = -CUDART_INF_F;
-    }
+    for (int g = 0; g < 4; ++g)
+        if (g * kGrp + my0 >= tail) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) w[4 * g + k] = 0xFF80FF80u;
+        }
 }
 
-// Sum over sixteen ids of 2^min(d log2e - Ld2, t log2e - Lt2), as a tree.
-__device__ __forceinline__ float minsum16(const float (&xd)[16], const float (&xt)[16], uint64_t c2, uint64_t nld2,
-                                          uint64_t nlt2) {
-    uint64_t e[8];
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Sum over the 32 ids of 2^(x c - m) (nm2 = -m in both lanes), four packed accumulators.
+__device__ __forceinline__ float exp_sum32(const uint32_t (&w)[16], uint64_t c2, uint64_t nm2) {
+    uint64_t acc[4];
 #pragma unroll
-    for (int h = 0; h < 8; ++h) {
-        const float2 yd = up2(fma2(pk2(xd[2 * h], xd[2 * h + 1]), c2, nld2));
-        const float2 yt = up2(fma2(pk2(xt[2 * h], xt[2 * h + 1]), c2, nlt2));
-        e[h] = pk2(ex2(fminf(yd.x, yt.x)), ex2(fminf(yd.y, yt.y)));
+    for (int k = 0; k < 16; ++k) {
+        const float2 y = up2(fma2(pk2(bf16_lo(w[k]), bf16_hi(w[k])), c2, nm2));
+        const uint64_t e = pk2(ex2(y.x), ex2(y.y));
+        acc[k & 3] = k < 4 ? e : add2(acc[k & 3], e);
     }
-    return tree_sum8x2(e);
+    const float2 r = up2(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])));
+    return r.x + r.y;
+}
+
+// One group of the online (max m, sum s of 2^(x log2e - m)) statistics.  The terms are taken
+// against the running maximum as it stands; only when their sum reaches 2^64 (a row's first group,
+// where m = -inf makes it inf or NaN, or a maximum that jumped far) is the group's maximum taken
+// (packed bf16 maxima of the words: the maximum of the values exactly) and the sum rescaled.
+// While every value so far is -inf the pair stays (-inf, 0).
+__device__ __forceinline__ void lse_step32w(const uint32_t (&w)[16], uint64_t c2, float& m, float& s) {
+    float g = exp_sum32(w, c2, pk2(-m, -m));
+    if (!(g < 0x1p64f)) {
+        uint32_t mw[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mw[k] = bmax2(w[k], w[8 + k]);
+        const uint32_t x = bmax2(bmax2(bmax2(mw[0], mw[1]), bmax2(mw[2], mw[3])),
+                                 bmax2(bmax2(mw[4], mw[5]), bmax2(mw[6], mw[7])));
+        const float gm = fmaxf(bf16_lo(x), bf16_hi(x)) * kLog2e;
+        const float mn = fmaxf(m, gm);
+        const bool none = mn == -CUDART_INF_F;
+        const float sc = none ? 0.f : ex2(m - mn);  // m = -inf, mn finite: 0
+        const float mo = none ? 0.f : mn;           // x = -inf then gives 2^-inf = 0, never NaN
+        g = exp_sum32(w, c2, pk2(-mo, -mo));
+        s *= sc;
+        m = mn;
+    }
+    s += g;
+}
+
+// Sum over the 32 ids of 2^min(d log2e - Ld2, t log2e - Lt2).
+__device__ __forceinline__ float minsum32w(const uint32_t (&wd)[16], const uint32_t (&wt)[16], uint64_t c2,
+                                           uint64_t nld2, uint64_t nlt2) {
+    uint64_t acc[4];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const float2 yd = up2(fma2(pk2(bf16_lo(wd[k]), bf16_hi(wd[k])), c2, nld2));
+        const float2 yt = up2(fma2(pk2(bf16_lo(wt[k]), bf16_hi(wt[k])), c2, nlt2));
+        const uint64_t e = pk2(ex2(fminf(yd.x, yt.x)), ex2(fminf(yd.y, yt.y)));
+        acc[k & 3] = k < 4 ? e : add2(acc[k & 3], e);
+    }
+    const float2 r = up2(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])));
+    return r.x + r.y;
 }
 
 // Warp-wide combine of (max, sum 2^(x - max)) pairs: the max first, then one rescale per lane.
@@ -316,10 +366,10 @@ __global__ void __launch_bounds__(kWSThreads, 1) tv_rows_kernel(TVRArgs a) {
         uint32_t phase = 0;
         // After an abort the waits return at once and the slots hold stale data: the arithmetic
         // runs on it (shared-memory reads cannot fault) and the result is never stored.
-        auto take = [&](float (&xd)[16], float (&xt)[16]) {
+        auto take = [&](uint32_t (&wd)[16], uint32_t (&wt)[16]) {
             mbar_wait_hint_or_abort(&S.full[slot], phase, abort, &a.hdr->status, a.limit_ns);
-            load16(&S.slots[slot][0][0], my0, xd);
-            load16(&S.slots[slot][1][0], my0, xt);
+            load32w(&S.slots[slot][0][0], my0, wd);
+            load32w(&S.slots[slot][1][0], my0, wt);
             __syncwarp();
             if (lane == 0) mbar_arrive_local(&S.empty[slot]);
             if (++slot == kNS) {
@@ -327,26 +377,28 @@ __global__ void __launch_bounds__(kWSThreads, 1) tv_rows_kernel(TVRArgs a) {
                 phase ^= 1u;
             }
         };
+        const uint64_t c2 = pk2(kLog2e, kLog2e);
         for (int rl = 0; rl < nrows; ++rl) {
             // ---- pass 1: softmax statistics of d and t (log2 domain)
             float md = -CUDART_INF_F, sd = 0.f, mt = -CUDART_INF_F, st = 0.f;
             for (int k = 0; k < nch - 1; ++k) {
-                float xd[16], xt[16];
-                take(xd, xt);
-                lse_step16(xd, kLog2e, md, sd);
-                lse_step16(xt, kLog2e, mt, st);
+                uint32_t wd[16], wt[16];
+                take(wd, wt);
+                lse_step32w(wd, c2, md, sd);
+                lse_step32w(wt, c2, mt, st);
             }
             {
-                float xd[16], xt[16];
-                take(xd, xt);
-                mask_tail16(xd, xt, my0, tail);
-                lse_step16(xd, kLog2e, md, sd);
-                lse_step16(xt, kLog2e, mt, st);
+                uint32_t wd[16], wt[16];
+                take(wd, wt);
+                mask_tail32(wd, my0, tail);
+                mask_tail32(wt, my0, tail);
+                lse_step32w(wd, c2, md, sd);
+                lse_step32w(wt, c2, mt, st);
             }
             {
-                const float2 wd = warp_lse_pair(md, sd);
-                const float2 wt = warp_lse_pair(mt, st);
-                if (lane == 0) S.red4[warp] = make_float4(wd.x, wd.y, wt.x, wt.y);
+                const float2 wdp = warp_lse_pair(md, sd);
+                const float2 wtp = warp_lse_pair(mt, st);
+                if (lane == 0) S.red4[warp] = make_float4(wdp.x, wdp.y, wtp.x, wtp.y);
             }
             named_barrier(1, kWSCons);
             float Ld2, Lt2;
@@ -358,18 +410,19 @@ __global__ void __launch_bounds__(kWSThreads, 1) tv_rows_kernel(TVRArgs a) {
                 Lt2 = ct.x + lg2(ct.y);
             }
             // ---- pass 2: sum of min(p, q) = 2^min(d log2e - Ld2, t log2e - Lt2)
-            const uint64_t c2 = pk2(kLog2e, kLog2e), nld2 = pk2(-Ld2, -Ld2), nlt2 = pk2(-Lt2, -Lt2);
+            const uint64_t nld2 = pk2(-Ld2, -Ld2), nlt2 = pk2(-Lt2, -Lt2);
             float acc = 0.f;
             for (int k = 0; k < nch - 1; ++k) {
-                float xd[16], xt[16];
-                take(xd, xt);
-                acc += minsum16(xd, xt, c2, nld2, nlt2);
+                uint32_t wd[16], wt[16];
+                take(wd, wt);
+                acc += minsum32w(wd, wt, c2, nld2, nlt2);
             }
             {
-                float xd[16], xt[16];
-                take(xd, xt);
-                mask_tail16(xd, xt, my0, tail);
-                acc += minsum16(xd, xt, c2, nld2, nlt2);
+                uint32_t wd[16], wt[16];
+                take(wd, wt);
+                mask_tail32(wd, my0, tail);
+                mask_tail32(wt, my0, tail);
+                acc += minsum32w(wd, wt, c2, nld2, nlt2);
             }
             const float w = warp_sum(acc);
             if (lane == 0) S.red1[warp] = w;

@@ -41,8 +41,28 @@ def test_small(V, dtype):
 
 
 def test_vocabulary_beyond_the_copy_ring():
-    # 262144 ids: a row segment no longer fits the shared-memory ring; the streaming path runs
+    # 262144 ids: sixteen ring slots per pass, the row far larger than the ring
     check(W.make_tv_workload(1, 2, 2, 262144, device="cuda", data_seed=5))
+
+
+def test_running_maximum_jumps():
+    # Logits far above everything before them (up to 120 against a spread of 3): the running sums are
+    # taken against the maximum seen so far, and a group whose terms reach 2^64 restarts them from its
+    # own maximum.  Spikes late in a row, early in a row, in d only, in t only, and at the last id.
+    tv = W.make_tv_workload(1, 2, 4, 40000, device="cuda", data_seed=11)
+    d, t = tv.tensors["d"], tv.tensors["t"]
+    d[0, 0, 0, 39000] = 120.0
+    t[0, 0, 0, 35000] = 90.0
+    d[0, 0, 1, 20000] = 70.0
+    t[0, 0, 1, 20001] = 70.0
+    d[0, 0, 2, 17000] = 80.0
+    t[0, 0, 2, 17000] = 80.0
+    d[0, 1, 2, 5] = 100.0
+    t[0, 1, 3, :] = -50.0
+    t[0, 1, 3, 39999] = 50.0
+    check(tv)
+    acc = api.accept_rate_tv(d, t, tv.tensors["keep"])[0].cpu().numpy()
+    assert acc[0, 0, 2] > 0.99 and acc[0, 0, 0] < 1e-6  # shared spike: p = q; apart: no overlap
 
 
 def test_identical_rows_give_one():
