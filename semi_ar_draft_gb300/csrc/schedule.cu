@@ -249,8 +249,8 @@ extern "C" dspark_status dspark_schedule_verify_len(int B, int gamma, const floa
         return DSPARK_ERR_CUDA;
     schedule_kernel<<<1, kSchedThreads, smem, s>>>(B, gamma, conf, budget_c, verify_len, offsets, objective,
                                                    &static_cast<WsHeader*>(workspace)->status);
-    note_launch();
     if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+    note_launch();
     return DSPARK_OK;
 }
 
@@ -259,7 +259,7 @@ extern "C" dspark_status dspark_theta_schedule(int B, int gamma, const float* co
     if (B < 1 || gamma < 1 || !conf || !sps || !ell) return DSPARK_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     theta_kernel<<<(unsigned)((B + 127) / 128), 128, 0, s>>>(B, gamma, conf, sps, ell, theta);
-    note_launch();
     if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+    note_launch();
     return DSPARK_OK;
 }

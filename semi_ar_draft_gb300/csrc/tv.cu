@@ -565,8 +565,8 @@ extern "C" dspark_status dspark_accept_rate_tv(int S, int A, int gamma, int V, i
         a.hdr = static_cast<WsHeader*>(workspace);
         a.limit_ns = wait_limit_ns();
         tv_rows_kernel<<<(unsigned)G, kWSThreads, kRowSmem, s>>>(a);
-        note_launch();
         if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+        note_launch();
     } else {
         void (*fn)(TVArgs) = dtype == DSPARK_BF16 ? tv_kernel<__nv_bfloat16> : tv_kernel<float>;
         cfg.blockDim = dim3(kTVThreads);
@@ -604,8 +604,8 @@ extern "C" dspark_status dspark_accept_rate_tv(int S, int A, int gamma, int V, i
     if (tau) {
         const long long nblk = (long long)S * A;
         tau_kernel<<<(unsigned)((nblk + 255) / 256), 256, 0, s>>>(nblk, gamma, accept_rate, eval_mask, tau);
-        note_launch();
         if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+        note_launch();
     }
     return DSPARK_OK;
 }
@@ -618,7 +618,7 @@ extern "C" dspark_status dspark_tv_l1_loss(int S, int A, int gamma, const float*
     const long long n = (long long)S * A * gamma;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     tv_l1_kernel<<<1, kL1Threads, 0, s>>>(n, gamma, accept_rate, eval_mask, (double)decay_gamma, l1, sums);
-    note_launch();
     if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+    note_launch();
     return DSPARK_OK;
 }
