@@ -1241,7 +1241,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bool ok = true;
             for (int ah = 0; ah < kTcAccs / 2; ++ah) {
                 const int acc = 2 * ah + h;
-                const int ga = u * kTcAccs + acc, sl = ga % kVtSlots, st = ga % kVtStages;
+                const int ga = u * kTcAccs + acc, sl = ga % kVtSlots;
                 float lnE[4] = {0.f, 0.f, 0.f, 0.f};
                 if (!GREEDY && mode != VJOB_NONE)
                     chunk_variates4(a.seed, (uint32_t)j, pos, (uint32_t)(tile * (kTcTile / 128) + acc), lnE, p_chunk);
