@@ -121,37 +121,78 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
     return r;
 }
 
-// Tree sum of eight packed pairs, then of the two lanes.
-__device__ __forceinline__ float tree_sum8x2(const uint64_t (&v)[8]) {
-    const uint64_t a = add2(add2(v[0], v[1]), add2(v[2], v[3]));
-    const uint64_t b = add2(add2(v[4], v[5]), add2(v[6], v[7]));
-    const float2 r = up2(add2(a, b));
+// ---------------------------------------------------------------- 32 bf16 values per thread
+// A thread's 32 values of a row chunk, as 16 packed bf16 pairs: four 16-byte groups at
+// my0 + g GRP (each a conflict-free 16-byte read across a warp whose lanes take consecutive
+// my0).  Word k holds elements (k / 4) GRP + my0 + 2 (k % 4) + {0, 1} in its low and high halves,
+// so the elements ascend with (k, half).
+template <int GRP>
+__device__ __forceinline__ void load32w(const uint16_t* arr, int my0, uint32_t (&w)[16]) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const uint4 v = *reinterpret_cast<const uint4*>(arr + g * GRP + my0);
+        w[4 * g] = v.x;
+        w[4 * g + 1] = v.y;
+        w[4 * g + 2] = v.z;
+        w[4 * g + 3] = v.w;
+    }
+}
+
+// Elements at or past `tail` (the ragged last chunk of a row) read as bf16 -inf: no mass, no max.
+// Row lengths are multiples of 8, so a 16-byte group is wholly inside or outside.
+template <int GRP>
+__device__ __forceinline__ void mask_tail32(uint32_t (&w)[16], int my0, int tail) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+        if (g * GRP + my0 >= tail) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) w[4 * g + k] = 0xFF80FF80u;
+        }
+}
+
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Sum over the 32 values of 2^(x c - m) (c2 = c, nm2 = -m in both lanes), four packed accumulators.
+__device__ __forceinline__ float exp_sum32(const uint32_t (&w)[16], uint64_t c2, uint64_t nm2) {
+    uint64_t acc[4];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const float2 y = up2(fma2(pk2(bf16_lo(w[k]), bf16_hi(w[k])), c2, nm2));
+        const uint64_t e = pk2(ex2(y.x), ex2(y.y));
+        acc[k & 3] = k < 4 ? e : add2(acc[k & 3], e);
+    }
+    const float2 r = up2(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])));
     return r.x + r.y;
 }
 
-// Online (max, sum 2^(x scale - max)) over sixteen more values (scale > 0; m and s in the log2
-// domain), without branches: the running sum is rescaled by 2^(m_old - m_new) (1 when the maximum
-// did not grow), and the sixteen terms are added as a tree.  While every value so far is -inf
-// the pair stays (-inf, 0).
-__device__ __forceinline__ void lse_step16(const float (&x)[16], float scale, float& m, float& s) {
-    float g[8];
+// One group of the online (max m, sum s of 2^(x scale - m)) statistics (scale > 0, c2 = scale in
+// both lanes; m and s in the log2 domain).  The terms are taken against the running maximum as it
+// stands; only when their sum reaches 2^64 (a row's first group, where m = -inf makes it inf or
+// NaN, or a maximum that jumped far) is the group's maximum taken (packed bf16 maxima of the words:
+// the maximum of the values exactly) and the sum rescaled.  While every value so far is -inf the
+// pair stays (-inf, 0).
+__device__ __forceinline__ void lse_step32w(const uint32_t (&w)[16], float scale, uint64_t c2, float& m, float& s) {
+    float g = exp_sum32(w, c2, pk2(-m, -m));
+    if (!(g < 0x1p64f)) {
+        uint32_t mw[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) g[e] = fmaxf(x[e], x[8 + e]);
-    const float gm = fmaxf(fmaxf(fmaxf(g[0], g[1]), fmaxf(g[2], g[3])), fmaxf(fmaxf(g[4], g[5]), fmaxf(g[6], g[7]))) *
-                     scale;
-    const float mn = fmaxf(m, gm);
-    const bool none = mn == -CUDART_INF_F;
-    const float sc = none ? 0.f : ex2(m - mn);  // m = -inf, mn finite: 0
-    const float mo = none ? 0.f : mn;           // x = -inf then gives 2^-inf = 0, never NaN
-    const uint64_t c2 = pk2(scale, scale), nm2 = pk2(-mo, -mo);
-    uint64_t e[8];
-#pragma unroll
-    for (int h = 0; h < 8; ++h) {
-        const float2 y = up2(fma2(pk2(x[2 * h], x[2 * h + 1]), c2, nm2));
-        e[h] = pk2(ex2(y.x), ex2(y.y));
+        for (int k = 0; k < 8; ++k) mw[k] = bmax2(w[k], w[8 + k]);
+        const uint32_t x = bmax2(bmax2(bmax2(mw[0], mw[1]), bmax2(mw[2], mw[3])),
+                                 bmax2(bmax2(mw[4], mw[5]), bmax2(mw[6], mw[7])));
+        const float gm = fmaxf(bf16_lo(x), bf16_hi(x)) * scale;
+        const float mn = fmaxf(m, gm);
+        const bool none = mn == -CUDART_INF_F;
+        const float sc = none ? 0.f : ex2(m - mn);  // m = -inf, mn finite: 0
+        const float mo = none ? 0.f : mn;           // x = -inf then gives 2^-inf = 0, never NaN
+        g = exp_sum32(w, c2, pk2(-mo, -mo));
+        s *= sc;
+        m = mn;
     }
-    s = fmaf(s, sc, tree_sum8x2(e));
-    m = mn;
+    s += g;
 }
 
 // ---------------------------------------------------------------- Philox4x32-10

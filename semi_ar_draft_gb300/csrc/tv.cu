@@ -229,75 +229,6 @@ struct TVRArgs {
 };
 
 
-// A consumer thread's 32 ids of one array in a slot, as 16 bf16 pairs: four 16-byte groups at
-// my0 + g kGrp (each a conflict-free 16-byte read across the warp).  Word k holds ids
-// (k / 4) kGrp + my0 + 2 (k % 4) + {0, 1} in its low and high halves.
-__device__ __forceinline__ void load32w(const uint16_t* arr, int my0, uint32_t (&w)[16]) {
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        const uint4 v = *reinterpret_cast<const uint4*>(arr + g * kGrp + my0);
-        w[4 * g] = v.x;
-        w[4 * g + 1] = v.y;
-        w[4 * g + 2] = v.z;
-        w[4 * g + 3] = v.w;
-    }
-}
-
-// Ids at or past the end of the row (the ragged last chunk) read as bf16 -inf: no mass, no max.
-// The row length is a multiple of 8, so a 16-byte group is wholly inside or outside.
-__device__ __forceinline__ void mask_tail32(uint32_t (&w)[16], int my0, int tail) {
-#pragma unroll
-    for (int g = 0; g < 4; ++g)
-        if (g * kGrp + my0 >= tail) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) w[4 * g + k] = 0xFF80FF80u;
-        }
-}
-
-__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-
-// Sum over the 32 ids of 2^(x c - m) (nm2 = -m in both lanes), four packed accumulators.
-__device__ __forceinline__ float exp_sum32(const uint32_t (&w)[16], uint64_t c2, uint64_t nm2) {
-    uint64_t acc[4];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        const float2 y = up2(fma2(pk2(bf16_lo(w[k]), bf16_hi(w[k])), c2, nm2));
-        const uint64_t e = pk2(ex2(y.x), ex2(y.y));
-        acc[k & 3] = k < 4 ? e : add2(acc[k & 3], e);
-    }
-    const float2 r = up2(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])));
-    return r.x + r.y;
-}
-
-// One group of the online (max m, sum s of 2^(x log2e - m)) statistics.  The terms are taken
-// against the running maximum as it stands; only when their sum reaches 2^64 (a row's first group,
-// where m = -inf makes it inf or NaN, or a maximum that jumped far) is the group's maximum taken
-// (packed bf16 maxima of the words: the maximum of the values exactly) and the sum rescaled.
-// While every value so far is -inf the pair stays (-inf, 0).
-__device__ __forceinline__ void lse_step32w(const uint32_t (&w)[16], uint64_t c2, float& m, float& s) {
-    float g = exp_sum32(w, c2, pk2(-m, -m));
-    if (!(g < 0x1p64f)) {
-        uint32_t mw[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mw[k] = bmax2(w[k], w[8 + k]);
-        const uint32_t x = bmax2(bmax2(bmax2(mw[0], mw[1]), bmax2(mw[2], mw[3])),
-                                 bmax2(bmax2(mw[4], mw[5]), bmax2(mw[6], mw[7])));
-        const float gm = fmaxf(bf16_lo(x), bf16_hi(x)) * kLog2e;
-        const float mn = fmaxf(m, gm);
-        const bool none = mn == -CUDART_INF_F;
-        const float sc = none ? 0.f : ex2(m - mn);  // m = -inf, mn finite: 0
-        const float mo = none ? 0.f : mn;           // x = -inf then gives 2^-inf = 0, never NaN
-        g = exp_sum32(w, c2, pk2(-mo, -mo));
-        s *= sc;
-        m = mn;
-    }
-    s += g;
-}
-
 // Sum over the 32 ids of 2^min(d log2e - Ld2, t log2e - Lt2).
 __device__ __forceinline__ float minsum32w(const uint32_t (&wd)[16], const uint32_t (&wt)[16], uint64_t c2,
                                            uint64_t nld2, uint64_t nlt2) {
@@ -368,8 +299,8 @@ __global__ void __launch_bounds__(kWSThreads, 1) tv_rows_kernel(TVRArgs a) {
         // runs on it (shared-memory reads cannot fault) and the result is never stored.
         auto take = [&](uint32_t (&wd)[16], uint32_t (&wt)[16]) {
             mbar_wait_hint_or_abort(&S.full[slot], phase, abort, &a.hdr->status, a.limit_ns);
-            load32w(&S.slots[slot][0][0], my0, wd);
-            load32w(&S.slots[slot][1][0], my0, wt);
+            load32w<kGrp>(&S.slots[slot][0][0], my0, wd);
+            load32w<kGrp>(&S.slots[slot][1][0], my0, wt);
             __syncwarp();
             if (lane == 0) mbar_arrive_local(&S.empty[slot]);
             if (++slot == kNS) {
@@ -384,16 +315,16 @@ __global__ void __launch_bounds__(kWSThreads, 1) tv_rows_kernel(TVRArgs a) {
             for (int k = 0; k < nch - 1; ++k) {
                 uint32_t wd[16], wt[16];
                 take(wd, wt);
-                lse_step32w(wd, c2, md, sd);
-                lse_step32w(wt, c2, mt, st);
+                lse_step32w(wd, kLog2e, c2, md, sd);
+                lse_step32w(wt, kLog2e, c2, mt, st);
             }
             {
                 uint32_t wd[16], wt[16];
                 take(wd, wt);
-                mask_tail32(wd, my0, tail);
-                mask_tail32(wt, my0, tail);
-                lse_step32w(wd, c2, md, sd);
-                lse_step32w(wt, c2, mt, st);
+                mask_tail32<kGrp>(wd, my0, tail);
+                mask_tail32<kGrp>(wt, my0, tail);
+                lse_step32w(wd, kLog2e, c2, md, sd);
+                lse_step32w(wt, kLog2e, c2, mt, st);
             }
             {
                 const float2 wdp = warp_lse_pair(md, sd);
@@ -420,8 +351,8 @@ __global__ void __launch_bounds__(kWSThreads, 1) tv_rows_kernel(TVRArgs a) {
             {
                 uint32_t wd[16], wt[16];
                 take(wd, wt);
-                mask_tail32(wd, my0, tail);
-                mask_tail32(wt, my0, tail);
+                mask_tail32<kGrp>(wd, my0, tail);
+                mask_tail32<kGrp>(wt, my0, tail);
                 acc += minsum32w(wd, wt, c2, nld2, nlt2);
             }
             const float w = warp_sum(acc);

@@ -335,8 +335,9 @@ __device__ void accept_walk_lanes(const VerifyArgs& a, int j, int L, int lane) {
 // engine; 16 consumer warps reduce it to (max, sum 2^(t * scale2 - max)) (T > 0) or (max, lowest
 // argmax) (T = 0).  The block that completes a request's last row runs the accept walk (rows then
 // have one segment).
-constexpr int kVCE = 8192;  // target ids per slot
-constexpr int kVNS = 8;     // ring slots (8 x 16 KB)
+constexpr int kVCE = 16384;        // target ids per slot (32 per consumer thread)
+constexpr int kVNS = 6;            // ring slots (6 x 32 KB)
+constexpr int kVGrp = kVCE / 4;    // ids between a consumer thread's 16-byte groups
 constexpr int kVThreads = kThreads + 32;
 constexpr int kVMaxB = 4096;  // requests (the prefix of their lengths is kept in shared memory)
 
@@ -462,11 +463,13 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_rows_ws_kernel(VerifyArgs
         }
         __syncwarp();
     } else {
-        // ---------------- 16 consumer warps; thread t takes ids 8t .. 8t+7 and 4096+8t .. 4096+8t+7
+        // ---------------- 16 consumer warps; thread t takes ids g kVGrp + 8t .. g kVGrp + 8t + 7, g < 4
         // After an abort the waits return at once and the slots hold stale data: the arithmetic runs
         // on it (shared-memory reads cannot fault) and nothing is stored.
+        static_assert(kVCE == 32 * kThreads, "four 16-byte groups per consumer thread per slot");
         const int my0 = 8 * tid;
         const int tail = a.V - (nch - 1) * kVCE;  // ids in the last chunk of a row
+        const uint64_t c2 = pk2(a.scale2, a.scale2);
         int par = 0, slot = 0;
         uint32_t phase = 0;
         for (int v = blockIdx.x; v < nver; v += gridDim.x) {
@@ -476,37 +479,31 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_rows_ws_kernel(VerifyArgs
             int idx = 0x7fffffff;
             auto chunk = [&](int k, bool last) {
                 mbar_wait_hint_or_abort(&S.full[slot], phase, abort, &a.hdr->status, a.limit_ns);
-                float x[16];
-                {
-                    float lo[8], hi[8];
-                    unpack_bf16x8(*reinterpret_cast<const uint4*>(&S.slots[slot][my0]), lo);
-                    unpack_bf16x8(*reinterpret_cast<const uint4*>(&S.slots[slot][kVCE / 2 + my0]), hi);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        x[e] = lo[e];
-                        x[8 + e] = hi[e];
-                    }
-                }
+                uint32_t w[16];
+                load32w<kVGrp>(&S.slots[slot][0], my0, w);
                 __syncwarp();
                 if (lane == 0) mbar_arrive_local(&S.empty[slot]);
                 if (++slot == kVNS) {
                     slot = 0;
                     phase ^= 1u;
                 }
-                if (last) {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        if ((e < 8 ? my0 + e : kVCE / 2 + my0 + e - 8) >= tail) x[e] = -CUDART_INF_F;
-                }
+                if (last) mask_tail32<kVGrp>(w, my0, tail);
                 if (a.greedy) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        if (x[e] > m) {  // ids ascend within a thread: the first maximum is kept
-                            m = x[e];
-                            idx = k * kVCE + (e < 8 ? my0 + e : kVCE / 2 + my0 + e - 8);
+                    for (int e = 0; e < 16; ++e) {  // ids ascend with (e, half): the first maximum is kept
+                        const int id = k * kVCE + (e >> 2) * kVGrp + my0 + 2 * (e & 3);
+                        const float lo = bf16_lo(w[e]), hi = bf16_hi(w[e]);
+                        if (lo > m) {
+                            m = lo;
+                            idx = id;
                         }
+                        if (hi > m) {
+                            m = hi;
+                            idx = id + 1;
+                        }
+                    }
                 } else {
-                    lse_step16(x, a.scale2, m, sacc);
+                    lse_step32w(w, a.scale2, c2, m, sacc);
                 }
             };
             for (int k = 0; k < nch - 1; ++k) chunk(k, false);
