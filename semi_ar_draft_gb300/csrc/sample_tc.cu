@@ -237,23 +237,45 @@ __device__ __forceinline__ void chunk_greedy(const uint32_t (&v)[32], int id0, i
 }
 
 // The four chunks of one accumulator for this thread's request: TMEM loads double-buffered, the
-// next chunk's in flight while the current one is reduced.
-template <bool GREEDY, bool MASK>
+// next chunk's in flight while the current one is reduced.  With ROLL the loop runs over pairs of
+// chunks and is not unrolled: two copies of the chunk code rather than four.  That keeps the
+// larger kernels of ranks 128 and 256 in the instruction cache (b128_r256: 0.33 ms against 0.38 ms);
+// at rank 64 the unrolled loop is faster (0.65 ms against 0.76 ms at b512).
+template <bool GREEDY, bool MASK, bool ROLL>
 __device__ __forceinline__ void accumulator_chunks(uint32_t taddr, int id0, int V, float scale2, float u,
                                                    const float (&lnE)[4], ChunkState& cs) {
     uint32_t va[32], vb[32];
     tmem_ld32(taddr, va);
     tmem_wait_ld(va);
-#pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-        uint32_t(&cur)[32] = (cc & 1) ? vb : va;
-        uint32_t(&nxt)[32] = (cc & 1) ? va : vb;
-        if (cc < 3) tmem_ld32(taddr + 32u * (uint32_t)(cc + 1), nxt);
-        if (!MASK || id0 + 32 * cc < V) {  // (uniform) a chunk wholly past V has no ids
-            if (GREEDY) chunk_greedy<MASK>(cur, id0 + 32 * cc, V, cs);
-            else chunk_sample<MASK>(cur, id0 + 32 * cc, V, scale2, u, lnE[cc], cs);
+    if constexpr (ROLL) {
+#pragma unroll 1
+        for (int p = 0; p < 2; ++p) {
+            const int c0 = 2 * p, c1 = c0 + 1;
+            tmem_ld32(taddr + 32u * (uint32_t)c1, vb);  // chunk c1 in flight while c0 is reduced
+            if (!MASK || id0 + 32 * c0 < V) {           // (uniform) a chunk wholly past V has no ids
+                if (GREEDY) chunk_greedy<MASK>(va, id0 + 32 * c0, V, cs);
+                else chunk_sample<MASK>(va, id0 + 32 * c0, V, scale2, u, p ? lnE[2] : lnE[0], cs);
+            }
+            tmem_wait_ld(vb);
+            if (p == 0) tmem_ld32(taddr + 32u * (uint32_t)(c1 + 1), va);  // chunk 2 in flight while 1 is reduced
+            if (!MASK || id0 + 32 * c1 < V) {
+                if (GREEDY) chunk_greedy<MASK>(vb, id0 + 32 * c1, V, cs);
+                else chunk_sample<MASK>(vb, id0 + 32 * c1, V, scale2, u, p ? lnE[3] : lnE[1], cs);
+            }
+            if (p == 0) tmem_wait_ld(va);
         }
-        if (cc < 3) tmem_wait_ld(nxt);
+    } else {
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            uint32_t(&cur)[32] = (cc & 1) ? vb : va;
+            uint32_t(&nxt)[32] = (cc & 1) ? va : vb;
+            if (cc < 3) tmem_ld32(taddr + 32u * (uint32_t)(cc + 1), nxt);
+            if (!MASK || id0 + 32 * cc < V) {  // (uniform) a chunk wholly past V has no ids
+                if (GREEDY) chunk_greedy<MASK>(cur, id0 + 32 * cc, V, cs);
+                else chunk_sample<MASK>(cur, id0 + 32 * cc, V, scale2, u, lnE[cc], cs);
+            }
+            if (cc < 3) tmem_wait_ld(nxt);
+        }
     }
 }
 
@@ -656,8 +678,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc_fence_after();
                 const uint32_t taddr = tl + (uint32_t)(sl * kTcN);
                 const int id0 = tile0 + kTcN * acc;
-                if (full_tile) accumulator_chunks<GREEDY, false>(taddr, id0, a.V, a.scale2, uin, lnE, cs);
-                else accumulator_chunks<GREEDY, true>(taddr, id0, a.V, a.scale2, uin, lnE, cs);
+                if (full_tile) accumulator_chunks<GREEDY, false, (R >= 128)>(taddr, id0, a.V, a.scale2, uin, lnE, cs);
+                else accumulator_chunks<GREEDY, true, (R >= 128)>(taddr, id0, a.V, a.scale2, uin, lnE, cs);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_local(&t_empty[sl]);
@@ -1257,8 +1279,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc_fence_after();
                 const uint32_t taddr = tl + (uint32_t)(sl * 2 * kTcN);  // z; t in the next 128 columns
                 const int id0 = tile0 + kTcN * acc;
-#pragma unroll
+                // one copy of the chunk code, not four (the variants of chunk_job are large): the
+                // instruction cache, not the arithmetic, held this loop back when it was unrolled
+#pragma unroll 1
                 for (int cc = 0; cc < 4; ++cc) {
+                    const float le = cc == 0 ? lnE[0] : (cc == 1 ? lnE[1] : (cc == 2 ? lnE[2] : lnE[3]));
                     uint32_t zv[32], tv[32];
                     tmem_ld32(taddr + 32u * (uint32_t)cc, zv);
                     tmem_ld32(taddr + (uint32_t)kTcN + 32u * (uint32_t)cc, tv);
@@ -1269,9 +1294,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int e = 0; e < 32; ++e) t[e] = __uint_as_float(tv[e]);
                     const int idc = id0 + 32 * cc;
                     if (full_tile)
-                        chunk_job<GREEDY, false>(t, zv, mode, idc, a.V, a.scale2, lse2, dl2, uin, lnE[cc], bkey, bcand);
+                        chunk_job<GREEDY, false>(t, zv, mode, idc, a.V, a.scale2, lse2, dl2, uin, le, bkey, bcand);
                     else if (idc < a.V)  // (uniform) a chunk wholly past V has no ids
-                        chunk_job<GREEDY, true>(t, zv, mode, idc, a.V, a.scale2, lse2, dl2, uin, lnE[cc], bkey, bcand);
+                        chunk_job<GREEDY, true>(t, zv, mode, idc, a.V, a.scale2, lse2, dl2, uin, le, bkey, bcand);
                 }
                 tc_fence_before();
                 __syncwarp();
