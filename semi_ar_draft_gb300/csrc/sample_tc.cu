@@ -854,7 +854,7 @@ constexpr int kVtSlots = 2;  // accumulator pairs {z, t}: 2 x 256 TMEM columns
 constexpr uint32_t kVtSmA = kVtStages * kVtStageBytes;     // [2] A operands (W1 rows of the prevs)
 constexpr uint32_t kVtSmId = kVtSmA + 2 * kVtTile;
 constexpr uint32_t kVtSmBars = kVtSmId + kIdBytes;
-constexpr int kVtNumBars = 4 + 2 * kVtStages + 2 * kVtSlots + 2;
+constexpr int kVtNumBars = 4 + 2 * kVtStages + 2 * kVtSlots + 3;
 constexpr uint32_t kVtSmFlags = kVtSmBars + 8 * kVtNumBars;
 constexpr uint32_t kVtSmRows = kVtSmFlags + 64;            // [2][128] the unit's base and target rows (-1: none)
 constexpr size_t kVtSmemBytes = kVtSmRows + 2 * kTcRows * 4;
@@ -988,12 +988,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t* t_empty = t_full + kVtSlots;      // [kVtSlots]
     uint64_t* done_bar = t_empty + kVtSlots;
     uint64_t* drain_bar = done_bar + 1;
+    uint64_t* drain_t = drain_bar + 1;  // the target mover's MMAs
     int* flags = reinterpret_cast<int*>(sm + kVtSmFlags);
     volatile int* abort = flags;
     int* wg_done = flags + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(flags + 2);
     volatile int* nb_issued = flags + 3;
     volatile int* n_mma = flags + 4;
+    volatile int* n_mma_t = flags + 5;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tile = blockIdx.x, tile0 = tile * kTcTile;
     const int total = a.nrb;
@@ -1005,15 +1007,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&a_empty[b], 1);
         }
         for (int b = 0; b < kVtStages; ++b) {
-            mbar_init(&b_full[b], 5);  // the W2 copy's arrival with its bytes + one per copying warp
-            mbar_init(&b_empty[b], 1);
+            mbar_init(&b_full[b], 5);   // the W2 copy's arrival with its bytes + one per copying warp
+            mbar_init(&b_empty[b], 2);  // both MMA issuers have read the stage
         }
         for (int b = 0; b < kVtSlots; ++b) {
-            mbar_init(&t_full[b], 1);
+            mbar_init(&t_full[b], 2);  // z and t are in: both MMA issuers' commits
             mbar_init(&t_empty[b], 4);
         }
         mbar_init(done_bar, 1);
         mbar_init(drain_bar, 1);
+        mbar_init(drain_t, 1);
         for (int f = 0; f < 16; ++f) flags[f] = 0;
         mbar_init_fence();
     }
@@ -1074,7 +1077,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t d = tmem + (uint32_t)(sl * 2 * kTcN), dt = d + (uint32_t)kTcN;
+                    const uint32_t d = tmem + (uint32_t)(sl * 2 * kTcN);
                     const uint64_t sd = ring_desc + (uint64_t)(st * (int)(kVtStageBytes >> 4));
 #pragma unroll
                     for (int k = 0; k < 4; ++k)  // D = W1[prev] . W2_rows^T
@@ -1087,16 +1090,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         for (int i = 0; i < kTcBox / 16; ++i)  // D[:, 64 bx + 16 i ..] += base[:, 16 i ..] . I
                             umma_bf16(d + (uint32_t)(kTcBox * bx + 16 * i),
                                       sd + (uint64_t)((1 + bx) * (int)(kVtTile >> 4) + 2 * i), id_desc, idesc_base, 1u);
-#pragma unroll
-                    for (int bx = 0; bx < 2; ++bx)
-#pragma unroll
-                        for (int i = 0; i < kTcBox / 16; ++i)  // T[:, 64 bx + 16 i ..] = target[:, 16 i ..] . I
-                            umma_bf16(dt + (uint32_t)(kTcBox * bx + 16 * i),
-                                      sd + (uint64_t)((3 + bx) * (int)(kVtTile >> 4) + 2 * i), id_desc, idesc_base, 0u);
-                    umma_commit(&b_empty[st]);  // the stage is free once these have read it
+                    umma_commit(&b_empty[st]);  // the stage is free once these (and the target mover's) have read it
                     umma_commit(&t_full[sl]);
                 }
                 if (ok) umma_commit(&a_empty[ab]);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 3) {
+        // ---------------------------------------------------------------- target mover
+        // A second MMA issuer: the eight identity MMAs per accumulator that move the jobs' target rows
+        // into the neighbouring TMEM columns (their own columns, so no order against warp 1's MMAs is
+        // needed); the stage and the slot each wait for both issuers' commits.
+        if (lane == 0) {
+            constexpr uint32_t idesc_base = umma_idesc_bf16(kTcRows, 16);
+            const uint64_t id_desc = umma_desc_sw128(smem_addr(sm + kVtSmId), 1024);
+            const uint64_t ring_desc = umma_desc_sw128(smem_addr(sm), 1024);
+            const int nacc = total * kTcAccs;
+            for (int ga = 0; ga < nacc; ++ga) {
+                const int sl = ga % kVtSlots, use = ga / kVtSlots, st = ga % kVtStages;
+                if ((use > 0 && !mbar_wait_hint_or_abort(&t_empty[sl], (uint32_t)((use - 1) & 1), abort, &hdr->status,
+                                                         lim)) ||
+                    !mbar_wait_hint_or_abort(&b_full[st], (uint32_t)((ga / kVtStages) & 1), abort, &hdr->status, lim))
+                    break;
+                tc_fence_after();
+                const uint32_t dt = tmem + (uint32_t)(sl * 2 * kTcN) + (uint32_t)kTcN;
+                const uint64_t sd = ring_desc + (uint64_t)(st * (int)(kVtStageBytes >> 4));
+                *n_mma_t = 1;
+#pragma unroll
+                for (int bx = 0; bx < 2; ++bx)
+#pragma unroll
+                    for (int i = 0; i < kTcBox / 16; ++i)  // T[:, 64 bx + 16 i ..] = target[:, 16 i ..] . I
+                        umma_bf16(dt + (uint32_t)(kTcBox * bx + 16 * i),
+                                  sd + (uint64_t)((3 + bx) * (int)(kVtTile >> 4) + 2 * i), id_desc, idesc_base, 0u);
+                umma_commit(&b_empty[st]);
+                umma_commit(&t_full[sl]);
+            }
+            if (*n_mma_t) {  // every MMA of this thread has completed before the tensor memory is freed
+                umma_commit(drain_t);
+                mbar_wait_bounded(drain_t, 0, &hdr->status, lim);
             }
         }
         __syncwarp();
