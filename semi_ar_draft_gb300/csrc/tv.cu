@@ -229,15 +229,28 @@ struct TVRArgs {
 };
 
 
-// Sum over the 32 ids of 2^min(d log2e - Ld2, t log2e - Lt2).
-__device__ __forceinline__ float minsum32w(const uint32_t (&wd)[16], const uint32_t (&wt)[16], uint64_t c2,
-                                           uint64_t nld2, uint64_t nlt2) {
+// Sum over the 32 ids of 2^min(d log2e - Ld2, t log2e - Lt2), as 2^(log2e min(d - ld, t - lt))
+// with ld = Ld2 / log2e, lt = Lt2 / log2e: each difference is one mixed-precision subtract (bf16
+// operand taken from its half of the word, fp32 result), the scale one packed multiply per pair.
+__device__ __forceinline__ float sub_bf16_lo(uint32_t w, float c) {
+    float r;
+    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; sub.rn.f32.bf16 %0, l, %2; }" : "=f"(r) : "r"(w), "f"(c));
+    return r;
+}
+__device__ __forceinline__ float sub_bf16_hi(uint32_t w, float c) {
+    float r;
+    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; sub.rn.f32.bf16 %0, h, %2; }" : "=f"(r) : "r"(w), "f"(c));
+    return r;
+}
+__device__ __forceinline__ float minsum32w(const uint32_t (&wd)[16], const uint32_t (&wt)[16], uint64_t c2, float ld,
+                                           float lt) {
     uint64_t acc[4];
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-        const float2 yd = up2(fma2(pk2(bf16_lo(wd[k]), bf16_hi(wd[k])), c2, nld2));
-        const float2 yt = up2(fma2(pk2(bf16_lo(wt[k]), bf16_hi(wt[k])), c2, nlt2));
-        const uint64_t e = pk2(ex2(fminf(yd.x, yt.x)), ex2(fminf(yd.y, yt.y)));
+        const float m0 = fminf(sub_bf16_lo(wd[k], ld), sub_bf16_lo(wt[k], lt));
+        const float m1 = fminf(sub_bf16_hi(wd[k], ld), sub_bf16_hi(wt[k], lt));
+        const float2 y = up2(mul2(pk2(m0, m1), c2));
+        const uint64_t e = pk2(ex2(y.x), ex2(y.y));
         acc[k & 3] = k < 4 ? e : add2(acc[k & 3], e);
     }
     const float2 r = up2(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])));
@@ -341,19 +354,19 @@ __global__ void __launch_bounds__(kWSThreads, 1) tv_rows_kernel(TVRArgs a) {
                 Lt2 = ct.x + lg2(ct.y);
             }
             // ---- pass 2: sum of min(p, q) = 2^min(d log2e - Ld2, t log2e - Lt2)
-            const uint64_t nld2 = pk2(-Ld2, -Ld2), nlt2 = pk2(-Lt2, -Lt2);
+            const float ld = Ld2 * kLn2, lt = Lt2 * kLn2;  // the normalisers in the logits' units
             float acc = 0.f;
             for (int k = 0; k < nch - 1; ++k) {
                 uint32_t wd[16], wt[16];
                 take(wd, wt);
-                acc += minsum32w(wd, wt, c2, nld2, nlt2);
+                acc += minsum32w(wd, wt, c2, ld, lt);
             }
             {
                 uint32_t wd[16], wt[16];
                 take(wd, wt);
                 mask_tail32<kGrp>(wd, my0, tail);
                 mask_tail32<kGrp>(wt, my0, tail);
-                acc += minsum32w(wd, wt, c2, nld2, nlt2);
+                acc += minsum32w(wd, wt, c2, ld, lt);
             }
             const float w = warp_sum(acc);
             if (lane == 0) S.red1[warp] = w;
