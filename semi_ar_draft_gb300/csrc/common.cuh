@@ -155,18 +155,33 @@ __device__ __forceinline__ void mask_tail32(uint32_t (&w)[16], int my0, int tail
         }
 }
 
+// x - c for the low or high bf16 half of a packed word, in fp32 with one rounding (a mixed-precision
+// subtract: the half is taken as it is, no unpacking).
+__device__ __forceinline__ float sub_bf16_lo(uint32_t w, float c) {
+    float r;
+    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; sub.rn.f32.bf16 %0, l, %2; }" : "=f"(r) : "r"(w), "f"(c));
+    return r;
+}
+__device__ __forceinline__ float sub_bf16_hi(uint32_t w, float c) {
+    float r;
+    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; sub.rn.f32.bf16 %0, h, %2; }" : "=f"(r) : "r"(w), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
     uint32_t r;
     asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
     return r;
 }
 
-// Sum over the 32 values of 2^(x c - m) (c2 = c, nm2 = -m in both lanes), four packed accumulators.
-__device__ __forceinline__ float exp_sum32(const uint32_t (&w)[16], uint64_t c2, uint64_t nm2) {
+// Sum over the 32 values of 2^(c (x - mu)) (c2 = c in both lanes; mu = m / c for the terms
+// 2^(x c - m)), four packed accumulators: one mixed-precision subtract per value, one packed
+// multiply per pair.
+__device__ __forceinline__ float exp_sum32(const uint32_t (&w)[16], uint64_t c2, float mu) {
     uint64_t acc[4];
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-        const float2 y = up2(fma2(pk2(bf16_lo(w[k]), bf16_hi(w[k])), c2, nm2));
+        const float2 y = up2(mul2(pk2(sub_bf16_lo(w[k], mu), sub_bf16_hi(w[k], mu)), c2));
         const uint64_t e = pk2(ex2(y.x), ex2(y.y));
         acc[k & 3] = k < 4 ? e : add2(acc[k & 3], e);
     }
@@ -174,14 +189,15 @@ __device__ __forceinline__ float exp_sum32(const uint32_t (&w)[16], uint64_t c2,
     return r.x + r.y;
 }
 
-// One group of the online (max m, sum s of 2^(x scale - m)) statistics (scale > 0, c2 = scale in
-// both lanes; m and s in the log2 domain).  The terms are taken against the running maximum as it
+// One group of the online (max m, sum s of 2^(x scale - m)) statistics (scale > 0, inv = 1 / scale,
+// c2 = scale in both lanes; m and s in the log2 domain).  The terms are taken against the running maximum as it
 // stands; only when their sum reaches 2^64 (a row's first group, where m = -inf makes it inf or
 // NaN, or a maximum that jumped far) is the group's maximum taken (packed bf16 maxima of the words:
 // the maximum of the values exactly) and the sum rescaled.  While every value so far is -inf the
 // pair stays (-inf, 0).
-__device__ __forceinline__ void lse_step32w(const uint32_t (&w)[16], float scale, uint64_t c2, float& m, float& s) {
-    float g = exp_sum32(w, c2, pk2(-m, -m));
+__device__ __forceinline__ void lse_step32w(const uint32_t (&w)[16], float scale, float inv, uint64_t c2, float& m,
+                                            float& s) {
+    float g = exp_sum32(w, c2, m * inv);  // (m = -inf: every term inf or NaN, so the exact path below)
     if (!(g < 0x1p64f)) {
         uint32_t mw[8];
 #pragma unroll
@@ -193,7 +209,7 @@ __device__ __forceinline__ void lse_step32w(const uint32_t (&w)[16], float scale
         const bool none = mn == -CUDART_INF_F;
         const float sc = none ? 0.f : ex2(m - mn);  // m = -inf, mn finite: 0
         const float mo = none ? 0.f : mn;           // x = -inf then gives 2^-inf = 0, never NaN
-        g = exp_sum32(w, c2, pk2(-mo, -mo));
+        g = exp_sum32(w, c2, mo * inv);
         s *= sc;
         m = mn;
     }

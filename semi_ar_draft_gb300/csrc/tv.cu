@@ -232,16 +232,6 @@ struct TVRArgs {
 // Sum over the 32 ids of 2^min(d log2e - Ld2, t log2e - Lt2), as 2^(log2e min(d - ld, t - lt))
 // with ld = Ld2 / log2e, lt = Lt2 / log2e: each difference is one mixed-precision subtract (bf16
 // operand taken from its half of the word, fp32 result), the scale one packed multiply per pair.
-__device__ __forceinline__ float sub_bf16_lo(uint32_t w, float c) {
-    float r;
-    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; sub.rn.f32.bf16 %0, l, %2; }" : "=f"(r) : "r"(w), "f"(c));
-    return r;
-}
-__device__ __forceinline__ float sub_bf16_hi(uint32_t w, float c) {
-    float r;
-    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; sub.rn.f32.bf16 %0, h, %2; }" : "=f"(r) : "r"(w), "f"(c));
-    return r;
-}
 __device__ __forceinline__ float minsum32w(const uint32_t (&wd)[16], const uint32_t (&wt)[16], uint64_t c2, float ld,
                                            float lt) {
     uint64_t acc[4];
@@ -328,16 +318,16 @@ __global__ void __launch_bounds__(kWSThreads, 1) tv_rows_kernel(TVRArgs a) {
             for (int k = 0; k < nch - 1; ++k) {
                 uint32_t wd[16], wt[16];
                 take(wd, wt);
-                lse_step32w(wd, kLog2e, c2, md, sd);
-                lse_step32w(wt, kLog2e, c2, mt, st);
+                lse_step32w(wd, kLog2e, kLn2, c2, md, sd);
+                lse_step32w(wt, kLog2e, kLn2, c2, mt, st);
             }
             {
                 uint32_t wd[16], wt[16];
                 take(wd, wt);
                 mask_tail32<kGrp>(wd, my0, tail);
                 mask_tail32<kGrp>(wt, my0, tail);
-                lse_step32w(wd, kLog2e, c2, md, sd);
-                lse_step32w(wt, kLog2e, c2, mt, st);
+                lse_step32w(wd, kLog2e, kLn2, c2, md, sd);
+                lse_step32w(wt, kLog2e, kLn2, c2, mt, st);
             }
             {
                 const float2 wdp = warp_lse_pair(md, sd);

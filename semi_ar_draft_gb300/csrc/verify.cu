@@ -470,6 +470,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_rows_ws_kernel(VerifyArgs
         const int my0 = 8 * tid;
         const int tail = a.V - (nch - 1) * kVCE;  // ids in the last chunk of a row
         const uint64_t c2 = pk2(a.scale2, a.scale2);
+        const float inv2 = 1.f / a.scale2;
         int par = 0, slot = 0;
         uint32_t phase = 0;
         for (int v = blockIdx.x; v < nver; v += gridDim.x) {
@@ -503,7 +504,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_rows_ws_kernel(VerifyArgs
                         }
                     }
                 } else {
-                    lse_step32w(w, a.scale2, c2, m, sacc);
+                    lse_step32w(w, a.scale2, inv2, c2, m, sacc);
                 }
             };
             for (int k = 0; k < nch - 1; ++k) chunk(k, false);
