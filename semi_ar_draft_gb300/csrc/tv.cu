@@ -190,11 +190,12 @@ __global__ void __launch_bounds__(kTVThreads, 1) tv_kernel(TVArgs a) {
 // ------------------------------------------------------------------------------------------
 // bf16 fast path: one block per row at a time (persistent over rows, no cluster), warp-specialised.
 // A producer warp streams every row twice through a ring of kNS shared-memory slots (kCE ids of
-// d and t per slot, 32 per consumer thread) with the bulk-copy engine: pass 1 from HBM with an L2 evict-last policy, so
-// that pass 2, which follows right after, reads the same bytes from L2 (evict-first); a slot
-// is refilled once all 16 consumer warps have released it.  The consumer warps take the softmax
-// statistics of d and t in pass 1, combine them across the block, then form
-// sum_v min(p_v, q_v) = sum_v 2^min(d_v log2e - Ld, t_v log2e - Lt) in pass 2.
+// d and t per slot, 32 per consumer thread) with the bulk-copy engine: pass 1 from HBM with an
+// L2 evict-last policy, so that pass 2, which follows right after, reads the same bytes from L2
+// (evict-first); a slot is refilled once all 16 consumer warps have released it.  The consumer
+// warps take the softmax statistics of d and t in pass 1, combine them across the block, then form
+// sum_v min(p_v, q_v) = sum_v 2^min(d_v log2e - Ld, t_v log2e - Lt) in pass 2.  Both passes read
+// the bf16 values straight from their packed words (mixed-precision subtracts, no unpacking).
 // Every wait is bounded; after a timeout the block-wide abort flag makes the consumers skip the
 // data while keeping the same sequence of named barriers, and in-flight copies are awaited.
 // ------------------------------------------------------------------------------------------
