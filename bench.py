@@ -23,6 +23,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -39,7 +40,7 @@ WORKLOADS = ("b32_r64", "b128_r256", "b512_sched")
 E2E_STEPS = 30  # steps per end-to-end window (each step copies the batch's inputs in: 5 GB at b512_sched)
 KERNEL_SOURCES = {
     "sample": ["sample.cu", "sample_tc.cu", "tc05.cuh", "markov_tile.cuh", "common.cuh"],
-    "verify": ["verify.cu", "markov_tile.cuh", "common.cuh"],
+    "verify": ["verify.cu", "sample_tc.cu", "tc05.cuh", "markov_tile.cuh", "common.cuh"],
     "tv": ["tv.cu", "common.cuh"],
     "schedule": ["schedule.cu", "common.cuh"],
 }
@@ -61,11 +62,19 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """The source without comments, blank lines or trailing spaces: a comment edit keeps the hash."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def source_hash(kernel: str) -> str:
+    """Hash of the code (not the comments) of a kernel's sources: profiled traffic applies while it holds."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "semi_ar_draft_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "semi_ar_draft_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
