@@ -63,10 +63,11 @@ def peaks():
 
 
 def _code_only(text: str) -> str:
-    """The source without comments, blank lines or trailing spaces: a comment edit keeps the hash."""
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    """The source without comments or blank lines, each line's whitespace collapsed: a comment or
+    layout edit keeps the hash."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
     text = re.sub(r"//[^\n]*", "", text)
-    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+    return "\n".join(" ".join(line.split()) for line in text.splitlines() if line.strip())
 
 
 def source_hash(kernel: str) -> str:
