@@ -3,15 +3,15 @@
 // Method (P2 "从 DFlash 到 dLLM Self-Spec（三）" section 3.4, VanillaMarkov and the
 // sample_block_tokens loop; P1 "03 · DSpark 建模：Markov 与 Confidence" section 3.7):
 // for i = 1..gamma, z = base_i + W2 . W1[prev]; sample; prev = sampled.  The sampling
-// contract is the tile-Gumbel draw stated in dspark.h.
+// contract is the chunk-Gumbel draw stated in dspark.h.
 //
 // One persistent cooperative kernel runs all gamma steps:
 //   - vocabulary split: block b owns tiles t = b, b + G, ... (G <= number of SMs);
 //   - per step and tile, rows go in blocks of 16 requests: the producer writes z = base + bias
 //     for 16 rows x 1024 ids to shared memory with per-32-id chunk statistics (tensor-core
 //     mma.sync bias with the accumulator initialised from the base logits, or a CUDA-core GEMV
-//     for fp32 weights); a warp per row turns them into the tile's record {Gumbel key, log-mass,
-//     in-tile candidate, z at it} in global scratch;
+//     for fp32 weights); a warp per row turns them into the tile's record {its best chunk key,
+//     log-mass, that chunk's candidate, z at it} in global scratch;
 //   - bounded grid-wide wait; block b reduces the records of requests b, b + G, ... to the
 //     step's token, LSE(z/T) and z at the token; bounded grid-wide wait; next step.
 // When each block owns a single tile and the W2 rows of it fit, they are staged in shared
@@ -33,7 +33,7 @@ namespace {
 
 constexpr int kMaxStagedTiles = 160;
 constexpr int kSlotStride = 16;   // 64-bit words between two requests' maxima
-constexpr int kCountStride = 32;  // 32-bit words between two row blocks' arrival counters  // tiles a request's log-masses are reduced over by one warp
+constexpr int kCountStride = 32;  // 32-bit words between two row blocks' arrival counters
 
 struct SampleArgs {
     int B, gamma, V, r, nt, G;
