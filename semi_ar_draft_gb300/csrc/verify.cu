@@ -6,17 +6,23 @@
 // target's; the verify tokens of all requests form one flattened list, P2 section 3.7.2).
 // Contract in dspark.h.
 //
-// Two launches, no grid-wide waits:
-//   1. rows: one block per (vocabulary segment, position, request) streams a target row segment
-//      and writes its (max, sum 2^(s2 - max)) (T > 0) or (max, argmax) (T = 0); the last block
-//      of a request (arrival counter) combines the segments and walks the accept tests
-//      left to right, writing n_accepted and, when needed, a job: RESID at the rejecting
+// Two stages, no grid-wide waits:
+//   1. rows: the target rows' (max, sum 2^(s2 - max)) (T > 0) or (max, argmax) (T = 0).  For bf16
+//      rows on 16-byte boundaries a persistent block per SM streams whole rows through a
+//      shared-memory ring (verify_rows_ws_kernel); otherwise one block per (vocabulary segment,
+//      position, request).  The block completing a request (arrival counter) walks the accept
+//      tests left to right, writing n_accepted and, when needed, a job: RESID at the rejecting
 //      position or BONUS from target row L+1.
-//   2. jobs: one block per (tile, 16 requests): z = base + bias for RESID rows (same producer as
-//      the sampler), then per-id weights max(0, p - q) (RESID) or the target softmax (BONUS),
-//      chunk statistics and the tile's Gumbel record; the last block of a row block reduces the
-//      tile records to the correction token.  A residual without any mass falls back to a draw
-//      from p, done by that last block alone.
+//   2. draws (the chunk-Gumbel contract of dspark.h, with the correction purposes):
+//      - bf16 logits and weights of rank 64, at least 64 requests, dense target rows, vanilla head:
+//        the tensor-core kernel of sample_tc.cu (z and the target rows in tensor memory, one CTA
+//        per tile over row blocks of 128 jobs), then verify_fallback_kernel for residuals that
+//        had no mass anywhere (a whole-row draw from p);
+//      - otherwise verify_jobs_kernel, one block per (tile, 16 requests): z = base + bias for
+//        RESID rows (the sampler's producer, or the head vectors), per-id weights max(0, p - q)
+//        (RESID) or the target softmax (BONUS), the tile's best chunk key; the last block of a row
+//        block reduces the tiles to the correction token, and draws from p where a residual had no
+//        mass.
 #include <algorithm>
 
 #include "host_util.h"
